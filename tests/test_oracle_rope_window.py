@@ -1,0 +1,128 @@
+"""Pins for the oracle's RoPE table and rotation and for the window ring (deepseek_v41_ref::attn
+rustdoc page: freqs_cis, apply_rotary, window_topk_idxs, WindowCache and the 12-into-8 ring fixture).
+"""
+import json
+import math
+import os
+
+import numpy as np
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def test_rope_table_closed_form(orc):
+    # one pair (rd = 2) turns at frequency theta^0 = 1: the angle is the position itself
+    t = orc.rope_table(2, 4000, 10000.0)
+    p = np.arange(4000, dtype=np.float64)
+    assert np.array_equal(t[:, 0, 0], np.cos(p).astype(np.float32))
+    assert np.array_equal(t[:, 0, 1], np.sin(p).astype(np.float32))
+    # rd = 64, theta = 10000: pair 16 turns at 10000^(-1/2) = 1/100 per position
+    t = orc.rope_table(64, 1001, 10000.0)
+    assert abs(float(t[1000, 16, 0]) - math.cos(10.0)) < 1e-7
+    assert abs(float(t[1000, 16, 1]) - math.sin(10.0)) < 1e-7
+    # position 0 is the identity rotation
+    assert (t[0, :, 0] == 1.0).all() and (t[0, :, 1] == 0.0).all()
+
+
+def test_rope_yarn_structure(orc):
+    # no interpolation while the table fits the original length
+    a = orc.rope_table(64, 4096, 160000.0, orig_seq=65536, factor=16.0)
+    b = orc.rope_table(64, 4096, 160000.0)
+    assert np.array_equal(a, b)
+    # beyond it: the fastest pairs keep their frequency, the slowest are divided by the factor
+    y = orc.rope_table(64, 65537 + 7, 160000.0, orig_seq=65536, factor=16.0)
+    f = 160000.0 ** (-2.0 * np.arange(32) / 64)
+    ang = np.arctan2(y[1, :, 1].astype(np.float64), y[1, :, 0].astype(np.float64))
+    assert abs(ang[0] - f[0]) < 1e-6 and abs(ang[1] - f[1]) < 1e-6
+    assert abs(ang[31] - f[31] / 16.0) < 1e-9
+    assert np.all(np.diff(ang) < 0)  # still monotone in the pair index
+
+
+def test_rotary_adjacent_pairs_and_inverse(orc):
+    rd, hd = 16, 64
+    tab = orc.rope_table(rd, 64, 10000.0)
+    x = np.zeros((1, hd), np.float32)
+    x[0, hd - rd] = 1.0  # first element of the rotated tail: real part of pair 0
+    xb = orc.f32_to_bf16(x)
+    y = orc.bf16_to_f32(orc.apply_rotary(xb, rd, np.array([5]), tab))
+    # adjacent pairs: (1, 0) -> (cos 5, sin 5) in elements (hd-rd, hd-rd+1); the rest untouched
+    assert y[0, hd - rd] == orc.bf16_to_f32(orc.f32_to_bf16(np.float32(math.cos(5.0))))
+    assert y[0, hd - rd + 1] == orc.bf16_to_f32(orc.f32_to_bf16(np.float32(math.sin(5.0))))
+    assert (y[0, hd - rd + 2:] == 0).all() and (y[0, : hd - rd] == 0).all()
+    rng = np.random.default_rng(5)
+    v = orc.f32_to_bf16(rng.standard_normal((300, hd)).astype(np.float32))
+    pos = rng.integers(0, 64, 300).astype(np.int32)
+    r = orc.apply_rotary(v, rd, pos, tab)
+    assert np.array_equal(r[:, : hd - rd], v[:, : hd - rd])
+    back = orc.apply_rotary(r, rd, pos, tab, inverse=True)
+    vf, bf = orc.bf16_to_f32(v).astype(np.float64), orc.bf16_to_f32(back).astype(np.float64)
+    # forward then inverse: identity up to two bf16 roundings of each element
+    assert np.all(np.abs(bf - vf) <= 2 ** -7 * (np.abs(vf) + np.abs(vf[:, ::-1]).max()) + 1e-30)
+    # a rotation keeps each pair's modulus up to bf16 rounding
+    rv = orc.bf16_to_f32(r).astype(np.float64)[:, hd - rd:].reshape(300, rd // 2, 2)
+    vv = vf[:, hd - rd:].reshape(300, rd // 2, 2)
+    assert np.allclose(np.hypot(rv[..., 0], rv[..., 1]), np.hypot(vv[..., 0], vv[..., 1]), rtol=2 ** -7, atol=1e-6)
+
+
+def test_rotary_composes_angles(orc):
+    rd, hd = 8, 8
+    tab = orc.rope_table(rd, 64, 10000.0)
+    x = orc.f32_to_bf16(np.tile(np.array([1.0, 0.0], np.float32), (1, 4)))
+    y = orc.bf16_to_f32(orc.apply_rotary(x, rd, np.array([7]), tab)).astype(np.float64)
+    f = 10000.0 ** (-2.0 * np.arange(4) / 8)
+    assert np.allclose(y[0, 0::2], np.cos(7 * f), atol=4e-3) and np.allclose(y[0, 1::2], np.sin(7 * f), atol=4e-3)
+
+
+def test_ring_fixture_helpers(orc):
+    g = json.load(open(os.path.join(GOLD, "ring_fixture.json")))
+    W, T = g["window"], g["prefill_tokens"]
+    rows = np.zeros((T, 4), np.uint16)
+    rows[:, 0] = np.arange(T) + 100  # tag rows by token
+    ring = np.zeros((W, 4), np.uint16)
+    orc.ring_write(ring, rows, 0)
+    assert list(ring[:, 0] - 100) == g["slot_token_after_prefill"]
+    for d in g["decode"]:
+        r = np.full((1, 4), 100 + d["pos"], np.uint16)
+        before = ring.copy()
+        orc.ring_write(ring, r, d["pos"])
+        changed = np.nonzero((ring != before).any(1))[0]
+        assert list(changed) == [d["write_slot"]]
+        if "read_slots_oldest_first" in d:
+            assert list(orc.window_idx_decode(d["pos"], W)) == d["read_slots_oldest_first"]
+            # oldest first means ascending token order along the read
+            toks = ring[orc.window_idx_decode(d["pos"], W), 0] - 100
+            assert list(toks) == list(range(d["pos"] - W + 1, d["pos"] + 1))
+
+
+def test_window_idx_prefill_and_young_ring(orc):
+    idx = orc.window_idx_prefill(12, 8)
+    assert list(idx[0]) == [-1] * 7 + [0]
+    assert list(idx[3]) == [-1] * 4 + [0, 1, 2, 3]
+    assert list(idx[11]) == list(range(4, 12))
+    # a decode step before the ring is full: slots never written are -1
+    assert list(orc.window_idx_decode(2, 8)) == [-1] * 5 + [0, 1, 2]
+    assert list(orc.window_idx_decode(7, 8)) == list(range(8))
+
+
+def test_ring_fixture_through_layer(orc):
+    """The fixture's three regimes in order through one ring, with the layer's own kv rows."""
+    from csa_inputs import WORKLOADS, weights, activations
+    wl = WORKLOADS["tiny_ratio0"]
+    g = wl.geom.as_dict()
+    fx = json.load(open(os.path.join(GOLD, "ring_fixture.json")))
+    w = weights(wl.geom, with_indexer=False)
+    x = activations(wl.geom, 1, 14)
+    tab = orc.rope_table(g["rope_dim"], g["max_seq"], g["rope_theta"])
+    ring = np.zeros((1, g["window"], g["head_dim"]), np.uint16)
+    r0 = orc.attn_forward(g, dict(ratio=0), w, ring, x[:, :12], 0, tab)
+    kv = r0["kv"]
+    for slot, tok in enumerate(fx["slot_token_after_prefill"]):
+        assert np.array_equal(ring[0, slot], kv[tok])
+    for step in fx["decode"]:
+        p = step["pos"]
+        r = orc.attn_forward(g, dict(ratio=0), w, ring, x[:, p:p + 1], p, tab)
+        assert np.array_equal(ring[0, step["write_slot"]], r["kv"][0])
+        if "read_slots_oldest_first" in step:
+            assert list(r["idx"][0]) == step["read_slots_oldest_first"]
+    # prefill window selection is the chunk's causal window
+    assert list(r0["idx"][11]) == list(range(4, 12)) and list(r0["idx"][2]) == [-1] * 5 + [0, 1, 2]
