@@ -1,0 +1,473 @@
+#!/usr/bin/env python3
+"""Benchmark of the compressed sparse attention layer core on GB300.
+
+One step = one pass of the whole layer (attn_v41_forward: projections, RoPE, fp8 window rows, ring,
+indexer scores, top-k, sparse attention with the sink, grouped output) for one batch of the
+workload, inputs resident in HBM.  The metric is decode tokens per second per layer; the line
+also reports the sparse-attention + indexer + top-k HBM bandwidth against 8 TB/s and the measured
+copy bandwidth, the dominant kernel's roofline, an end-to-end figure through the host-buffer entry
+point, and the CPU oracle timed on a bounded sample.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl csa|reference]
+
+Timing: W untimed steps, then K steps captured once as a CUDA graph and replayed, each bracketed
+by CUDA events on the launching stream; L2 is flushed (a 512 MiB memset) between timed steps and
+outside the event pair.  N > 1 (torchrun): every rank runs the full workload on its own GPU
+(replicas, weak scaling, no collective on the data path); value = all ranks' tokens / the slowest
+rank's time.
+"""
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode tokens/s per layer; sparse_attn+indexer HBM GB/s vs 8 TB/s (1×GB300)"
+DEFAULT_WORKLOAD = "reindex_decode_r2"
+NOMINAL_HBM_GBS = 8000.0
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="csa", choices=["csa", "reference"])
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle baseline")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def measured_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        return None
+
+
+# --------------------------------------------------------------------------------------- inputs
+
+def build_inputs(wl, rank=0):
+    """Seeded numpy inputs of the workload (bf16 as uint16 bit patterns)."""
+    from csa_inputs import activations, candidate_mask, latent_cache, positions, ring_rows, weights
+    g = wl.geom
+    B, T, start = wl.batch, wl.tokens, wl.start_pos
+    layers = []
+    for l in range(wl.layers):
+        layers.append(weights(g, with_indexer=wl.is_index_source, seed_base=1000 + 100 * l))
+    x = activations(g, B, T, seed_base=1000 + 7 * rank)
+    ring = ring_rows(g, B) if start else np.zeros((B, g.window, g.head_dim), np.uint16)
+    shared = None
+    if wl.ratio:
+        L = wl.compress_len
+        Z, KI = latent_cache(g, B, L)
+        pos = positions(B, T, start)
+        cand = None
+        if wl.uses_candidates:
+            cand = candidate_mask(B * T, pos, wl.ratio, L, g.cand_block, -(-L // g.cand_block), wl.cand_keep, 1015)
+        shared = dict(Z=Z, KI=KI, L=L, cand=cand)
+    return layers, x, ring, shared
+
+
+def algorithmic_bytes(wl, shared_np, idx_counts):
+    """Per-step algorithmic bytes of the sparse attention, indexer and top-k (all layers), from the
+    workload's selection sizes: q and output once, each gathered row once, each candidate key once."""
+    g = wl.geom
+    H, hd, NT = g.n_heads, g.head_dim, wl.batch * wl.tokens
+    rows, n_valid = idx_counts
+    attn = NT * (H * hd * 2 * 2 + (g.window + (g.index_topk if wl.ratio else 0)) * 4) + rows * hd * 2
+    idx = topk = 0
+    if wl.ratio and wl.is_index_source:
+        cw = 0 if shared_np["cand"] is None else shared_np["cand"].shape[1]
+        idx = NT * (g.index_heads * g.index_hd * 2 + g.index_heads * 4 + cw) + n_valid * (g.index_hd * 2 + 4)
+        topk = NT * (cw + g.index_topk * 4) + n_valid * 4
+    return attn * wl.layers, idx * wl.layers, topk * wl.layers
+
+
+def selection_counts(wl, shared_np):
+    """(gathered rows, valid compressed positions) summed over the batch's queries."""
+    g = wl.geom
+    B, T, start = wl.batch, wl.tokens, wl.start_pos
+    rows = n_valid = 0
+    for r in range(B * T):
+        t = r % T
+        p = start + t
+        rows += min(p + 1, g.window)
+        if wl.ratio:
+            limit = min((p + 1) // wl.ratio, shared_np["L"])
+            if shared_np["cand"] is not None:
+                c = shared_np["cand"][r]
+                nv = sum(min(g.cand_block, limit - b * g.cand_block) for b in range(len(c))
+                         if c[b] and b * g.cand_block < limit)
+            else:
+                nv = limit
+            n_valid += nv
+            rows += min(nv, g.index_topk)
+    return rows, n_valid
+
+
+# --------------------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.dev = device_index
+        self.p = None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + self.FIELDS,
+                                       "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f,
+                                      stderr=subprocess.DEVNULL)
+        except Exception:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return None
+        time.sleep(0.25)
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except Exception:
+            self.p.kill()
+        self.f.flush()
+        self.f.seek(0)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.f.read().splitlines():
+            parts = [s.strip() for s in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.f.name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------------------- CPU oracle
+
+def oracle_sample(wl, layers, x, ring, shared_np, seqs, tok_rows=None):
+    """One oracle layer pass (all layers of the workload) over a subset of the batch."""
+    import oracle as orc
+    g = wl.geom
+    gd = g.as_dict()
+    T, start = wl.tokens, wl.start_pos
+    tab = orc.rope_table(g.rope_dim, g.max_seq, g.compress_rope_theta if wl.ratio else g.rope_theta,
+                         g.orig_seq if wl.ratio else 0, g.rope_factor, g.beta_fast, g.beta_slow)
+    role = dict(ratio=wl.ratio, is_index_source=int(wl.is_index_source), uses_candidates=int(wl.uses_candidates))
+    ntok = 0
+    for b in seqs:
+        ring_b = orc.act_quant(ring[b:b + 1])[0] if start else ring[b:b + 1].copy()
+        sh = None
+        if shared_np is not None:
+            sh = dict(compress_kv=shared_np["Z"][b:b + 1], index_k=shared_np["KI"][b:b + 1], compress_len=shared_np["L"],
+                      topk_idxs=np.zeros((T, g.index_topk), np.int32))
+            if shared_np["cand"] is not None:
+                sh["candidates"] = shared_np["cand"][b * T:(b + 1) * T]
+        mask = None
+        if tok_rows is not None:
+            mask = np.zeros(T, np.uint8)
+            mask[tok_rows] = 1
+        for w in layers:
+            orc.attn_forward(gd, role, w, ring_b, x[b:b + 1], start, tab, sh, tok_mask=mask, debug=False)
+        ntok += T if tok_rows is None else len(tok_rows)
+    return ntok
+
+
+def cpu_baseline(wl, layers, x, ring, shared_np, target_s):
+    import oracle as orc
+    orc.build()
+    B, T = wl.batch, wl.tokens
+    tok_rows = None if T == 1 else list(range(0, T, max(1, T // 8)))[:8]
+    t0 = time.perf_counter()
+    ntok, nseq, b = 0, 0, 0
+    while True:
+        ntok += oracle_sample(wl, layers, x, ring, shared_np, [b % B], tok_rows)
+        nseq += 1
+        b += 1
+        if time.perf_counter() - t0 >= target_s or nseq >= 4 * B:
+            break
+    dt = time.perf_counter() - t0
+    what = "%d sequence(s) x %s of the %s workload, %d layer(s) each" % (
+        nseq, "1 decode token" if T == 1 else "%d sampled queries of the %d-token chunk" % (len(tok_rows), T),
+        wl.name, wl.layers)
+    return {"value": ntok / dt, "unit": "tokens/s", "cores": orc.num_threads(), "kind": "oracle", "sample": what,
+            "seconds": round(dt, 3)}
+
+
+# --------------------------------------------------------------------------------------- reference arm
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    from csa_inputs import WORKLOADS
+    import oracle as orc
+    orc.build()
+    wl = WORKLOADS[args.workload]
+    layers, x, ring, shared_np = build_inputs(wl)
+    T = wl.tokens
+    tok_rows = None if T == 1 else list(range(0, T, max(1, T // 4)))[:4]
+    seq_per_step = 1
+    for i in range(args.warmup):
+        oracle_sample(wl, layers, x, ring, shared_np, [i % wl.batch], tok_rows)
+    times, ntok = [], 0
+    for i in range(args.steps):
+        t0 = time.perf_counter()
+        ntok += oracle_sample(wl, layers, x, ring, shared_np, [(i * seq_per_step) % wl.batch], tok_rows)
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = ntok / total
+    sample = "per step: %s of one sequence of the %s workload, %d layer(s)" % (
+        "1 decode token" if T == 1 else "%d sampled queries" % len(tok_rows), wl.name, wl.layers)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": wl.name, "batch": wl.batch, "tokens": wl.tokens,
+                                            "start_pos": wl.start_pos, "ratio": wl.ratio, "layers": wl.layers},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": orc.num_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------------------- GPU arm
+
+def run_csa(args, rank, world, dist):
+    import torch
+    import compressed_sparse_attention_attn_gb300 as csa
+    from csa_inputs import WORKLOADS
+
+    dev = int(os.environ.get("LOCAL_RANK", 0))
+    torch.cuda.set_device(dev)
+    wl = WORKLOADS[args.workload]
+    g = wl.geom
+    gd = g.as_dict()
+    B, T, start, K = wl.batch, wl.tokens, wl.start_pos, g.index_topk
+    layers_np, x_np, ring_np, sh_np = build_inputs(wl, rank)
+
+    def dev_bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+
+    ctx = csa.Context(gd)
+    stream = torch.cuda.Stream()
+    torch.cuda.set_stream(stream)
+    role = dict(ratio=wl.ratio, is_index_source=int(wl.is_index_source), uses_candidates=int(wl.uses_candidates))
+    W = [{k: (dev_bf16(v) if v.dtype == np.uint16 else torch.from_numpy(v).cuda()) for k, v in w.items()}
+         for w in layers_np]
+    lws = [csa.Context.layer_weights(w, role) for w in W]
+    x = dev_bf16(x_np)
+    out = torch.empty_like(x)
+    rings = []
+    for _ in range(wl.layers):
+        r = dev_bf16(ring_np)
+        if start:
+            csa.act_quant(r)  # the ring holds fp8-rounded rows
+        rings.append(r)
+    shared = None
+    if sh_np is not None:
+        sel = torch.full((B * T, K), -1, dtype=torch.int32, device="cuda")
+        cand = None if sh_np["cand"] is None else torch.from_numpy(sh_np["cand"]).cuda()
+        shared = csa.Shared(dev_bf16(sh_np["Z"]), dev_bf16(sh_np["KI"]), sh_np["L"], sel, K, cand)
+
+    def step():
+        for l in range(wl.layers):
+            ctx.forward(None, role, rings[l], x, start, shared=shared, out=out, lw=lws[l])
+
+    flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+
+    def flush():
+        flush_buf.zero_()
+
+    def barrier():
+        torch.cuda.synchronize()
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    launches_per_step = ctx.last_launches() * wl.layers
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+
+    # ---- timed region
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(dev)
+    barrier()
+    clocks.start()
+    time.sleep(0.3)
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush()
+        ev[i][0].record(stream)
+        graph.replay()
+        ev[i][1].record(stream)
+    barrier()
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = sum(step_ms)
+    if dist is not None:
+        tmax = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
+        total_ms = float(tmax.item())
+    ms_per_step = total_ms / args.steps
+    tokens_per_step = B * T  # per layer per rank
+    value = world * tokens_per_step * wl.layers * args.steps / (total_ms / 1000.0)
+
+    # ---- per-stage kernel timing (traced forwards, flushed), for the roofline
+    ctx.trace(True)
+    acc = {}
+    for i in range(args.steps):
+        flush()
+        for l in range(wl.layers):
+            ctx.forward(None, role, rings[l], x, start, shared=shared, out=out, lw=lws[l])
+            for name, ms in ctx.trace_read():
+                a = acc.setdefault(name, [0.0, 0])
+                a[0] += ms
+                a[1] += 1
+    ctx.trace(False)
+    stage_ms = {k: v[0] / args.steps for k, v in acc.items()}  # per step (all layers)
+    lin_names = ("wq_a", "wq_b", "wkv", "idx_wq_b", "idx_wproj", "wo_a", "wo_b")
+    M = B * T
+    lin_shapes = {"wq_a": (g.q_rank, g.dim), "wq_b": (g.n_heads * g.head_dim, g.q_rank), "wkv": (g.head_dim, g.dim),
+                  "idx_wq_b": (g.index_heads * g.index_hd, g.q_rank), "idx_wproj": (g.index_heads, g.dim),
+                  "wo_a": (g.groups * g.o_rank, g.n_heads * g.head_dim // g.groups), "wo_b": (g.dim, g.groups * g.o_rank)}
+    lin_bytes = lin_ms = 0.0
+    for n in lin_names:
+        if n in stage_ms:
+            N_, K_ = lin_shapes[n]
+            xk = K_ * (g.groups if n == "wo_a" else 1)
+            lin_bytes += wl.layers * 2 * (N_ * K_ + M * xk + M * N_ * (g.groups if n == "wo_a" else 1))
+            lin_ms += stage_ms[n]
+    counts = selection_counts(wl, sh_np)
+    b_attn, b_idx, b_topk = algorithmic_bytes(wl, sh_np, counts)
+    t_attn = stage_ms.get("sparse_attn", 0.0)
+    t_idx = stage_ms.get("index scores", 0.0)
+    t_topk = stage_ms.get("index topk", 0.0)
+    ai_bytes = b_attn + b_idx + b_topk
+    ai_ms = t_attn + t_idx + t_topk
+    ai_gbs = ai_bytes / (ai_ms * 1e6) if ai_ms > 0 else None
+    peaks = measured_peaks()
+    hbm_peak = peaks["hbm_gbs"] if peaks else 6800.0
+    peak_src = "measured" if peaks else "fallback"
+    lin_gbs = lin_bytes / (lin_ms * 1e6) if lin_ms > 0 else 0.0
+    roofline = {"kernel": "linear (weight-streaming projections, all launches of one step)", "bound": "hbm",
+                "achieved": round(lin_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(lin_gbs / hbm_peak, 4), "traffic": None, "peak_source": peak_src,
+                "share_of_step": round(lin_ms / ms_per_step, 3) if ms_per_step else None}
+
+    # ---- end to end through the host-buffer entry point (pinned x in, out back to the host)
+    x_host = x.cpu().pin_memory()
+    out_host = torch.empty_like(x_host).pin_memory()
+
+    def step_host():
+        for l in range(wl.layers):
+            ctx.forward_host(lws[l], rings[l], x_host, start, shared, out_host, B, T)
+
+    for _ in range(2):
+        step_host()
+    torch.cuda.synchronize()
+    g2 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g2, stream=stream):
+        step_host()
+    ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier()
+    for i in range(args.steps):
+        flush()
+        ev2[i][0].record(stream)
+        g2.replay()
+        ev2[i][1].record(stream)
+    barrier()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in ev2)
+    if dist is not None:
+        tmax = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tmax.item())
+    e2e_value = world * tokens_per_step * wl.layers * args.steps / (e2e_ms / 1000.0)
+    io_bytes = wl.layers * B * T * g.dim * 2
+
+    line = None
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": wl.name, "batch": B, "tokens": T, "start_pos": start, "ratio": wl.ratio,
+                           "compress_len": wl.compress_len, "layers": wl.layers,
+                           "index_source": bool(wl.is_index_source), "candidates": bool(wl.uses_candidates),
+                           "l2": "flushed between timed steps (512 MiB memset outside the events)",
+                           "graph": "one step captured, replayed", "per_rank_batch": B},
+                "attn_indexer": {"bytes_per_step": int(ai_bytes), "ms_per_step": round(ai_ms, 5),
+                                 "achieved_gbs": None if ai_gbs is None else round(ai_gbs, 1),
+                                 "frac_of_8tbs": None if ai_gbs is None else round(ai_gbs / NOMINAL_HBM_GBS, 4),
+                                 "frac_of_measured": None if ai_gbs is None else round(ai_gbs / hbm_peak, 4),
+                                 "sparse_attn_ms": round(t_attn, 5), "index_scores_ms": round(t_idx, 5),
+                                 "index_topk_ms": round(t_topk, 5), "gathered_rows": counts[0],
+                                 "candidate_keys": counts[1]},
+                "stages_ms": {k: round(v, 5) for k, v in stage_ms.items()},
+                "roofline": roofline,
+                "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": io_bytes,
+                        "d2h_bytes_per_step": io_bytes},
+                "gpu_launches": launches_per_step * args.steps,
+                "clocks": clk, "wall_s": round(wall, 4)}
+    del graph, g2
+    return line, (wl, layers_np, x_np, ring_np, sh_np)
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist_
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        dist_.init_process_group("nccl")
+        dist = dist_
+    line, data = run_csa(args, rank, world, dist)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            wl, layers_np, x_np, ring_np, sh_np = data
+            line["cpu_baseline"] = cpu_baseline(wl, layers_np, x_np, ring_np, sh_np, args.cpu_seconds)
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

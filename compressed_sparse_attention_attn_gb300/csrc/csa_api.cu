@@ -1,0 +1,567 @@
+// csa_api.cu -- host side of the C ABI: context and workspaces, argument validation, the RoPE
+// tables, and the layer forward ("DeepSeek V4.1 - Compressed sparse attention", Attention.forward
+// excerpt; "metrale_model_arch::attn_v41" AttnV41 and its "Invariants").
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "csa_internal.cuh"
+
+using csa::bf16;
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char *where) {
+  return fail(CSA_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+#define CSA_CUDA(call, where)                         \
+  do {                                                \
+    cudaError_t e_ = (call);                          \
+    if (e_ != cudaSuccess) return cuda_fail(e_, where); \
+  } while (0)
+
+}  // namespace
+
+struct csa_ctx {
+  csa_cfg cfg;
+  int device = 0;
+  int num_sms = 0;
+  int max_nt = 0;
+  int tab_rows = 0;
+  float *tab_plain = nullptr, *tab_comp = nullptr;
+  bf16 *qr_raw = nullptr, *qr = nullptr, *q = nullptr, *kv_raw = nullptr, *kv = nullptr, *qI = nullptr,
+       *iw_raw = nullptr, *o = nullptr, *o_rot = nullptr, *og = nullptr, *x_stage = nullptr, *out_stage = nullptr;
+  float *wI = nullptr, *scores = nullptr;
+  int32_t *idx_win = nullptr;
+  int *status = nullptr;
+  float *ws = nullptr;  // split-K and split-row partials
+  size_t ws_bytes = 0;
+  int scores_stride = 0;
+  size_t bytes = 0;
+  std::vector<void *> allocs;
+  // tracing: one event pair per stage of the last forward, when enabled
+  struct Stage {
+    const char *name;
+    cudaEvent_t a, b;
+  };
+  int trace = 0;
+  std::vector<Stage> stages;
+  int n_stages = 0;
+  int launches = 0;
+
+  template <class T>
+  cudaError_t alloc(T **p, size_t n) {
+    void *v = nullptr;
+    size_t b = n * sizeof(T);
+    if (b == 0) b = 16;
+    cudaError_t e = cudaMalloc(&v, b);
+    if (e != cudaSuccess) return e;
+    allocs.push_back(v);
+    bytes += b;
+    *p = static_cast<T *>(v);
+    return cudaSuccess;
+  }
+  void release() {
+    for (void *p : allocs) cudaFree(p);
+    allocs.clear();
+    for (auto &st : stages) {
+      cudaEventDestroy(st.a);
+      cudaEventDestroy(st.b);
+    }
+    stages.clear();
+  }
+};
+
+namespace csa {
+
+// RoPE table, "deepseek_v41_ref::attn" freqs_cis: [max_seq][rd/2] of (cos, sin) with pair i at
+// frequency theta^(-2i/rd), angle p * f_i, taken in double and rounded to f32.  With YaRN
+// (Peng et al., 2023, frequency interpolation by parts) when max_seq exceeds the original length:
+// pairs that complete more than beta_fast turns over the original length keep f_i, those with
+// fewer than beta_slow turns use f_i / factor, with a linear ramp over the pair index between
+// floor(d(beta_fast)) and ceil(d(beta_slow)), d(n) = rd ln(L / (2 pi n)) / (2 ln theta).
+void build_rope_table(int rd, int max_seq, double theta, int orig_seq, double factor, double beta_fast,
+                      double beta_slow, float *tab) {
+  const int half = rd / 2;
+  std::vector<double> f(half);
+  for (int i = 0; i < half; ++i) f[i] = std::pow(theta, -2.0 * i / (double)rd);
+  if (orig_seq > 0 && max_seq > orig_seq) {
+    const double two_pi = 2.0 * 3.14159265358979323846264338327950288;
+    auto turns_to_index = [&](double n) { return rd * std::log(orig_seq / (two_pi * n)) / (2.0 * std::log(theta)); };
+    double lo = std::max(std::floor(turns_to_index(beta_fast)), 0.0);
+    double hi = std::min(std::ceil(turns_to_index(beta_slow)), (double)(rd - 1));
+    if (hi == lo) hi += 0.001;
+    for (int i = 0; i < half; ++i) {
+      const double ramp = std::min(std::max((i - lo) / (hi - lo), 0.0), 1.0);
+      f[i] = f[i] * (1.0 - ramp) + f[i] / factor * ramp;
+    }
+  }
+  for (int64_t p = 0; p < max_seq; ++p)
+    for (int i = 0; i < half; ++i) {
+      const double a = (double)p * f[i];
+      tab[(p * half + i) * 2] = (float)std::cos(a);
+      tab[(p * half + i) * 2 + 1] = (float)std::sin(a);
+    }
+}
+
+}  // namespace csa
+
+extern "C" {
+
+const char *attn_v41_last_error(void) { return g_err; }
+
+static int check_cfg(const csa_cfg *c) {
+  if (!c) return fail(CSA_ERR_ARG, "cfg is NULL");
+  if (c->dim <= 0 || c->n_heads <= 0 || c->head_dim <= 0 || c->q_rank <= 0 || c->o_rank <= 0 || c->groups <= 0 ||
+      c->window <= 0 || c->max_seq <= 0 || c->max_tokens <= 0 || c->max_batch <= 0)
+    return fail(CSA_ERR_ARG, "cfg: non-positive dimension");
+  if (c->head_dim % 64 != 0 || c->head_dim > 1024) return fail(CSA_ERR_ARG, "cfg: head_dim must be a multiple of 64, <= 1024");
+  if (c->rope_dim <= 0 || c->rope_dim % 2 || c->rope_dim > c->head_dim || (c->head_dim - c->rope_dim) % 2)
+    return fail(CSA_ERR_ARG, "cfg: rope_dim must be even and <= head_dim");
+  if ((c->n_heads * c->head_dim) % c->groups) return fail(CSA_ERR_ARG, "cfg: groups must divide n_heads*head_dim");
+  if (c->index_heads < 0 || c->index_hd < 0 || c->index_topk < 0) return fail(CSA_ERR_ARG, "cfg: negative indexer size");
+  if (c->index_heads > 0 && c->index_hd != 32 && c->index_hd != 64 && c->index_hd != 128)
+    return fail(CSA_ERR_ARG, "cfg: index_hd must be 32, 64 or 128");
+  if (c->index_topk > 2048) return fail(CSA_ERR_ARG, "cfg: index_topk above 2048");
+  if (c->cand_block <= 0) return fail(CSA_ERR_ARG, "cfg: cand_block must be positive");
+  return CSA_OK;
+}
+
+int csa_create(const csa_cfg *cfg, csa_ctx **out) {
+  if (!out) return fail(CSA_ERR_ARG, "out is NULL");
+  *out = nullptr;
+  int rc = check_cfg(cfg);
+  if (rc) return rc;
+  csa_ctx *c = new (std::nothrow) csa_ctx();
+  if (!c) return fail(CSA_ERR_NOMEM, "host allocation failed");
+  c->cfg = *cfg;
+  cudaError_t e = cudaGetDevice(&c->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device);
+  if (e != cudaSuccess) {
+    delete c;
+    return cuda_fail(e, "csa_create: device query");
+  }
+  const csa_cfg &g = *cfg;
+  const size_t nt = (size_t)g.max_batch * g.max_tokens;
+  c->max_nt = (int)nt;
+  const size_t H = g.n_heads, hd = g.head_dim;
+  const size_t Hi = g.index_heads, dI = g.index_hd;
+  c->tab_rows = g.max_seq;
+  c->scores_stride = g.max_seq;
+  const size_t tab_n = (size_t)g.max_seq * g.rope_dim;
+  c->ws_bytes = (size_t)128 << 20;
+#define ALLOC(ptr, n)                                            \
+  if (e == cudaSuccess) e = c->alloc(&c->ptr, (n));
+  ALLOC(tab_plain, tab_n);
+  ALLOC(tab_comp, tab_n);
+  ALLOC(qr_raw, nt * g.q_rank);
+  ALLOC(qr, nt * g.q_rank);
+  ALLOC(q, nt * H * hd);
+  ALLOC(kv_raw, nt * hd);
+  ALLOC(kv, nt * hd);
+  ALLOC(qI, nt * Hi * dI);
+  ALLOC(iw_raw, nt * Hi);
+  ALLOC(wI, nt * Hi);
+  ALLOC(scores, nt * (size_t)c->scores_stride);
+  ALLOC(idx_win, nt * (size_t)g.window);
+  ALLOC(o, nt * H * hd);
+  ALLOC(o_rot, nt * H * hd);
+  ALLOC(og, nt * (size_t)g.groups * g.o_rank);
+  ALLOC(x_stage, nt * g.dim);
+  ALLOC(out_stage, nt * g.dim);
+  ALLOC(status, 4);
+  {
+    float *w = nullptr;
+    if (e == cudaSuccess) e = c->alloc(&w, c->ws_bytes / sizeof(float));
+    c->ws = w;
+  }
+#undef ALLOC
+  if (e == cudaSuccess) e = cudaMemset(c->status, 0, 4 * sizeof(int));
+  if (e != cudaSuccess) {
+    c->release();
+    delete c;
+    return fail(CSA_ERR_NOMEM, "csa_create: workspace allocation: %s", cudaGetErrorString(e));
+  }
+  std::vector<float> tab(tab_n);
+  csa::build_rope_table(g.rope_dim, g.max_seq, g.rope_theta, 0, 1.0, g.beta_fast, g.beta_slow, tab.data());
+  e = cudaMemcpy(c->tab_plain, tab.data(), tab_n * sizeof(float), cudaMemcpyHostToDevice);
+  csa::build_rope_table(g.rope_dim, g.max_seq, g.compress_rope_theta, g.orig_seq, g.rope_factor, g.beta_fast,
+                        g.beta_slow, tab.data());
+  if (e == cudaSuccess) e = cudaMemcpy(c->tab_comp, tab.data(), tab_n * sizeof(float), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) {
+    c->release();
+    delete c;
+    return cuda_fail(e, "csa_create: table upload");
+  }
+  *out = c;
+  return CSA_OK;
+}
+
+int csa_destroy(csa_ctx *ctx) {
+  if (!ctx) return CSA_OK;
+  cudaDeviceSynchronize();
+  ctx->release();
+  delete ctx;
+  return CSA_OK;
+}
+
+size_t csa_workspace_bytes(const csa_ctx *ctx) { return ctx ? ctx->bytes : 0; }
+
+int csa_trace_enable(csa_ctx *ctx, int enable) {
+  if (!ctx) return fail(CSA_ERR_ARG, "csa_trace_enable: NULL context");
+  if (enable && ctx->stages.empty()) {
+    ctx->stages.resize(32);
+    for (auto &st : ctx->stages) {
+      CSA_CUDA(cudaEventCreate(&st.a), "csa_trace_enable");
+      CSA_CUDA(cudaEventCreate(&st.b), "csa_trace_enable");
+    }
+  }
+  ctx->trace = enable ? 1 : 0;
+  return CSA_OK;
+}
+
+int csa_trace_read(csa_ctx *ctx, int max, const char **names, float *ms) {
+  if (!ctx || (max > 0 && (!names || !ms))) return fail(CSA_ERR_ARG, "csa_trace_read: bad argument");
+  const int n = std::min(max, ctx->n_stages);
+  for (int i = 0; i < n; ++i) {
+    CSA_CUDA(cudaEventSynchronize(ctx->stages[i].b), "csa_trace_read");
+    names[i] = ctx->stages[i].name;
+    CSA_CUDA(cudaEventElapsedTime(&ms[i], ctx->stages[i].a, ctx->stages[i].b), "csa_trace_read");
+  }
+  return ctx->n_stages;
+}
+
+int csa_last_launches(const csa_ctx *ctx) { return ctx ? ctx->launches : 0; }
+
+int csa_rope_table_get(const csa_ctx *ctx, int ratio_class, float *tab_host) {
+  if (!ctx || !tab_host) return fail(CSA_ERR_ARG, "csa_rope_table_get: NULL argument");
+  const float *src = ratio_class ? ctx->tab_comp : ctx->tab_plain;
+  CSA_CUDA(cudaMemcpy(tab_host, src, sizeof(float) * (size_t)ctx->tab_rows * ctx->cfg.rope_dim, cudaMemcpyDeviceToHost),
+           "csa_rope_table_get");
+  return CSA_OK;
+}
+
+int csa_status(csa_ctx *ctx, int clear) {
+  if (!ctx) return fail(CSA_ERR_ARG, "csa_status: NULL context");
+  int st = 0;
+  CSA_CUDA(cudaDeviceSynchronize(), "csa_status: synchronize");
+  CSA_CUDA(cudaMemcpy(&st, ctx->status, sizeof(int), cudaMemcpyDeviceToHost), "csa_status: read");
+  if (clear) CSA_CUDA(cudaMemset(ctx->status, 0, sizeof(int)), "csa_status: clear");
+  if (st & csa::kStatusTimeout) return fail(CSA_ERR_DEVICE_TIMEOUT, "a bounded device-side wait ran out");
+  if (st & csa::kStatusBadIndex) return fail(CSA_ERR_ARG, "a selection index was outside [-1, rows)");
+  return CSA_OK;
+}
+
+int csa_state_init(csa_ctx *ctx, csa_layer_state *state, int batch, csa_stream stream) {
+  if (!ctx || !state || !state->window) return fail(CSA_ERR_ARG, "csa_state_init: NULL argument");
+  if (batch <= 0 || batch > ctx->cfg.max_batch) return fail(CSA_ERR_SHAPE, "csa_state_init: batch %d", batch);
+  CSA_CUDA(cudaMemsetAsync(state->window, 0, sizeof(bf16) * (size_t)batch * ctx->cfg.window * ctx->cfg.head_dim,
+                           (cudaStream_t)stream),
+           "csa_state_init");
+  return CSA_OK;
+}
+
+// ---------------------------------------------------------------------------------------------
+// per-step entry points
+// ---------------------------------------------------------------------------------------------
+
+int csa_linear(csa_ctx *ctx, const csa_bf16 *x, int M, int K, int ldx, const csa_bf16 *W, int N, int ldw, csa_bf16 *y,
+               int ldy, int groups, csa_stream stream) {
+  if (!ctx || !x || !W || !y) return fail(CSA_ERR_ARG, "csa_linear: NULL argument");
+  if (M < 0 || K <= 0 || N <= 0 || groups <= 0 || ldx < K * groups || ldw < K || ldy < N * groups)
+    return fail(CSA_ERR_ARG, "csa_linear: bad shape M=%d K=%d N=%d groups=%d", M, K, N, groups);
+  CSA_CUDA(csa::launch_linear((const bf16 *)x, M, K, ldx, (const bf16 *)W, N, ldw, (bf16 *)y, ldy, groups, ctx->ws,
+                              ctx->ws_bytes, ctx->num_sms, (cudaStream_t)stream),
+           "csa_linear");
+  return CSA_OK;
+}
+
+int csa_rmsnorm(const csa_bf16 *x, int M, int N, const float *w, float eps, csa_bf16 *y, csa_stream stream) {
+  if (!x || !w || !y || M < 0 || N <= 0) return fail(CSA_ERR_ARG, "csa_rmsnorm: bad argument");
+  CSA_CUDA(csa::launch_rmsnorm((const bf16 *)x, M, N, w, eps, (bf16 *)y, (cudaStream_t)stream), "csa_rmsnorm");
+  return CSA_OK;
+}
+
+int csa_rope(csa_bf16 *x, int64_t rows, int row_len, int rd, const int32_t *pos, int rows_per_pos, const float *tab,
+             int tab_rows, int inverse, csa_stream stream) {
+  if (!x || !pos || !tab || rows < 0 || rd <= 0 || rd % 2 || rd > row_len || (row_len - rd) % 2 || rows_per_pos <= 0 ||
+      tab_rows <= 0)
+    return fail(CSA_ERR_ARG, "csa_rope: bad argument");
+  csa::PosSpec ps{pos, 0, 1, rows_per_pos};
+  CSA_CUDA(csa::launch_rope((bf16 *)x, rows, row_len, rd, ps, tab, tab_rows, inverse, nullptr, (cudaStream_t)stream),
+           "csa_rope");
+  return CSA_OK;
+}
+
+int csa_act_quant(csa_bf16 *x, int64_t n, uint8_t *codes, int8_t *scale_exp, csa_stream stream) {
+  if (!x || n < 0 || n % 32) return fail(CSA_ERR_ARG, "csa_act_quant: n must be a multiple of 32");
+  CSA_CUDA(csa::launch_act_quant((bf16 *)x, n, codes, scale_exp, (cudaStream_t)stream), "csa_act_quant");
+  return CSA_OK;
+}
+
+int csa_kv_finish(const csa_bf16 *kv_in, csa_bf16 *kv_out, int B, int T, int start_pos, int hd, int rd,
+                  const float *tab, int tab_rows, csa_bf16 *ring, int W, int32_t *win_idx, int idx_stride,
+                  uint8_t *codes, int8_t *scales, csa_stream stream) {
+  if (!kv_in || !kv_out || !tab || !ring || B <= 0 || T <= 0 || start_pos < 0 || W <= 0)
+    return fail(CSA_ERR_ARG, "csa_kv_finish: bad argument");
+  if (hd % 32 || hd > 1024 || rd <= 0 || rd % 2 || rd > hd || (hd - rd) % 2)
+    return fail(CSA_ERR_ARG, "csa_kv_finish: hd must be a multiple of 32 (<= 1024), rd even");
+  if (start_pos > 0 && T != 1) return fail(CSA_ERR_SHAPE, "csa_kv_finish: decode takes one token per sequence");
+  if (start_pos + T > tab_rows) return fail(CSA_ERR_SHAPE, "csa_kv_finish: position beyond the table");
+  if (win_idx && idx_stride < W) return fail(CSA_ERR_ARG, "csa_kv_finish: idx_stride < W");
+  CSA_CUDA(csa::launch_kv_finish((const bf16 *)kv_in, (bf16 *)kv_out, B, T, start_pos, hd, rd, tab, (bf16 *)ring, W,
+                                 win_idx, idx_stride, codes, scales, (cudaStream_t)stream),
+           "csa_kv_finish");
+  return CSA_OK;
+}
+
+int csa_index_scores(const csa_bf16 *qI, const float *wI, const csa_bf16 *KI, int B, int T, int start_pos, int Hi,
+                     int dI, int Lstride, int compress_len, int ratio, const uint8_t *cand, int cand_width,
+                     int cand_block, float *S, csa_stream stream) {
+  if (!qI || !wI || !KI || !S || B <= 0 || T <= 0 || start_pos < 0 || Hi <= 0 || ratio <= 0 || Lstride <= 0 ||
+      compress_len < 0 || compress_len > Lstride)
+    return fail(CSA_ERR_ARG, "csa_index_scores: bad argument");
+  if (dI != 32 && dI != 64 && dI != 128) return fail(CSA_ERR_ARG, "csa_index_scores: dI must be 32, 64 or 128");
+  if (cand && (cand_block <= 0 || (int64_t)cand_width * cand_block < compress_len))
+    return fail(CSA_ERR_ARG, "csa_index_scores: candidate mask narrower than the cache");
+  CSA_CUDA(csa::launch_index_scores((const bf16 *)qI, wI, (const bf16 *)KI, B, T, start_pos, Hi, dI, Lstride,
+                                    compress_len, ratio, cand, cand_width, cand_block, S, (cudaStream_t)stream),
+           "csa_index_scores");
+  return CSA_OK;
+}
+
+int csa_index_topk(const float *S, int B, int T, int start_pos, int Lstride, int compress_len, int ratio,
+                   const uint8_t *cand, int cand_width, int cand_block, int K, int offset, int32_t *out,
+                   csa_stream stream) {
+  if (!S || !out || B <= 0 || T <= 0 || start_pos < 0 || ratio <= 0 || Lstride <= 0 || compress_len < 0 ||
+      compress_len > Lstride || K <= 0 || K > 2048)
+    return fail(CSA_ERR_ARG, "csa_index_topk: bad argument");
+  if (cand && (cand_block <= 0 || (int64_t)cand_width * cand_block < compress_len))
+    return fail(CSA_ERR_ARG, "csa_index_topk: candidate mask narrower than the cache");
+  CSA_CUDA(csa::launch_index_topk(S, B, T, start_pos, Lstride, compress_len, ratio, cand, cand_width, cand_block, K,
+                                  offset, out, (cudaStream_t)stream),
+           "csa_index_topk");
+  return CSA_OK;
+}
+
+int csa_sparse_attn(csa_ctx *ctx, const csa_bf16 *q, int B, int T, int H, int hd, const csa_bf16 *rows_a,
+                    int64_t a_seq_stride, int a_len, const csa_bf16 *rows_b, int64_t b_seq_stride, int b_len,
+                    const int32_t *idx_a, int na, const int32_t *idx_b, int nb, const float *sink, float scale,
+                    csa_bf16 *o, csa_bf16 *o_rot, int rd, int start_pos, const float *tab, int tab_rows,
+                    csa_stream stream) {
+  if (!ctx || !q || !rows_a || !idx_a || !sink || B <= 0 || T <= 0 || H <= 0 || a_len < 0 || b_len < 0 || na < 0 ||
+      nb < 0)
+    return fail(CSA_ERR_ARG, "csa_sparse_attn: bad argument");
+  if (hd % 64 || hd > 1024) return fail(CSA_ERR_ARG, "csa_sparse_attn: hd must be a multiple of 64, <= 1024");
+  if (nb > 0 && (!idx_b)) return fail(CSA_ERR_ARG, "csa_sparse_attn: idx_b is NULL");
+  if (b_len > 0 && !rows_b) return fail(CSA_ERR_ARG, "csa_sparse_attn: rows_b is NULL");
+  if (na + nb > 2048) return fail(CSA_ERR_TOO_WIDE, "csa_sparse_attn: selection of %d rows above 2048", na + nb);
+  if (o_rot && (!tab || rd <= 0 || rd % 2 || rd > hd || start_pos < 0 || start_pos + T > tab_rows))
+    return fail(CSA_ERR_ARG, "csa_sparse_attn: inverse rotation needs a table covering the positions");
+  csa::AttnArgs a{(const bf16 *)q, B, T, H, hd, (const bf16 *)rows_a, a_seq_stride, a_len, (const bf16 *)rows_b,
+                  b_seq_stride, b_len, idx_a, na, idx_b, nb, sink, scale, (bf16 *)o, (bf16 *)o_rot, rd, start_pos,
+                  tab, ctx->status};
+  CSA_CUDA(csa::launch_sparse_attn(a, ctx->ws, ctx->ws_bytes, ctx->num_sms, (cudaStream_t)stream), "csa_sparse_attn");
+  return CSA_OK;
+}
+
+// ---------------------------------------------------------------------------------------------
+// the layer
+// ---------------------------------------------------------------------------------------------
+
+static int check_forward(const csa_ctx *ctx, const csa_layer_weights *w, const csa_layer_state *st, const void *x,
+                         int B, int T, int start_pos, const csa_shared *sh, const void *out) {
+  if (!ctx || !w || !st || !st->window || !x || !out) return fail(CSA_ERR_ARG, "attn_v41_forward: NULL argument");
+  const csa_cfg &g = ctx->cfg;
+  const csa_role &r = w->role;
+  if (!w->sink || !w->q_norm || !w->kv_norm || !w->wq_a || !w->wq_b || !w->wkv || !w->wo_a || !w->wo_b)
+    return fail(CSA_ERR_ARG, "attn_v41_forward: a weight pointer is NULL");
+  if (r.ratio < 0) return fail(CSA_ERR_ARG, "attn_v41_forward: negative ratio");
+  if (r.is_kv_source || r.is_candidate_source)
+    return fail(CSA_ERR_UNSUPPORTED, "attn_v41_forward: kv-source and candidate-source roles are not implemented");
+  if (B <= 0 || B > g.max_batch) return fail(CSA_ERR_SHAPE, "attn_v41_forward: batch %d outside [1, %d]", B, g.max_batch);
+  if (T <= 0 || T > g.max_tokens) return fail(CSA_ERR_SHAPE, "attn_v41_forward: T %d outside [1, %d]", T, g.max_tokens);
+  if (start_pos < 0 || (int64_t)start_pos + T > g.max_seq)
+    return fail(CSA_ERR_SHAPE, "attn_v41_forward: positions [%d, %d) beyond max_seq %d", start_pos, start_pos + T, g.max_seq);
+  if (start_pos > 0 && T != 1) return fail(CSA_ERR_SHAPE, "attn_v41_forward: decode takes one token per sequence");
+  if (r.ratio > 0) {
+    if (!sh || !sh->compress_kv) return fail(CSA_ERR_NO_KV_SOURCE, "attn_v41_forward: ratio > 0 and no latent cache published");
+    if (sh->compress_len < 0 || sh->compress_stride < sh->compress_len || sh->compress_stride <= 0)
+      return fail(CSA_ERR_ARG, "attn_v41_forward: compress_len / compress_stride");
+    if (!sh->topk_idxs) return fail(CSA_ERR_ARG, "attn_v41_forward: shared topk_idxs buffer is NULL");
+    if (sh->topk != g.index_topk) return fail(CSA_ERR_ARG, "attn_v41_forward: shared topk %d != index_topk %d", sh->topk, g.index_topk);
+    const int width = g.window + g.index_topk;
+    if (width > 2048) return fail(CSA_ERR_TOO_WIDE, "attn_v41_forward: selection of %d rows above 2048", width);
+    if (r.is_index_source) {
+      if (!w->idx_wq_b || !w->idx_wproj) return fail(CSA_ERR_ARG, "attn_v41_forward: index source without indexer weights");
+      if (!sh->index_k) return fail(CSA_ERR_NO_KV_SOURCE, "attn_v41_forward: index source and no index keys published");
+      if (g.index_heads <= 0) return fail(CSA_ERR_ARG, "attn_v41_forward: cfg has no indexer");
+      if (sh->compress_stride > ctx->scores_stride) return fail(CSA_ERR_SHAPE, "attn_v41_forward: compress_stride above max_seq");
+      if (r.uses_candidates && (!sh->candidates || (int64_t)sh->cand_width * g.cand_block < sh->compress_len))
+        return fail(CSA_ERR_ARG, "attn_v41_forward: candidate mask missing or narrower than the cache");
+    } else if (!sh->has_topk) {
+      return fail(CSA_ERR_NO_SELECTION, "attn_v41_forward: reuse layer and no selection published");
+    }
+  }
+  return CSA_OK;
+}
+
+int attn_v41_forward(csa_ctx *ctx, const csa_layer_weights *w, csa_layer_state *st, const csa_bf16 *x_, int B, int T,
+                     int start_pos, csa_shared *sh, csa_bf16 *out_, const csa_debug *dbg, csa_stream stream_) {
+  int rc = check_forward(ctx, w, st, x_, B, T, start_pos, sh, out_);
+  if (rc) return rc;
+  const csa_cfg &g = ctx->cfg;
+  const csa_role &r = w->role;
+  cudaStream_t s = (cudaStream_t)stream_;
+  const bf16 *x = (const bf16 *)x_;
+  bf16 *out = (bf16 *)out_;
+  const int NT = B * T, H = g.n_heads, hd = g.head_dim, rd = g.rope_dim, W = g.window;
+  const int G = g.groups, gw = H * hd / G;
+  const bool decode = start_pos > 0;
+  const float *tab = r.ratio > 0 ? ctx->tab_comp : ctx->tab_plain;
+  const csa::PosSpec pos_q{nullptr, start_pos, T, H};
+  bf16 *q = dbg && dbg->q ? (bf16 *)dbg->q : ctx->q;
+  bf16 *kv = dbg && dbg->kv ? (bf16 *)dbg->kv : ctx->kv;
+  bf16 *qr = dbg && dbg->qr ? (bf16 *)dbg->qr : ctx->qr;
+  bf16 *o = dbg && dbg->o ? (bf16 *)dbg->o : nullptr;
+  bf16 *og = dbg && dbg->og ? (bf16 *)dbg->og : ctx->og;
+  int32_t *win_idx = ctx->idx_win;
+  int idx_stride = W;
+  if (dbg && dbg->idx) {
+    win_idx = dbg->idx;
+    idx_stride = W + (r.ratio > 0 ? g.index_topk : 0);
+  }
+  ctx->n_stages = 0;
+  ctx->launches = 0;
+  // one traced stage: events around it when tracing is on; counts the kernels it launches
+#define STAGE(call, what, kernels)                                                             \
+  do {                                                                                         \
+    csa_ctx::Stage *st_ = nullptr;                                                             \
+    if (ctx->trace && ctx->n_stages < (int)ctx->stages.size()) {                               \
+      st_ = &ctx->stages[ctx->n_stages++];                                                     \
+      st_->name = what;                                                                        \
+      cudaEventRecord(st_->a, s);                                                              \
+    }                                                                                          \
+    cudaError_t e_ = (call);                                                                   \
+    if (e_ != cudaSuccess) return cuda_fail(e_, what);                                         \
+    if (st_) cudaEventRecord(st_->b, s);                                                       \
+    ctx->launches += (kernels);                                                                \
+  } while (0)
+#define STEP(call, what) STAGE(call, what, 1)
+#define COPY(call, what) STAGE(call, what, 0)
+  // q path: qr = q_norm(wq_a x); q = wq_b qr; RoPE on the last rd of each head
+  STEP(csa::launch_linear(x, NT, g.dim, g.dim, (const bf16 *)w->wq_a, g.q_rank, g.dim, ctx->qr_raw, g.q_rank, 1, ctx->ws,
+                          ctx->ws_bytes, ctx->num_sms, s),
+       "wq_a");
+  STEP(csa::launch_rmsnorm(ctx->qr_raw, NT, g.q_rank, w->q_norm, g.eps, qr, s), "q_norm");
+  STEP(csa::launch_linear(qr, NT, g.q_rank, g.q_rank, (const bf16 *)w->wq_b, H * hd, g.q_rank, q, H * hd, 1, ctx->ws,
+                          ctx->ws_bytes, ctx->num_sms, s),
+       "wq_b");
+  STEP(csa::launch_rope(q, (int64_t)NT * H, hd, rd, pos_q, tab, ctx->tab_rows, 0, ctx->status, s), "rope q");
+  // kv path: kv_norm(wkv x) -> RoPE -> fp8 round trip -> ring + window selection
+  STEP(csa::launch_linear(x, NT, g.dim, g.dim, (const bf16 *)w->wkv, hd, g.dim, ctx->kv_raw, hd, 1, ctx->ws, ctx->ws_bytes,
+                          ctx->num_sms, s),
+       "wkv");
+  STEP(csa::launch_rmsnorm(ctx->kv_raw, NT, hd, w->kv_norm, g.eps, ctx->kv_raw, s), "kv_norm");
+  STEP(csa::launch_kv_finish(ctx->kv_raw, kv, B, T, start_pos, hd, rd, tab, (bf16 *)st->window, W, win_idx, idx_stride,
+                             dbg ? dbg->kv_codes : nullptr, dbg ? dbg->kv_scale : nullptr, s),
+       "kv_finish");
+  // the compressed selection
+  const int32_t *idx_b = nullptr;
+  int nb = 0;
+  const bf16 *rows_b = nullptr;
+  int b_len = 0;
+  int64_t b_stride = 0;
+  const int rows_a_len = decode ? W : T;
+  if (r.ratio > 0) {
+    const int K = g.index_topk;
+    if (r.is_index_source) {
+      const int Hi = g.index_heads, dI = g.index_hd;
+      bf16 *qI = dbg && dbg->qI ? (bf16 *)dbg->qI : ctx->qI;
+      float *wI = dbg && dbg->wI ? dbg->wI : ctx->wI;
+      float *S = dbg && dbg->scores ? dbg->scores : ctx->scores;
+      STEP(csa::launch_linear(qr, NT, g.q_rank, g.q_rank, (const bf16 *)w->idx_wq_b, Hi * dI, g.q_rank, qI, Hi * dI, 1,
+                              ctx->ws, ctx->ws_bytes, ctx->num_sms, s),
+           "idx_wq_b");
+      STEP(csa::launch_linear(x, NT, g.dim, g.dim, (const bf16 *)w->idx_wproj, Hi, g.dim, ctx->iw_raw, Hi, 1, ctx->ws,
+                              ctx->ws_bytes, ctx->num_sms, s),
+           "idx_wproj");
+      STEP(csa::launch_scale_bf16_to_f32(ctx->iw_raw, (int64_t)NT * Hi, (float)(1.0 / std::sqrt((double)dI * Hi)), wI, s),
+           "w^I scale");
+      const uint8_t *cand = r.uses_candidates ? sh->candidates : nullptr;
+      STEP(csa::launch_index_scores(qI, wI, (const bf16 *)sh->index_k, B, T, start_pos, Hi, dI, sh->compress_stride,
+                                    sh->compress_len, r.ratio, cand, sh->cand_width, g.cand_block, S, s),
+           "index scores");
+      STEP(csa::launch_index_topk(S, B, T, start_pos, sh->compress_stride, sh->compress_len, r.ratio, cand,
+                                  sh->cand_width, g.cand_block, K, rows_a_len, sh->topk_idxs, s),
+           "index topk");
+      sh->has_topk = 1;
+    }
+    idx_b = sh->topk_idxs;
+    nb = K;
+    rows_b = (const bf16 *)sh->compress_kv;
+    b_len = sh->compress_len;
+    b_stride = (int64_t)sh->compress_stride * hd;
+    if (dbg && dbg->idx)
+      COPY(cudaMemcpy2DAsync(dbg->idx + W, sizeof(int32_t) * (W + K), sh->topk_idxs, sizeof(int32_t) * K,
+                             sizeof(int32_t) * K, NT, cudaMemcpyDeviceToDevice, s),
+           "debug idx");
+  }
+  // sparse attention over [rows_a; rows_b] with the inverse rotation of the output fused
+  csa::AttnArgs a{q, B, T, H, hd,
+                  decode ? (const bf16 *)st->window : kv, decode ? (int64_t)W * hd : (int64_t)T * hd, rows_a_len,
+                  rows_b, b_stride, b_len,
+                  win_idx, W, idx_b, nb, w->sink, (float)(1.0 / std::sqrt((double)hd)), o, ctx->o_rot, rd, start_pos,
+                  tab, ctx->status};
+  // the window selection in the debug buffer is strided; pass the stride through idx_a's row length
+  if (idx_stride != W) {
+    // compact copy of the window columns for the kernel
+    COPY(cudaMemcpy2DAsync(ctx->idx_win, sizeof(int32_t) * W, win_idx, sizeof(int32_t) * idx_stride,
+                           sizeof(int32_t) * W, NT, cudaMemcpyDeviceToDevice, s),
+         "window idx");
+    a.idx_a = ctx->idx_win;
+  }
+  STEP(csa::launch_sparse_attn(a, ctx->ws, ctx->ws_bytes, ctx->num_sms, s), "sparse_attn");
+  // grouped output: og[:, g] = o_rot[:, g*gw:(g+1)*gw] wo_a[g]^T, then out = og wo_b^T
+  STEP(csa::launch_linear(ctx->o_rot, NT, gw, H * hd, (const bf16 *)w->wo_a, g.o_rank, gw, og, G * g.o_rank, G, ctx->ws,
+                          ctx->ws_bytes, ctx->num_sms, s),
+       "wo_a");
+  STEP(csa::launch_linear(og, NT, G * g.o_rank, G * g.o_rank, (const bf16 *)w->wo_b, g.dim, G * g.o_rank, out, g.dim, 1,
+                          ctx->ws, ctx->ws_bytes, ctx->num_sms, s),
+       "wo_b");
+#undef STEP
+#undef COPY
+#undef STAGE
+  return CSA_OK;
+}
+
+int attn_v41_forward_host(csa_ctx *ctx, const csa_layer_weights *w, csa_layer_state *st, const csa_bf16 *x_host, int B,
+                          int T, int start_pos, csa_shared *sh, csa_bf16 *out_host, csa_stream stream) {
+  if (!ctx || !x_host || !out_host) return fail(CSA_ERR_ARG, "attn_v41_forward_host: NULL argument");
+  int rc = check_forward(ctx, w, st, x_host, B, T, start_pos, sh, out_host);
+  if (rc) return rc;
+  const size_t bytes = sizeof(csa_bf16) * (size_t)B * T * ctx->cfg.dim;
+  cudaStream_t s = (cudaStream_t)stream;
+  CSA_CUDA(cudaMemcpyAsync(ctx->x_stage, x_host, bytes, cudaMemcpyHostToDevice, s), "attn_v41_forward_host: H2D");
+  rc = attn_v41_forward(ctx, w, st, (const csa_bf16 *)ctx->x_stage, B, T, start_pos, sh, (csa_bf16 *)ctx->out_stage,
+                        nullptr, stream);
+  if (rc) return rc;
+  CSA_CUDA(cudaMemcpyAsync(out_host, ctx->out_stage, bytes, cudaMemcpyDeviceToHost, s), "attn_v41_forward_host: D2H");
+  return CSA_OK;
+}
+
+}  // extern "C"

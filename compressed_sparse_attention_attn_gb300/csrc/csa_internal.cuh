@@ -1,0 +1,79 @@
+// csa_internal.cuh -- declarations shared by the library's translation units (not installed).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+#include <cstddef>
+
+#include "../../include/csa.h"
+
+namespace csa {
+
+using bf16 = __nv_bfloat16;
+
+// Bits of the device status word (csa_status).
+constexpr int kStatusBadIndex = 1;
+constexpr int kStatusTimeout = 2;
+
+// Position of row r: pos[r / rows_per_pos] from an array, or start + (r / rows_per_pos) % T.
+struct PosSpec {
+  const int32_t *arr;
+  int start;
+  int T;
+  int rows_per_pos;
+  __device__ __forceinline__ int at(int64_t r) const {
+    int64_t tok = r / rows_per_pos;
+    return arr ? arr[tok] : start + (int)(tok % T);
+  }
+};
+
+// ---- launchers (each returns a cudaError_t of the launch) ---------------------------------------
+
+cudaError_t launch_rmsnorm(const bf16 *x, int M, int N, const float *w, float eps, bf16 *y, cudaStream_t s);
+cudaError_t launch_rope(bf16 *x, int64_t rows, int row_len, int rd, PosSpec pos, const float *tab, int tab_rows,
+                        int inverse, int *status, cudaStream_t s);
+cudaError_t launch_act_quant(bf16 *x, int64_t n, uint8_t *codes, int8_t *scale_exp, cudaStream_t s);
+cudaError_t launch_kv_finish(const bf16 *kv_in, bf16 *kv_out, int B, int T, int start_pos, int hd, int rd,
+                             const float *tab, bf16 *ring, int W, int32_t *win_idx, int idx_stride, uint8_t *codes,
+                             int8_t *scales, cudaStream_t s);
+cudaError_t launch_scale_bf16_to_f32(const bf16 *x, int64_t n, float scale, float *y, cudaStream_t s);
+
+// y[M][N] (+ groups) = x W^T with f32 accumulation, bf16 out.  ws/ws_bytes: split-K workspace.
+cudaError_t launch_linear(const bf16 *x, int M, int K, int ldx, const bf16 *W, int N, int ldw, bf16 *y, int ldy,
+                          int groups, float *ws, size_t ws_bytes, int num_sms, cudaStream_t s);
+
+cudaError_t launch_index_scores(const bf16 *qI, const float *wI, const bf16 *KI, int B, int T, int start_pos, int Hi,
+                                int dI, int Lstride, int compress_len, int ratio, const uint8_t *cand, int cand_width,
+                                int cand_block, float *S, cudaStream_t s);
+cudaError_t launch_index_topk(const float *S, int B, int T, int start_pos, int Lstride, int compress_len, int ratio,
+                              const uint8_t *cand, int cand_width, int cand_block, int K, int offset, int32_t *out,
+                              cudaStream_t s);
+
+struct AttnArgs {
+  const bf16 *q;
+  int B, T, H, hd;
+  const bf16 *rows_a;
+  int64_t a_seq_stride;
+  int a_len;
+  const bf16 *rows_b;
+  int64_t b_seq_stride;
+  int b_len;
+  const int32_t *idx_a;
+  int na;
+  const int32_t *idx_b;
+  int nb;
+  const float *sink;
+  float scale;
+  bf16 *o, *o_rot;
+  int rd, start_pos;
+  const float *tab;
+  int *status;
+};
+cudaError_t launch_sparse_attn(const AttnArgs &a, float *ws, size_t ws_bytes, int num_sms, cudaStream_t s);
+
+// Host-side tables (double precision, rounded to f32).
+void build_rope_table(int rd, int max_seq, double theta, int orig_seq, double factor, double beta_fast,
+                      double beta_slow, float *tab);
+
+}  // namespace csa

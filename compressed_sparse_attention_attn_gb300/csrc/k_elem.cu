@@ -1,0 +1,216 @@
+// k_elem.cu -- row-wise kernels of the layer core: RMSNorm, RoPE, the fp8 round trip, and the fused
+// window-row finish (RoPE + fp8 + ring update + window selection).
+//
+// Each is bandwidth-trivial (a few KiB per token); they are written for exactness first: the RoPE
+// complex product rounds each product and each sum to f32 separately (__fmul_rn / __fadd_rn, no
+// contraction), the fp8 scale uses IEEE division (__fdiv_rn), and e4m3 conversion is the hardware
+// round-to-nearest-even saturating convert.
+#include <cuda_fp8.h>
+
+#include "csa_internal.cuh"
+
+namespace csa {
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// ---------------------------------------------------------------------------------------------
+// RMSNorm, "deepseek_v41_ref::attn" precision contract: f32 compute, bf16 result.
+// One CTA per row; the sum of squares in f32 (warp shuffles, then shared memory).
+// ---------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_rmsnorm(const bf16 *x, int N, const float *__restrict__ w,
+                                                 float eps, bf16 *y) {
+  const int64_t row = blockIdx.x;
+  const bf16 *xr = x + row * N;
+  bf16 *yr = y + row * N;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < N; i += blockDim.x) {
+    float v = __bfloat162float(xr[i]);
+    ss = fmaf(v, v, ss);
+  }
+  __shared__ float part[32];
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v = threadIdx.x < (blockDim.x >> 5) ? part[threadIdx.x] : 0.f;
+    v = warp_sum(v);
+    if (threadIdx.x == 0) part[0] = v;
+  }
+  __syncthreads();
+  const float r = 1.0f / sqrtf(part[0] / (float)N + eps);
+  for (int i = threadIdx.x; i < N; i += blockDim.x) yr[i] = __float2bfloat16_rn(__bfloat162float(xr[i]) * r * w[i]);
+}
+
+cudaError_t launch_rmsnorm(const bf16 *x, int M, int N, const float *w, float eps, bf16 *y, cudaStream_t s) {
+  if (M <= 0) return cudaSuccess;
+  k_rmsnorm<<<M, 256, 0, s>>>(x, N, w, eps, y);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------------------------
+// RoPE, "deepseek_v41_ref::attn" apply_rotary: last rd elements of each row, adjacent pairs as
+// complex numbers times (cos, sin) of the row's position (conjugate when inverse).
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ void rotate_pair(float a, float b, float c, float s, float &re, float &im) {
+  re = __fsub_rn(__fmul_rn(a, c), __fmul_rn(b, s));
+  im = __fadd_rn(__fmul_rn(a, s), __fmul_rn(b, c));
+}
+
+// One warp per row; lane i takes pairs i, i+32, ...
+__global__ void k_rope(bf16 *__restrict__ x, int64_t rows, int row_len, int rd, PosSpec pos,
+                       const float *__restrict__ tab, int tab_rows, int inverse, int *status) {
+  const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const int lane = threadIdx.x & 31;
+  const int half = rd >> 1;
+  const int p = pos.at(row);
+  if (p < 0 || p >= tab_rows) {  // a position outside the table: leave the row, report it
+    if (lane == 0 && status) atomicOr(status, kStatusBadIndex);
+    return;
+  }
+  __nv_bfloat162 *t = reinterpret_cast<__nv_bfloat162 *>(x + row * row_len + (row_len - rd));
+  const float2 *tp = reinterpret_cast<const float2 *>(tab) + (int64_t)p * half;
+  for (int i = lane; i < half; i += 32) {
+    float2 cs = tp[i];
+    float sn = inverse ? -cs.y : cs.y;
+    __nv_bfloat162 v = t[i];
+    float re, im;
+    rotate_pair(__low2float(v), __high2float(v), cs.x, sn, re, im);
+    t[i] = __halves2bfloat162(__float2bfloat16_rn(re), __float2bfloat16_rn(im));
+  }
+}
+
+cudaError_t launch_rope(bf16 *x, int64_t rows, int row_len, int rd, PosSpec pos, const float *tab, int tab_rows,
+                        int inverse, int *status, cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  const int warps = 8;
+  k_rope<<<(unsigned)((rows + warps - 1) / warps), warps * 32, 0, s>>>(x, rows, row_len, rd, pos, tab, tab_rows,
+                                                                       inverse, status);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------------------------
+// fp8 round trip of one block of 32 held one value per lane ("deepseek_v41_ref::attn"
+// act_quant_inplace, pow2_ceil).  Returns the new value; *code / *sexp for the lane's element and
+// the block's scale exponent.
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ float pow2_ceil_f(float v) {
+  uint32_t u = __float_as_uint(v);
+  if ((u & 0x007fffffu) == 0u) return v;
+  return __uint_as_float(((u >> 23) + 1u) << 23);
+}
+
+__device__ __forceinline__ float fp8_block_roundtrip(float v, uint8_t &code, int &sexp) {
+  float amax = warp_max(fabsf(v));
+  float s = pow2_ceil_f(__fdiv_rn(fmaxf(amax, 1e-4f), 448.0f));
+  float r = __fdiv_rn(v, s);
+  r = fminf(fmaxf(r, -448.0f), 448.0f);
+  __nv_fp8_storage_t c = __nv_cvt_float_to_fp8(r, __NV_SATFINITE, __NV_E4M3);
+  __half_raw hr = __nv_cvt_fp8_to_halfraw(c, __NV_E4M3);
+  float dq = __half2float(__half(hr));
+  code = (uint8_t)c;
+  sexp = (int)((__float_as_uint(s) >> 23) & 0xffu) - 127;
+  return __fmul_rn(dq, s);
+}
+
+// In-place act_quant over x [n]: one warp per block of 32.
+__global__ void k_act_quant(bf16 *__restrict__ x, int64_t nblocks, uint8_t *__restrict__ codes,
+                            int8_t *__restrict__ scale_exp) {
+  const int64_t blk = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (blk >= nblocks) return;
+  const int lane = threadIdx.x & 31;
+  const int64_t i = blk * 32 + lane;
+  uint8_t c;
+  int se;
+  float v = fp8_block_roundtrip(__bfloat162float(x[i]), c, se);
+  x[i] = __float2bfloat16_rn(v);
+  if (codes) codes[i] = c;
+  if (scale_exp && lane == 0) scale_exp[blk] = (int8_t)se;
+}
+
+cudaError_t launch_act_quant(bf16 *x, int64_t n, uint8_t *codes, int8_t *scale_exp, cudaStream_t s) {
+  const int64_t nb = n / 32;
+  if (nb <= 0) return cudaSuccess;
+  k_act_quant<<<(unsigned)((nb + 7) / 8), 256, 0, s>>>(x, nb, codes, scale_exp);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------------------------
+// Window rows ("DeepSeek V4.1 - Compressed sparse attention", "Window keys and values": RoPE of the
+// last rd, then FP8), plus the ring update and window selection ("deepseek_v41_ref::attn"
+// WindowCache, window_topk_idxs).  One CTA of hd threads per token row; warp w owns fp8 block w.
+// ---------------------------------------------------------------------------------------------
+__global__ void k_kv_finish(const bf16 *kv_in, bf16 *kv_out, int T, int start_pos, int hd,
+                            int rd, const float *__restrict__ tab, bf16 *__restrict__ ring, int W,
+                            int32_t *__restrict__ win_idx, int idx_stride, uint8_t *__restrict__ codes,
+                            int8_t *__restrict__ scales) {
+  const int64_t row = blockIdx.x;  // b * T + t
+  const int b = (int)(row / T), t = (int)(row % T);
+  const int i = threadIdx.x;
+  const int p = start_pos + t;
+  float v = __bfloat162float(kv_in[row * hd + i]);
+  const int tail = hd - rd;
+  // RoPE: lanes (2k, 2k+1) hold one complex number; each lane produces its own component.
+  const float partner = __shfl_xor_sync(0xffffffffu, v, 1);
+  if (i >= tail) {
+    const int pair = (i - tail) >> 1;
+    const float2 cs = reinterpret_cast<const float2 *>(tab)[(int64_t)p * (rd >> 1) + pair];
+    float re, im;
+    if ((i & 1) == 0)
+      rotate_pair(v, partner, cs.x, cs.y, re, im);
+    else
+      rotate_pair(partner, v, cs.x, cs.y, re, im);
+    v = __bfloat162float(__float2bfloat16_rn((i & 1) ? im : re));
+  }
+  uint8_t c;
+  int se;
+  const float q = fp8_block_roundtrip(v, c, se);
+  const bf16 qb = __float2bfloat16_rn(q);
+  kv_out[row * hd + i] = qb;
+  if (codes) codes[row * hd + i] = c;
+  if (scales && (i & 31) == 0) scales[row * (hd / 32) + (i >> 5)] = (int8_t)se;
+  // ring: position p lives in slot p mod W; of a chunk only the last W rows land
+  if (t >= T - W) ring[((int64_t)b * W + (p % W)) * hd + i] = qb;
+  // window selection
+  if (win_idx) {
+    int32_t *wi = win_idx + row * idx_stride;
+    for (int k = i; k < W; k += blockDim.x) {
+      const int pk = p - W + 1 + k;
+      if (start_pos == 0)
+        wi[k] = pk >= 0 ? pk : -1;  // the chunk's own rows
+      else
+        wi[k] = pk >= 0 ? (p + 1 + k) % W : -1;  // ring slots, oldest first
+    }
+  }
+}
+
+cudaError_t launch_kv_finish(const bf16 *kv_in, bf16 *kv_out, int B, int T, int start_pos, int hd, int rd,
+                             const float *tab, bf16 *ring, int W, int32_t *win_idx, int idx_stride, uint8_t *codes,
+                             int8_t *scales, cudaStream_t s) {
+  if (B * T <= 0) return cudaSuccess;
+  k_kv_finish<<<B * T, hd, 0, s>>>(kv_in, kv_out, T, start_pos, hd, rd, tab, ring, W, win_idx, idx_stride, codes,
+                                   scales);
+  return cudaGetLastError();
+}
+
+__global__ void k_scale_bf16_to_f32(const bf16 *__restrict__ x, int64_t n, float scale, float *__restrict__ y) {
+  int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) y[i] = __bfloat162float(x[i]) * scale;
+}
+
+cudaError_t launch_scale_bf16_to_f32(const bf16 *x, int64_t n, float scale, float *y, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  k_scale_bf16_to_f32<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(x, n, scale, y);
+  return cudaGetLastError();
+}
+
+}  // namespace csa

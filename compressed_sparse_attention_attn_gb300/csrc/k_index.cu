@@ -1,0 +1,240 @@
+// k_index.cu -- the indexer's scores and the index top-k ("DeepSeek V4.1 - Compressed sparse
+// attention", "Indexer, re-scored": S^I[t][j] = sum_h w^I[t][h] ReLU(Q^I[t][h] . K^I[j]),
+// I_t = top_K over valid j; "metrale_model_arch::attn_v41": selection offset past the window rows,
+// -1 = absent).
+#include "csa_internal.cuh"
+
+namespace csa {
+
+// Valid compressed position j for query position p: causal limit floor((p+1)/ratio), the published
+// length, and the candidate block mask when given.
+__device__ __forceinline__ bool comp_valid(int j, int limit, const uint8_t *cand_row, int cand_block) {
+  return j < limit && (cand_row == nullptr || cand_row[j / cand_block] != 0);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Scores: one CTA per (query, 128 positions); one thread per position.  Q^I of the query sits in
+// shared memory as f32; each thread keeps its key row's dI values in registers (dI == 128).
+// ---------------------------------------------------------------------------------------------
+template <int DI>
+__global__ void __launch_bounds__(128) k_index_scores(const bf16 *__restrict__ qI, const float *__restrict__ wI,
+                                                      const bf16 *__restrict__ KI, int T, int start_pos, int Hi,
+                                                      int Lstride, int compress_len, int ratio,
+                                                      const uint8_t *__restrict__ cand, int cand_width,
+                                                      int cand_block, float *__restrict__ S) {
+  extern __shared__ float qs[];  // [Hi][DI] then w [Hi]
+  const int64_t row = blockIdx.y;
+  const int b = (int)(row / T), t = (int)(row % T);
+  const int p = start_pos + t;
+  const int limit = min((p + 1) / ratio, compress_len);
+  const int j0 = blockIdx.x * 128;
+  if (j0 >= limit) return;
+  for (int e = threadIdx.x; e < Hi * DI; e += blockDim.x) qs[e] = __bfloat162float(qI[row * Hi * DI + e]);
+  for (int e = threadIdx.x; e < Hi; e += blockDim.x) qs[Hi * DI + e] = wI[row * Hi + e];
+  __syncthreads();
+  const int j = j0 + threadIdx.x;
+  const uint8_t *cr = cand ? cand + row * cand_width : nullptr;
+  if (!comp_valid(j, limit, cr, cand_block)) return;
+  float k[DI];
+  const uint4 *kp = reinterpret_cast<const uint4 *>(KI + ((int64_t)b * Lstride + j) * DI);
+#pragma unroll
+  for (int v = 0; v < DI / 8; ++v) {
+    uint4 u = kp[v];
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      k[v * 8 + 2 * e] = __low2float(h[e]);
+      k[v * 8 + 2 * e + 1] = __high2float(h[e]);
+    }
+  }
+  float acc = 0.f;
+  for (int h = 0; h < Hi; ++h) {
+    const float *q = qs + h * DI;
+    float d = 0.f;
+#pragma unroll
+    for (int e = 0; e < DI; ++e) d = fmaf(q[e], k[e], d);
+    acc = fmaf(qs[Hi * DI + h], fmaxf(d, 0.f), acc);
+  }
+  S[row * Lstride + j] = acc;
+}
+
+cudaError_t launch_index_scores(const bf16 *qI, const float *wI, const bf16 *KI, int B, int T, int start_pos, int Hi,
+                                int dI, int Lstride, int compress_len, int ratio, const uint8_t *cand, int cand_width,
+                                int cand_block, float *S, cudaStream_t s) {
+  if (B * T <= 0 || Lstride <= 0) return cudaSuccess;
+  const size_t smem = sizeof(float) * (size_t)Hi * (dI + 1);
+  dim3 grid((Lstride + 127) / 128, B * T);
+  switch (dI) {
+    case 128:
+      cudaFuncSetAttribute(k_index_scores<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      k_index_scores<128><<<grid, 128, smem, s>>>(qI, wI, KI, T, start_pos, Hi, Lstride, compress_len, ratio, cand,
+                                                  cand_width, cand_block, S);
+      break;
+    case 64:
+      k_index_scores<64><<<grid, 128, smem, s>>>(qI, wI, KI, T, start_pos, Hi, Lstride, compress_len, ratio, cand,
+                                                 cand_width, cand_block, S);
+      break;
+    case 32:
+      k_index_scores<32><<<grid, 128, smem, s>>>(qI, wI, KI, T, start_pos, Hi, Lstride, compress_len, ratio, cand,
+                                                 cand_width, cand_block, S);
+      break;
+    default:
+      return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------------------------
+// Top-k: one CTA per query.  Scores map to order-preserving 32-bit keys (-0 folded onto +0, NaN
+// below every number); a 4-pass radix select over the valid positions finds the K-th largest key;
+// keys above it are taken, and of the keys equal to it the lowest positions; the K chosen
+// (key, position) pairs are then sorted (key descending, position ascending) by a bitonic network.
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t order_key(float f) {
+  if (f != f) return 0u;   // NaN: below every number
+  if (f == 0.0f) f = 0.0f;  // -0 == +0
+  uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+constexpr int kTopkThreads = 1024;
+constexpr int kTopkMaxK = 2048;
+
+__global__ void __launch_bounds__(kTopkThreads) k_index_topk(const float *__restrict__ S, int T, int start_pos,
+                                                             int Lstride, int compress_len, int ratio,
+                                                             const uint8_t *__restrict__ cand, int cand_width,
+                                                             int cand_block, int K, int offset, int32_t *__restrict__ out) {
+  __shared__ unsigned hist[256];
+  __shared__ unsigned s_prefix, s_remain, s_count_gt, s_nvalid, s_eq_taken;
+  __shared__ unsigned long long sel[kTopkMaxK];  // (key << 32) | ~position
+  __shared__ unsigned warp_cnt[32];
+  const int64_t row = blockIdx.x;
+  const int t = (int)(row % T);
+  const int p = start_pos + t;
+  const int limit = min((p + 1) / ratio, compress_len);
+  const uint8_t *cr = cand ? cand + row * cand_width : nullptr;
+  const float *Sr = S + row * Lstride;
+  const int tid = threadIdx.x;
+  int cap = 1;
+  while (cap < K) cap <<= 1;
+
+  // count valid positions
+  if (tid == 0) s_nvalid = 0;
+  __syncthreads();
+  {
+    unsigned c = 0;
+    for (int j = tid; j < limit; j += blockDim.x) c += comp_valid(j, limit, cr, cand_block) ? 1u : 0u;
+    atomicAdd(&s_nvalid, c);
+  }
+  if (tid == 0) {
+    s_prefix = 0;
+    s_remain = (unsigned)K;
+  }
+  __syncthreads();
+  const unsigned nvalid = s_nvalid;
+  unsigned thr = 0, take_eq = 0;
+  const bool all = nvalid <= (unsigned)K;
+  if (!all) {
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0;
+      __syncthreads();
+      const unsigned prefix = s_prefix;
+      const unsigned hi_mask = shift == 24 ? 0u : (0xffffffffu << (shift + 8));
+      for (int j = tid; j < limit; j += blockDim.x) {
+        if (!comp_valid(j, limit, cr, cand_block)) continue;
+        const uint32_t key = order_key(Sr[j]);
+        if ((key & hi_mask) == (prefix & hi_mask)) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+      }
+      __syncthreads();
+      if (tid == 0) {
+        unsigned remain = s_remain, above = 0;
+        int d = 255;
+        for (; d > 0; --d) {
+          if (above + hist[d] >= remain) break;
+          above += hist[d];
+        }
+        s_prefix = prefix | ((unsigned)d << shift);
+        s_remain = remain - above;
+      }
+      __syncthreads();
+    }
+    thr = s_prefix;
+    take_eq = s_remain;  // how many of the keys equal to thr are taken (lowest positions first)
+  }
+  // collect: keys > thr (or every valid one), then the first take_eq equal keys in position order
+  if (tid == 0) {
+    s_count_gt = 0;
+    s_eq_taken = 0;
+  }
+  __syncthreads();
+  for (int j = tid; j < limit; j += blockDim.x) {
+    if (!comp_valid(j, limit, cr, cand_block)) continue;
+    const uint32_t key = order_key(Sr[j]);
+    if (all || key > thr) {
+      const unsigned slot = atomicAdd(&s_count_gt, 1u);
+      if (slot < (unsigned)K) sel[slot] = ((unsigned long long)key << 32) | (unsigned long long)(~(uint32_t)j);
+    }
+  }
+  __syncthreads();
+  if (!all) {
+    const unsigned base = s_count_gt;  // == K - take_eq
+    const int lane = tid & 31, wid = tid >> 5, nw = blockDim.x >> 5;
+    for (int j0 = 0; j0 < limit; j0 += blockDim.x) {
+      const int j = j0 + tid;
+      bool eq = false;
+      if (j < limit && comp_valid(j, limit, cr, cand_block)) eq = order_key(Sr[j]) == thr;
+      const unsigned ballot = __ballot_sync(0xffffffffu, eq);
+      if (lane == 0) warp_cnt[wid] = __popc(ballot);
+      __syncthreads();
+      unsigned before = s_eq_taken;
+      for (int w = 0; w < wid; ++w) before += warp_cnt[w];
+      before += __popc(ballot & ((1u << lane) - 1u));
+      if (eq && before < take_eq && base + before < (unsigned)K)
+        sel[base + before] = ((unsigned long long)thr << 32) | (unsigned long long)(~(uint32_t)j);
+      __syncthreads();
+      if (tid == 0) {
+        unsigned tot = 0;
+        for (int w = 0; w < nw; ++w) tot += warp_cnt[w];
+        s_eq_taken += tot;
+      }
+      __syncthreads();
+      if (s_eq_taken >= take_eq) break;
+    }
+  }
+  __syncthreads();
+  const int nsel = all ? (int)nvalid : K;
+  for (int i = nsel + tid; i < cap; i += blockDim.x) sel[i] = 0ull;  // sorts last
+  __syncthreads();
+  // bitonic sort, descending
+  for (int size = 2; size <= cap; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = tid; i < cap; i += blockDim.x) {
+        const int jx = i ^ stride;
+        if (jx > i) {
+          const bool desc = (i & size) == 0;
+          const unsigned long long a = sel[i], c = sel[jx];
+          if (desc ? (a < c) : (a > c)) {
+            sel[i] = c;
+            sel[jx] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  int32_t *o = out + row * K;
+  for (int k = tid; k < K; k += blockDim.x)
+    o[k] = k < nsel ? (int32_t)(~(uint32_t)(sel[k] & 0xffffffffull)) + offset : -1;
+}
+
+cudaError_t launch_index_topk(const float *S, int B, int T, int start_pos, int Lstride, int compress_len, int ratio,
+                              const uint8_t *cand, int cand_width, int cand_block, int K, int offset, int32_t *out,
+                              cudaStream_t s) {
+  if (B * T <= 0) return cudaSuccess;
+  if (K > kTopkMaxK) return cudaErrorInvalidValue;
+  k_index_topk<<<B * T, kTopkThreads, 0, s>>>(S, T, start_pos, Lstride, compress_len, ratio, cand, cand_width,
+                                              cand_block, K, offset, out);
+  return cudaGetLastError();
+}
+
+}  // namespace csa

@@ -1,0 +1,233 @@
+"""GPU parity of each step against the CPU oracle, through the C ABI.
+
+Bit-exact where the pages make the result an integer or an exactly-rounded value fed identical
+inputs: the fp8 codes, scales and values, the RoPE rotation, the ring slots, the window indices and
+the top-k index sets.  Tolerances elsewhere: bf16 outputs atol/rtol 2e-2 (plus a relative error norm),
+f32 indexer scores rtol 1e-3 with atol 1e-3 * max|S_row|.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from csa_inputs import WORKLOADS, Geometry, candidate_mask, latent_cache, positions, weights
+from _helpers import assert_close_bf16, bf, to_dev, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def csa():
+    import compressed_sparse_attention_attn_gb300 as m
+    m.lib()
+    return m
+
+
+def _rng_bf16(orc, rng, shape, scale=1.0):
+    return orc.f32_to_bf16((rng.standard_normal(shape) * scale).astype(np.float32))
+
+
+def _ctx(csa, **kw):
+    g = Geometry(**kw)
+    return csa.Context(g.as_dict()), g
+
+
+# ---------------------------------------------------------------------------------- fp8, RoPE
+
+def test_act_quant_bit_exact(csa, orc):
+    rng = np.random.default_rng(1)
+    x = (rng.standard_normal((300, 512)) * 10.0 ** rng.integers(-8, 8, (300, 1))).astype(np.float32)
+    x[7, 32:64] = 0.0
+    x[9, :32] = 448.0 * np.sign(rng.standard_normal(32))
+    xb = orc.f32_to_bf16(x)
+    want, codes, se = orc.act_quant(xb)
+    xd = to_dev(xb)
+    cd = torch.empty(xd.shape, dtype=torch.uint8, device="cuda")
+    sd = torch.empty((300, 16), dtype=torch.int8, device="cuda")
+    csa.act_quant(xd, cd, sd)
+    assert np.array_equal(to_np(xd), want)
+    assert np.array_equal(to_np(cd), codes)
+    assert np.array_equal(to_np(sd), se)
+
+
+@pytest.mark.parametrize("rd,hd,inverse", [(64, 512, False), (64, 512, True), (16, 64, False)])
+def test_rope_bit_exact(csa, orc, rd, hd, inverse):
+    rng = np.random.default_rng(2)
+    rows, rpp = 96, 4
+    x = _rng_bf16(orc, rng, (rows, hd))
+    tab = orc.rope_table(rd, 2048, 10000.0)
+    pos = rng.integers(0, 2048, rows // rpp).astype(np.int32)
+    want = orc.apply_rotary(x, rd, pos, tab, inverse=inverse, rows_per_pos=rpp)
+    xd = to_dev(x)
+    csa.rope(xd, rd, to_dev(pos), to_dev(tab), inverse=inverse, rows_per_pos=rpp)
+    assert np.array_equal(to_np(xd), want)
+
+
+def test_rope_tables_match_oracle(csa, orc):
+    for g in (WORKLOADS["tiny_ratio0"].geom, Geometry(max_seq=70000, max_tokens=1, max_batch=1)):
+        ctx = csa.Context(g.as_dict())
+        plain = ctx.rope_table(0).numpy()
+        comp = ctx.rope_table(1).numpy()
+        want_p = orc.rope_table(g.rope_dim, g.max_seq, g.rope_theta)
+        want_c = orc.rope_table(g.rope_dim, g.max_seq, g.compress_rope_theta, g.orig_seq, g.rope_factor, g.beta_fast,
+                                g.beta_slow)
+        for a, b in ((plain, want_p), (comp, want_c)):
+            ulp = np.abs(a.view(np.int32).astype(np.int64) - b.view(np.int32).astype(np.int64))
+            close = np.abs(a - b) <= 1.2e-7
+            assert ((ulp <= 1) | close).all()
+        ctx.close()
+
+
+# ---------------------------------------------------------------------------------- window rows
+
+@pytest.mark.parametrize("hd,rd,W,T,start", [(64, 16, 8, 12, 0), (64, 16, 8, 1, 12), (64, 16, 8, 1, 13),
+                                             (512, 64, 128, 200, 0), (512, 64, 128, 1, 1000), (512, 64, 128, 1, 5)])
+def test_kv_finish_bit_exact(csa, orc, hd, rd, W, T, start):
+    rng = np.random.default_rng(3 + T + start)
+    B = 3
+    kvn = _rng_bf16(orc, rng, (B * T, hd))
+    tab = orc.rope_table(rd, 2048, 160000.0)
+    ring0 = orc.act_quant(_rng_bf16(orc, rng, (B, W, hd)))[0]
+    pos = positions(B, T, start)
+    rot = orc.apply_rotary(kvn, rd, pos, tab)
+    want_kv, want_codes, want_se = orc.act_quant(rot)
+    want_ring = ring0.copy()
+    for b in range(B):
+        orc.ring_write(want_ring[b], want_kv[b * T:(b + 1) * T], start)
+    if start == 0:
+        want_idx = np.tile(orc.window_idx_prefill(T, W), (B, 1))
+    else:
+        want_idx = np.tile(orc.window_idx_decode(start, W)[None], (B, 1))
+    ring = to_dev(ring0)
+    kv_out = torch.empty((B * T, hd), dtype=torch.bfloat16, device="cuda")
+    idx = torch.full((B * T, W + 5), -9, dtype=torch.int32, device="cuda")
+    codes = torch.empty((B * T, hd), dtype=torch.uint8, device="cuda")
+    se = torch.empty((B * T, hd // 32), dtype=torch.int8, device="cuda")
+    csa.kv_finish(to_dev(kvn), kv_out, B, T, start, rd, to_dev(tab), ring, idx, codes, se)
+    assert np.array_equal(to_np(kv_out), want_kv)
+    assert np.array_equal(to_np(codes), want_codes) and np.array_equal(to_np(se), want_se)
+    assert np.array_equal(to_np(ring), want_ring)
+    got_idx = to_np(idx)
+    assert np.array_equal(got_idx[:, :W], want_idx) and (got_idx[:, W:] == -9).all()
+
+
+# ---------------------------------------------------------------------------------- projections
+
+@pytest.mark.parametrize("M,K,N,groups", [(12, 256, 64, 1), (32, 5120, 1280, 1), (33, 1280, 4096, 1),
+                                          (32, 4096, 1024, 8), (200, 512, 96, 2), (1, 64, 32, 1)])
+def test_linear(csa, orc, M, K, N, groups):
+    rng = np.random.default_rng(4 + M + N)
+    x = _rng_bf16(orc, rng, (M, K * groups))
+    W = _rng_bf16(orc, rng, (N * groups, K), 1.0 / math.sqrt(K))
+    want = np.concatenate([orc.linear_bf16(x[:, g * K:(g + 1) * K], W[g * N:(g + 1) * N]) for g in range(groups)], 1)
+    ctx, _ = _ctx(csa, dim=64, max_tokens=1, max_batch=1, max_seq=16)
+    got = ctx.linear(to_dev(x), to_dev(W), groups=groups)
+    assert_close_bf16(to_np(got), want, what="linear")
+    # f32 accumulation then one bf16 rounding: at most one bf16 ulp from the exact result
+    g, w = bf(to_np(got)).astype(np.float64), bf(want).astype(np.float64)
+    assert (np.abs(g - w) <= np.abs(w) * 2 ** -7 + 1e-6).all()
+
+
+def test_rmsnorm(csa, orc):
+    rng = np.random.default_rng(5)
+    x = _rng_bf16(orc, rng, (40, 1280), 3.0)
+    w = (1 + 0.1 * rng.standard_normal(1280)).astype(np.float32)
+    want = orc.rmsnorm(x, w, 1e-6)
+    got = csa.rmsnorm(to_dev(x), to_dev(w), 1e-6)
+    g, ww = bf(to_np(got)).astype(np.float64), bf(want).astype(np.float64)
+    assert (np.abs(g - ww) <= np.abs(ww) * 2 ** -7 + 1e-30).all()
+
+
+# ---------------------------------------------------------------------------------- indexer
+
+def _index_case(orc, rng, B, T, start, Hi, dI, L, compress_len, ratio, cand_keep, cand_block):
+    qI = _rng_bf16(orc, rng, (B * T, Hi, dI))
+    wI = (rng.standard_normal((B * T, Hi)) / 64).astype(np.float32)
+    KI = _rng_bf16(orc, rng, (B, L, dI))
+    pos = positions(B, T, start)
+    cand = None
+    if cand_keep:
+        cand = candidate_mask(B * T, pos, ratio, compress_len, cand_block, -(-L // cand_block), cand_keep, 77)
+    S = np.concatenate([orc.index_scores(qI[b * T:(b + 1) * T], wI[b * T:(b + 1) * T], KI[b], pos[b * T:(b + 1) * T],
+                                         ratio, compress_len, None if cand is None else cand[b * T:(b + 1) * T],
+                                         cand_block) for b in range(B)])
+    return qI, wI, KI, pos, cand, S
+
+
+@pytest.mark.parametrize("B,T,start,L,clen,ratio,keep,cb", [
+    (4, 1, 1000, 512, 500, 2, 0.5, 64),       # Reindex decode shape
+    (1, 300, 0, 1024, 1024, 4, 0, 64),        # prefill, causal only
+    (2, 1, 65535, 16384, 16384, 4, 64, 64),   # long context, 64 of 256 blocks
+    (3, 1, 40, 64, 7, 1, 0, 8),               # short cache
+])
+def test_index_scores(csa, orc, B, T, start, L, clen, ratio, keep, cb):
+    rng = np.random.default_rng(6 + T)
+    qI, wI, KI, pos, cand, S = _index_case(orc, rng, B, T, start, 32, 128, L, clen, ratio, keep, cb)
+    Sd = torch.full((B * T, L), float("nan"), device="cuda")
+    csa.index_scores(to_dev(qI), to_dev(wI), to_dev(KI), B, T, start, clen, ratio, Sd,
+                     None if cand is None else to_dev(cand), cb)
+    got = to_np(Sd)
+    valid = np.isfinite(S)
+    assert np.isnan(got[~valid]).all()  # invalid positions are not written
+    for r in range(B * T):
+        v = valid[r]
+        if not v.any():
+            continue
+        a, b = got[r, v].astype(np.float64), S[r, v].astype(np.float64)
+        tol = 1e-3 * np.abs(b) + 1e-3 * np.abs(b).max()
+        assert (np.abs(a - b) <= tol).all()
+
+
+@pytest.mark.parametrize("B,T,start,L,clen,ratio,keep,cb,K", [
+    (4, 1, 1000, 512, 500, 2, 0.5, 64, 512),
+    (1, 300, 0, 1024, 1024, 4, 0, 64, 512),
+    (2, 1, 65535, 16384, 16384, 4, 64, 64, 512),
+    (3, 1, 40, 64, 7, 1, 0, 8, 16),
+])
+def test_index_topk_bit_exact(csa, orc, B, T, start, L, clen, ratio, keep, cb, K):
+    rng = np.random.default_rng(7 + T)
+    qI, wI, KI, pos, cand, S = _index_case(orc, rng, B, T, start, 32, 128, L, clen, ratio, keep, cb)
+    S = np.where(np.isfinite(S), np.round(S * 4) / 4, S).astype(np.float32)  # many exact ties
+    S[:, ::7] = np.where(np.isfinite(S[:, ::7]), -0.0, S[:, ::7])
+    want = np.concatenate([orc.index_topk(S[b * T:(b + 1) * T], K, pos[b * T:(b + 1) * T], ratio, clen,
+                                          None if cand is None else cand[b * T:(b + 1) * T], cb, offset=128)
+                           for b in range(B)])
+    out = torch.full((B * T, K), -5, dtype=torch.int32, device="cuda")
+    csa.index_topk(to_dev(S), B, T, start, clen, ratio, K, out, offset=128,
+                   cand=None if cand is None else to_dev(cand), cand_block=cb)
+    assert np.array_equal(to_np(out), want)
+
+
+# ---------------------------------------------------------------------------------- attention
+
+@pytest.mark.parametrize("H,hd,na,nb,a_len,b_len,B,T", [(4, 64, 8, 16, 12, 40, 1, 12), (64, 512, 128, 512, 128, 500, 3, 1),
+                                                        (64, 512, 128, 512, 300, 1024, 1, 9)])
+def test_sparse_attn(csa, orc, H, hd, na, nb, a_len, b_len, B, T):
+    rng = np.random.default_rng(8 + H)
+    q = _rng_bf16(orc, rng, (B * T, H, hd))
+    ra = _rng_bf16(orc, rng, (B, a_len, hd))
+    rb = _rng_bf16(orc, rng, (B, b_len, hd))
+    sink = rng.standard_normal(H).astype(np.float32)
+    ia = rng.integers(-1, a_len, (B * T, na)).astype(np.int32)
+    ib = np.where(rng.random((B * T, nb)) < 0.2, -1, rng.integers(0, b_len, (B * T, nb)) + a_len).astype(np.int32)
+    ib[0, :] = -1
+    ia[0, :] = -1  # a query with nothing selected: O = 0
+    scale = 1 / math.sqrt(hd)
+    rd, start = hd // 8, 0
+    tab = orc.rope_table(rd, 64, 10000.0)
+    want = np.concatenate([orc.sparse_attn(q[b * T:(b + 1) * T], ra[b], rb[b],
+                                           np.concatenate([ia[b * T:(b + 1) * T], ib[b * T:(b + 1) * T]], 1), sink, scale)
+                           for b in range(B)])
+    pos = positions(B, T, start)
+    want_rot = orc.apply_rotary(want.reshape(-1, hd), rd, pos, tab, inverse=True, rows_per_pos=H).reshape(want.shape)
+    ctx, _ = _ctx(csa, dim=64, max_tokens=1, max_batch=1, max_seq=16)
+    o = torch.empty((B * T, H, hd), dtype=torch.bfloat16, device="cuda")
+    o_rot = torch.empty_like(o)
+    ctx.sparse_attn(to_dev(q), to_dev(ra), a_len, to_dev(ia), to_dev(sink), scale, rows_b=to_dev(rb), b_len=b_len,
+                    idx_b=to_dev(ib), o=o, o_rot=o_rot, rd=rd, start_pos=start, tab=to_dev(tab), B=B, T=T)
+    assert ctx.status() == 0
+    got = to_np(o)
+    assert (got[0] == 0).all()
+    assert_close_bf16(got, want, what="sparse_attn")
+    assert_close_bf16(to_np(o_rot), want_rot, what="sparse_attn o_rot")

@@ -1,0 +1,271 @@
+"""GPU parity of the whole layer (attn_v41_forward through the C ABI) against the CPU oracle.
+
+Small geometries run every token; the full-width workloads compare sampled queries (the oracle
+computes those rows one by one) in the launch configuration the benchmark times.  Tolerances:
+layer and attention outputs atol/rtol 2e-2 plus a relative error norm of 1e-2; fp8-rounded rows at
+most one e4m3 step apart (the projections feeding them round differently); window indices exact;
+the compressed selection equal to the oracle's wherever the K-th and (K+1)-th oracle scores are
+further apart than the score tolerance, otherwise a valid top-K within that tolerance.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from csa_inputs import (WORKLOADS, Geometry, activations, candidate_mask, latent_cache, positions, ring_rows,
+                        weights)
+from _helpers import assert_close_bf16, bf, to_dev, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def csa():
+    import compressed_sparse_attention_attn_gb300 as m
+    m.lib()
+    return m
+
+
+def _dev_weights(w):
+    return {k: to_dev(v) for k, v in w.items()}
+
+
+def _assert_fp8_rows_close(got, want, what):
+    g, w = bf(got).astype(np.float64), bf(want).astype(np.float64)
+    step = 0.13 * np.maximum(np.abs(g), np.abs(w)) + 1e-3
+    assert (np.abs(g - w) <= step).all(), "%s: rows more than one e4m3 step apart" % what
+    assert np.linalg.norm(g - w) <= 2e-2 * np.linalg.norm(w) + 1e-6, what
+
+
+def _check_selection(got, S_row, K, offset, tol):
+    """got: the GPU's selection row (j + offset, -1 padded); S_row: oracle scores (-inf = invalid)."""
+    valid = np.isfinite(S_row)
+    n = int(valid.sum())
+    sel = [v - offset for v in got if v >= 0]
+    assert len(sel) == min(n, K) and len(set(sel)) == len(sel)
+    assert all(valid[j] for j in sel)
+    if n <= K:
+        assert set(sel) == set(np.nonzero(valid)[0])
+        return
+    order = sorted(np.nonzero(valid)[0], key=lambda j: (-S_row[j], j))
+    kth, nxt = S_row[order[K - 1]], S_row[order[K]]
+    if kth - nxt > tol:
+        assert set(sel) == set(order[:K])
+    else:
+        assert min(S_row[j] for j in sel) >= kth - tol
+
+
+def _dbg(NT, g, L, with_idx_cols):
+    H, hd = g.n_heads, g.head_dim
+    z = lambda *s, dt=torch.bfloat16: torch.zeros(*s, dtype=dt, device="cuda")
+    return dict(q=z(NT, H, hd), kv=z(NT, hd), kv_codes=z(NT, hd, dt=torch.uint8), kv_scale=z(NT, hd // 32, dt=torch.int8),
+                idx=torch.full((NT, with_idx_cols), -9, dtype=torch.int32, device="cuda"),
+                scores=torch.full((NT, max(L, 1)), float("nan"), device="cuda"), o=z(NT, H, hd),
+                og=z(NT, g.groups * g.o_rank), qr=z(NT, g.q_rank), qI=z(NT, max(g.index_heads * g.index_hd, 1)),
+                wI=z(NT, max(g.index_heads, 1), dt=torch.float32))
+
+
+def _compare_rows(res, dbg, rows, g, what):
+    NT = len(rows)
+    out = res["out"].reshape(-1, g.dim)[rows]
+    assert_close_bf16(to_np(dbg["__out"]).reshape(-1, g.dim)[rows], out, what=what + " out")
+    assert_close_bf16(to_np(dbg["o"])[rows], res["o"][rows], what=what + " o")
+    assert_close_bf16(to_np(dbg["q"])[rows], res["q"][rows], what=what + " q")
+    _assert_fp8_rows_close(to_np(dbg["kv"])[rows], res["kv"][rows], what + " kv")
+
+
+# ------------------------------------------------------------------------------------- tiny
+
+def test_tiny_ratio0_prefill_then_decode(csa, orc):
+    """The ring fixture's three regimes through one cache, GPU against oracle."""
+    wl = WORKLOADS["tiny_ratio0"]
+    g = wl.geom
+    gd = g.as_dict()
+    w = weights(g, with_indexer=False)
+    x = activations(g, 1, 14)
+    tab = orc.rope_table(g.rope_dim, g.max_seq, g.rope_theta)
+    ring_o = np.zeros((1, g.window, g.head_dim), np.uint16)
+    ctx = csa.Context(gd)
+    wd = _dev_weights(w)
+    ring_d = torch.zeros((1, g.window, g.head_dim), dtype=torch.bfloat16, device="cuda")
+    ctx.state_init(ring_d, 1)
+    for start, T in ((0, 12), (12, 1), (13, 1)):
+        xs = x[:, start:start + T] if start else x[:, :12]
+        res = orc.attn_forward(gd, dict(ratio=0), w, ring_o, xs, start, tab)
+        dbg = _dbg(T, g, 1, g.window)
+        out = ctx.forward(wd, dict(ratio=0), ring_d, to_dev(xs), start, debug=dbg)
+        torch.cuda.synchronize()
+        dbg["__out"] = out
+        _compare_rows(res, dbg, np.arange(T), g, "tiny@%d" % start)
+        assert np.array_equal(to_np(dbg["idx"]), res["idx"])
+        _assert_fp8_rows_close(to_np(ring_d), ring_o, "ring@%d" % start)
+    assert ctx.status() == 0
+
+
+def _small_geom():
+    return Geometry(dim=96, n_heads=4, head_dim=64, rope_dim=16, q_rank=48, o_rank=24, groups=2, window=8,
+                    index_heads=4, index_hd=32, index_topk=8, cand_block=4, max_seq=256, max_tokens=40, max_batch=3)
+
+
+@pytest.mark.parametrize("start,T,B,cand", [(0, 40, 2, True), (0, 40, 1, False), (77, 1, 3, True), (5, 1, 3, False)])
+def test_small_ratio2_index_source_and_reuse(csa, orc, start, T, B, cand):
+    g = _small_geom()
+    gd = g.as_dict()
+    L = 64
+    w = weights(g, with_indexer=True, norm_ones=False)
+    x = activations(g, B, T, seed_base=2000 + start)
+    Z, KI = latent_cache(g, B, L, seed_base=3000)
+    clen = min(L, (start + T) // 2 + 3)
+    pos = positions(B, T, start)
+    cm = candidate_mask(B * T, pos, 2, clen, g.cand_block, L // g.cand_block, 0.5, 99) if cand else None
+    tab = orc.rope_table(g.rope_dim, g.max_seq, g.compress_rope_theta, g.orig_seq, g.rope_factor)
+    ring0 = orc.act_quant(ring_rows(g, B))[0] if start else np.zeros((B, g.window, g.head_dim), np.uint16)
+    ring_o = ring0.copy()
+    sel_o = np.full((B * T, g.index_topk), -7, np.int32)
+    shared_o = dict(compress_kv=Z, index_k=KI, compress_len=clen, topk_idxs=sel_o)
+    if cand:
+        shared_o["candidates"] = cm
+    role = dict(ratio=2, is_index_source=1, uses_candidates=int(cand))
+    res = orc.attn_forward(gd, role, w, ring_o, x, start, tab, shared_o)
+
+    ctx = csa.Context(gd)
+    wd = _dev_weights(w)
+    ring_d = to_dev(ring0)
+    sel_d = torch.full((B * T, g.index_topk), -7, dtype=torch.int32, device="cuda")
+    sh = csa.Shared(to_dev(Z), to_dev(KI), clen, sel_d, g.index_topk, None if cm is None else to_dev(cm))
+    dbg = _dbg(B * T, g, L, g.window + g.index_topk)
+    out = ctx.forward(wd, role, ring_d, to_dev(x), start, shared=sh, debug=dbg)
+    torch.cuda.synchronize()
+    assert sh.has_topk
+    dbg["__out"] = out
+    rows = np.arange(B * T)
+    _compare_rows(res, dbg, rows, g, "ratio2")
+    gi = to_np(dbg["idx"])
+    assert np.array_equal(gi[:, :g.window], res["idx"][:, :g.window])
+    # scores: inputs differ by the projections' bf16 rounding, so 1e-2 here (1e-3 at the kernel level)
+    S_g = to_np(dbg["scores"])[:, :L]
+    S_o = res["scores"]
+    for r in rows:
+        v = np.isfinite(S_o[r])
+        if v.any():
+            tol = 1e-2 * np.abs(S_o[r, v]).max()
+            assert (np.abs(S_g[r, v] - S_o[r, v]) <= 1e-2 * np.abs(S_o[r, v]) + tol).all()
+            _check_selection(gi[r, g.window:], S_o[r], g.index_topk, g.window if start else T, 2 * tol)
+    assert np.array_equal(to_np(sel_d), gi[:, g.window:])
+    # a reuse layer reads the published selection: same rows as the index source
+    reuse = dict(ratio=2, is_index_source=0)
+    ring_d2 = to_dev(ring0)
+    out2 = ctx.forward(wd, reuse, ring_d2, to_dev(x), start, shared=sh)
+    torch.cuda.synchronize()
+    assert np.array_equal(to_np(out2), to_np(out))
+    assert ctx.status() == 0
+
+
+def test_layer_refusals(csa):
+    g = _small_geom()
+    ctx = csa.Context(g.as_dict())
+    w = _dev_weights(weights(g, with_indexer=True))
+    ring = torch.zeros((3, g.window, g.head_dim), dtype=torch.bfloat16, device="cuda")
+    x = torch.zeros((1, 2, g.dim), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(csa.CsaError) as e:
+        ctx.forward(w, dict(ratio=2, is_index_source=1), ring, x, 0)
+    assert e.value.code == -3
+    with pytest.raises(csa.CsaError) as e:
+        ctx.forward(w, dict(ratio=0), ring, x, 5)
+    assert e.value.code == -2
+    sel = torch.zeros((2, g.index_topk), dtype=torch.int32, device="cuda")
+    Z = torch.zeros((1, 16, g.head_dim), dtype=torch.bfloat16, device="cuda")
+    sh = csa.Shared(Z, None, 4, sel, g.index_topk)
+    with pytest.raises(csa.CsaError) as e:
+        ctx.forward(w, dict(ratio=2, is_index_source=0), ring, x, 0, shared=sh)
+    assert e.value.code == -4
+    with pytest.raises(csa.CsaError) as e:
+        ctx.forward(w, dict(ratio=2, is_kv_source=1), ring, x, 0, shared=sh)
+    assert e.value.code == -6
+    with pytest.raises(csa.CsaError) as e:
+        ctx.forward(w, dict(ratio=0), ring, torch.zeros((1, 41, g.dim), dtype=torch.bfloat16, device="cuda"), 0)
+    assert e.value.code == -2
+
+
+# ------------------------------------------------------------------------------------- full width
+
+def _full_case(orc, name, seqs, toks=None):
+    wl = WORKLOADS[name]
+    g = wl.geom
+    B, T, start = wl.batch, wl.tokens, wl.start_pos
+    w = weights(g, with_indexer=wl.is_index_source)
+    x = activations(g, B, T)
+    pos = positions(B, T, start)
+    tab = orc.rope_table(g.rope_dim, g.max_seq, g.compress_rope_theta if wl.ratio else g.rope_theta, g.orig_seq
+                         if wl.ratio else 0, g.rope_factor, g.beta_fast, g.beta_slow)
+    ring0 = orc.act_quant(ring_rows(g, B))[0] if start else np.zeros((B, g.window, g.head_dim), np.uint16)
+    shared = None
+    if wl.ratio:
+        L = wl.compress_len
+        Z, KI = latent_cache(g, B, L)
+        shared = dict(compress_kv=Z, index_k=KI, compress_len=L, topk_idxs=None)
+        if wl.uses_candidates:
+            shared["candidates"] = candidate_mask(B * T, pos, wl.ratio, L, g.cand_block, -(-L // g.cand_block),
+                                                  wl.cand_keep, 1015)
+    return wl, g, w, x, tab, ring0, shared
+
+
+@pytest.mark.parametrize("name,seqs,toks", [
+    ("ratio0_decode", [0, 13, 31], None),
+    ("reindex_decode_r2", [0, 7, 31], None),
+    ("prefill_r4", [0], [0, 1, 127, 128, 1000, 2047, 2048, 3001, 4095]),
+    ("longctx_decode_r4", [0, 63], None),
+])
+def test_full_width_sampled(csa, orc, name, seqs, toks):
+    wl, g, w, x, tab, ring0, shared = _full_case(orc, name, seqs, toks)
+    gd = g.as_dict()
+    B, T, start = wl.batch, wl.tokens, wl.start_pos
+    K = g.index_topk
+    # GPU: the whole batch, as the benchmark runs it
+    ctx = csa.Context(gd)
+    wd = _dev_weights(w)
+    ring_d = to_dev(ring0)
+    role = dict(ratio=wl.ratio, is_index_source=int(wl.is_index_source), uses_candidates=int(wl.uses_candidates))
+    sh = None
+    if shared is not None:
+        sel_d = torch.full((B * T, K), -7, dtype=torch.int32, device="cuda")
+        sh = csa.Shared(to_dev(shared["compress_kv"]), to_dev(shared["index_k"]), shared["compress_len"], sel_d, K,
+                        None if "candidates" not in shared else to_dev(shared["candidates"]))
+    L = shared["compress_len"] if shared else 1
+    dbg = _dbg(B * T, g, L, g.window + (K if wl.ratio else 0))
+    out = ctx.forward(wd, role, ring_d, to_dev(x), start, shared=sh, debug=dbg)
+    torch.cuda.synchronize()
+    assert ctx.status() == 0
+    dbg["__out"] = out
+    # oracle: only the sampled sequences (and, for the prefill chunk, the sampled tokens)
+    for b in seqs:
+        xb = x[b:b + 1]
+        ring_o = ring0[b:b + 1].copy()
+        sh_o = None
+        if shared is not None:
+            sh_o = dict(compress_kv=shared["compress_kv"][b:b + 1], index_k=shared["index_k"][b:b + 1],
+                        compress_len=shared["compress_len"], topk_idxs=np.full((T, K), -7, np.int32))
+            if "candidates" in shared:
+                sh_o["candidates"] = shared["candidates"][b * T:(b + 1) * T]
+        mask = None
+        rows = np.arange(T)
+        if toks is not None:
+            mask = np.zeros(T, np.uint8)
+            mask[toks] = 1
+            rows = np.array(toks)
+        res = orc.attn_forward(gd, role, w, ring_o, xb, start, tab, sh_o, tok_mask=mask)
+        grows = b * T + rows
+        assert_close_bf16(to_np(out).reshape(-1, g.dim)[grows], res["out"].reshape(-1, g.dim)[rows], what=name + " out")
+        assert_close_bf16(to_np(dbg["o"])[grows], res["o"][rows], what=name + " o")
+        _assert_fp8_rows_close(to_np(dbg["kv"])[grows], res["kv"][rows], name + " kv")
+        gi = to_np(dbg["idx"])[grows]
+        assert np.array_equal(gi[:, :g.window], res["idx"][rows, :g.window])
+        _assert_fp8_rows_close(to_np(ring_d)[b], ring_o[0], name + " ring")
+        if wl.ratio:
+            S_o = res["scores"]
+            for i, r in enumerate(rows):
+                v = np.isfinite(S_o[r])
+                if v.any():
+                    tol = 1e-2 * np.abs(S_o[r, v]).max()
+                    _check_selection(gi[i, g.window:], S_o[r], K, g.window if start else T, 2 * tol)
