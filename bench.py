@@ -209,7 +209,7 @@ def cpu_baseline(wl, layers, x, ring, shared_np, target_s):
         ntok += oracle_sample(wl, layers, x, ring, shared_np, [b % B], tok_rows)
         nseq += 1
         b += 1
-        if time.perf_counter() - t0 >= target_s or nseq >= 4 * B:
+        if time.perf_counter() - t0 >= target_s or nseq >= 64 * B:
             break
     dt = time.perf_counter() - t0
     what = "%d sequence(s) x %s of the %s workload, %d layer(s) each" % (

@@ -1,0 +1,398 @@
+// k_gemm_tc.cu -- linear_bf16 on the 5th-generation tensor cores ("deepseek_v41_ref::attn"
+// precision contract: bf16 operands, f32 accumulation, bf16 result): y[m][n] = sum_k x[m][k] W[n][k].
+//
+// Orientation: the weight is the MMA's A operand (M = 128 output features per tile) and the
+// activations its B operand (N = BN tokens per tile, 16..256), so a decode step with a few dozen
+// tokens still issues full 128-row MMAs while the weights stream from HBM exactly once.
+// Both operands are K-major and arrive by TMA in 64-element (128-byte) swizzled slices; the
+// accumulator lives in TMEM (two BN-column buffers so the epilogue of one tile overlaps the MMAs of
+// the next).
+//
+// Work split: the (tile, 64-wide k-slice) units of up to four independent problems (several weights
+// applied to the same activations, or the groups of the block-diagonal wo_a) are laid end to end
+// and divided evenly over a persistent grid of one CTA per SM ("Stream-K").  A tile whose k-range
+// spans several CTAs is finished by whichever of them arrives last: each writes its f32 partial to
+// the workspace, bumps the tile's arrival counter, and the last one sums the partials in CTA order
+// (deterministic) and writes the bf16 result.  No CTA ever waits for another.
+//
+// Warp roles (192 threads): warps 0-3 epilogue (TMEM lane quadrant = warp), warp 4 TMA producer,
+// warp 5 TMEM allocation + MMA issue.  Every mbarrier wait is time-bounded; a timeout raises the
+// device status word and the CTA drains its copies and MMAs, frees TMEM and exits.
+#include "csa_internal.cuh"
+#include "tc_ptx.cuh"
+
+namespace csa {
+
+namespace gemm {
+
+constexpr int kMaxProblems = 4;
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int kThreads = 192;
+constexpr int kCounterInts = 65536;            // arrival counters at the head of the workspace
+constexpr size_t kCounterBytes = kCounterInts * sizeof(int);
+
+struct Problem {
+  CUtensorMap tmA;  // W [groups*N rows][Kg] bf16, box {64, 128}
+  CUtensorMap tmB;  // x [M rows][groups*Kg] bf16, box {64, BN}
+  bf16 *y;
+  int ldy, N, M, groups, Kg, kblocks, tiles_n, tiles_m, tiles, unit_begin, tile_begin;
+};
+
+struct Params {
+  Problem prob[kMaxProblems];
+  int nprob, total_units, total_tiles, BN, stages;
+  float *partials;  // [grid][2][BM][BN]
+  int *counters;    // [total_tiles]
+  int *status;
+};
+
+struct Unit {
+  int p, tile, kb;
+};
+
+__device__ __forceinline__ Unit decode_unit(const Params &P, int u) {
+  int p = 0;
+  while (p + 1 < P.nprob && u >= P.prob[p + 1].unit_begin) ++p;
+  const int local = u - P.prob[p].unit_begin;
+  return Unit{p, local / P.prob[p].kblocks, local % P.prob[p].kblocks};
+}
+
+__device__ __forceinline__ int64_t cta_start(int64_t c, int64_t U, int64_t G) { return c * U / G; }
+__device__ __forceinline__ int64_t unit_owner(int64_t v, int64_t U, int64_t G) { return ((v + 1) * G - 1) / U; }
+
+__global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__ Params P) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = tc::smem_u32(smem_raw);
+  uint8_t *smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
+  const int S = P.stages, BN = P.BN;
+  const uint32_t a_bytes = BM * BK * 2, b_bytes = (uint32_t)BN * BK * 2, stage_bytes = a_bytes + b_bytes;
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + S * stage_bytes);
+  uint64_t *empty = full + S;
+  uint64_t *accf = empty + S;  // [2]
+  uint64_t *acce = accf + 2;   // [2]
+  uint64_t *drain = acce + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  int *s_last = const_cast<int *>(abort_flag) + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t U = P.total_units, G = gridDim.x;
+  const int u0 = (int)cta_start(blockIdx.x, U, G), u1 = (int)cta_start(blockIdx.x + 1, U, G);
+  if (u0 >= u1) return;
+  const uint32_t tmem_cols = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128 : (2 * BN <= 256) ? 256 : 512;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&accf[b], 1);
+      tc::mbar_init(&acce[b], 128);
+    }
+    tc::mbar_init(drain, 1);
+    *abort_flag = 0;
+    tc::fence_barrier_init();
+  }
+  if (warp == 5) tc::tmem_alloc(tmem_slot, tmem_cols);
+  if (warp == 4 && lane == 0) {
+    for (int p = 0; p < P.nprob; ++p) {
+      tc::prefetch_tmap(&P.prob[p].tmA);
+      tc::prefetch_tmap(&P.prob[p].tmB);
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 4) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      const uint64_t pol_w = tc::policy_evict_first(), pol_x = tc::policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      for (int u = u0; u < u1; ++u) {
+        const Unit un = decode_unit(P, u);
+        const Problem &pr = P.prob[un.p];
+        const int tm = un.tile % pr.tiles_m, rest = un.tile / pr.tiles_m;
+        const int tn = rest % pr.tiles_n, g = rest / pr.tiles_n;
+        if (!tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag)) break;
+        uint8_t *sa = smem + stage * stage_bytes;
+        tc::mbar_expect_tx(&full[stage], stage_bytes);
+        tc::tma_load_2d(sa, &pr.tmA, &full[stage], un.kb * BK, g * pr.N + tn * BM, pol_w);
+        tc::tma_load_2d(sa + a_bytes, &pr.tmB, &full[stage], g * pr.Kg + un.kb * BK, tm * BN, pol_x);
+        ++issued;
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      // let every copy this CTA issued land before the CTA can exit
+      for (int i = issued - S > 0 ? issued - S : 0; i < issued; ++i) {
+        uint64_t *b = &full[i % S];
+        const uint32_t par = (uint32_t)((i / S) & 1);
+        const uint64_t t0 = tc::global_ns();
+        while (!tc::mbar_try_wait(b, par) && tc::global_ns() - t0 < tc::kWaitLimitNs) {
+        }
+      }
+    }
+  } else if (warp == 5) {
+    // ---------------------------------------------------------------- MMA issue
+    if (lane == 0) {
+      const uint32_t idesc = tc::idesc_bf16_f32(BM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int used[2] = {0, 0};
+      int buf = 0;
+      int u = u0;
+      bool ok = true;
+      while (u < u1 && ok) {
+        const Unit un = decode_unit(P, u);
+        const Problem &pr = P.prob[un.p];
+        const int seg_end = min(u1, pr.unit_begin + (un.tile + 1) * pr.kblocks);
+        if (!tc::mbar_wait(&acce[buf], (uint32_t)(used[buf] & 1) ^ 1u, abort_flag)) break;
+        tc::tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)(buf * BN);
+        bool first = true;
+        for (; u < seg_end; ++u) {
+          if (!tc::mbar_wait(&full[stage], phase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc::tc_fence_after();
+          const uint32_t sa = tc::smem_u32(smem + stage * stage_bytes);
+          const uint64_t ad = tc::sdesc_sw128(sa, 16, 1024), bd = tc::sdesc_sw128(sa + a_bytes, 16, 1024);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            tc::mma_bf16(d, ad + 2ull * k, bd + 2ull * k, idesc, (first && k == 0) ? 0u : 1u);
+          first = false;
+          tc::mma_commit(&empty[stage]);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc::mma_commit(&accf[buf]);
+        ++used[buf];
+        buf ^= 1;
+      }
+      // every MMA issued has completed once this arrives
+      tc::mma_commit(drain);
+      const uint64_t t0 = tc::global_ns();
+      while (!tc::mbar_try_wait(drain, 0) && tc::global_ns() - t0 < tc::kWaitLimitNs) {
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue (warps 0-3)
+    const int row = warp * 32 + lane;  // feature within the tile
+    int done[2] = {0, 0};
+    int buf = 0;
+    int u = u0;
+    const int first_tile_global = [&] {
+      const Unit f = decode_unit(P, u0);
+      return P.prob[f.p].tile_begin + f.tile;
+    }();
+    while (u < u1) {
+      const Unit un = decode_unit(P, u);
+      const Problem &pr = P.prob[un.p];
+      const int tile_u0 = pr.unit_begin + un.tile * pr.kblocks, tile_u1 = tile_u0 + pr.kblocks;
+      const int seg_end = min(u1, tile_u1);
+      const bool whole = (u == tile_u0) && (seg_end == tile_u1);
+      const int tm = un.tile % pr.tiles_m, rest = un.tile / pr.tiles_m;
+      const int tn = rest % pr.tiles_n, g = rest / pr.tiles_n;
+      const int f = tn * BM + row;
+      const bool f_ok = f < pr.N;
+      bf16 *ycol = pr.y + (int64_t)g * pr.N + f;
+      const int gtile = pr.tile_begin + un.tile;
+      if (!tc::mbar_wait(&accf[buf], (uint32_t)(done[buf] & 1), abort_flag)) break;
+      tc::tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(buf * BN);
+      const int slot = (int)blockIdx.x * 2 + (gtile == first_tile_global ? 0 : 1);
+      float *mine = P.partials + (size_t)slot * BM * BN + (size_t)row * BN;
+      for (int c0 = 0; c0 < BN; c0 += 16) {
+        uint32_t r[16];
+        tc::tmem_ld16(taddr + (uint32_t)c0, r);
+        tc::tmem_ld_wait();
+        if (whole) {
+          if (f_ok) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int j = tm * BN + c0 + i;
+              if (j < pr.M) ycol[(int64_t)j * pr.ldy] = __float2bfloat16_rn(__uint_as_float(r[i]));
+            }
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; i += 4)
+            *reinterpret_cast<float4 *>(mine + c0 + i) =
+                make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]), __uint_as_float(r[i + 2]),
+                            __uint_as_float(r[i + 3]));
+        }
+      }
+      tc::tc_fence_before();
+      tc::mbar_arrive(&acce[buf]);
+      ++done[buf];
+      buf ^= 1;
+      if (!whole) {
+        // Stream-K fixup: the last contributor of this tile sums the partials in CTA order.
+        __threadfence();
+        tc::named_bar(1, 128);
+        const int64_t c_first = unit_owner(tile_u0, U, G), c_last = unit_owner(tile_u1 - 1, U, G);
+        if (threadIdx.x == 0) {
+          const int old = atomicAdd(&P.counters[gtile], 1);
+          *s_last = (old == (int)(c_last - c_first)) ? 1 : 0;
+        }
+        tc::named_bar(1, 128);
+        if (*s_last) {
+          __threadfence();
+          for (int c0 = 0; c0 < BN; c0 += 4) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int64_t c = c_first; c <= c_last; ++c) {
+              const int cfirst_tile = [&] {
+                const Unit f0 = decode_unit(P, (int)cta_start(c, U, G));
+                return P.prob[f0.p].tile_begin + f0.tile;
+              }();
+              const int sl = (int)c * 2 + (gtile == cfirst_tile ? 0 : 1);
+              const float4 v = __ldcg(reinterpret_cast<const float4 *>(P.partials + (size_t)sl * BM * BN +
+                                                                      (size_t)row * BN + c0));
+              acc.x += v.x;
+              acc.y += v.y;
+              acc.z += v.z;
+              acc.w += v.w;
+            }
+            if (f_ok) {
+              const float vv[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const int j = tm * BN + c0 + i;
+                if (j < pr.M) ycol[(int64_t)j * pr.ldy] = __float2bfloat16_rn(vv[i]);
+              }
+            }
+          }
+          if (threadIdx.x == 0) P.counters[gtile] = 0;
+        }
+      }
+      u = seg_end;
+    }
+  }
+  __syncthreads();
+  if (warp == 5) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem_base, tmem_cols);
+  }
+  if (threadIdx.x == 0 && *abort_flag) atomicOr(P.status, kStatusTimeout);
+}
+
+// ---- host ---------------------------------------------------------------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encoder() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2-D bf16 map of a row-major [outer][inner] array with row stride `ld` elements, 128B swizzle.
+bool map_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint64_t ld, uint32_t box_inner,
+            uint32_t box_outer) {
+  EncodeTiledFn enc = encoder();
+  if (!enc) return false;
+  if (((uintptr_t)base & 15) || (ld * 2) % 16) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {ld * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace gemm
+
+int gemm_tc_bn(int M) {
+  if (M > 256) return 256;
+  int bn = (M + 15) / 16 * 16;
+  return bn < 16 ? 16 : bn;
+}
+
+// Launch up to kMaxProblems products that share M (token count) in one persistent Stream-K grid.
+cudaError_t launch_gemm_tc(const LinearProblem *probs, int nprob, float *ws, size_t ws_bytes, int num_sms,
+                           int *status, cudaStream_t s) {
+  using namespace gemm;
+  if (nprob <= 0 || nprob > kMaxProblems) return cudaErrorInvalidValue;
+  const int M = probs[0].M;
+  Params P;
+  memset(&P, 0, sizeof(P));
+  P.BN = gemm_tc_bn(M);
+  const int stage_bytes = BM * BK * 2 + P.BN * BK * 2;
+  P.stages = std::min(8, (200 * 1024) / stage_bytes);
+  int units = 0, tiles = 0;
+  for (int i = 0; i < nprob; ++i) {
+    const LinearProblem &q = probs[i];
+    if (q.M != M) return cudaErrorInvalidValue;
+    Problem &p = P.prob[i];
+    if (!map_2d(&p.tmA, q.W, (uint64_t)q.K, (uint64_t)q.N * q.groups, (uint64_t)q.ldw, BK, BM)) return cudaErrorInvalidValue;
+    if (!map_2d(&p.tmB, q.x, (uint64_t)q.K * q.groups, (uint64_t)M, (uint64_t)q.ldx, BK, (uint32_t)P.BN))
+      return cudaErrorInvalidValue;
+    p.y = q.y;
+    p.ldy = q.ldy;
+    p.N = q.N;
+    p.M = M;
+    p.groups = q.groups;
+    p.Kg = q.K;
+    p.kblocks = (q.K + BK - 1) / BK;
+    p.tiles_n = (q.N + BM - 1) / BM;
+    p.tiles_m = (M + P.BN - 1) / P.BN;
+    p.tiles = p.tiles_n * p.tiles_m * q.groups;
+    p.unit_begin = units;
+    p.tile_begin = tiles;
+    units += p.tiles * p.kblocks;
+    tiles += p.tiles;
+  }
+  P.nprob = nprob;
+  P.total_units = units;
+  P.total_tiles = tiles;
+  if (tiles > kCounterInts) return cudaErrorInvalidValue;
+  const int grid = std::min(num_sms, units);
+  const size_t part_bytes = (size_t)grid * 2 * BM * P.BN * sizeof(float);
+  if (kCounterBytes + part_bytes > ws_bytes) return cudaErrorInvalidValue;
+  P.counters = reinterpret_cast<int *>(ws);
+  P.partials = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(ws) + kCounterBytes);
+  P.status = status;
+  const size_t smem = 1024 + (size_t)P.stages * stage_bytes + 256;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  k_gemm_tc<<<grid, kThreads, smem, s>>>(P);
+  return cudaGetLastError();
+}
+
+// Whether the tensor-core path takes a problem: TMA needs 16-byte aligned bases and row strides;
+// grouped products need each group's K to be whole 64-wide slices.
+bool gemm_tc_supported(const LinearProblem &q) {
+  if (((uintptr_t)q.x & 15) || ((uintptr_t)q.W & 15)) return false;
+  if (q.ldx % 8 || q.ldw % 8 || q.K % 8) return false;
+  if (q.groups > 1 && q.K % gemm::BK) return false;
+  if (q.M <= 0 || q.N <= 0 || q.K <= 0) return false;
+  return gemm::encoder() != nullptr;
+}
+
+}  // namespace csa
