@@ -357,17 +357,22 @@ def run_csa(args, rank, world, dist):
                 a[1] += 1
     ctx.trace(False)
     stage_ms = {k: v[0] / args.steps for k, v in acc.items()}  # per step (all layers)
-    lin_names = ("wq_a", "wq_b", "wkv", "idx_wq_b", "idx_wproj", "wo_a", "wo_b")
     M = B * T
-    lin_shapes = {"wq_a": (g.q_rank, g.dim), "wq_b": (g.n_heads * g.head_dim, g.q_rank), "wkv": (g.head_dim, g.dim),
-                  "idx_wq_b": (g.index_heads * g.index_hd, g.q_rank), "idx_wproj": (g.index_heads, g.dim),
-                  "wo_a": (g.groups * g.o_rank, g.n_heads * g.head_dim // g.groups), "wo_b": (g.dim, g.groups * g.o_rank)}
+    isrc = bool(wl.ratio and wl.is_index_source)
+    gw = g.n_heads * g.head_dim // g.groups
+    # projection stages of one layer: (weights [out, in] read once, activation width read, output width written)
+    lin_stages = {
+        "proj x": ([(g.q_rank, g.dim), (g.head_dim, g.dim)] + ([(g.index_heads, g.dim)] if isrc else []), g.dim,
+                   g.q_rank + g.head_dim + (g.index_heads if isrc else 0)),
+        "proj qr": ([(g.n_heads * g.head_dim, g.q_rank)] + ([(g.index_heads * g.index_hd, g.q_rank)] if isrc else []),
+                    g.q_rank, g.n_heads * g.head_dim + (g.index_heads * g.index_hd if isrc else 0)),
+        "wo_a": ([(g.groups * g.o_rank, gw)], g.n_heads * g.head_dim, g.groups * g.o_rank),
+        "wo_b": ([(g.dim, g.groups * g.o_rank)], g.groups * g.o_rank, g.dim),
+    }
     lin_bytes = lin_ms = 0.0
-    for n in lin_names:
+    for n, (ws_, xin, yout) in lin_stages.items():
         if n in stage_ms:
-            N_, K_ = lin_shapes[n]
-            xk = K_ * (g.groups if n == "wo_a" else 1)
-            lin_bytes += wl.layers * 2 * (N_ * K_ + M * xk + M * N_ * (g.groups if n == "wo_a" else 1))
+            lin_bytes += wl.layers * 2 * (sum(a * b for a, b in ws_) + M * xin + M * yout)
             lin_ms += stage_ms[n]
     counts = selection_counts(wl, sh_np)
     b_attn, b_idx, b_topk = algorithmic_bytes(wl, sh_np, counts)

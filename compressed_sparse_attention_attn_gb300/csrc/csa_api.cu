@@ -191,6 +191,7 @@ int csa_create(const csa_cfg *cfg, csa_ctx **out) {
   }
 #undef ALLOC
   if (e == cudaSuccess) e = cudaMemset(c->status, 0, 4 * sizeof(int));
+  if (e == cudaSuccess) e = cudaMemset(c->ws, 0, csa::kGemmCounterBytes);  // Stream-K arrival counters
   if (e != cudaSuccess) {
     c->release();
     delete c;
@@ -284,8 +285,8 @@ int csa_linear(csa_ctx *ctx, const csa_bf16 *x, int M, int K, int ldx, const csa
   if (!ctx || !x || !W || !y) return fail(CSA_ERR_ARG, "csa_linear: NULL argument");
   if (M < 0 || K <= 0 || N <= 0 || groups <= 0 || ldx < K * groups || ldw < K || ldy < N * groups)
     return fail(CSA_ERR_ARG, "csa_linear: bad shape M=%d K=%d N=%d groups=%d", M, K, N, groups);
-  CSA_CUDA(csa::launch_linear((const bf16 *)x, M, K, ldx, (const bf16 *)W, N, ldw, (bf16 *)y, ldy, groups, ctx->ws,
-                              ctx->ws_bytes, ctx->num_sms, (cudaStream_t)stream),
+  csa::LinearProblem pr{(const bf16 *)x, M, K, ldx, (const bf16 *)W, N, ldw, (bf16 *)y, ldy, groups};
+  CSA_CUDA(csa::launch_linear(&pr, 1, ctx->ws, ctx->ws_bytes, ctx->num_sms, ctx->status, (cudaStream_t)stream),
            "csa_linear");
   return CSA_OK;
 }
@@ -463,19 +464,28 @@ int attn_v41_forward(csa_ctx *ctx, const csa_layer_weights *w, csa_layer_state *
   } while (0)
 #define STEP(call, what) STAGE(call, what, 1)
 #define COPY(call, what) STAGE(call, what, 0)
-  // q path: qr = q_norm(wq_a x); q = wq_b qr; RoPE on the last rd of each head
-  STEP(csa::launch_linear(x, NT, g.dim, g.dim, (const bf16 *)w->wq_a, g.q_rank, g.dim, ctx->qr_raw, g.q_rank, 1, ctx->ws,
-                          ctx->ws_bytes, ctx->num_sms, s),
-       "wq_a");
+  const bool idx_src = r.ratio > 0 && r.is_index_source;
+  const int Hi = g.index_heads, dI = g.index_hd;
+  bf16 *qI = dbg && dbg->qI ? (bf16 *)dbg->qI : ctx->qI;
+  auto lin = [&](const bf16 *xx, int K, int ldx, const csa_bf16 *Wt, int N, bf16 *y, int ldy, int groups) {
+    return csa::LinearProblem{xx, NT, K, ldx, (const bf16 *)Wt, N, K, y, ldy, groups};
+  };
+  // projections of x: wq_a, wkv and (index sources) the indexer's head weights, one launch
+  {
+    csa::LinearProblem px[3] = {lin(x, g.dim, g.dim, w->wq_a, g.q_rank, ctx->qr_raw, g.q_rank, 1),
+                                lin(x, g.dim, g.dim, w->wkv, hd, ctx->kv_raw, hd, 1),
+                                lin(x, g.dim, g.dim, w->idx_wproj, Hi, ctx->iw_raw, Hi, 1)};
+    STEP(csa::launch_linear(px, idx_src ? 3 : 2, ctx->ws, ctx->ws_bytes, ctx->num_sms, ctx->status, s), "proj x");
+  }
+  // q path: qr = q_norm(wq_a x); q = wq_b qr (+ the indexer query q^I = W_IQ qr); RoPE on each head's tail
   STEP(csa::launch_rmsnorm(ctx->qr_raw, NT, g.q_rank, w->q_norm, g.eps, qr, s), "q_norm");
-  STEP(csa::launch_linear(qr, NT, g.q_rank, g.q_rank, (const bf16 *)w->wq_b, H * hd, g.q_rank, q, H * hd, 1, ctx->ws,
-                          ctx->ws_bytes, ctx->num_sms, s),
-       "wq_b");
+  {
+    csa::LinearProblem pq[2] = {lin(qr, g.q_rank, g.q_rank, w->wq_b, H * hd, q, H * hd, 1),
+                                lin(qr, g.q_rank, g.q_rank, w->idx_wq_b, Hi * dI, qI, Hi * dI, 1)};
+    STEP(csa::launch_linear(pq, idx_src ? 2 : 1, ctx->ws, ctx->ws_bytes, ctx->num_sms, ctx->status, s), "proj qr");
+  }
   STEP(csa::launch_rope(q, (int64_t)NT * H, hd, rd, pos_q, tab, ctx->tab_rows, 0, ctx->status, s), "rope q");
   // kv path: kv_norm(wkv x) -> RoPE -> fp8 round trip -> ring + window selection
-  STEP(csa::launch_linear(x, NT, g.dim, g.dim, (const bf16 *)w->wkv, hd, g.dim, ctx->kv_raw, hd, 1, ctx->ws, ctx->ws_bytes,
-                          ctx->num_sms, s),
-       "wkv");
   STEP(csa::launch_rmsnorm(ctx->kv_raw, NT, hd, w->kv_norm, g.eps, ctx->kv_raw, s), "kv_norm");
   STEP(csa::launch_kv_finish(ctx->kv_raw, kv, B, T, start_pos, hd, rd, tab, (bf16 *)st->window, W, win_idx, idx_stride,
                              dbg ? dbg->kv_codes : nullptr, dbg ? dbg->kv_scale : nullptr, s),
@@ -490,16 +500,8 @@ int attn_v41_forward(csa_ctx *ctx, const csa_layer_weights *w, csa_layer_state *
   if (r.ratio > 0) {
     const int K = g.index_topk;
     if (r.is_index_source) {
-      const int Hi = g.index_heads, dI = g.index_hd;
-      bf16 *qI = dbg && dbg->qI ? (bf16 *)dbg->qI : ctx->qI;
       float *wI = dbg && dbg->wI ? dbg->wI : ctx->wI;
       float *S = dbg && dbg->scores ? dbg->scores : ctx->scores;
-      STEP(csa::launch_linear(qr, NT, g.q_rank, g.q_rank, (const bf16 *)w->idx_wq_b, Hi * dI, g.q_rank, qI, Hi * dI, 1,
-                              ctx->ws, ctx->ws_bytes, ctx->num_sms, s),
-           "idx_wq_b");
-      STEP(csa::launch_linear(x, NT, g.dim, g.dim, (const bf16 *)w->idx_wproj, Hi, g.dim, ctx->iw_raw, Hi, 1, ctx->ws,
-                              ctx->ws_bytes, ctx->num_sms, s),
-           "idx_wproj");
       STEP(csa::launch_scale_bf16_to_f32(ctx->iw_raw, (int64_t)NT * Hi, (float)(1.0 / std::sqrt((double)dI * Hi)), wI, s),
            "w^I scale");
       const uint8_t *cand = r.uses_candidates ? sh->candidates : nullptr;
@@ -537,12 +539,12 @@ int attn_v41_forward(csa_ctx *ctx, const csa_layer_weights *w, csa_layer_state *
   }
   STEP(csa::launch_sparse_attn(a, ctx->ws, ctx->ws_bytes, ctx->num_sms, s), "sparse_attn");
   // grouped output: og[:, g] = o_rot[:, g*gw:(g+1)*gw] wo_a[g]^T, then out = og wo_b^T
-  STEP(csa::launch_linear(ctx->o_rot, NT, gw, H * hd, (const bf16 *)w->wo_a, g.o_rank, gw, og, G * g.o_rank, G, ctx->ws,
-                          ctx->ws_bytes, ctx->num_sms, s),
-       "wo_a");
-  STEP(csa::launch_linear(og, NT, G * g.o_rank, G * g.o_rank, (const bf16 *)w->wo_b, g.dim, G * g.o_rank, out, g.dim, 1,
-                          ctx->ws, ctx->ws_bytes, ctx->num_sms, s),
-       "wo_b");
+  {
+    csa::LinearProblem pa = lin(ctx->o_rot, gw, H * hd, w->wo_a, g.o_rank, og, G * g.o_rank, G);
+    STEP(csa::launch_linear(&pa, 1, ctx->ws, ctx->ws_bytes, ctx->num_sms, ctx->status, s), "wo_a");
+    csa::LinearProblem pb = lin(og, G * g.o_rank, G * g.o_rank, w->wo_b, g.dim, out, g.dim, 1);
+    STEP(csa::launch_linear(&pb, 1, ctx->ws, ctx->ws_bytes, ctx->num_sms, ctx->status, s), "wo_b");
+  }
 #undef STEP
 #undef COPY
 #undef STAGE

@@ -39,9 +39,21 @@ cudaError_t launch_kv_finish(const bf16 *kv_in, bf16 *kv_out, int B, int T, int 
                              int8_t *scales, cudaStream_t s);
 cudaError_t launch_scale_bf16_to_f32(const bf16 *x, int64_t n, float scale, float *y, cudaStream_t s);
 
-// y[M][N] (+ groups) = x W^T with f32 accumulation, bf16 out.  ws/ws_bytes: split-K workspace.
-cudaError_t launch_linear(const bf16 *x, int M, int K, int ldx, const bf16 *W, int N, int ldw, bf16 *y, int ldy,
-                          int groups, float *ws, size_t ws_bytes, int num_sms, cudaStream_t s);
+// One product y[M][g*N + n] = sum_k x[m][g*K + k] W[g*N + n][k] for g < groups (f32 accumulation,
+// bf16 out); x row stride ldx, W row stride ldw, y row stride ldy (elements).
+struct LinearProblem {
+  const bf16 *x;
+  int M, K, ldx;
+  const bf16 *W;
+  int N, ldw;
+  bf16 *y;
+  int ldy, groups;
+};
+// Products sharing M run in one tensor-core launch (up to 4 at a time).  ws/ws_bytes: Stream-K
+// arrival counters and partials (the counters must be zero between launches).
+cudaError_t launch_linear(const LinearProblem *probs, int n, float *ws, size_t ws_bytes, int num_sms, int *status,
+                          cudaStream_t s);
+constexpr size_t kGemmCounterBytes = 65536 * sizeof(int);
 
 cudaError_t launch_index_scores(const bf16 *qI, const float *wI, const bf16 *KI, int B, int T, int start_pos, int Hi,
                                 int dI, int Lstride, int compress_len, int ratio, const uint8_t *cand, int cand_width,

@@ -7,12 +7,33 @@ cudaError_t launch_linear_simt(const bf16 *x, int M, int K, int ldx, const bf16 
                                int groups, cudaStream_t s);
 cudaError_t launch_sparse_attn_simt(const AttnArgs &a, cudaStream_t s);
 
-cudaError_t launch_linear(const bf16 *x, int M, int K, int ldx, const bf16 *W, int N, int ldw, bf16 *y, int ldy,
-                          int groups, float *ws, size_t ws_bytes, int num_sms, cudaStream_t s) {
-  (void)ws;
-  (void)ws_bytes;
-  (void)num_sms;
-  return launch_linear_simt(x, M, K, ldx, W, N, ldw, y, ldy, groups, s);
+cudaError_t launch_gemm_tc(const LinearProblem *probs, int nprob, float *ws, size_t ws_bytes, int num_sms,
+                           int *status, cudaStream_t s);
+bool gemm_tc_supported(const LinearProblem &q);
+
+// Tensor-core Stream-K GEMM for every product TMA can address (16-byte aligned bases and strides);
+// the CUDA-core kernel only for the rest.
+cudaError_t launch_linear(const LinearProblem *probs, int n, float *ws, size_t ws_bytes, int num_sms, int *status,
+                          cudaStream_t s) {
+  LinearProblem batch[4];
+  int nb = 0;
+  for (int i = 0; i < n; ++i) {
+    const LinearProblem &q = probs[i];
+    if (q.M <= 0) continue;
+    if (gemm_tc_supported(q)) {
+      if (nb == 4 || (nb > 0 && batch[0].M != q.M)) {
+        cudaError_t e = launch_gemm_tc(batch, nb, ws, ws_bytes, num_sms, status, s);
+        if (e != cudaSuccess) return e;
+        nb = 0;
+      }
+      batch[nb++] = q;
+    } else {
+      cudaError_t e = launch_linear_simt(q.x, q.M, q.K, q.ldx, q.W, q.N, q.ldw, q.y, q.ldy, q.groups, s);
+      if (e != cudaSuccess) return e;
+    }
+  }
+  if (nb) return launch_gemm_tc(batch, nb, ws, ws_bytes, num_sms, status, s);
+  return cudaSuccess;
 }
 
 cudaError_t launch_sparse_attn(const AttnArgs &a, float *ws, size_t ws_bytes, int num_sms, cudaStream_t s) {

@@ -72,7 +72,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
   uint64_t *accf = empty + S;  // [2]
   uint64_t *acce = accf + 2;   // [2]
   uint64_t *drain = acce + 2;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  uint64_t *epi = drain + 1;  // the 128 epilogue threads' own barrier
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(epi + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   int *s_last = const_cast<int *>(abort_flag) + 1;
 
@@ -92,6 +93,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
       tc::mbar_init(&acce[b], 128);
     }
     tc::mbar_init(drain, 1);
+    tc::mbar_init(epi, 128);
     *abort_flag = 0;
     tc::fence_barrier_init();
   }
@@ -190,6 +192,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
     // ---------------------------------------------------------------- epilogue (warps 0-3)
     const int row = warp * 32 + lane;  // feature within the tile
     int done[2] = {0, 0};
+    uint32_t epi_uses = 0;
+    auto epi_sync = [&]() -> bool {
+      tc::mbar_arrive(epi);
+      return tc::mbar_wait(epi, (epi_uses++) & 1u, abort_flag);
+    };
     int buf = 0;
     int u = u0;
     const int first_tile_global = [&] {
@@ -240,13 +247,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
       if (!whole) {
         // Stream-K fixup: the last contributor of this tile sums the partials in CTA order.
         __threadfence();
-        tc::named_bar(1, 128);
+        if (!epi_sync()) break;
         const int64_t c_first = unit_owner(tile_u0, U, G), c_last = unit_owner(tile_u1 - 1, U, G);
         if (threadIdx.x == 0) {
           const int old = atomicAdd(&P.counters[gtile], 1);
           *s_last = (old == (int)(c_last - c_first)) ? 1 : 0;
         }
-        tc::named_bar(1, 128);
+        if (!epi_sync()) break;
         if (*s_last) {
           __threadfence();
           for (int c0 = 0; c0 < BN; c0 += 4) {
@@ -275,6 +282,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
           }
           if (threadIdx.x == 0) P.counters[gtile] = 0;
         }
+        // the flag is rewritten for the next tile only after everyone has read it
+        if (!epi_sync()) break;
       }
       u = seg_end;
     }
