@@ -31,6 +31,7 @@ constexpr int BK = 64;
 constexpr int kThreads = 192;
 constexpr int kCounterInts = 65536;            // arrival counters at the head of the workspace
 constexpr size_t kCounterBytes = kCounterInts * sizeof(int);
+constexpr int kMaxContrib = 320;  // >= grid + 1 for any grid of one CTA per SM
 
 struct Problem {
   CUtensorMap tmA;  // W [groups*N rows][Kg] bf16, box {64, 128}
@@ -76,6 +77,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(epi + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   int *s_last = const_cast<int *>(abort_flag) + 1;
+  int *cslot = s_last + 1;  // [kMaxContrib] partial slots of a tile's contributors, in CTA order
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t U = P.total_units, G = gridDim.x;
@@ -256,27 +258,45 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__
         if (!epi_sync()) break;
         if (*s_last) {
           __threadfence();
-          for (int c0 = 0; c0 < BN; c0 += 4) {
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int64_t c = c_first; c <= c_last; ++c) {
-              const int cfirst_tile = [&] {
-                const Unit f0 = decode_unit(P, (int)cta_start(c, U, G));
-                return P.prob[f0.p].tile_begin + f0.tile;
-              }();
-              const int sl = (int)c * 2 + (gtile == cfirst_tile ? 0 : 1);
-              const float4 v = __ldcg(reinterpret_cast<const float4 *>(P.partials + (size_t)sl * BM * BN +
-                                                                      (size_t)row * BN + c0));
-              acc.x += v.x;
-              acc.y += v.y;
-              acc.z += v.z;
-              acc.w += v.w;
+          const int nc = (int)(c_last - c_first + 1);
+          for (int i = threadIdx.x; i < nc; i += 128) {
+            const int64_t c = c_first + i;
+            const Unit f0 = decode_unit(P, (int)cta_start(c, U, G));
+            cslot[i] = (int)c * 2 + (gtile == P.prob[f0.p].tile_begin + f0.tile ? 0 : 1);
+          }
+          if (!epi_sync()) break;
+          // sum the contributors' rows in CTA order, four contributors' 16-column chunks in flight
+          const float *base = P.partials + (size_t)row * BN;
+          for (int c0 = 0; c0 < BN; c0 += 16) {
+            float a[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) a[i] = 0.f;
+            for (int i = 0; i < nc; i += 4) {
+              float4 v[4][4];
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                if (i + q < nc) {
+                  const float4 *src = reinterpret_cast<const float4 *>(base + (size_t)cslot[i + q] * BM * BN + c0);
+#pragma unroll
+                  for (int k = 0; k < 4; ++k) v[q][k] = __ldcg(src + k);
+                }
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                if (i + q < nc) {
+#pragma unroll
+                  for (int k = 0; k < 4; ++k) {
+                    a[4 * k] += v[q][k].x;
+                    a[4 * k + 1] += v[q][k].y;
+                    a[4 * k + 2] += v[q][k].z;
+                    a[4 * k + 3] += v[q][k].w;
+                  }
+                }
             }
             if (f_ok) {
-              const float vv[4] = {acc.x, acc.y, acc.z, acc.w};
 #pragma unroll
-              for (int i = 0; i < 4; ++i) {
+              for (int i = 0; i < 16; ++i) {
                 const int j = tm * BN + c0 + i;
-                if (j < pr.M) ycol[(int64_t)j * pr.ldy] = __float2bfloat16_rn(vv[i]);
+                if (j < pr.M) ycol[(int64_t)j * pr.ldy] = __float2bfloat16_rn(a[i]);
               }
             }
           }
@@ -377,13 +397,13 @@ cudaError_t launch_gemm_tc(const LinearProblem *probs, int nprob, float *ws, siz
   P.total_units = units;
   P.total_tiles = tiles;
   if (tiles > kCounterInts) return cudaErrorInvalidValue;
-  const int grid = std::min(num_sms, units);
+  const int grid = std::min(std::min(num_sms, units), kMaxContrib - 1);
   const size_t part_bytes = (size_t)grid * 2 * BM * P.BN * sizeof(float);
   if (kCounterBytes + part_bytes > ws_bytes) return cudaErrorInvalidValue;
   P.counters = reinterpret_cast<int *>(ws);
   P.partials = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(ws) + kCounterBytes);
   P.status = status;
-  const size_t smem = 1024 + (size_t)P.stages * stage_bytes + 256;
+  const size_t smem = 1024 + (size_t)P.stages * stage_bytes + 256 + kMaxContrib * sizeof(int);
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
