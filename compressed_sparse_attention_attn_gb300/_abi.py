@@ -71,6 +71,7 @@ SIGNATURES = {
     "csa_trace_read": (I, [P, I, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(F)]),
     "csa_last_launches": (I, [P]),
     "csa_linear": (I, [P, P, I, I, I, P, I, I, P, I, I, P]),
+    "csa_linear_noalloc": (I, [P, I, I, I, P, I, I, P, I, I, P]),
     "csa_rmsnorm": (I, [P, I, I, P, F, P, P]),
     "csa_rope": (I, [P, I64, I, I, P, I, P, I, I, P]),
     "csa_act_quant": (I, [P, I64, P, P, P]),

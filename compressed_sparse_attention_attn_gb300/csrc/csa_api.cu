@@ -36,6 +36,14 @@ int cuda_fail(cudaError_t e, const char *where) {
 
 }  // namespace
 
+int csa::set_error(int code, const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
 struct csa_ctx {
   csa_cfg cfg;
   int device = 0;

@@ -84,6 +84,9 @@ struct AttnArgs {
 };
 cudaError_t launch_sparse_attn(const AttnArgs &a, float *ws, size_t ws_bytes, int num_sms, cudaStream_t s);
 
+// Record the calling thread's last error (attn_v41_last_error) and return `code`.
+int set_error(int code, const char *fmt, ...);
+
 // Host-side tables (double precision, rounded to f32).
 void build_rope_table(int rd, int max_seq, double theta, int orig_seq, double factor, double beta_fast,
                       double beta_slow, float *tab);

@@ -18,6 +18,8 @@
 // Warp roles (192 threads): warps 0-3 epilogue (TMEM lane quadrant = warp), warp 4 TMA producer,
 // warp 5 TMEM allocation + MMA issue.  Every mbarrier wait is time-bounded; a timeout raises the
 // device status word and the CTA drains its copies and MMAs, frees TMEM and exits.
+#include <mutex>
+
 #include "csa_internal.cuh"
 #include "tc_ptx.cuh"
 
@@ -425,3 +427,81 @@ bool gemm_tc_supported(const LinearProblem &q) {
 }
 
 }  // namespace csa
+
+// ---- allocation-free projection -------------------------------------------------------------------
+// csa_linear_noalloc: the same Stream-K product, for callers that cannot allocate device memory
+// (an embedding runtime that owns a fixed device-memory budget, or code that runs without a
+// csa_ctx, whose creation allocates workspaces).  Its scratch -- the arrival counters, the f32
+// partials and a status word -- is this file-scope device array, which every GPU that loads the
+// library holds until the process exits.  Host code must not hand the array's name to a kernel:
+// in host code it is only a stand-in; the device address comes from cudaGetSymbolAddress, looked up
+// once per device (with that device current) by the first call made on it.
+
+namespace csa {
+namespace {
+
+constexpr int kNoAllocMaxM = 32;     // tokens: the partials below are sized for BN <= 32
+constexpr int kNoAllocMaxGrid = 160;  // CTAs: one per SM on GB300 (152) with room to spare
+constexpr size_t kNoAllocPartialBytes = (size_t)kNoAllocMaxGrid * 2 * gemm::BM * kNoAllocMaxM * sizeof(float);
+constexpr size_t kNoAllocWsBytes = gemm::kCounterBytes + kNoAllocPartialBytes;
+constexpr size_t kNoAllocBytes = kNoAllocWsBytes + 256;  // + the status word
+constexpr int kNoAllocMaxDevices = 128;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+std::mutex g_noalloc_mu;
+void *g_noalloc_addr[kNoAllocMaxDevices];
+int g_noalloc_sms[kNoAllocMaxDevices];
+
+}  // namespace
+}  // namespace csa
+
+extern "C" int csa_linear_noalloc(const csa_bf16 *x, int M, int K, int ldx, const csa_bf16 *W, int N, int ldw,
+                                  csa_bf16 *y, int ldy, int groups, csa_stream stream) {
+  using namespace csa;
+  if (!x || !W || !y) return set_error(CSA_ERR_ARG, "csa_linear_noalloc: NULL argument");
+  if (M <= 0 || K <= 0 || N <= 0 || groups <= 0 || ldx < K * groups || ldw < K || ldy < N * groups)
+    return set_error(CSA_ERR_ARG, "csa_linear_noalloc: bad shape M=%d K=%d N=%d groups=%d", M, K, N, groups);
+  if (M > kNoAllocMaxM)
+    return set_error(CSA_ERR_SHAPE, "csa_linear_noalloc: M=%d above the %d tokens its static scratch holds", M,
+                     kNoAllocMaxM);
+  const int64_t tiles = (int64_t)((N + gemm::BM - 1) / gemm::BM) * groups;
+  if (tiles > gemm::kCounterInts)
+    return set_error(CSA_ERR_SHAPE, "csa_linear_noalloc: %lld output tiles above %d", (long long)tiles,
+                     gemm::kCounterInts);
+  LinearProblem pr{(const bf16 *)x, M, K, ldx, (const bf16 *)W, N, ldw, (bf16 *)y, ldy, groups};
+  if (!gemm_tc_supported(pr))
+    return set_error(CSA_ERR_ARG,
+                     "csa_linear_noalloc: operands and row strides must be 16-byte aligned, K a multiple of 8 "
+                     "(of 64 with groups)");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return set_error(CSA_ERR_CUDA, "csa_linear_noalloc: cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return set_error(CSA_ERR_ARG, "csa_linear_noalloc: device %d", dev);
+  void *scratch = nullptr;
+  int sms = 0;
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+      void *p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+      if (e != cudaSuccess || !p)
+        return set_error(CSA_ERR_CUDA, "csa_linear_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
+      e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      if (e != cudaSuccess)
+        return set_error(CSA_ERR_CUDA, "csa_linear_noalloc: device query: %s", cudaGetErrorString(e));
+      g_noalloc_sms[dev] = sms;
+      g_noalloc_addr[dev] = p;
+    }
+    scratch = g_noalloc_addr[dev];
+    sms = g_noalloc_sms[dev];
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  // the array keeps the last call's contents: the counters this launch uses must start at zero
+  e = cudaMemsetAsync(scratch, 0, (size_t)tiles * sizeof(int), s);
+  if (e != cudaSuccess) return set_error(CSA_ERR_CUDA, "csa_linear_noalloc: clear: %s", cudaGetErrorString(e));
+  int *status = reinterpret_cast<int *>(static_cast<unsigned char *>(scratch) + kNoAllocWsBytes);
+  e = launch_gemm_tc(&pr, 1, static_cast<float *>(scratch), kNoAllocWsBytes, std::min(sms, kNoAllocMaxGrid), status, s);
+  if (e != cudaSuccess) return set_error(CSA_ERR_CUDA, "csa_linear_noalloc: launch: %s", cudaGetErrorString(e));
+  return CSA_OK;
+}

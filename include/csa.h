@@ -260,6 +260,25 @@ CSA_API int csa_sparse_attn(csa_ctx *ctx, const csa_bf16 *q, int B, int T, int H
                     csa_bf16 *o, csa_bf16 *o_rot, int rd, int start_pos, const float *tab, int tab_rows,
                     csa_stream stream);
 
+/* Allocation-free projection.  The pages have no counterpart: this is an addition for callers that
+ * cannot allocate device memory -- a host runtime that owns a fixed device-memory budget and forbids
+ * allocations outside it, or code that has no csa_ctx (csa_create allocates the context's
+ * workspaces).  It computes exactly what csa_linear computes, y = x W^T with f32 accumulation and a
+ * bf16 result (same arguments, same grouping), with the same tensor-core kernel, and allocates
+ * nothing: no cudaMalloc, no cudaFree, no context.  Its scratch (Stream-K arrival counters, f32
+ * partials, a status word) is one static device array of 5,505,280 bytes (5.25 MiB) inside the
+ * library, which every GPU that loads the library holds until the process exits.
+ * Limits: M <= 32 tokens; ceil(N/128) * groups <= 65536; x and W 16-byte aligned, ldx and ldw
+ * multiples of 8, K a multiple of 8 (of 64 when groups > 1).  Beyond them it returns CSA_ERR_SHAPE or
+ * CSA_ERR_ARG and launches nothing.
+ * The first call on a device looks the array's device address up (cudaGetSymbolAddress, once per
+ * device, with that device current); make that first call before any stream capture.
+ * Every call shares the one array and it keeps the last call's contents: each call clears the
+ * counters it needs on `stream` before its launch, but calls whose work overlaps on the GPU (on
+ * different streams or from different threads) race on the array and must not be issued. */
+CSA_API int csa_linear_noalloc(const csa_bf16 *x, int M, int K, int ldx, const csa_bf16 *W, int N, int ldw,
+                               csa_bf16 *y, int ldy, int groups, csa_stream stream);
+
 #ifdef __cplusplus
 }
 #endif
