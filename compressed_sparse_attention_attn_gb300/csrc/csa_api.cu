@@ -379,6 +379,11 @@ int csa_sparse_attn(csa_ctx *ctx, const csa_bf16 *q, int B, int T, int H, int hd
   if (nb > 0 && (!idx_b)) return fail(CSA_ERR_ARG, "csa_sparse_attn: idx_b is NULL");
   if (b_len > 0 && !rows_b) return fail(CSA_ERR_ARG, "csa_sparse_attn: rows_b is NULL");
   if (na + nb > 2048) return fail(CSA_ERR_TOO_WIDE, "csa_sparse_attn: selection of %d rows above 2048", na + nb);
+  if ((int64_t)a_len * hd > a_seq_stride && B > 1) return fail(CSA_ERR_ARG, "csa_sparse_attn: a_len rows exceed a_seq_stride");
+  if ((int64_t)b_len * hd > b_seq_stride && B > 1 && b_len > 0)
+    return fail(CSA_ERR_ARG, "csa_sparse_attn: b_len rows exceed b_seq_stride");
+  if (a_seq_stride % hd || (b_len > 0 && b_seq_stride % hd))
+    return fail(CSA_ERR_ARG, "csa_sparse_attn: sequence strides must be whole rows");
   if (o_rot && (!tab || rd <= 0 || rd % 2 || rd > hd || start_pos < 0 || start_pos + T > tab_rows))
     return fail(CSA_ERR_ARG, "csa_sparse_attn: inverse rotation needs a table covering the positions");
   csa::AttnArgs a{(const bf16 *)q, B, T, H, hd, (const bf16 *)rows_a, a_seq_stride, a_len, (const bf16 *)rows_b,

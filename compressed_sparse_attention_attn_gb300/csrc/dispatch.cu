@@ -36,10 +36,14 @@ cudaError_t launch_linear(const LinearProblem *probs, int n, float *ws, size_t w
   return cudaSuccess;
 }
 
+bool sparse_attn_tc_supported(const AttnArgs &a);
+cudaError_t launch_sparse_attn_tc(const AttnArgs &a, int num_sms, cudaStream_t s);
+
+// Tensor-core kernel for head_dim 512 (the model's); the CUDA-core kernel for other head sizes.
 cudaError_t launch_sparse_attn(const AttnArgs &a, float *ws, size_t ws_bytes, int num_sms, cudaStream_t s) {
   (void)ws;
   (void)ws_bytes;
-  (void)num_sms;
+  if (sparse_attn_tc_supported(a)) return launch_sparse_attn_tc(a, num_sms, s);
   return launch_sparse_attn_simt(a, s);
 }
 
