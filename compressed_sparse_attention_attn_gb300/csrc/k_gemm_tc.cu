@@ -64,7 +64,7 @@ __device__ __forceinline__ Unit decode_unit(const Params &P, int u) {
 __device__ __forceinline__ int64_t cta_start(int64_t c, int64_t U, int64_t G) { return c * U / G; }
 __device__ __forceinline__ int64_t unit_owner(int64_t v, int64_t U, int64_t G) { return ((v + 1) * G - 1) / U; }
 
-__global__ void __launch_bounds__(kThreads, 1) k_gemm_tc(const __grid_constant__ Params P) {
+__global__ void __launch_bounds__(kThreads, 2) k_gemm_tc(const __grid_constant__ Params P) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = tc::smem_u32(smem_raw);
   uint8_t *smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
@@ -371,7 +371,9 @@ cudaError_t launch_gemm_tc(const LinearProblem *probs, int nprob, float *ws, siz
   memset(&P, 0, sizeof(P));
   P.BN = gemm_tc_bn(M);
   const int stage_bytes = BM * BK * 2 + P.BN * BK * 2;
-  P.stages = std::min(8, (200 * 1024) / stage_bytes);
+  // small token tiles: two CTAs per SM (two independent TMA streams), five stages each
+  const int per_sm = P.BN <= 64 ? 2 : 1;
+  P.stages = per_sm == 2 ? std::min(5, (100 * 1024) / stage_bytes) : std::min(8, (200 * 1024) / stage_bytes);
   int units = 0, tiles = 0;
   for (int i = 0; i < nprob; ++i) {
     const LinearProblem &q = probs[i];
@@ -399,9 +401,10 @@ cudaError_t launch_gemm_tc(const LinearProblem *probs, int nprob, float *ws, siz
   P.total_units = units;
   P.total_tiles = tiles;
   if (tiles > kCounterInts) return cudaErrorInvalidValue;
-  const int grid = std::min(std::min(num_sms, units), kMaxContrib - 1);
-  const size_t part_bytes = (size_t)grid * 2 * BM * P.BN * sizeof(float);
-  if (kCounterBytes + part_bytes > ws_bytes) return cudaErrorInvalidValue;
+  const size_t part_per_cta = (size_t)2 * BM * P.BN * sizeof(float);
+  if (ws_bytes < kCounterBytes + part_per_cta) return cudaErrorInvalidValue;
+  const int ws_grid = (int)std::min<size_t>((ws_bytes - kCounterBytes) / part_per_cta, (size_t)(kMaxContrib - 1));
+  const int grid = std::min(std::min(per_sm * num_sms, units), ws_grid);
   P.counters = reinterpret_cast<int *>(ws);
   P.partials = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(ws) + kCounterBytes);
   P.status = status;
