@@ -371,8 +371,9 @@ cudaError_t launch_gemm_tc(const LinearProblem *probs, int nprob, float *ws, siz
   memset(&P, 0, sizeof(P));
   P.BN = gemm_tc_bn(M);
   const int stage_bytes = BM * BK * 2 + P.BN * BK * 2;
-  // small token tiles: two CTAs per SM (two independent TMA streams), five stages each
-  const int per_sm = P.BN <= 64 ? 2 : 1;
+  // one CTA per SM: two per SM (five stages each) measured slower at decode, because twice the CTAs
+  // split each tile's k-range twice as often and the Stream-K fixups dominate
+  const int per_sm = 1;
   P.stages = per_sm == 2 ? std::min(5, (100 * 1024) / stage_bytes) : std::min(8, (200 * 1024) / stage_bytes);
   int units = 0, tiles = 0;
   for (int i = 0; i < nprob; ++i) {
