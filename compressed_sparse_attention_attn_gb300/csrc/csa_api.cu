@@ -54,6 +54,8 @@ struct csa_ctx {
   bf16 *qr_raw = nullptr, *qr = nullptr, *q = nullptr, *kv_raw = nullptr, *kv = nullptr, *qI = nullptr,
        *iw_raw = nullptr, *o = nullptr, *o_rot = nullptr, *og = nullptr, *x_stage = nullptr, *out_stage = nullptr;
   float *wI = nullptr, *scores = nullptr;
+  float *xpart = nullptr;  // split-K partials of the x projections [S][NT][q_rank + hd + Hi]
+  int xpart_rows = 0;
   int32_t *idx_win = nullptr;
   int *status = nullptr;
   float *ws = nullptr;  // split-K and split-row partials
@@ -186,6 +188,8 @@ int csa_create(const csa_cfg *cfg, csa_ctx **out) {
   ALLOC(wI, nt * Hi);
   ALLOC(scores, nt * (size_t)c->scores_stride);
   ALLOC(idx_win, nt * (size_t)g.window);
+  c->xpart_rows = (int)std::max<size_t>(nt, 16 * std::min<size_t>(nt, 256));
+  ALLOC(xpart, (size_t)c->xpart_rows * (g.q_rank + g.head_dim + g.index_heads));
   ALLOC(o, nt * H * hd);
   ALLOC(o_rot, nt * H * hd);
   ALLOC(og, nt * (size_t)g.groups * g.o_rank);
@@ -405,6 +409,13 @@ static int check_forward(const csa_ctx *ctx, const csa_layer_weights *w, const c
   if (!w->sink || !w->q_norm || !w->kv_norm || !w->wq_a || !w->wq_b || !w->wkv || !w->wo_a || !w->wo_b)
     return fail(CSA_ERR_ARG, "attn_v41_forward: a weight pointer is NULL");
   if (r.ratio < 0) return fail(CSA_ERR_ARG, "attn_v41_forward: negative ratio");
+  {
+    const void *al[] = {x, out, w->wq_a, w->wq_b, w->wkv, w->wo_a, w->wo_b, w->idx_wq_b, w->idx_wproj};
+    for (const void *p : al)
+      if ((uintptr_t)p & 15) return fail(CSA_ERR_ARG, "attn_v41_forward: tensors must be 16-byte aligned");
+    if (g.dim % 8 || g.q_rank % 8 || g.o_rank % 8 || (g.n_heads * g.head_dim / g.groups) % 64)
+      return fail(CSA_ERR_ARG, "attn_v41_forward: dim, q_rank, o_rank must be multiples of 8, the group width of 64");
+  }
   if (r.is_kv_source || r.is_candidate_source)
     return fail(CSA_ERR_UNSUPPORTED, "attn_v41_forward: kv-source and candidate-source roles are not implemented");
   if (B <= 0 || B > g.max_batch) return fail(CSA_ERR_SHAPE, "attn_v41_forward: batch %d outside [1, %d]", B, g.max_batch);
@@ -483,26 +494,35 @@ int attn_v41_forward(csa_ctx *ctx, const csa_layer_weights *w, csa_layer_state *
   auto lin = [&](const bf16 *xx, int K, int ldx, const csa_bf16 *Wt, int N, bf16 *y, int ldy, int groups) {
     return csa::LinearProblem{xx, NT, K, ldx, (const bf16 *)Wt, N, K, y, ldy, groups};
   };
-  // projections of x: wq_a, wkv and (index sources) the indexer's head weights, one launch
+  // projections of x: wq_a, wkv and (index sources) the indexer's head weights, one split-K launch
+  // writing f32 partials; one fused kernel reduces them into qr (RMSNorm), the window row (RMSNorm,
+  // RoPE, fp8, ring, window selection) and w^I
+  const int ldp = g.q_rank + hd + (idx_src ? Hi : 0);
+  float *wI = dbg && dbg->wI ? dbg->wI : ctx->wI;
   {
-    csa::LinearProblem px[3] = {lin(x, g.dim, g.dim, w->wq_a, g.q_rank, ctx->qr_raw, g.q_rank, 1),
-                                lin(x, g.dim, g.dim, w->wkv, hd, ctx->kv_raw, hd, 1),
-                                lin(x, g.dim, g.dim, w->idx_wproj, Hi, ctx->iw_raw, Hi, 1)};
-    STEP(csa::launch_linear(px, idx_src ? 3 : 2, ctx->ws, ctx->ws_bytes, ctx->num_sms, ctx->status, s), "proj x");
+    csa::LinearProblem px[3] = {lin(x, g.dim, g.dim, w->wq_a, g.q_rank, nullptr, 0, 1),
+                                lin(x, g.dim, g.dim, w->wkv, hd, nullptr, 0, 1),
+                                lin(x, g.dim, g.dim, w->idx_wproj, Hi, nullptr, 0, 1)};
+    px[0].part = ctx->xpart;
+    px[1].part = ctx->xpart + g.q_rank;
+    px[2].part = ctx->xpart + g.q_rank + hd;
+    for (auto &p : px) p.ldp = ldp;
+    const int np = idx_src ? 3 : 2;
+    const int S = csa::gemm_tc_split_count(px, np, ctx->num_sms, std::max(1, ctx->xpart_rows / NT));
+    STEP(csa::launch_gemm_tc_split(px, np, S, ctx->status, s), "proj x");
+    csa::XFinishArgs xa{ctx->xpart, S, ldp, g.q_rank, hd, idx_src ? Hi : 0, w->q_norm, w->kv_norm, g.eps, qr, kv, B,
+                        T, start_pos, rd, tab, (bf16 *)st->window, W, win_idx, idx_stride,
+                        dbg ? dbg->kv_codes : nullptr, dbg ? dbg->kv_scale : nullptr,
+                        (float)(1.0 / std::sqrt((double)dI * std::max(Hi, 1))), wI};
+    STEP(csa::launch_x_finish(xa, s), "x finish");
   }
-  // q path: qr = q_norm(wq_a x); q = wq_b qr (+ the indexer query q^I = W_IQ qr); RoPE on each head's tail
-  STEP(csa::launch_rmsnorm(ctx->qr_raw, NT, g.q_rank, w->q_norm, g.eps, qr, s), "q_norm");
+  // q path: q = wq_b qr (+ the indexer query q^I = W_IQ qr); RoPE on each head's tail
   {
     csa::LinearProblem pq[2] = {lin(qr, g.q_rank, g.q_rank, w->wq_b, H * hd, q, H * hd, 1),
                                 lin(qr, g.q_rank, g.q_rank, w->idx_wq_b, Hi * dI, qI, Hi * dI, 1)};
     STEP(csa::launch_linear(pq, idx_src ? 2 : 1, ctx->ws, ctx->ws_bytes, ctx->num_sms, ctx->status, s), "proj qr");
   }
   STEP(csa::launch_rope(q, (int64_t)NT * H, hd, rd, pos_q, tab, ctx->tab_rows, 0, ctx->status, s), "rope q");
-  // kv path: kv_norm(wkv x) -> RoPE -> fp8 round trip -> ring + window selection
-  STEP(csa::launch_rmsnorm(ctx->kv_raw, NT, hd, w->kv_norm, g.eps, ctx->kv_raw, s), "kv_norm");
-  STEP(csa::launch_kv_finish(ctx->kv_raw, kv, B, T, start_pos, hd, rd, tab, (bf16 *)st->window, W, win_idx, idx_stride,
-                             dbg ? dbg->kv_codes : nullptr, dbg ? dbg->kv_scale : nullptr, s),
-       "kv_finish");
   // the compressed selection
   const int32_t *idx_b = nullptr;
   int nb = 0;
@@ -513,10 +533,7 @@ int attn_v41_forward(csa_ctx *ctx, const csa_layer_weights *w, csa_layer_state *
   if (r.ratio > 0) {
     const int K = g.index_topk;
     if (r.is_index_source) {
-      float *wI = dbg && dbg->wI ? dbg->wI : ctx->wI;
       float *S = dbg && dbg->scores ? dbg->scores : ctx->scores;
-      STEP(csa::launch_scale_bf16_to_f32(ctx->iw_raw, (int64_t)NT * Hi, (float)(1.0 / std::sqrt((double)dI * Hi)), wI, s),
-           "w^I scale");
       const uint8_t *cand = r.uses_candidates ? sh->candidates : nullptr;
       STEP(csa::launch_index_scores(qI, wI, (const bf16 *)sh->index_k, B, T, start_pos, Hi, dI, sh->compress_stride,
                                     sh->compress_len, r.ratio, cand, sh->cand_width, g.cand_block, S, s),

@@ -48,12 +48,43 @@ struct LinearProblem {
   int N, ldw;
   bf16 *y;
   int ldy, groups;
+  float *part = nullptr;  // split-K mode: f32 partials [S][M][ldp], this problem's columns at part
+  int ldp = 0;
 };
 // Products sharing M run in one tensor-core launch (up to 4 at a time).  ws/ws_bytes: Stream-K
 // arrival counters and partials (the counters must be zero between launches).
 cudaError_t launch_linear(const LinearProblem *probs, int n, float *ws, size_t ws_bytes, int num_sms, int *status,
                           cudaStream_t s);
 constexpr size_t kGemmCounterBytes = 65536 * sizeof(int);
+// Split-K without fixup: products sharing M and K; CTA (tile, s) writes its f32 partial sum over
+// its K range to part[s][m][col] (every problem's part/ldp set).  The consumer sums the S slices.
+cudaError_t launch_gemm_tc_split(const LinearProblem *probs, int nprob, int S, int *status, cudaStream_t s);
+// The largest split count S <= max_S dividing the problems' k-slices with tiles * S <= max_ctas (>= 1).
+int gemm_tc_split_count(const LinearProblem *probs, int nprob, int max_ctas, int max_S);
+bool gemm_tc_supported(const LinearProblem &q);
+
+// The window rows and the query latent from split-K partials of [wq_a | wkv | weights_proj] x:
+// per token, the sum of the S slices rounded to bf16 (linear_bf16), then qr = RMSNorm * q_norm,
+// kv = RMSNorm * kv_norm -> RoPE -> fp8 -> ring + window selection (as csa_kv_finish), and
+// w^I = bf16 * wscale.  Hi may be 0.
+struct XFinishArgs {
+  const float *part;
+  int S, ldp, q_rank, hd, Hi;
+  const float *q_norm, *kv_norm;
+  float eps;
+  bf16 *qr, *kv;
+  int B, T, start_pos, rd;
+  const float *tab;
+  bf16 *ring;
+  int W;
+  int32_t *win_idx;
+  int idx_stride;
+  uint8_t *codes;
+  int8_t *scales;
+  float wscale;
+  float *wI;
+};
+cudaError_t launch_x_finish(const XFinishArgs &a, cudaStream_t s);
 
 cudaError_t launch_index_scores(const bf16 *qI, const float *wI, const bf16 *KI, int B, int T, int start_pos, int Hi,
                                 int dI, int Lstride, int compress_len, int ratio, const uint8_t *cand, int cand_width,

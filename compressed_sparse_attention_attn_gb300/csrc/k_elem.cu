@@ -149,15 +149,14 @@ cudaError_t launch_act_quant(bf16 *x, int64_t n, uint8_t *codes, int8_t *scale_e
 // last rd, then FP8), plus the ring update and window selection ("deepseek_v41_ref::attn"
 // WindowCache, window_topk_idxs).  One CTA of hd threads per token row; warp w owns fp8 block w.
 // ---------------------------------------------------------------------------------------------
-__global__ void k_kv_finish(const bf16 *kv_in, bf16 *kv_out, int T, int start_pos, int hd,
-                            int rd, const float *__restrict__ tab, bf16 *__restrict__ ring, int W,
-                            int32_t *__restrict__ win_idx, int idx_stride, uint8_t *__restrict__ codes,
-                            int8_t *__restrict__ scales) {
-  const int64_t row = blockIdx.x;  // b * T + t
-  const int b = (int)(row / T), t = (int)(row % T);
-  const int i = threadIdx.x;
+// Element i of window row `row` (b, t): v is the normed bf16 value.  Called by every thread of
+// whole warps (the pair partner and the fp8 block come from lane shuffles).
+__device__ __forceinline__ void kv_row_finish(float v, int64_t row, int b, int t, int i, int T, int start_pos,
+                                              int hd, int rd, const float *__restrict__ tab, bf16 *kv_out,
+                                              bf16 *__restrict__ ring, int W, int32_t *__restrict__ win_idx,
+                                              int idx_stride, uint8_t *__restrict__ codes,
+                                              int8_t *__restrict__ scales, int nthreads) {
   const int p = start_pos + t;
-  float v = __bfloat162float(kv_in[row * hd + i]);
   const int tail = hd - rd;
   // RoPE: lanes (2k, 2k+1) hold one complex number; each lane produces its own component.
   const float partner = __shfl_xor_sync(0xffffffffu, v, 1);
@@ -183,7 +182,7 @@ __global__ void k_kv_finish(const bf16 *kv_in, bf16 *kv_out, int T, int start_po
   // window selection
   if (win_idx) {
     int32_t *wi = win_idx + row * idx_stride;
-    for (int k = i; k < W; k += blockDim.x) {
+    for (int k = i; k < W; k += nthreads) {
       const int pk = p - W + 1 + k;
       if (start_pos == 0)
         wi[k] = pk >= 0 ? pk : -1;  // the chunk's own rows
@@ -191,6 +190,85 @@ __global__ void k_kv_finish(const bf16 *kv_in, bf16 *kv_out, int T, int start_po
         wi[k] = pk >= 0 ? (p + 1 + k) % W : -1;  // ring slots, oldest first
     }
   }
+}
+
+__global__ void k_kv_finish(const bf16 *kv_in, bf16 *kv_out, int T, int start_pos, int hd, int rd,
+                            const float *__restrict__ tab, bf16 *__restrict__ ring, int W,
+                            int32_t *__restrict__ win_idx, int idx_stride, uint8_t *__restrict__ codes,
+                            int8_t *__restrict__ scales) {
+  const int64_t row = blockIdx.x;  // b * T + t
+  const int b = (int)(row / T), t = (int)(row % T);
+  const int i = threadIdx.x;
+  const float v = __bfloat162float(kv_in[row * hd + i]);
+  kv_row_finish(v, row, b, t, i, T, start_pos, hd, rd, tab, kv_out, ring, W, win_idx, idx_stride, codes, scales,
+                blockDim.x);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Split-K reduction of [wq_a | wkv | weights_proj] x fused with everything that consumes it:
+// qr = RMSNorm(sum) * q_norm, the window row (RMSNorm * kv_norm, RoPE, fp8, ring, selection), and
+// w^I = bf16(sum) * wscale.  One CTA per token, blockDim >= hd, a multiple of 32.
+// ---------------------------------------------------------------------------------------------
+__global__ void k_x_finish(XFinishArgs a) {
+  extern __shared__ float xs[];  // [ldp] the token's projections, rounded to bf16
+  __shared__ float red[2][32];
+  const int64_t row = blockIdx.x;
+  const int b = (int)(row / a.T), t = (int)(row % a.T);
+  const int M = a.B * a.T;
+  const int n = a.q_rank + a.hd + a.Hi;
+  float sq = 0.f, skv = 0.f;
+  for (int c = threadIdx.x; c < n; c += blockDim.x) {
+    float v = 0.f;
+    for (int s = 0; s < a.S; ++s) v += a.part[((int64_t)s * M + row) * a.ldp + c];
+    v = __bfloat162float(__float2bfloat16_rn(v));  // linear_bf16 rounds the projection to bf16
+    xs[c] = v;
+    if (c < a.q_rank)
+      sq = fmaf(v, v, sq);
+    else if (c < a.q_rank + a.hd)
+      skv = fmaf(v, v, skv);
+  }
+  sq = warp_sum(sq);
+  skv = warp_sum(skv);
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  if (lane == 0) {
+    red[0][wid] = sq;
+    red[1][wid] = skv;
+  }
+  __syncthreads();
+  if (wid == 0) {
+    float x0 = lane < nw ? red[0][lane] : 0.f, x1 = lane < nw ? red[1][lane] : 0.f;
+    x0 = warp_sum(x0);
+    x1 = warp_sum(x1);
+    if (lane == 0) {
+      red[0][0] = x0;
+      red[1][0] = x1;
+    }
+  }
+  __syncthreads();
+  const float rq = 1.0f / sqrtf(red[0][0] / (float)a.q_rank + a.eps);
+  const float rkv = 1.0f / sqrtf(red[1][0] / (float)a.hd + a.eps);
+  for (int c = threadIdx.x; c < a.q_rank; c += blockDim.x)
+    a.qr[row * a.q_rank + c] = __float2bfloat16_rn(xs[c] * rq * a.q_norm[c]);
+  for (int h = threadIdx.x; h < a.Hi; h += blockDim.x) a.wI[row * a.Hi + h] = xs[a.q_rank + a.hd + h] * a.wscale;
+  if (threadIdx.x < a.hd) {
+    const int i = threadIdx.x;
+    const float v = __bfloat162float(__float2bfloat16_rn(xs[a.q_rank + i] * rkv * a.kv_norm[i]));
+    kv_row_finish(v, row, b, t, i, a.T, a.start_pos, a.hd, a.rd, a.tab, a.kv, a.ring, a.W, a.win_idx, a.idx_stride,
+                  a.codes, a.scales, a.hd);
+  }
+}
+
+cudaError_t launch_x_finish(const XFinishArgs &a, cudaStream_t s) {
+  const int M = a.B * a.T;
+  if (M <= 0) return cudaSuccess;
+  const int threads = a.hd > 256 ? a.hd : 256;
+  const size_t smem = sizeof(float) * (size_t)(a.q_rank + a.hd + a.Hi);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(k_x_finish, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  k_x_finish<<<M, threads, smem, s>>>(a);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_kv_finish(const bf16 *kv_in, bf16 *kv_out, int B, int T, int start_pos, int hd, int rd,

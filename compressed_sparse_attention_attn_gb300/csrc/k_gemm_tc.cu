@@ -29,7 +29,11 @@ namespace gemm {
 
 constexpr int kMaxProblems = 4;
 constexpr int BM = 128;
-constexpr int BK = 64;
+constexpr int BK = 64;  // one 128-byte swizzle atom of K
+#ifndef CSA_GEMM_ATOMS
+#define CSA_GEMM_ATOMS 1
+#endif
+constexpr int ATOMS = CSA_GEMM_ATOMS;  // k-slices per pipeline stage: ATOMS * 128 contiguous bytes per weight row
 constexpr int kThreads = 192;
 constexpr int kCounterInts = 65536;            // arrival counters at the head of the workspace
 constexpr size_t kCounterBytes = kCounterInts * sizeof(int);
@@ -40,11 +44,14 @@ struct Problem {
   CUtensorMap tmB;  // x [M rows][groups*Kg] bf16, box {64, BN}
   bf16 *y;
   int ldy, N, M, groups, Kg, kblocks, tiles_n, tiles_m, tiles, unit_begin, tile_begin;
+  float *part;  // split-K mode
+  int ldp;
 };
 
 struct Params {
   Problem prob[kMaxProblems];
   int nprob, total_units, total_tiles, BN, stages;
+  int split_S;  // > 0: split-K mode, CTA c = (tile c / S, k-range c % S), partials out, no fixup
   float *partials;  // [grid][2][BM][BN]
   int *counters;    // [total_tiles]
   int *status;
@@ -69,7 +76,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemm_tc(const __grid_constant__
   const uint32_t raw = tc::smem_u32(smem_raw);
   uint8_t *smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
   const int S = P.stages, BN = P.BN;
-  const uint32_t a_bytes = BM * BK * 2, b_bytes = (uint32_t)BN * BK * 2, stage_bytes = a_bytes + b_bytes;
+  const uint32_t a_atom = BM * BK * 2, b_atom = (uint32_t)BN * BK * 2;
+  const uint32_t a_bytes = ATOMS * a_atom, b_bytes = ATOMS * b_atom, stage_bytes = a_bytes + b_bytes;
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + S * stage_bytes);
   uint64_t *empty = full + S;
   uint64_t *accf = empty + S;  // [2]
@@ -83,7 +91,18 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemm_tc(const __grid_constant__
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t U = P.total_units, G = gridDim.x;
-  const int u0 = (int)cta_start(blockIdx.x, U, G), u1 = (int)cta_start(blockIdx.x + 1, U, G);
+  int u0, u1;
+  if (P.split_S > 0) {
+    const int tg = blockIdx.x / P.split_S, sp = blockIdx.x % P.split_S;
+    int p = 0;
+    while (p + 1 < P.nprob && tg >= P.prob[p + 1].tile_begin) ++p;
+    const int kps = P.prob[p].kblocks / P.split_S;
+    u0 = P.prob[p].unit_begin + (tg - P.prob[p].tile_begin) * P.prob[p].kblocks + sp * kps;
+    u1 = u0 + kps;
+  } else {
+    u0 = (int)cta_start(blockIdx.x, U, G);
+    u1 = (int)cta_start(blockIdx.x + 1, U, G);
+  }
   if (u0 >= u1) return;
   const uint32_t tmem_cols = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128 : (2 * BN <= 256) ? 256 : 512;
 
@@ -128,8 +147,12 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemm_tc(const __grid_constant__
         if (!tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag)) break;
         uint8_t *sa = smem + stage * stage_bytes;
         tc::mbar_expect_tx(&full[stage], stage_bytes);
-        tc::tma_load_2d(sa, &pr.tmA, &full[stage], un.kb * BK, g * pr.N + tn * BM, pol_w);
-        tc::tma_load_2d(sa + a_bytes, &pr.tmB, &full[stage], g * pr.Kg + un.kb * BK, tm * BN, pol_x);
+#pragma unroll
+        for (int a = 0; a < ATOMS; ++a) {
+          const int k0 = (un.kb * ATOMS + a) * BK;
+          tc::tma_load_2d(sa + a * a_atom, &pr.tmA, &full[stage], k0, g * pr.N + tn * BM, pol_w);
+          tc::tma_load_2d(sa + a_bytes + a * b_atom, &pr.tmB, &full[stage], g * pr.Kg + k0, tm * BN, pol_x);
+        }
         ++issued;
         if (++stage == S) {
           stage = 0;
@@ -170,10 +193,14 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemm_tc(const __grid_constant__
           }
           tc::tc_fence_after();
           const uint32_t sa = tc::smem_u32(smem + stage * stage_bytes);
-          const uint64_t ad = tc::sdesc_sw128(sa, 16, 1024), bd = tc::sdesc_sw128(sa + a_bytes, 16, 1024);
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k)
-            tc::mma_bf16(d, ad + 2ull * k, bd + 2ull * k, idesc, (first && k == 0) ? 0u : 1u);
+          for (int a = 0; a < ATOMS; ++a) {
+            const uint64_t ad = tc::sdesc_sw128(sa + a * a_atom, 16, 1024);
+            const uint64_t bd = tc::sdesc_sw128(sa + a_bytes + a * b_atom, 16, 1024);
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k)
+              tc::mma_bf16(d, ad + 2ull * k, bd + 2ull * k, idesc, (first && a == 0 && k == 0) ? 0u : 1u);
+          }
           first = false;
           tc::mma_commit(&empty[stage]);
           if (++stage == S) {
@@ -222,6 +249,29 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemm_tc(const __grid_constant__
       if (!tc::mbar_wait(&accf[buf], (uint32_t)(done[buf] & 1), abort_flag)) break;
       tc::tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(buf * BN);
+      if (P.split_S > 0) {
+        // split-K: this CTA's partial sum for (tile, k-range) as f32, coalesced over features
+        const int sp = blockIdx.x % P.split_S;
+        float *pcol = pr.part + (int64_t)g * pr.N + f;
+        for (int c0 = 0; c0 < BN; c0 += 16) {
+          uint32_t r[16];
+          tc::tmem_ld16(taddr + (uint32_t)c0, r);
+          tc::tmem_ld_wait();
+          if (f_ok) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int j = tm * BN + c0 + i;
+              if (j < pr.M) pcol[((int64_t)sp * pr.M + j) * pr.ldp] = __uint_as_float(r[i]);
+            }
+          }
+        }
+        tc::tc_fence_before();
+        tc::mbar_arrive(&acce[buf]);
+        ++done[buf];
+        buf ^= 1;
+        u = seg_end;
+        continue;
+      }
       const int slot = (int)blockIdx.x * 2 + (gtile == first_tile_global ? 0 : 1);
       float *mine = P.partials + (size_t)slot * BM * BN + (size_t)row * BN;
       for (int c0 = 0; c0 < BN; c0 += 16) {
@@ -370,11 +420,12 @@ cudaError_t launch_gemm_tc(const LinearProblem *probs, int nprob, float *ws, siz
   Params P;
   memset(&P, 0, sizeof(P));
   P.BN = gemm_tc_bn(M);
-  const int stage_bytes = BM * BK * 2 + P.BN * BK * 2;
+  const int stage_bytes = ATOMS * (BM * BK * 2 + P.BN * BK * 2);
   // one CTA per SM: two per SM (five stages each) measured slower at decode, because twice the CTAs
   // split each tile's k-range twice as often and the Stream-K fixups dominate
   const int per_sm = 1;
   P.stages = per_sm == 2 ? std::min(5, (100 * 1024) / stage_bytes) : std::min(8, (200 * 1024) / stage_bytes);
+  if (P.stages < 2) return cudaErrorInvalidValue;
   int units = 0, tiles = 0;
   for (int i = 0; i < nprob; ++i) {
     const LinearProblem &q = probs[i];
@@ -389,7 +440,7 @@ cudaError_t launch_gemm_tc(const LinearProblem *probs, int nprob, float *ws, siz
     p.M = M;
     p.groups = q.groups;
     p.Kg = q.K;
-    p.kblocks = (q.K + BK - 1) / BK;
+    p.kblocks = (q.K + BK * ATOMS - 1) / (BK * ATOMS);
     p.tiles_n = (q.N + BM - 1) / BM;
     p.tiles_m = (M + P.BN - 1) / P.BN;
     p.tiles = p.tiles_n * p.tiles_m * q.groups;
@@ -401,6 +452,7 @@ cudaError_t launch_gemm_tc(const LinearProblem *probs, int nprob, float *ws, siz
   P.nprob = nprob;
   P.total_units = units;
   P.total_tiles = tiles;
+  P.split_S = 0;
   if (tiles > kCounterInts) return cudaErrorInvalidValue;
   const size_t part_per_cta = (size_t)2 * BM * P.BN * sizeof(float);
   if (ws_bytes < kCounterBytes + part_per_cta) return cudaErrorInvalidValue;
@@ -420,12 +472,77 @@ cudaError_t launch_gemm_tc(const LinearProblem *probs, int nprob, float *ws, siz
   return cudaGetLastError();
 }
 
+int gemm_tc_split_count(const LinearProblem *probs, int nprob, int max_ctas, int max_S) {
+  using namespace gemm;
+  const int BN = gemm_tc_bn(probs[0].M);
+  int tiles = 0;
+  for (int i = 0; i < nprob; ++i)
+    tiles += ((probs[i].N + BM - 1) / BM) * ((probs[i].M + BN - 1) / BN) * probs[i].groups;
+  const int kblocks = (probs[0].K + BK * ATOMS - 1) / (BK * ATOMS);
+  int best = 1;
+  for (int s = 1; s <= kblocks && s <= max_S; ++s)
+    if (kblocks % s == 0 && (int64_t)tiles * s <= max_ctas) best = s;
+  return best;
+}
+
+cudaError_t launch_gemm_tc_split(const LinearProblem *probs, int nprob, int S, int *status, cudaStream_t s) {
+  using namespace gemm;
+  if (nprob <= 0 || nprob > kMaxProblems || S <= 0) return cudaErrorInvalidValue;
+  const int M = probs[0].M, K = probs[0].K;
+  Params P;
+  memset(&P, 0, sizeof(P));
+  P.BN = gemm_tc_bn(M);
+  const int stage_bytes = ATOMS * (BM * BK * 2 + P.BN * BK * 2);
+  P.stages = std::min(8, (200 * 1024) / stage_bytes);
+  if (P.stages < 2) return cudaErrorInvalidValue;
+  int units = 0, tiles = 0;
+  for (int i = 0; i < nprob; ++i) {
+    const LinearProblem &q = probs[i];
+    if (q.M != M || q.K != K || !q.part) return cudaErrorInvalidValue;
+    Problem &p = P.prob[i];
+    if (!map_2d(&p.tmA, q.W, (uint64_t)q.K, (uint64_t)q.N * q.groups, (uint64_t)q.ldw, BK, BM)) return cudaErrorInvalidValue;
+    if (!map_2d(&p.tmB, q.x, (uint64_t)q.K * q.groups, (uint64_t)M, (uint64_t)q.ldx, BK, (uint32_t)P.BN))
+      return cudaErrorInvalidValue;
+    p.y = q.y;
+    p.part = q.part;
+    p.ldp = q.ldp;
+    p.ldy = q.ldy;
+    p.N = q.N;
+    p.M = M;
+    p.groups = q.groups;
+    p.Kg = q.K;
+    p.kblocks = (q.K + BK * ATOMS - 1) / (BK * ATOMS);
+    if (p.kblocks % S) return cudaErrorInvalidValue;
+    p.tiles_n = (q.N + BM - 1) / BM;
+    p.tiles_m = (M + P.BN - 1) / P.BN;
+    p.tiles = p.tiles_n * p.tiles_m * q.groups;
+    p.unit_begin = units;
+    p.tile_begin = tiles;
+    units += p.tiles * p.kblocks;
+    tiles += p.tiles;
+  }
+  P.nprob = nprob;
+  P.total_units = units;
+  P.total_tiles = tiles;
+  P.split_S = S;
+  P.status = status;
+  const size_t smem = 1024 + (size_t)P.stages * stage_bytes + 256 + kMaxContrib * sizeof(int);
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  k_gemm_tc<<<tiles * S, kThreads, smem, s>>>(P);
+  return cudaGetLastError();
+}
+
 // Whether the tensor-core path takes a problem: TMA needs 16-byte aligned bases and row strides;
 // grouped products need each group's K to be whole 64-wide slices.
 bool gemm_tc_supported(const LinearProblem &q) {
   if (((uintptr_t)q.x & 15) || ((uintptr_t)q.W & 15)) return false;
   if (q.ldx % 8 || q.ldw % 8 || q.K % 8) return false;
-  if (q.groups > 1 && q.K % gemm::BK) return false;
+  if (q.groups > 1 && q.K % (gemm::BK * gemm::ATOMS)) return false;
   if (q.M <= 0 || q.N <= 0 || q.K <= 0) return false;
   return gemm::encoder() != nullptr;
 }
