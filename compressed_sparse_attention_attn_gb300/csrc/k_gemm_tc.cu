@@ -405,6 +405,11 @@ bool map_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, ui
 
 }  // namespace gemm
 
+bool tma_map_2d_bf16(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint64_t ld, uint32_t box_inner,
+                     uint32_t box_outer) {
+  return gemm::map_2d(m, base, inner, outer, ld, box_inner, box_outer);
+}
+
 int gemm_tc_bn(int M) {
   if (M > 256) return 256;
   int bn = (M + 15) / 16 * 16;
