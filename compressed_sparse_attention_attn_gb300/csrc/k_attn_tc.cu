@@ -37,7 +37,7 @@ constexpr int HD = 512;              // head_dim this kernel serves
 constexpr int KB = HD / 64;          // 64-feature K-blocks = ring slots
 constexpr int TILE = 128;            // rows per tile
 constexpr int kThreads = 288;
-constexpr int kMaxTiles = 5;         // selections up to 640 valid rows (+ 3 rows of source padding)
+constexpr int kMaxTiles = 6;         // selections up to 765 valid rows (+ 3 rows of source padding)
 constexpr int kMaxEntries = kMaxTiles * TILE;
 constexpr int kSlotBytes = TILE * 128;
 

@@ -204,7 +204,9 @@ def test_index_topk_bit_exact(csa, orc, B, T, start, L, clen, ratio, keep, cb, K
 # ---------------------------------------------------------------------------------- attention
 
 @pytest.mark.parametrize("H,hd,na,nb,a_len,b_len,B,T", [(4, 64, 8, 16, 12, 40, 1, 12), (64, 512, 128, 512, 128, 500, 3, 1),
-                                                        (64, 512, 128, 512, 300, 1024, 1, 9)])
+                                                        (64, 512, 128, 512, 300, 1024, 1, 9),
+                                                        (64, 512, 128, 512, 128, 700, 80, 1),
+                                                        (64, 512, 7, 300, 7, 64, 2, 5)])
 def test_sparse_attn(csa, orc, H, hd, na, nb, a_len, b_len, B, T):
     rng = np.random.default_rng(8 + H)
     q = _rng_bf16(orc, rng, (B * T, H, hd))
