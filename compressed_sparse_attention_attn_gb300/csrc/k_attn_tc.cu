@@ -4,9 +4,10 @@
 //
 // One CTA per (query, group of HG heads).  All heads of a query share one K = V row per selected
 // position.  Y = [rows_a; rows_b] and J = [idx_a; idx_b] are never materialised: the valid entries
-// of both index lists are compacted per source, and TMA tile::gather4 loads fetch four selected rows
-// of one source per instruction, 64 features (one 128-byte swizzle row) at a time, into a ring of
-// eight 16 KiB K-block slots (slot kb holds features [64 kb, 64 kb + 64) of a 128-row tile).
+// of both index lists are compacted per source, and the four loader warps copy the selected rows
+// (cp.async, 16 lanes per 256-byte row segment, so each warp instruction reads two whole segments)
+// into a ring of eight 16 KiB K-block slots in the 128-byte swizzled layout (slot kb holds features
+// [64 kb, 64 kb + 64) of a 128-row tile; loader warp w owns slots 2w and 2w + 1).
 //
 //   pass 1  S^T_k[r][h] = sum_d G_k[r][d] q[h][d]   for every tile k (M = 128 rows, N = HG, K = 512),
 //           each tile's scores in their own TMEM columns;
@@ -20,8 +21,8 @@
 //           bf16 value at the query's position.
 //
 // Warps 0-3: softmax and epilogue (TMEM lane quadrant = warp); warps 4-7: compaction of the index
-// lists, warp 4 lane 0 then issues every TMA load; warp 8: TMEM allocation and MMA issue.  Every
-// mbarrier wait is time-bounded.
+// lists, then the row copies (warp 4 lane 0 also loads q by TMA); warp 8: TMEM allocation and MMA
+// issue.  Every mbarrier wait is time-bounded.
 #include "csa_internal.cuh"
 #include "tc_ptx.cuh"
 
@@ -37,14 +38,13 @@ constexpr int HD = 512;              // head_dim this kernel serves
 constexpr int KB = HD / 64;          // 64-feature K-blocks = ring slots
 constexpr int TILE = 128;            // rows per tile
 constexpr int kThreads = 288;
-constexpr int kMaxTiles = 6;         // selections up to 765 valid rows (+ 3 rows of source padding)
+constexpr int kMaxTiles = 6;         // selections up to 768 rows
 constexpr int kMaxEntries = kMaxTiles * TILE;
 constexpr int kSlotBytes = TILE * 128;
 
 struct Params {
   CUtensorMap tm_q;  // q [NT*H][512], box {64, HG}
-  CUtensorMap tm_a;  // rows_a [B*a_seq_rows][512], box {64, 1}
-  CUtensorMap tm_b;  // rows_b [B*b_seq_rows][512], box {64, 1}
+  const bf16 *rows_a, *rows_b;
   int T, H;
   int64_t a_seq_rows, b_seq_rows;
   int a_len, b_len;
@@ -60,14 +60,10 @@ struct Params {
   int *status;
 };
 
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap *tm, uint64_t *bar, int col, int r0, int r1,
-                                            int r2, int r3) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
-      "l"((uint64_t)tm), "r"(tc::smem_u32(bar)), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
-      : "memory");
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0) : "memory");
 }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 __device__ __forceinline__ void tma_load_2d_nohint(uint32_t dst, const CUtensorMap *tm, uint64_t *bar, int c0, int c1) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
@@ -93,13 +89,13 @@ struct Smem {
   static constexpr size_t slots = 0;                                      // KB x 16 KiB
   static constexpr size_t q = slots + (size_t)KB * kSlotBytes;              // KB x HG x 128
   static constexpr size_t p = q + (size_t)KB * HG * 128;                    // kMaxTiles x 2 x HG x 128
-  static constexpr size_t list = p + (size_t)kMaxTiles * 2 * HG * 128;      // int32 [kMaxEntries]
-  static constexpr size_t valid = list + (size_t)kMaxEntries * 4;          // uint8 [kMaxEntries]
+  static constexpr size_t list = p + (size_t)kMaxTiles * 2 * HG * 128;      // int32 [2][kMaxEntries] (A, B)
+  static constexpr size_t valid = list + (size_t)2 * kMaxEntries * 4;      // uint8 [kMaxEntries]
   static constexpr size_t red = valid + (size_t)kMaxEntries;              // float [2][4][HG]
   static constexpr size_t stat = red + (size_t)2 * 4 * HG * 4;            // float m[HG], l[HG]
   static constexpr size_t bars = (stat + (size_t)2 * HG * 4 + 7) / 8 * 8;  // u64 [2*KB + 6]
   static constexpr size_t misc = bars + (size_t)(2 * KB + 6) * 8;         // tmem slot, flags, counts
-  static constexpr size_t total = misc + 64;
+  static constexpr size_t total = misc + 128;
 };
 
 template <int HG>
@@ -111,7 +107,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
   const uint32_t s_slots = tc::smem_u32(smem + L::slots), s_q = tc::smem_u32(smem + L::q),
                  s_p = tc::smem_u32(smem + L::p);
   uint8_t *sP = smem + L::p;
-  int32_t *list = reinterpret_cast<int32_t *>(smem + L::list);
+  int32_t *listA = reinterpret_cast<int32_t *>(smem + L::list), *listB = listA + kMaxEntries;
   uint8_t *valid = smem + L::valid;
   float *red_max = reinterpret_cast<float *>(smem + L::red), *red_sum = red_max + 4 * HG;
   float *m_sm = reinterpret_cast<float *>(smem + L::stat), *l_sm = m_sm + HG;
@@ -120,8 +116,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
            *p_full = q_full + 2, *o_done = q_full + 3, *sm_bar = q_full + 4, *drain = q_full + 5;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::misc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-  int *s_cnt = const_cast<int *>(abort_flag) + 1;  // [4] per loader warp
-  int *s_nA = s_cnt + 4, *s_nB = s_nA + 1;
+  int *s_cnt = const_cast<int *>(abort_flag) + 1;  // [2 buffers][2 sources][4 loader warps]
+  int *s_nA = s_cnt + 16, *s_nB = s_nA + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = blockIdx.y;  // query b*T + t
@@ -131,7 +127,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < KB; ++i) {
-      tc::mbar_init(&slot_full[i], 1);
+      tc::mbar_init(&slot_full[i], 32);  // the lanes of the loader warp that owns the slot
       tc::mbar_init(&slot_empty[i], 1);
     }
     tc::mbar_init(q_full, 1);
@@ -146,9 +142,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
   if (warp == 8) tc::tmem_alloc(tmem_slot, kCols);
   __syncthreads();
 
-  // ---- compaction (warps 4-7): valid entries of [idx_a; idx_b], rows of rows_a first (padded to a
-  //      multiple of 4 so a gather4 never mixes sources), then rows of rows_b; the rest of the last
-  //      tile is padding (a real row of the source, masked out of the softmax)
+  // ---- compaction (warps 4-7): the valid entries of [idx_a; idx_b] in order, split by source (rows
+  //      of rows_a in listA, of rows_b in listB); one block-wide count per 128 entries
   const int n_all = P.na + P.nb;
   const int n_rows = P.a_len + P.b_len;
   if (warp >= 4 && warp < 8) {
@@ -159,98 +154,95 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
     for (int i = 0; i < kPer; ++i) {  // every index of this query, loaded up front
       const int e = i * 128 + j;
       v[i] = e < P.na ? P.idx_a[row * P.na + e] : (e < n_all ? P.idx_b[row * P.nb + (e - P.na)] : -1);
-      if (e < n_all && (v[i] < -1 || v[i] >= n_rows)) atomicOr(P.status, kStatusBadIndex);
     }
-    int base = 0, nA = 0;
-    for (int pass = 0; pass < 2; ++pass) {
+    int baseA = 0, baseB = 0;
 #pragma unroll
-      for (int i = 0; i < kPer; ++i) {
-        const int e = i * 128 + j;
-        const bool in = e < n_all && v[i] >= 0 && v[i] < n_rows && ((v[i] < P.a_len) == (pass == 0));
-        const unsigned bal = __ballot_sync(0xffffffffu, in);
-        if (lane == 0) s_cnt[lw] = __popc(bal);
-        tc::named_bar(2, 128);
-        int before = base;
-        for (int w = 0; w < lw; ++w) before += s_cnt[w];
-        before += __popc(bal & ((1u << lane) - 1u));
-        if (in && before < kMaxEntries) {
-          list[before] =
-              pass == 0 ? (int32_t)(b * P.a_seq_rows + v[i]) : (int32_t)(b * P.b_seq_rows + (v[i] - P.a_len));
-          valid[before] = 1;
-        }
-        base += s_cnt[0] + s_cnt[1] + s_cnt[2] + s_cnt[3];
-        tc::named_bar(2, 128);
+    for (int i = 0; i < kPer; ++i) {
+      const int e = i * 128 + j;
+      if (e < n_all && (v[i] < -1 || v[i] >= n_rows)) atomicOr(P.status, kStatusBadIndex);
+      const bool ok = e < n_all && v[i] >= 0 && v[i] < n_rows;
+      const bool inA = ok && v[i] < P.a_len, inB = ok && v[i] >= P.a_len;
+      const unsigned balA = __ballot_sync(0xffffffffu, inA), balB = __ballot_sync(0xffffffffu, inB);
+      int *cnt = s_cnt + (i & 1) * 8;
+      if (lane == 0) {
+        cnt[lw] = __popc(balA);
+        cnt[4 + lw] = __popc(balB);
       }
-      if (pass == 0) {
-        nA = base;
-        const int nA4 = (nA + 3) & ~3;
-        if (j < nA4 - nA && nA + j < kMaxEntries) {
-          list[nA + j] = (int32_t)(b * P.a_seq_rows);
-          valid[nA + j] = 0;
-        }
-        base = nA4;
+      tc::named_bar(2, 128);
+      int bA = baseA, bB = baseB;
+      for (int w = 0; w < lw; ++w) {
+        bA += cnt[w];
+        bB += cnt[4 + w];
       }
+      const unsigned below = (1u << lane) - 1u;
+      if (inA) {
+        const int at = bA + __popc(balA & below);
+        if (at < kMaxEntries) listA[at] = (int32_t)(b * P.a_seq_rows + v[i]);
+      }
+      if (inB) {
+        const int at = bB + __popc(balB & below);
+        if (at < kMaxEntries) listB[at] = (int32_t)(b * P.b_seq_rows + (v[i] - P.a_len));
+      }
+      baseA += cnt[0] + cnt[1] + cnt[2] + cnt[3];
+      baseB += cnt[4] + cnt[5] + cnt[6] + cnt[7];
     }
-    const int total = min(base, kMaxEntries);
-    const int padded = min((total + TILE - 1) / TILE * TILE, kMaxEntries);
-    for (int e = total + j; e < padded; e += 128) {
-      list[e] = (int32_t)(P.b_len > 0 ? b * P.b_seq_rows : b * P.a_seq_rows);
-      valid[e] = 0;
-    }
+    const int nA = min(baseA, kMaxEntries), nB = min(baseB, kMaxEntries - nA);
+    const int padded = min((nA + nB + TILE - 1) / TILE * TILE, kMaxEntries);
+    for (int e = j; e < padded; e += 128) valid[e] = e < nA + nB;
     if (j == 0) {
-      *s_nA = (nA + 3) & ~3;
-      *s_nB = total - ((nA + 3) & ~3);
+      *s_nA = nA;
+      *s_nB = nB;
     }
   }
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int nA4 = *s_nA, nB = *s_nB;
-  const int ntiles = min((nA4 + nB + TILE - 1) / TILE, kMaxTiles);
+  const int nA = *s_nA, nB = *s_nB;
+  const int ntiles = min((nA + nB + TILE - 1) / TILE, kMaxTiles);
   const uint32_t tS = tmem, tO = tmem + (uint32_t)(kMaxTiles * HG);  // S_k at tS + k*HG; O^T chunk c at tO + c*HG
 
-  if (warp == 4) {
-    // ------------------------------------------------------------------ TMA producer
-    if (lane == 0 && ntiles > 0) {
+  if (warp >= 4 && warp < 8) {
+    // ------------------------------------------------------------------ loaders
+    const int w = warp - 4;
+    if (w == 0 && lane == 0 && ntiles > 0) {
       tc::prefetch_tmap(&P.tm_q);
-      tc::prefetch_tmap(&P.tm_a);
-      tc::prefetch_tmap(&P.tm_b);
       tc::mbar_expect_tx(q_full, KB * HG * 128);
 #pragma unroll 1
       for (int kb = 0; kb < KB; ++kb)
         tma_load_2d_nohint(s_q + kb * HG * 128, &P.tm_q, q_full, kb * 64, (int)(row * P.H + hg * HG));
-      // fills in order: pass 1 tiles 0..n-1, then pass 2 tiles n-2..0 (tile n-1 stays from pass 1)
-      int fill = 0;
-      const int nfills = 2 * ntiles - 1;
-      bool ok = true;
-      int last_fill[KB];  // the latest fill issued into each slot (-1: none)
-#pragma unroll
-      for (int kb = 0; kb < KB; ++kb) last_fill[kb] = -1;
-      for (int fi = 0; fi < nfills && ok; ++fi) {
-        const int k = fi < ntiles ? fi : 2 * ntiles - 2 - fi;
-        for (int kb = 0; kb < KB; ++kb) {
-          if (!(ok = tc::mbar_wait(&slot_empty[kb], (uint32_t)(fill & 1) ^ 1u, abort_flag))) break;
-          tc::mbar_expect_tx(&slot_full[kb], kSlotBytes);
-          last_fill[kb] = fill;
-          const uint32_t dst = s_slots + kb * kSlotBytes;
-#pragma unroll 1
-          for (int g = 0; g < TILE / 4; ++g) {
-            const int e = k * TILE + 4 * g;
-            const CUtensorMap *tm = e < nA4 ? &P.tm_a : &P.tm_b;
-            tma_gather4(dst + g * 512, tm, &slot_full[kb], kb * 64, list[e], list[e + 1], list[e + 2], list[e + 3]);
-          }
-        }
-        if (ok) ++fill;
+    }
+    // fills in order: pass 1 tiles 0..n-1, then pass 2 tiles n-2..0 (tile n-1 stays from pass 1).
+    // This warp writes features [128 w, 128 w + 128) = slots 2w, 2w+1 of every row of the tile:
+    // lanes 0-15 one row, lanes 16-31 the next, 16 bytes each.
+    const int half = lane >> 4, sub = lane & 15;
+    const int kb = 2 * w + (sub >> 3), cc = sub & 7;
+    const uint32_t slot_base = s_slots + kb * kSlotBytes;
+    int fill = 0;
+    bool ok = true;
+    const int nfills = ntiles > 0 ? 2 * ntiles - 1 : 0;
+    for (int fi = 0; fi < nfills && ok; ++fi) {
+      const int k = fi < ntiles ? fi : 2 * ntiles - 2 - fi;
+      const uint32_t par = (uint32_t)(fill & 1) ^ 1u;
+      if (!(ok = tc::mbar_wait(&slot_empty[2 * w], par, abort_flag) &&
+                 tc::mbar_wait(&slot_empty[2 * w + 1], par, abort_flag)))
+        break;
+#pragma unroll 4
+      for (int i = 0; i < TILE / 2; ++i) {
+        const int r = 2 * i + half, e = k * TILE + r;
+        const bool vr = e < nA + nB;
+        const bf16 *src = P.rows_a;
+        if (vr) src = e < nA ? P.rows_a + (int64_t)listA[e] * HD : P.rows_b + (int64_t)listB[e - nA] * HD;
+        cp_async16(slot_base + r * 128 + ((cc ^ (r & 7)) << 4), src + (vr ? 128 * w + 8 * sub : 0), vr);
       }
-      // every copy issued has landed before the CTA can exit: each slot's latest fill completes
-      for (int kb = 0; kb < KB; ++kb) {
-        if (last_fill[kb] < 0) continue;
-        const uint32_t par = (uint32_t)(last_fill[kb] & 1);
-        const uint64_t t0 = tc::global_ns();
-        while (!tc::mbar_try_wait(&slot_full[kb], par) && tc::global_ns() - t0 < tc::kWaitLimitNs) {
-        }
-      }
+      cp_async_wait_all();
+      fence_proxy_async();
+      tc::mbar_arrive(&slot_full[2 * w]);
+      tc::mbar_arrive(&slot_full[2 * w + 1]);
+      ++fill;
+    }
+    cp_async_wait_all();
+    if (w == 0 && lane == 0 && ntiles > 0) {  // the q copies have landed before the CTA can exit
       const uint64_t t0 = tc::global_ns();
       while (!tc::mbar_try_wait(q_full, 0) && tc::global_ns() - t0 < tc::kWaitLimitNs) {
       }
@@ -453,8 +445,8 @@ cudaError_t launch_hg(const Params &p, int nq, cudaStream_t s) {
 }  // namespace attn
 
 bool sparse_attn_tc_supported(const AttnArgs &a) {
-  // every selection must fit kMaxTiles tiles: at most na + nb valid rows plus 3 of source padding
-  return a.hd == attn::HD && a.H % 16 == 0 && a.na + a.nb + 3 <= attn::kMaxEntries && a.a_seq_stride % attn::HD == 0 &&
+  // every selection must fit kMaxTiles tiles of rows
+  return a.hd == attn::HD && a.H % 16 == 0 && a.na + a.nb <= attn::kMaxEntries && a.a_seq_stride % attn::HD == 0 &&
          (a.rows_b == nullptr || a.b_seq_stride % attn::HD == 0) && (a.o_rot == nullptr || a.rd % 2 == 0) &&
          ((uintptr_t)a.q & 15) == 0 && ((uintptr_t)a.rows_a & 15) == 0 && ((uintptr_t)a.rows_b & 15) == 0;
 }
@@ -467,21 +459,11 @@ cudaError_t launch_sparse_attn_tc(const AttnArgs &a, int num_sms, cudaStream_t s
   memset(&p, 0, sizeof(p));
   // heads per CTA: 32 once that still gives about one CTA per SM, else 16
   const int HG = ((int64_t)nq * (a.H / 32) >= num_sms && a.H % 32 == 0) ? 32 : 16;
-  const int64_t a_rows = (int64_t)a.B * (a.a_seq_stride / HD);
   if (!tma_map_2d_bf16(&p.tm_q, a.q, HD, (uint64_t)nq * a.H, HD, 64, (uint32_t)HG)) return cudaErrorInvalidValue;
-  if (!tma_map_2d_bf16(&p.tm_a, a.rows_a, HD, (uint64_t)std::max<int64_t>(a_rows, 1), HD, 64, 1))
-    return cudaErrorInvalidValue;
-  if (a.rows_b) {
-    const int64_t b_rows = (int64_t)a.B * (a.b_seq_stride / HD);
-    if (!tma_map_2d_bf16(&p.tm_b, a.rows_b, HD, (uint64_t)std::max<int64_t>(b_rows, 1), HD, 64, 1))
-      return cudaErrorInvalidValue;
-    p.b_seq_rows = a.b_seq_stride / HD;
-    p.b_len = a.b_len;
-  } else {
-    p.tm_b = p.tm_a;
-    p.b_seq_rows = 0;
-    p.b_len = 0;
-  }
+  p.rows_a = a.rows_a;
+  p.rows_b = a.rows_b ? a.rows_b : a.rows_a;
+  p.b_seq_rows = a.rows_b ? a.b_seq_stride / HD : 0;
+  p.b_len = a.rows_b ? a.b_len : 0;
   p.T = a.T;
   p.H = a.H;
   p.a_seq_rows = a.a_seq_stride / HD;
