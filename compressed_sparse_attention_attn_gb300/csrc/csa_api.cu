@@ -567,7 +567,9 @@ int attn_v41_forward(csa_ctx *ctx, const csa_layer_weights *w, csa_layer_state *
          "window idx");
     a.idx_a = ctx->idx_win;
   }
-  STEP(csa::launch_sparse_attn(a, ctx->ws, ctx->ws_bytes, ctx->num_sms, s), "sparse_attn");
+  int attn_kernels = 0;
+  STAGE(csa::launch_sparse_attn(a, ctx->ws, ctx->ws_bytes, ctx->num_sms, s, &attn_kernels), "sparse_attn",
+        attn_kernels);
   // grouped output: og[:, g] = o_rot[:, g*gw:(g+1)*gw] wo_a[g]^T, then out = og wo_b^T
   {
     csa::LinearProblem pa = lin(ctx->o_rot, gw, H * hd, w->wo_a, g.o_rank, og, G * g.o_rank, G);

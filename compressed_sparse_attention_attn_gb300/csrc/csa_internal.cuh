@@ -113,7 +113,11 @@ struct AttnArgs {
   const float *tab;
   int *status;
 };
-cudaError_t launch_sparse_attn(const AttnArgs &a, float *ws, size_t ws_bytes, int num_sms, cudaStream_t s);
+// Tensor-core kernel where the shapes allow (head_dim 512, heads in groups of 64), else the SIMT one.
+// ws: the tensor-core path's per-split shares (after the GEMM counters).  *kernels (if given): the
+// number of kernels launched.
+cudaError_t launch_sparse_attn(const AttnArgs &a, float *ws, size_t ws_bytes, int num_sms, cudaStream_t s,
+                               int *kernels = nullptr);
 
 // Record the calling thread's last error (attn_v41_last_error) and return `code`.
 int set_error(int code, const char *fmt, ...);

@@ -37,14 +37,22 @@ cudaError_t launch_linear(const LinearProblem *probs, int n, float *ws, size_t w
 }
 
 bool sparse_attn_tc_supported(const AttnArgs &a);
-cudaError_t launch_sparse_attn_tc(const AttnArgs &a, int num_sms, cudaStream_t s);
+cudaError_t launch_sparse_attn_tc(const AttnArgs &a, float *ws, size_t ws_bytes, int num_sms, cudaStream_t s,
+                                  int *kernels);
 
 // Tensor-core kernel for head_dim 512 (the model's); the CUDA-core kernel for other head sizes.
-cudaError_t launch_sparse_attn(const AttnArgs &a, float *ws, size_t ws_bytes, int num_sms, cudaStream_t s) {
-  (void)ws;
-  (void)ws_bytes;
-  if (sparse_attn_tc_supported(a)) return launch_sparse_attn_tc(a, num_sms, s);
-  return launch_sparse_attn_simt(a, s);
+cudaError_t launch_sparse_attn(const AttnArgs &a, float *ws, size_t ws_bytes, int num_sms, cudaStream_t s,
+                               int *kernels) {
+  int k = 0;
+  cudaError_t e;
+  if (sparse_attn_tc_supported(a)) {
+    e = launch_sparse_attn_tc(a, ws, ws_bytes, num_sms, s, &k);
+  } else {
+    e = launch_sparse_attn_simt(a, s);
+    k = a.B * a.T > 0 ? 1 : 0;
+  }
+  if (kernels) *kernels = k;
+  return e;
 }
 
 }  // namespace csa

@@ -2,27 +2,31 @@
 // ("deepseek_v41_ref::attn" sparse_attn; "DeepSeek V4.1 - Compressed sparse attention", "Sparse
 // attention" and "Grouped output"; "Join rows").
 //
-// One CTA per (query, group of HG heads).  All heads of a query share one K = V row per selected
-// position.  Y = [rows_a; rows_b] and J = [idx_a; idx_b] are never materialised: the valid entries
-// of both index lists are compacted per source, and the four loader warps copy the selected rows
-// (cp.async, 16 lanes per 256-byte row segment, so each warp instruction reads two whole segments)
-// into a ring of eight 16 KiB K-block slots in the 128-byte swizzled layout (slot kb holds features
-// [64 kb, 64 kb + 64) of a 128-row tile; loader warp w owns slots 2w and 2w + 1).
+// All heads of a query share one K = V row per selected position, so a CTA works on one query, a
+// group of 64 heads, and a range of 128-entry tiles of the query's index list J = [idx_a; idx_b]:
+// tile k covers entries 128k .. 128k+127 as they stand (an invalid entry, -1, is a masked row that
+// fetches nothing; a tile with no valid entry is skipped).  Y = [rows_a; rows_b] is never
+// materialised: the four loader warps copy each tile's rows straight from the two sources
+// (cp.async, 16 lanes per 256-byte row segment) into the 128-byte swizzled layout.  Per tile, with
+// the accumulators in TMEM:
+//   S^T[r][h] = sum_d G[r][d] q[h][d]       (M = 128 rows, N = 64 heads, K = 512; G and q K-major)
+//   softmax step: a running maximum per head, raised only when a tile's maximum exceeds it by more
+//   than 2^8 (the accumulated output and sum are then rescaled), p = exp(S - m) rounded to bf16 in
+//   shared memory (K-major [64][128]); the maxima and sums over the rows are butterfly reductions
+//   that leave each lane with two heads
+//   O^T[d][h] += sum_r G[r][d] P[h][r]      (M = 4 x 128 features, N = 64, K = 128 rows; the same tile
+//                                            read as an MN-major operand)
+// When a query's tiles are split over several CTAs (decode: few queries, so one tile per CTA keeps
+// the SMs busy), each CTA writes (m, l, O / l) for its tiles and a second, wide kernel merges the
+// shares in CTA order with the sink, which enters the denominator only:
+//   O = sum_c e^{m_c - M} O_c / (e^{sink - M} + sum_c e^{m_c - M} l_c).
+// A query held by one CTA (prefill: many queries) is finished in place.  The result is staged in
+// shared memory and written with 16-byte stores as bf16, together with the inverse rotation of its
+// last rope_dim features at the query's position.
 //
-//   pass 1  S^T_k[r][h] = sum_d G_k[r][d] q[h][d]   for every tile k (M = 128 rows, N = HG, K = 512),
-//           each tile's scores in their own TMEM columns;
-//   softmax over all tiles at once: m_h = max(sink_h, max S), p = exp(S - m) (0 for padding rows),
-//           l_h = exp(sink_h - m_h) + sum p (the sink in the denominator only), P_k bf16 in shared
-//           memory, K-major [HG][128];
-//   pass 2  O^T[d][h] += sum_r G_k[r][d] P_k[h][r]  (M = 4 x 128 features, N = HG, K = 128 rows; the
-//           slots read as MN-major operands), the last tile of pass 1 reused in place, the others
-//           gathered again (their loads overlap the softmax);
-//   epilogue O = O^T / l as bf16, and the inverse rotation of the last rope_dim features of the
-//           bf16 value at the query's position.
-//
-// Warps 0-3: softmax and epilogue (TMEM lane quadrant = warp); warps 4-7: compaction of the index
-// lists, then the row copies (warp 4 lane 0 also loads q by TMA); warp 8: TMEM allocation and MMA
-// issue.  Every mbarrier wait is time-bounded.
+// Warps 0-3: softmax and epilogue (TMEM lane quadrant = warp); warps 4-7: index pass and row
+// copies; warp 8: TMEM allocation and MMA issue; all nine warps write the result or the share.
+// Every mbarrier wait is time-bounded.
 #include "csa_internal.cuh"
 #include "tc_ptx.cuh"
 
@@ -34,16 +38,18 @@ bool tma_map_2d_bf16(CUtensorMap *m, const void *base, uint64_t inner, uint64_t 
 
 namespace attn {
 
-constexpr int HD = 512;              // head_dim this kernel serves
-constexpr int KB = HD / 64;          // 64-feature K-blocks = ring slots
-constexpr int TILE = 128;            // rows per tile
+constexpr int HD = 512;       // head_dim this kernel serves
+constexpr int KB = HD / 64;   // 64-feature K-blocks
+constexpr int TILE = 128;     // entries per tile
+constexpr int HG = 64;        // heads per CTA
 constexpr int kThreads = 288;
-constexpr int kMaxTiles = 6;         // selections up to 768 rows
-constexpr int kMaxEntries = kMaxTiles * TILE;
-constexpr int kSlotBytes = TILE * 128;
+constexpr int kMaxTiles = 6;  // index lists up to 768 entries
+constexpr int kBlockBytes = TILE * 128;  // one K-block of a tile
+constexpr int kMaxHeadGroups = 4;        // H <= 256
+constexpr int kVecs = HG * (HD / 8);     // 16-byte vectors of one head group's output
 
 struct Params {
-  CUtensorMap tm_q;  // q [NT*H][512], box {64, HG}
+  CUtensorMap tm_q;  // q [NT*H][512], box {64, 64}
   const bf16 *rows_a, *rows_b;
   int T, H;
   int64_t a_seq_rows, b_seq_rows;
@@ -58,6 +64,10 @@ struct Params {
   int rd, start_pos;
   const float *tab;
   int *status;
+  int ntiles;       // tiles of the index list
+  int tpc, nsplit;  // tiles per CTA, CTAs per query
+  bf16 *part_o;     // [NT][nsplit][H][512]  O_c / l_c of each split
+  float *part_ml;   // [NT][nsplit][H][2]    (m_c, l_c), log2 domain
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid) {
@@ -71,236 +81,310 @@ __device__ __forceinline__ void tma_load_2d_nohint(uint32_t dst, const CUtensorM
       : "memory");
 }
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-template <int HG>
+// 32 lanes x 64 consecutive columns, then the wait; the registers are operands of the wait so
+// that no use of them can be scheduled before it.
 __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[HG]) {
+  uint32_t r[64];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {"
+      "%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, "
+      "%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
+      "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63"
+      "}, [%64];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
+        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
+        "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
+        "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
+        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]),
+                 "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                 "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]),
+                 "+r"(r[32]), "+r"(r[33]), "+r"(r[34]), "+r"(r[35]), "+r"(r[36]), "+r"(r[37]), "+r"(r[38]), "+r"(r[39]),
+                 "+r"(r[40]), "+r"(r[41]), "+r"(r[42]), "+r"(r[43]), "+r"(r[44]), "+r"(r[45]), "+r"(r[46]), "+r"(r[47]),
+                 "+r"(r[48]), "+r"(r[49]), "+r"(r[50]), "+r"(r[51]), "+r"(r[52]), "+r"(r[53]), "+r"(r[54]), "+r"(r[55]),
+                 "+r"(r[56]), "+r"(r[57]), "+r"(r[58]), "+r"(r[59]), "+r"(r[60]), "+r"(r[61]), "+r"(r[62]), "+r"(r[63])
+               :
+               : "memory");
 #pragma unroll
-  for (int c = 0; c < HG; c += 16) {
-    uint32_t r[16];
-    tc::tmem_ld16(taddr + (uint32_t)c, r);
-    tc::tmem_ld_wait();
+  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Reduce v[h] (h < 64) over the 32 lanes of the warp, for max or sum.  Each of five butterfly
+// stages halves the values a lane holds: the lane keeps the half its stage bit selects and adds in
+// (or takes the max with) its partner's copy of that half.  Lane l ends with heads 2l and 2l+1.
+template <bool kMax>
+__device__ __forceinline__ float2 warp_reduce_heads(const float (&v)[HG], int lane) {
+  auto op = [](float a, float b) { return kMax ? fmaxf(a, b) : a + b; };
+  float a[32], b[16], c[8], d[4], e[2];
+  bool up = (lane & 16) != 0;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[c + i] = __uint_as_float(r[i]);
+  for (int j = 0; j < 32; ++j) a[j] = op(up ? v[j + 32] : v[j], __shfl_xor_sync(0xffffffffu, up ? v[j] : v[j + 32], 16));
+  up = (lane & 8) != 0;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) b[j] = op(up ? a[j + 16] : a[j], __shfl_xor_sync(0xffffffffu, up ? a[j] : a[j + 16], 8));
+  up = (lane & 4) != 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) c[j] = op(up ? b[j + 8] : b[j], __shfl_xor_sync(0xffffffffu, up ? b[j] : b[j + 8], 4));
+  up = (lane & 2) != 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) d[j] = op(up ? c[j + 4] : c[j], __shfl_xor_sync(0xffffffffu, up ? c[j] : c[j + 4], 2));
+  up = (lane & 1) != 0;
+#pragma unroll
+  for (int j = 0; j < 2; ++j) e[j] = op(up ? d[j + 2] : d[j], __shfl_xor_sync(0xffffffffu, up ? d[j] : d[j + 2], 1));
+  return make_float2(e[0], e[1]);
+}
+
+// 16 floats from shared memory (16-byte aligned) into registers
+__device__ __forceinline__ void lds16(float (&d)[16], const float *src) {
+#pragma unroll
+  for (int k = 0; k < 16; k += 4) *reinterpret_cast<float4 *>(d + k) = *reinterpret_cast<const float4 *>(src + k);
+}
+
+// bf16 of the inverse rotation of the pair (x0, x1) (both already bf16 values) at table entry cs
+__device__ __forceinline__ void unrotate(float x0, float x1, float2 cs, float &re, float &im) {
+  const float sn = -cs.y;
+  re = __fsub_rn(__fmul_rn(x0, cs.x), __fmul_rn(x1, sn));
+  im = __fadd_rn(__fmul_rn(x0, sn), __fmul_rn(x1, cs.x));
+}
+
+// Write the bf16 vector ob (features d0 .. d0+7 of one head, element offset off) to o, and its
+// inverse rotation to o_rot: pairs at or past `tail` turn back by their angle at the query's
+// position (tp: that position's row of the cos/sin table), the others are copied.
+__device__ __forceinline__ void store_out(bf16 *o, bf16 *o_rot, int64_t off, int d0, int tail, const float2 *tp,
+                                          uint4 ob) {
+  if (o) *reinterpret_cast<uint4 *>(o + off) = ob;
+  if (o_rot) {
+    uint4 orr = ob;
+    if (d0 >= tail) {
+      const float4 c01 = *reinterpret_cast<const float4 *>(tp + ((d0 - tail) >> 1));
+      const float4 c23 = *reinterpret_cast<const float4 *>(tp + ((d0 - tail) >> 1) + 2);
+      const float2 cs[4] = {make_float2(c01.x, c01.y), make_float2(c01.z, c01.w), make_float2(c23.x, c23.y),
+                            make_float2(c23.z, c23.w)};
+      const bf16 *xb = reinterpret_cast<const bf16 *>(&ob);
+      bf16 *yb = reinterpret_cast<bf16 *>(&orr);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float re, im;
+        unrotate(__bfloat162float(xb[2 * q]), __bfloat162float(xb[2 * q + 1]), cs[q], re, im);
+        yb[2 * q] = __float2bfloat16_rn(re);
+        yb[2 * q + 1] = __float2bfloat16_rn(im);
+      }
+    }
+    *reinterpret_cast<uint4 *>(o_rot + off) = orr;
   }
 }
 
-template <int HG>
 struct Smem {
-  static constexpr size_t slots = 0;                                      // KB x 16 KiB
-  static constexpr size_t q = slots + (size_t)KB * kSlotBytes;              // KB x HG x 128
-  static constexpr size_t p = q + (size_t)KB * HG * 128;                    // kMaxTiles x 2 x HG x 128
-  static constexpr size_t list = p + (size_t)kMaxTiles * 2 * HG * 128;      // int32 [2][kMaxEntries] (A, B)
-  static constexpr size_t valid = list + (size_t)2 * kMaxEntries * 4;      // uint8 [kMaxEntries]
-  static constexpr size_t red = valid + (size_t)kMaxEntries;              // float [2][4][HG]
-  static constexpr size_t stat = red + (size_t)2 * 4 * HG * 4;            // float m[HG], l[HG]
-  static constexpr size_t bars = (stat + (size_t)2 * HG * 4 + 7) / 8 * 8;  // u64 [2*KB + 6]
-  static constexpr size_t misc = bars + (size_t)(2 * KB + 6) * 8;         // tmem slot, flags, counts
-  static constexpr size_t total = misc + 128;
+  static constexpr size_t g = 0;                                         // KB x 16 KiB: one tile; output staging
+  static constexpr size_t q = g + (size_t)KB * kBlockBytes;              // KB x 64 x 128
+  static constexpr size_t p = q + (size_t)KB * HG * 128;                 // 2 x 64 x 128
+  static constexpr size_t src = p + (size_t)2 * HG * 128;                // const bf16 * [kMaxTiles][TILE]
+  static constexpr size_t valid = src + (size_t)kMaxTiles * TILE * 8;    // uint8 [kMaxTiles][TILE]
+  static constexpr size_t red = valid + (size_t)kMaxTiles * TILE;        // float [2][4][HG]
+  static constexpr size_t stat = red + (size_t)2 * 4 * HG * 4;           // float m, l, alpha, f [HG]
+  static constexpr size_t wcnt = stat + (size_t)4 * HG * 4;              // int [kMaxTiles][4]
+  static constexpr size_t bars = wcnt + (size_t)kMaxTiles * 4 * 4;       // u64 [12]
+  static constexpr size_t misc = bars + (size_t)12 * 8;
+  static constexpr size_t total = misc + 64;
 };
 
-template <int HG>
 __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_constant__ Params P) {
-  using L = Smem<HG>;
+  using L = Smem;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = tc::smem_u32(smem_raw);
   uint8_t *smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
-  const uint32_t s_slots = tc::smem_u32(smem + L::slots), s_q = tc::smem_u32(smem + L::q),
-                 s_p = tc::smem_u32(smem + L::p);
+  const uint32_t s_g = tc::smem_u32(smem + L::g), s_q = tc::smem_u32(smem + L::q), s_p = tc::smem_u32(smem + L::p);
   uint8_t *sP = smem + L::p;
-  int32_t *listA = reinterpret_cast<int32_t *>(smem + L::list), *listB = listA + kMaxEntries;
+  const bf16 **src_list = reinterpret_cast<const bf16 **>(smem + L::src);
   uint8_t *valid = smem + L::valid;
   float *red_max = reinterpret_cast<float *>(smem + L::red), *red_sum = red_max + 4 * HG;
-  float *m_sm = reinterpret_cast<float *>(smem + L::stat), *l_sm = m_sm + HG;
+  float *m_sm = reinterpret_cast<float *>(smem + L::stat), *l_sm = m_sm + HG, *alpha_sm = l_sm + HG,
+        *f_sm = alpha_sm + HG;
+  int *wcnt = reinterpret_cast<int *>(smem + L::wcnt);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::bars);
-  uint64_t *slot_full = bars, *slot_empty = bars + KB, *q_full = bars + 2 * KB, *s_done = q_full + 1,
-           *p_full = q_full + 2, *o_done = q_full + 3, *sm_bar = q_full + 4, *drain = q_full + 5;
+  uint64_t *g_full = bars, *q_full = bars + 4, *s_full = bars + 5, *p_full = bars + 6, *o_done = bars + 7,
+           *sm_bar = bars + 8, *drain = bars + 9;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::misc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-  int *s_cnt = const_cast<int *>(abort_flag) + 1;  // [2 buffers][2 sources][4 loader warps]
-  int *s_nA = s_cnt + 16, *s_nB = s_nA + 1;
+  int *s_rescale = const_cast<int *>(abort_flag) + 1;
 
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t row = blockIdx.y;  // query b*T + t
-  const int hg = blockIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t row = blockIdx.x;  // query b*T + t
+  const int split = blockIdx.y;
+  const int hg = blockIdx.z;  // head group of 64
   const int b = (int)(row / P.T), t = (int)(row % P.T);
-  constexpr uint32_t kCols = ((kMaxTiles + 4) * HG <= 128) ? 128 : ((kMaxTiles + 4) * HG <= 256) ? 256 : 512;
+  const int k0 = split * P.tpc, nk = max(0, min(k0 + P.tpc, P.ntiles) - k0);
+  constexpr uint32_t kCols = 512;  // S: 64 columns, O^T: 4 x 64
 
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < KB; ++i) {
-      tc::mbar_init(&slot_full[i], 32);  // the lanes of the loader warp that owns the slot
-      tc::mbar_init(&slot_empty[i], 1);
-    }
+  // ---- phase 1: barriers, q, TMEM, and the index pass with the first tile's copies in flight
+  if (tid == 0) {
+    for (int i = 0; i < 4; ++i) tc::mbar_init(&g_full[i], 32);  // the lanes of the loader warp
     tc::mbar_init(q_full, 1);
-    tc::mbar_init(s_done, 1);
+    tc::mbar_init(s_full, 1);
     tc::mbar_init(p_full, 128);
     tc::mbar_init(o_done, 1);
     tc::mbar_init(sm_bar, 128);
     tc::mbar_init(drain, 1);
     *abort_flag = 0;
+    *s_rescale = 0;
     tc::fence_barrier_init();
+    // q of this query's head group, independent of the selection
+    tc::prefetch_tmap(&P.tm_q);
+    tc::mbar_expect_tx(q_full, KB * HG * 128);
+#pragma unroll 1
+    for (int kb = 0; kb < KB; ++kb)
+      tma_load_2d_nohint(s_q + kb * HG * 128, &P.tm_q, q_full, kb * 64, (int)(row * P.H + hg * HG));
   }
   if (warp == 8) tc::tmem_alloc(tmem_slot, kCols);
-  __syncthreads();
 
-  // ---- compaction (warps 4-7): the valid entries of [idx_a; idx_b] in order, split by source (rows
-  //      of rows_a in listA, of rows_b in listB); one block-wide count per 128 entries
   const int n_all = P.na + P.nb;
   const int n_rows = P.a_len + P.b_len;
+  // loader geometry: warp w copies K-blocks 2w, 2w+1 (one 256-byte segment of each row), two rows
+  // per instruction, 16 lanes per row
+  const int lw = warp - 4, half = lane >> 4, sub = lane & 15;
+  auto issue_tile = [&](int i) {
+    const uint32_t blk = s_g + (2 * lw + (sub >> 3)) * kBlockBytes;
+    const int cc = sub & 7;
+    const bf16 *const *srcs = src_list + i * TILE;
+#pragma unroll 1
+    for (int i0 = 0; i0 < TILE / 2; i0 += 8) {
+      const bf16 *ps[8];  // eight row addresses read before the copies that use them are issued
+#pragma unroll
+      for (int u = 0; u < 8; ++u) ps[u] = srcs[2 * (i0 + u) + half];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int r = 2 * (i0 + u) + half;
+        cp_async16(blk + r * 128 + ((cc ^ (r & 7)) << 4), ps[u] ? ps[u] + 128 * lw + 8 * sub : P.rows_a,
+                   ps[u] != nullptr);
+      }
+    }
+  };
+  auto tile_ok = [&](int i) { return (wcnt[4 * i] | wcnt[4 * i + 1] | wcnt[4 * i + 2] | wcnt[4 * i + 3]) != 0; };
   if (warp >= 4 && warp < 8) {
-    const int j = threadIdx.x - 128, lw = warp - 4;
-    constexpr int kPer = kMaxEntries / 128;
-    int v[kPer];
+    const int j = tid - 128;
+    int v[kMaxTiles];
 #pragma unroll
-    for (int i = 0; i < kPer; ++i) {  // every index of this query, loaded up front
-      const int e = i * 128 + j;
-      v[i] = e < P.na ? P.idx_a[row * P.na + e] : (e < n_all ? P.idx_b[row * P.nb + (e - P.na)] : -1);
+    for (int i = 0; i < kMaxTiles; ++i) {  // every index of this CTA's tiles, loaded up front
+      const int e = (k0 + i) * TILE + j;
+      v[i] = -1;
+      if (i < nk) v[i] = e < P.na ? P.idx_a[row * P.na + e] : (e < n_all ? P.idx_b[row * P.nb + (e - P.na)] : -1);
     }
-    int baseA = 0, baseB = 0;
 #pragma unroll
-    for (int i = 0; i < kPer; ++i) {
-      const int e = i * 128 + j;
-      if (e < n_all && (v[i] < -1 || v[i] >= n_rows)) atomicOr(P.status, kStatusBadIndex);
-      const bool ok = e < n_all && v[i] >= 0 && v[i] < n_rows;
-      const bool inA = ok && v[i] < P.a_len, inB = ok && v[i] >= P.a_len;
-      const unsigned balA = __ballot_sync(0xffffffffu, inA), balB = __ballot_sync(0xffffffffu, inB);
-      int *cnt = s_cnt + (i & 1) * 8;
-      if (lane == 0) {
-        cnt[lw] = __popc(balA);
-        cnt[4 + lw] = __popc(balB);
+    for (int i = 0; i < kMaxTiles; ++i) {
+      if (i < nk) {
+        const int e = (k0 + i) * TILE + j;
+        if (e < n_all && (v[i] < -1 || v[i] >= n_rows)) atomicOr(P.status, kStatusBadIndex);
+        const bool ok = e < n_all && v[i] >= 0 && v[i] < n_rows;
+        const bf16 *p = nullptr;
+        if (ok)
+          p = v[i] < P.a_len ? P.rows_a + (b * P.a_seq_rows + v[i]) * HD
+                             : P.rows_b + (b * P.b_seq_rows + (v[i] - P.a_len)) * HD;
+        src_list[i * TILE + j] = p;
+        valid[i * TILE + j] = ok;
+        const unsigned bal = __ballot_sync(0xffffffffu, ok);
+        if (lane == 0) wcnt[4 * i + lw] = __popc(bal);
       }
-      tc::named_bar(2, 128);
-      int bA = baseA, bB = baseB;
-      for (int w = 0; w < lw; ++w) {
-        bA += cnt[w];
-        bB += cnt[4 + w];
-      }
-      const unsigned below = (1u << lane) - 1u;
-      if (inA) {
-        const int at = bA + __popc(balA & below);
-        if (at < kMaxEntries) listA[at] = (int32_t)(b * P.a_seq_rows + v[i]);
-      }
-      if (inB) {
-        const int at = bB + __popc(balB & below);
-        if (at < kMaxEntries) listB[at] = (int32_t)(b * P.b_seq_rows + (v[i] - P.a_len));
-      }
-      baseA += cnt[0] + cnt[1] + cnt[2] + cnt[3];
-      baseB += cnt[4] + cnt[5] + cnt[6] + cnt[7];
     }
-    const int nA = min(baseA, kMaxEntries), nB = min(baseB, kMaxEntries - nA);
-    const int padded = min((nA + nB + TILE - 1) / TILE * TILE, kMaxEntries);
-    for (int e = j; e < padded; e += 128) valid[e] = e < nA + nB;
-    if (j == 0) {
-      *s_nA = nA;
-      *s_nB = nB;
-    }
+    tc::named_bar(1, 128);
+    for (int i = 0; i < nk; ++i)
+      if (tile_ok(i)) {
+        issue_tile(i);
+        break;
+      }
   }
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int nA = *s_nA, nB = *s_nB;
-  const int ntiles = min((nA + nB + TILE - 1) / TILE, kMaxTiles);
-  const uint32_t tS = tmem, tO = tmem + (uint32_t)(kMaxTiles * HG);  // S_k at tS + k*HG; O^T chunk c at tO + c*HG
+  int nmine = 0;
+  for (int i = 0; i < nk; ++i) nmine += tile_ok(i) ? 1 : 0;
+  const uint32_t tS = tmem, tO = tmem + HG;  // O^T chunk c at tO + c*HG
+  const bool single = P.nsplit == 1;
 
+  // ---- phase 2: the tile pipeline
   if (warp >= 4 && warp < 8) {
-    // ------------------------------------------------------------------ loaders
-    const int w = warp - 4;
-    if (w == 0 && lane == 0 && ntiles > 0) {
-      tc::prefetch_tmap(&P.tm_q);
-      tc::mbar_expect_tx(q_full, KB * HG * 128);
-#pragma unroll 1
-      for (int kb = 0; kb < KB; ++kb)
-        tma_load_2d_nohint(s_q + kb * HG * 128, &P.tm_q, q_full, kb * 64, (int)(row * P.H + hg * HG));
-    }
-    // fills in order: pass 1 tiles 0..n-1, then pass 2 tiles n-2..0 (tile n-1 stays from pass 1).
-    // This warp writes features [128 w, 128 w + 128) = slots 2w, 2w+1 of every row of the tile:
-    // lanes 0-15 one row, lanes 16-31 the next, 16 bytes each.
-    const int half = lane >> 4, sub = lane & 15;
-    const int kb = 2 * w + (sub >> 3), cc = sub & 7;
-    const uint32_t slot_base = s_slots + kb * kSlotBytes;
-    int fill = 0;
+    // ------------------------------------------------------------------ row copies
+    int n = 0;
     bool ok = true;
-    const int nfills = ntiles > 0 ? 2 * ntiles - 1 : 0;
-    for (int fi = 0; fi < nfills && ok; ++fi) {
-      const int k = fi < ntiles ? fi : 2 * ntiles - 2 - fi;
-      const uint32_t par = (uint32_t)(fill & 1) ^ 1u;
-      if (!(ok = tc::mbar_wait(&slot_empty[2 * w], par, abort_flag) &&
-                 tc::mbar_wait(&slot_empty[2 * w + 1], par, abort_flag)))
-        break;
-#pragma unroll 4
-      for (int i = 0; i < TILE / 2; ++i) {
-        const int r = 2 * i + half, e = k * TILE + r;
-        const bool vr = e < nA + nB;
-        const bf16 *src = P.rows_a;
-        if (vr) src = e < nA ? P.rows_a + (int64_t)listA[e] * HD : P.rows_b + (int64_t)listB[e - nA] * HD;
-        cp_async16(slot_base + r * 128 + ((cc ^ (r & 7)) << 4), src + (vr ? 128 * w + 8 * sub : 0), vr);
+    for (int i = 0; i < nk && ok; ++i) {
+      if (!tile_ok(i)) continue;
+      if (n > 0) {
+        if (!(ok = tc::mbar_wait(o_done, (uint32_t)((n - 1) & 1), abort_flag))) break;
+        issue_tile(i);
       }
       cp_async_wait_all();
       fence_proxy_async();
-      tc::mbar_arrive(&slot_full[2 * w]);
-      tc::mbar_arrive(&slot_full[2 * w + 1]);
-      ++fill;
+      tc::mbar_arrive(&g_full[lw]);
+      ++n;
     }
     cp_async_wait_all();
-    if (w == 0 && lane == 0 && ntiles > 0) {  // the q copies have landed before the CTA can exit
-      const uint64_t t0 = tc::global_ns();
-      while (!tc::mbar_try_wait(q_full, 0) && tc::global_ns() - t0 < tc::kWaitLimitNs) {
-      }
-    }
   } else if (warp == 8) {
     // ------------------------------------------------------------------ MMA issue
-    if (lane == 0 && ntiles > 0) {
+    if (lane == 0) {
       const uint32_t id1 = tc::idesc_bf16_f32(TILE, HG);
       const uint32_t id2 = tc::idesc_bf16_f32(TILE, HG, /*a_mn_major=*/true, /*b_mn_major=*/false);
-      bool ok = tc::mbar_wait(q_full, 0, abort_flag);
-      int fill = 0;
-      // pass 1: scores of every tile
-      for (int k = 0; k < ntiles && ok; ++k) {
-        for (int kb = 0; kb < KB; ++kb) {
-          if (!(ok = tc::mbar_wait(&slot_full[kb], (uint32_t)(fill & 1), abort_flag))) break;
+      bool ok = tc::mbar_wait(q_full, 0, abort_flag);  // also keeps the CTA alive until q has landed
+      int n = 0;
+      bool issued = false;
+      for (int i = 0; i < nk && ok; ++i) {
+        if (!tile_ok(i)) continue;
+        const uint32_t par = (uint32_t)(n & 1);
+        // S^T = G q^T, each K-block pair as soon as its loader warp is done
+        for (int w = 0; w < 4 && ok; ++w) {
+          if (!(ok = tc::mbar_wait(&g_full[w], par, abort_flag))) break;
           tc::tc_fence_after();
-          const uint64_t ad = tc::sdesc_sw128(s_slots + kb * kSlotBytes, 16, 1024);
-          const uint64_t bd = tc::sdesc_sw128(s_q + kb * HG * 128, 16, 1024);
+          issued = true;
 #pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4)
-            tc::mma_bf16(tS + (uint32_t)(k * HG), ad + 2ull * k4, bd + 2ull * k4, id1, (kb | k4) ? 1u : 0u);
-          if (k + 1 < ntiles) tc::mma_commit(&slot_empty[kb]);  // the last tile stays for pass 2
-        }
-        ++fill;
-      }
-      if (ok) tc::mma_commit(s_done);
-      if (ok) ok = tc::mbar_wait(p_full, 0, abort_flag);
-      // pass 2: O^T += G^T P^T, the last tile first (still in the slots), then the refills
-      for (int pi = 0; pi < ntiles && ok; ++pi) {
-        const int k = ntiles - 1 - pi;
-        const bool resident = pi == 0;
-#pragma unroll 1
-        for (int c = 0; c < KB / 2 && ok; ++c) {
-          if (!resident) {
-            if (!(ok = tc::mbar_wait(&slot_full[2 * c], (uint32_t)(fill & 1), abort_flag))) break;
-            if (!(ok = tc::mbar_wait(&slot_full[2 * c + 1], (uint32_t)(fill & 1), abort_flag))) break;
-            tc::tc_fence_after();
-          }
+          for (int kb = 2 * w; kb < 2 * w + 2; ++kb) {
+            const uint64_t ad = tc::sdesc_sw128(s_g + kb * kBlockBytes, 16, 1024);
+            const uint64_t bd = tc::sdesc_sw128(s_q + kb * HG * 128, 16, 1024);
 #pragma unroll
-          for (int i = 0; i < TILE / 16; ++i) {
-            const uint64_t ad = tc::sdesc_sw128(s_slots + (2 * c) * kSlotBytes + i * 2048, kSlotBytes, 1024);
-            const uint64_t bd =
-                tc::sdesc_sw128(s_p + k * 2 * HG * 128 + (i / 4) * HG * 128 + (i % 4) * 32, 16, 1024);
-            tc::mma_bf16(tO + (uint32_t)(c * HG), ad, bd, id2, (pi > 0 || i > 0) ? 1u : 0u);
+            for (int k4 = 0; k4 < 4; ++k4) tc::mma_bf16(tS, ad + 2ull * k4, bd + 2ull * k4, id1, (kb | k4) ? 1u : 0u);
           }
-          tc::mma_commit(&slot_empty[2 * c]);
-          tc::mma_commit(&slot_empty[2 * c + 1]);
         }
-        if (!resident) ++fill;
+        if (!ok) break;
+        tc::mma_commit(s_full);
+        if (!(ok = tc::mbar_wait(p_full, par, abort_flag))) break;
+        tc::tc_fence_after();
+        // O^T += G^T P^T, feature chunk c = K-blocks 2c, 2c+1
+#pragma unroll
+        for (int c = 0; c < KB / 2; ++c) {
+#pragma unroll
+          for (int ii = 0; ii < TILE / 16; ++ii) {
+            const uint64_t ad = tc::sdesc_sw128(s_g + (2 * c) * kBlockBytes + ii * 2048, kBlockBytes, 1024);
+            const uint64_t bd = tc::sdesc_sw128(s_p + (ii / 4) * HG * 128 + (ii % 4) * 32, 16, 1024);
+            tc::mma_bf16(tO + (uint32_t)(c * HG), ad, bd, id2, (n > 0 || ii > 0) ? 1u : 0u);
+          }
+        }
+        tc::mma_commit(o_done);
+        ++n;
       }
-      if (ok) tc::mma_commit(o_done);
-      tc::mma_commit(drain);
-      const uint64_t t0 = tc::global_ns();
-      while (!tc::mbar_try_wait(drain, 0) && tc::global_ns() - t0 < tc::kWaitLimitNs) {
+      if (issued) {  // nothing may still write TMEM or read shared memory when the CTA moves on
+        tc::mma_commit(drain);
+        const uint64_t t0 = tc::global_ns();
+        while (!tc::mbar_try_wait(drain, 0) && tc::global_ns() - t0 < tc::kWaitLimitNs) {
+        }
       }
     }
-  } else if (warp < 4) {
-    // ------------------------------------------------------------------ softmax + epilogue (warps 0-3)
+  } else {
+    // ------------------------------------------------------------------ softmax + staging (warps 0-3)
     const int r = warp * 32 + lane;  // tile row (S^T) and feature within a chunk (O^T)
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
     uint32_t sm_uses = 0;
@@ -308,116 +392,130 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
       tc::mbar_arrive(sm_bar);
       return tc::mbar_wait(sm_bar, (sm_uses++) & 1u, abort_flag);
     };
-    bool ok = true;
-    if (ntiles > 0) {
-      ok = tc::mbar_wait(s_done, 0, abort_flag);
-      if (ok) tc::tc_fence_after();
-      float m[HG], l[HG];
+    if (r < HG) {
+      m_sm[r] = -INFINITY;
+      l_sm[r] = 0.f;
+    }
+    bool ok = sm_sync();
+    int n = 0;
+    for (int i = 0; i < nk && ok; ++i) {
+      if (!tile_ok(i)) continue;
+      if (!(ok = tc::mbar_wait(s_full, (uint32_t)(n & 1), abort_flag))) break;
+      tc::tc_fence_after();
+      float s[HG];
+      tmem_ld_cols(tS + lane_off, s);
+      const bool vr = valid[i * TILE + r] != 0;
 #pragma unroll
-      for (int h = 0; h < HG; ++h) {
-        m[h] = -INFINITY;
-        l[h] = 0.f;
-      }
-      // maximum over every row of every tile
-      for (int k = 0; k < ntiles && ok; ++k) {
-        float s[HG];
-        tmem_ld_cols<HG>(tS + (uint32_t)(k * HG) + lane_off, s);
-        if (valid[k * TILE + r]) {
-#pragma unroll
-          for (int h = 0; h < HG; ++h) m[h] = fmaxf(m[h], s[h] * P.scale_log2);
-        }
-      }
-#pragma unroll
-      for (int h = 0; h < HG; ++h) {
-        float x = m[h];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
-        if (lane == 0) red_max[warp * HG + h] = x;
-      }
-      if (ok) ok = sm_sync();
+      for (int h = 0; h < HG; ++h) s[h] = vr ? s[h] * P.scale_log2 : -INFINITY;
+      reinterpret_cast<float2 *>(red_max + warp * HG)[lane] = warp_reduce_heads<true>(s, lane);
+      if (!(ok = sm_sync())) break;
       if (r < HG) {
-        const float sink2 = P.sink[hg * HG + r] * 1.4426950408889634f;
-        m_sm[r] = fmaxf(fmaxf(fmaxf(red_max[r], red_max[HG + r]), fmaxf(red_max[2 * HG + r], red_max[3 * HG + r])),
-                        sink2);
-      }
-      if (ok) ok = sm_sync();
-#pragma unroll
-      for (int h = 0; h < HG; ++h) m[h] = m_sm[h];
-      // probabilities (bf16, K-major [HG][128 rows] per tile, swizzled) and their sums
-      const int rc = (r % 64) / 8, ro = (r % 8) * 2;
-      for (int k = 0; k < ntiles && ok; ++k) {
-        float s[HG];
-        tmem_ld_cols<HG>(tS + (uint32_t)(k * HG) + lane_off, s);
-        const bool vr = valid[k * TILE + r] != 0;
-        uint8_t *prow = sP + k * 2 * HG * 128 + (r / 64) * HG * 128;
-#pragma unroll
-        for (int h = 0; h < HG; ++h) {
-          const float p = vr ? exp2f(s[h] * P.scale_log2 - m[h]) : 0.f;
-          l[h] += p;
-          *reinterpret_cast<bf16 *>(prow + h * 128 + ((rc ^ (h & 7)) << 4) + ro) = __float2bfloat16_rn(p);
+        const float tmax = fmaxf(fmaxf(red_max[r], red_max[HG + r]), fmaxf(red_max[2 * HG + r], red_max[3 * HG + r]));
+        float a = 1.0f;
+        if (tmax > m_sm[r] + 8.0f) {  // keep exp2(s - m) below 2^8; rescale what has accumulated
+          a = exp2f(m_sm[r] - tmax);
+          m_sm[r] = tmax;
+          l_sm[r] *= a;
+          if (n > 0) *s_rescale = 1;
         }
+        alpha_sm[r] = a;
       }
+      if (!(ok = sm_sync())) break;
+      if (*s_rescale) {
+        // the previous tile's product has completed: its commit released this tile's rows
+#pragma unroll 1
+        for (int c = 0; c < KB / 2; ++c) {
 #pragma unroll
-      for (int h = 0; h < HG; ++h) {
-        float x = l[h];
+          for (int c0 = 0; c0 < HG; c0 += 16) {
+            uint32_t v[16];
+            const uint32_t ta = tO + (uint32_t)(c * HG + c0) + lane_off;
+            float av[16];
+            lds16(av, alpha_sm + c0);
+            tc::tmem_ld16(ta, v);
+            tc::tmem_ld_wait();
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-        if (lane == 0) red_sum[warp * HG + h] = x;
+            for (int q = 0; q < 16; ++q) v[q] = __float_as_uint(__uint_as_float(v[q]) * av[q]);
+            tmem_st16(ta, v);
+          }
+        }
+        tmem_st_wait();
+      }
+      uint8_t *prow = sP + (r / 64) * HG * 128;
+      const int rc = (r % 64) / 8, ro = (r % 8) * 2;
+#pragma unroll
+      for (int h0 = 0; h0 < HG; h0 += 16) {
+        float mv[16];  // the maxima read before the stores below (which the compiler cannot tell apart)
+        lds16(mv, m_sm + h0);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const int h = h0 + k;
+          s[h] = exp2f(s[h] - mv[k]);  // 0 for masked rows
+          *reinterpret_cast<bf16 *>(prow + h * 128 + ((rc ^ (h & 7)) << 4) + ro) = __float2bfloat16_rn(s[h]);
+        }
       }
       fence_proxy_async();
       tc::tc_fence_before();
       tc::mbar_arrive(p_full);
-      if (ok) ok = sm_sync();
+      reinterpret_cast<float2 *>(red_sum + warp * HG)[lane] = warp_reduce_heads<false>(s, lane);
+      if (!(ok = sm_sync())) break;
       if (r < HG) {
-        const float sink2 = P.sink[hg * HG + r] * 1.4426950408889634f;
-        l_sm[r] =
-            exp2f(sink2 - m_sm[r]) + ((red_sum[r] + red_sum[HG + r]) + (red_sum[2 * HG + r] + red_sum[3 * HG + r]));
+        l_sm[r] += (red_sum[r] + red_sum[HG + r]) + (red_sum[2 * HG + r] + red_sum[3 * HG + r]);
+        if (r == 0) *s_rescale = 0;
       }
-      if (ok) ok = sm_sync();
-      if (ok) ok = tc::mbar_wait(o_done, 0, abort_flag);
-    } else {
-      if (r < HG) l_sm[r] = 1.f;
-      ok = sm_sync();
+      ++n;
     }
-    ok = __all_sync(0xffffffffu, ok);  // the shuffles below need the whole warp
-    // epilogue: O = O^T / l, bf16; inverse rotation of the last rd features at the query's position
-    if (ok) {
+    if (ok && nmine > 0) ok = tc::mbar_wait(o_done, (uint32_t)((nmine - 1) & 1), abort_flag);
+    if (ok && r < HG) {
+      if (single) {  // finish in place: the sink joins the denominator
+        const float s2 = P.sink[hg * HG + r] * 1.4426950408889634f;
+        const float M = fmaxf(m_sm[r], s2);
+        const float em = nmine > 0 ? exp2f(m_sm[r] - M) : 0.f;
+        f_sm[r] = em / (l_sm[r] * em + exp2f(s2 - M));
+      } else {
+        f_sm[r] = nmine > 0 ? 1.0f / l_sm[r] : 0.f;
+        float *ml = P.part_ml + ((row * P.nsplit + split) * P.H + hg * HG + r) * 2;
+        ml[0] = m_sm[r];
+        ml[1] = l_sm[r];
+      }
+    }
+    if (ok) ok = sm_sync();
+    if (ok && nmine > 0) {
+      // stage O * f as bf16 [64 heads][512] in the (now idle) tile buffer
       tc::tc_fence_after();
-      const int p_pos = P.start_pos + t;
-      const int tail = HD - P.rd;
+      bf16 *stage = reinterpret_cast<bf16 *>(smem + L::g);
 #pragma unroll 1
       for (int c = 0; c < KB / 2; ++c) {
         float v[HG];
-        if (ntiles > 0) {
-          tmem_ld_cols<HG>(tO + (uint32_t)(c * HG) + lane_off, v);
-        } else {
+        tmem_ld_cols(tO + (uint32_t)(c * HG) + lane_off, v);
 #pragma unroll
-          for (int h = 0; h < HG; ++h) v[h] = 0.f;
-        }
-        const int d = c * 128 + r;
-        float2 cs = make_float2(1.f, 0.f);
-        const bool rot = P.o_rot && d >= tail;
-        if (rot) cs = reinterpret_cast<const float2 *>(P.tab)[(int64_t)p_pos * (P.rd >> 1) + ((d - tail) >> 1)];
+        for (int h0 = 0; h0 < HG; h0 += 16) {
+          float fv[16];  // the factors read before the stores below
+          lds16(fv, f_sm + h0);
 #pragma unroll
-        for (int h = 0; h < HG; ++h) {
-          const bf16 ob = __float2bfloat16_rn(v[h] / l_sm[h]);
-          const int64_t off = (row * P.H + hg * HG + h) * (int64_t)HD + d;
-          if (P.o) P.o[off] = ob;
-          if (P.o_rot) {
-            const float x = __bfloat162float(ob);
-            const float partner = __shfl_xor_sync(0xffffffffu, x, 1);
-            bf16 out = ob;
-            if (rot) {
-              const float sn = -cs.y;
-              const float x0 = (d & 1) ? partner : x, x1 = (d & 1) ? x : partner;
-              const float re = __fsub_rn(__fmul_rn(x0, cs.x), __fmul_rn(x1, sn));
-              const float im = __fadd_rn(__fmul_rn(x0, sn), __fmul_rn(x1, cs.x));
-              out = __float2bfloat16_rn((d & 1) ? im : re);
-            }
-            P.o_rot[off] = out;
-          }
+          for (int k = 0; k < 16; ++k) stage[(h0 + k) * HD + c * 128 + r] = __float2bfloat16_rn(v[h0 + k] * fv[k]);
         }
       }
+    }
+  }
+  __syncthreads();
+
+  // ---- phase 3: the result, or this CTA's share of it, by all nine warps (16-byte vectors: head h,
+  // features d0 .. d0+7)
+  const bf16 *stage = reinterpret_cast<const bf16 *>(smem + L::g);
+  if (single) {
+    const float2 *tp = P.o_rot ? reinterpret_cast<const float2 *>(P.tab) + (int64_t)(P.start_pos + t) * (P.rd >> 1)
+                               : nullptr;
+    for (int it = tid; it < kVecs; it += kThreads) {
+      const int h = it >> 6, d0 = (it & 63) * 8;
+      uint4 ob = make_uint4(0u, 0u, 0u, 0u);
+      if (nmine > 0) ob = *reinterpret_cast<const uint4 *>(stage + h * HD + d0);
+      store_out(P.o, P.o_rot, (row * P.H + hg * HG + h) * (int64_t)HD + d0, d0, HD - P.rd, tp, ob);
+    }
+  } else if (nmine > 0) {
+    bf16 *mine = P.part_o + ((row * P.nsplit + split) * P.H + hg * HG) * (int64_t)HD;
+    for (int it = tid; it < kVecs; it += kThreads) {
+      const int h = it >> 6, d0 = (it & 63) * 8;
+      *reinterpret_cast<uint4 *>(mine + h * HD + d0) = *reinterpret_cast<const uint4 *>(stage + h * HD + d0);
     }
   }
   __syncthreads();
@@ -425,40 +523,107 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, kCols);
   }
-  if (threadIdx.x == 0 && *abort_flag) atomicOr(P.status, kStatusTimeout);
+  if (tid == 0 && *abort_flag) atomicOr(P.status, kStatusTimeout);
 }
 
-template <int HG>
-cudaError_t launch_hg(const Params &p, int nq, cudaStream_t s) {
-  static bool attr = false;
-  const size_t smem = 1024 + Smem<HG>::total;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_sparse_attn_tc<HG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr = true;
+// Merge of the split shares: block (query, 8 heads), one thread per 16-byte vector pair.  The
+// weights e^{m_c - M} l_c / den put each share O_c / l_c back on the common scale, with the sink in
+// den; shares of CTAs that found nothing (l_c = 0) weigh 0.
+constexpr int kCombHeads = 8;
+constexpr int kCombThreads = 256;
+struct CombineParams {
+  const bf16 *part_o;
+  const float *part_ml;
+  int nsplit, H, T;
+  const float *sink;
+  bf16 *o, *o_rot;
+  int rd, start_pos;
+  const float *tab;
+};
+
+__global__ void __launch_bounds__(kCombThreads) k_attn_combine(const __grid_constant__ CombineParams C) {
+  __shared__ float wgt[kMaxTiles][kCombHeads];
+  const int64_t row = blockIdx.x;
+  const int h0 = blockIdx.y * kCombHeads, tid = threadIdx.x;
+  if (tid < kCombHeads) {
+    const int h = h0 + tid;
+    const float s2 = C.sink[h] * 1.4426950408889634f;
+    float M = s2;
+    for (int c = 0; c < C.nsplit; ++c) {
+      const float *ml = C.part_ml + ((row * C.nsplit + c) * C.H + h) * 2;
+      if (ml[1] > 0.f) M = fmaxf(M, ml[0]);
+    }
+    float den = exp2f(s2 - M), w[kMaxTiles];
+#pragma unroll
+    for (int c = 0; c < kMaxTiles; ++c) {
+      w[c] = 0.f;
+      if (c < C.nsplit) {
+        const float *ml = C.part_ml + ((row * C.nsplit + c) * C.H + h) * 2;
+        w[c] = ml[1] > 0.f ? ml[1] * exp2f(ml[0] - M) : 0.f;
+        den += w[c];
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < kMaxTiles; ++c) wgt[c][tid] = w[c] / den;
   }
-  dim3 grid(p.H / HG, nq);
-  k_sparse_attn_tc<HG><<<grid, kThreads, smem, s>>>(p);
-  return cudaGetLastError();
+  __syncthreads();
+  const int t = (int)(row % C.T);
+  const float2 *tp = C.o_rot ? reinterpret_cast<const float2 *>(C.tab) + (int64_t)(C.start_pos + t) * (C.rd >> 1)
+                             : nullptr;
+  constexpr int kPer = kCombHeads * (HD / 8) / kCombThreads;  // vectors per thread
+  uint4 u[kPer][kMaxTiles];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {  // every share of every vector in flight together
+    const int it = tid + k * kCombThreads, hl = it >> 6, d0 = (it & 63) * 8;
+#pragma unroll
+    for (int c = 0; c < kMaxTiles; ++c) {
+      u[k][c] = make_uint4(0u, 0u, 0u, 0u);
+      if (c < C.nsplit && wgt[c][hl] != 0.f)
+        u[k][c] = *reinterpret_cast<const uint4 *>(C.part_o + ((row * C.nsplit + c) * C.H + h0 + hl) * (int64_t)HD +
+                                                   d0);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int it = tid + k * kCombThreads, hl = it >> 6, d0 = (it & 63) * 8;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int c = 0; c < kMaxTiles; ++c) {
+      const float wv = wgt[c][hl];
+      const __nv_bfloat162 *pv = reinterpret_cast<const __nv_bfloat162 *>(&u[k][c]);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        acc[2 * q] = fmaf(wv, __low2float(pv[q]), acc[2 * q]);
+        acc[2 * q + 1] = fmaf(wv, __high2float(pv[q]), acc[2 * q + 1]);
+      }
+    }
+    uint4 ob;
+    __nv_bfloat162 *po = reinterpret_cast<__nv_bfloat162 *>(&ob);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) po[q] = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
+    store_out(C.o, C.o_rot, (row * C.H + h0 + hl) * (int64_t)HD + d0, d0, HD - C.rd, tp, ob);
+  }
 }
 
 }  // namespace attn
 
 bool sparse_attn_tc_supported(const AttnArgs &a) {
-  // every selection must fit kMaxTiles tiles of rows
-  return a.hd == attn::HD && a.H % 16 == 0 && a.na + a.nb <= attn::kMaxEntries && a.a_seq_stride % attn::HD == 0 &&
-         (a.rows_b == nullptr || a.b_seq_stride % attn::HD == 0) && (a.o_rot == nullptr || a.rd % 2 == 0) &&
-         ((uintptr_t)a.q & 15) == 0 && ((uintptr_t)a.rows_a & 15) == 0 && ((uintptr_t)a.rows_b & 15) == 0;
+  return a.hd == attn::HD && a.H % attn::HG == 0 && a.H / attn::HG <= attn::kMaxHeadGroups &&
+         a.na + a.nb <= attn::kMaxTiles * attn::TILE && a.a_seq_stride % attn::HD == 0 &&
+         (a.rows_b == nullptr || a.b_seq_stride % attn::HD == 0) &&
+         (a.o_rot == nullptr || (a.rd % 8 == 0 && ((uintptr_t)a.tab & 15) == 0)) && ((uintptr_t)a.q & 15) == 0 &&
+         ((uintptr_t)a.rows_a & 15) == 0 && ((uintptr_t)a.rows_b & 15) == 0 && ((uintptr_t)a.o & 15) == 0 &&
+         ((uintptr_t)a.o_rot & 15) == 0;
 }
 
-cudaError_t launch_sparse_attn_tc(const AttnArgs &a, int num_sms, cudaStream_t s) {
+cudaError_t launch_sparse_attn_tc(const AttnArgs &a, float *ws, size_t ws_bytes, int num_sms, cudaStream_t s,
+                                  int *kernels) {
+  *kernels = 0;
   using namespace attn;
   const int nq = a.B * a.T;
   if (nq <= 0) return cudaSuccess;
   Params p;
   memset(&p, 0, sizeof(p));
-  // heads per CTA: 32 once that still gives about one CTA per SM, else 16
-  const int HG = ((int64_t)nq * (a.H / 32) >= num_sms && a.H % 32 == 0) ? 32 : 16;
   if (!tma_map_2d_bf16(&p.tm_q, a.q, HD, (uint64_t)nq * a.H, HD, 64, (uint32_t)HG)) return cudaErrorInvalidValue;
   p.rows_a = a.rows_a;
   p.rows_b = a.rows_b ? a.rows_b : a.rows_a;
@@ -480,7 +645,52 @@ cudaError_t launch_sparse_attn_tc(const AttnArgs &a, int num_sms, cudaStream_t s
   p.start_pos = a.start_pos;
   p.tab = a.tab;
   p.status = a.status;
-  return HG == 32 ? launch_hg<32>(p, nq, s) : launch_hg<16>(p, nq, s);
+  p.ntiles = std::max(1, (a.na + p.nb + TILE - 1) / TILE);
+  // tiles per CTA: split a query's tiles over CTAs only while there are few queries to fill the
+  // SMs (up to two CTAs per SM in the grid: tiles of entries that are all -1 cost a CTA only its
+  // index pass), and only as far as the workspace holds the shares (the GEMM's counters precede it)
+  const int groups = a.H / HG;
+  const size_t avail = ws_bytes > kGemmCounterBytes ? ws_bytes - kGemmCounterBytes : 0;
+  int tpc = p.ntiles;
+  for (int c = 1; c < p.ntiles; ++c) {
+    const int ns = (p.ntiles + c - 1) / c;
+    const size_t need = (size_t)nq * ns * a.H * (HD * sizeof(bf16) + 2 * sizeof(float));
+    if ((int64_t)nq * groups * ns <= 2 * num_sms && need <= avail) {
+      tpc = c;
+      break;
+    }
+  }
+  p.tpc = tpc;
+  p.nsplit = (p.ntiles + tpc - 1) / tpc;
+  uint8_t *base = reinterpret_cast<uint8_t *>(ws) + kGemmCounterBytes;
+  p.part_o = reinterpret_cast<bf16 *>(base);
+  p.part_ml = reinterpret_cast<float *>(base + (size_t)nq * p.nsplit * a.H * HD * sizeof(bf16));
+  static bool attr = false;
+  const size_t smem = 1024 + Smem::total;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(k_sparse_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  dim3 grid(nq, p.nsplit, groups);
+  k_sparse_attn_tc<<<grid, kThreads, smem, s>>>(p);
+  *kernels = 1;
+  if (p.nsplit == 1) return cudaGetLastError();
+  CombineParams c;
+  c.part_o = p.part_o;
+  c.part_ml = p.part_ml;
+  c.nsplit = p.nsplit;
+  c.H = a.H;
+  c.T = a.T;
+  c.sink = a.sink;
+  c.o = a.o;
+  c.o_rot = a.o_rot;
+  c.rd = a.rd;
+  c.start_pos = a.start_pos;
+  c.tab = a.tab;
+  k_attn_combine<<<dim3(nq, a.H / kCombHeads), kCombThreads, 0, s>>>(c);
+  *kernels = 2;
+  return cudaGetLastError();
 }
 
 }  // namespace csa

@@ -206,7 +206,9 @@ def test_index_topk_bit_exact(csa, orc, B, T, start, L, clen, ratio, keep, cb, K
 @pytest.mark.parametrize("H,hd,na,nb,a_len,b_len,B,T", [(4, 64, 8, 16, 12, 40, 1, 12), (64, 512, 128, 512, 128, 500, 3, 1),
                                                         (64, 512, 128, 512, 300, 1024, 1, 9),
                                                         (64, 512, 128, 512, 128, 700, 80, 1),
-                                                        (64, 512, 7, 300, 7, 64, 2, 5)])
+                                                        (64, 512, 7, 300, 7, 64, 2, 5),
+                                                        (128, 512, 128, 256, 128, 300, 2, 1),
+                                                        (64, 512, 64, 256, 64, 400, 2, 100)])
 def test_sparse_attn(csa, orc, H, hd, na, nb, a_len, b_len, B, T):
     rng = np.random.default_rng(8 + H)
     q = _rng_bf16(orc, rng, (B * T, H, hd))
@@ -219,7 +221,7 @@ def test_sparse_attn(csa, orc, H, hd, na, nb, a_len, b_len, B, T):
     ia[0, :] = -1  # a query with nothing selected: O = 0
     scale = 1 / math.sqrt(hd)
     rd, start = hd // 8, 0
-    tab = orc.rope_table(rd, 64, 10000.0)
+    tab = orc.rope_table(rd, max(64, T), 10000.0)
     want = np.concatenate([orc.sparse_attn(q[b * T:(b + 1) * T], ra[b], rb[b],
                                            np.concatenate([ia[b * T:(b + 1) * T], ib[b * T:(b + 1) * T]], 1), sink, scale)
                            for b in range(B)])
