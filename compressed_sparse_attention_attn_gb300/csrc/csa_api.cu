@@ -536,7 +536,8 @@ int attn_v41_forward(csa_ctx *ctx, const csa_layer_weights *w, csa_layer_state *
       float *S = dbg && dbg->scores ? dbg->scores : ctx->scores;
       const uint8_t *cand = r.uses_candidates ? sh->candidates : nullptr;
       STEP(csa::launch_index_scores(qI, wI, (const bf16 *)sh->index_k, B, T, start_pos, Hi, dI, sh->compress_stride,
-                                    sh->compress_len, r.ratio, cand, sh->cand_width, g.cand_block, S, s),
+                                    sh->compress_len, r.ratio, cand, sh->cand_width, g.cand_block, S, s,
+                                    ctx->status),
            "index scores");
       STEP(csa::launch_index_topk(S, B, T, start_pos, sh->compress_stride, sh->compress_len, r.ratio, cand,
                                   sh->cand_width, g.cand_block, K, rows_a_len, sh->topk_idxs, s),

@@ -675,7 +675,8 @@ cudaError_t launch_sparse_attn_tc(const AttnArgs &a, float *ws, size_t ws_bytes,
   dim3 grid(nq, p.nsplit, groups);
   k_sparse_attn_tc<<<grid, kThreads, smem, s>>>(p);
   *kernels = 1;
-  if (p.nsplit == 1) return cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
+  if (p.nsplit == 1 || e != cudaSuccess) return e;
   CombineParams c;
   c.part_o = p.part_o;
   c.part_ml = p.part_ml;

@@ -209,7 +209,7 @@ __global__ void k_kv_finish(const bf16 *kv_in, bf16 *kv_out, int T, int start_po
 // qr = RMSNorm(sum) * q_norm, the window row (RMSNorm * kv_norm, RoPE, fp8, ring, selection), and
 // w^I = bf16(sum) * wscale.  One CTA per token, blockDim >= hd, a multiple of 32.
 // ---------------------------------------------------------------------------------------------
-__global__ void k_x_finish(XFinishArgs a) {
+__global__ void __launch_bounds__(1024) k_x_finish(XFinishArgs a) {
   extern __shared__ float xs[];  // [ldp] the token's projections, rounded to bf16
   __shared__ float red[2][32];
   const int64_t row = blockIdx.x;
@@ -217,15 +217,53 @@ __global__ void k_x_finish(XFinishArgs a) {
   const int M = a.B * a.T;
   const int n = a.q_rank + a.hd + a.Hi;
   float sq = 0.f, skv = 0.f;
-  for (int c = threadIdx.x; c < n; c += blockDim.x) {
-    float v = 0.f;
-    for (int s = 0; s < a.S; ++s) v += a.part[((int64_t)s * M + row) * a.ldp + c];
+  auto take = [&](int c, float v) {
     v = __bfloat162float(__float2bfloat16_rn(v));  // linear_bf16 rounds the projection to bf16
     xs[c] = v;
     if (c < a.q_rank)
       sq = fmaf(v, v, sq);
     else if (c < a.q_rank + a.hd)
       skv = fmaf(v, v, skv);
+  };
+  // the split partials of a column are summed in split order; up to 8 of them in flight at once
+  constexpr int kB = 8;
+  if ((n & 3) == 0 && (a.ldp & 3) == 0 && ((uintptr_t)a.part & 15) == 0) {
+    for (int c4 = threadIdx.x; c4 < n / 4; c4 += blockDim.x) {
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int s0 = 0; s0 < a.S; s0 += kB) {
+        float4 v[kB];
+#pragma unroll
+        for (int u = 0; u < kB; ++u)
+          if (s0 + u < a.S)
+            v[u] = __ldcg(reinterpret_cast<const float4 *>(a.part + ((int64_t)(s0 + u) * M + row) * a.ldp) + c4);
+#pragma unroll
+        for (int u = 0; u < kB; ++u)
+          if (s0 + u < a.S) {
+            acc.x += v[u].x;
+            acc.y += v[u].y;
+            acc.z += v[u].z;
+            acc.w += v[u].w;
+          }
+      }
+      take(4 * c4, acc.x);
+      take(4 * c4 + 1, acc.y);
+      take(4 * c4 + 2, acc.z);
+      take(4 * c4 + 3, acc.w);
+    }
+  } else {
+    for (int c = threadIdx.x; c < n; c += blockDim.x) {
+      float acc = 0.f;
+      for (int s0 = 0; s0 < a.S; s0 += kB) {
+        float v[kB];
+#pragma unroll
+        for (int u = 0; u < kB; ++u)
+          if (s0 + u < a.S) v[u] = __ldcg(a.part + ((int64_t)(s0 + u) * M + row) * a.ldp + c);
+#pragma unroll
+        for (int u = 0; u < kB; ++u)
+          if (s0 + u < a.S) acc += v[u];
+      }
+      take(c, acc);
+    }
   }
   sq = warp_sum(sq);
   skv = warp_sum(skv);

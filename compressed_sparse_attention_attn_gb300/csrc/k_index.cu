@@ -58,10 +58,18 @@ __global__ void __launch_bounds__(128) k_index_scores(const bf16 *__restrict__ q
   S[row * Lstride + j] = acc;
 }
 
+bool index_scores_tc_supported(const bf16 *qI, const bf16 *KI, int Hi, int dI);
+cudaError_t launch_index_scores_tc(const bf16 *qI, const float *wI, const bf16 *KI, int B, int T, int start_pos,
+                                   int Hi, int Lstride, int compress_len, int ratio, const uint8_t *cand,
+                                   int cand_width, int cand_block, float *S, int *status, cudaStream_t s);
+
 cudaError_t launch_index_scores(const bf16 *qI, const float *wI, const bf16 *KI, int B, int T, int start_pos, int Hi,
                                 int dI, int Lstride, int compress_len, int ratio, const uint8_t *cand, int cand_width,
-                                int cand_block, float *S, cudaStream_t s) {
+                                int cand_block, float *S, cudaStream_t s, int *status) {
   if (B * T <= 0 || Lstride <= 0) return cudaSuccess;
+  if (index_scores_tc_supported(qI, KI, Hi, dI))
+    return launch_index_scores_tc(qI, wI, KI, B, T, start_pos, Hi, Lstride, compress_len, ratio, cand, cand_width,
+                                  cand_block, S, status, s);
   const size_t smem = sizeof(float) * (size_t)Hi * (dI + 1);
   dim3 grid((Lstride + 127) / 128, B * T);
   switch (dI) {
@@ -86,9 +94,12 @@ cudaError_t launch_index_scores(const bf16 *qI, const float *wI, const bf16 *KI,
 
 // ---------------------------------------------------------------------------------------------
 // Top-k: one CTA per query.  Scores map to order-preserving 32-bit keys (-0 folded onto +0, NaN
-// below every number); a 4-pass radix select over the valid positions finds the K-th largest key;
-// keys above it are taken, and of the keys equal to it the lowest positions; the K chosen
-// (key, position) pairs are then sorted (key descending, position ascending) by a bitonic network.
+// below every number).  A first pass compacts the valid positions' (key, position) pairs; when
+// they are at most K, all are taken.  Otherwise a 4-pass radix select over the valid positions
+// finds the K-th largest key: keys above it are taken, and of the keys equal to it the lowest
+// positions.  The chosen pairs are then sorted (key descending, position ascending) by a bitonic
+// network whose stages within a warp run on shuffles and whose wider stages go through shared
+// memory.
 // ---------------------------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t order_key(float f) {
   if (f != f) return 0u;   // NaN: below every number
@@ -105,8 +116,9 @@ __global__ void __launch_bounds__(kTopkThreads) k_index_topk(const float *__rest
                                                              const uint8_t *__restrict__ cand, int cand_width,
                                                              int cand_block, int K, int offset, int32_t *__restrict__ out) {
   __shared__ unsigned hist[256];
-  __shared__ unsigned s_prefix, s_remain, s_count_gt, s_nvalid, s_eq_taken;
-  __shared__ unsigned long long sel[kTopkMaxK];  // (key << 32) | ~position
+  __shared__ unsigned s_prefix, s_remain, s_count, s_eq_taken;
+  __shared__ unsigned long long sel[kTopkMaxK];   // (key << 32) | ~position
+  __shared__ unsigned long long swap[kTopkThreads];  // second buffer of the shared-memory sort stages
   __shared__ unsigned warp_cnt[32];
   const int64_t row = blockIdx.x;
   const int t = (int)(row % T);
@@ -114,27 +126,35 @@ __global__ void __launch_bounds__(kTopkThreads) k_index_topk(const float *__rest
   const int limit = min((p + 1) / ratio, compress_len);
   const uint8_t *cr = cand ? cand + row * cand_width : nullptr;
   const float *Sr = S + row * Lstride;
-  const int tid = threadIdx.x;
-  int cap = 1;
-  while (cap < K) cap <<= 1;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const unsigned below = (1u << lane) - 1u;
+  auto pack = [](uint32_t key, int j) {
+    return ((unsigned long long)key << 32) | (unsigned long long)(~(uint32_t)j);
+  };
 
-  // count valid positions
-  if (tid == 0) s_nvalid = 0;
-  __syncthreads();
-  {
-    unsigned c = 0;
-    for (int j = tid; j < limit; j += blockDim.x) c += comp_valid(j, limit, cr, cand_block) ? 1u : 0u;
-    atomicAdd(&s_nvalid, c);
-  }
+  // pass 1: count the valid positions, compacting their pairs while they fit
   if (tid == 0) {
+    s_count = 0;
     s_prefix = 0;
     s_remain = (unsigned)K;
   }
   __syncthreads();
-  const unsigned nvalid = s_nvalid;
-  unsigned thr = 0, take_eq = 0;
+  for (int j0 = 0; j0 < limit; j0 += blockDim.x) {
+    const int j = j0 + tid;
+    const bool v = j < limit && comp_valid(j, limit, cr, cand_block);
+    const uint32_t key = v ? order_key(Sr[j]) : 0u;
+    const unsigned bal = __ballot_sync(0xffffffffu, v);
+    unsigned base = 0;
+    if (lane == 0 && bal) base = atomicAdd(&s_count, (unsigned)__popc(bal));
+    base = __shfl_sync(0xffffffffu, base, 0);
+    const unsigned slot = base + __popc(bal & below);
+    if (v && slot < (unsigned)kTopkMaxK) sel[slot] = pack(key, j);
+  }
+  __syncthreads();
+  const unsigned nvalid = s_count;
   const bool all = nvalid <= (unsigned)K;
   if (!all) {
+    unsigned thr, take_eq;
     for (int shift = 24; shift >= 0; shift -= 8) {
       for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0;
       __syncthreads();
@@ -146,39 +166,62 @@ __global__ void __launch_bounds__(kTopkThreads) k_index_topk(const float *__rest
         if ((key & hi_mask) == (prefix & hi_mask)) atomicAdd(&hist[(key >> shift) & 255u], 1u);
       }
       __syncthreads();
-      if (tid == 0) {
-        unsigned remain = s_remain, above = 0;
-        int d = 255;
-        for (; d > 0; --d) {
-          if (above + hist[d] >= remain) break;
-          above += hist[d];
+      if (wid == 0) {
+        // the digit holding the remain-th largest key: lane l scans digits 255-8l down to 248-8l
+        unsigned c[8], tot = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          c[k] = hist[255 - 8 * lane - k];
+          tot += c[k];
         }
-        s_prefix = prefix | ((unsigned)d << shift);
-        s_remain = remain - above;
+        unsigned incl = tot;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const unsigned n = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += n;
+        }
+        const unsigned excl = incl - tot, remain = s_remain;
+        if (excl < remain && remain <= incl) {
+          unsigned above = excl;
+          int d = 255 - 8 * lane;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            d = 255 - 8 * lane - k;
+            if (above + c[k] >= remain) break;
+            above += c[k];
+          }
+          s_prefix = prefix | ((unsigned)d << shift);
+          s_remain = remain - above;
+        }
       }
       __syncthreads();
     }
     thr = s_prefix;
     take_eq = s_remain;  // how many of the keys equal to thr are taken (lowest positions first)
-  }
-  // collect: keys > thr (or every valid one), then the first take_eq equal keys in position order
-  if (tid == 0) {
-    s_count_gt = 0;
-    s_eq_taken = 0;
-  }
-  __syncthreads();
-  for (int j = tid; j < limit; j += blockDim.x) {
-    if (!comp_valid(j, limit, cr, cand_block)) continue;
-    const uint32_t key = order_key(Sr[j]);
-    if (all || key > thr) {
-      const unsigned slot = atomicAdd(&s_count_gt, 1u);
-      if (slot < (unsigned)K) sel[slot] = ((unsigned long long)key << 32) | (unsigned long long)(~(uint32_t)j);
+    // collect the keys above thr (any order), then the first take_eq equal ones in position order
+    if (tid == 0) {
+      s_count = 0;
+      s_eq_taken = 0;
     }
-  }
-  __syncthreads();
-  if (!all) {
-    const unsigned base = s_count_gt;  // == K - take_eq
-    const int lane = tid & 31, wid = tid >> 5, nw = blockDim.x >> 5;
+    __syncthreads();
+    for (int j0 = 0; j0 < limit; j0 += blockDim.x) {
+      const int j = j0 + tid;
+      bool gt = false;
+      uint32_t key = 0;
+      if (j < limit && comp_valid(j, limit, cr, cand_block)) {
+        key = order_key(Sr[j]);
+        gt = key > thr;
+      }
+      const unsigned bal = __ballot_sync(0xffffffffu, gt);
+      unsigned base = 0;
+      if (lane == 0 && bal) base = atomicAdd(&s_count, (unsigned)__popc(bal));
+      base = __shfl_sync(0xffffffffu, base, 0);
+      const unsigned slot = base + __popc(bal & below);
+      if (gt && slot < (unsigned)K) sel[slot] = pack(key, j);
+    }
+    __syncthreads();
+    const unsigned base_eq = s_count;  // == K - take_eq
+    const int nw = blockDim.x >> 5;
     for (int j0 = 0; j0 < limit; j0 += blockDim.x) {
       const int j = j0 + tid;
       bool eq = false;
@@ -188,9 +231,8 @@ __global__ void __launch_bounds__(kTopkThreads) k_index_topk(const float *__rest
       __syncthreads();
       unsigned before = s_eq_taken;
       for (int w = 0; w < wid; ++w) before += warp_cnt[w];
-      before += __popc(ballot & ((1u << lane) - 1u));
-      if (eq && before < take_eq && base + before < (unsigned)K)
-        sel[base + before] = ((unsigned long long)thr << 32) | (unsigned long long)(~(uint32_t)j);
+      before += __popc(ballot & below);
+      if (eq && before < take_eq && base_eq + before < (unsigned)K) sel[base_eq + before] = pack(thr, j);
       __syncthreads();
       if (tid == 0) {
         unsigned tot = 0;
@@ -203,28 +245,53 @@ __global__ void __launch_bounds__(kTopkThreads) k_index_topk(const float *__rest
   }
   __syncthreads();
   const int nsel = all ? (int)nvalid : K;
-  for (int i = nsel + tid; i < cap; i += blockDim.x) sel[i] = 0ull;  // sorts last
-  __syncthreads();
-  // bitonic sort, descending
-  for (int size = 2; size <= cap; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = tid; i < cap; i += blockDim.x) {
-        const int jx = i ^ stride;
-        if (jx > i) {
-          const bool desc = (i & size) == 0;
-          const unsigned long long a = sel[i], c = sel[jx];
-          if (desc ? (a < c) : (a > c)) {
-            sel[i] = c;
-            sel[jx] = a;
+  int cap = 32;
+  while (cap < nsel) cap <<= 1;
+  int32_t *o = out + row * K;
+  auto pos_of = [&](unsigned long long x) { return (int32_t)(~(uint32_t)(x & 0xffffffffull)) + offset; };
+  if (cap <= kTopkThreads) {
+    // bitonic sort, descending: thread i holds element i
+    unsigned long long x = 0ull;  // padding sorts last
+    if (tid < nsel) x = sel[tid];
+    int nb = 0;
+    for (int size = 2; size <= cap; size <<= 1) {
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        unsigned long long y;
+        if (stride >= 32) {
+          unsigned long long *bp = nb ? swap : sel;
+          if (tid < cap) bp[tid] = x;
+          __syncthreads();
+          y = tid < cap ? bp[tid ^ stride] : 0ull;
+          nb ^= 1;  // the next shared stage writes the other buffer: no second barrier needed
+        } else {
+          y = __shfl_xor_sync(0xffffffffu, x, stride);
+        }
+        const bool keep_max = ((tid & size) == 0) == ((tid & stride) == 0);
+        x = keep_max ? (x > y ? x : y) : (x < y ? x : y);
+      }
+    }
+    for (int k = tid; k < K; k += blockDim.x) o[k] = (k == tid && k < nsel) ? pos_of(x) : -1;
+  } else {
+    for (int i = nsel + tid; i < cap; i += blockDim.x) sel[i] = 0ull;
+    __syncthreads();
+    for (int size = 2; size <= cap; size <<= 1) {
+      for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        for (int i = tid; i < cap; i += blockDim.x) {
+          const int jx = i ^ stride;
+          if (jx > i) {
+            const bool desc = (i & size) == 0;
+            const unsigned long long a = sel[i], c = sel[jx];
+            if (desc ? (a < c) : (a > c)) {
+              sel[i] = c;
+              sel[jx] = a;
+            }
           }
         }
+        __syncthreads();
       }
-      __syncthreads();
     }
+    for (int k = tid; k < K; k += blockDim.x) o[k] = k < nsel ? pos_of(sel[k]) : -1;
   }
-  int32_t *o = out + row * K;
-  for (int k = tid; k < K; k += blockDim.x)
-    o[k] = k < nsel ? (int32_t)(~(uint32_t)(sel[k] & 0xffffffffull)) + offset : -1;
 }
 
 cudaError_t launch_index_topk(const float *S, int B, int T, int start_pos, int Lstride, int compress_len, int ratio,

@@ -181,6 +181,20 @@ def test_index_scores(csa, orc, B, T, start, L, clen, ratio, keep, cb):
         assert (np.abs(a - b) <= tol).all()
 
 
+@pytest.mark.parametrize("Hi,B,T,start,L,clen,ratio", [(64, 2, 7, 200, 256, 200, 2), (16, 1, 20, 0, 300, 300, 1)])
+def test_index_scores_head_counts(csa, orc, Hi, B, T, start, L, clen, ratio):
+    """Other indexer head counts: the query groups of the tensor-core kernel hold 256 / Hi queries."""
+    rng = np.random.default_rng(60 + Hi)
+    qI, wI, KI, pos, cand, S = _index_case(orc, rng, B, T, start, Hi, 128, L, clen, ratio, 0, 64)
+    Sd = torch.full((B * T, L), float("nan"), device="cuda")
+    csa.index_scores(to_dev(qI), to_dev(wI), to_dev(KI), B, T, start, clen, ratio, Sd, None, 64)
+    got = to_np(Sd)
+    valid = np.isfinite(S)
+    assert np.isnan(got[~valid]).all()
+    tol = 1e-3 * np.abs(S[valid]) + 1e-3 * np.abs(S[valid]).max()
+    assert (np.abs(got[valid].astype(np.float64) - S[valid]) <= tol).all()
+
+
 @pytest.mark.parametrize("B,T,start,L,clen,ratio,keep,cb,K", [
     (4, 1, 1000, 512, 500, 2, 0.5, 64, 512),
     (1, 300, 0, 1024, 1024, 4, 0, 64, 512),
