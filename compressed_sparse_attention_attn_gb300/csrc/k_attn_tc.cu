@@ -526,9 +526,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
   if (tid == 0 && *abort_flag) atomicOr(P.status, kStatusTimeout);
 }
 
-// Merge of the split shares: block (query, 8 heads), one thread per 16-byte vector pair.  The
-// weights e^{m_c - M} l_c / den put each share O_c / l_c back on the common scale, with the sink in
-// den; shares of CTAs that found nothing (l_c = 0) weigh 0.
+// Merge of the split shares: block (query, 8 heads), one warp per head, two 16-byte vectors per
+// thread.  The weights e^{m_c - M} l_c / den put each share O_c / l_c back on the common scale, with
+// the sink in den; every thread forms its head's weights itself (no barrier), and shares of CTAs
+// that found nothing (l_c = 0) weigh 0 and are not read.
 constexpr int kCombHeads = 8;
 constexpr int kCombThreads = 256;
 struct CombineParams {
@@ -542,54 +543,54 @@ struct CombineParams {
 };
 
 __global__ void __launch_bounds__(kCombThreads) k_attn_combine(const __grid_constant__ CombineParams C) {
-  __shared__ float wgt[kMaxTiles][kCombHeads];
   const int64_t row = blockIdx.x;
   const int h0 = blockIdx.y * kCombHeads, tid = threadIdx.x;
-  if (tid < kCombHeads) {
-    const int h = h0 + tid;
-    const float s2 = C.sink[h] * 1.4426950408889634f;
-    float M = s2;
-    for (int c = 0; c < C.nsplit; ++c) {
-      const float *ml = C.part_ml + ((row * C.nsplit + c) * C.H + h) * 2;
-      if (ml[1] > 0.f) M = fmaxf(M, ml[0]);
-    }
-    float den = exp2f(s2 - M), w[kMaxTiles];
-#pragma unroll
-    for (int c = 0; c < kMaxTiles; ++c) {
-      w[c] = 0.f;
-      if (c < C.nsplit) {
-        const float *ml = C.part_ml + ((row * C.nsplit + c) * C.H + h) * 2;
-        w[c] = ml[1] > 0.f ? ml[1] * exp2f(ml[0] - M) : 0.f;
-        den += w[c];
-      }
-    }
-#pragma unroll
-    for (int c = 0; c < kMaxTiles; ++c) wgt[c][tid] = w[c] / den;
-  }
-  __syncthreads();
   const int t = (int)(row % C.T);
   const float2 *tp = C.o_rot ? reinterpret_cast<const float2 *>(C.tab) + (int64_t)(C.start_pos + t) * (C.rd >> 1)
                              : nullptr;
-  constexpr int kPer = kCombHeads * (HD / 8) / kCombThreads;  // vectors per thread
+  constexpr int kPer = kCombHeads * (HD / 8) / kCombThreads;  // consecutive vectors per thread
+  static_assert((HD / 8) % kPer == 0, "a thread's vectors belong to one head");
+  const int h = h0 + (tid * kPer) / (HD / 8);
+  // this head's weights e^{m_c - M} l_c / den, computed by each of its threads (same addresses)
+  const float s2 = C.sink[h] * 1.4426950408889634f;
+  float mc[kMaxTiles], lc[kMaxTiles];
+  float M = s2;
+#pragma unroll
+  for (int c = 0; c < kMaxTiles; ++c) {
+    mc[c] = -INFINITY;
+    lc[c] = 0.f;
+    if (c < C.nsplit) {
+      const float2 ml = *reinterpret_cast<const float2 *>(C.part_ml + ((row * C.nsplit + c) * C.H + h) * 2);
+      mc[c] = ml.x;
+      lc[c] = ml.y;
+      if (lc[c] > 0.f) M = fmaxf(M, mc[c]);
+    }
+  }
+  float den = exp2f(s2 - M), w[kMaxTiles];
+#pragma unroll
+  for (int c = 0; c < kMaxTiles; ++c) {
+    w[c] = lc[c] > 0.f ? lc[c] * exp2f(mc[c] - M) : 0.f;
+    den += w[c];
+  }
+  const float inv = 1.0f / den;
   uint4 u[kPer][kMaxTiles];
 #pragma unroll
   for (int k = 0; k < kPer; ++k) {  // every share of every vector in flight together
-    const int it = tid + k * kCombThreads, hl = it >> 6, d0 = (it & 63) * 8;
+    const int d0 = ((tid * kPer + k) % (HD / 8)) * 8;
 #pragma unroll
     for (int c = 0; c < kMaxTiles; ++c) {
       u[k][c] = make_uint4(0u, 0u, 0u, 0u);
-      if (c < C.nsplit && wgt[c][hl] != 0.f)
-        u[k][c] = *reinterpret_cast<const uint4 *>(C.part_o + ((row * C.nsplit + c) * C.H + h0 + hl) * (int64_t)HD +
-                                                   d0);
+      if (w[c] != 0.f)
+        u[k][c] = *reinterpret_cast<const uint4 *>(C.part_o + ((row * C.nsplit + c) * C.H + h) * (int64_t)HD + d0);
     }
   }
 #pragma unroll
   for (int k = 0; k < kPer; ++k) {
-    const int it = tid + k * kCombThreads, hl = it >> 6, d0 = (it & 63) * 8;
+    const int d0 = ((tid * kPer + k) % (HD / 8)) * 8;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int c = 0; c < kMaxTiles; ++c) {
-      const float wv = wgt[c][hl];
+      const float wv = w[c] * inv;
       const __nv_bfloat162 *pv = reinterpret_cast<const __nv_bfloat162 *>(&u[k][c]);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -601,7 +602,7 @@ __global__ void __launch_bounds__(kCombThreads) k_attn_combine(const __grid_cons
     __nv_bfloat162 *po = reinterpret_cast<__nv_bfloat162 *>(&ob);
 #pragma unroll
     for (int q = 0; q < 4; ++q) po[q] = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
-    store_out(C.o, C.o_rot, (row * C.H + h0 + hl) * (int64_t)HD + d0, d0, HD - C.rd, tp, ob);
+    store_out(C.o, C.o_rot, (row * C.H + h) * (int64_t)HD + d0, d0, HD - C.rd, tp, ob);
   }
 }
 

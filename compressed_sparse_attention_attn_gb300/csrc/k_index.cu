@@ -250,24 +250,31 @@ __global__ void __launch_bounds__(kTopkThreads) k_index_topk(const float *__rest
   int32_t *o = out + row * K;
   auto pos_of = [&](unsigned long long x) { return (int32_t)(~(uint32_t)(x & 0xffffffffull)) + offset; };
   if (cap <= kTopkThreads) {
-    // bitonic sort, descending: thread i holds element i
+    // bitonic sort, descending: thread i holds element i; warps past the padded length only keep
+    // the shared stages' barriers
+    const bool holds = (tid & ~31) < cap;
     unsigned long long x = 0ull;  // padding sorts last
     if (tid < nsel) x = sel[tid];
     int nb = 0;
     for (int size = 2; size <= cap; size <<= 1) {
-      for (int stride = size >> 1; stride > 0; stride >>= 1) {
-        unsigned long long y;
-        if (stride >= 32) {
-          unsigned long long *bp = nb ? swap : sel;
-          if (tid < cap) bp[tid] = x;
-          __syncthreads();
-          y = tid < cap ? bp[tid ^ stride] : 0ull;
-          nb ^= 1;  // the next shared stage writes the other buffer: no second barrier needed
-        } else {
-          y = __shfl_xor_sync(0xffffffffu, x, stride);
+      // stages of stride 32 and up go through shared memory, the rest are shuffles
+      for (int stride = size >> 1; stride >= 32; stride >>= 1) {
+        unsigned long long *bp = nb ? swap : sel;
+        if (tid < cap) bp[tid] = x;
+        __syncthreads();
+        if (tid < cap) {
+          const unsigned long long y = bp[tid ^ stride];
+          const bool keep_max = ((tid & size) == 0) == ((tid & stride) == 0);
+          x = keep_max ? (x > y ? x : y) : (x < y ? x : y);
         }
-        const bool keep_max = ((tid & size) == 0) == ((tid & stride) == 0);
-        x = keep_max ? (x > y ? x : y) : (x < y ? x : y);
+        nb ^= 1;  // the next shared stage writes the other buffer: no second barrier needed
+      }
+      if (holds) {
+        for (int stride = min(size >> 1, 16); stride > 0; stride >>= 1) {
+          const unsigned long long y = __shfl_xor_sync(0xffffffffu, x, stride);
+          const bool keep_max = ((tid & size) == 0) == ((tid & stride) == 0);
+          x = keep_max ? (x > y ? x : y) : (x < y ? x : y);
+        }
       }
     }
     for (int k = tid; k < K; k += blockDim.x) o[k] = (k == tid && k < nsel) ? pos_of(x) : -1;
