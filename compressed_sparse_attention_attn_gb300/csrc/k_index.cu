@@ -94,12 +94,14 @@ cudaError_t launch_index_scores(const bf16 *qI, const float *wI, const bf16 *KI,
 
 // ---------------------------------------------------------------------------------------------
 // Top-k: one CTA per query.  Scores map to order-preserving 32-bit keys (-0 folded onto +0, NaN
-// below every number).  A first pass compacts the valid positions' (key, position) pairs; when
-// they are at most K, all are taken.  Otherwise a 4-pass radix select over the valid positions
-// finds the K-th largest key: keys above it are taken, and of the keys equal to it the lowest
-// positions.  The chosen pairs are then sorted (key descending, position ascending) by a bitonic
-// network whose stages within a warp run on shuffles and whose wider stages go through shared
-// memory.
+// below every number) and each valid position j to the 64-bit value (key << 32) | ~j, so that the
+// values are distinct and larger means selected first (higher score, then lower position).  A first
+// pass compacts the valid values into shared memory; when they are at most K, all are taken.
+// Otherwise a radix select on the 64-bit values (8 bits per pass, warp-aggregated histograms, over
+// shared memory) finds the K-th largest, and the values at or above it are taken.  (A query with more
+// valid positions than shared memory holds runs the same passes over its scores in global memory.)
+// The chosen values are then sorted descending by a bitonic network whose stages within a warp run
+// on shuffles and whose wider stages go through shared memory.
 // ---------------------------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t order_key(float f) {
   if (f != f) return 0u;   // NaN: below every number
@@ -110,16 +112,24 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 
 constexpr int kTopkThreads = 1024;
 constexpr int kTopkMaxK = 2048;
+constexpr int kTopkCap = 12288;  // valid positions of one query held in shared memory (96 KiB at most)
+// dynamic shared memory for candidate buffers of `cap` values
+constexpr size_t topk_smem(int cap) { return (size_t)(cap + kTopkMaxK + kTopkThreads) * 8; }
 
-__global__ void __launch_bounds__(kTopkThreads) k_index_topk(const float *__restrict__ S, int T, int start_pos,
+__global__ void __launch_bounds__(kTopkThreads, 2) k_index_topk(const float *__restrict__ S, int T, int start_pos,
                                                              int Lstride, int compress_len, int ratio,
                                                              const uint8_t *__restrict__ cand, int cand_width,
-                                                             int cand_block, int K, int offset, int32_t *__restrict__ out) {
+                                                             int cand_block, int K, int offset, int32_t *__restrict__ out,
+                                                             int cap_vals) {
+  extern __shared__ unsigned long long tk_smem[];
+  unsigned long long *vals = tk_smem;                 // [cap_vals] the valid values
+  unsigned long long *chosen = vals + cap_vals;       // [kTopkMaxK] the selection
+  unsigned long long *swap = chosen + kTopkMaxK;      // [kTopkThreads] sort buffer
   __shared__ unsigned hist[256];
-  __shared__ unsigned s_prefix, s_remain, s_count, s_eq_taken;
-  __shared__ unsigned long long sel[kTopkMaxK];   // (key << 32) | ~position
-  __shared__ unsigned long long swap[kTopkThreads];  // second buffer of the shared-memory sort stages
-  __shared__ unsigned warp_cnt[32];
+  __shared__ unsigned s_count, s_nchosen;
+  __shared__ unsigned long long s_prefix;
+  __shared__ unsigned s_remain, s_done;
+  __shared__ int s_shift;
   const int64_t row = blockIdx.x;
   const int t = (int)(row % T);
   const int p = start_pos + t;
@@ -128,46 +138,67 @@ __global__ void __launch_bounds__(kTopkThreads) k_index_topk(const float *__rest
   const float *Sr = S + row * Lstride;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   const unsigned below = (1u << lane) - 1u;
-  auto pack = [](uint32_t key, int j) {
-    return ((unsigned long long)key << 32) | (unsigned long long)(~(uint32_t)j);
+  auto value_at = [&](int j) {
+    return ((unsigned long long)order_key(Sr[j]) << 32) | (unsigned long long)(~(uint32_t)j);
+  };
+  // append v (where take) to buf[cap] through counter cnt: one atomic per warp
+  auto append = [&](bool take, unsigned long long v, unsigned *cnt, unsigned long long *buf, unsigned cap) {
+    const unsigned bal = __ballot_sync(0xffffffffu, take);
+    unsigned base = 0;
+    if (lane == 0 && bal) base = atomicAdd(cnt, (unsigned)__popc(bal));
+    base = __shfl_sync(0xffffffffu, base, 0);
+    const unsigned slot = base + __popc(bal & below);
+    if (take && slot < cap) buf[slot] = v;
   };
 
-  // pass 1: count the valid positions, compacting their pairs while they fit
+  // pass 1: count the valid positions, compacting their values while they fit
   if (tid == 0) {
     s_count = 0;
-    s_prefix = 0;
+    s_nchosen = 0;
+    s_prefix = 0ull;
     s_remain = (unsigned)K;
+    s_done = 0;
+    s_shift = 0;
   }
   __syncthreads();
   for (int j0 = 0; j0 < limit; j0 += blockDim.x) {
     const int j = j0 + tid;
     const bool v = j < limit && comp_valid(j, limit, cr, cand_block);
-    const uint32_t key = v ? order_key(Sr[j]) : 0u;
-    const unsigned bal = __ballot_sync(0xffffffffu, v);
-    unsigned base = 0;
-    if (lane == 0 && bal) base = atomicAdd(&s_count, (unsigned)__popc(bal));
-    base = __shfl_sync(0xffffffffu, base, 0);
-    const unsigned slot = base + __popc(bal & below);
-    if (v && slot < (unsigned)kTopkMaxK) sel[slot] = pack(key, j);
+    append(v, v ? value_at(j) : 0ull, &s_count, vals, (unsigned)cap_vals);
   }
   __syncthreads();
   const unsigned nvalid = s_count;
   const bool all = nvalid <= (unsigned)K;
+  const bool in_smem = nvalid <= (unsigned)cap_vals;
+  const int n_iter = in_smem ? (int)nvalid : limit;  // candidates: vals[0..nvalid) or positions 0..limit
+  unsigned long long *sorted = vals;
   if (!all) {
-    unsigned thr, take_eq;
-    for (int shift = 24; shift >= 0; shift -= 8) {
+    // radix select of the K-th largest value, 8 bits per pass from the top
+    for (int shift = 56; shift >= 0; shift -= 8) {
       for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0;
       __syncthreads();
-      const unsigned prefix = s_prefix;
-      const unsigned hi_mask = shift == 24 ? 0u : (0xffffffffu << (shift + 8));
-      for (int j = tid; j < limit; j += blockDim.x) {
-        if (!comp_valid(j, limit, cr, cand_block)) continue;
-        const uint32_t key = order_key(Sr[j]);
-        if ((key & hi_mask) == (prefix & hi_mask)) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+      const unsigned long long prefix = s_prefix;
+      const unsigned long long hi_mask = shift == 56 ? 0ull : (~0ull << (shift + 8));
+      for (int i0 = 0; i0 < n_iter; i0 += blockDim.x) {
+        const int i = i0 + tid;
+        int bin = 256 + lane;  // no bin: a value of every lane of its own
+        if (i < n_iter) {
+          bool ok = true;
+          unsigned long long v = 0ull;
+          if (in_smem) {
+            v = vals[i];
+          } else {
+            ok = comp_valid(i, limit, cr, cand_block);
+            if (ok) v = value_at(i);
+          }
+          if (ok && (v & hi_mask) == (prefix & hi_mask)) bin = (int)((v >> shift) & 255u);
+        }
+        const unsigned peers = __match_any_sync(0xffffffffu, bin);
+        if (bin < 256 && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], (unsigned)__popc(peers));
       }
       __syncthreads();
       if (wid == 0) {
-        // the digit holding the remain-th largest key: lane l scans digits 255-8l down to 248-8l
+        // the digit holding the remain-th largest value: lane l scans digits 255-8l down to 248-8l
         unsigned c[8], tot = 0;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
@@ -184,66 +215,45 @@ __global__ void __launch_bounds__(kTopkThreads) k_index_topk(const float *__rest
         if (excl < remain && remain <= incl) {
           unsigned above = excl;
           int d = 255 - 8 * lane;
+          unsigned cd = 0;
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             d = 255 - 8 * lane - k;
-            if (above + c[k] >= remain) break;
-            above += c[k];
+            cd = c[k];
+            if (above + cd >= remain) break;
+            above += cd;
           }
-          s_prefix = prefix | ((unsigned)d << shift);
+          s_prefix = prefix | ((unsigned long long)d << shift);
           s_remain = remain - above;
+          s_shift = shift;
+          if (cd == remain - above) s_done = 1;  // every value with this prefix is taken
         }
       }
       __syncthreads();
+      if (s_done) break;
     }
-    thr = s_prefix;
-    take_eq = s_remain;  // how many of the keys equal to thr are taken (lowest positions first)
-    // collect the keys above thr (any order), then the first take_eq equal ones in position order
-    if (tid == 0) {
-      s_count = 0;
-      s_eq_taken = 0;
+    // the selection: values above the prefix at the final digit, and every value equal to it there
+    const int sh = s_shift;
+    const unsigned long long thr = s_prefix >> sh;
+    for (int i0 = 0; i0 < n_iter; i0 += blockDim.x) {
+      const int i = i0 + tid;
+      bool take = false;
+      unsigned long long v = 0ull;
+      if (i < n_iter) {
+        bool ok = true;
+        if (in_smem) {
+          v = vals[i];
+        } else {
+          ok = comp_valid(i, limit, cr, cand_block);
+          if (ok) v = value_at(i);
+        }
+        take = ok && (v >> sh) >= thr;
+      }
+      append(take, v, &s_nchosen, chosen, (unsigned)kTopkMaxK);
     }
     __syncthreads();
-    for (int j0 = 0; j0 < limit; j0 += blockDim.x) {
-      const int j = j0 + tid;
-      bool gt = false;
-      uint32_t key = 0;
-      if (j < limit && comp_valid(j, limit, cr, cand_block)) {
-        key = order_key(Sr[j]);
-        gt = key > thr;
-      }
-      const unsigned bal = __ballot_sync(0xffffffffu, gt);
-      unsigned base = 0;
-      if (lane == 0 && bal) base = atomicAdd(&s_count, (unsigned)__popc(bal));
-      base = __shfl_sync(0xffffffffu, base, 0);
-      const unsigned slot = base + __popc(bal & below);
-      if (gt && slot < (unsigned)K) sel[slot] = pack(key, j);
-    }
-    __syncthreads();
-    const unsigned base_eq = s_count;  // == K - take_eq
-    const int nw = blockDim.x >> 5;
-    for (int j0 = 0; j0 < limit; j0 += blockDim.x) {
-      const int j = j0 + tid;
-      bool eq = false;
-      if (j < limit && comp_valid(j, limit, cr, cand_block)) eq = order_key(Sr[j]) == thr;
-      const unsigned ballot = __ballot_sync(0xffffffffu, eq);
-      if (lane == 0) warp_cnt[wid] = __popc(ballot);
-      __syncthreads();
-      unsigned before = s_eq_taken;
-      for (int w = 0; w < wid; ++w) before += warp_cnt[w];
-      before += __popc(ballot & below);
-      if (eq && before < take_eq && base_eq + before < (unsigned)K) sel[base_eq + before] = pack(thr, j);
-      __syncthreads();
-      if (tid == 0) {
-        unsigned tot = 0;
-        for (int w = 0; w < nw; ++w) tot += warp_cnt[w];
-        s_eq_taken += tot;
-      }
-      __syncthreads();
-      if (s_eq_taken >= take_eq) break;
-    }
+    sorted = chosen;
   }
-  __syncthreads();
   const int nsel = all ? (int)nvalid : K;
   int cap = 32;
   while (cap < nsel) cap <<= 1;
@@ -254,12 +264,12 @@ __global__ void __launch_bounds__(kTopkThreads) k_index_topk(const float *__rest
     // the shared stages' barriers
     const bool holds = (tid & ~31) < cap;
     unsigned long long x = 0ull;  // padding sorts last
-    if (tid < nsel) x = sel[tid];
+    if (tid < nsel) x = sorted[tid];
     int nb = 0;
     for (int size = 2; size <= cap; size <<= 1) {
       // stages of stride 32 and up go through shared memory, the rest are shuffles
       for (int stride = size >> 1; stride >= 32; stride >>= 1) {
-        unsigned long long *bp = nb ? swap : sel;
+        unsigned long long *bp = nb ? swap : chosen;  // alternate buffers: one barrier per stage
         if (tid < cap) bp[tid] = x;
         __syncthreads();
         if (tid < cap) {
@@ -267,7 +277,7 @@ __global__ void __launch_bounds__(kTopkThreads) k_index_topk(const float *__rest
           const bool keep_max = ((tid & size) == 0) == ((tid & stride) == 0);
           x = keep_max ? (x > y ? x : y) : (x < y ? x : y);
         }
-        nb ^= 1;  // the next shared stage writes the other buffer: no second barrier needed
+        nb ^= 1;
       }
       if (holds) {
         for (int stride = min(size >> 1, 16); stride > 0; stride >>= 1) {
@@ -279,7 +289,8 @@ __global__ void __launch_bounds__(kTopkThreads) k_index_topk(const float *__rest
     }
     for (int k = tid; k < K; k += blockDim.x) o[k] = (k == tid && k < nsel) ? pos_of(x) : -1;
   } else {
-    for (int i = nsel + tid; i < cap; i += blockDim.x) sel[i] = 0ull;
+    unsigned long long *a = sorted;
+    for (int i = nsel + tid; i < cap; i += blockDim.x) a[i] = 0ull;
     __syncthreads();
     for (int size = 2; size <= cap; size <<= 1) {
       for (int stride = size >> 1; stride > 0; stride >>= 1) {
@@ -287,17 +298,17 @@ __global__ void __launch_bounds__(kTopkThreads) k_index_topk(const float *__rest
           const int jx = i ^ stride;
           if (jx > i) {
             const bool desc = (i & size) == 0;
-            const unsigned long long a = sel[i], c = sel[jx];
-            if (desc ? (a < c) : (a > c)) {
-              sel[i] = c;
-              sel[jx] = a;
+            const unsigned long long u = a[i], w = a[jx];
+            if (desc ? (u < w) : (u > w)) {
+              a[i] = w;
+              a[jx] = u;
             }
           }
         }
         __syncthreads();
       }
     }
-    for (int k = tid; k < K; k += blockDim.x) o[k] = k < nsel ? pos_of(sel[k]) : -1;
+    for (int k = tid; k < K; k += blockDim.x) o[k] = k < nsel ? pos_of(a[k]) : -1;
   }
 }
 
@@ -306,8 +317,19 @@ cudaError_t launch_index_topk(const float *S, int B, int T, int start_pos, int L
                               cudaStream_t s) {
   if (B * T <= 0) return cudaSuccess;
   if (K > kTopkMaxK) return cudaErrorInvalidValue;
-  k_index_topk<<<B * T, kTopkThreads, 0, s>>>(S, T, start_pos, Lstride, compress_len, ratio, cand, cand_width,
-                                              cand_block, K, offset, out);
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e =
+        cudaFuncSetAttribute(k_index_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)topk_smem(kTopkCap));
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  // room for the largest causal limit of the launch (the last query's), so that short ones keep
+  // two CTAs per SM; the sort buffers need at least as many values as the sort's padded length
+  const int max_limit = std::min((start_pos + T) / std::max(ratio, 1), compress_len);
+  const int cap = std::min(kTopkCap, std::max(max_limit, kTopkMaxK));
+  k_index_topk<<<B * T, kTopkThreads, topk_smem(cap), s>>>(S, T, start_pos, Lstride, compress_len, ratio, cand,
+                                                           cand_width, cand_block, K, offset, out, cap);
   return cudaGetLastError();
 }
 

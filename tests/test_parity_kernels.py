@@ -200,6 +200,8 @@ def test_index_scores_head_counts(csa, orc, Hi, B, T, start, L, clen, ratio):
     (1, 300, 0, 1024, 1024, 4, 0, 64, 512),
     (2, 1, 65535, 16384, 16384, 4, 64, 64, 512),
     (3, 1, 40, 64, 7, 1, 0, 8, 16),
+    (1, 1, 65535, 16384, 16384, 4, 0, 64, 512),    # more valid positions than shared memory holds
+    (1, 2, 8191, 4096, 4096, 2, 0, 64, 2048),      # K above the one-element-per-thread sort
 ])
 def test_index_topk_bit_exact(csa, orc, B, T, start, L, clen, ratio, keep, cb, K):
     rng = np.random.default_rng(7 + T)
