@@ -522,16 +522,24 @@ int attn_v41_forward(csa_ctx *ctx, const csa_layer_weights *w, csa_layer_state *
                                 lin(qr, g.q_rank, g.q_rank, w->idx_wq_b, Hi * dI, qI, Hi * dI, 1)};
     STEP(csa::launch_linear(pq, idx_src ? 2 : 1, ctx->ws, ctx->ws_bytes, ctx->num_sms, ctx->status, s), "proj qr");
   }
-  STEP(csa::launch_rope(q, (int64_t)NT * H, hd, rd, pos_q, tab, ctx->tab_rows, 0, ctx->status, s), "rope q");
-  // the compressed selection
-  const int32_t *idx_b = nullptr;
-  int nb = 0;
-  const bf16 *rows_b = nullptr;
-  int b_len = 0;
-  int64_t b_stride = 0;
+  // the sparse attention's arguments: the selection's buffers are known before the index stages fill
+  // them; rows_a = the window ring at decode, the chunk's own kv rows at prefill
   const int rows_a_len = decode ? W : T;
+  const int K = r.ratio > 0 ? g.index_topk : 0;
+  csa::AttnArgs a{q, B, T, H, hd,
+                  decode ? (const bf16 *)st->window : kv, decode ? (int64_t)W * hd : (int64_t)T * hd, rows_a_len,
+                  r.ratio > 0 ? (const bf16 *)sh->compress_kv : nullptr,
+                  r.ratio > 0 ? (int64_t)sh->compress_stride * hd : 0, r.ratio > 0 ? sh->compress_len : 0,
+                  win_idx, W, r.ratio > 0 ? sh->topk_idxs : nullptr, K, w->sink, (float)(1.0 / std::sqrt((double)hd)),
+                  o, ctx->o_rot, rd, start_pos, tab, ctx->status};
+  // RoPE on q: inside the tensor-core attention kernel (on its own copy of q), unless the caller wants
+  // the turned q itself in its debug buffer or the attention runs on the CUDA-core path
+  a.rope_q = (dbg && dbg->q) ? 0 : 1;
+  if (a.rope_q && !csa::sparse_attn_tc_supported(a)) a.rope_q = 0;
+  if (!a.rope_q)
+    STEP(csa::launch_rope(q, (int64_t)NT * H, hd, rd, pos_q, tab, ctx->tab_rows, 0, ctx->status, s), "rope q");
+  // the compressed selection
   if (r.ratio > 0) {
-    const int K = g.index_topk;
     if (r.is_index_source) {
       float *S = dbg && dbg->scores ? dbg->scores : ctx->scores;
       const uint8_t *cand = r.uses_candidates ? sh->candidates : nullptr;
@@ -544,22 +552,11 @@ int attn_v41_forward(csa_ctx *ctx, const csa_layer_weights *w, csa_layer_state *
            "index topk");
       sh->has_topk = 1;
     }
-    idx_b = sh->topk_idxs;
-    nb = K;
-    rows_b = (const bf16 *)sh->compress_kv;
-    b_len = sh->compress_len;
-    b_stride = (int64_t)sh->compress_stride * hd;
     if (dbg && dbg->idx)
       COPY(cudaMemcpy2DAsync(dbg->idx + W, sizeof(int32_t) * (W + K), sh->topk_idxs, sizeof(int32_t) * K,
                              sizeof(int32_t) * K, NT, cudaMemcpyDeviceToDevice, s),
            "debug idx");
   }
-  // sparse attention over [rows_a; rows_b] with the inverse rotation of the output fused
-  csa::AttnArgs a{q, B, T, H, hd,
-                  decode ? (const bf16 *)st->window : kv, decode ? (int64_t)W * hd : (int64_t)T * hd, rows_a_len,
-                  rows_b, b_stride, b_len,
-                  win_idx, W, idx_b, nb, w->sink, (float)(1.0 / std::sqrt((double)hd)), o, ctx->o_rot, rd, start_pos,
-                  tab, ctx->status};
   // the window selection in the debug buffer is strided; pass the stride through idx_a's row length
   if (idx_stride != W) {
     // compact copy of the window columns for the kernel

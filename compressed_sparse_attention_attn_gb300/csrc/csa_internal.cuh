@@ -114,12 +114,17 @@ struct AttnArgs {
   int rd, start_pos;
   const float *tab;
   int *status;
+  // 1: q has not been rotated yet; the kernel turns the last rd features of each head by the
+  // query's position (RoPE, tab) on its own copy before the scores.  0: q is used as given.
+  int rope_q = 0;
 };
 // Tensor-core kernel where the shapes allow (head_dim 512, heads in groups of 64), else the SIMT one.
 // ws: the tensor-core path's per-split shares (after the GEMM counters).  *kernels (if given): the
 // number of kernels launched.
 cudaError_t launch_sparse_attn(const AttnArgs &a, float *ws, size_t ws_bytes, int num_sms, cudaStream_t s,
                                int *kernels = nullptr);
+// Whether the tensor-core kernel takes these arguments (it alone applies rope_q, for rd <= 64).
+bool sparse_attn_tc_supported(const AttnArgs &a);
 
 // Record the calling thread's last error (attn_v41_last_error) and return `code`.
 int set_error(int code, const char *fmt, ...);

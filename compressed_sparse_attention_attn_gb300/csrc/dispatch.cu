@@ -48,6 +48,7 @@ cudaError_t launch_sparse_attn(const AttnArgs &a, float *ws, size_t ws_bytes, in
   if (sparse_attn_tc_supported(a)) {
     e = launch_sparse_attn_tc(a, ws, ws_bytes, num_sms, s, &k);
   } else {
+    if (a.rope_q) return cudaErrorInvalidValue;  // the CUDA-core kernel takes q as given
     e = launch_sparse_attn_simt(a, s);
     k = a.B * a.T > 0 ? 1 : 0;
   }

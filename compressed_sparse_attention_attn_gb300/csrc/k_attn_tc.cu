@@ -12,8 +12,8 @@
 //   S^T[r][h] = sum_d G[r][d] q[h][d]       (M = 128 rows, N = 64 heads, K = 512; G and q K-major)
 //   softmax step: a running maximum per head, raised only when a tile's maximum exceeds it by more
 //   than 2^8 (the accumulated output and sum are then rescaled), p = exp(S - m) rounded to bf16 in
-//   shared memory (K-major [64][128]); the maxima and sums over the rows are butterfly reductions
-//   that leave each lane with two heads
+//   shared memory (K-major [64][128]); eight warps share it (a TMEM lane quadrant and 32 heads each),
+//   and the maxima and sums over the rows are butterfly reductions that leave each lane one head
 //   O^T[d][h] += sum_r G[r][d] P[h][r]      (M = 4 x 128 features, N = 64, K = 128 rows; the same tile
 //                                            read as an MN-major operand)
 // When a query's tiles are split over several CTAs (decode: few queries, so one tile per CTA keeps
@@ -24,9 +24,10 @@
 // shared memory and written with 16-byte stores as bf16, together with the inverse rotation of its
 // last rope_dim features at the query's position.
 //
-// Warps 0-3: softmax and epilogue (TMEM lane quadrant = warp); warps 4-7: index pass and row
-// copies; warp 8: TMEM allocation and MMA issue; all nine warps write the result or the share.
-// Every mbarrier wait is time-bounded.
+// Warps 0-7: softmax and staging of the result; warps 4-7 also run the index pass and the row
+// copies, each owning two 64-feature K-blocks of the tile, which it refills for the next tile as
+// soon as the P.V chunk reading them has completed; warp 8: TMEM allocation and MMA issue; all nine
+// warps write the result or the share.  Every mbarrier wait is time-bounded.
 #include "csa_internal.cuh"
 #include "tc_ptx.cuh"
 
@@ -64,6 +65,7 @@ struct Params {
   int rd, start_pos;
   const float *tab;
   int *status;
+  int rope_q;       // turn q's last rd features by RoPE in shared memory before the scores
   int ntiles;       // tiles of the index list
   int tpc, nsplit;  // tiles per CTA, CTAs per query
   bf16 *part_o;     // [NT][nsplit][H][512]  O_c / l_c of each split
@@ -91,64 +93,40 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// 32 lanes x 64 consecutive columns, then the wait; the registers are operands of the wait so
-// that no use of them can be scheduled before it.
-__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[HG]) {
-  uint32_t r[64];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {"
-      "%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, "
-      "%32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, "
-      "%48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63"
-      "}, [%64];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
-        "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
-        "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
-        "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
-        "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
-      : "r"(taddr));
+// 32 lanes x 32 consecutive columns, then the wait (the registers are operands of the wait)
+__device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  tc::tmem_ld32(taddr, r);
   asm volatile("tcgen05.wait::ld.sync.aligned;"
                : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
                  "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]),
                  "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
-                 "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]),
-                 "+r"(r[32]), "+r"(r[33]), "+r"(r[34]), "+r"(r[35]), "+r"(r[36]), "+r"(r[37]), "+r"(r[38]), "+r"(r[39]),
-                 "+r"(r[40]), "+r"(r[41]), "+r"(r[42]), "+r"(r[43]), "+r"(r[44]), "+r"(r[45]), "+r"(r[46]), "+r"(r[47]),
-                 "+r"(r[48]), "+r"(r[49]), "+r"(r[50]), "+r"(r[51]), "+r"(r[52]), "+r"(r[53]), "+r"(r[54]), "+r"(r[55]),
-                 "+r"(r[56]), "+r"(r[57]), "+r"(r[58]), "+r"(r[59]), "+r"(r[60]), "+r"(r[61]), "+r"(r[62]), "+r"(r[63])
+                 "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
                :
                : "memory");
 #pragma unroll
-  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// Reduce v[h] (h < 64) over the 32 lanes of the warp, for max or sum.  Each of five butterfly
-// stages halves the values a lane holds: the lane keeps the half its stage bit selects and adds in
-// (or takes the max with) its partner's copy of that half.  Lane l ends with heads 2l and 2l+1.
+// Reduce v[h] (h < 32) over the 32 lanes of the warp for max or sum; lane l ends with head l.
 template <bool kMax>
-__device__ __forceinline__ float2 warp_reduce_heads(const float (&v)[HG], int lane) {
+__device__ __forceinline__ float warp_reduce_32(const float (&v)[32], int lane) {
   auto op = [](float a, float b) { return kMax ? fmaxf(a, b) : a + b; };
-  float a[32], b[16], c[8], d[4], e[2];
+  float b[16], c[8], d[4], e[2];
   bool up = (lane & 16) != 0;
 #pragma unroll
-  for (int j = 0; j < 32; ++j) a[j] = op(up ? v[j + 32] : v[j], __shfl_xor_sync(0xffffffffu, up ? v[j] : v[j + 32], 16));
+  for (int j = 0; j < 16; ++j) b[j] = op(up ? v[j + 16] : v[j], __shfl_xor_sync(0xffffffffu, up ? v[j] : v[j + 16], 16));
   up = (lane & 8) != 0;
 #pragma unroll
-  for (int j = 0; j < 16; ++j) b[j] = op(up ? a[j + 16] : a[j], __shfl_xor_sync(0xffffffffu, up ? a[j] : a[j + 16], 8));
+  for (int j = 0; j < 8; ++j) c[j] = op(up ? b[j + 8] : b[j], __shfl_xor_sync(0xffffffffu, up ? b[j] : b[j + 8], 8));
   up = (lane & 4) != 0;
 #pragma unroll
-  for (int j = 0; j < 8; ++j) c[j] = op(up ? b[j + 8] : b[j], __shfl_xor_sync(0xffffffffu, up ? b[j] : b[j + 8], 4));
+  for (int j = 0; j < 4; ++j) d[j] = op(up ? c[j + 4] : c[j], __shfl_xor_sync(0xffffffffu, up ? c[j] : c[j + 4], 4));
   up = (lane & 2) != 0;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) d[j] = op(up ? c[j + 4] : c[j], __shfl_xor_sync(0xffffffffu, up ? c[j] : c[j + 4], 2));
+  for (int j = 0; j < 2; ++j) e[j] = op(up ? d[j + 2] : d[j], __shfl_xor_sync(0xffffffffu, up ? d[j] : d[j + 2], 2));
   up = (lane & 1) != 0;
-#pragma unroll
-  for (int j = 0; j < 2; ++j) e[j] = op(up ? d[j + 2] : d[j], __shfl_xor_sync(0xffffffffu, up ? d[j] : d[j + 2], 1));
-  return make_float2(e[0], e[1]);
+  return op(up ? e[1] : e[0], __shfl_xor_sync(0xffffffffu, up ? e[0] : e[1], 1));
 }
 
 // 16 floats from shared memory (16-byte aligned) into registers
@@ -200,8 +178,8 @@ struct Smem {
   static constexpr size_t red = valid + (size_t)kMaxTiles * TILE;        // float [2][4][HG]
   static constexpr size_t stat = red + (size_t)2 * 4 * HG * 4;           // float m, l, alpha, f [HG]
   static constexpr size_t wcnt = stat + (size_t)4 * HG * 4;              // int [kMaxTiles][4]
-  static constexpr size_t bars = wcnt + (size_t)kMaxTiles * 4 * 4;       // u64 [12]
-  static constexpr size_t misc = bars + (size_t)12 * 8;
+  static constexpr size_t bars = wcnt + (size_t)kMaxTiles * 4 * 4;       // u64 [16]
+  static constexpr size_t misc = bars + (size_t)16 * 8;
   static constexpr size_t total = misc + 64;
 };
 
@@ -219,8 +197,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
         *f_sm = alpha_sm + HG;
   int *wcnt = reinterpret_cast<int *>(smem + L::wcnt);
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::bars);
-  uint64_t *g_full = bars, *q_full = bars + 4, *s_full = bars + 5, *p_full = bars + 6, *o_done = bars + 7,
-           *sm_bar = bars + 8, *drain = bars + 9;
+  uint64_t *g_full = bars, *q_full = bars + 4, *s_full = bars + 5, *p_full = bars + 6, *pv_done = bars + 7,
+           *sm_bar = bars + 11, *drain = bars + 12, *q_ready = bars + 13;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::misc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   int *s_rescale = const_cast<int *>(abort_flag) + 1;
@@ -238,9 +216,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
     for (int i = 0; i < 4; ++i) tc::mbar_init(&g_full[i], 32);  // the lanes of the loader warp
     tc::mbar_init(q_full, 1);
     tc::mbar_init(s_full, 1);
-    tc::mbar_init(p_full, 128);
-    tc::mbar_init(o_done, 1);
-    tc::mbar_init(sm_bar, 128);
+    tc::mbar_init(p_full, 256);
+    for (int c = 0; c < 4; ++c) tc::mbar_init(&pv_done[c], 1);
+    tc::mbar_init(sm_bar, 256);
+    tc::mbar_init(q_ready, 256);
     tc::mbar_init(drain, 1);
     *abort_flag = 0;
     *s_rescale = 0;
@@ -319,28 +298,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
   const bool single = P.nsplit == 1;
 
   // ---- phase 2: the tile pipeline
-  if (warp >= 4 && warp < 8) {
-    // ------------------------------------------------------------------ row copies
-    int n = 0;
-    bool ok = true;
-    for (int i = 0; i < nk && ok; ++i) {
-      if (!tile_ok(i)) continue;
-      if (n > 0) {
-        if (!(ok = tc::mbar_wait(o_done, (uint32_t)((n - 1) & 1), abort_flag))) break;
-        issue_tile(i);
-      }
-      cp_async_wait_all();
-      fence_proxy_async();
-      tc::mbar_arrive(&g_full[lw]);
-      ++n;
-    }
-    cp_async_wait_all();
-  } else if (warp == 8) {
+  if (warp == 8) {
     // ------------------------------------------------------------------ MMA issue
     if (lane == 0) {
       const uint32_t id1 = tc::idesc_bf16_f32(TILE, HG);
       const uint32_t id2 = tc::idesc_bf16_f32(TILE, HG, /*a_mn_major=*/true, /*b_mn_major=*/false);
-      bool ok = tc::mbar_wait(q_full, 0, abort_flag);  // also keeps the CTA alive until q has landed
+      // q has landed (and, with RoPE, been turned): this also keeps the CTA alive until the copy is in
+      bool ok = tc::mbar_wait(q_ready, 0, abort_flag);
       int n = 0;
       bool issued = false;
       for (int i = 0; i < nk && ok; ++i) {
@@ -363,7 +327,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
         tc::mma_commit(s_full);
         if (!(ok = tc::mbar_wait(p_full, par, abort_flag))) break;
         tc::tc_fence_after();
-        // O^T += G^T P^T, feature chunk c = K-blocks 2c, 2c+1
+        // O^T += G^T P^T, feature chunk c = K-blocks 2c, 2c+1; each chunk's completion frees those
+        // K-blocks for loader warp c
 #pragma unroll
         for (int c = 0; c < KB / 2; ++c) {
 #pragma unroll
@@ -372,8 +337,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
             const uint64_t bd = tc::sdesc_sw128(s_p + (ii / 4) * HG * 128 + (ii % 4) * 32, 16, 1024);
             tc::mma_bf16(tO + (uint32_t)(c * HG), ad, bd, id2, (n > 0 || ii > 0) ? 1u : 0u);
           }
+          tc::mma_commit(&pv_done[c]);
         }
-        tc::mma_commit(o_done);
         ++n;
       }
       if (issued) {  // nothing may still write TMEM or read shared memory when the CTA moves on
@@ -384,41 +349,96 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
       }
     }
   } else {
-    // ------------------------------------------------------------------ softmax + staging (warps 0-3)
-    const int r = warp * 32 + lane;  // tile row (S^T) and feature within a chunk (O^T)
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    // ------------------------------------------------------------------ warps 0-7: softmax + staging
+    // warp w: TMEM lane quadrant w % 4 (tile rows, and features of an O^T chunk), heads hh .. hh+31;
+    // warps 4-7 also copy the rows (loader warp lw = w - 4 owns K-blocks 2lw, 2lw+1)
+    const bool loader = warp >= 4;
+    const int quad = warp & 3, hh = (warp >> 2) * 32;
+    const int r = quad * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     uint32_t sm_uses = 0;
     auto sm_sync = [&]() -> bool {
       tc::mbar_arrive(sm_bar);
       return tc::mbar_wait(sm_bar, (sm_uses++) & 1u, abort_flag);
     };
-    if (r < HG) {
-      m_sm[r] = -INFINITY;
-      l_sm[r] = 0.f;
+    if (tid < HG) {
+      m_sm[tid] = -INFINITY;
+      l_sm[tid] = 0.f;
     }
-    bool ok = sm_sync();
+    // RoPE on q's last rd features, in place in the swizzled K-blocks: one 16-byte chunk (four
+    // adjacent pairs) of one head per unit, at most two units per thread; the same f32 arithmetic
+    // as the separate pass.  The angles are read while q is still in flight.
+    const int q_tail = HD - P.rd, q_nch = P.rd / 8;
+    float4 qcs[2][2];
+    if (P.rope_q) {
+      const float2 *tp = reinterpret_cast<const float2 *>(P.tab) + (int64_t)(P.start_pos + t) * (P.rd >> 1);
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int u = tid + 256 * k;
+        if (u < HG * q_nch) {
+          const int f0 = q_tail + 8 * (u % q_nch);
+          qcs[k][0] = *reinterpret_cast<const float4 *>(tp + (f0 - q_tail) / 2);
+          qcs[k][1] = *reinterpret_cast<const float4 *>(tp + (f0 - q_tail) / 2 + 2);
+        }
+      }
+    }
+    bool ok = tc::mbar_wait(q_full, 0, abort_flag);
+    if (ok && P.rope_q) {
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int u = tid + 256 * k;
+        if (u >= HG * q_nch) continue;
+        const int h = u / q_nch, f0 = q_tail + 8 * (u % q_nch);
+        uint8_t *cp = smem + L::q + (f0 / 64) * HG * 128 + h * 128 + ((((f0 % 64) / 8) ^ (h & 7)) << 4);
+        uint4 x = *reinterpret_cast<const uint4 *>(cp);
+        const float cs[8] = {qcs[k][0].x, qcs[k][0].y, qcs[k][0].z, qcs[k][0].w,
+                             qcs[k][1].x, qcs[k][1].y, qcs[k][1].z, qcs[k][1].w};
+        __nv_bfloat162 *pv = reinterpret_cast<__nv_bfloat162 *>(&x);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float a = __low2float(pv[j]), bb = __high2float(pv[j]), c = cs[2 * j], sn = cs[2 * j + 1];
+          const float re = __fsub_rn(__fmul_rn(a, c), __fmul_rn(bb, sn));
+          const float im = __fadd_rn(__fmul_rn(a, sn), __fmul_rn(bb, c));
+          pv[j] = __halves2bfloat162(__float2bfloat16_rn(re), __float2bfloat16_rn(im));
+        }
+        *reinterpret_cast<uint4 *>(cp) = x;
+      }
+      fence_proxy_async();  // the turned q is read by the MMA (async proxy)
+    }
+    tc::mbar_arrive(q_ready);
+    if (ok) ok = sm_sync();
     int n = 0;
     for (int i = 0; i < nk && ok; ++i) {
       if (!tile_ok(i)) continue;
+      if (loader) {
+        if (n > 0) {  // this warp's K-blocks of the previous tile have been read by its P.V chunk
+          if (!(ok = tc::mbar_wait(&pv_done[lw], (uint32_t)((n - 1) & 1), abort_flag))) break;
+          issue_tile(i);
+        }
+        cp_async_wait_all();
+        fence_proxy_async();
+        tc::mbar_arrive(&g_full[lw]);
+      }
       if (!(ok = tc::mbar_wait(s_full, (uint32_t)(n & 1), abort_flag))) break;
       tc::tc_fence_after();
-      float s[HG];
-      tmem_ld_cols(tS + lane_off, s);
+      float s[32];
+      tmem_ld_32cols(tS + (uint32_t)hh + lane_off, s);
       const bool vr = valid[i * TILE + r] != 0;
 #pragma unroll
-      for (int h = 0; h < HG; ++h) s[h] = vr ? s[h] * P.scale_log2 : -INFINITY;
-      reinterpret_cast<float2 *>(red_max + warp * HG)[lane] = warp_reduce_heads<true>(s, lane);
+      for (int h = 0; h < 32; ++h) s[h] = vr ? s[h] * P.scale_log2 : -INFINITY;
+      red_max[quad * HG + hh + lane] = warp_reduce_32<true>(s, lane);
       if (!(ok = sm_sync())) break;
-      if (r < HG) {
-        const float tmax = fmaxf(fmaxf(red_max[r], red_max[HG + r]), fmaxf(red_max[2 * HG + r], red_max[3 * HG + r]));
+      if (tid < HG) {
+        const float tmax =
+            fmaxf(fmaxf(red_max[tid], red_max[HG + tid]), fmaxf(red_max[2 * HG + tid], red_max[3 * HG + tid]));
         float a = 1.0f;
-        if (tmax > m_sm[r] + 8.0f) {  // keep exp2(s - m) below 2^8; rescale what has accumulated
-          a = exp2f(m_sm[r] - tmax);
-          m_sm[r] = tmax;
-          l_sm[r] *= a;
+        if (tmax > m_sm[tid] + 8.0f) {  // keep exp2(s - m) below 2^8; rescale what has accumulated
+          a = exp2f(m_sm[tid] - tmax);
+          m_sm[tid] = tmax;
+          l_sm[tid] *= a;
           if (n > 0) *s_rescale = 1;
         }
-        alpha_sm[r] = a;
+        alpha_sm[tid] = a;
       }
       if (!(ok = sm_sync())) break;
       if (*s_rescale) {
@@ -426,11 +446,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
 #pragma unroll 1
         for (int c = 0; c < KB / 2; ++c) {
 #pragma unroll
-          for (int c0 = 0; c0 < HG; c0 += 16) {
+          for (int c0 = 0; c0 < 32; c0 += 16) {
             uint32_t v[16];
-            const uint32_t ta = tO + (uint32_t)(c * HG + c0) + lane_off;
+            const uint32_t ta = tO + (uint32_t)(c * HG + hh + c0) + lane_off;
             float av[16];
-            lds16(av, alpha_sm + c0);
+            lds16(av, alpha_sm + hh + c0);
             tc::tmem_ld16(ta, v);
             tc::tmem_ld_wait();
 #pragma unroll
@@ -443,39 +463,40 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
       uint8_t *prow = sP + (r / 64) * HG * 128;
       const int rc = (r % 64) / 8, ro = (r % 8) * 2;
 #pragma unroll
-      for (int h0 = 0; h0 < HG; h0 += 16) {
+      for (int h0 = 0; h0 < 32; h0 += 16) {
         float mv[16];  // the maxima read before the stores below (which the compiler cannot tell apart)
-        lds16(mv, m_sm + h0);
+        lds16(mv, m_sm + hh + h0);
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
-          const int h = h0 + k;
-          s[h] = exp2f(s[h] - mv[k]);  // 0 for masked rows
-          *reinterpret_cast<bf16 *>(prow + h * 128 + ((rc ^ (h & 7)) << 4) + ro) = __float2bfloat16_rn(s[h]);
+          const int h = hh + h0 + k;
+          s[h0 + k] = exp2f(s[h0 + k] - mv[k]);  // 0 for masked rows
+          *reinterpret_cast<bf16 *>(prow + h * 128 + ((rc ^ (h & 7)) << 4) + ro) = __float2bfloat16_rn(s[h0 + k]);
         }
       }
       fence_proxy_async();
       tc::tc_fence_before();
       tc::mbar_arrive(p_full);
-      reinterpret_cast<float2 *>(red_sum + warp * HG)[lane] = warp_reduce_heads<false>(s, lane);
+      red_sum[quad * HG + hh + lane] = warp_reduce_32<false>(s, lane);
       if (!(ok = sm_sync())) break;
-      if (r < HG) {
-        l_sm[r] += (red_sum[r] + red_sum[HG + r]) + (red_sum[2 * HG + r] + red_sum[3 * HG + r]);
-        if (r == 0) *s_rescale = 0;
+      if (tid < HG) {
+        l_sm[tid] += (red_sum[tid] + red_sum[HG + tid]) + (red_sum[2 * HG + tid] + red_sum[3 * HG + tid]);
+        if (tid == 0) *s_rescale = 0;
       }
       ++n;
     }
-    if (ok && nmine > 0) ok = tc::mbar_wait(o_done, (uint32_t)((nmine - 1) & 1), abort_flag);
-    if (ok && r < HG) {
+    if (loader) cp_async_wait_all();
+    if (ok && nmine > 0) ok = tc::mbar_wait(&pv_done[3], (uint32_t)((nmine - 1) & 1), abort_flag);
+    if (ok && tid < HG) {
       if (single) {  // finish in place: the sink joins the denominator
-        const float s2 = P.sink[hg * HG + r] * 1.4426950408889634f;
-        const float M = fmaxf(m_sm[r], s2);
-        const float em = nmine > 0 ? exp2f(m_sm[r] - M) : 0.f;
-        f_sm[r] = em / (l_sm[r] * em + exp2f(s2 - M));
+        const float s2 = P.sink[hg * HG + tid] * 1.4426950408889634f;
+        const float M = fmaxf(m_sm[tid], s2);
+        const float em = nmine > 0 ? exp2f(m_sm[tid] - M) : 0.f;
+        f_sm[tid] = em / (l_sm[tid] * em + exp2f(s2 - M));
       } else {
-        f_sm[r] = nmine > 0 ? 1.0f / l_sm[r] : 0.f;
-        float *ml = P.part_ml + ((row * P.nsplit + split) * P.H + hg * HG + r) * 2;
-        ml[0] = m_sm[r];
-        ml[1] = l_sm[r];
+        f_sm[tid] = nmine > 0 ? 1.0f / l_sm[tid] : 0.f;
+        float *ml = P.part_ml + ((row * P.nsplit + split) * P.H + hg * HG + tid) * 2;
+        ml[0] = m_sm[tid];
+        ml[1] = l_sm[tid];
       }
     }
     if (ok) ok = sm_sync();
@@ -485,14 +506,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
       bf16 *stage = reinterpret_cast<bf16 *>(smem + L::g);
 #pragma unroll 1
       for (int c = 0; c < KB / 2; ++c) {
-        float v[HG];
-        tmem_ld_cols(tO + (uint32_t)(c * HG) + lane_off, v);
+        float v[32];
+        tmem_ld_32cols(tO + (uint32_t)(c * HG + hh) + lane_off, v);
 #pragma unroll
-        for (int h0 = 0; h0 < HG; h0 += 16) {
+        for (int h0 = 0; h0 < 32; h0 += 16) {
           float fv[16];  // the factors read before the stores below
-          lds16(fv, f_sm + h0);
+          lds16(fv, f_sm + hh + h0);
 #pragma unroll
-          for (int k = 0; k < 16; ++k) stage[(h0 + k) * HD + c * 128 + r] = __float2bfloat16_rn(v[h0 + k] * fv[k]);
+          for (int k = 0; k < 16; ++k)
+            stage[(hh + h0 + k) * HD + c * 128 + r] = __float2bfloat16_rn(v[h0 + k] * fv[k]);
         }
       }
     }
@@ -614,7 +636,8 @@ bool sparse_attn_tc_supported(const AttnArgs &a) {
          (a.rows_b == nullptr || a.b_seq_stride % attn::HD == 0) &&
          (a.o_rot == nullptr || (a.rd % 8 == 0 && ((uintptr_t)a.tab & 15) == 0)) && ((uintptr_t)a.q & 15) == 0 &&
          ((uintptr_t)a.rows_a & 15) == 0 && ((uintptr_t)a.rows_b & 15) == 0 && ((uintptr_t)a.o & 15) == 0 &&
-         ((uintptr_t)a.o_rot & 15) == 0;
+         ((uintptr_t)a.o_rot & 15) == 0 &&
+         (a.rope_q == 0 || (a.rd % 8 == 0 && a.rd <= 64 && ((uintptr_t)a.tab & 15) == 0));  // two units a thread
 }
 
 cudaError_t launch_sparse_attn_tc(const AttnArgs &a, float *ws, size_t ws_bytes, int num_sms, cudaStream_t s,
@@ -646,6 +669,7 @@ cudaError_t launch_sparse_attn_tc(const AttnArgs &a, float *ws, size_t ws_bytes,
   p.start_pos = a.start_pos;
   p.tab = a.tab;
   p.status = a.status;
+  p.rope_q = a.rope_q;
   p.ntiles = std::max(1, (a.na + p.nb + TILE - 1) / TILE);
   // tiles per CTA: split a query's tiles over CTAs only while there are few queries to fill the
   // SMs (up to two CTAs per SM in the grid: tiles of entries that are all -1 cost a CTA only its

@@ -246,10 +246,15 @@ def test_full_width_sampled(csa, orc, name, seqs, toks):
         sh = csa.Shared(to_dev(shared["compress_kv"]), to_dev(shared["index_k"]), shared["compress_len"], sel_d, K,
                         None if "candidates" not in shared else to_dev(shared["candidates"]))
     L = shared["compress_len"] if shared else 1
+    xd = to_dev(x)
+    # the benchmark's path first (no debug buffers: q's RoPE runs inside the attention kernel), then the
+    # debug path (RoPE as its own pass, so the turned q can be read back); same inputs, same ring update
+    out_fast = ctx.forward(wd, role, ring_d, xd, start, shared=sh)
     dbg = _dbg(B * T, g, L, g.window + (K if wl.ratio else 0))
-    out = ctx.forward(wd, role, ring_d, to_dev(x), start, shared=sh, debug=dbg)
+    out = ctx.forward(wd, role, ring_d, xd, start, shared=sh, debug=dbg)
     torch.cuda.synchronize()
     assert ctx.status() == 0
+    assert torch.equal(out_fast, out), name + ": the fused q RoPE changes the layer output"
     dbg["__out"] = out
     # oracle: only the sampled sequences (and, for the prefill chunk, the sampled tokens)
     for b in seqs:
