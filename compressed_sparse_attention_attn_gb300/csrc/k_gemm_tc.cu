@@ -139,24 +139,40 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemm_tc(const __grid_constant__
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
+      // the unit's coordinates, decoded once and then advanced without divisions (this loop paces
+      // the copies)
+      Unit un = decode_unit(P, u0);
+      const Problem *pr = &P.prob[un.p];
+      int tm = un.tile % pr->tiles_m, tn = (un.tile / pr->tiles_m) % pr->tiles_n;
+      int g = un.tile / (pr->tiles_m * pr->tiles_n);
       for (int u = u0; u < u1; ++u) {
-        const Unit un = decode_unit(P, u);
-        const Problem &pr = P.prob[un.p];
-        const int tm = un.tile % pr.tiles_m, rest = un.tile / pr.tiles_m;
-        const int tn = rest % pr.tiles_n, g = rest / pr.tiles_n;
         if (!tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag)) break;
         uint8_t *sa = smem + stage * stage_bytes;
         tc::mbar_expect_tx(&full[stage], stage_bytes);
 #pragma unroll
         for (int a = 0; a < ATOMS; ++a) {
           const int k0 = (un.kb * ATOMS + a) * BK;
-          tc::tma_load_2d(sa + a * a_atom, &pr.tmA, &full[stage], k0, g * pr.N + tn * BM, pol_w);
-          tc::tma_load_2d(sa + a_bytes + a * b_atom, &pr.tmB, &full[stage], g * pr.Kg + k0, tm * BN, pol_x);
+          tc::tma_load_2d(sa + a * a_atom, &pr->tmA, &full[stage], k0, g * pr->N + tn * BM, pol_w);
+          tc::tma_load_2d(sa + a_bytes + a * b_atom, &pr->tmB, &full[stage], g * pr->Kg + k0, tm * BN, pol_x);
         }
         ++issued;
         if (++stage == S) {
           stage = 0;
           phase ^= 1;
+        }
+        if (++un.kb == pr->kblocks) {  // next tile: token tile fastest, then weight tile, then group
+          un.kb = 0;
+          if (++un.tile == pr->tiles) {
+            un.tile = 0;
+            tm = tn = g = 0;
+            if (++un.p < P.nprob) pr = &P.prob[un.p];
+          } else if (++tm == pr->tiles_m) {
+            tm = 0;
+            if (++tn == pr->tiles_n) {
+              tn = 0;
+              ++g;
+            }
+          }
         }
       }
       // let every copy this CTA issued land before the CTA can exit
