@@ -7,9 +7,14 @@
 //   D[j][(t, h)] = sum_d K^I[j][d] Q^I[t][h][d]      (M = 128 keys, N = QG * Hi, K = 128; TMEM)
 // The four warps then read their 32 keys' rows of D and form sum_h w^I[t][h] ReLU(D) in f32 for
 // each query, writing the valid positions only (j below the causal limit floor((p+1)/ratio) and the
-// published length, and inside an allowed candidate block).  Every mbarrier wait is time-bounded.
+// published length, and inside an allowed candidate block).  A decode query whose candidate mask
+// spans more than 1024 keys goes to a gathered variant that reads the kept blocks' keys only.  Every
+// mbarrier wait is time-bounded.
 #include "csa_internal.cuh"
 #include "tc_ptx.cuh"
+
+#include <algorithm>
+#include <cstring>
 
 namespace csa {
 
@@ -129,10 +134,238 @@ __global__ void __launch_bounds__(kThreads) k_index_scores_tc(const __grid_const
   if (tid == 0 && *abort_flag && P.status) atomicOr(P.status, kStatusTimeout);
 }
 
+
+// ---- candidate-gathered variant (one query per CTA group, T == 1) --------------------------------
+// With a candidate block mask, only the kept blocks' keys can be selected, so only those are read:
+// each CTA scans the query's mask row into the ordered list of kept 64-key units (a block of
+// cand_block keys is cand_block / 64 units), and takes the unit pairs c, c + P, c + 2P, ... of it.
+// A pair is two TMA boxes of 64 keys stacked into one 128-row operand (the 128-byte swizzle repeats
+// every 8 rows, so two 64-row boxes form the layout of one 128-row box); pairs are double-buffered
+// against the MMA and the epilogue, each buffer with its own TMEM accumulator.
+constexpr int kGatherBufs = 3;
+
+struct GatherParams {
+  CUtensorMap tm_k;  // K^I [B*Lstride][128], box {64, 64}
+  CUtensorMap tm_q;  // Q^I [B*Hi][128], box {64, Hi}
+  const float *wI;   // [B][Hi]
+  int Hi, Lstride, compress_len, ratio, start_pos, P, max_units;
+  const uint8_t *cand;
+  int cand_width, cand_block;
+  float *S;  // [B][Lstride]
+  int *status;
+};
+
+__global__ void __launch_bounds__(kThreads) k_index_scores_gather_tc(const __grid_constant__ GatherParams P) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = tc::smem_u32(smem_raw);
+  uint8_t *smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
+  const int N = P.Hi;
+  constexpr uint32_t k_buf = TILE * 128 * 2;  // a pair: two 64-column halves of 128 keys
+  const uint32_t q_half = (uint32_t)N * 128;
+  uint8_t *sk = smem, *sq = smem + kGatherBufs * k_buf;
+  float *w_s = reinterpret_cast<float *>(sq + 2 * q_half);        // [Hi]
+  int *units = reinterpret_cast<int *>(w_s + kMaxN);              // [max_units] kept 64-key units
+  uint64_t *bars = reinterpret_cast<uint64_t *>(units + ((P.max_units + 1) & ~1));
+  uint64_t *full = bars, *done = bars + kGatherBufs, *qbar = bars + 2 * kGatherBufs;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(qbar + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  int *s_nunits = const_cast<int *>(abort_flag) + 1;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int c = blockIdx.x, b = blockIdx.y;
+  const int limit = min((P.start_pos + 1) / P.ratio, P.compress_len);
+  const int per_block = P.cand_block / 64;
+  const uint32_t ncols = N * kGatherBufs <= 32 ? 32 : N * kGatherBufs <= 64 ? 64 : N * kGatherBufs <= 128 ? 128
+                         : N * kGatherBufs <= 256 ? 256 : 512;
+
+  if (tid == 0) {
+    for (int i = 0; i < 2 * kGatherBufs + 1; ++i) tc::mbar_init(&bars[i], 1);
+    *abort_flag = 0;
+    tc::fence_barrier_init();
+    tc::prefetch_tmap(&P.tm_k);
+    tc::prefetch_tmap(&P.tm_q);
+    tc::mbar_expect_tx(qbar, 2 * q_half);
+    const uint64_t pol = tc::policy_evict_first();
+    for (int kb = 0; kb < 2; ++kb) tc::tma_load_2d(sq + kb * q_half, &P.tm_q, qbar, kb * 64, b * N, pol);
+  }
+  for (int e = tid; e < N; e += kThreads) w_s[e] = P.wI[(int64_t)b * N + e];
+  if (warp == 1) {
+    // the kept units in ascending key order
+    const uint8_t *cr = P.cand + (int64_t)b * P.cand_width;
+    const int nblk = min((limit + P.cand_block - 1) / P.cand_block, P.cand_width);
+    int n = 0;
+    for (int b0 = 0; b0 < nblk; b0 += 8 * 32) {
+      uint32_t kv[8];  // eight rounds of mask bytes in flight at once
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int blk = b0 + k * 32 + lane;
+        kv[k] = blk < nblk ? cr[blk] : 0u;
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int blk = b0 + k * 32 + lane;
+        const bool keep = kv[k] != 0u;
+        const unsigned bal = __ballot_sync(0xffffffffu, keep);
+        if (keep) {
+          const int base = n + __popc(bal & ((1u << lane) - 1u)) * per_block;
+          for (int s = 0; s < per_block; ++s)
+            if (base + s < P.max_units) units[base + s] = blk * per_block + s;
+        }
+        n += __popc(bal) * per_block;
+      }
+    }
+    // units past the causal limit hold no valid key
+    if (lane == 0) {
+      while (n > 0 && n <= P.max_units && units[n - 1] * 64 >= limit) --n;
+      *s_nunits = min(n, P.max_units);
+    }
+  }
+  if (warp == 0) tc::tmem_alloc(tmem_slot, ncols);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int nunits = *s_nunits;
+  const int npairs_all = (nunits + 1) / 2;
+  const int mine = c < npairs_all ? (npairs_all - c + P.P - 1) / P.P : 0;
+  auto issue = [&](int i) {  // pair i of this CTA into buffer i % kGatherBufs
+    const int pi = c + i * P.P;
+    const int u0 = units[2 * pi], two = 2 * pi + 1 < nunits;
+    uint64_t *bar = &full[i % kGatherBufs];
+    uint8_t *dst = sk + (i % kGatherBufs) * k_buf;
+    const uint64_t pol = tc::policy_evict_first();
+    tc::mbar_expect_tx(bar, (two ? 2u : 1u) * 2u * 64u * 128u);
+    for (int kb = 0; kb < 2; ++kb) {
+      tc::tma_load_2d(dst + kb * (k_buf / 2), &P.tm_k, bar, kb * 64, b * P.Lstride + u0 * 64, pol);
+      if (two)
+        tc::tma_load_2d(dst + kb * (k_buf / 2) + 64 * 128, &P.tm_k, bar, kb * 64,
+                        b * P.Lstride + units[2 * pi + 1] * 64, pol);
+    }
+  };
+  int issued = 0, landed = 0;  // (thread 0) pairs whose copies were issued / seen complete
+  bool q_landed = false;
+  if (tid == 0)
+    for (; issued < min(mine, kGatherBufs); ++issued) issue(issued);
+  bool ok = true;
+  if (tid == 0 && mine > 0) ok = q_landed = tc::mbar_wait(qbar, 0, abort_flag);
+  const uint32_t id = tc::idesc_bf16_f32(TILE, N);
+  const float *Srow_w = w_s;
+  float *Srow = P.S + (int64_t)b * P.Lstride;
+  for (int i = 0; i < mine; ++i) {
+    const int buf = i % kGatherBufs;
+    const uint32_t par = (uint32_t)(i / kGatherBufs) & 1u;
+    if (tid == 0 && ok) {
+      ok = tc::mbar_wait(&full[buf], par, abort_flag);
+      if (ok) {
+        ++landed;
+        tc::tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(buf * N);
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb) {
+          const uint64_t ad = tc::sdesc_sw128(tc::smem_u32(sk + buf * k_buf + kb * (k_buf / 2)), 16, 1024);
+          const uint64_t bd = tc::sdesc_sw128(tc::smem_u32(sq + kb * q_half), 16, 1024);
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) tc::mma_bf16(d, ad + 2ull * k4, bd + 2ull * k4, id, (kb | k4) ? 1u : 0u);
+        }
+        tc::mma_commit(&done[buf]);
+      }
+    }
+    const bool got = tc::mbar_wait(&done[buf], par, abort_flag);
+    tc::tc_fence_after();
+    // the buffer is free once the MMA has read it: refill it with pair i + kGatherBufs
+    if (got && tid == 0 && i + kGatherBufs < mine) issue(issued++);
+    const int pi = c + i * P.P;
+    const int r = tid;
+    const int slot = 2 * pi + (r >> 6);
+    const int j = slot < nunits ? units[slot] * 64 + (r & 63) : limit;
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(buf * N);
+    float acc = 0.f;
+    for (int h0 = 0; h0 < N; h0 += 16) {
+      uint32_t v[16];
+      tc::tmem_ld16_wait(lane_base + (uint32_t)h0, v);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) acc = fmaf(Srow_w[h0 + k], fmaxf(__uint_as_float(v[k]), 0.f), acc);
+    }
+    if (got && j < limit) Srow[j] = acc;
+    // every thread has read accumulator buf before the MMA of pair i + kGatherBufs overwrites it;
+    // a wait that gave up anywhere ends the loop for every thread alike
+    tc::tc_fence_before();
+    const int failed = __syncthreads_or(!got);
+    tc::tc_fence_after();
+    if (failed) break;
+  }
+  if (tid == 0) {
+    // copies that may still be in flight (none unless a wait gave up): let them land, bounded,
+    // before the CTA exits
+    const uint64_t t0w = tc::global_ns();
+    auto drain = [&](uint64_t *bar, uint32_t par) {
+      while (!tc::mbar_try_wait(bar, par) && tc::global_ns() - t0w < tc::kWaitLimitNs) {
+      }
+    };
+    if (!q_landed) drain(qbar, 0);
+    for (int i = landed; i < issued; ++i) drain(&full[i % kGatherBufs], (uint32_t)(i / kGatherBufs) & 1u);
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, ncols);
+  }
+  if (tid == 0 && *abort_flag && P.status) atomicOr(P.status, kStatusTimeout);
+}
+
 }  // namespace idx
 
 bool index_scores_tc_supported(const bf16 *qI, const bf16 *KI, int Hi, int dI) {
   return dI == idx::DI && Hi % 16 == 0 && Hi <= idx::kMaxN && ((uintptr_t)qI & 15) == 0 && ((uintptr_t)KI & 15) == 0;
+}
+
+// One query per sequence with a candidate mask: CTA group of P per query over its kept 64-key units.
+static cudaError_t launch_index_scores_gather_tc(const bf16 *qI, const float *wI, const bf16 *KI, int B, int start_pos,
+                                                 int Hi, int Lstride, int compress_len, int ratio, const uint8_t *cand,
+                                                 int cand_width, int cand_block, float *S, int *status,
+                                                 cudaStream_t s) {
+  using namespace idx;
+  GatherParams p;
+  memset(&p, 0, sizeof(p));
+  const int limit = std::min((start_pos + 1) / ratio, compress_len);
+  if (limit <= 0 || B <= 0) return cudaSuccess;
+  const int per_block = cand_block / 64;
+  const int nblk = std::min((limit + cand_block - 1) / cand_block, cand_width);
+  p.max_units = nblk * per_block;
+  if (p.max_units <= 0) return cudaSuccess;
+  if (!tma_map_2d_bf16(&p.tm_k, KI, DI, (uint64_t)B * Lstride, DI, 64, 64)) return cudaErrorInvalidValue;
+  if (!tma_map_2d_bf16(&p.tm_q, qI, DI, (uint64_t)B * Hi, DI, 64, (uint32_t)Hi)) return cudaErrorInvalidValue;
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  const int max_pairs = (p.max_units + 1) / 2;
+  // CTAs per query: as many as fill the SMs in one wave (two CTAs fit on an SM), rounded down so
+  // that no CTA waits for a second wave
+  p.P = std::max(1, std::min(max_pairs, 2 * sms / B));
+  p.wI = wI;
+  p.Hi = Hi;
+  p.Lstride = Lstride;
+  p.compress_len = compress_len;
+  p.ratio = ratio;
+  p.start_pos = start_pos;
+  p.cand = cand;
+  p.cand_width = cand_width;
+  p.cand_block = cand_block;
+  p.S = S;
+  p.status = status;
+  const size_t smem = 1024 + (size_t)kGatherBufs * TILE * 128 * 2 + 2 * (size_t)Hi * 128 + kMaxN * 4 +
+                      4 * (size_t)((p.max_units + 1) & ~1) + (2 * kGatherBufs + 1) * 8 + 16;
+  if (smem > 227 * 1024) return cudaErrorInvalidValue;
+  static int attr = 0;
+  if ((int)smem > attr) {
+    e = cudaFuncSetAttribute(k_index_scores_gather_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr = (int)smem;
+  }
+  k_index_scores_gather_tc<<<dim3(p.P, B), kThreads, smem, s>>>(p);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_index_scores_tc(const bf16 *qI, const float *wI, const bf16 *KI, int B, int T, int start_pos,
@@ -167,6 +400,13 @@ cudaError_t launch_index_scores_tc(const bf16 *qI, const float *wI, const bf16 *
   }
   const int tiles = (p.compress_len + TILE - 1) / TILE;
   if (tiles <= 0) return cudaSuccess;
+  // gathering pays once the candidate keys of a query span more than a few tiles: its key copies wait
+  // for the mask scan, while the dense kernel's start at once
+  if (cand && T == 1 && cand_block % 64 == 0 && Hi * kGatherBufs <= 512 &&
+      (int64_t)std::min((std::min((start_pos + 1) / ratio, compress_len) + cand_block - 1) / cand_block, cand_width) *
+              cand_block > 1024)
+    return launch_index_scores_gather_tc(qI, wI, KI, B, start_pos, Hi, Lstride, p.compress_len, ratio, cand,
+                                         cand_width, cand_block, S, status, s);
   dim3 grid(tiles, (T + p.QG - 1) / p.QG, B);
   k_index_scores_tc<<<grid, kThreads, smem, s>>>(p);
   return cudaGetLastError();

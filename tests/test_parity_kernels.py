@@ -195,6 +195,46 @@ def test_index_scores_head_counts(csa, orc, Hi, B, T, start, L, clen, ratio):
     assert (np.abs(got[valid].astype(np.float64) - S[valid]) <= tol).all()
 
 
+@pytest.mark.parametrize("Hi,B,start,L,clen,ratio,keep,cb", [
+    (32, 5, 4000, 2048, 2000, 2, 7, 64),        # odd number of kept units
+    (32, 3, 3000, 2048, 1500, 2, 0.3, 128),     # blocks of two 64-key units, last one partial
+    (64, 4, 20000, 8192, 5001, 4, 17, 64),      # 64 heads
+    (16, 70, 8000, 4096, 2000, 4, 0.6, 64),     # many queries: a small CTA group per query
+    (32, 2, 5000, 4096, 2500, 2, 1, 64),        # one kept block
+    (32, 4, 1000, 512, 500, 2, 0.5, 64),        # short candidate span (the dense kernel)
+])
+def test_index_scores_gathered(csa, orc, Hi, B, start, L, clen, ratio, keep, cb):
+    """One query per sequence with a candidate mask spanning more than 1024 keys: only the kept
+    blocks' keys are read.  Row 0 of the mask keeps every causal block and row 1 (when there is one)
+    none."""
+    rng = np.random.default_rng(90 + Hi + B)
+    T = 1
+    qI = _rng_bf16(orc, rng, (B, Hi, 128))
+    wI = (rng.standard_normal((B, Hi)) / 64).astype(np.float32)
+    KI = _rng_bf16(orc, rng, (B, L, 128))
+    pos = positions(B, T, start)
+    width = -(-L // cb)
+    cand = candidate_mask(B, pos, ratio, clen, cb, width, keep, 78)
+    lim0 = min((start + 1) // ratio, clen)
+    cand[0, :-(-lim0 // cb)] = 1
+    if B > 1:
+        cand[1, :] = 0
+    S = np.concatenate([orc.index_scores(qI[b:b + 1], wI[b:b + 1], KI[b], pos[b:b + 1], ratio, clen,
+                                         cand[b:b + 1], cb) for b in range(B)])
+    Sd = torch.full((B, L), float("nan"), device="cuda")
+    csa.index_scores(to_dev(qI), to_dev(wI), to_dev(KI), B, T, start, clen, ratio, Sd, to_dev(cand), cb)
+    got = to_np(Sd)
+    valid = np.isfinite(S)
+    assert np.isnan(got[~valid]).all()
+    for r in range(B):
+        v = valid[r]
+        if not v.any():
+            continue
+        a, b = got[r, v].astype(np.float64), S[r, v].astype(np.float64)
+        tol = 1e-3 * np.abs(b) + 1e-3 * np.abs(b).max()
+        assert (np.abs(a - b) <= tol).all()
+
+
 @pytest.mark.parametrize("B,T,start,L,clen,ratio,keep,cb,K", [
     (4, 1, 1000, 512, 500, 2, 0.5, 64, 512),
     (1, 300, 0, 1024, 1024, 4, 0, 64, 512),
