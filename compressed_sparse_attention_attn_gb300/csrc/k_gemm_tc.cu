@@ -15,6 +15,12 @@
 // the workspace, bumps the tile's arrival counter, and the last one sums the partials in CTA order
 // (deterministic) and writes the bf16 result.  No CTA ever waits for another.
 //
+// Prefill-sized launches (many token tiles, activations far beyond L2) run k_gemm_tc_waves instead:
+// whole tiles in data-parallel waves (CTA c takes tiles c, c + G, ...), so that the tiles in flight
+// together are consecutive ones whose operands share L2, then Stream-K over the last partial wave.
+// L2 policies follow the reuse: weights read by one token tile only stream past evict-first,
+// activations small next to L2 stay evict-last, everything else is normal.
+//
 // Warp roles (192 threads): warps 0-3 epilogue (TMEM lane quadrant = warp), warp 4 TMA producer,
 // warp 5 TMEM allocation + MMA issue.  Every mbarrier wait is time-bounded; a timeout raises the
 // device status word and the CTA drains its copies and MMAs, frees TMEM and exits.
@@ -38,6 +44,10 @@ constexpr int kThreads = 192;
 constexpr int kCounterInts = 65536;            // arrival counters at the head of the workspace
 constexpr size_t kCounterBytes = kCounterInts * sizeof(int);
 constexpr int kMaxContrib = 320;  // >= grid + 1 for any grid of one CTA per SM
+// activations above this size (well beyond the 126 MiB L2 once the weights stream beside them) are
+// read in whole-tile waves; smaller ones stay in L2 under Stream-K's contiguous ranges, which
+// measured faster there
+constexpr size_t kWaveActBytes = (size_t)96 << 20;
 
 struct Problem {
   CUtensorMap tmA;  // W [groups*N rows][Kg] bf16, box {64, 128}
@@ -46,12 +56,17 @@ struct Problem {
   int ldy, N, M, groups, Kg, kblocks, tiles_n, tiles_m, tiles, unit_begin, tile_begin;
   float *part;  // split-K mode
   int ldp;
+  // L2 policies of the two operands' copies: 0 evict-first, 1 normal, 2 evict-last
+  int pol_a, pol_b;
 };
 
 struct Params {
   Problem prob[kMaxProblems];
   int nprob, total_units, total_tiles, BN, stages;
   int split_S;  // > 0: split-K mode, CTA c = (tile c / S, k-range c % S), partials out, no fixup
+  // data-parallel waves: CTA c first takes the whole tiles c, c + G, ... (dp_waves of them; tiles
+  // [0, dp_waves G) in all), then its Stream-K share of the units from sk_unit0 on
+  int dp_waves, sk_unit0;
   float *partials;  // [grid][2][BM][BN]
   int *counters;    // [total_tiles]
   int *status;
@@ -71,6 +86,34 @@ __device__ __forceinline__ Unit decode_unit(const Params &P, int u) {
 __device__ __forceinline__ int64_t cta_start(int64_t c, int64_t U, int64_t G) { return c * U / G; }
 __device__ __forceinline__ int64_t unit_owner(int64_t v, int64_t U, int64_t G) { return ((v + 1) * G - 1) / U; }
 
+// Units [ub, ue) of segment s of this CTA: whole tile blockIdx.x + s G for s < dp_waves, then the
+// Stream-K share of the rest (split-K mode: the one k-range of the CTA's tile).
+template <bool kWaves>
+__device__ __forceinline__ void seg_range(const Params &P, int s, int &ub, int &ue) {
+  const int64_t G = gridDim.x;
+  if (!kWaves && P.split_S > 0) {
+    const int tg = blockIdx.x / P.split_S, sp = blockIdx.x % P.split_S;
+    int p = 0;
+    while (p + 1 < P.nprob && tg >= P.prob[p + 1].tile_begin) ++p;
+    const int kps = P.prob[p].kblocks / P.split_S;
+    ub = P.prob[p].unit_begin + (tg - P.prob[p].tile_begin) * P.prob[p].kblocks + sp * kps;
+    ue = ub + kps;
+  } else if (kWaves && s < P.dp_waves) {
+    const int t = blockIdx.x + s * (int)G;
+    int p = 0;
+    while (p + 1 < P.nprob && t >= P.prob[p + 1].tile_begin) ++p;
+    ub = P.prob[p].unit_begin + (t - P.prob[p].tile_begin) * P.prob[p].kblocks;
+    ue = ub + P.prob[p].kblocks;
+  } else {
+    const int sk0 = kWaves ? P.sk_unit0 : 0;  // (no waves: the whole launch is Stream-K)
+    const int64_t Usk = P.total_units - sk0;
+    ub = sk0 + (int)cta_start(blockIdx.x, Usk, G);
+    ue = sk0 + (int)cta_start(blockIdx.x + 1, Usk, G);
+  }
+}
+
+// The product for few token tiles (decode) and split-K: each CTA one contiguous Stream-K range of
+// units (or one k-range of a tile).
 __global__ void __launch_bounds__(kThreads, 2) k_gemm_tc(const __grid_constant__ Params P) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = tc::smem_u32(smem_raw);
@@ -135,7 +178,10 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemm_tc(const __grid_constant__
   if (warp == 4) {
     // ---------------------------------------------------------------- TMA producer
     if (lane == 0) {
-      const uint64_t pol_w = tc::policy_evict_first(), pol_x = tc::policy_evict_last();
+      const uint64_t pol_first = tc::policy_evict_first(), pol_normal = tc::policy_evict_normal(),
+                     pol_last = tc::policy_evict_last();
+      auto pol = [&](int sel) { return sel == 0 ? pol_first : (sel == 1 ? pol_normal : pol_last); };
+      const uint64_t pol_w = pol(P.prob[0].pol_a), pol_x = pol(P.prob[0].pol_b);
       int stage = 0;
       uint32_t phase = 0;
       int issued = 0;
@@ -384,6 +430,347 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemm_tc(const __grid_constant__
   if (threadIdx.x == 0 && *abort_flag) atomicOr(P.status, kStatusTimeout);
 }
 
+// The same product with data-parallel waves (many token tiles, large activations): each CTA takes
+// the whole tiles c, c + G, ... and then its Stream-K share of the tiles of the last, partial wave.
+// (A separate kernel: folding the segment loops into the one above measured slower at decode.)
+__global__ void __launch_bounds__(kThreads, 2) k_gemm_tc_waves(const __grid_constant__ Params P) {
+  constexpr bool kWaves = true;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = tc::smem_u32(smem_raw);
+  uint8_t *smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
+  const int S = P.stages, BN = P.BN;
+  const uint32_t a_atom = BM * BK * 2, b_atom = (uint32_t)BN * BK * 2;
+  const uint32_t a_bytes = ATOMS * a_atom, b_bytes = ATOMS * b_atom, stage_bytes = a_bytes + b_bytes;
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + S * stage_bytes);
+  uint64_t *empty = full + S;
+  uint64_t *accf = empty + S;  // [2]
+  uint64_t *acce = accf + 2;   // [2]
+  uint64_t *drain = acce + 2;
+  uint64_t *epi = drain + 1;  // the 128 epilogue threads' own barrier
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(epi + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  int *s_last = const_cast<int *>(abort_flag) + 1;
+  int *cslot = s_last + 1;  // [kMaxContrib] partial slots of a tile's contributors, in CTA order
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t U = P.total_units, G = gridDim.x;
+  const int nseg = kWaves ? P.dp_waves + 1 : 1;
+  int sk_b, sk_e;  // the last segment: the Stream-K share (or the split-K range)
+  seg_range<kWaves>(P, nseg - 1, sk_b, sk_e);
+  if (nseg == 1 && sk_b >= sk_e) return;
+  const uint32_t tmem_cols = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128 : (2 * BN <= 256) ? 256 : 512;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&accf[b], 1);
+      tc::mbar_init(&acce[b], 128);
+    }
+    tc::mbar_init(drain, 1);
+    tc::mbar_init(epi, 128);
+    *abort_flag = 0;
+    tc::fence_barrier_init();
+  }
+  if (warp == 5) tc::tmem_alloc(tmem_slot, tmem_cols);
+  if (warp == 4 && lane == 0) {
+    for (int p = 0; p < P.nprob; ++p) {
+      tc::prefetch_tmap(&P.prob[p].tmA);
+      tc::prefetch_tmap(&P.prob[p].tmB);
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 4) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      const uint64_t pol_first = tc::policy_evict_first(), pol_normal = tc::policy_evict_normal(),
+                     pol_last = tc::policy_evict_last();
+      auto pol = [&](int sel) { return sel == 0 ? pol_first : (sel == 1 ? pol_normal : pol_last); };
+      int stage = 0;
+      uint32_t phase = 0;
+      int issued = 0;
+      bool ok = true;
+      for (int sg = 0; sg < nseg && ok; ++sg) {
+      int ub, ue;
+      seg_range<kWaves>(P, sg, ub, ue);
+      if (ub >= ue) continue;
+      // the unit's coordinates, decoded once per segment and then advanced without divisions (this
+      // loop paces the copies)
+      Unit un = decode_unit(P, ub);
+      const Problem *pr = &P.prob[un.p];
+      int tm = un.tile % pr->tiles_m, tn = (un.tile / pr->tiles_m) % pr->tiles_n;
+      int g = un.tile / (pr->tiles_m * pr->tiles_n);
+      // the problem's fields in registers, refreshed when the problem changes
+      int kblocks = pr->kblocks, ntiles = pr->tiles, tiles_m = pr->tiles_m, tiles_n = pr->tiles_n, N = pr->N,
+          Kg = pr->Kg;
+      uint64_t pa = pol(pr->pol_a), pb = pol(pr->pol_b);
+      for (int u = ub; u < ue; ++u) {
+        if (!(ok = tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag))) break;
+        uint8_t *sa = smem + stage * stage_bytes;
+        tc::mbar_expect_tx(&full[stage], stage_bytes);
+#pragma unroll
+        for (int a = 0; a < ATOMS; ++a) {
+          const int k0 = (un.kb * ATOMS + a) * BK;
+          tc::tma_load_2d(sa + a * a_atom, &pr->tmA, &full[stage], k0, g * N + tn * BM, pa);
+          tc::tma_load_2d(sa + a_bytes + a * b_atom, &pr->tmB, &full[stage], g * Kg + k0, tm * BN, pb);
+        }
+        ++issued;
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1;
+        }
+        if (++un.kb == kblocks) {  // next tile: token tile fastest, then weight tile, then group
+          un.kb = 0;
+          if (++un.tile == ntiles) {
+            un.tile = 0;
+            tm = tn = g = 0;
+            if (++un.p < P.nprob) {
+              pr = &P.prob[un.p];
+              kblocks = pr->kblocks;
+              ntiles = pr->tiles;
+              tiles_m = pr->tiles_m;
+              tiles_n = pr->tiles_n;
+              N = pr->N;
+              Kg = pr->Kg;
+              pa = pol(pr->pol_a);
+              pb = pol(pr->pol_b);
+            }
+          } else if (++tm == tiles_m) {
+            tm = 0;
+            if (++tn == tiles_n) {
+              tn = 0;
+              ++g;
+            }
+          }
+        }
+      }
+      }
+      // let every copy this CTA issued land before the CTA can exit
+      for (int i = issued - S > 0 ? issued - S : 0; i < issued; ++i) {
+        uint64_t *b = &full[i % S];
+        const uint32_t par = (uint32_t)((i / S) & 1);
+        const uint64_t t0 = tc::global_ns();
+        while (!tc::mbar_try_wait(b, par) && tc::global_ns() - t0 < tc::kWaitLimitNs) {
+        }
+      }
+    }
+  } else if (warp == 5) {
+    // ---------------------------------------------------------------- MMA issue
+    if (lane == 0) {
+      const uint32_t idesc = tc::idesc_bf16_f32(BM, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int used[2] = {0, 0};
+      int buf = 0;
+      bool ok = true;
+      for (int sg = 0; sg < nseg && ok; ++sg) {
+      int ub, ue;
+      seg_range<kWaves>(P, sg, ub, ue);
+      for (int u = ub; u < ue && ok;) {
+        const Unit un = decode_unit(P, u);
+        const Problem &pr = P.prob[un.p];
+        const int seg_end = min(ue, pr.unit_begin + (un.tile + 1) * pr.kblocks);
+        if (!tc::mbar_wait(&acce[buf], (uint32_t)(used[buf] & 1) ^ 1u, abort_flag)) break;
+        tc::tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)(buf * BN);
+        bool first = true;
+        for (; u < seg_end; ++u) {
+          if (!tc::mbar_wait(&full[stage], phase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc::tc_fence_after();
+          const uint32_t sa = tc::smem_u32(smem + stage * stage_bytes);
+#pragma unroll
+          for (int a = 0; a < ATOMS; ++a) {
+            const uint64_t ad = tc::sdesc_sw128(sa + a * a_atom, 16, 1024);
+            const uint64_t bd = tc::sdesc_sw128(sa + a_bytes + a * b_atom, 16, 1024);
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k)
+              tc::mma_bf16(d, ad + 2ull * k, bd + 2ull * k, idesc, (first && a == 0 && k == 0) ? 0u : 1u);
+          }
+          first = false;
+          tc::mma_commit(&empty[stage]);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc::mma_commit(&accf[buf]);
+        ++used[buf];
+        buf ^= 1;
+      }
+      }
+      // every MMA issued has completed once this arrives
+      tc::mma_commit(drain);
+      const uint64_t t0 = tc::global_ns();
+      while (!tc::mbar_try_wait(drain, 0) && tc::global_ns() - t0 < tc::kWaitLimitNs) {
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue (warps 0-3)
+    const int row = warp * 32 + lane;  // feature within the tile
+    int done[2] = {0, 0};
+    uint32_t epi_uses = 0;
+    auto epi_sync = [&]() -> bool {
+      tc::mbar_arrive(epi);
+      return tc::mbar_wait(epi, (epi_uses++) & 1u, abort_flag);
+    };
+    int buf = 0;
+    // the Stream-K share's first tile (its partial goes to slot 0, the last tile's to slot 1)
+    const int first_tile_global = [&] {
+      if (sk_b >= sk_e) return -1;
+      const Unit f = decode_unit(P, sk_b);
+      return P.prob[f.p].tile_begin + f.tile;
+    }();
+    const int sk0 = kWaves ? P.sk_unit0 : 0;
+    const int64_t Usk = U - sk0;
+    bool eok = true;
+    for (int sg = 0; sg < nseg && eok; ++sg) {
+    int ub, ue;
+    seg_range<kWaves>(P, sg, ub, ue);
+    for (int u = ub; u < ue;) {
+      const Unit un = decode_unit(P, u);
+      const Problem &pr = P.prob[un.p];
+      const int tile_u0 = pr.unit_begin + un.tile * pr.kblocks, tile_u1 = tile_u0 + pr.kblocks;
+      const int seg_end = min(ue, tile_u1);
+      const bool whole = (u == tile_u0) && (seg_end == tile_u1);
+      const int tm = un.tile % pr.tiles_m, rest = un.tile / pr.tiles_m;
+      const int tn = rest % pr.tiles_n, g = rest / pr.tiles_n;
+      const int f = tn * BM + row;
+      const bool f_ok = f < pr.N;
+      bf16 *ycol = pr.y + (int64_t)g * pr.N + f;
+      const int gtile = pr.tile_begin + un.tile;
+      if (!(eok = tc::mbar_wait(&accf[buf], (uint32_t)(done[buf] & 1), abort_flag))) break;
+      tc::tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(buf * BN);
+      if (P.split_S > 0) {
+        // split-K: this CTA's partial sum for (tile, k-range) as f32, coalesced over features
+        const int sp = blockIdx.x % P.split_S;
+        float *pcol = pr.part + (int64_t)g * pr.N + f;
+        for (int c0 = 0; c0 < BN; c0 += 16) {
+          uint32_t r[16];
+          tc::tmem_ld16(taddr + (uint32_t)c0, r);
+          tc::tmem_ld_wait();
+          if (f_ok) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int j = tm * BN + c0 + i;
+              if (j < pr.M) pcol[((int64_t)sp * pr.M + j) * pr.ldp] = __uint_as_float(r[i]);
+            }
+          }
+        }
+        tc::tc_fence_before();
+        tc::mbar_arrive(&acce[buf]);
+        ++done[buf];
+        buf ^= 1;
+        u = seg_end;
+        continue;
+      }
+      const int slot = (int)blockIdx.x * 2 + (gtile == first_tile_global ? 0 : 1);
+      float *mine = P.partials + (size_t)slot * BM * BN + (size_t)row * BN;
+      for (int c0 = 0; c0 < BN; c0 += 16) {
+        uint32_t r[16];
+        tc::tmem_ld16(taddr + (uint32_t)c0, r);
+        tc::tmem_ld_wait();
+        if (whole) {
+          if (f_ok) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int j = tm * BN + c0 + i;
+              if (j < pr.M) ycol[(int64_t)j * pr.ldy] = __float2bfloat16_rn(__uint_as_float(r[i]));
+            }
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; i += 4)
+            *reinterpret_cast<float4 *>(mine + c0 + i) =
+                make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]), __uint_as_float(r[i + 2]),
+                            __uint_as_float(r[i + 3]));
+        }
+      }
+      tc::tc_fence_before();
+      tc::mbar_arrive(&acce[buf]);
+      ++done[buf];
+      buf ^= 1;
+      if (!whole) {
+        // Stream-K fixup: the last contributor of this tile sums the partials in CTA order.
+        __threadfence();
+        if (!(eok = epi_sync())) break;
+        const int64_t c_first = unit_owner(tile_u0 - sk0, Usk, G), c_last = unit_owner(tile_u1 - 1 - sk0, Usk, G);
+        if (threadIdx.x == 0) {
+          const int old = atomicAdd(&P.counters[gtile], 1);
+          *s_last = (old == (int)(c_last - c_first)) ? 1 : 0;
+        }
+        if (!(eok = epi_sync())) break;
+        if (*s_last) {
+          __threadfence();
+          const int nc = (int)(c_last - c_first + 1);
+          for (int i = threadIdx.x; i < nc; i += 128) {
+            const int64_t c = c_first + i;
+            const Unit f0 = decode_unit(P, sk0 + (int)cta_start(c, Usk, G));
+            cslot[i] = (int)c * 2 + (gtile == P.prob[f0.p].tile_begin + f0.tile ? 0 : 1);
+          }
+          if (!(eok = epi_sync())) break;
+          // sum the contributors' rows in CTA order, four contributors' 16-column chunks in flight
+          const float *base = P.partials + (size_t)row * BN;
+          for (int c0 = 0; c0 < BN; c0 += 16) {
+            float a[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) a[i] = 0.f;
+            for (int i = 0; i < nc; i += 4) {
+              float4 v[4][4];
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                if (i + q < nc) {
+                  const float4 *src = reinterpret_cast<const float4 *>(base + (size_t)cslot[i + q] * BM * BN + c0);
+#pragma unroll
+                  for (int k = 0; k < 4; ++k) v[q][k] = __ldcg(src + k);
+                }
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                if (i + q < nc) {
+#pragma unroll
+                  for (int k = 0; k < 4; ++k) {
+                    a[4 * k] += v[q][k].x;
+                    a[4 * k + 1] += v[q][k].y;
+                    a[4 * k + 2] += v[q][k].z;
+                    a[4 * k + 3] += v[q][k].w;
+                  }
+                }
+            }
+            if (f_ok) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const int j = tm * BN + c0 + i;
+                if (j < pr.M) ycol[(int64_t)j * pr.ldy] = __float2bfloat16_rn(a[i]);
+              }
+            }
+          }
+          if (threadIdx.x == 0) P.counters[gtile] = 0;
+        }
+        // the flag is rewritten for the next tile only after everyone has read it
+        if (!(eok = epi_sync())) break;
+      }
+      u = seg_end;
+    }
+    }
+  }
+  __syncthreads();
+  if (warp == 5) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem_base, tmem_cols);
+  }
+  if (threadIdx.x == 0 && *abort_flag) atomicOr(P.status, kStatusTimeout);
+}
+
 // ---- host ---------------------------------------------------------------------------------------
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -426,6 +813,26 @@ bool tma_map_2d_bf16(CUtensorMap *m, const void *base, uint64_t inner, uint64_t 
   return gemm::map_2d(m, base, inner, outer, ld, box_inner, box_outer);
 }
 
+// L2 policies: a weight read by one token tile only (few tokens) streams past evict-first; one
+// re-read by several token tiles stays normal.  Activations that all weight tiles re-read stay
+// evict-last while they are small next to L2, normal otherwise.
+static void set_policies(gemm::Problem &p, const LinearProblem &q, int M) {
+  p.pol_a = p.tiles_m == 1 ? 0 : 1;
+  const size_t x_bytes = (size_t)M * q.K * q.groups * 2;
+  p.pol_b = x_bytes <= ((size_t)16 << 20) ? 2 : 1;
+}
+// The kernels take the launch's policies from its first problem: problems that disagree get normal.
+static void unify_policies(gemm::Params &P, int nprob) {
+  for (int i = 1; i < nprob; ++i) {
+    if (P.prob[i].pol_a != P.prob[0].pol_a) P.prob[0].pol_a = 1;
+    if (P.prob[i].pol_b != P.prob[0].pol_b) P.prob[0].pol_b = 1;
+  }
+  for (int i = 1; i < nprob; ++i) {
+    P.prob[i].pol_a = P.prob[0].pol_a;
+    P.prob[i].pol_b = P.prob[0].pol_b;
+  }
+}
+
 int gemm_tc_bn(int M) {
   if (M > 256) return 256;
   int bn = (M + 15) / 16 * 16;
@@ -465,12 +872,14 @@ cudaError_t launch_gemm_tc(const LinearProblem *probs, int nprob, float *ws, siz
     p.tiles_n = (q.N + BM - 1) / BM;
     p.tiles_m = (M + P.BN - 1) / P.BN;
     p.tiles = p.tiles_n * p.tiles_m * q.groups;
+    set_policies(p, q, M);
     p.unit_begin = units;
     p.tile_begin = tiles;
     units += p.tiles * p.kblocks;
     tiles += p.tiles;
   }
   P.nprob = nprob;
+  unify_policies(P, nprob);
   P.total_units = units;
   P.total_tiles = tiles;
   P.split_S = 0;
@@ -479,6 +888,31 @@ cudaError_t launch_gemm_tc(const LinearProblem *probs, int nprob, float *ws, siz
   if (ws_bytes < kCounterBytes + part_per_cta) return cudaErrorInvalidValue;
   const int ws_grid = (int)std::min<size_t>((ws_bytes - kCounterBytes) / part_per_cta, (size_t)(kMaxContrib - 1));
   const int grid = std::min(std::min(per_sm * num_sms, units), ws_grid);
+  // many token tiles and large activations (prefill): whole tiles in data-parallel waves first, so that the tiles in
+  // flight at a time are consecutive ones whose operands fit in L2 together (contiguous Stream-K
+  // ranges would have every CTA stream its own far-apart tiles, re-reading each operand tile from
+  // DRAM); Stream-K only over the tiles of the last, partial wave.  Few token tiles: Stream-K alone.
+  bool many_m = true;  // many token tiles, and activations well beyond what L2 holds
+  for (int i = 0; i < nprob; ++i)
+    many_m = many_m && P.prob[i].tiles_m > 1 && (size_t)M * probs[i].K * probs[i].groups * 2 > kWaveActBytes;
+  P.dp_waves = many_m ? tiles / grid : 0;
+  {
+    // the Stream-K part must give every CTA at least one unit (the fixup counts every CTA between a
+    // tile's first and last owner as a contributor): keep one more wave in it when it would not
+    auto unit_of_tile = [&](int t) {
+      int p = 0;
+      while (p + 1 < nprob && t >= P.prob[p + 1].tile_begin) ++p;
+      return t >= tiles ? units : P.prob[p].unit_begin + (t - P.prob[p].tile_begin) * P.prob[p].kblocks;
+    };
+    if (P.dp_waves > 0 && units - unit_of_tile(P.dp_waves * grid) < grid && units - unit_of_tile(P.dp_waves * grid) > 0)
+      --P.dp_waves;
+  }
+  {
+    const int t = P.dp_waves * grid;  // first tile of the Stream-K part
+    int p = 0;
+    while (p + 1 < nprob && t >= P.prob[p + 1].tile_begin) ++p;
+    P.sk_unit0 = t >= tiles ? units : P.prob[p].unit_begin + (t - P.prob[p].tile_begin) * P.prob[p].kblocks;
+  }
   P.counters = reinterpret_cast<int *>(ws);
   P.partials = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(ws) + kCounterBytes);
   P.status = status;
@@ -486,10 +920,15 @@ cudaError_t launch_gemm_tc(const LinearProblem *probs, int nprob, float *ws, siz
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k_gemm_tc_waves, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  k_gemm_tc<<<grid, kThreads, smem, s>>>(P);
+  if (P.dp_waves > 0)
+    k_gemm_tc_waves<<<grid, kThreads, smem, s>>>(P);
+  else
+    k_gemm_tc<<<grid, kThreads, smem, s>>>(P);
   return cudaGetLastError();
 }
 
@@ -537,15 +976,19 @@ cudaError_t launch_gemm_tc_split(const LinearProblem *probs, int nprob, int S, i
     p.tiles_n = (q.N + BM - 1) / BM;
     p.tiles_m = (M + P.BN - 1) / P.BN;
     p.tiles = p.tiles_n * p.tiles_m * q.groups;
+    set_policies(p, q, M);
     p.unit_begin = units;
     p.tile_begin = tiles;
     units += p.tiles * p.kblocks;
     tiles += p.tiles;
   }
   P.nprob = nprob;
+  unify_policies(P, nprob);
   P.total_units = units;
   P.total_tiles = tiles;
   P.split_S = S;
+  P.dp_waves = 0;
+  P.sk_unit0 = 0;
   P.status = status;
   const size_t smem = 1024 + (size_t)P.stages * stage_bytes + 256 + kMaxContrib * sizeof(int);
   static bool attr = false;

@@ -115,7 +115,9 @@ def test_kv_finish_bit_exact(csa, orc, hd, rd, W, T, start):
 # ---------------------------------------------------------------------------------- projections
 
 @pytest.mark.parametrize("M,K,N,groups", [(12, 256, 64, 1), (32, 5120, 1280, 1), (33, 1280, 4096, 1),
-                                          (32, 4096, 1024, 8), (200, 512, 96, 2), (1, 64, 32, 1)])
+                                          (32, 4096, 1024, 8), (200, 512, 96, 2), (1, 64, 32, 1),
+                                          # many token tiles, activations that fit in L2: Stream-K
+                                          (600, 512, 8192, 1), (520, 256, 1024, 8), (1030, 320, 4096, 2)])
 def test_linear(csa, orc, M, K, N, groups):
     rng = np.random.default_rng(4 + M + N)
     x = _rng_bf16(orc, rng, (M, K * groups))
@@ -129,6 +131,22 @@ def test_linear(csa, orc, M, K, N, groups):
     xa, wa = np.abs(bf(x).astype(np.float64)), np.abs(bf(W).astype(np.float64))
     absdot = np.concatenate([xa[:, gi * K:(gi + 1) * K] @ wa[gi * N:(gi + 1) * N].T for gi in range(groups)], 1)
     assert (np.abs(g - w) <= np.abs(w) * 2 ** -7 + K * 2.0 ** -24 * absdot * 2 + 1e-30).all()
+
+
+@pytest.mark.parametrize("M,K,N,groups", [(7680, 1024, 128, 8), (6200, 2048, 256, 8)])
+def test_linear_waves(csa, orc, M, K, N, groups):
+    """Activations above 96 MiB with many token tiles: whole tiles in waves, then Stream-K over the
+    last partial wave.  The oracle computes sampled rows (every token tile, its edges and the ragged
+    last one), all columns."""
+    rng = np.random.default_rng(40 + M)
+    x = _rng_bf16(orc, rng, (M, K * groups))
+    W = _rng_bf16(orc, rng, (N * groups, K), 1.0 / math.sqrt(K))
+    ctx, _ = _ctx(csa, dim=64, max_tokens=1, max_batch=1, max_seq=16)
+    got = to_np(ctx.linear(to_dev(x), to_dev(W), groups=groups))
+    rows = sorted(set([0, 1, 255, 256, 257, M - 1, M - 2] + list(range(100, M, 256)) +
+                      list(rng.integers(0, M, 24))))
+    want = np.concatenate([orc.linear_bf16(x[rows, g * K:(g + 1) * K], W[g * N:(g + 1) * N]) for g in range(groups)], 1)
+    assert_close_bf16(got[rows], want, what="linear (waves)")
 
 
 def test_rmsnorm(csa, orc):
