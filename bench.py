@@ -34,9 +34,10 @@ sys.path.insert(0, ROOT)
 METRIC = "decode tokens/s per layer; sparse_attn+indexer HBM GB/s vs 8 TB/s (1×GB300)"
 DEFAULT_WORKLOAD = "reindex_decode_r2"
 NOMINAL_HBM_GBS = 8000.0
-# ncu dram__bytes_read.sum + dram__bytes_write.sum of one forward's k_gemm_tc launches
-GEMM_TRAFFIC_BYTES = {"reindex_decode_r2": int((19.05152 + 95.388928 + 3.118592 + 69.261824 + 1.008896 + 84.780544 +
-                                                2.23232) * 1e6)}
+# ncu dram__bytes_read.sum + dram__bytes_write.sum of one forward's k_gemm_tc launches (proj x, proj qr,
+# wo_a, wo_b), captured on the current kernel build
+GEMM_TRAFFIC_BYTES = {"reindex_decode_r2": (19058688 + 0) + (95180032 + 187904) + (69254912 + 88576) +
+                                           (84550400 + 189440)}
 
 
 def parse():
@@ -389,8 +390,8 @@ def run_csa(args, rank, world, dist):
     hbm_peak = peaks["hbm_gbs"] if peaks else 6800.0
     peak_src = "measured" if peaks else "fallback"
     lin_gbs = lin_bytes / (lin_ms * 1e6) if lin_ms > 0 else 0.0
-    # DRAM bytes (read + write) of the four projection launches of one forward, from the ncu capture
-    # summarised in profiles/k_gemm_tc_reindex_decode_r2.md (same kernel build); other workloads: none
+    # DRAM bytes (read + write) of the four projection launches of one forward, from an ncu capture of
+    # the same kernel build; other workloads: none
     traffic = GEMM_TRAFFIC_BYTES.get(wl.name)
     roofline = {"kernel": "linear (weight-streaming projections, all launches of one step)", "bound": "hbm",
                 "achieved": round(lin_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
