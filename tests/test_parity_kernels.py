@@ -260,6 +260,10 @@ def test_index_scores_gathered(csa, orc, Hi, B, start, L, clen, ratio, keep, cb)
     (3, 1, 40, 64, 7, 1, 0, 8, 16),
     (1, 1, 65535, 16384, 16384, 4, 0, 64, 512),    # more valid positions than shared memory holds
     (1, 2, 8191, 4096, 4096, 2, 0, 64, 2048),      # K above the one-element-per-thread sort
+    (1, 64, 4032, 1024, 1024, 4, 0, 64, 512),      # 1008..1024 valid, the selection a real cut
+    (3, 1, 700, 512, 400, 2, 0.5, 64, 512),        # masked, fewer valid than K
+    (1, 2, 100, 128, 128, 1, 0, 64, 600),          # K beyond the positions: -1 tail
+    (2, 5, 250, 256, 256, 1, 0.25, 128, 64),       # blocks of 128, K below the valid count
 ])
 def test_index_topk_bit_exact(csa, orc, B, T, start, L, clen, ratio, keep, cb, K):
     rng = np.random.default_rng(7 + T)
