@@ -110,13 +110,14 @@ __device__ __forceinline__ uint32_t order_key(float f) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-constexpr int kTopkThreads = 1024;
 constexpr int kTopkMaxK = 2048;
 constexpr int kTopkCap = 12288;  // valid positions of one query held in shared memory (96 KiB at most)
 // dynamic shared memory for candidate buffers of `cap` values
-constexpr size_t topk_smem(int cap) { return (size_t)(cap + kTopkMaxK + kTopkThreads) * 8; }
+constexpr size_t topk_smem(int cap, int nt) { return (size_t)(cap + kTopkMaxK + nt) * 8; }
 
-__global__ void __launch_bounds__(kTopkThreads, 2) k_index_topk(const float *__restrict__ S, int T, int start_pos,
+// NT threads: 1024 for long rows, 512 (four CTAs an SM) for rows of at most 2048 positions
+template <int NT>
+__global__ void __launch_bounds__(NT, 2048 / NT) k_index_topk(const float *__restrict__ S, int T, int start_pos,
                                                              int Lstride, int compress_len, int ratio,
                                                              const uint8_t *__restrict__ cand, int cand_width,
                                                              int cand_block, int K, int offset, int32_t *__restrict__ out,
@@ -124,7 +125,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k_index_topk(const float *__r
   extern __shared__ unsigned long long tk_smem[];
   unsigned long long *vals = tk_smem;                 // [cap_vals] the valid values
   unsigned long long *chosen = vals + cap_vals;       // [kTopkMaxK] the selection
-  unsigned long long *swap = chosen + kTopkMaxK;      // [kTopkThreads] sort buffer
+  unsigned long long *swap = chosen + kTopkMaxK;      // [NT] sort buffer
   __shared__ unsigned hist[256];
   __shared__ unsigned s_count, s_nchosen;
   __shared__ unsigned long long s_prefix;
@@ -259,7 +260,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2) k_index_topk(const float *__r
   while (cap < nsel) cap <<= 1;
   int32_t *o = out + row * K;
   auto pos_of = [&](unsigned long long x) { return (int32_t)(~(uint32_t)(x & 0xffffffffull)) + offset; };
-  if (cap <= kTopkThreads) {
+  if (cap <= NT) {
     // bitonic sort, descending: thread i holds element i; warps past the padded length only keep
     // the shared stages' barriers
     const bool holds = (tid & ~31) < cap;
@@ -319,8 +320,11 @@ cudaError_t launch_index_topk(const float *S, int B, int T, int start_pos, int L
   if (K > kTopkMaxK) return cudaErrorInvalidValue;
   static bool attr = false;
   if (!attr) {
-    cudaError_t e =
-        cudaFuncSetAttribute(k_index_topk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)topk_smem(kTopkCap));
+    cudaError_t e = cudaFuncSetAttribute(k_index_topk<1024>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)topk_smem(kTopkCap, 1024));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k_index_topk<512>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)topk_smem(kTopkCap, 512));
     if (e != cudaSuccess) return e;
     attr = true;
   }
@@ -328,8 +332,14 @@ cudaError_t launch_index_topk(const float *S, int B, int T, int start_pos, int L
   // two CTAs per SM; the sort buffers need at least as many values as the sort's padded length
   const int max_limit = std::min((start_pos + T) / std::max(ratio, 1), compress_len);
   const int cap = std::min(kTopkCap, std::max(max_limit, kTopkMaxK));
-  k_index_topk<<<B * T, kTopkThreads, topk_smem(cap), s>>>(S, T, start_pos, Lstride, compress_len, ratio, cand,
-                                                           cand_width, cand_block, K, offset, out, cap);
+  // short rows (every query's limit within 2048, K within the 512-thread sort): 512 threads, four
+  // CTAs an SM, cheaper block barriers
+  if (max_limit <= 2048 && K <= 512)
+    k_index_topk<512><<<B * T, 512, topk_smem(cap, 512), s>>>(S, T, start_pos, Lstride, compress_len, ratio, cand,
+                                                              cand_width, cand_block, K, offset, out, cap);
+  else
+    k_index_topk<1024><<<B * T, 1024, topk_smem(cap, 1024), s>>>(S, T, start_pos, Lstride, compress_len, ratio, cand,
+                                                                 cand_width, cand_block, K, offset, out, cap);
   return cudaGetLastError();
 }
 
