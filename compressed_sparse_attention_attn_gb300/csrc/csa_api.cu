@@ -543,13 +543,23 @@ int attn_v41_forward(csa_ctx *ctx, const csa_layer_weights *w, csa_layer_state *
     if (r.is_index_source) {
       float *S = dbg && dbg->scores ? dbg->scores : ctx->scores;
       const uint8_t *cand = r.uses_candidates ? sh->candidates : nullptr;
-      STEP(csa::launch_index_scores(qI, wI, (const bf16 *)sh->index_k, B, T, start_pos, Hi, dI, sh->compress_stride,
-                                    sh->compress_len, r.ratio, cand, sh->cand_width, g.cand_block, S, s,
-                                    ctx->status),
-           "index scores");
-      STEP(csa::launch_index_topk(S, B, T, start_pos, sh->compress_stride, sh->compress_len, r.ratio, cand,
-                                  sh->cand_width, g.cand_block, K, rows_a_len, sh->topk_idxs, s),
-           "index topk");
+      // short decode rows: scores and selection in one kernel, the scores kept on chip (unless the
+      // caller wants them in its debug buffer)
+      if (!(dbg && dbg->scores) && csa::index_fused_supported(qI, (const bf16 *)sh->index_k, T, start_pos, Hi, dI,
+                                                               sh->compress_len, r.ratio, K)) {
+        STEP(csa::launch_index_topk_fused(qI, wI, (const bf16 *)sh->index_k, B, start_pos, Hi, sh->compress_stride,
+                                          sh->compress_len, r.ratio, cand, sh->cand_width, g.cand_block, K,
+                                          rows_a_len, sh->topk_idxs, ctx->status, s),
+             "index scores + topk");
+      } else {
+        STEP(csa::launch_index_scores(qI, wI, (const bf16 *)sh->index_k, B, T, start_pos, Hi, dI,
+                                      sh->compress_stride, sh->compress_len, r.ratio, cand, sh->cand_width,
+                                      g.cand_block, S, s, ctx->status),
+             "index scores");
+        STEP(csa::launch_index_topk(S, B, T, start_pos, sh->compress_stride, sh->compress_len, r.ratio, cand,
+                                    sh->cand_width, g.cand_block, K, rows_a_len, sh->topk_idxs, s),
+             "index topk");
+      }
       sh->has_topk = 1;
     }
     if (dbg && dbg->idx)

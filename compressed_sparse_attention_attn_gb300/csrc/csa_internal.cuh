@@ -94,6 +94,13 @@ cudaError_t launch_index_scores(const bf16 *qI, const float *wI, const bf16 *KI,
 cudaError_t launch_index_topk(const float *S, int B, int T, int start_pos, int Lstride, int compress_len, int ratio,
                               const uint8_t *cand, int cand_width, int cand_block, int K, int offset, int32_t *out,
                               cudaStream_t s);
+// Scores and top-k in one kernel for decode rows (T == 1) with at most 512 valid positions (the
+// scores stay on chip); same conditions on the operands as the tensor-core scores, K <= 512.
+bool index_fused_supported(const bf16 *qI, const bf16 *KI, int T, int start_pos, int Hi, int dI, int compress_len,
+                           int ratio, int K);
+cudaError_t launch_index_topk_fused(const bf16 *qI, const float *wI, const bf16 *KI, int B, int start_pos, int Hi,
+                                    int Lstride, int compress_len, int ratio, const uint8_t *cand, int cand_width,
+                                    int cand_block, int K, int offset, int32_t *out, int *status, cudaStream_t s);
 
 struct AttnArgs {
   const bf16 *q;

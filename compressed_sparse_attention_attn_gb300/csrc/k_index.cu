@@ -3,6 +3,7 @@
 // I_t = top_K over valid j; "metrale_model_arch::attn_v41": selection offset past the window rows,
 // -1 = absent).
 #include "csa_internal.cuh"
+#include "topk_core.cuh"
 
 namespace csa {
 
@@ -103,14 +104,6 @@ cudaError_t launch_index_scores(const bf16 *qI, const float *wI, const bf16 *KI,
 // The chosen values are then sorted descending by a bitonic network whose stages within a warp run
 // on shuffles and whose wider stages go through shared memory.
 // ---------------------------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t order_key(float f) {
-  if (f != f) return 0u;   // NaN: below every number
-  if (f == 0.0f) f = 0.0f;  // -0 == +0
-  uint32_t u = __float_as_uint(f);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-constexpr int kTopkMaxK = 2048;
 constexpr int kTopkCap = 12288;  // valid positions of one query held in shared memory (96 KiB at most)
 // dynamic shared memory for candidate buffers of `cap` values
 constexpr size_t topk_smem(int cap, int nt) { return (size_t)(cap + kTopkMaxK + nt) * 8; }
@@ -126,191 +119,35 @@ __global__ void __launch_bounds__(NT, 2048 / NT) k_index_topk(const float *__res
   unsigned long long *vals = tk_smem;                 // [cap_vals] the valid values
   unsigned long long *chosen = vals + cap_vals;       // [kTopkMaxK] the selection
   unsigned long long *swap = chosen + kTopkMaxK;      // [NT] sort buffer
-  __shared__ unsigned hist[256];
-  __shared__ unsigned s_count, s_nchosen;
-  __shared__ unsigned long long s_prefix;
-  __shared__ unsigned s_remain, s_done;
-  __shared__ int s_shift;
+  __shared__ TopkShared sh;
   const int64_t row = blockIdx.x;
   const int t = (int)(row % T);
   const int p = start_pos + t;
   const int limit = min((p + 1) / ratio, compress_len);
   const uint8_t *cr = cand ? cand + row * cand_width : nullptr;
   const float *Sr = S + row * Lstride;
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const unsigned below = (1u << lane) - 1u;
+  const int tid = threadIdx.x;
   auto value_at = [&](int j) {
     return ((unsigned long long)order_key(Sr[j]) << 32) | (unsigned long long)(~(uint32_t)j);
   };
-  // append v (where take) to buf[cap] through counter cnt: one atomic per warp
-  auto append = [&](bool take, unsigned long long v, unsigned *cnt, unsigned long long *buf, unsigned cap) {
-    const unsigned bal = __ballot_sync(0xffffffffu, take);
-    unsigned base = 0;
-    if (lane == 0 && bal) base = atomicAdd(cnt, (unsigned)__popc(bal));
-    base = __shfl_sync(0xffffffffu, base, 0);
-    const unsigned slot = base + __popc(bal & below);
-    if (take && slot < cap) buf[slot] = v;
-  };
 
   // pass 1: count the valid positions, compacting their values while they fit
-  if (tid == 0) {
-    s_count = 0;
-    s_nchosen = 0;
-    s_prefix = 0ull;
-    s_remain = (unsigned)K;
-    s_done = 0;
-    s_shift = 0;
-  }
+  if (tid == 0) topk_shared_init(sh, K);
   __syncthreads();
   for (int j0 = 0; j0 < limit; j0 += blockDim.x) {
     const int j = j0 + tid;
     const bool v = j < limit && comp_valid(j, limit, cr, cand_block);
-    append(v, v ? value_at(j) : 0ull, &s_count, vals, (unsigned)cap_vals);
+    topk_append(v, v ? value_at(j) : 0ull, &sh.count, vals, (unsigned)cap_vals);
   }
   __syncthreads();
-  const unsigned nvalid = s_count;
-  const bool all = nvalid <= (unsigned)K;
+  const unsigned nvalid = sh.count;
   const bool in_smem = nvalid <= (unsigned)cap_vals;
-  const int n_iter = in_smem ? (int)nvalid : limit;  // candidates: vals[0..nvalid) or positions 0..limit
-  unsigned long long *sorted = vals;
-  if (!all) {
-    // radix select of the K-th largest value, 8 bits per pass from the top
-    for (int shift = 56; shift >= 0; shift -= 8) {
-      for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0;
-      __syncthreads();
-      const unsigned long long prefix = s_prefix;
-      const unsigned long long hi_mask = shift == 56 ? 0ull : (~0ull << (shift + 8));
-      for (int i0 = 0; i0 < n_iter; i0 += blockDim.x) {
-        const int i = i0 + tid;
-        int bin = 256 + lane;  // no bin: a value of every lane of its own
-        if (i < n_iter) {
-          bool ok = true;
-          unsigned long long v = 0ull;
-          if (in_smem) {
-            v = vals[i];
-          } else {
-            ok = comp_valid(i, limit, cr, cand_block);
-            if (ok) v = value_at(i);
-          }
-          if (ok && (v & hi_mask) == (prefix & hi_mask)) bin = (int)((v >> shift) & 255u);
-        }
-        const unsigned peers = __match_any_sync(0xffffffffu, bin);
-        if (bin < 256 && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], (unsigned)__popc(peers));
-      }
-      __syncthreads();
-      if (wid == 0) {
-        // the digit holding the remain-th largest value: lane l scans digits 255-8l down to 248-8l
-        unsigned c[8], tot = 0;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          c[k] = hist[255 - 8 * lane - k];
-          tot += c[k];
-        }
-        unsigned incl = tot;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const unsigned n = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += n;
-        }
-        const unsigned excl = incl - tot, remain = s_remain;
-        if (excl < remain && remain <= incl) {
-          unsigned above = excl;
-          int d = 255 - 8 * lane;
-          unsigned cd = 0;
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            d = 255 - 8 * lane - k;
-            cd = c[k];
-            if (above + cd >= remain) break;
-            above += cd;
-          }
-          s_prefix = prefix | ((unsigned long long)d << shift);
-          s_remain = remain - above;
-          s_shift = shift;
-          if (cd == remain - above) s_done = 1;  // every value with this prefix is taken
-        }
-      }
-      __syncthreads();
-      if (s_done) break;
-    }
-    // the selection: values above the prefix at the final digit, and every value equal to it there
-    const int sh = s_shift;
-    const unsigned long long thr = s_prefix >> sh;
-    for (int i0 = 0; i0 < n_iter; i0 += blockDim.x) {
-      const int i = i0 + tid;
-      bool take = false;
-      unsigned long long v = 0ull;
-      if (i < n_iter) {
-        bool ok = true;
-        if (in_smem) {
-          v = vals[i];
-        } else {
-          ok = comp_valid(i, limit, cr, cand_block);
-          if (ok) v = value_at(i);
-        }
-        take = ok && (v >> sh) >= thr;
-      }
-      append(take, v, &s_nchosen, chosen, (unsigned)kTopkMaxK);
-    }
-    __syncthreads();
-    sorted = chosen;
-  }
-  const int nsel = all ? (int)nvalid : K;
-  int cap = 32;
-  while (cap < nsel) cap <<= 1;
-  int32_t *o = out + row * K;
-  auto pos_of = [&](unsigned long long x) { return (int32_t)(~(uint32_t)(x & 0xffffffffull)) + offset; };
-  if (cap <= NT) {
-    // bitonic sort, descending: thread i holds element i; warps past the padded length only keep
-    // the shared stages' barriers
-    const bool holds = (tid & ~31) < cap;
-    unsigned long long x = 0ull;  // padding sorts last
-    if (tid < nsel) x = sorted[tid];
-    int nb = 0;
-    for (int size = 2; size <= cap; size <<= 1) {
-      // stages of stride 32 and up go through shared memory, the rest are shuffles
-      for (int stride = size >> 1; stride >= 32; stride >>= 1) {
-        unsigned long long *bp = nb ? swap : chosen;  // alternate buffers: one barrier per stage
-        if (tid < cap) bp[tid] = x;
-        __syncthreads();
-        if (tid < cap) {
-          const unsigned long long y = bp[tid ^ stride];
-          const bool keep_max = ((tid & size) == 0) == ((tid & stride) == 0);
-          x = keep_max ? (x > y ? x : y) : (x < y ? x : y);
-        }
-        nb ^= 1;
-      }
-      if (holds) {
-        for (int stride = min(size >> 1, 16); stride > 0; stride >>= 1) {
-          const unsigned long long y = __shfl_xor_sync(0xffffffffu, x, stride);
-          const bool keep_max = ((tid & size) == 0) == ((tid & stride) == 0);
-          x = keep_max ? (x > y ? x : y) : (x < y ? x : y);
-        }
-      }
-    }
-    for (int k = tid; k < K; k += blockDim.x) o[k] = (k == tid && k < nsel) ? pos_of(x) : -1;
-  } else {
-    unsigned long long *a = sorted;
-    for (int i = nsel + tid; i < cap; i += blockDim.x) a[i] = 0ull;
-    __syncthreads();
-    for (int size = 2; size <= cap; size <<= 1) {
-      for (int stride = size >> 1; stride > 0; stride >>= 1) {
-        for (int i = tid; i < cap; i += blockDim.x) {
-          const int jx = i ^ stride;
-          if (jx > i) {
-            const bool desc = (i & size) == 0;
-            const unsigned long long u = a[i], w = a[jx];
-            if (desc ? (u < w) : (u > w)) {
-              a[i] = w;
-              a[jx] = u;
-            }
-          }
-        }
-        __syncthreads();
-      }
-    }
-    for (int k = tid; k < K; k += blockDim.x) o[k] = k < nsel ? pos_of(a[k]) : -1;
-  }
+  auto value_at_i = [&](int i, bool &ok) -> unsigned long long {  // (the positions, in global memory)
+    ok = comp_valid(i, limit, cr, cand_block);
+    return ok ? value_at(i) : 0ull;
+  };
+  topk_finish<NT>(sh, nvalid, in_smem, in_smem ? (int)nvalid : limit, value_at_i, K, offset, vals, chosen, swap,
+                  out + row * K);
 }
 
 cudaError_t launch_index_topk(const float *S, int B, int T, int start_pos, int Lstride, int compress_len, int ratio,

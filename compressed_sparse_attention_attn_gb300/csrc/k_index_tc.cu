@@ -12,6 +12,7 @@
 // mbarrier wait is time-bounded.
 #include "csa_internal.cuh"
 #include "tc_ptx.cuh"
+#include "topk_core.cuh"
 
 #include <algorithm>
 #include <cstring>
@@ -314,6 +315,134 @@ __global__ void __launch_bounds__(kThreads) k_index_scores_gather_tc(const __gri
   if (tid == 0 && *abort_flag && P.status) atomicOr(P.status, kStatusTimeout);
 }
 
+
+// ---- fused scores + top-k for short decode rows --------------------------------------------------
+// A decode query (T == 1) with at most kFusedTiles * 128 valid positions: one CTA loads all its key
+// tiles and Q^I by TMA, runs one MMA chain per tile into its own TMEM columns, and the epilogue turns
+// each valid key's score straight into the top-k's 64-bit value in shared memory; the selection
+// and ordering then run in the same CTA (the scores never go to global memory, and the top-k needs
+// no launch of its own).  The scores' arithmetic is the dense kernel's, so the selection is the same.
+constexpr int kFusedTiles = 4;
+constexpr int kFusedThreads = 512;
+
+struct FusedParams {
+  CUtensorMap tm_k;  // K^I [B*Lstride][128], box {64, 128}
+  CUtensorMap tm_q;  // Q^I [B*Hi][128], box {64, Hi}
+  const float *wI;   // [B][Hi]
+  int Hi, Lstride, compress_len, ratio, start_pos;
+  const uint8_t *cand;
+  int cand_width, cand_block, K, offset;
+  int32_t *out;      // [B][K]
+  int *status;
+};
+
+__global__ void __launch_bounds__(kFusedThreads, 1) k_index_topk_fused_tc(const __grid_constant__ FusedParams P) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = tc::smem_u32(smem_raw);
+  uint8_t *smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
+  __shared__ TopkShared sh;
+  const int N = P.Hi;
+  constexpr uint32_t k_blk = TILE * 128;  // one 64-column half of a 128-key tile
+  const uint32_t q_blk = (uint32_t)N * 128;
+  uint8_t *sk = smem, *sq = smem + kFusedTiles * 2 * k_blk;
+  float *w_s = reinterpret_cast<float *>(sq + 2 * q_blk);                        // [Hi]
+  unsigned long long *vals = reinterpret_cast<unsigned long long *>(w_s + kMaxN);  // [512]
+  unsigned long long *chosen = vals + kFusedTiles * TILE;                        // [kTopkMaxK]
+  unsigned long long *swap = chosen + kTopkMaxK;                                 // [512]
+  uint64_t *bars = reinterpret_cast<uint64_t *>(swap + kFusedThreads);
+  uint64_t *full = bars, *done = bars + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int b = blockIdx.x;
+  const int limit = max(0, min((P.start_pos + 1) / P.ratio, P.compress_len));
+  const int ntiles = min(kFusedTiles, (limit + TILE - 1) / TILE);
+  const uint32_t ncols = N * kFusedTiles <= 32 ? 32 : N * kFusedTiles <= 64 ? 64 : N * kFusedTiles <= 128 ? 128
+                         : N * kFusedTiles <= 256 ? 256 : 512;
+  if (tid == 0) {
+    tc::mbar_init(full, 1);
+    tc::mbar_init(done, 1);
+    *abort_flag = 0;
+    topk_shared_init(sh, P.K);
+    tc::fence_barrier_init();
+    if (ntiles > 0) {
+      tc::prefetch_tmap(&P.tm_k);
+      tc::prefetch_tmap(&P.tm_q);
+      tc::mbar_expect_tx(full, (uint32_t)ntiles * 2 * k_blk + 2 * q_blk);
+      const uint64_t pol = tc::policy_evict_first();
+      for (int kb = 0; kb < 2; ++kb) tc::tma_load_2d(sq + kb * q_blk, &P.tm_q, full, kb * 64, b * N, pol);
+      for (int i = 0; i < ntiles; ++i)
+        for (int kb = 0; kb < 2; ++kb)
+          tc::tma_load_2d(sk + (2 * i + kb) * k_blk, &P.tm_k, full, kb * 64, b * P.Lstride + i * TILE, pol);
+    }
+  }
+  for (int e = tid; e < N; e += kFusedThreads) w_s[e] = P.wI[(int64_t)b * N + e];
+  if (warp == 0) tc::tmem_alloc(tmem_slot, ncols);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  if (tid == 0 && ntiles > 0) {
+    if (tc::mbar_wait(full, 0, abort_flag)) {
+      tc::tc_fence_after();
+      const uint32_t id = tc::idesc_bf16_f32(TILE, N);
+      for (int i = 0; i < ntiles; ++i) {
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb) {
+          const uint64_t ad = tc::sdesc_sw128(tc::smem_u32(sk + (2 * i + kb) * k_blk), 16, 1024);
+          const uint64_t bd = tc::sdesc_sw128(tc::smem_u32(sq + kb * q_blk), 16, 1024);
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4)
+            tc::mma_bf16(tmem + (uint32_t)(i * N), ad + 2ull * k4, bd + 2ull * k4, id, (kb | k4) ? 1u : 0u);
+        }
+      }
+      tc::mma_commit(done);
+    } else {
+      // the copies may still land: wait for them (bounded) before the CTA can exit
+      const uint64_t t0w = tc::global_ns();
+      while (!tc::mbar_try_wait(full, 0) && tc::global_ns() - t0w < tc::kWaitLimitNs) {
+      }
+    }
+  }
+  // scores of the valid keys, appended as 64-bit values (warps 0-3: TMEM lane = key within a tile)
+  const bool got = ntiles == 0 || tc::mbar_wait(done, 0, abort_flag);
+  tc::tc_fence_after();
+  if (warp < 4) {
+    const uint8_t *cr = P.cand ? P.cand + (int64_t)b * P.cand_width : nullptr;
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    for (int i = 0; i < ntiles; ++i) {
+      const int j = i * TILE + tid;
+      float acc = 0.f;
+      for (int h0 = 0; h0 < N; h0 += 16) {
+        uint32_t v[16];
+        tc::tmem_ld16_wait(lane_base + (uint32_t)(i * N + h0), v);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) acc = fmaf(w_s[h0 + k], fmaxf(__uint_as_float(v[k]), 0.f), acc);
+      }
+      const bool ok = got && j < limit && (cr == nullptr || cr[j / P.cand_block] != 0);
+      topk_append(ok, ((unsigned long long)order_key(acc) << 32) | (unsigned long long)(~(uint32_t)j), &sh.count,
+                  vals, (unsigned)(kFusedTiles * TILE));
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  auto none = [](int, bool &ok) -> unsigned long long {
+    ok = false;
+    return 0ull;
+  };
+  const unsigned nvalid = sh.count;
+  topk_finish<kFusedThreads>(sh, nvalid, true, (int)nvalid, none, P.K, P.offset, vals, chosen, swap,
+                             P.out + (int64_t)b * P.K);
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, ncols);
+  }
+  if (tid == 0 && *abort_flag && P.status) atomicOr(P.status, kStatusTimeout);
+}
+
 }  // namespace idx
 
 bool index_scores_tc_supported(const bf16 *qI, const bf16 *KI, int Hi, int dI) {
@@ -409,6 +538,49 @@ cudaError_t launch_index_scores_tc(const bf16 *qI, const float *wI, const bf16 *
                                          cand_width, cand_block, S, status, s);
   dim3 grid(tiles, (T + p.QG - 1) / p.QG, B);
   k_index_scores_tc<<<grid, kThreads, smem, s>>>(p);
+  return cudaGetLastError();
+}
+
+bool index_fused_supported(const bf16 *qI, const bf16 *KI, int T, int start_pos, int Hi, int dI, int compress_len,
+                           int ratio, int K) {
+  if (T != 1 || ratio <= 0 || K > idx::kFusedThreads || !index_scores_tc_supported(qI, KI, Hi, dI)) return false;
+  if (Hi * idx::kFusedTiles > 512) return false;
+  return std::min((start_pos + 1) / ratio, compress_len) <= idx::kFusedTiles * idx::TILE;
+}
+
+cudaError_t launch_index_topk_fused(const bf16 *qI, const float *wI, const bf16 *KI, int B, int start_pos, int Hi,
+                                    int Lstride, int compress_len, int ratio, const uint8_t *cand, int cand_width,
+                                    int cand_block, int K, int offset, int32_t *out, int *status, cudaStream_t s) {
+  using namespace idx;
+  if (B <= 0) return cudaSuccess;
+  FusedParams p;
+  memset(&p, 0, sizeof(p));
+  if (!tma_map_2d_bf16(&p.tm_k, KI, DI, (uint64_t)B * Lstride, DI, 64, TILE)) return cudaErrorInvalidValue;
+  if (!tma_map_2d_bf16(&p.tm_q, qI, DI, (uint64_t)B * Hi, DI, 64, (uint32_t)Hi)) return cudaErrorInvalidValue;
+  p.wI = wI;
+  p.Hi = Hi;
+  p.Lstride = Lstride;
+  p.compress_len = std::min(compress_len, Lstride);
+  p.ratio = ratio;
+  p.start_pos = start_pos;
+  p.cand = cand;
+  p.cand_width = cand_width;
+  p.cand_block = cand_block;
+  p.K = K;
+  p.offset = offset;
+  p.out = out;
+  p.status = status;
+  const size_t smem = 1024 + (size_t)kFusedTiles * 2 * TILE * 128 + 2 * (size_t)Hi * 128 + kMaxN * 4 +
+                      (size_t)(kFusedTiles * TILE + kTopkMaxK + kFusedThreads) * 8 + 2 * 8 + 16;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(k_index_topk_fused_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)(1024 + kFusedTiles * 2 * TILE * 128 + 2 * kMaxN * 128 + kMaxN * 4 +
+                                               (kFusedTiles * TILE + kTopkMaxK + kFusedThreads) * 8 + 2 * 8 + 16));
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  k_index_topk_fused_tc<<<B, kFusedThreads, smem, s>>>(p);
   return cudaGetLastError();
 }
 

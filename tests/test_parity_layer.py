@@ -250,11 +250,16 @@ def test_full_width_sampled(csa, orc, name, seqs, toks):
     # the benchmark's path first (no debug buffers: q's RoPE runs inside the attention kernel), then the
     # debug path (RoPE as its own pass, so the turned q can be read back); same inputs, same ring update
     out_fast = ctx.forward(wd, role, ring_d, xd, start, shared=sh)
+    sel_fast = sel_d.clone() if shared is not None else None
     dbg = _dbg(B * T, g, L, g.window + (K if wl.ratio else 0))
     out = ctx.forward(wd, role, ring_d, xd, start, shared=sh, debug=dbg)
     torch.cuda.synchronize()
     assert ctx.status() == 0
-    assert torch.equal(out_fast, out), name + ": the fused q RoPE changes the layer output"
+    # the fast path (q's RoPE inside the attention kernel; at short decode rows, scores and top-k in one
+    # kernel) must give the debug path's selection and output bit for bit
+    if sel_fast is not None and wl.is_index_source:
+        assert torch.equal(sel_fast, sel_d), name + ": the fused indexer + top-k changes the selection"
+    assert torch.equal(out_fast, out), name + ": the fast path changes the layer output"
     dbg["__out"] = out
     # oracle: only the sampled sequences (and, for the prefill chunk, the sampled tokens)
     for b in seqs:
