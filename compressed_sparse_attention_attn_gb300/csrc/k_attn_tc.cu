@@ -671,18 +671,29 @@ cudaError_t launch_sparse_attn_tc(const AttnArgs &a, float *ws, size_t ws_bytes,
   p.status = a.status;
   p.rope_q = a.rope_q;
   p.ntiles = std::max(1, (a.na + p.nb + TILE - 1) / TILE);
-  // tiles per CTA: split a query's tiles over CTAs only while there are few queries to fill the
-  // SMs (up to two CTAs per SM in the grid: tiles of entries that are all -1 cost a CTA only its
-  // index pass), and only as far as the workspace holds the shares (the GEMM's counters precede it)
+  // tiles per CTA: the choice with the least (tiles a CTA runs) x (waves of CTAs), where CTAs past
+  // the first wave that all hold the list's last tile count half a wave (that tile is the selection's
+  // tail, padding whenever fewer than K positions are valid, so its CTAs mostly end after their index
+  // pass); ties go to fewer CTAs.  The shares must fit the workspace (after the GEMM's counters).
   const int groups = a.H / HG;
   const size_t avail = ws_bytes > kGemmCounterBytes ? ws_bytes - kGemmCounterBytes : 0;
   int tpc = p.ntiles;
-  for (int c = 1; c < p.ntiles; ++c) {
+  int64_t best = INT64_MAX;
+  for (int c = 1; c <= p.ntiles; ++c) {
     const int ns = (p.ntiles + c - 1) / c;
     const size_t need = (size_t)nq * ns * a.H * (HD * sizeof(bf16) + 2 * sizeof(float));
-    if ((int64_t)nq * groups * ns <= 2 * num_sms && need <= avail) {
+    if (ns > 1 && need > avail) continue;
+    const int64_t units = (int64_t)nq * groups, ctas = units * ns;
+    int64_t cost2;  // twice the cost
+    if (ctas <= num_sms)
+      cost2 = 2 * (int64_t)c;
+    else if (ctas - num_sms <= units && (ns - 1) * c < p.ntiles)
+      cost2 = 3 * (int64_t)c;  // only CTAs of the last split spill over
+    else
+      cost2 = 2 * (int64_t)c * ((ctas + num_sms - 1) / num_sms);
+    if (cost2 <= best) {
+      best = cost2;
       tpc = c;
-      break;
     }
   }
   p.tpc = tpc;
