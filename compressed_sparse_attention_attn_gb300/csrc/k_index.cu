@@ -132,12 +132,53 @@ __global__ void __launch_bounds__(NT, 2048 / NT) k_index_topk(const float *__res
   };
 
   // pass 1: count the valid positions, compacting their values while they fit
-  if (tid == 0) topk_shared_init(sh, K);
+  __shared__ int s_wsum[NT / 32];
+  __shared__ int s_nkept;
+  if (tid == 0) {
+    topk_shared_init(sh, K);
+    s_nkept = 0;
+  }
   __syncthreads();
-  for (int j0 = 0; j0 < limit; j0 += blockDim.x) {
-    const int j = j0 + tid;
-    const bool v = j < limit && comp_valid(j, limit, cr, cand_block);
-    topk_append(v, v ? value_at(j) : 0ull, &sh.count, vals, (unsigned)cap_vals);
+  const int nblk = cr ? min((limit + cand_block - 1) / cand_block, cand_width) : 0;
+  if (cr && nblk <= 2 * NT) {
+    // with a mask: the kept blocks listed first (in the sort buffer, idle until the end), then only
+    // their positions visited
+    const int lane = tid & 31, wid = tid >> 5;
+    int *klist = reinterpret_cast<int *>(swap);
+    for (int b0 = 0; b0 < nblk; b0 += NT) {
+      const int blk = b0 + tid;
+      const bool keep = blk < nblk && cr[blk] != 0;
+      const unsigned bal = __ballot_sync(0xffffffffu, keep);
+      if (lane == 0) s_wsum[wid] = __popc(bal);
+      __syncthreads();
+      int base = s_nkept;
+      for (int w = 0; w < wid; ++w) base += s_wsum[w];
+      if (keep) klist[base + __popc(bal & ((1u << lane) - 1u))] = blk;
+      __syncthreads();
+      if (tid == 0) {
+        int tot = 0;
+        for (int w = 0; w < NT / 32; ++w) tot += s_wsum[w];
+        s_nkept += tot;
+      }
+      __syncthreads();
+    }
+    const int npos = s_nkept * cand_block;
+    for (int i0 = 0; i0 < npos; i0 += NT) {
+      const int i = i0 + tid;
+      int j = 0;
+      bool v = false;
+      if (i < npos) {
+        j = klist[i / cand_block] * cand_block + i % cand_block;
+        v = j < limit;
+      }
+      topk_append(v, v ? value_at(j) : 0ull, &sh.count, vals, (unsigned)cap_vals);
+    }
+  } else {
+    for (int j0 = 0; j0 < limit; j0 += NT) {
+      const int j = j0 + tid;
+      const bool v = j < limit && comp_valid(j, limit, cr, cand_block);
+      topk_append(v, v ? value_at(j) : 0ull, &sh.count, vals, (unsigned)cap_vals);
+    }
   }
   __syncthreads();
   const unsigned nvalid = sh.count;
