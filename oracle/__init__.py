@@ -7,7 +7,10 @@ gcc and exposes it to numpy through ctypes.  Only ``tests/``, ``__graft_entry__.
 benchmark's ``cpu_baseline`` leg may import it; the GPU library never does, and the two share no
 code.  bf16 tensors travel as ``uint16`` arrays of their bit patterns.
 
-Parity unpinned: the YaRN form of :func:`rope_table` (the pages give its constants only).
+Partly pinned: the YaRN form of :func:`rope_table` (the pages give its constants only).  Its classes
+are pinned (pairs with at least beta_fast turns over the original length keep their frequency, those
+with at most beta_slow turns run at frequency / factor, the others lie strictly between); the blend
+weights inside the ramp have no printed value to check.
 """
 import ctypes
 import os

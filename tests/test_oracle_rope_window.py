@@ -38,6 +38,23 @@ def test_rope_yarn_structure(orc):
     assert np.all(np.diff(ang) < 0)  # still monotone in the pair index
 
 
+def test_rope_yarn_pairs_by_rotation_count(orc):
+    """YaRN's frequency classes (Peng et al., 2023): a pair that completes at least beta_fast turns over
+    the original length keeps its frequency, one that completes at most beta_slow turns runs at
+    frequency / factor, and the pairs in between lie strictly between the two."""
+    L, theta, factor, rd = 65536, 160000.0, 16.0, 64
+    y = orc.rope_table(rd, L + 2, theta, orig_seq=L, factor=factor, beta_fast=32.0, beta_slow=1.0)
+    f = theta ** (-2.0 * np.arange(rd // 2) / rd)
+    turns = L * f / (2 * math.pi)
+    ang = np.arctan2(y[1, :, 1].astype(np.float64), y[1, :, 0].astype(np.float64))  # position 1: the frequency
+    fast, slow = turns >= 32.0, turns <= 1.0
+    assert fast.any() and slow.any() and (~fast & ~slow).any()
+    assert np.allclose(ang[fast], f[fast], rtol=2e-7, atol=0)
+    assert np.allclose(ang[slow], f[slow] / factor, rtol=2e-7, atol=0)
+    mid = ~fast & ~slow
+    assert np.all(ang[mid] < f[mid] * (1 - 1e-6)) and np.all(ang[mid] > f[mid] / factor * (1 + 1e-6))
+
+
 def test_rotary_adjacent_pairs_and_inverse(orc):
     rd, hd = 16, 64
     tab = orc.rope_table(rd, 64, 10000.0)
