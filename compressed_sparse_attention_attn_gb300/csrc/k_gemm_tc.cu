@@ -887,7 +887,20 @@ cudaError_t launch_gemm_tc(const LinearProblem *probs, int nprob, float *ws, siz
   const size_t part_per_cta = (size_t)2 * BM * P.BN * sizeof(float);
   if (ws_bytes < kCounterBytes + part_per_cta) return cudaErrorInvalidValue;
   const int ws_grid = (int)std::min<size_t>((ws_bytes - kCounterBytes) / part_per_cta, (size_t)(kMaxContrib - 1));
-  const int grid = std::min(std::min(per_sm * num_sms, units), ws_grid);
+  int grid = std::min(std::min(per_sm * num_sms, units), ws_grid);
+  {
+    // weight streaming (one token tile): a slightly smaller grid whose Stream-K ranges are whole
+    // tiles needs no fixup at all -- take it when one exists within 80% of the SMs (the problems of
+    // the launch sharing one k-slice count).  Compute-bound launches keep every SM.
+    bool same_kb = P.prob[0].tiles_m == 1;
+    for (int i = 1; i < nprob; ++i) same_kb = same_kb && P.prob[i].kblocks == P.prob[0].kblocks;
+    const int kb = P.prob[0].kblocks;
+    for (int gsz = grid; same_kb && gsz * 5 >= grid * 4; --gsz)
+      if (units % gsz == 0 && (units / gsz) % kb == 0) {
+        grid = gsz;
+        break;
+      }
+  }
   // many token tiles and large activations (prefill): whole tiles in data-parallel waves first, so that the tiles in
   // flight at a time are consecutive ones whose operands fit in L2 together (contiguous Stream-K
   // ranges would have every CTA stream its own far-apart tiles, re-reading each operand tile from
