@@ -895,11 +895,14 @@ cudaError_t launch_gemm_tc(const LinearProblem *probs, int nprob, float *ws, siz
     bool same_kb = P.prob[0].tiles_m == 1;
     for (int i = 1; i < nprob; ++i) same_kb = same_kb && P.prob[i].kblocks == P.prob[0].kblocks;
     const int kb = P.prob[0].kblocks;
-    for (int gsz = grid; same_kb && gsz * 5 >= grid * 4; --gsz)
-      if (units % gsz == 0 && (units / gsz) % kb == 0) {
-        grid = gsz;
-        break;
-      }
+    int pick = 0;
+    for (int gsz = grid; same_kb && gsz * 5 >= grid * 4 && !pick; --gsz)
+      if (units % gsz == 0 && (units / gsz) % kb == 0) pick = gsz;
+    // else one whose ranges are equal fractions of a tile: every fixup then has the same few
+    // contributors, all finishing together
+    for (int gsz = grid; same_kb && gsz * 5 >= grid * 4 && !pick; --gsz)
+      if (units % gsz == 0 && kb % (units / gsz) == 0) pick = gsz;
+    if (pick) grid = pick;
   }
   // many token tiles and large activations (prefill): whole tiles in data-parallel waves first, so that the tiles in
   // flight at a time are consecutive ones whose operands fit in L2 together (contiguous Stream-K
