@@ -36,8 +36,8 @@ DEFAULT_WORKLOAD = "reindex_decode_r2"
 NOMINAL_HBM_GBS = 8000.0
 # ncu dram__bytes_read.sum + dram__bytes_write.sum of one forward's k_gemm_tc launches (proj x, proj qr,
 # wo_a, wo_b), captured on the current kernel build
-GEMM_TRAFFIC_BYTES = {"reindex_decode_r2": (19058688 + 0) + (95180032 + 187904) + (69254912 + 88576) +
-                                           (84550400 + 189440)}
+GEMM_TRAFFIC_BYTES = {"reindex_decode_r2": (19058688 + 0) + (94515456 + 446976) + (69254656 + 12544) +
+                                           (84549120 + 157440)}
 
 
 def parse():
