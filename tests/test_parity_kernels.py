@@ -117,7 +117,9 @@ def test_kv_finish_bit_exact(csa, orc, hd, rd, W, T, start):
 @pytest.mark.parametrize("M,K,N,groups", [(12, 256, 64, 1), (32, 5120, 1280, 1), (33, 1280, 4096, 1),
                                           (32, 4096, 1024, 8), (200, 512, 96, 2), (1, 64, 32, 1),
                                           # many token tiles, activations that fit in L2: Stream-K
-                                          (600, 512, 8192, 1), (520, 256, 1024, 8), (1030, 320, 4096, 2)])
+                                          (600, 512, 8192, 1), (520, 256, 1024, 8), (1030, 320, 4096, 2),
+                                          # one token tile: a grid of whole tiles (144 x 1 tile, no fixup)
+                                          (32, 1280, 18432, 1)])
 def test_linear(csa, orc, M, K, N, groups):
     rng = np.random.default_rng(4 + M + N)
     x = _rng_bf16(orc, rng, (M, K * groups))
