@@ -201,13 +201,18 @@ def test_index_scores(csa, orc, B, T, start, L, clen, ratio, keep, cb):
         assert (np.abs(a - b) <= tol).all()
 
 
-@pytest.mark.parametrize("Hi,B,T,start,L,clen,ratio", [(64, 2, 7, 200, 256, 200, 2), (16, 1, 20, 0, 300, 300, 1)])
-def test_index_scores_head_counts(csa, orc, Hi, B, T, start, L, clen, ratio):
-    """Other indexer head counts: the query groups of the tensor-core kernel hold 256 / Hi queries."""
-    rng = np.random.default_rng(60 + Hi)
-    qI, wI, KI, pos, cand, S = _index_case(orc, rng, B, T, start, Hi, 128, L, clen, ratio, 0, 64)
+@pytest.mark.parametrize("Hi,B,T,start,L,clen,ratio,keep", [
+    (64, 2, 7, 200, 256, 200, 2, 0), (16, 1, 20, 0, 300, 300, 1, 0),
+    # many queries: Q^I resident, the key tiles looped over (ragged last group, a mask at prefill)
+    (64, 2, 50, 600, 700, 700, 1, 0), (16, 1, 100, 300, 512, 400, 1, 0.5), (32, 1, 200, 800, 1024, 1000, 1, 0.3),
+])
+def test_index_scores_head_counts(csa, orc, Hi, B, T, start, L, clen, ratio, keep):
+    """Other indexer head counts: the query groups of the tensor-core kernels hold 256 / Hi queries."""
+    rng = np.random.default_rng(60 + Hi + T)
+    qI, wI, KI, pos, cand, S = _index_case(orc, rng, B, T, start, Hi, 128, L, clen, ratio, keep, 64)
     Sd = torch.full((B * T, L), float("nan"), device="cuda")
-    csa.index_scores(to_dev(qI), to_dev(wI), to_dev(KI), B, T, start, clen, ratio, Sd, None, 64)
+    csa.index_scores(to_dev(qI), to_dev(wI), to_dev(KI), B, T, start, clen, ratio, Sd,
+                     None if cand is None else to_dev(cand), 64)
     got = to_np(Sd)
     valid = np.isfinite(S)
     assert np.isnan(got[~valid]).all()
