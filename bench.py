@@ -260,6 +260,21 @@ def run_reference(args, rank, world):
 
 # --------------------------------------------------------------------------------------- GPU arm
 
+def max_over_ranks(ms, dist, device):
+    """The timed region's length is the slowest rank's (every rank gets it back)."""
+    if dist is None:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world, tokens_per_step, layers, steps, total_ms):
+    """Whole-job throughput: every rank processes its own full batch (weak scaling)."""
+    return world * tokens_per_step * layers * steps / (total_ms / 1000.0)
+
+
 def run_csa(args, rank, world, dist):
     import torch
     import compressed_sparse_attention_attn_gb300 as csa
@@ -340,13 +355,10 @@ def run_csa(args, rank, world, dist):
     clk = clocks.stop()
     step_ms = [a.elapsed_time(b) for a, b in ev]
     total_ms = sum(step_ms)
-    if dist is not None:
-        tmax = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
-        total_ms = float(tmax.item())
+    total_ms = max_over_ranks(total_ms, dist, "cuda")
     ms_per_step = total_ms / args.steps
     tokens_per_step = B * T  # per layer per rank
-    value = world * tokens_per_step * wl.layers * args.steps / (total_ms / 1000.0)
+    value = job_tokens_per_s(world, tokens_per_step, wl.layers, args.steps, total_ms)
 
     # ---- per-stage kernel timing (traced forwards, flushed), for the roofline
     ctx.trace(True)
@@ -424,11 +436,8 @@ def run_csa(args, rank, world, dist):
         ev2[i][1].record(stream)
     barrier()
     e2e_ms = sum(a.elapsed_time(b) for a, b in ev2)
-    if dist is not None:
-        tmax = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tmax.item())
-    e2e_value = world * tokens_per_step * wl.layers * args.steps / (e2e_ms / 1000.0)
+    e2e_ms = max_over_ranks(e2e_ms, dist, "cuda")
+    e2e_value = job_tokens_per_s(world, tokens_per_step, wl.layers, args.steps, e2e_ms)
     io_bytes = wl.layers * B * T * g.dim * 2
 
     line = None
