@@ -28,6 +28,23 @@ struct PosSpec {
   }
 };
 
+// The dynamic shared-memory limit of a kernel is a per-device attribute: each launcher keeps one of
+// these (static) and sets the attribute once per device, raising it when a launch needs more.
+constexpr int kAttrDevices = 64;
+struct SmemAttr {
+  int set[kAttrDevices] = {};
+  cudaError_t ensure(const void *func, int need) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const bool tracked = dev >= 0 && dev < kAttrDevices;
+    if (tracked && set[dev] >= need) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, need);
+    if (e == cudaSuccess && tracked) set[dev] = need;
+    return e;
+  }
+};
+
 // ---- launchers (each returns a cudaError_t of the launch) ---------------------------------------
 
 cudaError_t launch_rmsnorm(const bf16 *x, int M, int N, const float *w, float eps, bf16 *y, cudaStream_t s);

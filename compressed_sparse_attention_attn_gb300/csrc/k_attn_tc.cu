@@ -701,12 +701,11 @@ cudaError_t launch_sparse_attn_tc(const AttnArgs &a, float *ws, size_t ws_bytes,
   uint8_t *base = reinterpret_cast<uint8_t *>(ws) + kGemmCounterBytes;
   p.part_o = reinterpret_cast<bf16 *>(base);
   p.part_ml = reinterpret_cast<float *>(base + (size_t)nq * p.nsplit * a.H * HD * sizeof(bf16));
-  static bool attr = false;
+  static SmemAttr attr;
   const size_t smem = 1024 + Smem::total;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_sparse_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  {
+    cudaError_t e = attr.ensure((const void *)k_sparse_attn_tc, (int)smem);
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   dim3 grid(nq, p.nsplit, groups);
   k_sparse_attn_tc<<<grid, kThreads, smem, s>>>(p);

@@ -933,13 +933,11 @@ cudaError_t launch_gemm_tc(const LinearProblem *probs, int nprob, float *ws, siz
   P.partials = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(ws) + kCounterBytes);
   P.status = status;
   const size_t smem = 1024 + (size_t)P.stages * stage_bytes + 256 + kMaxContrib * sizeof(int);
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(k_gemm_tc_waves, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  static SmemAttr attr, attr_waves;
+  {
+    cudaError_t e = P.dp_waves > 0 ? attr_waves.ensure((const void *)k_gemm_tc_waves, 227 * 1024)
+                                   : attr.ensure((const void *)k_gemm_tc, 227 * 1024);
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   if (P.dp_waves > 0)
     k_gemm_tc_waves<<<grid, kThreads, smem, s>>>(P);
@@ -1007,11 +1005,10 @@ cudaError_t launch_gemm_tc_split(const LinearProblem *probs, int nprob, int S, i
   P.sk_unit0 = 0;
   P.status = status;
   const size_t smem = 1024 + (size_t)P.stages * stage_bytes + 256 + kMaxContrib * sizeof(int);
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+  static SmemAttr attr;
+  {
+    cudaError_t e = attr.ensure((const void *)k_gemm_tc, 227 * 1024);
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   k_gemm_tc<<<tiles * S, kThreads, smem, s>>>(P);
   return cudaGetLastError();

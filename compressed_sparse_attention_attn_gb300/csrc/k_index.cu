@@ -74,11 +74,14 @@ cudaError_t launch_index_scores(const bf16 *qI, const float *wI, const bf16 *KI,
   const size_t smem = sizeof(float) * (size_t)Hi * (dI + 1);
   dim3 grid((Lstride + 127) / 128, B * T);
   switch (dI) {
-    case 128:
-      cudaFuncSetAttribute(k_index_scores<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    case 128: {
+      static SmemAttr attr;
+      const cudaError_t e = attr.ensure((const void *)k_index_scores<128>, (int)smem);
+      if (e != cudaSuccess) return e;
       k_index_scores<128><<<grid, 128, smem, s>>>(qI, wI, KI, T, start_pos, Hi, Lstride, compress_len, ratio, cand,
                                                   cand_width, cand_block, S);
       break;
+    }
     case 64:
       k_index_scores<64><<<grid, 128, smem, s>>>(qI, wI, KI, T, start_pos, Hi, Lstride, compress_len, ratio, cand,
                                                  cand_width, cand_block, S);
@@ -196,15 +199,11 @@ cudaError_t launch_index_topk(const float *S, int B, int T, int start_pos, int L
                               cudaStream_t s) {
   if (B * T <= 0) return cudaSuccess;
   if (K > kTopkMaxK) return cudaErrorInvalidValue;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_index_topk<1024>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)topk_smem(kTopkCap, 1024));
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(k_index_topk<512>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)topk_smem(kTopkCap, 512));
+  static SmemAttr attr512, attr1024;
+  {
+    cudaError_t e = attr1024.ensure((const void *)k_index_topk<1024>, (int)topk_smem(kTopkCap, 1024));
+    if (e == cudaSuccess) e = attr512.ensure((const void *)k_index_topk<512>, (int)topk_smem(kTopkCap, 512));
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   // room for the largest causal limit of the launch (the last query's), so that short ones keep
   // two CTAs per SM; the sort buffers need at least as many values as the sort's padded length

@@ -487,12 +487,9 @@ static cudaError_t launch_index_scores_gather_tc(const bf16 *qI, const float *wI
   const size_t smem = 1024 + (size_t)kGatherBufs * TILE * 128 * 2 + 2 * (size_t)Hi * 128 + kMaxN * 4 +
                       4 * (size_t)((p.max_units + 1) & ~1) + (2 * kGatherBufs + 1) * 8 + 16;
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
-  static int attr = 0;
-  if ((int)smem > attr) {
-    e = cudaFuncSetAttribute(k_index_scores_gather_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr = (int)smem;
-  }
+  static SmemAttr attr;
+  e = attr.ensure((const void *)k_index_scores_gather_tc, (int)smem);
+  if (e != cudaSuccess) return e;
   k_index_scores_gather_tc<<<dim3(p.P, B), kThreads, smem, s>>>(p);
   return cudaGetLastError();
 }
@@ -520,12 +517,11 @@ cudaError_t launch_index_scores_tc(const bf16 *qI, const float *wI, const bf16 *
   p.S = S;
   p.status = status;
   const size_t smem = 1024 + 2 * (size_t)TILE * 128 + 2 * (size_t)p.QG * Hi * 128 + kMaxN * 4 + 64;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_index_scores_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(1024 + 2 * TILE * 128 + 2 * kMaxN * 128 + kMaxN * 4 + 64));
+  static SmemAttr attr;
+  {
+    cudaError_t e = attr.ensure((const void *)k_index_scores_tc,
+                                (int)(1024 + 2 * TILE * 128 + 2 * kMaxN * 128 + kMaxN * 4 + 64));
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   const int tiles = (p.compress_len + TILE - 1) / TILE;
   if (tiles <= 0) return cudaSuccess;
@@ -572,13 +568,12 @@ cudaError_t launch_index_topk_fused(const bf16 *qI, const float *wI, const bf16 
   p.status = status;
   const size_t smem = 1024 + (size_t)kFusedTiles * 2 * TILE * 128 + 2 * (size_t)Hi * 128 + kMaxN * 4 +
                       (size_t)(kFusedTiles * TILE + kTopkMaxK + kFusedThreads) * 8 + 2 * 8 + 16;
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_index_topk_fused_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(1024 + kFusedTiles * 2 * TILE * 128 + 2 * kMaxN * 128 + kMaxN * 4 +
-                                               (kFusedTiles * TILE + kTopkMaxK + kFusedThreads) * 8 + 2 * 8 + 16));
+  static SmemAttr attr;
+  {
+    cudaError_t e = attr.ensure((const void *)k_index_topk_fused_tc,
+                                (int)(1024 + kFusedTiles * 2 * TILE * 128 + 2 * kMaxN * 128 + kMaxN * 4 +
+                                      (kFusedTiles * TILE + kTopkMaxK + kFusedThreads) * 8 + 2 * 8 + 16));
     if (e != cudaSuccess) return e;
-    attr = true;
   }
   k_index_topk_fused_tc<<<B, kFusedThreads, smem, s>>>(p);
   return cudaGetLastError();
