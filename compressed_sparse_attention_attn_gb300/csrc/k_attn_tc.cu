@@ -550,8 +550,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
 
 // Merge of the split shares: block (query, 8 heads), one warp per head, two 16-byte vectors per
 // thread.  The weights e^{m_c - M} l_c / den put each share O_c / l_c back on the common scale, with
-// the sink in den; every thread forms its head's weights itself (no barrier), and shares of CTAs
-// that found nothing (l_c = 0) weigh 0 and are not read.
+// the sink in den; every thread forms its head's weights itself (no barrier), after loading the
+// weights' inputs and its vectors of every share at once, and shares of CTAs that found nothing
+// (l_c = 0) weigh 0 and are skipped.
 constexpr int kCombHeads = 8;
 constexpr int kCombThreads = 256;
 struct CombineParams {
@@ -575,43 +576,44 @@ __global__ void __launch_bounds__(kCombThreads) k_attn_combine(const __grid_cons
   const int h = h0 + (tid * kPer) / (HD / 8);
   // this head's weights e^{m_c - M} l_c / den, computed by each of its threads (same addresses)
   const float s2 = C.sink[h] * 1.4426950408889634f;
-  float mc[kMaxTiles], lc[kMaxTiles];
-  float M = s2;
-#pragma unroll
-  for (int c = 0; c < kMaxTiles; ++c) {
-    mc[c] = -INFINITY;
-    lc[c] = 0.f;
-    if (c < C.nsplit) {
-      const float2 ml = *reinterpret_cast<const float2 *>(C.part_ml + ((row * C.nsplit + c) * C.H + h) * 2);
-      mc[c] = ml.x;
-      lc[c] = ml.y;
-      if (lc[c] > 0.f) M = fmaxf(M, mc[c]);
-    }
-  }
-  float den = exp2f(s2 - M), w[kMaxTiles];
-#pragma unroll
-  for (int c = 0; c < kMaxTiles; ++c) {
-    w[c] = lc[c] > 0.f ? lc[c] * exp2f(mc[c] - M) : 0.f;
-    den += w[c];
-  }
-  const float inv = 1.0f / den;
+  // every share's (m, l) and vectors in flight together; shares of CTAs that found nothing (l = 0,
+  // their buffers never written) are read but never used
+  float2 ml[kMaxTiles];
   uint4 u[kPer][kMaxTiles];
 #pragma unroll
-  for (int k = 0; k < kPer; ++k) {  // every share of every vector in flight together
+  for (int c = 0; c < kMaxTiles; ++c) {
+    ml[c] = make_float2(-INFINITY, 0.f);
+    if (c < C.nsplit) ml[c] = __ldcg(reinterpret_cast<const float2 *>(C.part_ml + ((row * C.nsplit + c) * C.H + h) * 2));
+  }
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
     const int d0 = ((tid * kPer + k) % (HD / 8)) * 8;
 #pragma unroll
     for (int c = 0; c < kMaxTiles; ++c) {
       u[k][c] = make_uint4(0u, 0u, 0u, 0u);
-      if (w[c] != 0.f)
-        u[k][c] = *reinterpret_cast<const uint4 *>(C.part_o + ((row * C.nsplit + c) * C.H + h) * (int64_t)HD + d0);
+      if (c < C.nsplit)
+        u[k][c] = __ldcg(reinterpret_cast<const uint4 *>(C.part_o + ((row * C.nsplit + c) * C.H + h) * (int64_t)HD + d0));
     }
   }
+  // this head's weights e^{m_c - M} l_c / den
+  float M = s2;
+#pragma unroll
+  for (int c = 0; c < kMaxTiles; ++c)
+    if (ml[c].y > 0.f) M = fmaxf(M, ml[c].x);
+  float den = exp2f(s2 - M), w[kMaxTiles];
+#pragma unroll
+  for (int c = 0; c < kMaxTiles; ++c) {
+    w[c] = ml[c].y > 0.f ? ml[c].y * exp2f(ml[c].x - M) : 0.f;
+    den += w[c];
+  }
+  const float inv = 1.0f / den;
 #pragma unroll
   for (int k = 0; k < kPer; ++k) {
     const int d0 = ((tid * kPer + k) % (HD / 8)) * 8;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int c = 0; c < kMaxTiles; ++c) {
+      if (w[c] == 0.f) continue;
       const float wv = w[c] * inv;
       const __nv_bfloat162 *pv = reinterpret_cast<const __nv_bfloat162 *>(&u[k][c]);
 #pragma unroll
