@@ -175,6 +175,45 @@ def test_small_ratio2_index_source_and_reuse(csa, orc, start, T, B, cand):
     assert ctx.status() == 0
 
 
+@pytest.mark.parametrize("cand", [False, True])
+def test_fused_indexer_topk_selection(csa, orc, cand):
+    """Decode rows of at most 512 positions take scores and top-k in one kernel (tensor-core indexer
+    shapes: 16 heads x 128); with K = 64 below the valid count the selection is a real cut.  The fast
+    path (no debug buffers) must publish exactly the selection of the two-kernel path (debug scores
+    requested), which must be the oracle's top-k of those very scores, bit for bit."""
+    g = Geometry(dim=128, n_heads=4, head_dim=64, rope_dim=16, q_rank=64, o_rank=32, groups=2, window=8,
+                 index_heads=16, index_hd=128, index_topk=64, cand_block=64, max_seq=1024, max_tokens=1, max_batch=4)
+    gd = g.as_dict()
+    B, T, start, L = 4, 1, 700, 384
+    clen = 300  # limit min(701 // 2, 300) = 300 positions: three key tiles
+    w = weights(g, with_indexer=True, norm_ones=False)
+    x = activations(g, B, T, seed_base=2100 + int(cand))
+    Z, KI = latent_cache(g, B, L, seed_base=3100)
+    pos = positions(B, T, start)
+    cm = candidate_mask(B * T, pos, 2, clen, g.cand_block, L // g.cand_block, 4, 98) if cand else None
+    ring0 = orc.act_quant(ring_rows(g, B))[0]
+    role = dict(ratio=2, is_index_source=1, uses_candidates=int(cand))
+    ctx = csa.Context(gd)
+    wd = _dev_weights(w)
+    K = g.index_topk
+    sel_d = torch.full((B * T, K), -7, dtype=torch.int32, device="cuda")
+    sh = csa.Shared(to_dev(Z), to_dev(KI), clen, sel_d, K, None if cm is None else to_dev(cm))
+    out_fast = ctx.forward(wd, role, to_dev(ring0), to_dev(x), start, shared=sh)
+    sel_fast = sel_d.clone()
+    dbg = _dbg(B * T, g, L, g.window + K)
+    out = ctx.forward(wd, role, to_dev(ring0), to_dev(x), start, shared=sh, debug=dbg)
+    torch.cuda.synchronize()
+    assert ctx.status() == 0
+    assert torch.equal(sel_fast, sel_d)
+    assert torch.equal(out_fast, out)
+    S = to_np(dbg["scores"])[:, :L].astype(np.float32)
+    S = np.where(np.isnan(S), -np.inf, S).astype(np.float32)
+    want = orc.index_topk(S, K, pos, 2, clen, cm, g.cand_block, offset=g.window)
+    assert np.array_equal(to_np(sel_fast), want)
+    n_valid = np.isfinite(S).sum(1)
+    assert (n_valid > K).all()  # the cut is real on every row
+
+
 def test_layer_refusals(csa):
     g = _small_geom()
     ctx = csa.Context(g.as_dict())
