@@ -16,9 +16,9 @@
 //   and the maxima and sums over the rows are butterfly reductions that leave each lane one head
 //   O^T[d][h] += sum_r G[r][d] P[h][r]      (M = 4 x 128 features, N = 64, K = 128 rows; the same tile
 //                                            read as an MN-major operand)
-// When a query's tiles are split over several CTAs (decode: few queries, so one tile per CTA keeps
-// the SMs busy), each CTA writes (m, l, O / l) for its tiles and a second, wide kernel merges the
-// shares in CTA order with the sink, which enters the denominator only:
+// When a query's tiles are split over several CTAs (decode: few queries; the split minimises tiles
+// per CTA x waves of CTAs), each CTA writes (m, l, O / l) for its tiles and a second, wide kernel
+// merges the shares in CTA order with the sink, which enters the denominator only:
 //   O = sum_c e^{m_c - M} O_c / (e^{sink - M} + sum_c e^{m_c - M} l_c).
 // A query held by one CTA (prefill: many queries) is finished in place.  The result is staged in
 // shared memory and written with 16-byte stores as bf16, together with the inverse rotation of its

@@ -10,7 +10,9 @@
 //
 // Work split: the (tile, 64-wide k-slice) units of up to four independent problems (several weights
 // applied to the same activations, or the groups of the block-diagonal wo_a) are laid end to end
-// and divided evenly over a persistent grid of one CTA per SM ("Stream-K").  A tile whose k-range
+// and divided evenly over a persistent grid of at most one CTA per SM ("Stream-K"; a weight-streaming
+// launch takes a slightly smaller grid when one of at least 80% of the SMs gives every CTA whole
+// tiles, or equal fractions of one, which removes or evens out the fixups).  A tile whose k-range
 // spans several CTAs is finished by whichever of them arrives last: each writes its f32 partial to
 // the workspace, bumps the tile's arrival counter, and the last one sums the partials in CTA order
 // (deterministic) and writes the bf16 result.  No CTA ever waits for another.

@@ -97,10 +97,12 @@ cudaError_t launch_index_scores(const bf16 *qI, const float *wI, const bf16 *KI,
 }
 
 // ---------------------------------------------------------------------------------------------
-// Top-k: one CTA per query.  Scores map to order-preserving 32-bit keys (-0 folded onto +0, NaN
-// below every number) and each valid position j to the 64-bit value (key << 32) | ~j, so that the
-// values are distinct and larger means selected first (higher score, then lower position).  A first
-// pass compacts the valid values into shared memory; when they are at most K, all are taken.
+// Top-k: one CTA per query (512 threads, four CTAs an SM, for rows of at most 2048 positions; 1024
+// otherwise).  Scores map to order-preserving 32-bit keys (-0 folded onto +0, NaN below every number)
+// and each valid position j to the 64-bit value (key << 32) | ~j, so that the values are distinct and
+// larger means selected first (higher score, then lower position).  A first pass compacts the valid
+// values into shared memory (with a candidate mask: the kept blocks listed first, only their
+// positions visited); when they are at most K, all are taken.  The rest (topk_core.cuh):
 // Otherwise a radix select on the 64-bit values (8 bits per pass, warp-aggregated histograms, over
 // shared memory) finds the K-th largest, and the values at or above it are taken.  (A query with more
 // valid positions than shared memory holds runs the same passes over its scores in global memory.)
