@@ -293,7 +293,9 @@ def test_index_topk_bit_exact(csa, orc, B, T, start, L, clen, ratio, keep, cb, K
                                                         (64, 512, 128, 512, 128, 700, 80, 1),
                                                         (64, 512, 7, 300, 7, 64, 2, 5),
                                                         (128, 512, 128, 256, 128, 300, 2, 1),
-                                                        (64, 512, 64, 256, 64, 400, 2, 100)])
+                                                        (64, 512, 64, 256, 64, 400, 2, 100),
+                                                        # the widest list the tensor-core kernel takes: 6 tiles
+                                                        (64, 512, 128, 640, 128, 900, 4, 1)])
 def test_sparse_attn(csa, orc, H, hd, na, nb, a_len, b_len, B, T):
     rng = np.random.default_rng(8 + H)
     q = _rng_bf16(orc, rng, (B * T, H, hd))

@@ -214,6 +214,49 @@ def test_fused_indexer_topk_selection(csa, orc, cand):
     assert (n_valid > K).all()  # the cut is real on every row
 
 
+@pytest.mark.parametrize("case", ["no latent rows yet", "masks keeping nothing"])
+def test_ratio2_decode_degenerate_selection(csa, orc, case):
+    """Degenerate selections of a ratio-2 index-source decode: before any latent row is published
+    (compress_len 0) every selected entry is -1 and the attention runs over the window alone; with a
+    candidate mask keeping no block for some queries, those queries select nothing either."""
+    g = _small_geom()
+    gd = g.as_dict()
+    B, T, start, L = 3, 1, 40, 64
+    w = weights(g, with_indexer=True, norm_ones=False)
+    x = activations(g, B, T, seed_base=2200)
+    Z, KI = latent_cache(g, B, L, seed_base=3200)
+    clen = 0 if case == "no latent rows yet" else 20
+    pos = positions(B, T, start)
+    cm = None
+    if case != "no latent rows yet":
+        cm = candidate_mask(B * T, pos, 2, clen, g.cand_block, L // g.cand_block, 0.5, 97)
+        cm[0, :] = 0
+        cm[2, :] = 0
+    tab = orc.rope_table(g.rope_dim, g.max_seq, g.compress_rope_theta, g.orig_seq, g.rope_factor)
+    ring0 = orc.act_quant(ring_rows(g, B))[0]
+    ring_o = ring0.copy()
+    sel_o = np.full((B * T, g.index_topk), -7, np.int32)
+    shared_o = dict(compress_kv=Z, index_k=KI, compress_len=clen, topk_idxs=sel_o)
+    if cm is not None:
+        shared_o["candidates"] = cm
+    role = dict(ratio=2, is_index_source=1, uses_candidates=int(cm is not None))
+    res = orc.attn_forward(gd, role, w, ring_o, x, start, tab, shared_o)
+    ctx = csa.Context(gd)
+    sel_d = torch.full((B * T, g.index_topk), -7, dtype=torch.int32, device="cuda")
+    sh = csa.Shared(to_dev(Z), to_dev(KI), clen, sel_d, g.index_topk, None if cm is None else to_dev(cm))
+    dbg = _dbg(B * T, g, L, g.window + g.index_topk)
+    out = ctx.forward(_dev_weights(w), role, to_dev(ring0), to_dev(x), start, shared=sh, debug=dbg)
+    torch.cuda.synchronize()
+    assert ctx.status() == 0
+    sel = to_np(sel_d)
+    if case == "no latent rows yet":
+        assert (sel == -1).all()
+    else:
+        assert (sel[0] == -1).all() and (sel[2] == -1).all() and (sel[1] >= 0).any()
+    dbg["__out"] = out
+    _compare_rows(res, dbg, np.arange(B * T), g, case)
+
+
 def test_layer_refusals(csa):
     g = _small_geom()
     ctx = csa.Context(g.as_dict())
