@@ -7,10 +7,11 @@ gcc and exposes it to numpy through ctypes.  Only ``tests/``, ``__graft_entry__.
 benchmark's ``cpu_baseline`` leg may import it; the GPU library never does, and the two share no
 code.  bf16 tensors travel as ``uint16`` arrays of their bit patterns.
 
-Partly pinned: the YaRN form of :func:`rope_table` (the pages give its constants only).  Its classes
-are pinned (pairs with at least beta_fast turns over the original length keep their frequency, those
-with at most beta_slow turns run at frequency / factor, the others lie strictly between); the blend
-weights inside the ramp have no printed value to check.
+The YaRN form of :func:`rope_table` follows the published method (the pages give its constants
+only).  Pinned are its classes (pairs with at least beta_fast turns over the original length keep
+their frequency, those with at most beta_slow turns run at frequency / factor, the others lie strictly
+between) and every pair's blend weight inside the ramp, against ramp ends found by searching the
+rotation counts rather than from the closed-form index.
 """
 import ctypes
 import os

@@ -25,8 +25,9 @@
  * Parity pins: every function here is checked by tests/test_oracle_*.py against facts the pages or
  * mathematics fix (the 12-into-8 ring fixture, the e4m3 format table, closed forms of the softmax
  * with sink, brute force on tiny inputs, the published parameter counts).  The YaRN variant of the
- * RoPE table is pinned only in part (the pages give its constants, not its formula): its frequency
- * classes by rotation count and its two ends are checked, the blend weights inside the ramp are not.
+ * RoPE table follows the published method, as the pages give its constants but not its formula: its
+ * frequency classes by rotation count and the blend weight of every pair inside the ramp are checked
+ * against ramp ends found by searching the rotation counts.
  */
 #include <math.h>
 #include <stdint.h>
@@ -156,8 +157,8 @@ void orc_rmsnorm(const uint16_t *x, int64_t M, int64_t N, const float *w, float 
  * d(n) = rd * ln(L / (2 pi n)) / (2 ln theta); pairs below floor(d(beta_fast)) keep f_i, pairs above
  * ceil(d(beta_slow)) use f_i / factor, and a linear ramp over the pair index blends the two in
  * between.  Applied only when max_seq exceeds the original length, as the excerpt passes
- * original_seq_len through to the table.  Pinned in part: the frequency classes and ends (tests),
- * not the ramp's blend weights, for which nothing is printed. */
+ * original_seq_len through to the table.  Pinned by the tests: the frequency classes, and each pair's
+ * blend weight against ramp ends found by searching the rotation counts. */
 int orc_rope_table(int rd, int64_t max_seq, double theta, int64_t orig_seq, double factor, double beta_fast,
                    double beta_slow, float *tab) {
   if (rd <= 0 || (rd & 1) || max_seq <= 0 || !tab) return ORC_ERR_ARG;

@@ -6,6 +6,7 @@ import math
 import os
 
 import numpy as np
+import pytest
 
 GOLD = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -53,6 +54,38 @@ def test_rope_yarn_pairs_by_rotation_count(orc):
     assert np.allclose(ang[slow], f[slow] / factor, rtol=2e-7, atol=0)
     mid = ~fast & ~slow
     assert np.all(ang[mid] < f[mid] * (1 - 1e-6)) and np.all(ang[mid] > f[mid] / factor * (1 + 1e-6))
+
+
+@pytest.mark.parametrize(
+    "rd,theta,L,factor,beta_fast,beta_slow",
+    [
+        (64, 160000.0, 65536, 16.0, 32.0, 1.0),  # the compressed layers' rope constants
+        (64, 10000.0, 4096, 40.0, 32.0, 1.0),  # the YaRN paper's long-context extension of a 4k model
+        (32, 10.0, 1024, 8.0, 32.0, 1.0),  # the ceiling index past rd - 1: the ramp is cut there
+    ],
+)
+def test_rope_yarn_ramp_weights(orc, rd, theta, L, factor, beta_fast, beta_slow):
+    """YaRN's blend inside the ramp (Peng et al., 2023, frequency interpolation by parts): pair i runs
+    at f_i (1 - w_i) + (f_i / factor) w_i with w_i = clamp((i - lo) / (hi - lo), 0, 1), lo the last
+    pair index (counted on past rd / 2 where needed) that still completes beta_fast turns over the
+    original length, hi the first that completes at most beta_slow, capped at rd - 1.  Both ends are
+    found here by searching the rotation counts, not from the closed-form index, and the weights are
+    read back from the table's angle at position 1."""
+    y = orc.rope_table(rd, L + 2, theta, orig_seq=L, factor=factor, beta_fast=beta_fast, beta_slow=beta_slow)
+    idx = np.arange(4 * rd, dtype=np.float64)
+    turns = L * theta ** (-2.0 * idx / rd) / (2 * math.pi)  # strictly decreasing in the index
+    lo = max(int(np.nonzero(turns >= beta_fast)[0].max()) if (turns >= beta_fast).any() else 0, 0)
+    hi = min(int(np.nonzero(turns <= beta_slow)[0].min()), rd - 1)
+    assert hi > lo
+    half = rd // 2
+    i = np.arange(half, dtype=np.float64)
+    f = theta ** (-2.0 * i / rd)
+    ang = np.arctan2(y[1, :, 1].astype(np.float64), y[1, :, 0].astype(np.float64))
+    w = (1.0 - ang / f) / (1.0 - 1.0 / factor)  # 0: the pair keeps f_i, 1: it runs at f_i / factor
+    expect = np.clip((i - lo) / (hi - lo), 0.0, 1.0)
+    assert np.all(np.abs(w - expect) < 2e-6), np.abs(w - expect).max()
+    # the ramp is really exercised: some pairs strictly inside it
+    assert ((expect > 0) & (expect < 1)).sum() >= 3
 
 
 def test_rotary_adjacent_pairs_and_inverse(orc):
