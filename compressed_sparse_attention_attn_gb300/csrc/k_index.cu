@@ -103,7 +103,7 @@ cudaError_t launch_index_scores(const bf16 *qI, const float *wI, const bf16 *KI,
 // larger means selected first (higher score, then lower position).  A first pass compacts the valid
 // values into shared memory (with a candidate mask: the kept blocks listed first, only their
 // positions visited); when they are at most K, all are taken.  The rest (topk_core.cuh):
-// Otherwise a radix select on the 64-bit values (8 bits per pass, warp-aggregated histograms, over
+// Otherwise a radix select on the 64-bit values (8 bits per pass, one shared atomic per value, over
 // shared memory) finds the K-th largest, and the values at or above it are taken.  (A query with more
 // valid positions than shared memory holds runs the same passes over its scores in global memory.)
 // The chosen values are then sorted descending by a bitonic network whose stages within a warp run

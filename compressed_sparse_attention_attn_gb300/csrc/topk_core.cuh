@@ -6,10 +6,14 @@
 // valid position j to the 64-bit value (key << 32) | ~j, so that the values are distinct and larger
 // means selected first.  Given the count of valid values (compacted into shared memory when they
 // fit), topk_finish takes all of them when they are at most K; otherwise a radix select on the 64-bit
-// values (8 bits per pass from the top, warp-aggregated histograms) finds the K-th largest and the
-// values at or above it are taken.  The chosen values are then sorted descending by a bitonic network
-// whose stages within a warp run on shuffles and whose wider stages go through shared memory, and
-// written as j + offset, -1 past the valid ones.
+// values (8 bits per pass from the top) finds the K-th largest and the values at or above it are
+// taken.  The histograms count with one shared atomic per value: measured at 4096 values a query,
+// that is 2-5x faster a pass than aggregating equal digits across a warp first (__match_any_sync),
+// even in the top digit where most values share one or two bins.  The chosen values are then sorted
+// descending by a bitonic network whose stages within a warp run on shuffles and whose wider stages
+// go through shared memory, and written as j + offset, -1 past the valid ones.  (Four values a
+// thread, so that strides 1 and 2 stay in registers, measured 1.6x slower at 512 values: only four
+// warps then hold values, and each stage's shuffle latency is exposed.)
 #pragma once
 
 #include <cstdint>
@@ -77,7 +81,7 @@ __device__ __forceinline__ void topk_finish(TopkShared &sh, unsigned nvalid, boo
       const unsigned long long hi_mask = shift == 56 ? 0ull : (~0ull << (shift + 8));
       for (int i0 = 0; i0 < n_iter; i0 += blockDim.x) {
         const int i = i0 + tid;
-        int bin = 256 + lane;  // no bin: a value of every lane of its own
+        int bin = 256;  // no bin
         if (i < n_iter) {
           bool ok = true;
           unsigned long long v = 0ull;
@@ -88,8 +92,7 @@ __device__ __forceinline__ void topk_finish(TopkShared &sh, unsigned nvalid, boo
           }
           if (ok && (v & hi_mask) == (prefix & hi_mask)) bin = (int)((v >> shift) & 255u);
         }
-        const unsigned peers = __match_any_sync(0xffffffffu, bin);
-        if (bin < 256 && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], (unsigned)__popc(peers));
+        if (bin < 256) atomicAdd(&hist[bin], 1u);
       }
       __syncthreads();
       if (wid == 0) {

@@ -271,6 +271,8 @@ def test_index_scores_gathered(csa, orc, Hi, B, start, L, clen, ratio, keep, cb)
     (3, 1, 700, 512, 400, 2, 0.5, 64, 512),        # masked, fewer valid than K
     (1, 2, 100, 128, 128, 1, 0, 64, 600),          # K beyond the positions: -1 tail
     (2, 5, 250, 256, 256, 1, 0.25, 128, 64),       # blocks of 128, K below the valid count
+    (1, 2, 8191, 4096, 4096, 2, 0, 64, 1000),      # a cut sorted over 1024 slots (three shared stages)
+    (1, 1, 1300, 1024, 1024, 2, 0, 64, 700),       # 650 valid, all taken, sorted over 1024 slots
 ])
 def test_index_topk_bit_exact(csa, orc, B, T, start, L, clen, ratio, keep, cb, K):
     rng = np.random.default_rng(7 + T)
