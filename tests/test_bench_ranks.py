@@ -1,6 +1,6 @@
 """The benchmark's N > 1 logic on CPU: two gloo ranks, each with its own timed length, agree on the
 slowest one, and the whole-job throughput counts every rank's full batch (weak scaling).  The
-reference arm's other ranks do no work."""
+reference arm's other ranks do no work, and its rank 0 prints one line of the benchmark contract."""
 import os
 import socket
 import sys
@@ -56,3 +56,28 @@ def test_reference_arm_other_ranks_do_nothing(capsys):
     ns = type("A", (), dict(workload="reindex_decode_r2", steps=1, warmup=0))()
     assert bench.run_reference(ns, 1, 2) is None
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_prints_one_contract_line():
+    """The reference arm (the oracle on the host cores) at N = 1: one JSON line carrying the keys the
+    benchmark contract names, the throughput consistent with the step time, no transfers counted."""
+    import json
+    import subprocess
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "3"], cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert k in d, k
+    assert d["impl"] == "reference" and d["n_gpus"] == 1 and d["steps"] == 1 and d["warmup"] == 3
+    assert d["unit"] == "tokens/s" and d["higher_is_better"] is True and d["vs_baseline"] is None
+    assert d["config"]["workload"] == "reindex_decode_r2"
+    assert d["value"] > 0 and d["ms_per_step"] > 0
+    # tokens per step over the step time (the sample is one token of one layer)
+    assert d["value"] == pytest.approx(1000.0 / d["ms_per_step"], rel=1e-6)
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
