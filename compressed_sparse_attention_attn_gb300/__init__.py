@@ -32,8 +32,26 @@ def _check(rc, where):
         raise CsaError(rc, where)
 
 
-def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+def _checked(t, dtype, cuda, what):
+    if t.is_cuda != cuda:
+        raise ValueError("%s: expected a %s tensor, got one on %s" % (what, "CUDA" if cuda else "host", t.device))
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError("%s: expected %s, got %s" % (what, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s: expected a contiguous tensor (shape %s, strides %s)" % (what, tuple(t.shape), t.stride()))
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _dev(t, dtype=None, what="tensor"):
+    """Device pointer of a contiguous CUDA tensor of the given dtype; None -> NULL.  The kernels read
+    and write through raw pointers, so a host tensor, a strided view or a narrower dtype is refused
+    here rather than read out of bounds on the GPU."""
+    return None if t is None else _checked(t, dtype, True, what)
+
+
+def _host(t, dtype=None, what="tensor"):
+    """Host pointer of a contiguous CPU tensor of the given dtype (pinned for copies that overlap)."""
+    return None if t is None else _checked(t, dtype, False, what)
 
 
 def _stream(stream=None):
@@ -74,8 +92,9 @@ class Shared:
 
     def struct(self):
         stride = self.compress_kv.shape[1] if self.compress_kv is not None else 0
-        self._c = _abi.Shared(_ptr(self.compress_kv), _ptr(self.index_k), self.compress_len, stride,
-                              _ptr(self.topk_idxs), self.topk, int(self.has_topk), _ptr(self.candidates),
+        self._c = _abi.Shared(_dev(self.compress_kv, torch.bfloat16, "compress_kv"), _dev(self.index_k, torch.bfloat16, "index_k"),
+                              self.compress_len, stride, _dev(self.topk_idxs, torch.int32, "topk_idxs"), self.topk,
+                              int(self.has_topk), _dev(self.candidates, torch.uint8, "candidates"),
                               0 if self.candidates is None else self.candidates.shape[-1])
         return self._c
 
@@ -85,6 +104,9 @@ class Shared:
 
 
 DEBUG_FIELDS = ("q", "kv", "kv_codes", "kv_scale", "idx", "scores", "o", "og", "qr", "qI", "wI")
+DEBUG_DTYPES = (torch.bfloat16, torch.bfloat16, torch.uint8, torch.int8, torch.int32, torch.float32, torch.bfloat16, torch.bfloat16, torch.bfloat16, torch.bfloat16, torch.float32)
+WEIGHT_FIELDS = ("sink", "q_norm", "kv_norm", "wq_a", "wq_b", "wkv", "wo_a", "wo_b", "idx_wq_b", "idx_wproj")
+WEIGHT_DTYPES = (torch.float32, torch.float32, torch.float32, torch.bfloat16, torch.bfloat16, torch.bfloat16, torch.bfloat16, torch.bfloat16, torch.bfloat16, torch.bfloat16)
 
 
 class Context:
@@ -111,11 +133,10 @@ class Context:
     # -- layer ---------------------------------------------------------------------------------
     @staticmethod
     def layer_weights(w, role):
-        return _abi.LayerWeights(make_role(role), *[_ptr(w.get(n)) for n in (
-            "sink", "q_norm", "kv_norm", "wq_a", "wq_b", "wkv", "wo_a", "wo_b", "idx_wq_b", "idx_wproj")])
+        return _abi.LayerWeights(make_role(role), *[_dev(w.get(n), dt, n) for n, dt in zip(WEIGHT_FIELDS, WEIGHT_DTYPES)])
 
     def state_init(self, ring, batch, stream=None):
-        st = _abi.LayerState(_ptr(ring))
+        st = _abi.LayerState(_dev(ring, torch.bfloat16, "ring"))
         _check(lib().csa_state_init(self.h, ctypes.byref(st), batch, _stream(stream)), "csa_state_init")
 
     def forward(self, w, role, ring, x, start_pos, shared=None, out=None, debug=None, stream=None, lw=None):
@@ -127,13 +148,13 @@ class Context:
             out = torch.empty_like(x)
         if lw is None:
             lw = self.layer_weights(w, role)
-        st = _abi.LayerState(_ptr(ring))
+        st = _abi.LayerState(_dev(ring, torch.bfloat16, "ring"))
         sh = shared.struct() if shared is not None else None
         dbg = None
         if debug:
-            dbg = _abi.Debug(*[_ptr(debug.get(n)) for n in DEBUG_FIELDS])
-        rc = lib().attn_v41_forward(self.h, ctypes.byref(lw), ctypes.byref(st), _ptr(x), B, T, start_pos,
-                                    ctypes.byref(sh) if sh is not None else None, _ptr(out),
+            dbg = _abi.Debug(*[_dev(debug.get(n), dt, n) for n, dt in zip(DEBUG_FIELDS, DEBUG_DTYPES)])
+        rc = lib().attn_v41_forward(self.h, ctypes.byref(lw), ctypes.byref(st), _dev(x, torch.bfloat16, "x"), B, T, start_pos,
+                                    ctypes.byref(sh) if sh is not None else None, _dev(out, torch.bfloat16, "out"),
                                     ctypes.byref(dbg) if dbg is not None else None, _stream(stream))
         _check(rc, "attn_v41_forward")
         if shared is not None:
@@ -142,10 +163,11 @@ class Context:
 
     def forward_host(self, lw, ring, x_host, start_pos, shared, out_host, B, T, stream=None):
         """attn_v41_forward_host with host tensors (pinned for overlap)."""
-        st = _abi.LayerState(_ptr(ring))
+        st = _abi.LayerState(_dev(ring, torch.bfloat16, "ring"))
         sh = shared.struct() if shared is not None else None
-        rc = lib().attn_v41_forward_host(self.h, ctypes.byref(lw), ctypes.byref(st), _ptr(x_host), B, T, start_pos,
-                                         ctypes.byref(sh) if sh is not None else None, _ptr(out_host), _stream(stream))
+        rc = lib().attn_v41_forward_host(self.h, ctypes.byref(lw), ctypes.byref(st), _host(x_host, torch.bfloat16, "x_host"), B, T,
+                                         start_pos, ctypes.byref(sh) if sh is not None else None,
+                                         _host(out_host, torch.bfloat16, "out_host"), _stream(stream))
         _check(rc, "attn_v41_forward_host")
         if shared is not None:
             shared.sync_back()
@@ -153,7 +175,7 @@ class Context:
     def rope_table(self, ratio_class):
         g = self.cfg
         t = torch.empty(g.max_seq, g.rope_dim // 2, 2, dtype=torch.float32)
-        _check(lib().csa_rope_table_get(self.h, ratio_class, _ptr(t)), "csa_rope_table_get")
+        _check(lib().csa_rope_table_get(self.h, ratio_class, _host(t, torch.float32, "table")), "csa_rope_table_get")
         return t
 
     def status(self, clear=True):
@@ -185,8 +207,8 @@ class Context:
         M = x.numel() // x.shape[-1]
         if out is None:
             out = torch.empty(x.shape[:-1] + (N * groups,), dtype=torch.bfloat16, device=x.device)
-        _check(lib().csa_linear(self.h, _ptr(x), M, K, x.shape[-1], _ptr(W), N, K, _ptr(out), out.shape[-1], groups,
-                                _stream(stream)), "csa_linear")
+        _check(lib().csa_linear(self.h, _dev(x, torch.bfloat16, "x"), M, K, x.shape[-1], _dev(W, torch.bfloat16, "W"), N, K, _dev(out, torch.bfloat16, "out"),
+                                out.shape[-1], groups, _stream(stream)), "csa_linear")
         return out
 
     def sparse_attn(self, q, rows_a, a_len, idx_a, sink, scale, rows_b=None, b_len=0, idx_b=None, o=None, o_rot=None,
@@ -194,52 +216,58 @@ class Context:
         """q [B*T, H, hd]; rows_a [B, ., hd]; rows_b [B, ., hd]; idx_a [B*T, na]; idx_b [B*T, nb]."""
         n, H, hd = q.shape
         T = n // B if T is None else T
-        _check(lib().csa_sparse_attn(self.h, _ptr(q), B, T, H, hd, _ptr(rows_a), rows_a.shape[1] * hd, a_len,
-                                     _ptr(rows_b), 0 if rows_b is None else rows_b.shape[1] * hd, b_len, _ptr(idx_a),
-                                     idx_a.shape[1], _ptr(idx_b), 0 if idx_b is None else idx_b.shape[1], _ptr(sink),
-                                     scale, _ptr(o), _ptr(o_rot), rd, start_pos, _ptr(tab),
-                                     0 if tab is None else tab.shape[0], _stream(stream)), "csa_sparse_attn")
+        _check(lib().csa_sparse_attn(self.h, _dev(q, torch.bfloat16, "q"), B, T, H, hd, _dev(rows_a, torch.bfloat16, "rows_a"),
+                                     rows_a.shape[1] * hd, a_len, _dev(rows_b, torch.bfloat16, "rows_b"),
+                                     0 if rows_b is None else rows_b.shape[1] * hd, b_len, _dev(idx_a, torch.int32, "idx_a"),
+                                     idx_a.shape[1], _dev(idx_b, torch.int32, "idx_b"), 0 if idx_b is None else idx_b.shape[1],
+                                     _dev(sink, torch.float32, "sink"), scale, _dev(o, torch.bfloat16, "o"), _dev(o_rot, torch.bfloat16, "o_rot"), rd,
+                                     start_pos, _dev(tab, torch.float32, "tab"), 0 if tab is None else tab.shape[0],
+                                     _stream(stream)), "csa_sparse_attn")
 
 
 def rmsnorm(x, w, eps, out=None, stream=None):
     N = x.shape[-1]
     out = torch.empty_like(x) if out is None else out
-    _check(lib().csa_rmsnorm(_ptr(x), x.numel() // N, N, _ptr(w), eps, _ptr(out), _stream(stream)), "csa_rmsnorm")
+    _check(lib().csa_rmsnorm(_dev(x, torch.bfloat16, "x"), x.numel() // N, N, _dev(w, torch.float32, "w"), eps, _dev(out, torch.bfloat16, "out"),
+                             _stream(stream)), "csa_rmsnorm")
     return out
 
 
 def rope(x, rd, pos, tab, inverse=False, rows_per_pos=1, stream=None):
     """In place on x [rows, row_len]."""
     row_len = x.shape[-1]
-    _check(lib().csa_rope(_ptr(x), x.numel() // row_len, row_len, rd, _ptr(pos), rows_per_pos, _ptr(tab), tab.shape[0],
-                          int(inverse), _stream(stream)), "csa_rope")
+    _check(lib().csa_rope(_dev(x, torch.bfloat16, "x"), x.numel() // row_len, row_len, rd, _dev(pos, torch.int32, "pos"), rows_per_pos,
+                          _dev(tab, torch.float32, "tab"), tab.shape[0], int(inverse), _stream(stream)), "csa_rope")
     return x
 
 
 def act_quant(x, codes=None, scale_exp=None, stream=None):
     """In place on x; codes uint8 like x, scale_exp int8 [n/32]."""
-    _check(lib().csa_act_quant(_ptr(x), x.numel(), _ptr(codes), _ptr(scale_exp), _stream(stream)), "csa_act_quant")
+    _check(lib().csa_act_quant(_dev(x, torch.bfloat16, "x"), x.numel(), _dev(codes, torch.uint8, "codes"), _dev(scale_exp, torch.int8, "scale_exp"),
+                               _stream(stream)), "csa_act_quant")
     return x
 
 
 def kv_finish(kv_in, kv_out, B, T, start_pos, rd, tab, ring, win_idx=None, codes=None, scales=None, stream=None):
     hd = kv_in.shape[-1]
     W = ring.shape[1]
-    _check(lib().csa_kv_finish(_ptr(kv_in), _ptr(kv_out), B, T, start_pos, hd, rd, _ptr(tab), tab.shape[0], _ptr(ring), W,
-                               _ptr(win_idx), 0 if win_idx is None else win_idx.shape[-1], _ptr(codes), _ptr(scales),
-                               _stream(stream)), "csa_kv_finish")
+    _check(lib().csa_kv_finish(_dev(kv_in, torch.bfloat16, "kv_in"), _dev(kv_out, torch.bfloat16, "kv_out"), B, T, start_pos, hd, rd,
+                               _dev(tab, torch.float32, "tab"), tab.shape[0], _dev(ring, torch.bfloat16, "ring"), W, _dev(win_idx, torch.int32, "win_idx"),
+                               0 if win_idx is None else win_idx.shape[-1], _dev(codes, torch.uint8, "codes"),
+                               _dev(scales, torch.int8, "scales"), _stream(stream)), "csa_kv_finish")
 
 
 def index_scores(qI, wI, KI, B, T, start_pos, compress_len, ratio, S, cand=None, cand_block=1, stream=None):
     n, Hi, dI = qI.shape
-    _check(lib().csa_index_scores(_ptr(qI), _ptr(wI), _ptr(KI), B, T, start_pos, Hi, dI, KI.shape[1], compress_len,
-                                  ratio, _ptr(cand), 0 if cand is None else cand.shape[-1], cand_block, _ptr(S),
-                                  _stream(stream)), "csa_index_scores")
+    _check(lib().csa_index_scores(_dev(qI, torch.bfloat16, "qI"), _dev(wI, torch.float32, "wI"), _dev(KI, torch.bfloat16, "KI"), B, T, start_pos, Hi, dI,
+                                  KI.shape[1], compress_len, ratio, _dev(cand, torch.uint8, "cand"),
+                                  0 if cand is None else cand.shape[-1], cand_block, _dev(S, torch.float32, "S"), _stream(stream)),
+           "csa_index_scores")
     return S
 
 
 def index_topk(S, B, T, start_pos, compress_len, ratio, K, out, offset=0, cand=None, cand_block=1, stream=None):
-    _check(lib().csa_index_topk(_ptr(S), B, T, start_pos, S.shape[-1], compress_len, ratio, _ptr(cand),
-                                0 if cand is None else cand.shape[-1], cand_block, K, offset, _ptr(out),
-                                _stream(stream)), "csa_index_topk")
+    _check(lib().csa_index_topk(_dev(S, torch.float32, "S"), B, T, start_pos, S.shape[-1], compress_len, ratio,
+                                _dev(cand, torch.uint8, "cand"), 0 if cand is None else cand.shape[-1], cand_block, K, offset,
+                                _dev(out, torch.int32, "out"), _stream(stream)), "csa_index_topk")
     return out

@@ -3,8 +3,10 @@
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <atomic>
 #include <cstdint>
 #include <cstddef>
+#include <mutex>
 
 #include "../../include/csa.h"
 
@@ -29,19 +31,31 @@ struct PosSpec {
 };
 
 // The dynamic shared-memory limit of a kernel is a per-device attribute: each launcher keeps one of
-// these (static) and sets the attribute once per device, raising it when a launch needs more.
+// these (static) and raises the attribute of the current device when a launch needs more than it
+// has, never lowering it, so that host threads launching the same kernel with different needs do
+// not undo one another.  The per-device value last set is cached for the common case.
 constexpr int kAttrDevices = 64;
 struct SmemAttr {
-  int set[kAttrDevices] = {};
+  std::atomic<int> set[kAttrDevices] = {};
+  std::mutex mu;
   cudaError_t ensure(const void *func, int need) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const bool tracked = dev >= 0 && dev < kAttrDevices;
-    if (tracked && set[dev] >= need) return cudaSuccess;
-    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, need);
-    if (e == cudaSuccess && tracked) set[dev] = need;
-    return e;
+    if (tracked && set[dev].load(std::memory_order_acquire) >= need) return cudaSuccess;
+    std::lock_guard<std::mutex> lock(mu);
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, func);
+    if (e != cudaSuccess) return e;
+    int have = fa.maxDynamicSharedSizeBytes;
+    if (have < need) {
+      e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, need);
+      if (e != cudaSuccess) return e;
+      have = need;
+    }
+    if (tracked) set[dev].store(have, std::memory_order_release);
+    return cudaSuccess;
   }
 };
 

@@ -21,6 +21,10 @@
  * the last error of the calling thread is attn_v41_last_error().  Arguments are validated on the
  * host before anything is enqueued: on an error nothing is launched.  CSA_ERR_CUDA reports a launch
  * or runtime failure seen by the host (asynchronous faults surface at the caller's next sync).
+ *
+ * Threads: the entry points may be called from several host threads at once.  A csa_ctx, though,
+ * serves one stream at a time: its workspaces are shared by every call made with it, so calls on
+ * one context whose work could overlap on the GPU must be ordered by the caller.
  */
 #ifndef CSA_H_
 #define CSA_H_
