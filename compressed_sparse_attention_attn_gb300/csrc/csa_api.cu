@@ -96,6 +96,21 @@ struct csa_ctx {
   }
 };
 
+namespace {
+
+// A context's workspaces live on the device that was current at csa_create: the calls that launch
+// work with them, or wait for it, must find that device current.
+int check_device(const csa_ctx *ctx, const char *where) {
+  int dev = -1;
+  const cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, where);
+  if (dev != ctx->device)
+    return fail(CSA_ERR_ARG, "%s: the context lives on device %d, the current device is %d", where, ctx->device, dev);
+  return CSA_OK;
+}
+
+}  // namespace
+
 namespace csa {
 
 // RoPE table, "deepseek_v41_ref::attn" freqs_cis: [max_seq][rd/2] of (cos, sin) with pair i at
@@ -226,8 +241,13 @@ int csa_create(const csa_cfg *cfg, csa_ctx **out) {
 
 int csa_destroy(csa_ctx *ctx) {
   if (!ctx) return CSA_OK;
+  // wait for and free on the context's own device, then give the caller back its current device
+  int cur = -1;
+  const bool other = cudaGetDevice(&cur) == cudaSuccess && cur != ctx->device;
+  if (other) cudaSetDevice(ctx->device);
   cudaDeviceSynchronize();
   ctx->release();
+  if (other) cudaSetDevice(cur);
   delete ctx;
   return CSA_OK;
 }
@@ -236,6 +256,7 @@ size_t csa_workspace_bytes(const csa_ctx *ctx) { return ctx ? ctx->bytes : 0; }
 
 int csa_trace_enable(csa_ctx *ctx, int enable) {
   if (!ctx) return fail(CSA_ERR_ARG, "csa_trace_enable: NULL context");
+  if (int rc = check_device(ctx, "csa_trace_enable")) return rc;
   if (enable && ctx->stages.empty()) {
     ctx->stages.resize(32);
     for (auto &st : ctx->stages) {
@@ -270,6 +291,7 @@ int csa_rope_table_get(const csa_ctx *ctx, int ratio_class, float *tab_host) {
 
 int csa_status(csa_ctx *ctx, int clear) {
   if (!ctx) return fail(CSA_ERR_ARG, "csa_status: NULL context");
+  if (int rc = check_device(ctx, "csa_status")) return rc;
   int st = 0;
   CSA_CUDA(cudaDeviceSynchronize(), "csa_status: synchronize");
   CSA_CUDA(cudaMemcpy(&st, ctx->status, sizeof(int), cudaMemcpyDeviceToHost), "csa_status: read");
@@ -282,6 +304,7 @@ int csa_status(csa_ctx *ctx, int clear) {
 int csa_state_init(csa_ctx *ctx, csa_layer_state *state, int batch, csa_stream stream) {
   if (!ctx || !state || !state->window) return fail(CSA_ERR_ARG, "csa_state_init: NULL argument");
   if (batch <= 0 || batch > ctx->cfg.max_batch) return fail(CSA_ERR_SHAPE, "csa_state_init: batch %d", batch);
+  if (int rc = check_device(ctx, "csa_state_init")) return rc;
   CSA_CUDA(cudaMemsetAsync(state->window, 0, sizeof(bf16) * (size_t)batch * ctx->cfg.window * ctx->cfg.head_dim,
                            (cudaStream_t)stream),
            "csa_state_init");
@@ -297,6 +320,7 @@ int csa_linear(csa_ctx *ctx, const csa_bf16 *x, int M, int K, int ldx, const csa
   if (!ctx || !x || !W || !y) return fail(CSA_ERR_ARG, "csa_linear: NULL argument");
   if (M < 0 || K <= 0 || N <= 0 || groups <= 0 || ldx < K * groups || ldw < K || ldy < N * groups)
     return fail(CSA_ERR_ARG, "csa_linear: bad shape M=%d K=%d N=%d groups=%d", M, K, N, groups);
+  if (int rc = check_device(ctx, "csa_linear")) return rc;
   csa::LinearProblem pr{(const bf16 *)x, M, K, ldx, (const bf16 *)W, N, ldw, (bf16 *)y, ldy, groups};
   CSA_CUDA(csa::launch_linear(&pr, 1, ctx->ws, ctx->ws_bytes, ctx->num_sms, ctx->status, (cudaStream_t)stream),
            "csa_linear");
@@ -390,6 +414,7 @@ int csa_sparse_attn(csa_ctx *ctx, const csa_bf16 *q, int B, int T, int H, int hd
     return fail(CSA_ERR_ARG, "csa_sparse_attn: sequence strides must be whole rows");
   if (o_rot && (!tab || rd <= 0 || rd % 2 || rd > hd || start_pos < 0 || start_pos + T > tab_rows))
     return fail(CSA_ERR_ARG, "csa_sparse_attn: inverse rotation needs a table covering the positions");
+  if (int rc = check_device(ctx, "csa_sparse_attn")) return rc;
   csa::AttnArgs a{(const bf16 *)q, B, T, H, hd, (const bf16 *)rows_a, a_seq_stride, a_len, (const bf16 *)rows_b,
                   b_seq_stride, b_len, idx_a, na, idx_b, nb, sink, scale, (bf16 *)o, (bf16 *)o_rot, rd, start_pos,
                   tab, ctx->status};
@@ -404,6 +429,7 @@ int csa_sparse_attn(csa_ctx *ctx, const csa_bf16 *q, int B, int T, int H, int hd
 static int check_forward(const csa_ctx *ctx, const csa_layer_weights *w, const csa_layer_state *st, const void *x,
                          int B, int T, int start_pos, const csa_shared *sh, const void *out) {
   if (!ctx || !w || !st || !st->window || !x || !out) return fail(CSA_ERR_ARG, "attn_v41_forward: NULL argument");
+  if (int rc = check_device(ctx, "attn_v41_forward")) return rc;
   const csa_cfg &g = ctx->cfg;
   const csa_role &r = w->role;
   if (!w->sink || !w->q_norm || !w->kv_norm || !w->wq_a || !w->wq_b || !w->wkv || !w->wo_a || !w->wo_b)

@@ -24,7 +24,9 @@
  *
  * Threads: the entry points may be called from several host threads at once.  A csa_ctx, though,
  * serves one stream at a time: its workspaces are shared by every call made with it, so calls on
- * one context whose work could overlap on the GPU must be ordered by the caller.
+ * one context whose work could overlap on the GPU must be ordered by the caller.  A csa_ctx belongs
+ * to the device current at csa_create; the calls that launch work with it, or wait for it, return
+ * CSA_ERR_ARG when another device is current.
  */
 #ifndef CSA_H_
 #define CSA_H_
