@@ -114,6 +114,23 @@ def test_rotary_adjacent_pairs_and_inverse(orc):
     assert np.allclose(np.hypot(rv[..., 0], rv[..., 1]), np.hypot(vv[..., 0], vv[..., 1]), rtol=2 ** -7, atol=1e-6)
 
 
+def test_rotary_rounds_each_product_to_f32(orc):
+    """The complex product rounds each product and each sum to f32 on its own ([ref-attn] apply_rotary:
+    the pairs multiplied in f32).  With a = b = 1 + 2^-7 and (c, s) = (1 + 2^-23, 1), a c = 1 + 2^-7 +
+    2^-23 + 2^-30 rounds to 1 + 2^-7 + 2^-23, so re = fl(a c) - fl(b s) is exactly 2^-23; a fused
+    multiply-add, or a wider sum, keeps the 2^-30 and gives 2^-23 (1 + 2^-7), another bf16 value."""
+    u = 2.0 ** -7
+    x = orc.f32_to_bf16(np.array([[1 + u, 1 + u]], np.float32))
+    tab = np.array([[[1 + 2.0 ** -23, 1.0]]], np.float32)
+    y = orc.apply_rotary(x, 2, np.array([0], np.int32), tab)
+    bits = lambda v: int(orc.f32_to_bf16(np.array([v], np.float32))[0])
+    re_bits = int(y[0, 0])
+    assert re_bits == bits(2.0 ** -23)
+    assert re_bits != bits(2.0 ** -23 * (1 + u))
+    # im = fl(fl(a s) + fl(b c)) = fl(2 + 2^-6 + 2^-23): a tie in f32, to even: 2 + 2^-6
+    assert int(y[0, 1]) == bits(2 + 2.0 ** -6)
+
+
 def test_rotary_composes_angles(orc):
     rd, hd = 8, 8
     tab = orc.rope_table(rd, 64, 10000.0)

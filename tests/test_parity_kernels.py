@@ -64,6 +64,25 @@ def test_rope_bit_exact(csa, orc, rd, hd, inverse):
     assert np.array_equal(to_np(xd), want)
 
 
+def test_rope_rounds_each_product(csa, orc):
+    """A pair where rounding each product to f32 on its own and a fused multiply-add part at bf16:
+    a = b = 1 + 2^-7, (c, s) = (1 + 2^-23, 1) gives re = 2^-23 exactly (0x3400), 2^-23 (1 + 2^-7) with
+    the 2^-30 of a c kept."""
+    rng = np.random.default_rng(12)
+    rd, hd, rows = 16, 64, 4
+    x = _rng_bf16(orc, rng, (rows, hd))
+    x[:, hd - rd:hd - rd + 2] = orc.f32_to_bf16(np.full((rows, 2), 1 + 2.0 ** -7, np.float32))
+    tab = np.zeros((1, rd // 2, 2), np.float32)
+    tab[0, :, 0] = 1.0
+    tab[0, 0] = (1 + 2.0 ** -23, 1.0)
+    pos = np.zeros(rows, np.int32)
+    want = orc.apply_rotary(x, rd, pos, tab)
+    assert (want[:, hd - rd] == 0x3400).all()
+    xd = to_dev(x)
+    csa.rope(xd, rd, to_dev(pos), to_dev(tab))
+    assert np.array_equal(to_np(xd), want)
+
+
 def test_rope_tables_match_oracle(csa, orc):
     for g in (WORKLOADS["tiny_ratio0"].geom, Geometry(max_seq=70000, max_tokens=1, max_batch=1)):
         ctx = csa.Context(g.as_dict())
