@@ -98,6 +98,25 @@ def algorithmic_bytes(wl, shared_np, idx_counts):
     return attn * wl.layers, idx * wl.layers, topk * wl.layers
 
 
+def projection_bytes(wl):
+    """Per-step algorithmic bytes of each projection stage (all layers), bf16: its weights [out, in]
+    read once, its input activations read once and its outputs written once."""
+    g = wl.geom
+    M = wl.batch * wl.tokens
+    isrc = bool(wl.ratio and wl.is_index_source)
+    gw = g.n_heads * g.head_dim // g.groups
+    # (weights [out, in], activation width read, output width written) of one layer
+    stages = {
+        "proj x": ([(g.q_rank, g.dim), (g.head_dim, g.dim)] + ([(g.index_heads, g.dim)] if isrc else []), g.dim,
+                   g.q_rank + g.head_dim + (g.index_heads if isrc else 0)),
+        "proj qr": ([(g.n_heads * g.head_dim, g.q_rank)] + ([(g.index_heads * g.index_hd, g.q_rank)] if isrc else []),
+                    g.q_rank, g.n_heads * g.head_dim + (g.index_heads * g.index_hd if isrc else 0)),
+        "wo_a": ([(g.groups * g.o_rank, gw)], g.n_heads * g.head_dim, g.groups * g.o_rank),
+        "wo_b": ([(g.dim, g.groups * g.o_rank)], g.groups * g.o_rank, g.dim),
+    }
+    return {n: wl.layers * 2 * (sum(a * b for a, b in ws_) + M * xin + M * yout) for n, (ws_, xin, yout) in stages.items()}
+
+
 def selection_counts(wl, shared_np):
     """(gathered rows, valid compressed positions) summed over the batch's queries."""
     g = wl.geom
@@ -373,22 +392,10 @@ def run_csa(args, rank, world, dist):
                 a[1] += 1
     ctx.trace(False)
     stage_ms = {k: v[0] / args.steps for k, v in acc.items()}  # per step (all layers)
-    M = B * T
-    isrc = bool(wl.ratio and wl.is_index_source)
-    gw = g.n_heads * g.head_dim // g.groups
-    # projection stages of one layer: (weights [out, in] read once, activation width read, output width written)
-    lin_stages = {
-        "proj x": ([(g.q_rank, g.dim), (g.head_dim, g.dim)] + ([(g.index_heads, g.dim)] if isrc else []), g.dim,
-                   g.q_rank + g.head_dim + (g.index_heads if isrc else 0)),
-        "proj qr": ([(g.n_heads * g.head_dim, g.q_rank)] + ([(g.index_heads * g.index_hd, g.q_rank)] if isrc else []),
-                    g.q_rank, g.n_heads * g.head_dim + (g.index_heads * g.index_hd if isrc else 0)),
-        "wo_a": ([(g.groups * g.o_rank, gw)], g.n_heads * g.head_dim, g.groups * g.o_rank),
-        "wo_b": ([(g.dim, g.groups * g.o_rank)], g.groups * g.o_rank, g.dim),
-    }
     lin_bytes = lin_ms = 0.0
-    for n, (ws_, xin, yout) in lin_stages.items():
+    for n, nbytes in projection_bytes(wl).items():
         if n in stage_ms:
-            lin_bytes += wl.layers * 2 * (sum(a * b for a, b in ws_) + M * xin + M * yout)
+            lin_bytes += nbytes
             lin_ms += stage_ms[n]
     counts = selection_counts(wl, sh_np)
     b_attn, b_idx, b_topk = algorithmic_bytes(wl, sh_np, counts)

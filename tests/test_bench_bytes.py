@@ -79,3 +79,23 @@ def test_reindex_decode_counts_follow_the_mask():
     rows, n_valid = bench.selection_counts(wl, sh)
     assert n_valid == 32 * 4 * 64 - 12 * last_kept
     assert rows == 32 * 128 + n_valid
+
+
+def test_projection_bytes_match_the_parameter_table():
+    """The projections' algorithmic bytes of the Reindex decode step: every projection weight of the
+    layer once (the pages' parameter table, less the sink and the two norm vectors, which are not
+    projection weights), plus the 32 tokens' activations in and out of the four stages, bf16."""
+    import json
+    import bench
+    wl = WORKLOADS["reindex_decode_r2"]
+    g = wl.geom
+    pc = json.load(open(os.path.join(ROOT, "tests", "golden", "param_counts.json")))
+    weights = pc["per_instance_total"] - g.n_heads - g.q_rank - g.head_dim  # sink, q_norm, kv_norm
+    M = wl.batch * wl.tokens
+    acts = M * ((g.dim + g.q_rank + g.head_dim + g.index_heads)  # proj x: x in; qr, kv, w^I out
+                + (g.q_rank + g.n_heads * g.head_dim + g.index_heads * g.index_hd)  # proj qr: qr in; q, q^I out
+                + (g.n_heads * g.head_dim + g.groups * g.o_rank)  # wo_a: O in, og out
+                + (g.groups * g.o_rank + g.dim))  # wo_b: og in, out
+    got = bench.projection_bytes(wl)
+    assert set(got) == {"proj x", "proj qr", "wo_a", "wo_b"}
+    assert sum(got.values()) == 2 * (weights + acts) == 270403584
