@@ -115,6 +115,19 @@ def bf16_normal(shape, std, seed):
     return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16).copy()
 
 
+def fp8_weight(shape, seed, block=128):
+    """Random e4m3 weight storage: codes uint8 [N, K] drawn uniformly from the finite e4m3 codes (every
+    byte but 0x7f and 0xff, the NaNs) and one positive f32 scale per block x block tile, 2^u with u
+    uniform in [-12, -4).  Only random data: the dequantisation is the oracle's."""
+    N, K = shape
+    gen = _gen(seed)
+    codes = torch.randint(0, 254, (N, K), generator=gen, dtype=torch.int32)
+    codes = codes + (codes >= 0x7f).to(torch.int32)  # skip 0x7f; 0xff is above the drawn range
+    u = torch.rand(-(-N // block), -(-K // block), generator=gen, dtype=torch.float64) * 8.0 - 12.0
+    scales = torch.exp2(u).to(torch.float32)
+    return codes.to(torch.uint8).numpy().copy(), scales.numpy().copy()
+
+
 def f32_normal(shape, std, seed):
     return (torch.randn(*shape, generator=_gen(seed), dtype=torch.float32) * float(std)).numpy().copy()
 

@@ -4,8 +4,9 @@
 ``deepseek_v41_ref::attn`` rustdoc page, the DeepSeek V4.1 "Compressed sparse attention" and
 "Join rows" atlas pages, the ``metrale_model_arch::attn_v41`` docs).  This module builds it with
 gcc and exposes it to numpy through ctypes.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
-benchmark's ``cpu_baseline`` leg may import it; the GPU library never does, and the two share no
-code.  bf16 tensors travel as ``uint16`` arrays of their bit patterns.
+benchmark's ``cpu_baseline`` leg and reference arm may import it; the GPU library never does, and the
+two share no code.  bf16 tensors travel as ``uint16`` arrays of their bit patterns.
+:func:`dequant_fp8_blocks` (fp8 weight storage back to bf16) composes the C primitives in numpy.
 
 The YaRN form of :func:`rope_table` follows the published method (the pages give its constants
 only).  Pinned are its classes (pairs with at least beta_fast turns over the original length keep
@@ -152,6 +153,23 @@ def linear_bf16(x, W):
     y = np.empty(x.shape[:-1] + (N,), np.uint16)
     lib().orc_linear_bf16(_p(x), M, K, K, _p(W), N, K, _p(y), N)
     return y
+
+
+def dequant_fp8_blocks(codes, scales, block=128):
+    """Projection weights stored as e4m3 codes uint8 [N, K] with one f32 scale per block x block tile
+    (scales [ceil(N/block), ceil(K/block)]), back to bf16 as the converter does before the bf16
+    projections ([atlas] Attention excerpt: the grouped output projection is dequantised to bf16, and
+    an fp8 grouped GEMM would halve its memory): w = bf16(f32(e4m3(code) * scale)).  The product of a
+    4-bit significand and an f32 is exact in double, so one rounding to f32 gives the f32 product.
+    The tile layout is a reading (the published fp8 weight format of DeepSeek-V3: 128 x 128 tiles);
+    the pages print none."""
+    codes = _c(codes, np.uint8)
+    N, K = codes.shape
+    s = _c(scales, np.float32)
+    assert s.shape == (-(-N // block), -(-K // block)), (s.shape, N, K, block)
+    full = np.repeat(np.repeat(s, block, 0), block, 1)[:N, :K].astype(np.float64)
+    v = e4m3_decode(codes).astype(np.float64) * full
+    return f32_to_bf16(v.astype(np.float32))
 
 
 def rmsnorm(x, w, eps):

@@ -163,3 +163,53 @@ def test_act_quant_properties_random(orc):
     # idempotent
     out2, codes2, se2 = orc.act_quant(out)
     assert np.array_equal(out2, out)
+
+
+# ------------------------------------------------------------------- fp8 weight storage (128 x 128 tiles)
+
+def _fp8_case(seed, shape=(300, 260)):
+    import os
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    if root not in sys.path:
+        sys.path.insert(0, root)
+    from csa_inputs import fp8_weight
+    return fp8_weight(shape, seed)
+
+
+def test_fp8_weight_dequant_matches_torch(orc):
+    """bf16(f32(e4m3(code) * tile scale)) against torch's own float8_e4m3fn decode, f32 product and bf16
+    cast (library routines), on a ragged 300 x 260 matrix (tiles of 128: the last row and column of
+    tiles are partial)."""
+    codes, scales = _fp8_case(31)
+    got = orc.dequant_fp8_blocks(codes, scales, 128)
+    t = torch.from_numpy(codes).view(torch.float8_e4m3fn).float()
+    full = torch.from_numpy(scales).repeat_interleave(128, 0).repeat_interleave(128, 1)[:300, :260]
+    want = (t * full).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, want)
+
+
+def test_fp8_weight_dequant_power_of_two_scales_exact(orc):
+    """With power-of-two tile scales nothing rounds: a 4-bit significand times 2^k is a bf16 value."""
+    codes, _ = _fp8_case(32)
+    k = np.array([[-12, -3, 0], [4, -7, 2], [1, -1, -9]], np.float64)
+    scales = np.exp2(k).astype(np.float32)
+    got = orc.bf16_to_f32(orc.dequant_fp8_blocks(codes, scales, 128)).astype(np.float64)
+    full = np.repeat(np.repeat(k, 128, 0), 128, 1)[:300, :260]
+    assert np.array_equal(got, orc.e4m3_decode(codes).astype(np.float64) * np.exp2(full))
+
+
+def test_fp8_weight_dequant_tile_index(orc):
+    """Doubling the scale of tile (row tile 1, column tile 2) changes exactly the nonzero codes of rows
+    128..255 and columns 256..259, and nothing else (a transposed or shifted tile index fails)."""
+    codes, scales = _fp8_case(33)
+    s2 = scales.copy()
+    s2[1, 2] *= 2
+    d1 = orc.dequant_fp8_blocks(codes, scales, 128)
+    d2 = orc.dequant_fp8_blocks(codes, s2, 128)
+    changed = d1 != d2
+    inside = np.zeros_like(changed)
+    inside[128:256, 256:260] = True
+    nonzero = (codes & 0x7F) != 0
+    assert not (changed & ~inside).any()
+    assert np.array_equal(changed[inside], nonzero[inside])
