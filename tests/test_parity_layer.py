@@ -88,6 +88,16 @@ def _compare_rows(res, dbg, rows, g, what):
     _assert_fp8_rows_close(to_np(dbg["kv"])[rows], res["kv"][rows], what + " kv")
 
 
+def _compare_indexer_inputs(res, dbg, grows, rows, what):
+    """The indexer's query q^I = qr W_IQ^T (bf16) and head weights w^I = bf16(x W_IW^T) / sqrt(dI Hi)
+    (f32), read back from the forward: within the bf16 output tolerance, as their inputs differ by the
+    projections' rounding."""
+    assert_close_bf16(to_np(dbg["qI"])[grows], res["qI"][rows], what=what + " qI")
+    wg = to_np(dbg["wI"])[grows].astype(np.float64)
+    wo = res["wI"][rows].astype(np.float64)
+    assert np.all(np.abs(wg - wo) <= 2e-2 * np.abs(wo) + 2e-2 * np.abs(wo).max()), what + " wI"
+
+
 # ------------------------------------------------------------------------------------- tiny
 
 def test_tiny_ratio0_prefill_then_decode(csa, orc):
@@ -154,6 +164,7 @@ def test_small_ratio2_index_source_and_reuse(csa, orc, start, T, B, cand):
     dbg["__out"] = out
     rows = np.arange(B * T)
     _compare_rows(res, dbg, rows, g, "ratio2")
+    _compare_indexer_inputs(res, dbg, rows, rows, "ratio2")
     gi = to_np(dbg["idx"])
     assert np.array_equal(gi[:, :g.window], res["idx"][:, :g.window])
     # scores: inputs differ by the projections' bf16 rounding, so 1e-2 here (1e-3 at the kernel level)
@@ -364,6 +375,8 @@ def test_full_width_sampled(csa, orc, name, seqs, toks):
         assert_close_bf16(to_np(out).reshape(-1, g.dim)[grows], res["out"].reshape(-1, g.dim)[rows], what=name + " out")
         assert_close_bf16(to_np(dbg["o"])[grows], res["o"][rows], what=name + " o")
         _assert_fp8_rows_close(to_np(dbg["kv"])[grows], res["kv"][rows], name + " kv")
+        if wl.ratio and wl.is_index_source:
+            _compare_indexer_inputs(res, dbg, grows, rows, name)
         if toks is not None:  # every window row the oracle built: the sampled queries' windows and the ring's
             built = np.nonzero(np.abs(res["kv"].astype(np.int64)).sum(1))[0]
             _assert_fp8_rows_close(to_np(dbg["kv"])[b * T + built], res["kv"][built], name + " kv(all built)")
