@@ -34,8 +34,10 @@ sys.path.insert(0, ROOT)
 METRIC = "decode tokens/s per layer; sparse_attn+indexer HBM GB/s vs 8 TB/s (1×GB300)"
 DEFAULT_WORKLOAD = "reindex_decode_r2"
 NOMINAL_HBM_GBS = 8000.0
-# ncu dram__bytes_read.sum + dram__bytes_write.sum of one forward's k_gemm_tc launches (proj x, proj qr,
-# wo_a, wo_b), captured on the current kernel build
+# ncu dram__bytes_read.sum + dram__bytes_write.sum of one forward's projection launches (proj x, proj
+# qr, wo_a, wo_b), copied from the ncu capture summarised in the file below (not measured in this
+# run); set to None whenever those kernels change after the capture
+GEMM_TRAFFIC_SOURCE = "ncu capture, profiles/k_gemm_tc_reindex_decode_r2.md"
 GEMM_TRAFFIC_BYTES = {"reindex_decode_r2": (19058688 + 0) + (94515456 + 446976) + (69254656 + 12544) +
                                            (84549120 + 157440)}
 
@@ -49,6 +51,8 @@ def parse():
     p.add_argument("--workload", default=DEFAULT_WORKLOAD)
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-extra", action="store_true",
+                   help="skip the long-context and prefill figures the default workload's line adds")
     return p.parse_args()
 
 
@@ -294,51 +298,179 @@ def job_tokens_per_s(world, tokens_per_step, layers, steps, total_ms):
     return world * tokens_per_step * layers * steps / (total_ms / 1000.0)
 
 
+class Session:
+    """One workload's device inputs, context and step on this rank's GPU."""
+
+    def __init__(self, wl, rank, fp8_wo_a=False):
+        import torch
+        import compressed_sparse_attention_attn_gb300 as csa
+        self.wl = wl
+        g = wl.geom
+        B, T, start, K = wl.batch, wl.tokens, wl.start_pos, g.index_topk
+        self.np = build_inputs(wl, rank)
+        layers_np, x_np, ring_np, sh_np = self.np
+        if fp8_wo_a:
+            # the grouped wo_a kept as e4m3 codes with one f32 scale per 128 x 128 tile (seeded storage)
+            from csa_inputs import fp8_weight
+            gw = g.n_heads * g.head_dim // g.groups
+            layers_np = [dict(w) for w in layers_np]
+            for l, w in enumerate(layers_np):
+                w["wo_a_fp8"], w["wo_a_scale"] = fp8_weight((g.groups * g.o_rank, gw), 4100 + 100 * l)
+                del w["wo_a"]
+
+        def dev_bf16(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+
+        self.ctx = csa.Context(g.as_dict())
+        self.stream = torch.cuda.Stream()
+        torch.cuda.set_stream(self.stream)
+        self.role = dict(ratio=wl.ratio, is_index_source=int(wl.is_index_source),
+                         uses_candidates=int(wl.uses_candidates))
+        W = [{k: (dev_bf16(v) if v.dtype == np.uint16 else torch.from_numpy(v).cuda()) for k, v in w.items()}
+             for w in layers_np]
+        self.W = W
+        self.lws = [csa.Context.layer_weights(w, self.role) for w in W]
+        self.x = dev_bf16(x_np)
+        self.out = torch.empty_like(self.x)
+        self.rings = []
+        for _ in range(wl.layers):
+            r = dev_bf16(ring_np)
+            if start:
+                csa.act_quant(r)  # the ring holds fp8-rounded rows
+            self.rings.append(r)
+        self.shared = None
+        if sh_np is not None:
+            sel = torch.full((B * T, K), -1, dtype=torch.int32, device="cuda")
+            cand = None if sh_np["cand"] is None else torch.from_numpy(sh_np["cand"]).cuda()
+            self.shared = csa.Shared(dev_bf16(sh_np["Z"]), dev_bf16(sh_np["KI"]), sh_np["L"], sel, K, cand)
+        self.flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+
+    def step(self):
+        wl = self.wl
+        for l in range(wl.layers):
+            self.ctx.forward(None, self.role, self.rings[l], self.x, wl.start_pos, shared=self.shared, out=self.out,
+                             lw=self.lws[l])
+
+    def flush(self):
+        self.flush_buf.zero_()
+
+    def warm(self, n):
+        import torch
+        for _ in range(max(n, 3)):
+            self.step()
+        torch.cuda.synchronize()
+
+    def capture(self):
+        import torch
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=self.stream):
+            self.step()
+        for _ in range(2):
+            graph.replay()
+        torch.cuda.synchronize()
+        return graph
+
+    def timed(self, graph, steps):
+        """CUDA-event milliseconds of `steps` replays of graph, L2 flushed before each (outside the events)."""
+        import torch
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        torch.cuda.synchronize()
+        for i in range(steps):
+            self.flush()
+            ev[i][0].record(self.stream)
+            graph.replay()
+            ev[i][1].record(self.stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in ev]
+
+    def stage_times(self, steps):
+        """Per-step milliseconds of each stage (summed over the layers), from a captured step whose
+        stages are bracketed by event-record nodes, replayed `steps` times with L2 flushed before each
+        replay.  Falls back to eager traced forwards if the driver cannot time graph events."""
+        import torch
+        ctx = self.ctx
+        acc = {}
+        how = "graph replay (event-record nodes around each stage)"
+        try:
+            ctx.trace(True, append=True)
+            graph = self.capture()
+            for _ in range(steps):
+                self.flush()
+                graph.replay()
+                for name, ms in ctx.trace_read():
+                    acc[name] = acc.get(name, 0.0) + ms
+            del graph
+        except Exception:
+            acc = {}
+            how = "eager forwards (an event pair around each stage)"
+            ctx.trace(True)
+            for _ in range(steps):
+                self.flush()
+                for l in range(self.wl.layers):
+                    ctx.forward(None, self.role, self.rings[l], self.x, self.wl.start_pos, shared=self.shared,
+                                out=self.out, lw=self.lws[l])
+                    for name, ms in ctx.trace_read():
+                        acc[name] = acc.get(name, 0.0) + ms
+        ctx.trace(False)
+        torch.cuda.synchronize()
+        return {k: v / steps for k, v in acc.items()}, how
+
+    def close(self):
+        import torch
+        self.ctx.close()
+        self.W = self.lws = self.x = self.out = self.rings = self.shared = self.flush_buf = None
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+
+
+def attn_indexer_report(wl, sh_np, stage_ms, hbm_peak):
+    counts = selection_counts(wl, sh_np)
+    b_attn, b_idx, b_topk = algorithmic_bytes(wl, sh_np, counts)
+    t_attn = stage_ms.get("sparse_attn", 0.0)
+    # (short decode rows run scores and top-k as one kernel: its time counts as the indexer's)
+    t_idx = stage_ms.get("index scores", 0.0) + stage_ms.get("index scores + topk", 0.0)
+    t_topk = stage_ms.get("index topk", 0.0)
+    ai_bytes = b_attn + b_idx + b_topk
+    ai_ms = t_attn + t_idx + t_topk
+    ai_gbs = ai_bytes / (ai_ms * 1e6) if ai_ms > 0 else None
+    return {"bytes_per_step": int(ai_bytes), "ms_per_step": round(ai_ms, 5),
+            "achieved_gbs": None if ai_gbs is None else round(ai_gbs, 1),
+            "frac_of_8tbs": None if ai_gbs is None else round(ai_gbs / NOMINAL_HBM_GBS, 4),
+            "frac_of_measured": None if ai_gbs is None else round(ai_gbs / hbm_peak, 4),
+            "sparse_attn_ms": round(t_attn, 5), "index_scores_ms": round(t_idx, 5),
+            "index_topk_ms": round(t_topk, 5), "gathered_rows": counts[0], "candidate_keys": counts[1]}
+
+
+def prefill_tensor_report(wl, sh_np, stage_ms, tflops_peak):
+    """Algorithmic tensor work of the prefill's sparse attention (QK^T and PV over the gathered rows,
+    4 H hd flops a row) and indexer scores (2 Hi dI flops per valid query-key pair) over their times."""
+    g = wl.geom
+    rows, n_valid = selection_counts(wl, sh_np)
+    f_attn = 4.0 * g.n_heads * g.head_dim * rows * wl.layers
+    f_idx = 2.0 * g.index_heads * g.index_hd * n_valid * wl.layers
+    t_attn = stage_ms.get("sparse_attn", 0.0)
+    t_idx = stage_ms.get("index scores", 0.0) + stage_ms.get("index scores + topk", 0.0)
+    out = {}
+    for name, f, t in (("sparse_attn", f_attn, t_attn), ("index_scores", f_idx, t_idx)):
+        tf = f / (t * 1e9) if t > 0 else None
+        out[name] = {"gflop": round(f / 1e9, 2), "ms": round(t, 5), "tflops": None if tf is None else round(tf, 1),
+                     "frac_of_measured_bf16": None if tf is None else round(tf / tflops_peak, 4)}
+    out["index_topk_ms"] = round(stage_ms.get("index topk", 0.0), 5)
+    return out
+
+
 def run_csa(args, rank, world, dist):
     import torch
-    import compressed_sparse_attention_attn_gb300 as csa
     from csa_inputs import WORKLOADS
 
     dev = int(os.environ.get("LOCAL_RANK", 0))
     torch.cuda.set_device(dev)
     wl = WORKLOADS[args.workload]
     g = wl.geom
-    gd = g.as_dict()
-    B, T, start, K = wl.batch, wl.tokens, wl.start_pos, g.index_topk
-    layers_np, x_np, ring_np, sh_np = build_inputs(wl, rank)
-
-    def dev_bf16(a):
-        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
-
-    ctx = csa.Context(gd)
-    stream = torch.cuda.Stream()
-    torch.cuda.set_stream(stream)
-    role = dict(ratio=wl.ratio, is_index_source=int(wl.is_index_source), uses_candidates=int(wl.uses_candidates))
-    W = [{k: (dev_bf16(v) if v.dtype == np.uint16 else torch.from_numpy(v).cuda()) for k, v in w.items()}
-         for w in layers_np]
-    lws = [csa.Context.layer_weights(w, role) for w in W]
-    x = dev_bf16(x_np)
-    out = torch.empty_like(x)
-    rings = []
-    for _ in range(wl.layers):
-        r = dev_bf16(ring_np)
-        if start:
-            csa.act_quant(r)  # the ring holds fp8-rounded rows
-        rings.append(r)
-    shared = None
-    if sh_np is not None:
-        sel = torch.full((B * T, K), -1, dtype=torch.int32, device="cuda")
-        cand = None if sh_np["cand"] is None else torch.from_numpy(sh_np["cand"]).cuda()
-        shared = csa.Shared(dev_bf16(sh_np["Z"]), dev_bf16(sh_np["KI"]), sh_np["L"], sel, K, cand)
-
-    def step():
-        for l in range(wl.layers):
-            ctx.forward(None, role, rings[l], x, start, shared=shared, out=out, lw=lws[l])
-
-    flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
-
-    def flush():
-        flush_buf.zero_()
+    B, T, start = wl.batch, wl.tokens, wl.start_pos
+    S = Session(wl, rank)
+    ctx, stream = S.ctx, S.stream
+    sh_np = S.np[3]
 
     def barrier():
         torch.cuda.synchronize()
@@ -346,16 +478,9 @@ def run_csa(args, rank, world, dist):
             dist.barrier()
         torch.cuda.synchronize()
 
-    for _ in range(max(args.warmup, 3)):
-        step()
-    torch.cuda.synchronize()
+    S.warm(args.warmup)
     launches_per_step = ctx.last_launches() * wl.layers
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        step()
-    for _ in range(2):
-        graph.replay()
-    torch.cuda.synchronize()
+    graph = S.capture()
 
     # ---- timed region
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
@@ -365,7 +490,7 @@ def run_csa(args, rank, world, dist):
     time.sleep(0.3)
     wall0 = time.perf_counter()
     for i in range(args.steps):
-        flush()
+        S.flush()
         ev[i][0].record(stream)
         graph.replay()
         ev[i][1].record(stream)
@@ -379,54 +504,34 @@ def run_csa(args, rank, world, dist):
     tokens_per_step = B * T  # per layer per rank
     value = job_tokens_per_s(world, tokens_per_step, wl.layers, args.steps, total_ms)
 
-    # ---- per-stage kernel timing (traced forwards, flushed), for the roofline
-    ctx.trace(True)
-    acc = {}
-    for i in range(args.steps):
-        flush()
-        for l in range(wl.layers):
-            ctx.forward(None, role, rings[l], x, start, shared=shared, out=out, lw=lws[l])
-            for name, ms in ctx.trace_read():
-                a = acc.setdefault(name, [0.0, 0])
-                a[0] += ms
-                a[1] += 1
-    ctx.trace(False)
-    stage_ms = {k: v[0] / args.steps for k, v in acc.items()}  # per step (all layers)
+    # ---- per-stage kernel timing (replayed traced graph, flushed), for the roofline
+    stage_ms, stage_how = S.stage_times(args.steps)
     lin_bytes = lin_ms = 0.0
     for n, nbytes in projection_bytes(wl).items():
         if n in stage_ms:
             lin_bytes += nbytes
             lin_ms += stage_ms[n]
-    counts = selection_counts(wl, sh_np)
-    b_attn, b_idx, b_topk = algorithmic_bytes(wl, sh_np, counts)
-    t_attn = stage_ms.get("sparse_attn", 0.0)
-    # (short decode rows run scores and top-k as one kernel: its time counts as the indexer's)
-    t_idx = stage_ms.get("index scores", 0.0) + stage_ms.get("index scores + topk", 0.0)
-    t_topk = stage_ms.get("index topk", 0.0)
-    ai_bytes = b_attn + b_idx + b_topk
-    ai_ms = t_attn + t_idx + t_topk
-    ai_gbs = ai_bytes / (ai_ms * 1e6) if ai_ms > 0 else None
     peaks = measured_peaks()
     hbm_peak = peaks["hbm_gbs"] if peaks else 6800.0
+    tflops_peak = peaks["bf16_tflops"] if peaks else 1900.0
     peak_src = "measured" if peaks else "fallback"
     lin_gbs = lin_bytes / (lin_ms * 1e6) if lin_ms > 0 else 0.0
-    # DRAM bytes (read + write) of the four projection launches of one forward, from an ncu capture of
-    # the same kernel build; other workloads: none
     traffic = GEMM_TRAFFIC_BYTES.get(wl.name)
     roofline = {"kernel": "linear (weight-streaming projections, all launches of one step)", "bound": "hbm",
                 "achieved": round(lin_gbs, 1), "peak": hbm_peak, "unit": "GB/s",
                 "frac": round(lin_gbs / hbm_peak, 4),
                 "traffic": None if traffic is None else traffic * wl.layers,
+                "traffic_source": None if traffic is None else GEMM_TRAFFIC_SOURCE,
                 "algorithmic_bytes": int(lin_bytes), "peak_source": peak_src,
                 "share_of_step": round(lin_ms / ms_per_step, 3) if ms_per_step else None}
 
     # ---- end to end through the host-buffer entry point (pinned x in, out back to the host)
-    x_host = x.cpu().pin_memory()
+    x_host = S.x.cpu().pin_memory()
     out_host = torch.empty_like(x_host).pin_memory()
 
     def step_host():
         for l in range(wl.layers):
-            ctx.forward_host(lws[l], rings[l], x_host, start, shared, out_host, B, T)
+            ctx.forward_host(S.lws[l], S.rings[l], x_host, start, S.shared, out_host, B, T)
 
     for _ in range(2):
         step_host()
@@ -437,7 +542,7 @@ def run_csa(args, rank, world, dist):
     ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     barrier()
     for i in range(args.steps):
-        flush()
+        S.flush()
         ev2[i][0].record(stream)
         g2.replay()
         ev2[i][1].record(stream)
@@ -457,21 +562,55 @@ def run_csa(args, rank, world, dist):
                            "index_source": bool(wl.is_index_source), "candidates": bool(wl.uses_candidates),
                            "l2": "flushed between timed steps (512 MiB memset outside the events)",
                            "graph": "one step captured, replayed", "per_rank_batch": B},
-                "attn_indexer": {"bytes_per_step": int(ai_bytes), "ms_per_step": round(ai_ms, 5),
-                                 "achieved_gbs": None if ai_gbs is None else round(ai_gbs, 1),
-                                 "frac_of_8tbs": None if ai_gbs is None else round(ai_gbs / NOMINAL_HBM_GBS, 4),
-                                 "frac_of_measured": None if ai_gbs is None else round(ai_gbs / hbm_peak, 4),
-                                 "sparse_attn_ms": round(t_attn, 5), "index_scores_ms": round(t_idx, 5),
-                                 "index_topk_ms": round(t_topk, 5), "gathered_rows": counts[0],
-                                 "candidate_keys": counts[1]},
+                "attn_indexer": attn_indexer_report(wl, sh_np, stage_ms, hbm_peak),
                 "stages_ms": {k: round(v, 5) for k, v in stage_ms.items()},
+                "stage_timing": stage_how,
                 "roofline": roofline,
                 "e2e": {"value": round(e2e_value, 1), "unit": "tokens/s", "h2d_bytes_per_step": io_bytes,
                         "d2h_bytes_per_step": io_bytes},
                 "gpu_launches": launches_per_step * args.steps,
                 "clocks": clk, "wall_s": round(wall, 4)}
     del graph, g2
-    return line, (wl, layers_np, x_np, ring_np, sh_np)
+    data = (wl, S.np[0], S.np[1], S.np[2], sh_np)
+    S.close()
+
+    # ---- the other configurations' figures of the metric's second part, timed in the same run: the
+    # long-context decode's sparse attention + indexer + top-k bandwidth and the prefill chunk's
+    # attention and indexer tensor throughput
+    if line is not None and args.workload == DEFAULT_WORKLOAD and not args.no_extra:
+        # the same decode step with the grouped wo_a kept in fp8 (e4m3 codes, one scale per 128 x 128 tile)
+        Sf = Session(wl, rank, fp8_wo_a=True)
+        Sf.warm(args.warmup)
+        gf = Sf.capture()
+        fms = sum(Sf.timed(gf, args.steps)) / args.steps
+        del gf
+        stf, how = Sf.stage_times(args.steps)
+        gw = g.n_heads * g.head_dim // g.groups
+        wbytes = g.groups * g.o_rank * gw + 4 * (-(-g.groups * g.o_rank // 128)) * (-(-gw // 128)) + \
+            2 * B * T * (g.n_heads * g.head_dim + g.groups * g.o_rank)
+        wo_ms = stf.get("wo_a", 0.0)
+        line["fp8_wo_a"] = {"ms_per_step": round(fms, 5), "tokens_per_s": round(B * T * wl.layers / (fms / 1000.0), 1),
+                            "wo_a_ms": round(wo_ms, 5), "wo_a_bytes": int(wbytes),
+                            "wo_a_gbs": round(wbytes / (wo_ms * 1e6), 1) if wo_ms > 0 else None,
+                            "wo_a_frac_of_measured": round(wbytes / (wo_ms * 1e6) / hbm_peak, 4) if wo_ms > 0 else None,
+                            "stages_ms": {k: round(v, 5) for k, v in stf.items()}, "stage_timing": how,
+                            "weights": "wo_a e4m3 codes + f32 scale per 128x128 tile (seeded); other weights bf16"}
+        Sf.close()
+        for name, key in (("longctx_decode_r4", "longctx_attn_indexer"), ("prefill_r4", "prefill_tensor")):
+            wx = WORKLOADS[name]
+            Sx = Session(wx, rank)
+            Sx.warm(args.warmup)
+            st, how = Sx.stage_times(max(3, min(args.steps, 10)))
+            if name == "prefill_r4":
+                rep = prefill_tensor_report(wx, Sx.np[3], st, tflops_peak)
+            else:
+                rep = attn_indexer_report(wx, Sx.np[3], st, hbm_peak)
+            rep["workload"] = name
+            rep["layers"] = wx.layers
+            rep["stage_timing"] = how
+            line[key] = rep
+            Sx.close()
+    return line, data
 
 
 def main():

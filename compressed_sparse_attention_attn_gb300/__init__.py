@@ -105,8 +105,10 @@ class Shared:
 
 DEBUG_FIELDS = ("q", "kv", "kv_codes", "kv_scale", "idx", "scores", "o", "og", "qr", "qI", "wI")
 DEBUG_DTYPES = (torch.bfloat16, torch.bfloat16, torch.uint8, torch.int8, torch.int32, torch.float32, torch.bfloat16, torch.bfloat16, torch.bfloat16, torch.bfloat16, torch.float32)
-WEIGHT_FIELDS = ("sink", "q_norm", "kv_norm", "wq_a", "wq_b", "wkv", "wo_a", "wo_b", "idx_wq_b", "idx_wproj")
-WEIGHT_DTYPES = (torch.float32, torch.float32, torch.float32, torch.bfloat16, torch.bfloat16, torch.bfloat16, torch.bfloat16, torch.bfloat16, torch.bfloat16, torch.bfloat16)
+WEIGHT_FIELDS = ("sink", "q_norm", "kv_norm", "wq_a", "wq_b", "wkv", "wo_a", "wo_b", "idx_wq_b", "idx_wproj",
+                 "wo_a_fp8", "wo_a_scale")
+WEIGHT_DTYPES = (torch.float32, torch.float32, torch.float32, torch.bfloat16, torch.bfloat16, torch.bfloat16, torch.bfloat16,
+                 torch.bfloat16, torch.bfloat16, torch.bfloat16, torch.uint8, torch.float32)
 
 
 class Context:
@@ -184,17 +186,19 @@ class Context:
     def workspace_bytes(self):
         return lib().csa_workspace_bytes(self.h)
 
-    def trace(self, enable=True):
-        _check(lib().csa_trace_enable(self.h, int(enable)), "csa_trace_enable")
+    def trace(self, enable=True, append=False):
+        """Stage tracing: enable (each forward lists its own stages) or, with append, every forward
+        appends to one list that restarts here (several layers, or a captured and replayed step)."""
+        _check(lib().csa_trace_enable(self.h, 2 if (enable and append) else int(bool(enable))), "csa_trace_enable")
 
     def trace_read(self):
-        """[(stage name, milliseconds)] of the last traced forward (waits for its events)."""
-        names = (ctypes.c_char_p * 32)()
-        ms = (ctypes.c_float * 32)()
-        n = lib().csa_trace_read(self.h, 32, names, ms)
+        """[(stage name, milliseconds)] of the listed stages (waits for their events)."""
+        names = (ctypes.c_char_p * 64)()
+        ms = (ctypes.c_float * 64)()
+        n = lib().csa_trace_read(self.h, 64, names, ms)
         if n < 0:
             _check(n, "csa_trace_read")
-        return [(names[i].decode(), float(ms[i])) for i in range(min(n, 32))]
+        return [(names[i].decode(), float(ms[i])) for i in range(min(n, 64))]
 
     def last_launches(self):
         return lib().csa_last_launches(self.h)
@@ -209,6 +213,19 @@ class Context:
             out = torch.empty(x.shape[:-1] + (N * groups,), dtype=torch.bfloat16, device=x.device)
         _check(lib().csa_linear(self.h, _dev(x, torch.bfloat16, "x"), M, K, x.shape[-1], _dev(W, torch.bfloat16, "W"), N, K, _dev(out, torch.bfloat16, "out"),
                                 out.shape[-1], groups, _stream(stream)), "csa_linear")
+        return out
+
+    def linear_fp8w(self, x, W8, scale, out=None, groups=1, stream=None):
+        """y = x w^T with w = bf16(e4m3(W8) * scale per 128 x 128 tile); W8 uint8 [groups*N, K] codes,
+        scale f32 [ceil(groups*N/128), ceil(K/128)]."""
+        K = W8.shape[1]
+        N = W8.shape[0] // groups
+        M = x.numel() // x.shape[-1]
+        if out is None:
+            out = torch.empty(x.shape[:-1] + (N * groups,), dtype=torch.bfloat16, device=x.device)
+        _check(lib().csa_linear_fp8w(self.h, _dev(x, torch.bfloat16, "x"), M, K, x.shape[-1], _dev(W8, torch.uint8, "W8"),
+                                     _dev(scale, torch.float32, "scale"), N, K, _dev(out, torch.bfloat16, "out"),
+                                     out.shape[-1], groups, _stream(stream)), "csa_linear_fp8w")
         return out
 
     def sparse_attn(self, q, rows_a, a_len, idx_a, sink, scale, rows_b=None, b_len=0, idx_b=None, o=None, o_rot=None,

@@ -38,7 +38,7 @@ class Role(ctypes.Structure):
 
 class LayerWeights(ctypes.Structure):
     _fields_ = [("role", Role)] + [(n, P) for n in ("sink", "q_norm", "kv_norm", "wq_a", "wq_b", "wkv", "wo_a",
-                                                      "wo_b", "idx_wq_b", "idx_wproj")]
+                                                      "wo_b", "idx_wq_b", "idx_wproj", "wo_a_fp8", "wo_a_scale")]
 
 
 class LayerState(ctypes.Structure):
@@ -72,6 +72,9 @@ SIGNATURES = {
     "csa_last_launches": (I, [P]),
     "csa_linear": (I, [P, P, I, I, I, P, I, I, P, I, I, P]),
     "csa_linear_noalloc": (I, [P, I, I, I, P, I, I, P, I, I, P]),
+    "csa_linear_noalloc_status": (I, [I]),
+    "csa_debug_stall": (I, [ctypes.c_ulonglong]),
+    "csa_linear_fp8w": (I, [P, P, I, I, I, P, P, I, I, P, I, I, P]),
     "csa_rmsnorm": (I, [P, I, I, P, F, P, P]),
     "csa_rope": (I, [P, I64, I, I, P, I, P, I, I, P]),
     "csa_act_quant": (I, [P, I64, P, P, P]),

@@ -58,12 +58,15 @@ struct csa_ctx {
   int xpart_rows = 0;
   int32_t *idx_win = nullptr;
   int *status = nullptr;
-  float *ws = nullptr;  // split-K and split-row partials
+  float *ws = nullptr;  // split-K and split-row partials; the attention's arrival counters at the end
   size_t ws_bytes = 0;
+  size_t gemm_ws_bytes() const { return ws_bytes - csa::kAttnCounterBytes; }  // the projections' part
   int scores_stride = 0;
   size_t bytes = 0;
   std::vector<void *> allocs;
-  // tracing: one event pair per stage of the last forward, when enabled
+  // tracing: one event pair per stage of the last forward (mode 1) or of every forward since
+  // tracing was enabled (mode 2), when enabled
+  static constexpr int kTraceStages = 64;
   struct Stage {
     const char *name;
     cudaEvent_t a, b;
@@ -219,6 +222,8 @@ int csa_create(const csa_cfg *cfg, csa_ctx **out) {
 #undef ALLOC
   if (e == cudaSuccess) e = cudaMemset(c->status, 0, 4 * sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(c->ws, 0, csa::kGemmCounterBytes);  // Stream-K arrival counters
+  if (e == cudaSuccess)  // the attention's split arrival counters
+    e = cudaMemset(reinterpret_cast<uint8_t *>(c->ws) + c->ws_bytes - csa::kAttnCounterBytes, 0, csa::kAttnCounterBytes);
   if (e != cudaSuccess) {
     c->release();
     delete c;
@@ -255,16 +260,18 @@ int csa_destroy(csa_ctx *ctx) {
 size_t csa_workspace_bytes(const csa_ctx *ctx) { return ctx ? ctx->bytes : 0; }
 
 int csa_trace_enable(csa_ctx *ctx, int enable) {
+  constexpr int kTraceStages = csa_ctx::kTraceStages;
   if (!ctx) return fail(CSA_ERR_ARG, "csa_trace_enable: NULL context");
   if (int rc = check_device(ctx, "csa_trace_enable")) return rc;
   if (enable && ctx->stages.empty()) {
-    ctx->stages.resize(32);
+    ctx->stages.resize(kTraceStages);
     for (auto &st : ctx->stages) {
       CSA_CUDA(cudaEventCreate(&st.a), "csa_trace_enable");
       CSA_CUDA(cudaEventCreate(&st.b), "csa_trace_enable");
     }
   }
-  ctx->trace = enable ? 1 : 0;
+  ctx->trace = enable == 2 ? 2 : (enable ? 1 : 0);
+  ctx->n_stages = 0;
   return CSA_OK;
 }
 
@@ -295,9 +302,24 @@ int csa_status(csa_ctx *ctx, int clear) {
   int st = 0;
   CSA_CUDA(cudaDeviceSynchronize(), "csa_status: synchronize");
   CSA_CUDA(cudaMemcpy(&st, ctx->status, sizeof(int), cudaMemcpyDeviceToHost), "csa_status: read");
-  if (clear) CSA_CUDA(cudaMemset(ctx->status, 0, sizeof(int)), "csa_status: clear");
+  if (clear) {
+    CSA_CUDA(cudaMemset(ctx->status, 0, sizeof(int)), "csa_status: clear");
+    // a kernel that gave up may have left arrival counters raised: start them at zero
+    if (st & csa::kStatusTimeout) {
+      CSA_CUDA(cudaMemset(ctx->ws, 0, csa::kGemmCounterBytes), "csa_status: counters");
+      CSA_CUDA(cudaMemset(reinterpret_cast<uint8_t *>(ctx->ws) + ctx->ws_bytes - csa::kAttnCounterBytes, 0,
+                          csa::kAttnCounterBytes),
+               "csa_status: counters");
+    }
+    CSA_CUDA(cudaDeviceSynchronize(), "csa_status: clear");
+  }
   if (st & csa::kStatusTimeout) return fail(CSA_ERR_DEVICE_TIMEOUT, "a bounded device-side wait ran out");
   if (st & csa::kStatusBadIndex) return fail(CSA_ERR_ARG, "a selection index was outside [-1, rows)");
+  return CSA_OK;
+}
+
+int csa_debug_stall(unsigned long long ns) {
+  CSA_CUDA(csa::set_gemm_stall(ns), "csa_debug_stall");
   return CSA_OK;
 }
 
@@ -322,8 +344,26 @@ int csa_linear(csa_ctx *ctx, const csa_bf16 *x, int M, int K, int ldx, const csa
     return fail(CSA_ERR_ARG, "csa_linear: bad shape M=%d K=%d N=%d groups=%d", M, K, N, groups);
   if (int rc = check_device(ctx, "csa_linear")) return rc;
   csa::LinearProblem pr{(const bf16 *)x, M, K, ldx, (const bf16 *)W, N, ldw, (bf16 *)y, ldy, groups};
-  CSA_CUDA(csa::launch_linear(&pr, 1, ctx->ws, ctx->ws_bytes, ctx->num_sms, ctx->status, (cudaStream_t)stream),
+  CSA_CUDA(csa::launch_linear(&pr, 1, ctx->ws, ctx->gemm_ws_bytes(), ctx->num_sms, ctx->status, (cudaStream_t)stream),
            "csa_linear");
+  return CSA_OK;
+}
+
+int csa_linear_fp8w(csa_ctx *ctx, const csa_bf16 *x, int M, int K, int ldx, const uint8_t *W8, const float *scale,
+                    int N, int ldw8, csa_bf16 *y, int ldy, int groups, csa_stream stream) {
+  if (!ctx || !x || !W8 || !scale || !y) return fail(CSA_ERR_ARG, "csa_linear_fp8w: NULL argument");
+  if (M < 0 || K <= 0 || N <= 0 || groups <= 0 || ldx < K * groups || ldw8 < K || ldy < N * groups)
+    return fail(CSA_ERR_ARG, "csa_linear_fp8w: bad shape M=%d K=%d N=%d groups=%d", M, K, N, groups);
+  if (int rc = check_device(ctx, "csa_linear_fp8w")) return rc;
+  csa::LinearProblem pr{(const bf16 *)x, M, K, ldx, nullptr, N, ldw8, (bf16 *)y, ldy, groups};
+  pr.W8 = W8;
+  pr.w8_scale = scale;
+  if (M == 0) return CSA_OK;
+  if (!csa::gemm_tc_supported(pr))
+    return fail(CSA_ERR_ARG, "csa_linear_fp8w: x and W8 16-byte aligned, ldx a multiple of 8, ldw8 and K of 16 "
+                             "(K of 64 with groups)");
+  CSA_CUDA(csa::launch_linear(&pr, 1, ctx->ws, ctx->gemm_ws_bytes(), ctx->num_sms, ctx->status, (cudaStream_t)stream),
+           "csa_linear_fp8w");
   return CSA_OK;
 }
 
@@ -432,8 +472,14 @@ static int check_forward(const csa_ctx *ctx, const csa_layer_weights *w, const c
   if (int rc = check_device(ctx, "attn_v41_forward")) return rc;
   const csa_cfg &g = ctx->cfg;
   const csa_role &r = w->role;
-  if (!w->sink || !w->q_norm || !w->kv_norm || !w->wq_a || !w->wq_b || !w->wkv || !w->wo_a || !w->wo_b)
+  if (!w->sink || !w->q_norm || !w->kv_norm || !w->wq_a || !w->wq_b || !w->wkv || !w->wo_b ||
+      (!w->wo_a && !w->wo_a_fp8))
     return fail(CSA_ERR_ARG, "attn_v41_forward: a weight pointer is NULL");
+  if (w->wo_a_fp8) {
+    const int gw = g.n_heads * g.head_dim / g.groups;
+    if (!w->wo_a_scale || ((uintptr_t)w->wo_a_fp8 & 15) || gw % 64)
+      return fail(CSA_ERR_ARG, "attn_v41_forward: fp8 wo_a needs its scales, 16-byte alignment and gw a multiple of 64");
+  }
   if (r.ratio < 0) return fail(CSA_ERR_ARG, "attn_v41_forward: negative ratio");
   {
     const void *al[] = {x, out, w->wq_a, w->wq_b, w->wkv, w->wo_a, w->wo_b, w->idx_wq_b, w->idx_wproj};
@@ -496,20 +542,21 @@ int attn_v41_forward(csa_ctx *ctx, const csa_layer_weights *w, csa_layer_state *
     win_idx = dbg->idx;
     idx_stride = W + (r.ratio > 0 ? g.index_topk : 0);
   }
-  ctx->n_stages = 0;
+  if (ctx->trace != 2) ctx->n_stages = 0;
   ctx->launches = 0;
-  // one traced stage: events around it when tracing is on; counts the kernels it launches
+  // one traced stage: events around it when tracing is on (recorded as event nodes when the stream
+  // is being captured, so a replayed graph times its stages too); counts the kernels it launches
 #define STAGE(call, what, kernels)                                                             \
   do {                                                                                         \
     csa_ctx::Stage *st_ = nullptr;                                                             \
     if (ctx->trace && ctx->n_stages < (int)ctx->stages.size()) {                               \
       st_ = &ctx->stages[ctx->n_stages++];                                                     \
       st_->name = what;                                                                        \
-      cudaEventRecord(st_->a, s);                                                              \
+      cudaEventRecordWithFlags(st_->a, s, cudaEventRecordExternal);                            \
     }                                                                                          \
     cudaError_t e_ = (call);                                                                   \
     if (e_ != cudaSuccess) return cuda_fail(e_, what);                                         \
-    if (st_) cudaEventRecord(st_->b, s);                                                       \
+    if (st_) cudaEventRecordWithFlags(st_->b, s, cudaEventRecordExternal);                     \
     ctx->launches += (kernels);                                                                \
   } while (0)
 #define STEP(call, what) STAGE(call, what, 1)
@@ -546,7 +593,7 @@ int attn_v41_forward(csa_ctx *ctx, const csa_layer_weights *w, csa_layer_state *
   {
     csa::LinearProblem pq[2] = {lin(qr, g.q_rank, g.q_rank, w->wq_b, H * hd, q, H * hd, 1),
                                 lin(qr, g.q_rank, g.q_rank, w->idx_wq_b, Hi * dI, qI, Hi * dI, 1)};
-    STEP(csa::launch_linear(pq, idx_src ? 2 : 1, ctx->ws, ctx->ws_bytes, ctx->num_sms, ctx->status, s), "proj qr");
+    STEP(csa::launch_linear(pq, idx_src ? 2 : 1, ctx->ws, ctx->gemm_ws_bytes(), ctx->num_sms, ctx->status, s), "proj qr");
   }
   // the sparse attention's arguments: the selection's buffers are known before the index stages fill
   // them; rows_a = the window ring at decode, the chunk's own kv rows at prefill
@@ -607,9 +654,15 @@ int attn_v41_forward(csa_ctx *ctx, const csa_layer_weights *w, csa_layer_state *
   // grouped output: og[:, g] = o_rot[:, g*gw:(g+1)*gw] wo_a[g]^T, then out = og wo_b^T
   {
     csa::LinearProblem pa = lin(ctx->o_rot, gw, H * hd, w->wo_a, g.o_rank, og, G * g.o_rank, G);
-    STEP(csa::launch_linear(&pa, 1, ctx->ws, ctx->ws_bytes, ctx->num_sms, ctx->status, s), "wo_a");
+    if (w->wo_a_fp8) {  // the codes and tile scales in place of the bf16 weights
+      pa.W = nullptr;
+      pa.W8 = w->wo_a_fp8;
+      pa.w8_scale = w->wo_a_scale;
+      pa.ldw = gw;
+    }
+    STEP(csa::launch_linear(&pa, 1, ctx->ws, ctx->gemm_ws_bytes(), ctx->num_sms, ctx->status, s), "wo_a");
     csa::LinearProblem pb = lin(og, G * g.o_rank, G * g.o_rank, w->wo_b, g.dim, out, g.dim, 1);
-    STEP(csa::launch_linear(&pb, 1, ctx->ws, ctx->ws_bytes, ctx->num_sms, ctx->status, s), "wo_b");
+    STEP(csa::launch_linear(&pb, 1, ctx->ws, ctx->gemm_ws_bytes(), ctx->num_sms, ctx->status, s), "wo_b");
   }
 #undef STEP
 #undef COPY

@@ -81,12 +81,22 @@ struct LinearProblem {
   int ldy, groups;
   float *part = nullptr;  // split-K mode: f32 partials [S][M][ldp], this problem's columns at part
   int ldp = 0;
+  // fp8 weights (W unused): e4m3 codes uint8 [groups*N][ldw bytes] and one f32 scale per 128 x 128
+  // tile, w8_scale [ceil(groups*N/128)][ceil(K/128)]; the product uses w = bf16(e4m3 * scale)
+  const uint8_t *W8 = nullptr;
+  const float *w8_scale = nullptr;
 };
 // Products sharing M run in one tensor-core launch (up to 4 at a time).  ws/ws_bytes: Stream-K
 // arrival counters and partials (the counters must be zero between launches).
 cudaError_t launch_linear(const LinearProblem *probs, int n, float *ws, size_t ws_bytes, int num_sms, int *status,
                           cudaStream_t s);
 constexpr size_t kGemmCounterBytes = 65536 * sizeof(int);
+// Arrival counters of the sparse attention's split queries, at the END of a context's workspace
+// (zero between launches; the last CTA of a query resets its counter).
+constexpr size_t kAttnCounterBytes = 65536 * sizeof(int);
+// Failure-detection test hook of the current device: while ns != 0 the projection kernels first
+// wait, up to ns nanoseconds, on a barrier phase that nothing completes, then take their timeout path.
+cudaError_t set_gemm_stall(unsigned long long ns);
 // Split-K without fixup: products sharing M and K; CTA (tile, s) writes its f32 partial sum over
 // its K range to part[s][m][col] (every problem's part/ldp set).  The consumer sums the S slices.
 cudaError_t launch_gemm_tc_split(const LinearProblem *probs, int nprob, int S, int *status, cudaStream_t s);

@@ -21,13 +21,14 @@ cudaError_t launch_linear(const LinearProblem *probs, int n, float *ws, size_t w
     const LinearProblem &q = probs[i];
     if (q.M <= 0) continue;
     if (gemm_tc_supported(q)) {
-      if (nb == 4 || (nb > 0 && batch[0].M != q.M)) {
+      if (nb == 4 || (nb > 0 && (batch[0].M != q.M || (batch[0].W8 != nullptr) != (q.W8 != nullptr)))) {
         cudaError_t e = launch_gemm_tc(batch, nb, ws, ws_bytes, num_sms, status, s);
         if (e != cudaSuccess) return e;
         nb = 0;
       }
       batch[nb++] = q;
     } else {
+      if (q.W8) return cudaErrorInvalidValue;  // fp8 weights: tensor-core path only
       cudaError_t e = launch_linear_simt(q.x, q.M, q.K, q.ldx, q.W, q.N, q.ldw, q.y, q.ldy, q.groups, s);
       if (e != cudaSuccess) return e;
     }

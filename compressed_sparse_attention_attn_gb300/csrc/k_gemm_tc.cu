@@ -31,6 +31,9 @@
 #include "csa_internal.cuh"
 #include "tc_ptx.cuh"
 
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
 namespace csa {
 
 namespace gemm {
@@ -60,11 +63,16 @@ struct Problem {
   int ldp;
   // L2 policies of the two operands' copies: 0 evict-first, 1 normal, 2 evict-last
   int pol_a, pol_b;
+  // fp8 weights (kernels instantiated with kF8): tmA maps the e4m3 codes (uint8 [groups*N][Kg], box
+  // {64, 128}, unswizzled), with one f32 scale per 128 x 128 tile at scale[(row/128) * ld_scale + k/128]
+  const float *scale;
+  int ld_scale;
 };
 
 struct Params {
   Problem prob[kMaxProblems];
   int nprob, total_units, total_tiles, BN, stages;
+  int cstages;  // kF8: stages of the converted (bf16) weight ring
   int split_S;  // > 0: split-K mode, CTA c = (tile c / S, k-range c % S), partials out, no fixup
   // data-parallel waves: CTA c first takes the whole tiles c, c + G, ... (dp_waves of them; tiles
   // [0, dp_waves G) in all), then its Stream-K share of the units from sk_unit0 on
@@ -77,6 +85,14 @@ struct Params {
 struct Unit {
   int p, tile, kb;
 };
+
+// Failure-detection test hook of this device (csa_debug_stall): while nonzero, the MMA issuer of
+// every CTA first waits -- giving up after this many nanoseconds -- for a phase of its drain barrier
+// that nothing completes before its own final commit, so that the CTA takes its timeout path for
+// certain: the other roles see the abort flag, the producer lets its copies in flight land, the
+// status word records the timeout.
+__device__ unsigned long long g_stall_ns = 0ull;
+__device__ __forceinline__ uint64_t stall_ns() { return *const_cast<volatile unsigned long long *>(&g_stall_ns); }
 
 __device__ __forceinline__ Unit decode_unit(const Params &P, int u) {
   int p = 0;
@@ -114,18 +130,64 @@ __device__ __forceinline__ void seg_range(const Params &P, int s, int &ub, int &
   }
 }
 
+// fp8 weights: the 128 epilogue threads expand one stage's e4m3 weight slice (128 rows x 64 codes,
+// row-major, 64 bytes a row) into the bf16 operand the MMA reads (128 rows x 128 bytes, 128-byte
+// swizzle: 16-byte chunk c of row r at r * 128 + ((c ^ (r % 8)) << 4)), each value times its tile's
+// scale: w = bf16(f32(e4m3) * scale) with one f32 rounding of the product (exact e4m3 -> f32), which is
+// the bf16 weight the converter of the pages' checkpoint would produce.  Thread t takes the 16-byte
+// code chunks t, t + 128, ... (contiguous per warp); row0 = the tile's first weight row, rows at or
+// past nrows (the ragged end) get scale 0.
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ void fp8_expand_stage(const uint8_t *raw, uint8_t *dst, const float *scale, int ld_scale,
+                                                 int row0, int nrows, int kcol, int t) {
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const int q = it * 128 + t, r = q >> 2, part = q & 3;
+    const int gr = row0 + r;
+    const float sc = gr < nrows ? __ldg(scale + (int64_t)(gr >> 7) * ld_scale + kcol) : 0.f;
+    const uint4 v = *reinterpret_cast<const uint4 *>(raw + q * 16);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)((w[k] >> (16 * h)) & 0xffffu), __NV_E4M3);
+        const float2 f = __half22float2(__half2(hr));
+        const __nv_bfloat162 b2 = __floats2bfloat162_rn(__fmul_rn(f.x, sc), __fmul_rn(f.y, sc));
+        o[2 * k + h] = *reinterpret_cast<const uint32_t *>(&b2);
+      }
+    }
+    uint8_t *rp = dst + r * 128;
+    *reinterpret_cast<uint4 *>(rp + (((2 * part) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<uint4 *>(rp + (((2 * part + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+}
+
 // The product for few token tiles (decode) and split-K: each CTA one contiguous Stream-K range of
 // units (or one k-range of a tile).
+template <bool kF8>
 __global__ void __launch_bounds__(kThreads, 2) k_gemm_tc(const __grid_constant__ Params P) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = tc::smem_u32(smem_raw);
   uint8_t *smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
   const int S = P.stages, BN = P.BN;
   const uint32_t a_atom = BM * BK * 2, b_atom = (uint32_t)BN * BK * 2;
-  const uint32_t a_bytes = ATOMS * a_atom, b_bytes = ATOMS * b_atom, stage_bytes = a_bytes + b_bytes;
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + S * stage_bytes);
+  const uint32_t a_bytes = ATOMS * a_atom, b_bytes = ATOMS * b_atom;
+  // kF8: a stage holds the fp8 codes (a8_bytes) and B; the expanded bf16 weights go to a ring of
+  // SC slots of a_bytes after the stages
+  constexpr uint32_t a8_bytes = BM * BK;
+  static_assert(!kF8 || ATOMS == 1, "fp8 weights take one k-slice a stage");
+  const uint32_t a_in = kF8 ? a8_bytes : a_bytes;  // bytes of A in a stage
+  const uint32_t stage_bytes = a_in + b_bytes;
+  const int SC = kF8 ? P.cstages : 0;
+  uint8_t *conv = smem + S * stage_bytes;
+  uint64_t *full = reinterpret_cast<uint64_t *>(conv + SC * a_bytes);
   uint64_t *empty = full + S;
-  uint64_t *accf = empty + S;  // [2]
+  uint64_t *cfull = empty + S;    // kF8 [SC]: expanded weights ready (the 128 converter threads)
+  uint64_t *cempty = cfull + SC;  // kF8 [SC]: slot read by its MMAs
+  uint64_t *accf = cempty + SC;   // [2]
   uint64_t *acce = accf + 2;   // [2]
   uint64_t *drain = acce + 2;
   uint64_t *epi = drain + 1;  // the 128 epilogue threads' own barrier
@@ -155,6 +217,10 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemm_tc(const __grid_constant__
     for (int s = 0; s < S; ++s) {
       tc::mbar_init(&full[s], 1);
       tc::mbar_init(&empty[s], 1);
+    }
+    for (int c = 0; c < SC; ++c) {
+      tc::mbar_init(&cfull[c], 128);
+      tc::mbar_init(&cempty[c], 1);
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&accf[b], 1);
@@ -201,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemm_tc(const __grid_constant__
         for (int a = 0; a < ATOMS; ++a) {
           const int k0 = (un.kb * ATOMS + a) * BK;
           tc::tma_load_2d(sa + a * a_atom, &pr->tmA, &full[stage], k0, g * pr->N + tn * BM, pol_w);
-          tc::tma_load_2d(sa + a_bytes + a * b_atom, &pr->tmB, &full[stage], g * pr->Kg + k0, tm * BN, pol_x);
+          tc::tma_load_2d(sa + a_in + a * b_atom, &pr->tmB, &full[stage], g * pr->Kg + k0, tm * BN, pol_x);
         }
         ++issued;
         if (++stage == S) {
@@ -238,10 +304,13 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemm_tc(const __grid_constant__
       const uint32_t idesc = tc::idesc_bf16_f32(BM, BN);
       int stage = 0;
       uint32_t phase = 0;
+      int cst = 0;  // kF8: slot of the expanded-weight ring, and its phase
+      uint32_t cph = 0;
       int used[2] = {0, 0};
       int buf = 0;
       int u = u0;
       bool ok = true;
+      if (const uint64_t st = stall_ns()) ok = tc::mbar_wait(drain, 0, abort_flag, st);  // test hook
       while (u < u1 && ok) {
         const Unit un = decode_unit(P, u);
         const Problem &pr = P.prob[un.p];
@@ -255,18 +324,32 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemm_tc(const __grid_constant__
             ok = false;
             break;
           }
+          if constexpr (kF8) {  // the expanded weights of this unit
+            if (!tc::mbar_wait(&cfull[cst], cph, abort_flag)) {
+              ok = false;
+              break;
+            }
+          }
           tc::tc_fence_after();
           const uint32_t sa = tc::smem_u32(smem + stage * stage_bytes);
+          const uint32_t sa_w = kF8 ? tc::smem_u32(conv + cst * a_bytes) : sa;
 #pragma unroll
           for (int a = 0; a < ATOMS; ++a) {
-            const uint64_t ad = tc::sdesc_sw128(sa + a * a_atom, 16, 1024);
-            const uint64_t bd = tc::sdesc_sw128(sa + a_bytes + a * b_atom, 16, 1024);
+            const uint64_t ad = tc::sdesc_sw128(sa_w + a * a_atom, 16, 1024);
+            const uint64_t bd = tc::sdesc_sw128(sa + a_in + a * b_atom, 16, 1024);
 #pragma unroll
             for (int k = 0; k < BK / 16; ++k)
               tc::mma_bf16(d, ad + 2ull * k, bd + 2ull * k, idesc, (first && a == 0 && k == 0) ? 0u : 1u);
           }
           first = false;
           tc::mma_commit(&empty[stage]);
+          if constexpr (kF8) {
+            tc::mma_commit(&cempty[cst]);
+            if (++cst == SC) {
+              cst = 0;
+              cph ^= 1u;
+            }
+          }
           if (++stage == S) {
             stage = 0;
             phase ^= 1;
@@ -292,6 +375,29 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemm_tc(const __grid_constant__
       tc::mbar_arrive(epi);
       return tc::mbar_wait(epi, (epi_uses++) & 1u, abort_flag);
     };
+    // kF8: expand the weights of units [v0, v1) of one tile (first k-slice kb0, weight rows from
+    // row0), in unit order, into the expanded-weight ring
+    int rst = 0, cst = 0;
+    uint32_t rph = 0, cph = 0;
+    auto convert_units = [&](int v0, int v1, const Problem &pr, int row0, int kb0) -> bool {
+      for (int v = v0; v < v1; ++v) {
+        if (!tc::mbar_wait(&full[rst], rph, abort_flag)) return false;
+        if (!tc::mbar_wait(&cempty[cst], cph ^ 1u, abort_flag)) return false;
+        fp8_expand_stage(smem + rst * stage_bytes, conv + cst * a_bytes, pr.scale, pr.ld_scale, row0,
+                         pr.N * pr.groups, ((kb0 + v - v0) * BK) >> 7, threadIdx.x);
+        fence_proxy_async_smem();
+        tc::mbar_arrive(&cfull[cst]);
+        if (++rst == S) {
+          rst = 0;
+          rph ^= 1u;
+        }
+        if (++cst == SC) {
+          cst = 0;
+          cph ^= 1u;
+        }
+      }
+      return true;
+    };
     int buf = 0;
     int u = u0;
     const int first_tile_global = [&] {
@@ -310,6 +416,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemm_tc(const __grid_constant__
       const bool f_ok = f < pr.N;
       bf16 *ycol = pr.y + (int64_t)g * pr.N + f;
       const int gtile = pr.tile_begin + un.tile;
+      if constexpr (kF8) {
+        if (!convert_units(u, seg_end, pr, g * pr.N + tn * BM, un.kb)) break;
+      }
       if (!tc::mbar_wait(&accf[buf], (uint32_t)(done[buf] & 1), abort_flag)) break;
       tc::tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(buf * BN);
@@ -435,6 +544,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemm_tc(const __grid_constant__
 // The same product with data-parallel waves (many token tiles, large activations): each CTA takes
 // the whole tiles c, c + G, ... and then its Stream-K share of the tiles of the last, partial wave.
 // (A separate kernel: folding the segment loops into the one above measured slower at decode.)
+template <bool kF8>
 __global__ void __launch_bounds__(kThreads, 2) k_gemm_tc_waves(const __grid_constant__ Params P) {
   constexpr bool kWaves = true;
   extern __shared__ uint8_t smem_raw[];
@@ -442,10 +552,20 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemm_tc_waves(const __grid_cons
   uint8_t *smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
   const int S = P.stages, BN = P.BN;
   const uint32_t a_atom = BM * BK * 2, b_atom = (uint32_t)BN * BK * 2;
-  const uint32_t a_bytes = ATOMS * a_atom, b_bytes = ATOMS * b_atom, stage_bytes = a_bytes + b_bytes;
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + S * stage_bytes);
+  const uint32_t a_bytes = ATOMS * a_atom, b_bytes = ATOMS * b_atom;
+  // kF8: a stage holds the fp8 codes (a8_bytes) and B; the expanded bf16 weights go to a ring of
+  // SC slots of a_bytes after the stages
+  constexpr uint32_t a8_bytes = BM * BK;
+  static_assert(!kF8 || ATOMS == 1, "fp8 weights take one k-slice a stage");
+  const uint32_t a_in = kF8 ? a8_bytes : a_bytes;  // bytes of A in a stage
+  const uint32_t stage_bytes = a_in + b_bytes;
+  const int SC = kF8 ? P.cstages : 0;
+  uint8_t *conv = smem + S * stage_bytes;
+  uint64_t *full = reinterpret_cast<uint64_t *>(conv + SC * a_bytes);
   uint64_t *empty = full + S;
-  uint64_t *accf = empty + S;  // [2]
+  uint64_t *cfull = empty + S;    // kF8 [SC]: expanded weights ready (the 128 converter threads)
+  uint64_t *cempty = cfull + SC;  // kF8 [SC]: slot read by its MMAs
+  uint64_t *accf = cempty + SC;   // [2]
   uint64_t *acce = accf + 2;   // [2]
   uint64_t *drain = acce + 2;
   uint64_t *epi = drain + 1;  // the 128 epilogue threads' own barrier
@@ -466,6 +586,10 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemm_tc_waves(const __grid_cons
     for (int s = 0; s < S; ++s) {
       tc::mbar_init(&full[s], 1);
       tc::mbar_init(&empty[s], 1);
+    }
+    for (int c = 0; c < SC; ++c) {
+      tc::mbar_init(&cfull[c], 128);
+      tc::mbar_init(&cempty[c], 1);
     }
     for (int b = 0; b < 2; ++b) {
       tc::mbar_init(&accf[b], 1);
@@ -520,7 +644,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemm_tc_waves(const __grid_cons
         for (int a = 0; a < ATOMS; ++a) {
           const int k0 = (un.kb * ATOMS + a) * BK;
           tc::tma_load_2d(sa + a * a_atom, &pr->tmA, &full[stage], k0, g * N + tn * BM, pa);
-          tc::tma_load_2d(sa + a_bytes + a * b_atom, &pr->tmB, &full[stage], g * Kg + k0, tm * BN, pb);
+          tc::tma_load_2d(sa + a_in + a * b_atom, &pr->tmB, &full[stage], g * Kg + k0, tm * BN, pb);
         }
         ++issued;
         if (++stage == S) {
@@ -568,9 +692,12 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemm_tc_waves(const __grid_cons
       const uint32_t idesc = tc::idesc_bf16_f32(BM, BN);
       int stage = 0;
       uint32_t phase = 0;
+      int cst = 0;  // kF8: slot of the expanded-weight ring, and its phase
+      uint32_t cph = 0;
       int used[2] = {0, 0};
       int buf = 0;
       bool ok = true;
+      if (const uint64_t st = stall_ns()) ok = tc::mbar_wait(drain, 0, abort_flag, st);  // test hook
       for (int sg = 0; sg < nseg && ok; ++sg) {
       int ub, ue;
       seg_range<kWaves>(P, sg, ub, ue);
@@ -587,18 +714,32 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemm_tc_waves(const __grid_cons
             ok = false;
             break;
           }
+          if constexpr (kF8) {  // the expanded weights of this unit
+            if (!tc::mbar_wait(&cfull[cst], cph, abort_flag)) {
+              ok = false;
+              break;
+            }
+          }
           tc::tc_fence_after();
           const uint32_t sa = tc::smem_u32(smem + stage * stage_bytes);
+          const uint32_t sa_w = kF8 ? tc::smem_u32(conv + cst * a_bytes) : sa;
 #pragma unroll
           for (int a = 0; a < ATOMS; ++a) {
-            const uint64_t ad = tc::sdesc_sw128(sa + a * a_atom, 16, 1024);
-            const uint64_t bd = tc::sdesc_sw128(sa + a_bytes + a * b_atom, 16, 1024);
+            const uint64_t ad = tc::sdesc_sw128(sa_w + a * a_atom, 16, 1024);
+            const uint64_t bd = tc::sdesc_sw128(sa + a_in + a * b_atom, 16, 1024);
 #pragma unroll
             for (int k = 0; k < BK / 16; ++k)
               tc::mma_bf16(d, ad + 2ull * k, bd + 2ull * k, idesc, (first && a == 0 && k == 0) ? 0u : 1u);
           }
           first = false;
           tc::mma_commit(&empty[stage]);
+          if constexpr (kF8) {
+            tc::mma_commit(&cempty[cst]);
+            if (++cst == SC) {
+              cst = 0;
+              cph ^= 1u;
+            }
+          }
           if (++stage == S) {
             stage = 0;
             phase ^= 1;
@@ -625,6 +766,29 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemm_tc_waves(const __grid_cons
       tc::mbar_arrive(epi);
       return tc::mbar_wait(epi, (epi_uses++) & 1u, abort_flag);
     };
+    // kF8: expand the weights of units [v0, v1) of one tile (first k-slice kb0, weight rows from
+    // row0), in unit order, into the expanded-weight ring
+    int rst = 0, cst = 0;
+    uint32_t rph = 0, cph = 0;
+    auto convert_units = [&](int v0, int v1, const Problem &pr, int row0, int kb0) -> bool {
+      for (int v = v0; v < v1; ++v) {
+        if (!tc::mbar_wait(&full[rst], rph, abort_flag)) return false;
+        if (!tc::mbar_wait(&cempty[cst], cph ^ 1u, abort_flag)) return false;
+        fp8_expand_stage(smem + rst * stage_bytes, conv + cst * a_bytes, pr.scale, pr.ld_scale, row0,
+                         pr.N * pr.groups, ((kb0 + v - v0) * BK) >> 7, threadIdx.x);
+        fence_proxy_async_smem();
+        tc::mbar_arrive(&cfull[cst]);
+        if (++rst == S) {
+          rst = 0;
+          rph ^= 1u;
+        }
+        if (++cst == SC) {
+          cst = 0;
+          cph ^= 1u;
+        }
+      }
+      return true;
+    };
     int buf = 0;
     // the Stream-K share's first tile (its partial goes to slot 0, the last tile's to slot 1)
     const int first_tile_global = [&] {
@@ -650,6 +814,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemm_tc_waves(const __grid_cons
       const bool f_ok = f < pr.N;
       bf16 *ycol = pr.y + (int64_t)g * pr.N + f;
       const int gtile = pr.tile_begin + un.tile;
+      if constexpr (kF8) {
+        if (!(eok = convert_units(u, seg_end, pr, g * pr.N + tn * BM, un.kb))) break;
+      }
       if (!(eok = tc::mbar_wait(&accf[buf], (uint32_t)(done[buf] & 1), abort_flag))) break;
       tc::tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(buf * BN);
@@ -807,6 +974,22 @@ bool map_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, ui
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D uint8 map (fp8 weight codes) of a row-major [outer][inner] byte array with row stride `ld`
+// bytes, unswizzled.
+bool map_2d_u8(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint64_t ld, uint32_t box_inner,
+               uint32_t box_outer) {
+  EncodeTiledFn enc = encoder();
+  if (!enc) return false;
+  if (((uintptr_t)base & 15) || ld % 16) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {ld};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace gemm
 
 bool tma_map_2d_bf16(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint64_t ld, uint32_t box_inner,
@@ -849,18 +1032,35 @@ cudaError_t launch_gemm_tc(const LinearProblem *probs, int nprob, float *ws, siz
   Params P;
   memset(&P, 0, sizeof(P));
   P.BN = gemm_tc_bn(M);
-  const int stage_bytes = ATOMS * (BM * BK * 2 + P.BN * BK * 2);
+  // fp8 weights: every problem of the launch, one k-slice a stage; the stages hold the codes (half
+  // the bytes of bf16, so twice the stages fit and twice the weight k-slices are in flight) and a ring
+  // of four expanded bf16 slices feeds the MMA
+  const bool f8 = probs[0].W8 != nullptr;
+  for (int i = 1; i < nprob; ++i)
+    if ((probs[i].W8 != nullptr) != f8) return cudaErrorInvalidValue;
+  if (f8 && ATOMS != 1) return cudaErrorInvalidValue;
+  const int stage_bytes = f8 ? BM * BK + P.BN * BK * 2 : ATOMS * (BM * BK * 2 + P.BN * BK * 2);
   // one CTA per SM: two per SM (five stages each) measured slower at decode, because twice the CTAs
   // split each tile's k-range twice as often and the Stream-K fixups dominate
   const int per_sm = 1;
-  P.stages = per_sm == 2 ? std::min(5, (100 * 1024) / stage_bytes) : std::min(8, (200 * 1024) / stage_bytes);
+  P.cstages = f8 ? 4 : 0;
+  const int conv_bytes = P.cstages * BM * BK * 2;
+  P.stages = per_sm == 2 ? std::min(5, (100 * 1024) / stage_bytes)
+                         : std::min(f8 ? 16 : 8, (200 * 1024 - conv_bytes) / stage_bytes);
   if (P.stages < 2) return cudaErrorInvalidValue;
   int units = 0, tiles = 0;
   for (int i = 0; i < nprob; ++i) {
     const LinearProblem &q = probs[i];
     if (q.M != M) return cudaErrorInvalidValue;
     Problem &p = P.prob[i];
-    if (!map_2d(&p.tmA, q.W, (uint64_t)q.K, (uint64_t)q.N * q.groups, (uint64_t)q.ldw, BK, BM)) return cudaErrorInvalidValue;
+    if (f8) {
+      if (!q.w8_scale || !map_2d_u8(&p.tmA, q.W8, (uint64_t)q.K, (uint64_t)q.N * q.groups, (uint64_t)q.ldw, BK, BM))
+        return cudaErrorInvalidValue;
+      p.scale = q.w8_scale;
+      p.ld_scale = (q.K + 127) / 128;
+    } else if (!map_2d(&p.tmA, q.W, (uint64_t)q.K, (uint64_t)q.N * q.groups, (uint64_t)q.ldw, BK, BM)) {
+      return cudaErrorInvalidValue;
+    }
     if (!map_2d(&p.tmB, q.x, (uint64_t)q.K * q.groups, (uint64_t)M, (uint64_t)q.ldx, BK, (uint32_t)P.BN))
       return cudaErrorInvalidValue;
     p.y = q.y;
@@ -933,17 +1133,28 @@ cudaError_t launch_gemm_tc(const LinearProblem *probs, int nprob, float *ws, siz
   P.counters = reinterpret_cast<int *>(ws);
   P.partials = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(ws) + kCounterBytes);
   P.status = status;
-  const size_t smem = 1024 + (size_t)P.stages * stage_bytes + 256 + kMaxContrib * sizeof(int);
-  static SmemAttr attr, attr_waves;
+  const size_t smem = 1024 + (size_t)P.stages * stage_bytes + conv_bytes +
+                      (size_t)(2 * P.stages + 2 * P.cstages + 8) * 8 + 64 + kMaxContrib * sizeof(int);
+  if (smem > 227 * 1024) return cudaErrorInvalidValue;
+  static SmemAttr attr, attr_waves, attr8, attr8_waves;
+  const void *fn = P.dp_waves > 0 ? (f8 ? (const void *)k_gemm_tc_waves<true> : (const void *)k_gemm_tc_waves<false>)
+                                  : (f8 ? (const void *)k_gemm_tc<true> : (const void *)k_gemm_tc<false>);
   {
-    cudaError_t e = P.dp_waves > 0 ? attr_waves.ensure((const void *)k_gemm_tc_waves, 227 * 1024)
-                                   : attr.ensure((const void *)k_gemm_tc, 227 * 1024);
+    SmemAttr &at = P.dp_waves > 0 ? (f8 ? attr8_waves : attr_waves) : (f8 ? attr8 : attr);
+    cudaError_t e = at.ensure(fn, 227 * 1024);
     if (e != cudaSuccess) return e;
   }
-  if (P.dp_waves > 0)
-    k_gemm_tc_waves<<<grid, kThreads, smem, s>>>(P);
-  else
-    k_gemm_tc<<<grid, kThreads, smem, s>>>(P);
+  if (P.dp_waves > 0) {
+    if (f8)
+      k_gemm_tc_waves<true><<<grid, kThreads, smem, s>>>(P);
+    else
+      k_gemm_tc_waves<false><<<grid, kThreads, smem, s>>>(P);
+  } else {
+    if (f8)
+      k_gemm_tc<true><<<grid, kThreads, smem, s>>>(P);
+    else
+      k_gemm_tc<false><<<grid, kThreads, smem, s>>>(P);
+  }
   return cudaGetLastError();
 }
 
@@ -973,7 +1184,7 @@ cudaError_t launch_gemm_tc_split(const LinearProblem *probs, int nprob, int S, i
   int units = 0, tiles = 0;
   for (int i = 0; i < nprob; ++i) {
     const LinearProblem &q = probs[i];
-    if (q.M != M || q.K != K || !q.part) return cudaErrorInvalidValue;
+    if (q.M != M || q.K != K || !q.part || q.W8) return cudaErrorInvalidValue;
     Problem &p = P.prob[i];
     if (!map_2d(&p.tmA, q.W, (uint64_t)q.K, (uint64_t)q.N * q.groups, (uint64_t)q.ldw, BK, BM)) return cudaErrorInvalidValue;
     if (!map_2d(&p.tmB, q.x, (uint64_t)q.K * q.groups, (uint64_t)M, (uint64_t)q.ldx, BK, (uint32_t)P.BN))
@@ -1008,16 +1219,22 @@ cudaError_t launch_gemm_tc_split(const LinearProblem *probs, int nprob, int S, i
   const size_t smem = 1024 + (size_t)P.stages * stage_bytes + 256 + kMaxContrib * sizeof(int);
   static SmemAttr attr;
   {
-    cudaError_t e = attr.ensure((const void *)k_gemm_tc, 227 * 1024);
+    cudaError_t e = attr.ensure((const void *)k_gemm_tc<false>, 227 * 1024);
     if (e != cudaSuccess) return e;
   }
-  k_gemm_tc<<<tiles * S, kThreads, smem, s>>>(P);
+  k_gemm_tc<false><<<tiles * S, kThreads, smem, s>>>(P);
   return cudaGetLastError();
 }
 
 // Whether the tensor-core path takes a problem: TMA needs 16-byte aligned bases and row strides;
 // grouped products need each group's K to be whole 64-wide slices.
 bool gemm_tc_supported(const LinearProblem &q) {
+  if (q.W8) {  // fp8 weights: 16-byte aligned codes and rows
+    if (((uintptr_t)q.W8 & 15) || q.ldw % 16 || q.K % 16 || !q.w8_scale || ((uintptr_t)q.x & 15) || q.ldx % 8)
+      return false;
+    if (q.groups > 1 && q.K % gemm::BK) return false;
+    return q.M > 0 && q.N > 0 && gemm::encoder() != nullptr;
+  }
   if (((uintptr_t)q.x & 15) || ((uintptr_t)q.W & 15)) return false;
   if (q.ldx % 8 || q.ldw % 8 || q.K % 8) return false;
   if (q.groups > 1 && q.K % (gemm::BK * gemm::ATOMS)) return false;
@@ -1034,9 +1251,14 @@ bool gemm_tc_supported(const LinearProblem &q) {
 // partials and a status word -- is this file-scope device array, which every GPU that loads the
 // library holds until the process exits.  Host code must not hand the array's name to a kernel:
 // in host code it is only a stand-in; the device address comes from cudaGetSymbolAddress, looked up
-// once per device (with that device current) by the first call made on it.
+// by the first call made with a given device and CUDA context current (a device reset makes a new
+// context, whose first call looks the address up again).
 
 namespace csa {
+
+// failure-detection test hook of the projection kernels on the current device (0: off)
+cudaError_t set_gemm_stall(unsigned long long ns) { return cudaMemcpyToSymbol(gemm::g_stall_ns, &ns, sizeof(ns)); }
+
 namespace {
 
 constexpr int kNoAllocMaxM = 32;     // tokens: the partials below are sized for BN <= 32
@@ -1048,9 +1270,58 @@ constexpr int kNoAllocMaxDevices = 128;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
 
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+CtxGetCurrentFn ctx_get_current() {
+  static const CtxGetCurrentFn fn = [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      return reinterpret_cast<CtxGetCurrentFn>(p);
+    return static_cast<CtxGetCurrentFn>(nullptr);
+  }();
+  return fn;
+}
+
 std::mutex g_noalloc_mu;
-void *g_noalloc_addr[kNoAllocMaxDevices];
-int g_noalloc_sms[kNoAllocMaxDevices];
+struct NoAllocSlot {
+  CUcontext ctx;  // the context the address belongs to
+  void *addr;
+  int sms;
+};
+NoAllocSlot g_noalloc[kNoAllocMaxDevices];
+
+// The array's device address on the current device and context, looked up on first use there
+// (under the lock, so concurrent first calls look it up once).  Returns CSA_OK or an error code.
+int noalloc_scratch(const char *who, bool lookup, void **addr, int *sms) {
+  *addr = nullptr;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return set_error(CSA_ERR_CUDA, "%s: cudaGetDevice: %s", who, cudaGetErrorString(e));
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return set_error(CSA_ERR_ARG, "%s: device %d", who, dev);
+  // the current context (NULL while the runtime has not made one current yet on this thread)
+  CUcontext cur = nullptr;
+  CtxGetCurrentFn get = ctx_get_current();
+  if (!get || get(&cur) != CUDA_SUCCESS) return set_error(CSA_ERR_CUDA, "%s: cuCtxGetCurrent unavailable", who);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  NoAllocSlot &sl = g_noalloc[dev];
+  if (!cur || !sl.addr || sl.ctx != cur) {
+    if (!lookup) return CSA_OK;  // nothing has run with this context
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);  // (makes the device's primary context current)
+    if (e != cudaSuccess || !p) return set_error(CSA_ERR_CUDA, "%s: cudaGetSymbolAddress: %s", who, cudaGetErrorString(e));
+    if (get(&cur) != CUDA_SUCCESS || !cur) return set_error(CSA_ERR_CUDA, "%s: no current context", who);
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return set_error(CSA_ERR_CUDA, "%s: device query: %s", who, cudaGetErrorString(e));
+    sl.ctx = cur;
+    sl.addr = p;
+    sl.sms = n;
+  }
+  *addr = sl.addr;
+  if (sms) *sms = sl.sms;
+  return CSA_OK;
+}
 
 }  // namespace
 }  // namespace csa
@@ -1073,34 +1344,32 @@ extern "C" int csa_linear_noalloc(const csa_bf16 *x, int M, int K, int ldx, cons
     return set_error(CSA_ERR_ARG,
                      "csa_linear_noalloc: operands and row strides must be 16-byte aligned, K a multiple of 8 "
                      "(of 64 with groups)");
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return set_error(CSA_ERR_CUDA, "csa_linear_noalloc: cudaGetDevice: %s", cudaGetErrorString(e));
-  if (dev < 0 || dev >= kNoAllocMaxDevices) return set_error(CSA_ERR_ARG, "csa_linear_noalloc: device %d", dev);
   void *scratch = nullptr;
   int sms = 0;
-  {
-    std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_addr[dev]) {
-      void *p = nullptr;
-      e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-      if (e != cudaSuccess || !p)
-        return set_error(CSA_ERR_CUDA, "csa_linear_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
-      e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-      if (e != cudaSuccess)
-        return set_error(CSA_ERR_CUDA, "csa_linear_noalloc: device query: %s", cudaGetErrorString(e));
-      g_noalloc_sms[dev] = sms;
-      g_noalloc_addr[dev] = p;
-    }
-    scratch = g_noalloc_addr[dev];
-    sms = g_noalloc_sms[dev];
-  }
+  if (int rc = noalloc_scratch("csa_linear_noalloc", true, &scratch, &sms)) return rc;
   cudaStream_t s = (cudaStream_t)stream;
-  // the array keeps the last call's contents: the counters this launch uses must start at zero
-  e = cudaMemsetAsync(scratch, 0, (size_t)tiles * sizeof(int), s);
+  // the array keeps the last call's contents: the counters this launch uses must start at zero (the
+  // status word is not cleared: it keeps a timeout until csa_linear_noalloc_status clears it)
+  cudaError_t e = cudaMemsetAsync(scratch, 0, (size_t)tiles * sizeof(int), s);
   if (e != cudaSuccess) return set_error(CSA_ERR_CUDA, "csa_linear_noalloc: clear: %s", cudaGetErrorString(e));
   int *status = reinterpret_cast<int *>(static_cast<unsigned char *>(scratch) + kNoAllocWsBytes);
   e = launch_gemm_tc(&pr, 1, static_cast<float *>(scratch), kNoAllocWsBytes, std::min(sms, kNoAllocMaxGrid), status, s);
   if (e != cudaSuccess) return set_error(CSA_ERR_CUDA, "csa_linear_noalloc: launch: %s", cudaGetErrorString(e));
+  return CSA_OK;
+}
+
+extern "C" int csa_linear_noalloc_status(int clear) {
+  using namespace csa;
+  void *scratch = nullptr;
+  if (int rc = noalloc_scratch("csa_linear_noalloc_status", false, &scratch, nullptr)) return rc;
+  if (!scratch) return CSA_OK;  // no call has run on this device and context
+  int *status = reinterpret_cast<int *>(static_cast<unsigned char *>(scratch) + kNoAllocWsBytes);
+  int st = 0;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(&st, status, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && clear) e = cudaMemset(status, 0, sizeof(int));
+  if (e == cudaSuccess && clear) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return set_error(CSA_ERR_CUDA, "csa_linear_noalloc_status: %s", cudaGetErrorString(e));
+  if (st & kStatusTimeout) return set_error(CSA_ERR_DEVICE_TIMEOUT, "csa_linear_noalloc: a bounded device-side wait ran out");
   return CSA_OK;
 }

@@ -98,20 +98,15 @@ cudaError_t launch_index_scores(const bf16 *qI, const float *wI, const bf16 *KI,
 
 // ---------------------------------------------------------------------------------------------
 // Top-k: one CTA per query (512 threads, four CTAs an SM, for rows of at most 2048 positions; 1024
-// otherwise).  Scores map to order-preserving 32-bit keys (-0 folded onto +0, NaN below every number)
-// and each valid position j to the 64-bit value (key << 32) | ~j, so that the values are distinct and
-// larger means selected first (higher score, then lower position).  A first pass compacts the valid
-// values into shared memory (with a candidate mask: the kept blocks listed first, only their
-// positions visited); when they are at most K, all are taken.  The rest (topk_core.cuh):
-// Otherwise a radix select on the 64-bit values (8 bits per pass, one shared atomic per value, over
-// shared memory) finds the K-th largest, and the values at or above it are taken.  (A query with more
-// valid positions than shared memory holds runs the same passes over its scores in global memory.)
-// The chosen values are then sorted descending by a bitonic network whose stages within a warp run
-// on shuffles and whose wider stages go through shared memory.
+// otherwise).  A first pass gathers the valid positions' 64-bit values into shared memory in
+// ascending position (with a candidate mask: the kept blocks listed first, only their positions
+// visited, each round compacted in order); the selection and its position-ordered output are
+// topk_core.cuh's.  (A query with more valid positions than shared memory holds runs the same
+// passes over its scores in global memory.)
 // ---------------------------------------------------------------------------------------------
 constexpr int kTopkCap = 12288;  // valid positions of one query held in shared memory (96 KiB at most)
-// dynamic shared memory for candidate buffers of `cap` values
-constexpr size_t topk_smem(int cap, int nt) { return (size_t)(cap + kTopkMaxK + nt) * 8; }
+// dynamic shared memory: `cap` values and the kept-block list
+constexpr size_t topk_smem(int cap, int nt) { return (size_t)cap * 8 + (size_t)2 * nt * 4; }
 
 // NT threads: 1024 for long rows, 512 (four CTAs an SM) for rows of at most 2048 positions
 template <int NT>
@@ -121,9 +116,8 @@ __global__ void __launch_bounds__(NT, 2048 / NT) k_index_topk(const float *__res
                                                              int cand_block, int K, int offset, int32_t *__restrict__ out,
                                                              int cap_vals) {
   extern __shared__ unsigned long long tk_smem[];
-  unsigned long long *vals = tk_smem;                 // [cap_vals] the valid values
-  unsigned long long *chosen = vals + cap_vals;       // [kTopkMaxK] the selection
-  unsigned long long *swap = chosen + kTopkMaxK;      // [NT] sort buffer
+  unsigned long long *vals = tk_smem;                      // [cap_vals] valid values, ascending position
+  int *klist = reinterpret_cast<int *>(vals + cap_vals);   // [2 NT] kept blocks
   __shared__ TopkShared sh;
   const int64_t row = blockIdx.x;
   const int t = (int)(row % T);
@@ -132,42 +126,26 @@ __global__ void __launch_bounds__(NT, 2048 / NT) k_index_topk(const float *__res
   const uint8_t *cr = cand ? cand + row * cand_width : nullptr;
   const float *Sr = S + row * Lstride;
   const int tid = threadIdx.x;
-  auto value_at = [&](int j) {
-    return ((unsigned long long)order_key(Sr[j]) << 32) | (unsigned long long)(~(uint32_t)j);
-  };
 
-  // pass 1: count the valid positions, compacting their values while they fit
-  __shared__ int s_wsum[NT / 32];
-  __shared__ int s_nkept;
-  if (tid == 0) {
-    topk_shared_init(sh, K);
-    s_nkept = 0;
-  }
+  if (tid == 0) topk_shared_init(sh, K);
   __syncthreads();
   const int nblk = cr ? min((limit + cand_block - 1) / cand_block, cand_width) : 0;
-  if (cr && nblk <= 2 * NT) {
-    // with a mask: the kept blocks listed first (in the sort buffer, idle until the end), then only
-    // their positions visited
-    const int lane = tid & 31, wid = tid >> 5;
-    int *klist = reinterpret_cast<int *>(swap);
+  unsigned nvalid = 0;
+  if (!cr) {
+    // every position below the limit is valid: value j at slot j
+    for (int j = tid; j < min(limit, cap_vals); j += NT) vals[j] = topk_value(Sr[j], j);
+    nvalid = (unsigned)max(limit, 0);
+  } else if (nblk <= 2 * NT) {
+    // the kept blocks in order, then only their positions
+    unsigned nk = 0;
     for (int b0 = 0; b0 < nblk; b0 += NT) {
       const int blk = b0 + tid;
       const bool keep = blk < nblk && cr[blk] != 0;
-      const unsigned bal = __ballot_sync(0xffffffffu, keep);
-      if (lane == 0) s_wsum[wid] = __popc(bal);
-      __syncthreads();
-      int base = s_nkept;
-      for (int w = 0; w < wid; ++w) base += s_wsum[w];
-      if (keep) klist[base + __popc(bal & ((1u << lane) - 1u))] = blk;
-      __syncthreads();
-      if (tid == 0) {
-        int tot = 0;
-        for (int w = 0; w < NT / 32; ++w) tot += s_wsum[w];
-        s_nkept += tot;
-      }
-      __syncthreads();
+      const unsigned slot = ordered_slot(sh, keep, nk);
+      if (keep) klist[slot] = blk;
     }
-    const int npos = s_nkept * cand_block;
+    __syncthreads();
+    const int npos = (int)nk * cand_block;
     for (int i0 = 0; i0 < npos; i0 += NT) {
       const int i = i0 + tid;
       int j = 0;
@@ -176,24 +154,31 @@ __global__ void __launch_bounds__(NT, 2048 / NT) k_index_topk(const float *__res
         j = klist[i / cand_block] * cand_block + i % cand_block;
         v = j < limit;
       }
-      topk_append(v, v ? value_at(j) : 0ull, &sh.count, vals, (unsigned)cap_vals);
+      const unsigned slot = ordered_slot(sh, v, nvalid);
+      if (v && slot < (unsigned)cap_vals) vals[slot] = topk_value(Sr[j], j);
     }
   } else {
     for (int j0 = 0; j0 < limit; j0 += NT) {
       const int j = j0 + tid;
       const bool v = j < limit && comp_valid(j, limit, cr, cand_block);
-      topk_append(v, v ? value_at(j) : 0ull, &sh.count, vals, (unsigned)cap_vals);
+      const unsigned slot = ordered_slot(sh, v, nvalid);
+      if (v && slot < (unsigned)cap_vals) vals[slot] = topk_value(Sr[j], j);
     }
   }
   __syncthreads();
-  const unsigned nvalid = sh.count;
-  const bool in_smem = nvalid <= (unsigned)cap_vals;
-  auto value_at_i = [&](int i, bool &ok) -> unsigned long long {  // (the positions, in global memory)
-    ok = comp_valid(i, limit, cr, cand_block);
-    return ok ? value_at(i) : 0ull;
-  };
-  topk_finish<NT>(sh, nvalid, in_smem, in_smem ? (int)nvalid : limit, value_at_i, K, offset, vals, chosen, swap,
-                  out + row * K);
+  if (nvalid <= (unsigned)cap_vals) {
+    auto from_smem = [&](int i, bool &ok) -> unsigned long long {
+      ok = true;
+      return vals[i];
+    };
+    topk_select(sh, nvalid, (int)nvalid, from_smem, K, offset, out + row * K);
+  } else {
+    auto from_global = [&](int i, bool &ok) -> unsigned long long {  // position i, read from S
+      ok = comp_valid(i, limit, cr, cand_block);
+      return ok ? topk_value(Sr[i], i) : 0ull;
+    };
+    topk_select(sh, nvalid, limit, from_global, K, offset, out + row * K);
+  }
 }
 
 cudaError_t launch_index_topk(const float *S, int B, int T, int start_pos, int Lstride, int compress_len, int ratio,
@@ -208,12 +193,11 @@ cudaError_t launch_index_topk(const float *S, int B, int T, int start_pos, int L
     if (e != cudaSuccess) return e;
   }
   // room for the largest causal limit of the launch (the last query's), so that short ones keep
-  // two CTAs per SM; the sort buffers need at least as many values as the sort's padded length
-  const int max_limit = std::min((start_pos + T) / std::max(ratio, 1), compress_len);
-  const int cap = std::min(kTopkCap, std::max(max_limit, kTopkMaxK));
-  // short rows (every query's limit within 2048, K within the 512-thread sort): 512 threads, four
-  // CTAs an SM, cheaper block barriers
-  if (max_limit <= 2048 && K <= 512)
+  // several CTAs per SM
+  const int max_limit = std::max(0, std::min((start_pos + T) / std::max(ratio, 1), compress_len));
+  const int cap = std::max(32, std::min(kTopkCap, max_limit));
+  // short rows (every query's limit within 2048): 512 threads, four CTAs an SM, cheaper barriers
+  if (max_limit <= 2048)
     k_index_topk<512><<<B * T, 512, topk_smem(cap, 512), s>>>(S, T, start_pos, Lstride, compress_len, ratio, cand,
                                                               cand_width, cand_block, K, offset, out, cap);
   else

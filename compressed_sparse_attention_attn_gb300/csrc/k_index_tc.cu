@@ -346,10 +346,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1) k_index_topk_fused_tc(const 
   const uint32_t q_blk = (uint32_t)N * 128;
   uint8_t *sk = smem, *sq = smem + kFusedTiles * 2 * k_blk;
   float *w_s = reinterpret_cast<float *>(sq + 2 * q_blk);                        // [Hi]
-  unsigned long long *vals = reinterpret_cast<unsigned long long *>(w_s + kMaxN);  // [512]
-  unsigned long long *chosen = vals + kFusedTiles * TILE;                        // [kTopkMaxK]
-  unsigned long long *swap = chosen + kTopkMaxK;                                 // [512]
-  uint64_t *bars = reinterpret_cast<uint64_t *>(swap + kFusedThreads);
+  unsigned long long *vals = reinterpret_cast<unsigned long long *>(w_s + kMaxN);  // [512] by position
+  uint64_t *bars = reinterpret_cast<uint64_t *>(vals + kFusedTiles * TILE);
   uint64_t *full = bars, *done = bars + 1;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
@@ -405,7 +403,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1) k_index_topk_fused_tc(const 
       }
     }
   }
-  // scores of the valid keys, appended as 64-bit values (warps 0-3: TMEM lane = key within a tile)
+  // scores of the valid keys as 64-bit values at their positions, 0 for an invalid one (warps 0-3:
+  // TMEM lane = key within a tile)
   const bool got = ntiles == 0 || tc::mbar_wait(done, 0, abort_flag);
   tc::tc_fence_after();
   if (warp < 4) {
@@ -421,19 +420,22 @@ __global__ void __launch_bounds__(kFusedThreads, 1) k_index_topk_fused_tc(const 
         for (int k = 0; k < 16; ++k) acc = fmaf(w_s[h0 + k], fmaxf(__uint_as_float(v[k]), 0.f), acc);
       }
       const bool ok = got && j < limit && (cr == nullptr || cr[j / P.cand_block] != 0);
-      topk_append(ok, ((unsigned long long)order_key(acc) << 32) | (unsigned long long)(~(uint32_t)j), &sh.count,
-                  vals, (unsigned)(kFusedTiles * TILE));
+      vals[j] = ok ? topk_value(acc, j) : 0ull;
+      const unsigned bal = __ballot_sync(0xffffffffu, ok);
+      if ((tid & 31) == 0 && bal) atomicAdd(&sh.count, (unsigned)__popc(bal));
     }
   }
   tc::tc_fence_before();
   __syncthreads();
-  auto none = [](int, bool &ok) -> unsigned long long {
-    ok = false;
-    return 0ull;
+  if (tid == 0 && *abort_flag) sh.count = 0;  // a wait gave up: no score is trusted, nothing selected
+  __syncthreads();
+  auto at = [&](int i, bool &ok) -> unsigned long long {
+    const unsigned long long v = vals[i];
+    ok = v != 0ull;
+    return v;
   };
   const unsigned nvalid = sh.count;
-  topk_finish<kFusedThreads>(sh, nvalid, true, (int)nvalid, none, P.K, P.offset, vals, chosen, swap,
-                             P.out + (int64_t)b * P.K);
+  topk_select(sh, nvalid, nvalid ? ntiles * TILE : 0, at, P.K, P.offset, P.out + (int64_t)b * P.K);
   tc::tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -539,7 +541,7 @@ cudaError_t launch_index_scores_tc(const bf16 *qI, const float *wI, const bf16 *
 
 bool index_fused_supported(const bf16 *qI, const bf16 *KI, int T, int start_pos, int Hi, int dI, int compress_len,
                            int ratio, int K) {
-  if (T != 1 || ratio <= 0 || K > idx::kFusedThreads || !index_scores_tc_supported(qI, KI, Hi, dI)) return false;
+  if (T != 1 || ratio <= 0 || K > kTopkMaxK || !index_scores_tc_supported(qI, KI, Hi, dI)) return false;
   if (Hi * idx::kFusedTiles > 512) return false;
   return std::min((start_pos + 1) / ratio, compress_len) <= idx::kFusedTiles * idx::TILE;
 }
@@ -567,12 +569,12 @@ cudaError_t launch_index_topk_fused(const bf16 *qI, const float *wI, const bf16 
   p.out = out;
   p.status = status;
   const size_t smem = 1024 + (size_t)kFusedTiles * 2 * TILE * 128 + 2 * (size_t)Hi * 128 + kMaxN * 4 +
-                      (size_t)(kFusedTiles * TILE + kTopkMaxK + kFusedThreads) * 8 + 2 * 8 + 16;
+                      (size_t)kFusedTiles * TILE * 8 + 2 * 8 + 16;
   static SmemAttr attr;
   {
     cudaError_t e = attr.ensure((const void *)k_index_topk_fused_tc,
                                 (int)(1024 + kFusedTiles * 2 * TILE * 128 + 2 * kMaxN * 128 + kMaxN * 4 +
-                                      (kFusedTiles * TILE + kTopkMaxK + kFusedThreads) * 8 + 2 * 8 + 16));
+                                      kFusedTiles * TILE * 8 + 2 * 8 + 16));
     if (e != cudaSuccess) return e;
   }
   k_index_topk_fused_tc<<<B, kFusedThreads, smem, s>>>(p);

@@ -87,11 +87,18 @@ typedef struct csa_role {
  * wq_a [q_rank, dim], wq_b [n_heads*head_dim, q_rank], wkv [head_dim, dim],
  * wo_a [groups*o_rank, gw], wo_b [dim, groups*o_rank], idx_wq_b [index_heads*index_hd, q_rank],
  * idx_wproj [index_heads, dim].  sink [n_heads], q_norm [q_rank], kv_norm [head_dim] are f32.
- * idx_* may be NULL unless role.is_index_source. */
+ * idx_* may be NULL unless role.is_index_source.
+ * The grouped wo_a may instead stay in fp8 ([atlas] Attention excerpt: the checkpoint's converter
+ * dequantises it to bf16, and an fp8 grouped product would halve its memory): wo_a_fp8 uint8
+ * [groups*o_rank, gw] holds e4m3 codes and wo_a_scale f32 [groups*o_rank/128 rounded up][gw/128
+ * rounded up] one scale per 128 x 128 tile; the layer then computes with w = bf16(e4m3 * scale), the
+ * converter's bf16 weight, and wo_a may be NULL.  Both NULL: wo_a (bf16) is used. */
 typedef struct csa_layer_weights {
   csa_role role;
   const float *sink, *q_norm, *kv_norm;
   const csa_bf16 *wq_a, *wq_b, *wkv, *wo_a, *wo_b, *idx_wq_b, *idx_wproj;
+  const uint8_t *wo_a_fp8;
+  const float *wo_a_scale;
 } csa_layer_weights;
 
 /* One layer's per-sequence state ([attn_v41] AttnV41LayerState): the window ring bf16
@@ -178,16 +185,30 @@ CSA_API int csa_rope_table_get(const csa_ctx *ctx, int ratio_class, float *tab_h
 
 /* Synchronise the device and return the context's device status word as an error code:
  * CSA_OK, CSA_ERR_ARG (a kernel met an out-of-range index and skipped it) or CSA_ERR_DEVICE_TIMEOUT
- * (a bounded device-side wait ran out).  clear != 0 resets the word afterwards. */
+ * (a bounded device-side wait ran out; the outputs since the last clear are invalid).  The word is
+ * sticky: every kernel ORs its findings in until a call with clear != 0 resets it (after a timeout
+ * that also re-zeroes the projections' Stream-K arrival counters, so the next call starts clean). */
 CSA_API int csa_status(csa_ctx *ctx, int clear);
+
+/* Test hook of failure detection, for checking how a device-side timeout is reported without any
+ * fault: while ns != 0, every projection kernel launched on the current device (csa_linear,
+ * csa_linear_noalloc, the layer's projections; every context) first waits on a barrier phase that
+ * nothing completes, and gives up after ns nanoseconds (each wait of the kernels is bounded: 2 s by
+ * default).  The kernel then takes its timeout path -- it lets the copies it has in flight land,
+ * frees its tensor memory, returns, and sets CSA_ERR_DEVICE_TIMEOUT in the status word (csa_status,
+ * csa_linear_noalloc_status); its output is invalid.  ns = 0 turns the hook off.  Synchronous. */
+CSA_API int csa_debug_stall(unsigned long long ns);
 
 /* Bytes of device workspace the context holds. */
 CSA_API size_t csa_workspace_bytes(const csa_ctx *ctx);
 
 /* Tracing.  While enabled, attn_v41_forward records a CUDA event pair on its stream around each of
- * its stages (at most 32); csa_trace_read waits for the last forward's events and writes, for the
- * first `max` stages, a static stage name and the elapsed milliseconds.  Returns the number of
- * stages of the last forward (>= 0) or an error code. */
+ * its stages (at most 64 in all); on a stream being captured into a CUDA graph the pairs become
+ * event-record nodes, so each replay of the graph re-times its stages.  enable 1: each forward
+ * replaces the list with its own stages; enable 2: forwards append theirs to the list, which
+ * restarts empty at this call (one list for several layers, or for a captured step); 0: off.
+ * csa_trace_read waits for the listed events and writes, for the first `max` stages, a static stage
+ * name and the elapsed milliseconds.  Returns the number of listed stages (>= 0) or an error code. */
 CSA_API int csa_trace_enable(csa_ctx *ctx, int enable);
 CSA_API int csa_trace_read(csa_ctx *ctx, int max, const char **names, float *ms);
 
@@ -205,6 +226,16 @@ CSA_API int csa_last_launches(const csa_ctx *ctx);
  * y columns [g*N, (g+1)*N).  ctx provides the split-K workspace. */
 CSA_API int csa_linear(csa_ctx *ctx, const csa_bf16 *x, int M, int K, int ldx, const csa_bf16 *W, int N, int ldw, csa_bf16 *y,
                int ldy, int groups, csa_stream stream);
+
+/* linear_bf16 with fp8 weights ([atlas] Attention excerpt: the grouped wo_a is dequantised to bf16
+ * by the checkpoint's converter; an fp8 grouped product halves its memory): y[m][n] = bf16(sum_k
+ * x[m][k] w[n][k]) with w[n][k] = bf16(e4m3(W8[n][k]) * scale[n/128][k/128]), f32 accumulation --
+ * the result of csa_linear on the dequantised bf16 weights, reading half the weight bytes.
+ * W8 uint8 [groups*N][ldw8 bytes] e4m3 codes (16-byte aligned, ldw8 a multiple of 16, K a multiple
+ * of 16, of 64 when groups > 1); scale f32 [ceil(groups*N/128)][ceil(K/128)]; x, y and groups as
+ * in csa_linear (product g reads x columns [g*K, (g+1)*K) and W8 rows [g*N, (g+1)*N)). */
+CSA_API int csa_linear_fp8w(csa_ctx *ctx, const csa_bf16 *x, int M, int K, int ldx, const uint8_t *W8,
+                            const float *scale, int N, int ldw8, csa_bf16 *y, int ldy, int groups, csa_stream stream);
 
 /* RMSNorm ([ref-attn] "Precision"): y = bf16(x / sqrt(mean(x^2) + eps) * w) per row; x, y [M][N]
  * (may alias), w f32 [N]. */
@@ -278,12 +309,22 @@ CSA_API int csa_sparse_attn(csa_ctx *ctx, const csa_bf16 *q, int B, int T, int H
  * multiples of 8, K a multiple of 8 (of 64 when groups > 1).  Beyond them it returns CSA_ERR_SHAPE or
  * CSA_ERR_ARG and launches nothing.
  * The first call on a device looks the array's device address up (cudaGetSymbolAddress, once per
- * device, with that device current); make that first call before any stream capture.
+ * device and CUDA context, with that device current); make that first call before any stream
+ * capture.  After a device reset the next call looks the address up again.
  * Every call shares the one array and it keeps the last call's contents: each call clears the
  * counters it needs on `stream` before its launch, but calls whose work overlaps on the GPU (on
- * different streams or from different threads) race on the array and must not be issued. */
+ * different streams or from different threads) race on the array and must not be issued.
+ * A bounded device-side wait that runs out is not reported by the return code (the call returns
+ * once the work is enqueued): it sets the array's status word, which csa_linear_noalloc_status
+ * reads. */
 CSA_API int csa_linear_noalloc(const csa_bf16 *x, int M, int K, int ldx, const csa_bf16 *W, int N, int ldw,
                                csa_bf16 *y, int ldy, int groups, csa_stream stream);
+
+/* The status word of csa_linear_noalloc on the current device: synchronises the device, then returns
+ * CSA_OK, or CSA_ERR_DEVICE_TIMEOUT when a bounded wait of some call since the last clear ran out (the
+ * outputs of those calls are invalid).  The word is sticky; clear != 0 resets it.  Allocates
+ * nothing.  CSA_OK when no call has run on this device. */
+CSA_API int csa_linear_noalloc_status(int clear);
 
 #ifdef __cplusplus
 }

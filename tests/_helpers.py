@@ -37,3 +37,18 @@ def assert_close_bf16(got_u16, want_u16, atol=2e-2, rtol=2e-2, rel_norm=1e-2, wh
     if n > 0:
         r = np.linalg.norm(g - w) / n
         assert r <= rel_norm, "%s: relative error norm %g > %g" % (what, r, rel_norm)
+
+
+def assert_same_selection(got, want, what="selection"):
+    """Top-k selections, bit for bit as sets: each row of `got` holds exactly the non-negative entries
+    of the same row of `want` (the oracle lists them by score), written in ascending position and
+    followed by -1 padding (the library's order: the pages leave the order open)."""
+    got = np.asarray(got)
+    want = np.asarray(want)
+    assert got.shape == want.shape, (got.shape, want.shape)
+    for r in range(got.shape[0]):
+        g, w = got[r], want[r]
+        n = int((w >= 0).sum())
+        assert (g[n:] == -1).all() and (g[:n] >= 0).all(), "%s row %d: %d selected, padding %s" % (what, r, n, g[n:][:8])
+        assert (np.diff(g[:n]) > 0).all(), "%s row %d: not in ascending position" % (what, r)
+        assert np.array_equal(g[:n], np.sort(w[w >= 0])), "%s row %d: the selected sets differ" % (what, r)

@@ -12,7 +12,7 @@ import pytest
 import torch
 
 from csa_inputs import WORKLOADS, Geometry, candidate_mask, latent_cache, positions, weights
-from _helpers import assert_close_bf16, bf, to_dev, to_np
+from _helpers import assert_close_bf16, assert_same_selection, bf, to_dev, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -170,6 +170,30 @@ def test_linear_waves(csa, orc, M, K, N, groups):
     assert_close_bf16(got[rows], want, what="linear (waves)")
 
 
+@pytest.mark.parametrize("M,K,N,groups", [(32, 4096, 1024, 8), (1, 4096, 1024, 8), (7, 256, 200, 1),
+                                           (33, 1280, 384, 1), (20, 5120, 1280, 1), (6200, 1024, 128, 8)])
+def test_linear_fp8w(csa, orc, M, K, N, groups):
+    """Projection with e4m3 weights and one f32 scale per 128 x 128 tile (the fp8 grouped wo_a): the
+    oracle's linear_bf16 on the oracle's dequantised weights, within the linear tolerance, and bit for
+    bit the bf16 product on those weights (the kernel expands each tile to exactly them, and the
+    launch splits the work as the bf16 one does).  Ragged N and token tiles; the last case is a
+    prefill-sized grouped launch (whole-tile waves), checked on sampled rows."""
+    from csa_inputs import fp8_weight
+    rng = np.random.default_rng(60 + M + N)
+    x = _rng_bf16(orc, rng, (M, K * groups))
+    codes, scales = fp8_weight((N * groups, K), 4000 + N)
+    W = orc.dequant_fp8_blocks(codes, scales)
+    ctx, _ = _ctx(csa, dim=64, max_tokens=1, max_batch=1, max_seq=16)
+    xd = to_dev(x)
+    got = to_np(ctx.linear_fp8w(xd, to_dev(codes), to_dev(scales), groups=groups))
+    ref = to_np(ctx.linear(xd, to_dev(W), groups=groups))
+    assert np.array_equal(got, ref), "fp8-weight product differs from the bf16 product on the dequantised weights"
+    rows = np.arange(M) if M < 512 else np.array(sorted(set([0, 1, 255, 256, M - 1] + list(rng.integers(0, M, 12)))))
+    want = np.concatenate([orc.linear_bf16(x[rows, g * K:(g + 1) * K], W[g * N:(g + 1) * N]) for g in range(groups)], 1)
+    assert_close_bf16(got[rows], want, what="linear_fp8w")
+    assert ctx.status() == 0
+
+
 def test_rmsnorm(csa, orc):
     rng = np.random.default_rng(5)
     x = _rng_bf16(orc, rng, (40, 1280), 3.0)
@@ -304,7 +328,7 @@ def test_index_topk_bit_exact(csa, orc, B, T, start, L, clen, ratio, keep, cb, K
     out = torch.full((B * T, K), -5, dtype=torch.int32, device="cuda")
     csa.index_topk(to_dev(S), B, T, start, clen, ratio, K, out, offset=128,
                    cand=None if cand is None else to_dev(cand), cand_block=cb)
-    assert np.array_equal(to_np(out), want)
+    assert_same_selection(to_np(out), want)
 
 
 # ---------------------------------------------------------------------------------- attention

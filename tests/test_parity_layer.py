@@ -15,7 +15,7 @@ import torch
 
 from csa_inputs import (WORKLOADS, Geometry, activations, candidate_mask, latent_cache, positions, ring_rows,
                         weights)
-from _helpers import assert_close_bf16, bf, to_dev, to_np
+from _helpers import assert_close_bf16, assert_same_selection, bf, to_dev, to_np
 
 pytestmark = pytest.mark.gpu
 
@@ -220,7 +220,7 @@ def test_fused_indexer_topk_selection(csa, orc, cand):
     S = to_np(dbg["scores"])[:, :L].astype(np.float32)
     S = np.where(np.isnan(S), -np.inf, S).astype(np.float32)
     want = orc.index_topk(S, K, pos, 2, clen, cm, g.cand_block, offset=g.window)
-    assert np.array_equal(to_np(sel_fast), want)
+    assert_same_selection(to_np(sel_fast), want)
     n_valid = np.isfinite(S).sum(1)
     assert (n_valid > K).all()  # the cut is real on every row
 
@@ -390,3 +390,43 @@ def test_full_width_sampled(csa, orc, name, seqs, toks):
                 if v.any():
                     tol = 1e-2 * np.abs(S_o[r, v]).max()
                     _check_selection(gi[i, g.window:], S_o[r], K, g.window if start else T, 2 * tol)
+
+
+def test_fp8_wo_a_layer(csa, orc):
+    """The Reindex decode layer (full width, 32 sequences at p = 1000) with the grouped wo_a kept in fp8
+    (e4m3 codes and one scale per 128 x 128 tile): its output equals, bit for bit, the layer with the
+    dequantised bf16 wo_a, and the oracle on those weights on sampled sequences.  The fp8 storage is the
+    workload's bf16 wo_a encoded with the oracle's e4m3 rounding at scale amax / 448 per tile, so the
+    layer keeps its usual magnitudes."""
+    wl, g, w, x, tab, ring0, shared = _full_case(orc, "reindex_decode_r2", [0, 31])
+    gd = g.as_dict()
+    B, T, start, K = wl.batch, wl.tokens, wl.start_pos, g.index_topk
+    gw = g.n_heads * g.head_dim // g.groups
+    wf = bf(w["wo_a"]).reshape(g.groups * g.o_rank // 128, 128, gw // 128, 128)
+    scales = (np.abs(wf).max(axis=(1, 3)) / 448.0).astype(np.float32)
+    codes = orc.e4m3_encode((wf / scales[:, None, :, None]).astype(np.float32)).reshape(g.groups * g.o_rank, gw)
+    w = dict(w)
+    w["wo_a"] = orc.dequant_fp8_blocks(codes, scales)
+    role = dict(ratio=wl.ratio, is_index_source=1, uses_candidates=1)
+    ctx = csa.Context(gd)
+    outs = []
+    for fp8 in (True, False):
+        wd = _dev_weights(w)
+        if fp8:
+            wd["wo_a"] = None
+            wd["wo_a_fp8"] = to_dev(codes)
+            wd["wo_a_scale"] = to_dev(scales)
+        sel_d = torch.full((B * T, K), -7, dtype=torch.int32, device="cuda")
+        sh = csa.Shared(to_dev(shared["compress_kv"]), to_dev(shared["index_k"]), shared["compress_len"], sel_d, K,
+                        to_dev(shared["candidates"]))
+        outs.append(ctx.forward(wd, role, to_dev(ring0), to_dev(x), start, shared=sh))
+    torch.cuda.synchronize()
+    assert ctx.status() == 0
+    assert torch.equal(outs[0], outs[1]), "fp8 wo_a changes the layer output"
+    got = to_np(outs[0]).reshape(-1, g.dim)
+    for b in (0, 31):
+        sh_o = dict(compress_kv=shared["compress_kv"][b:b + 1], index_k=shared["index_k"][b:b + 1],
+                    compress_len=shared["compress_len"], topk_idxs=np.full((T, K), -7, np.int32),
+                    candidates=shared["candidates"][b * T:(b + 1) * T])
+        res = orc.attn_forward(gd, role, w, ring0[b:b + 1].copy(), x[b:b + 1], start, tab, sh_o)
+        assert_close_bf16(got[b * T:(b + 1) * T], res["out"].reshape(-1, g.dim), what="fp8 wo_a layer out")
