@@ -98,17 +98,39 @@ class Shared:
                               0 if self.candidates is None else self.candidates.shape[-1])
         return self._c
 
-    def sync_back(self):
+    def sync_back(self, kv_state=None, with_keys=False):
+        """What the library published into the struct: the selection flag and, after a kv source (its
+        kv_state), its caches and their length."""
         if self._c is not None:
             self.has_topk = bool(self._c.has_topk)
+            self.compress_len = int(self._c.compress_len)
+        if kv_state is not None:
+            self.compress_kv = kv_state["latent"]
+            if with_keys:
+                self.index_k = kv_state["index_keys"]
 
 
 DEBUG_FIELDS = ("q", "kv", "kv_codes", "kv_scale", "idx", "scores", "o", "og", "qr", "qI", "wI")
 DEBUG_DTYPES = (torch.bfloat16, torch.bfloat16, torch.uint8, torch.int8, torch.int32, torch.float32, torch.bfloat16, torch.bfloat16, torch.bfloat16, torch.bfloat16, torch.float32)
 WEIGHT_FIELDS = ("sink", "q_norm", "kv_norm", "wq_a", "wq_b", "wkv", "wo_a", "wo_b", "idx_wq_b", "idx_wproj",
-                 "wo_a_fp8", "wo_a_scale")
+                 "wo_a_fp8", "wo_a_scale", "comp_wkv", "comp_wgate", "comp_norm", "idx_wk", "idx_k_norm")
+# (comp_wkv is f32 at ratio > 1 and bf16 at ratio 1: its dtype is checked against the role)
 WEIGHT_DTYPES = (torch.float32, torch.float32, torch.float32, torch.bfloat16, torch.bfloat16, torch.bfloat16, torch.bfloat16,
-                 torch.bfloat16, torch.bfloat16, torch.bfloat16, torch.uint8, torch.float32)
+                 torch.bfloat16, torch.bfloat16, torch.bfloat16, torch.uint8, torch.float32, None, torch.float32,
+                 torch.float32, torch.bfloat16, torch.float32)
+
+
+def make_state(ring, kv_state=None):
+    """csa_layer_state: the window ring, and for a kv source the dict kv_state with comp_kv,
+    comp_score (f32 [max_batch, ratio, hd]), latent (bf16 [max_batch, rows, hd]) and index_keys (bf16
+    [max_batch, rows, index_hd], may be None)."""
+    if kv_state is None:
+        return _abi.LayerState(_dev(ring, torch.bfloat16, "ring"))
+    kv, sc, lat = kv_state["comp_kv"], kv_state["comp_score"], kv_state["latent"]
+    ik = kv_state.get("index_keys")
+    return _abi.LayerState(_dev(ring, torch.bfloat16, "ring"), _dev(kv, torch.float32, "comp_kv"),
+                           _dev(sc, torch.float32, "comp_score"), kv.shape[1], _dev(lat, torch.bfloat16, "latent"),
+                           _dev(ik, torch.bfloat16, "index_keys"), lat.shape[1])
 
 
 class Context:
@@ -135,13 +157,30 @@ class Context:
     # -- layer ---------------------------------------------------------------------------------
     @staticmethod
     def layer_weights(w, role):
+        wkv = w.get("comp_wkv")
+        if wkv is not None:
+            want = torch.float32 if int(role.get("ratio", 0)) > 1 else torch.bfloat16
+            _dev(wkv, want, "comp_wkv")
         return _abi.LayerWeights(make_role(role), *[_dev(w.get(n), dt, n) for n, dt in zip(WEIGHT_FIELDS, WEIGHT_DTYPES)])
 
-    def state_init(self, ring, batch, stream=None):
-        st = _abi.LayerState(_dev(ring, torch.bfloat16, "ring"))
+    def state_init(self, ring, batch, stream=None, kv_state=None):
+        st = make_state(ring, kv_state)
         _check(lib().csa_state_init(self.h, ctypes.byref(st), batch, _stream(stream)), "csa_state_init")
 
-    def forward(self, w, role, ring, x, start_pos, shared=None, out=None, debug=None, stream=None, lw=None):
+    def compress(self, w, role, ring, kv_state, x, start_pos, shared=None, y_dbg=None, stream=None):
+        """csa_compress: the kv source's compressor over x [B, T, dim]; publishes into shared."""
+        B, T, _ = x.shape
+        lw = self.layer_weights(w, role)
+        st = make_state(ring, kv_state)
+        sh = shared.struct() if shared is not None else None
+        _check(lib().csa_compress(self.h, ctypes.byref(lw), ctypes.byref(st), _dev(x, torch.bfloat16, "x"), B, T,
+                                  start_pos, ctypes.byref(sh) if sh is not None else None,
+                                  _dev(y_dbg, torch.bfloat16, "y_dbg"), _stream(stream)), "csa_compress")
+        if shared is not None:
+            shared.sync_back(kv_state, w.get("idx_wk") is not None)
+
+    def forward(self, w, role, ring, x, start_pos, shared=None, out=None, debug=None, stream=None, lw=None,
+                kv_state=None):
         """attn_v41_forward.  x [B, T, dim] bf16 -> out [B, T, dim] bf16; ring [max_batch, W, hd] bf16.
         ``debug``: dict of preallocated device tensors named as in csa_debug.  ``lw``: a prebuilt
         LayerWeights struct (skips re-marshalling)."""
@@ -150,7 +189,7 @@ class Context:
             out = torch.empty_like(x)
         if lw is None:
             lw = self.layer_weights(w, role)
-        st = _abi.LayerState(_dev(ring, torch.bfloat16, "ring"))
+        st = make_state(ring, kv_state)
         sh = shared.struct() if shared is not None else None
         dbg = None
         if debug:
@@ -160,7 +199,7 @@ class Context:
                                     ctypes.byref(dbg) if dbg is not None else None, _stream(stream))
         _check(rc, "attn_v41_forward")
         if shared is not None:
-            shared.sync_back()
+            shared.sync_back(kv_state if int(role.get("is_kv_source", 0)) else None, bool(lw.idx_wk))
         return out
 
     def forward_host(self, lw, ring, x_host, start_pos, shared, out_host, B, T, stream=None):
@@ -281,6 +320,14 @@ def index_scores(qI, wI, KI, B, T, start_pos, compress_len, ratio, S, cand=None,
                                   0 if cand is None else cand.shape[-1], cand_block, _dev(S, torch.float32, "S"), _stream(stream)),
            "csa_index_scores")
     return S
+
+
+def candidate_blocks(S, B, T, start_pos, compress_len, ratio, cand_block, K, mask, stream=None):
+    """csa_candidate_blocks: mask uint8 [B*T, cand_width] from the scores S f32 [B*T, L]."""
+    _check(lib().csa_candidate_blocks(_dev(S, torch.float32, "S"), B, T, start_pos, S.shape[-1], compress_len, ratio,
+                                      cand_block, K, _dev(mask, torch.uint8, "mask"), mask.shape[-1], _stream(stream)),
+           "csa_candidate_blocks")
+    return mask
 
 
 def index_topk(S, B, T, start_pos, compress_len, ratio, K, out, offset=0, cand=None, cand_block=1, stream=None):

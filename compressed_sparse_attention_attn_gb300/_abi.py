@@ -38,11 +38,14 @@ class Role(ctypes.Structure):
 
 class LayerWeights(ctypes.Structure):
     _fields_ = [("role", Role)] + [(n, P) for n in ("sink", "q_norm", "kv_norm", "wq_a", "wq_b", "wkv", "wo_a",
-                                                      "wo_b", "idx_wq_b", "idx_wproj", "wo_a_fp8", "wo_a_scale")]
+                                                      "wo_b", "idx_wq_b", "idx_wproj", "wo_a_fp8", "wo_a_scale",
+                                                      "comp_wkv", "comp_wgate", "comp_norm", "idx_wk",
+                                                      "idx_k_norm")]
 
 
 class LayerState(ctypes.Structure):
-    _fields_ = [("window", P)]
+    _fields_ = [("window", P), ("comp_kv", P), ("comp_score", P), ("comp_ratio", I), ("latent", P),
+                ("index_keys", P), ("cache_rows", I)]
 
 
 class Shared(ctypes.Structure):
@@ -75,12 +78,15 @@ SIGNATURES = {
     "csa_linear_noalloc_status": (I, [I]),
     "csa_debug_stall": (I, [ctypes.c_ulonglong]),
     "csa_linear_fp8w": (I, [P, P, I, I, I, P, P, I, I, P, I, I, P]),
+    "csa_compress": (I, [P, ctypes.POINTER(LayerWeights), ctypes.POINTER(LayerState), P, I, I, I,
+                         ctypes.POINTER(Shared), P, P]),
     "csa_rmsnorm": (I, [P, I, I, P, F, P, P]),
     "csa_rope": (I, [P, I64, I, I, P, I, P, I, I, P]),
     "csa_act_quant": (I, [P, I64, P, P, P]),
     "csa_kv_finish": (I, [P, P, I, I, I, I, I, P, I, P, I, P, I, P, P, P]),
     "csa_index_scores": (I, [P, P, P, I, I, I, I, I, I, I, I, P, I, I, P, P]),
     "csa_index_topk": (I, [P, I, I, I, I, I, I, P, I, I, I, I, P, P]),
+    "csa_candidate_blocks": (I, [P, I, I, I, I, I, I, I, I, P, I, P]),
     "csa_sparse_attn": (I, [P, P, I, I, I, I, P, I64, I, P, I64, I, P, I, P, I, P, F, P, P, I, I, P, I, P]),
 }
 

@@ -1,6 +1,7 @@
 // csa_api.cu -- host side of the C ABI: context and workspaces, argument validation, the RoPE
 // tables, and the layer forward ("DeepSeek V4.1 - Compressed sparse attention", Attention.forward
 // excerpt; "metrale_model_arch::attn_v41" AttnV41 and its "Invariants").
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -58,9 +59,12 @@ struct csa_ctx {
   int xpart_rows = 0;
   int32_t *idx_win = nullptr;
   int *status = nullptr;
-  float *ws = nullptr;  // split-K and split-row partials; the attention's arrival counters at the end
+  float *ws = nullptr;  // Stream-K counters and partials, the attention's split shares, the compressor's partials
   size_t ws_bytes = 0;
-  size_t gemm_ws_bytes() const { return ws_bytes - csa::kAttnCounterBytes; }  // the projections' part
+  size_t gemm_ws_bytes() const { return ws_bytes; }
+  // the compressor's partial products: past the projections' arrival counters, which must stay zero
+  float *comp_ws() const { return ws + csa::kGemmCounterBytes / sizeof(float); }
+  size_t comp_ws_bytes() const { return ws_bytes - csa::kGemmCounterBytes; }
   int scores_stride = 0;
   size_t bytes = 0;
   std::vector<void *> allocs;
@@ -222,8 +226,6 @@ int csa_create(const csa_cfg *cfg, csa_ctx **out) {
 #undef ALLOC
   if (e == cudaSuccess) e = cudaMemset(c->status, 0, 4 * sizeof(int));
   if (e == cudaSuccess) e = cudaMemset(c->ws, 0, csa::kGemmCounterBytes);  // Stream-K arrival counters
-  if (e == cudaSuccess)  // the attention's split arrival counters
-    e = cudaMemset(reinterpret_cast<uint8_t *>(c->ws) + c->ws_bytes - csa::kAttnCounterBytes, 0, csa::kAttnCounterBytes);
   if (e != cudaSuccess) {
     c->release();
     delete c;
@@ -304,13 +306,8 @@ int csa_status(csa_ctx *ctx, int clear) {
   CSA_CUDA(cudaMemcpy(&st, ctx->status, sizeof(int), cudaMemcpyDeviceToHost), "csa_status: read");
   if (clear) {
     CSA_CUDA(cudaMemset(ctx->status, 0, sizeof(int)), "csa_status: clear");
-    // a kernel that gave up may have left arrival counters raised: start them at zero
-    if (st & csa::kStatusTimeout) {
-      CSA_CUDA(cudaMemset(ctx->ws, 0, csa::kGemmCounterBytes), "csa_status: counters");
-      CSA_CUDA(cudaMemset(reinterpret_cast<uint8_t *>(ctx->ws) + ctx->ws_bytes - csa::kAttnCounterBytes, 0,
-                          csa::kAttnCounterBytes),
-               "csa_status: counters");
-    }
+    // a projection that gave up may have left Stream-K arrival counters raised: start them at zero
+    if (st & csa::kStatusTimeout) CSA_CUDA(cudaMemset(ctx->ws, 0, csa::kGemmCounterBytes), "csa_status: counters");
     CSA_CUDA(cudaDeviceSynchronize(), "csa_status: clear");
   }
   if (st & csa::kStatusTimeout) return fail(CSA_ERR_DEVICE_TIMEOUT, "a bounded device-side wait ran out");
@@ -326,10 +323,84 @@ int csa_debug_stall(unsigned long long ns) {
 int csa_state_init(csa_ctx *ctx, csa_layer_state *state, int batch, csa_stream stream) {
   if (!ctx || !state || !state->window) return fail(CSA_ERR_ARG, "csa_state_init: NULL argument");
   if (batch <= 0 || batch > ctx->cfg.max_batch) return fail(CSA_ERR_SHAPE, "csa_state_init: batch %d", batch);
+  if ((state->comp_kv || state->comp_score) && (!state->comp_kv || !state->comp_score || state->comp_ratio <= 0))
+    return fail(CSA_ERR_ARG, "csa_state_init: a compressor state needs comp_kv, comp_score and comp_ratio");
   if (int rc = check_device(ctx, "csa_state_init")) return rc;
-  CSA_CUDA(cudaMemsetAsync(state->window, 0, sizeof(bf16) * (size_t)batch * ctx->cfg.window * ctx->cfg.head_dim,
-                           (cudaStream_t)stream),
+  cudaStream_t s = (cudaStream_t)stream;
+  CSA_CUDA(cudaMemsetAsync(state->window, 0, sizeof(bf16) * (size_t)batch * ctx->cfg.window * ctx->cfg.head_dim, s),
            "csa_state_init");
+  if (state->comp_kv) {
+    const int64_t n = (int64_t)batch * state->comp_ratio * ctx->cfg.head_dim;
+    CSA_CUDA(cudaMemsetAsync(state->comp_kv, 0, sizeof(float) * (size_t)n, s), "csa_state_init");
+    CSA_CUDA(csa::launch_fill_f32(state->comp_score, n, -INFINITY, s), "csa_state_init");
+  }
+  return CSA_OK;
+}
+
+// The compressor's arguments of a kv-source layer (validated); CSA_OK or an error code.
+static int compress_args(const csa_ctx *ctx, const csa_layer_weights *w, const csa_layer_state *st, const void *x,
+                         int B, int T, int start_pos, csa_bf16 *y_dbg, csa::CompressArgs *a, const char *who) {
+  const csa_cfg &g = ctx->cfg;
+  const int ratio = w->role.ratio;
+  if (ratio < 1 || ratio > 16) return fail(CSA_ERR_ARG, "%s: a kv source needs a ratio in 1..16", who);
+  if (!w->comp_wkv || !w->comp_norm || (ratio > 1 && !w->comp_wgate))
+    return fail(CSA_ERR_ARG, "%s: compressor weights missing", who);
+  if (w->idx_wk && (!w->idx_k_norm || g.index_hd <= 0 || g.index_hd > 256))
+    return fail(CSA_ERR_ARG, "%s: index-key weights need idx_k_norm and index_hd in 1..256", who);
+  if (!st->comp_kv || !st->comp_score || st->comp_ratio != ratio || !st->latent || (w->idx_wk && !st->index_keys))
+    return fail(CSA_ERR_ARG, "%s: the state lacks the compressor's partial group or caches for ratio %d", who, ratio);
+  if (B <= 0 || B > g.max_batch || T <= 0 || T > g.max_tokens || start_pos < 0 || (int64_t)start_pos + T > g.max_seq)
+    return fail(CSA_ERR_SHAPE, "%s: batch %d, T %d at %d", who, B, T, start_pos);
+  if (start_pos > 0 && T != 1) return fail(CSA_ERR_SHAPE, "%s: decode takes one token per sequence", who);
+  if ((start_pos + T) / ratio > st->cache_rows)
+    return fail(CSA_ERR_SHAPE, "%s: cache_rows %d below the groups written", who, st->cache_rows);
+  a->x = (const bf16 *)x;
+  a->B = B;
+  a->T = T;
+  a->start_pos = start_pos;
+  a->ratio = ratio;
+  a->dim = g.dim;
+  a->hd = g.head_dim;
+  a->rd = g.rope_dim;
+  a->dI = g.index_hd;
+  a->wkv = w->comp_wkv;
+  a->wgate = w->comp_wgate;
+  a->norm = w->comp_norm;
+  a->wk = (const bf16 *)w->idx_wk;
+  a->k_norm = w->idx_k_norm;
+  a->st_kv = st->comp_kv;
+  a->st_score = st->comp_score;
+  a->Z = (bf16 *)st->latent;
+  a->KI = (bf16 *)st->index_keys;
+  a->y_dbg = (bf16 *)y_dbg;
+  a->Lstride = st->cache_rows;
+  a->tab = ctx->tab_comp;
+  a->eps = g.eps;
+  if (!csa::compress_supported(*a))
+    return fail(CSA_ERR_ARG, "%s: head_dim a multiple of 64 (<= 1024), dim of 8, x 16-byte aligned", who);
+  return CSA_OK;
+}
+
+// A kv source's caches as the shared slots later layers read ([attn_v41] SharedV41: compress_len
+// only grows).
+static void publish_caches(const csa_layer_weights *w, const csa_layer_state *st, int T, int start_pos,
+                           csa_shared *sh) {
+  if (!sh) return;
+  sh->compress_kv = st->latent;
+  if (w->idx_wk) sh->index_k = st->index_keys;
+  sh->compress_stride = st->cache_rows;
+  sh->compress_len = std::max(sh->compress_len, (start_pos + T) / w->role.ratio);
+}
+
+int csa_compress(csa_ctx *ctx, const csa_layer_weights *w, csa_layer_state *st, const csa_bf16 *x, int B, int T,
+                 int start_pos, csa_shared *sh, csa_bf16 *y_dbg, csa_stream stream) {
+  if (!ctx || !w || !st || !x) return fail(CSA_ERR_ARG, "csa_compress: NULL argument");
+  if (int rc = check_device(ctx, "csa_compress")) return rc;
+  csa::CompressArgs a;
+  if (int rc = compress_args(ctx, w, st, x, B, T, start_pos, y_dbg, &a, "csa_compress")) return rc;
+  CSA_CUDA(csa::launch_compress(a, ctx->comp_ws(), ctx->comp_ws_bytes(), ctx->num_sms, (cudaStream_t)stream),
+           "csa_compress");
+  publish_caches(w, st, T, start_pos, sh);
   return CSA_OK;
 }
 
@@ -421,6 +492,19 @@ int csa_index_scores(const csa_bf16 *qI, const float *wI, const csa_bf16 *KI, in
   return CSA_OK;
 }
 
+int csa_candidate_blocks(const float *S, int B, int T, int start_pos, int Lstride, int compress_len, int ratio,
+                         int cand_block, int K, uint8_t *mask, int cand_width, csa_stream stream) {
+  if (!S || !mask || B <= 0 || T <= 0 || start_pos < 0 || ratio <= 0 || Lstride <= 0 || compress_len < 0 ||
+      compress_len > Lstride || cand_block <= 0 || K <= 0 || K > 2048 || cand_width <= 0 || cand_width > 25600)
+    return fail(CSA_ERR_ARG, "csa_candidate_blocks: bad argument");
+  if ((int64_t)cand_width * cand_block < compress_len)
+    return fail(CSA_ERR_ARG, "csa_candidate_blocks: the mask is narrower than the cache");
+  CSA_CUDA(csa::launch_cand_blocks(S, B, T, start_pos, Lstride, compress_len, ratio, cand_block, K, mask, cand_width,
+                                   (cudaStream_t)stream),
+           "csa_candidate_blocks");
+  return CSA_OK;
+}
+
 int csa_index_topk(const float *S, int B, int T, int start_pos, int Lstride, int compress_len, int ratio,
                    const uint8_t *cand, int cand_width, int cand_block, int K, int offset, int32_t *out,
                    csa_stream stream) {
@@ -488,13 +572,29 @@ static int check_forward(const csa_ctx *ctx, const csa_layer_weights *w, const c
     if (g.dim % 8 || g.q_rank % 8 || g.o_rank % 8 || (g.n_heads * g.head_dim / g.groups) % 64)
       return fail(CSA_ERR_ARG, "attn_v41_forward: dim, q_rank, o_rank must be multiples of 8, the group width of 64");
   }
-  if (r.is_kv_source || r.is_candidate_source)
-    return fail(CSA_ERR_UNSUPPORTED, "attn_v41_forward: kv-source and candidate-source roles are not implemented");
+  if (r.is_candidate_source) {
+    if (r.ratio <= 0 || !r.is_index_source || r.uses_candidates)
+      return fail(CSA_ERR_ARG, "attn_v41_forward: a candidate source is an index source at ratio > 0 that applies no mask");
+    if (!sh || !sh->candidates || g.cand_topk_blocks <= 0 || g.cand_topk_blocks > 2048 || sh->cand_width > 25600)
+      return fail(CSA_ERR_ARG, "attn_v41_forward: a candidate source needs shared->candidates and cand_topk_blocks in 1..2048");
+  }
+  if (r.is_kv_source) {
+    if (r.ratio <= 0) return fail(CSA_ERR_ARG, "attn_v41_forward: a kv source compresses at ratio > 0");
+    if (!sh) return fail(CSA_ERR_ARG, "attn_v41_forward: a kv source publishes through shared, which is NULL");
+    csa::CompressArgs a;
+    if (int rc = compress_args(ctx, w, st, x, B, T, start_pos, nullptr, &a, "attn_v41_forward")) return rc;
+  }
   if (B <= 0 || B > g.max_batch) return fail(CSA_ERR_SHAPE, "attn_v41_forward: batch %d outside [1, %d]", B, g.max_batch);
   if (T <= 0 || T > g.max_tokens) return fail(CSA_ERR_SHAPE, "attn_v41_forward: T %d outside [1, %d]", T, g.max_tokens);
   if (start_pos < 0 || (int64_t)start_pos + T > g.max_seq)
     return fail(CSA_ERR_SHAPE, "attn_v41_forward: positions [%d, %d) beyond max_seq %d", start_pos, start_pos + T, g.max_seq);
   if (start_pos > 0 && T != 1) return fail(CSA_ERR_SHAPE, "attn_v41_forward: decode takes one token per sequence");
+  csa_shared pub;  // a kv source publishes its own caches before it attends
+  if (r.ratio > 0 && r.is_kv_source && sh) {
+    pub = *sh;
+    publish_caches(w, st, T, start_pos, &pub);
+    sh = &pub;
+  }
   if (r.ratio > 0) {
     if (!sh || !sh->compress_kv) return fail(CSA_ERR_NO_KV_SOURCE, "attn_v41_forward: ratio > 0 and no latent cache published");
     if (sh->compress_len < 0 || sh->compress_stride < sh->compress_len || sh->compress_stride <= 0)
@@ -561,6 +661,14 @@ int attn_v41_forward(csa_ctx *ctx, const csa_layer_weights *w, csa_layer_state *
   } while (0)
 #define STEP(call, what) STAGE(call, what, 1)
 #define COPY(call, what) STAGE(call, what, 0)
+  // a kv source first compresses this call's tokens and publishes its caches ([atlas] the excerpt's
+  // _compress_kv precedes the selection and the attention)
+  if (r.is_kv_source) {
+    csa::CompressArgs ca;
+    if (int rc2 = compress_args(ctx, w, st, x_, B, T, start_pos, nullptr, &ca, "attn_v41_forward")) return rc2;
+    STAGE(csa::launch_compress(ca, ctx->comp_ws(), ctx->comp_ws_bytes(), ctx->num_sms, s), "compress", 2);
+    publish_caches(w, st, T, start_pos, sh);
+  }
   const bool idx_src = r.ratio > 0 && r.is_index_source;
   const int Hi = g.index_heads, dI = g.index_hd;
   bf16 *qI = dbg && dbg->qI ? (bf16 *)dbg->qI : ctx->qI;
@@ -618,11 +726,21 @@ int attn_v41_forward(csa_ctx *ctx, const csa_layer_weights *w, csa_layer_state *
       const uint8_t *cand = r.uses_candidates ? sh->candidates : nullptr;
       // short decode rows: scores and selection in one kernel, the scores kept on chip (unless the
       // caller wants them in its debug buffer)
-      if (!(dbg && dbg->scores) && csa::index_fused_supported(qI, (const bf16 *)sh->index_k, T, start_pos, Hi, dI,
-                                                               sh->compress_len, r.ratio, K)) {
+      if (!(dbg && dbg->scores) && !r.is_candidate_source &&
+          csa::index_fused_supported(qI, (const bf16 *)sh->index_k, T, start_pos, Hi, dI, sh->compress_len, r.ratio,
+                                     K)) {
         STEP(csa::launch_index_topk_fused(qI, wI, (const bf16 *)sh->index_k, B, start_pos, Hi, sh->compress_stride,
                                           sh->compress_len, r.ratio, cand, sh->cand_width, g.cand_block, K,
                                           rows_a_len, sh->topk_idxs, ctx->status, s),
+             "index scores + topk");
+      } else if (!(dbg && dbg->scores) && !r.is_candidate_source &&
+                 csa::index_gather_topk_supported(qI, (const bf16 *)sh->index_k, B, T, start_pos, Hi, dI,
+                                                  sh->compress_len, r.ratio, cand, sh->cand_width, g.cand_block, K,
+                                                  ctx->num_sms)) {
+        // long rows under a mask: gathered scores and the selection in one cluster launch
+        STEP(csa::launch_index_gather_topk(qI, wI, (const bf16 *)sh->index_k, B, start_pos, Hi, sh->compress_stride,
+                                           sh->compress_len, r.ratio, cand, sh->cand_width, g.cand_block, K,
+                                           rows_a_len, sh->topk_idxs, ctx->status, ctx->num_sms, s),
              "index scores + topk");
       } else {
         STEP(csa::launch_index_scores(qI, wI, (const bf16 *)sh->index_k, B, T, start_pos, Hi, dI,
@@ -632,6 +750,11 @@ int attn_v41_forward(csa_ctx *ctx, const csa_layer_weights *w, csa_layer_state *
         STEP(csa::launch_index_topk(S, B, T, start_pos, sh->compress_stride, sh->compress_len, r.ratio, cand,
                                     sh->cand_width, g.cand_block, K, rows_a_len, sh->topk_idxs, s),
              "index topk");
+        // the candidate source publishes the block mask of its own scores for later index sources
+        if (r.is_candidate_source)
+          STEP(csa::launch_cand_blocks(S, B, T, start_pos, sh->compress_stride, sh->compress_len, r.ratio,
+                                       g.cand_block, g.cand_topk_blocks, sh->candidates, sh->cand_width, s),
+               "candidate blocks");
       }
       sh->has_topk = 1;
     }

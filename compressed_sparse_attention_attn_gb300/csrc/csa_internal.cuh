@@ -91,9 +91,6 @@ struct LinearProblem {
 cudaError_t launch_linear(const LinearProblem *probs, int n, float *ws, size_t ws_bytes, int num_sms, int *status,
                           cudaStream_t s);
 constexpr size_t kGemmCounterBytes = 65536 * sizeof(int);
-// Arrival counters of the sparse attention's split queries, at the END of a context's workspace
-// (zero between launches; the last CTA of a query resets its counter).
-constexpr size_t kAttnCounterBytes = 65536 * sizeof(int);
 // Failure-detection test hook of the current device: while ns != 0 the projection kernels first
 // wait, up to ns nanoseconds, on a barrier phase that nothing completes, then take their timeout path.
 cudaError_t set_gemm_stall(unsigned long long ns);
@@ -135,6 +132,19 @@ cudaError_t launch_index_scores(const bf16 *qI, const float *wI, const bf16 *KI,
 cudaError_t launch_index_topk(const float *S, int B, int T, int start_pos, int Lstride, int compress_len, int ratio,
                               const uint8_t *cand, int cand_width, int cand_block, int K, int offset, int32_t *out,
                               cudaStream_t s);
+// Long decode rows under a candidate mask: the gathered scores and the top-k in one launch, one
+// thread-block cluster per query that selects together (the scores stay on chip).
+bool index_gather_topk_supported(const bf16 *qI, const bf16 *KI, int B, int T, int start_pos, int Hi, int dI,
+                                 int compress_len, int ratio, const uint8_t *cand, int cand_width, int cand_block,
+                                 int K, int num_sms);
+cudaError_t launch_index_gather_topk(const bf16 *qI, const float *wI, const bf16 *KI, int B, int start_pos, int Hi,
+                                     int Lstride, int compress_len, int ratio, const uint8_t *cand, int cand_width,
+                                     int cand_block, int K, int offset, int32_t *out, int *status, int num_sms,
+                                     cudaStream_t s);
+// The candidate source's block mask from its own scores: per query the top K blocks of cand_block
+// positions by their largest valid score, mask uint8 [B*T][cand_width] (1 = candidate).
+cudaError_t launch_cand_blocks(const float *S, int B, int T, int start_pos, int Lstride, int compress_len, int ratio,
+                               int cand_block, int K, uint8_t *mask, int cand_width, cudaStream_t s);
 // Scores and top-k in one kernel for decode rows (T == 1) with at most 512 valid positions (the
 // scores stay on chip); same conditions on the operands as the tensor-core scores, K <= 512.
 bool index_fused_supported(const bf16 *qI, const bf16 *KI, int T, int start_pos, int Hi, int dI, int compress_len,
@@ -173,6 +183,28 @@ cudaError_t launch_sparse_attn(const AttnArgs &a, float *ws, size_t ws_bytes, in
                                int *kernels = nullptr);
 // Whether the tensor-core kernel takes these arguments (it alone applies rope_q, for rd <= 64).
 bool sparse_attn_tc_supported(const AttnArgs &a);
+
+// The compressor of a kv-source layer (k_compress.cu): products of x [B*T][dim] with wkv (f32 at
+// ratio > 1, bf16 at ratio 1) and wgate, the partial group st_kv / st_score [B][ratio][hd], the
+// closed groups' latent rows Z and index keys KI (with wk) at rows j of [B][Lstride][.]; y_dbg (may be
+// NULL) receives the normed rows before RoPE and fp8.  Prefill (start_pos 0) or one decode token.
+struct CompressArgs {
+  const bf16 *x;
+  int B, T, start_pos, ratio, dim, hd, rd, dI;
+  const void *wkv;
+  const float *wgate, *norm;
+  const bf16 *wk;
+  const float *k_norm;
+  float *st_kv, *st_score;
+  bf16 *Z, *KI, *y_dbg;
+  int64_t Lstride;
+  const float *tab;
+  float eps;
+};
+bool compress_supported(const CompressArgs &a);
+// ws: f32 partial sums (the splits are chosen to fit ws_bytes)
+cudaError_t launch_compress(const CompressArgs &a, float *ws, size_t ws_bytes, int num_sms, cudaStream_t s);
+cudaError_t launch_fill_f32(float *p, int64_t n, float v, cudaStream_t s);
 
 // Record the calling thread's last error (attn_v41_last_error) and return `code`.
 int set_error(int code, const char *fmt, ...);

@@ -70,7 +70,6 @@ struct Params {
   int tpc, nsplit;  // tiles per CTA, CTAs per query
   bf16 *part_o;     // [NT][nsplit][H][512]  O_c / l_c of each split
   float *part_ml;   // [NT][nsplit][H][2]    (m_c, l_c), log2 domain
-  int *counters;    // [NT][H / 64] arrivals of a query's splits (zero between launches)
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid) {
@@ -203,7 +202,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::misc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   int *s_rescale = const_cast<int *>(abort_flag) + 1;
-  int *s_last = s_rescale + 1;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t row = blockIdx.x;  // query b*T + t
@@ -234,6 +232,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
       tma_load_2d_nohint(s_q + kb * HG * 128, &P.tm_q, q_full, kb * 64, (int)(row * P.H + hg * HG));
   }
   if (warp == 8) tc::tmem_alloc(tmem_slot, kCols);
+  // Launched as a programmatic dependent of the selection kernel before it: everything above (and
+  // q, written two launches earlier) overlaps that kernel; the index lists it writes are read only
+  // after this wait.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   const int n_all = P.na + P.nb;
   const int n_rows = P.a_len + P.b_len;
@@ -535,87 +537,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
       if (nmine > 0) ob = *reinterpret_cast<const uint4 *>(stage + h * HD + d0);
       store_out(P.o, P.o_rot, (row * P.H + hg * HG + h) * (int64_t)HD + d0, d0, HD - P.rd, tp, ob);
     }
-  } else {
-    if (nmine > 0) {
-      bf16 *mine = P.part_o + ((row * P.nsplit + split) * P.H + hg * HG) * (int64_t)HD;
-      for (int it = tid; it < kVecs; it += kThreads) {
-        const int h = it >> 6, d0 = (it & 63) * 8;
-        *reinterpret_cast<uint4 *>(mine + h * HD + d0) = *reinterpret_cast<const uint4 *>(stage + h * HD + d0);
-      }
-    }
-    // the query's last CTA to arrive merges every split's share (its own from shared memory), with
-    // the sink in the denominator only:  O = sum_c e^{m_c - M} l_c (O_c / l_c) / (e^{sink - M} + sum_c
-    // e^{m_c - M} l_c),  M = max(sink, m_c), summed in split order
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-      const int old = atomicAdd(P.counters + row * (P.H / HG) + hg, 1);
-      *s_last = old == P.nsplit - 1;
-    }
-    __syncthreads();
-    if (*s_last) {
-      __threadfence();
-      float *wts = red_max;  // [nsplit][HG] weights / den (the reduction buffers are idle now)
-      if (tid < HG) {
-        const float s2 = P.sink[hg * HG + tid] * 1.4426950408889634f;
-        float2 ml[kMaxTiles];
-#pragma unroll
-        for (int c = 0; c < kMaxTiles; ++c) {
-          ml[c] = make_float2(-INFINITY, 0.f);
-          if (c == split)
-            ml[c] = make_float2(m_sm[tid], l_sm[tid]);
-          else if (c < P.nsplit)
-            ml[c] = __ldcg(reinterpret_cast<const float2 *>(P.part_ml + ((row * P.nsplit + c) * P.H + hg * HG + tid) * 2));
-        }
-        float M = s2;
-#pragma unroll
-        for (int c = 0; c < kMaxTiles; ++c)
-          if (ml[c].y > 0.f) M = fmaxf(M, ml[c].x);
-        float den = exp2f(s2 - M), w[kMaxTiles];
-#pragma unroll
-        for (int c = 0; c < kMaxTiles; ++c) {
-          w[c] = ml[c].y > 0.f ? ml[c].y * exp2f(ml[c].x - M) : 0.f;
-          den += w[c];
-        }
-        const float inv = 1.0f / den;
-#pragma unroll
-        for (int c = 0; c < kMaxTiles; ++c)
-          if (c < P.nsplit) wts[c * HG + tid] = w[c] * inv;
-      }
-      __syncthreads();
-      const float2 *tp = P.o_rot ? reinterpret_cast<const float2 *>(P.tab) + (int64_t)(P.start_pos + t) * (P.rd >> 1)
-                                 : nullptr;
-      const bf16 *shares = P.part_o + (row * P.nsplit * P.H + hg * HG) * (int64_t)HD;
-      for (int it = tid; it < kVecs; it += kThreads) {
-        const int h = it >> 6, d0 = (it & 63) * 8;
-        uint4 u[kMaxTiles];
-        float wv[kMaxTiles];
-#pragma unroll
-        for (int c = 0; c < kMaxTiles; ++c) {  // every share's vector in flight at once
-          wv[c] = c < P.nsplit ? wts[c * HG + h] : 0.f;
-          u[c] = make_uint4(0u, 0u, 0u, 0u);
-          if (wv[c] != 0.f)
-            u[c] = c == split ? *reinterpret_cast<const uint4 *>(stage + h * HD + d0)
-                              : __ldcg(reinterpret_cast<const uint4 *>(shares + ((int64_t)c * P.H + h) * HD + d0));
-        }
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int c = 0; c < kMaxTiles; ++c) {
-          if (wv[c] == 0.f) continue;
-          const __nv_bfloat162 *pv = reinterpret_cast<const __nv_bfloat162 *>(&u[c]);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            acc[2 * q] = fmaf(wv[c], __low2float(pv[q]), acc[2 * q]);
-            acc[2 * q + 1] = fmaf(wv[c], __high2float(pv[q]), acc[2 * q + 1]);
-          }
-        }
-        uint4 ob;
-        __nv_bfloat162 *po = reinterpret_cast<__nv_bfloat162 *>(&ob);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) po[q] = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
-        store_out(P.o, P.o_rot, (row * P.H + hg * HG + h) * (int64_t)HD + d0, d0, HD - P.rd, tp, ob);
-      }
-      if (tid == 0) P.counters[row * (P.H / HG) + hg] = 0;  // ready for the next launch
+  } else if (nmine > 0) {
+    bf16 *mine = P.part_o + ((row * P.nsplit + split) * P.H + hg * HG) * (int64_t)HD;
+    for (int it = tid; it < kVecs; it += kThreads) {
+      const int h = it >> 6, d0 = (it & 63) * 8;
+      *reinterpret_cast<uint4 *>(mine + h * HD + d0) = *reinterpret_cast<const uint4 *>(stage + h * HD + d0);
     }
   }
   __syncthreads();
@@ -624,6 +550,90 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
     tc::tmem_dealloc(tmem, kCols);
   }
   if (tid == 0 && *abort_flag) atomicOr(P.status, kStatusTimeout);
+}
+
+// Merge of the split shares: block (query, 8 heads), one warp per head, two 16-byte vectors per
+// thread.  The weights e^{m_c - M} l_c / den put each share O_c / l_c back on the common scale, with
+// the sink in den; every thread forms its head's weights itself (no barrier), after loading the
+// weights' inputs and its vectors of every share at once, and shares of CTAs that found nothing
+// (l_c = 0) weigh 0 and are skipped.
+constexpr int kCombHeads = 8;
+constexpr int kCombThreads = 256;
+struct CombineParams {
+  const bf16 *part_o;
+  const float *part_ml;
+  int nsplit, H, T;
+  const float *sink;
+  bf16 *o, *o_rot;
+  int rd, start_pos;
+  const float *tab;
+};
+
+__global__ void __launch_bounds__(kCombThreads) k_attn_combine(const __grid_constant__ CombineParams C) {
+  const int64_t row = blockIdx.x;
+  const int h0 = blockIdx.y * kCombHeads, tid = threadIdx.x;
+  const int t = (int)(row % C.T);
+  const float2 *tp = C.o_rot ? reinterpret_cast<const float2 *>(C.tab) + (int64_t)(C.start_pos + t) * (C.rd >> 1)
+                             : nullptr;
+  constexpr int kPer = kCombHeads * (HD / 8) / kCombThreads;  // consecutive vectors per thread
+  static_assert((HD / 8) % kPer == 0, "a thread's vectors belong to one head");
+  const int h = h0 + (tid * kPer) / (HD / 8);
+  // this head's weights e^{m_c - M} l_c / den, computed by each of its threads (same addresses)
+  const float s2 = C.sink[h] * 1.4426950408889634f;
+  // (a programmatic dependent of the attention kernel: the shares are read after this wait)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // every share's (m, l) and vectors in flight together; shares of CTAs that found nothing (l = 0,
+  // their buffers never written) are read but never used
+  float2 ml[kMaxTiles];
+  uint4 u[kPer][kMaxTiles];
+#pragma unroll
+  for (int c = 0; c < kMaxTiles; ++c) {
+    ml[c] = make_float2(-INFINITY, 0.f);
+    if (c < C.nsplit) ml[c] = __ldcg(reinterpret_cast<const float2 *>(C.part_ml + ((row * C.nsplit + c) * C.H + h) * 2));
+  }
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int d0 = ((tid * kPer + k) % (HD / 8)) * 8;
+#pragma unroll
+    for (int c = 0; c < kMaxTiles; ++c) {
+      u[k][c] = make_uint4(0u, 0u, 0u, 0u);
+      if (c < C.nsplit)
+        u[k][c] = __ldcg(reinterpret_cast<const uint4 *>(C.part_o + ((row * C.nsplit + c) * C.H + h) * (int64_t)HD + d0));
+    }
+  }
+  // this head's weights e^{m_c - M} l_c / den
+  float M = s2;
+#pragma unroll
+  for (int c = 0; c < kMaxTiles; ++c)
+    if (ml[c].y > 0.f) M = fmaxf(M, ml[c].x);
+  float den = exp2f(s2 - M), w[kMaxTiles];
+#pragma unroll
+  for (int c = 0; c < kMaxTiles; ++c) {
+    w[c] = ml[c].y > 0.f ? ml[c].y * exp2f(ml[c].x - M) : 0.f;
+    den += w[c];
+  }
+  const float inv = 1.0f / den;
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int d0 = ((tid * kPer + k) % (HD / 8)) * 8;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int c = 0; c < kMaxTiles; ++c) {
+      if (w[c] == 0.f) continue;
+      const float wv = w[c] * inv;
+      const __nv_bfloat162 *pv = reinterpret_cast<const __nv_bfloat162 *>(&u[k][c]);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        acc[2 * q] = fmaf(wv, __low2float(pv[q]), acc[2 * q]);
+        acc[2 * q + 1] = fmaf(wv, __high2float(pv[q]), acc[2 * q + 1]);
+      }
+    }
+    uint4 ob;
+    __nv_bfloat162 *po = reinterpret_cast<__nv_bfloat162 *>(&ob);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) po[q] = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
+    store_out(C.o, C.o_rot, (row * C.H + h) * (int64_t)HD + d0, d0, HD - C.rd, tp, ob);
+  }
 }
 
 }  // namespace attn
@@ -674,15 +684,13 @@ cudaError_t launch_sparse_attn_tc(const AttnArgs &a, float *ws, size_t ws_bytes,
   // tail, padding whenever fewer than K positions are valid, so its CTAs mostly end after their index
   // pass); ties go to fewer CTAs.  The shares must fit the workspace (after the GEMM's counters).
   const int groups = a.H / HG;
-  const size_t reserved = kGemmCounterBytes + kAttnCounterBytes;
-  const size_t avail = ws_bytes > reserved ? ws_bytes - reserved : 0;
-  const bool can_split = (int64_t)nq * groups <= (int64_t)(kAttnCounterBytes / sizeof(int));
+  const size_t avail = ws_bytes > kGemmCounterBytes ? ws_bytes - kGemmCounterBytes : 0;
   int tpc = p.ntiles;
   int64_t best = INT64_MAX;
   for (int c = 1; c <= p.ntiles; ++c) {
     const int ns = (p.ntiles + c - 1) / c;
     const size_t need = (size_t)nq * ns * a.H * (HD * sizeof(bf16) + 2 * sizeof(float));
-    if (ns > 1 && (need > avail || !can_split)) continue;
+    if (ns > 1 && need > avail) continue;
     const int64_t units = (int64_t)nq * groups, ctas = units * ns;
     int64_t cost2;  // twice the cost
     if (ctas <= num_sms)
@@ -701,16 +709,52 @@ cudaError_t launch_sparse_attn_tc(const AttnArgs &a, float *ws, size_t ws_bytes,
   uint8_t *base = reinterpret_cast<uint8_t *>(ws) + kGemmCounterBytes;
   p.part_o = reinterpret_cast<bf16 *>(base);
   p.part_ml = reinterpret_cast<float *>(base + (size_t)nq * p.nsplit * a.H * HD * sizeof(bf16));
-  p.counters = reinterpret_cast<int *>(reinterpret_cast<uint8_t *>(ws) + ws_bytes - kAttnCounterBytes);
   static SmemAttr attr;
   const size_t smem = 1024 + Smem::total;
   {
     cudaError_t e = attr.ensure((const void *)k_sparse_attn_tc, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  dim3 grid(nq, p.nsplit, groups);
-  k_sparse_attn_tc<<<grid, kThreads, smem, s>>>(p);
+  // a programmatic dependent launch: the CTAs start (barriers, TMEM, q's copy) while the kernel before
+  // them on the stream still runs, and wait for it before they read the selection
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(nq, p.nsplit, groups);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, k_sparse_attn_tc, p);
+  if (e == cudaSuccess) e = cudaGetLastError();
   *kernels = 1;
+  if (p.nsplit == 1 || e != cudaSuccess) return e;
+  CombineParams c;
+  c.part_o = p.part_o;
+  c.part_ml = p.part_ml;
+  c.nsplit = p.nsplit;
+  c.H = a.H;
+  c.T = a.T;
+  c.sink = a.sink;
+  c.o = a.o;
+  c.o_rot = a.o_rot;
+  c.rd = a.rd;
+  c.start_pos = a.start_pos;
+  c.tab = a.tab;
+  // launched as a programmatic dependent, so its launch overlaps the attention kernel's tail
+  cudaLaunchConfig_t cc;
+  memset(&cc, 0, sizeof(cc));
+  cc.gridDim = dim3(nq, a.H / kCombHeads);
+  cc.blockDim = dim3(kCombThreads);
+  cc.stream = s;
+  cc.attrs = at;
+  cc.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cc, k_attn_combine, c);
+  *kernels = 2;
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

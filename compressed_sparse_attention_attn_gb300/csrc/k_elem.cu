@@ -8,19 +8,10 @@
 #include <cuda_fp8.h>
 
 #include "csa_internal.cuh"
+#include "rowops.cuh"
 
 namespace csa {
 
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
 
 // ---------------------------------------------------------------------------------------------
 // RMSNorm, "deepseek_v41_ref::attn" precision contract: f32 compute, bf16 result.
@@ -60,10 +51,6 @@ cudaError_t launch_rmsnorm(const bf16 *x, int M, int N, const float *w, float ep
 // RoPE, "deepseek_v41_ref::attn" apply_rotary: last rd elements of each row, adjacent pairs as
 // complex numbers times (cos, sin) of the row's position (conjugate when inverse).
 // ---------------------------------------------------------------------------------------------
-__device__ __forceinline__ void rotate_pair(float a, float b, float c, float s, float &re, float &im) {
-  re = __fsub_rn(__fmul_rn(a, c), __fmul_rn(b, s));
-  im = __fadd_rn(__fmul_rn(a, s), __fmul_rn(b, c));
-}
 
 // One warp per row; lane i takes pairs i, i+32, ...
 __global__ void k_rope(bf16 *__restrict__ x, int64_t rows, int row_len, int rd, PosSpec pos,
@@ -98,29 +85,6 @@ cudaError_t launch_rope(bf16 *x, int64_t rows, int row_len, int rd, PosSpec pos,
   return cudaGetLastError();
 }
 
-// ---------------------------------------------------------------------------------------------
-// fp8 round trip of one block of 32 held one value per lane ("deepseek_v41_ref::attn"
-// act_quant_inplace, pow2_ceil).  Returns the new value; *code / *sexp for the lane's element and
-// the block's scale exponent.
-// ---------------------------------------------------------------------------------------------
-__device__ __forceinline__ float pow2_ceil_f(float v) {
-  uint32_t u = __float_as_uint(v);
-  if ((u & 0x007fffffu) == 0u) return v;
-  return __uint_as_float(((u >> 23) + 1u) << 23);
-}
-
-__device__ __forceinline__ float fp8_block_roundtrip(float v, uint8_t &code, int &sexp) {
-  float amax = warp_max(fabsf(v));
-  float s = pow2_ceil_f(__fdiv_rn(fmaxf(amax, 1e-4f), 448.0f));
-  float r = __fdiv_rn(v, s);
-  r = fminf(fmaxf(r, -448.0f), 448.0f);
-  __nv_fp8_storage_t c = __nv_cvt_float_to_fp8(r, __NV_SATFINITE, __NV_E4M3);
-  __half_raw hr = __nv_cvt_fp8_to_halfraw(c, __NV_E4M3);
-  float dq = __half2float(__half(hr));
-  code = (uint8_t)c;
-  sexp = (int)((__float_as_uint(s) >> 23) & 0xffu) - 127;
-  return __fmul_rn(dq, s);
-}
 
 // In-place act_quant over x [n]: one warp per block of 32.
 __global__ void k_act_quant(bf16 *__restrict__ x, int64_t nblocks, uint8_t *__restrict__ codes,

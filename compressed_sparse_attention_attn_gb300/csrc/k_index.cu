@@ -115,6 +115,9 @@ __global__ void __launch_bounds__(NT, 2048 / NT) k_index_topk(const float *__res
                                                              const uint8_t *__restrict__ cand, int cand_width,
                                                              int cand_block, int K, int offset, int32_t *__restrict__ out,
                                                              int cap_vals) {
+  // the attention after this kernel may start its set-up now (it waits for this grid before it reads
+  // the selection)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   extern __shared__ unsigned long long tk_smem[];
   unsigned long long *vals = tk_smem;                      // [cap_vals] valid values, ascending position
   int *klist = reinterpret_cast<int *>(vals + cap_vals);   // [2 NT] kept blocks
@@ -179,6 +182,69 @@ __global__ void __launch_bounds__(NT, 2048 / NT) k_index_topk(const float *__res
     };
     topk_select(sh, nvalid, limit, from_global, K, offset, out + row * K);
   }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Candidate blocks (the candidate source's mask, "metrale_model_arch::attn_v41": a block-level
+// candidate mask published for later index sources; config.json candidate_block_size and
+// candidate_topk_blocks): per query, block c scores the largest valid score S[t][j] inside it
+// (blocks without a valid position are not candidates), the top cand_topk by that score (ties to the
+// lower block, the index top-k's order keys) are marked 1, the others 0.  One CTA per query; the
+// selection is topk_core.cuh's over the block values, written to shared memory, then scattered.
+// ---------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(512) k_cand_blocks(const float *__restrict__ S, int T, int start_pos, int Lstride,
+                                                     int compress_len, int ratio, int cand_block, int K,
+                                                     uint8_t *__restrict__ mask, int cand_width) {
+  extern __shared__ unsigned long long cb_smem[];
+  unsigned long long *vals = cb_smem;                           // [cand_width] block values (0: none)
+  int32_t *sel = reinterpret_cast<int32_t *>(vals + cand_width);  // [K] chosen blocks
+  __shared__ TopkShared sh;
+  const int64_t row = blockIdx.x;
+  const int p = start_pos + (int)(row % T);
+  const int limit = min((p + 1) / ratio, compress_len);
+  const float *Sr = S + row * Lstride;
+  const int nb = min((limit + cand_block - 1) / cand_block, cand_width);
+  if (threadIdx.x == 0) topk_shared_init(sh, K);
+  __syncthreads();
+  unsigned mine = 0;
+  for (int c = threadIdx.x; c < cand_width; c += blockDim.x) {
+    unsigned long long v = 0ull;
+    if (c < nb) {
+      const int j1 = min((c + 1) * cand_block, limit);
+      float m = Sr[c * cand_block];
+      for (int j = c * cand_block + 1; j < j1; ++j) m = fmaxf(m, Sr[j]);
+      v = topk_value(m, c);
+      ++mine;
+    }
+    vals[c] = v;
+  }
+  if (mine) atomicAdd(&sh.count, mine);
+  __syncthreads();
+  const unsigned nvalid = sh.count;
+  auto at = [&](int i, bool &ok) -> unsigned long long {
+    ok = vals[i] != 0ull;
+    return vals[i];
+  };
+  topk_select(sh, nvalid, nb, at, K, 0, sel);
+  __syncthreads();
+  uint8_t *mr = mask + row * cand_width;
+  for (int c = threadIdx.x; c < cand_width; c += blockDim.x) mr[c] = 0;
+  __syncthreads();
+  const int nsel = (int)min(nvalid, (unsigned)K);
+  for (int k = threadIdx.x; k < nsel; k += blockDim.x) mr[sel[k]] = 1;
+}
+
+cudaError_t launch_cand_blocks(const float *S, int B, int T, int start_pos, int Lstride, int compress_len, int ratio,
+                               int cand_block, int K, uint8_t *mask, int cand_width, cudaStream_t s) {
+  if (B * T <= 0) return cudaSuccess;
+  const size_t smem = (size_t)cand_width * 8 + (size_t)K * 4;
+  if (smem > 200 * 1024) return cudaErrorInvalidValue;
+  static SmemAttr attr;
+  cudaError_t e = attr.ensure((const void *)k_cand_blocks, (int)smem);
+  if (e != cudaSuccess) return e;
+  k_cand_blocks<<<B * T, 512, smem, s>>>(S, T, start_pos, Lstride, compress_len, ratio, cand_block, K, mask,
+                                         cand_width);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_index_topk(const float *S, int B, int T, int start_pos, int Lstride, int compress_len, int ratio,

@@ -316,6 +316,264 @@ __global__ void __launch_bounds__(kThreads) k_index_scores_gather_tc(const __gri
 }
 
 
+// ---- gathered scores + top-k across a cluster (long decode rows) ---------------------------------
+// The gathered variant's work for one query split over a thread-block cluster of P CTAs: CTA c takes
+// the contiguous run of kept unit pairs [c np / P, (c+1) np / P), so the CTAs' ranges are in
+// ascending position.  Each keeps its keys' scores in shared memory as the top-k's 64-bit values
+// (0 where a key is not valid), and the cluster then selects together: the counts and, per radix
+// pass, the 256-bin histograms are read from every CTA through distributed shared memory, every CTA
+// takes the same digit, and each writes its taken positions in ascending order at the offset of the
+// CTAs before it.  The scores never go to global memory and the top-k needs no launch of its own.
+constexpr int kFuseBufs = 2;
+constexpr int kFuseVals = 4096;  // values a CTA keeps (its pairs x 128 keys)
+
+struct GatherTopkParams {
+  CUtensorMap tm_k;  // K^I [B*Lstride][128], box {64, 64}
+  CUtensorMap tm_q;  // Q^I [B*Hi][128], box {64, Hi}
+  const float *wI;   // [B][Hi]
+  int Hi, Lstride, compress_len, ratio, start_pos, P, max_units;
+  const uint8_t *cand;
+  int cand_width, cand_block, K, offset;
+  int32_t *out;  // [B][K]
+  int *status;
+};
+
+__global__ void __launch_bounds__(kThreads) k_index_gather_topk_tc(const __grid_constant__ GatherTopkParams P) {
+  // the attention after this kernel may start its set-up now (it waits for this grid before it reads
+  // the selection)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = tc::smem_u32(smem_raw);
+  uint8_t *smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
+  const int N = P.Hi;
+  constexpr uint32_t k_buf = TILE * 128 * 2;  // a pair: two 64-column halves of 128 keys
+  const uint32_t q_half = (uint32_t)N * 128;
+  uint8_t *sk = smem, *sq = smem + kFuseBufs * k_buf;
+  float *w_s = reinterpret_cast<float *>(sq + 2 * q_half);                              // [Hi]
+  unsigned long long *vals = reinterpret_cast<unsigned long long *>(w_s + kMaxN);       // [kFuseVals]
+  unsigned *hists = reinterpret_cast<unsigned *>(vals + kFuseVals);                     // [2][256] per pass
+  unsigned *xchg = hists + 512;                                                         // [2]: count, taken
+  int *units = reinterpret_cast<int *>(xchg + 2);                                       // [max_units]
+  uint64_t *bars = reinterpret_cast<uint64_t *>(units + ((P.max_units + 1) & ~1));
+  uint64_t *full = bars, *done = bars + kFuseBufs, *qbar = bars + 2 * kFuseBufs;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(qbar + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  int *s_nunits = const_cast<int *>(abort_flag) + 1;
+  __shared__ TopkShared sh;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t rank = tc::cluster_ctarank();
+  const int b = blockIdx.y;
+  const int limit = min((P.start_pos + 1) / P.ratio, P.compress_len);
+  const int per_block = P.cand_block / 64;
+  const uint32_t ncols = N * kFuseBufs <= 32 ? 32 : N * kFuseBufs <= 64 ? 64 : N * kFuseBufs <= 128 ? 128
+                         : N * kFuseBufs <= 256 ? 256 : 512;
+
+  if (tid == 0) {
+    for (int i = 0; i < 2 * kFuseBufs + 1; ++i) tc::mbar_init(&bars[i], 1);
+    *abort_flag = 0;
+    topk_shared_init(sh, P.K);
+    tc::fence_barrier_init();
+    tc::prefetch_tmap(&P.tm_k);
+    tc::prefetch_tmap(&P.tm_q);
+    tc::mbar_expect_tx(qbar, 2 * q_half);
+    const uint64_t pol = tc::policy_evict_first();
+    for (int kb = 0; kb < 2; ++kb) tc::tma_load_2d(sq + kb * q_half, &P.tm_q, qbar, kb * 64, b * N, pol);
+  }
+  for (int e = tid; e < N; e += kThreads) w_s[e] = P.wI[(int64_t)b * N + e];
+  if (warp == 1) {
+    // the kept units in ascending key order
+    const uint8_t *cr = P.cand + (int64_t)b * P.cand_width;
+    const int nblk = min((limit + P.cand_block - 1) / P.cand_block, P.cand_width);
+    int n = 0;
+    for (int b0 = 0; b0 < nblk; b0 += 8 * 32) {
+      uint32_t kv[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int blk = b0 + k * 32 + lane;
+        kv[k] = blk < nblk ? cr[blk] : 0u;
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int blk = b0 + k * 32 + lane;
+        const bool keep = kv[k] != 0u;
+        const unsigned bal = __ballot_sync(0xffffffffu, keep);
+        if (keep) {
+          const int base = n + __popc(bal & ((1u << lane) - 1u)) * per_block;
+          for (int s2 = 0; s2 < per_block; ++s2)
+            if (base + s2 < P.max_units) units[base + s2] = blk * per_block + s2;
+        }
+        n += __popc(bal) * per_block;
+      }
+    }
+    if (lane == 0) {
+      while (n > 0 && n <= P.max_units && units[n - 1] * 64 >= limit) --n;
+      *s_nunits = min(n, P.max_units);
+    }
+  }
+  if (warp == 0) tc::tmem_alloc(tmem_slot, ncols);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int nunits = *s_nunits;
+  const int npairs_all = (nunits + 1) / 2;
+  const int pa = (int)(((int64_t)rank * npairs_all) / P.P), pb = (int)(((int64_t)(rank + 1) * npairs_all) / P.P);
+  const int mine = min(pb - pa, kFuseVals / TILE);  // (the host sizes P so that every range fits)
+  auto issue = [&](int i) {  // pair pa + i into buffer i % kFuseBufs
+    const int pi = pa + i;
+    const int u0 = units[2 * pi], two = 2 * pi + 1 < nunits;
+    uint64_t *bar = &full[i % kFuseBufs];
+    uint8_t *dst = sk + (i % kFuseBufs) * k_buf;
+    const uint64_t pol = tc::policy_evict_first();
+    tc::mbar_expect_tx(bar, (two ? 2u : 1u) * 2u * 64u * 128u);
+    for (int kb = 0; kb < 2; ++kb) {
+      tc::tma_load_2d(dst + kb * (k_buf / 2), &P.tm_k, bar, kb * 64, b * P.Lstride + u0 * 64, pol);
+      if (two)
+        tc::tma_load_2d(dst + kb * (k_buf / 2) + 64 * 128, &P.tm_k, bar, kb * 64,
+                        b * P.Lstride + units[2 * pi + 1] * 64, pol);
+    }
+  };
+  int issued = 0, landed = 0;
+  bool q_landed = false;
+  if (tid == 0)
+    for (; issued < min(mine, kFuseBufs); ++issued) issue(issued);
+  bool ok = true;
+  if (tid == 0 && mine > 0) ok = q_landed = tc::mbar_wait(qbar, 0, abort_flag);
+  const uint32_t id = tc::idesc_bf16_f32(TILE, N);
+  unsigned my_valid = 0;
+  int done_pairs = 0;
+  for (int i = 0; i < mine; ++i) {
+    const int buf = i % kFuseBufs;
+    const uint32_t par = (uint32_t)(i / kFuseBufs) & 1u;
+    if (tid == 0 && ok) {
+      ok = tc::mbar_wait(&full[buf], par, abort_flag);
+      if (ok) {
+        ++landed;
+        tc::tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(buf * N);
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb) {
+          const uint64_t ad = tc::sdesc_sw128(tc::smem_u32(sk + buf * k_buf + kb * (k_buf / 2)), 16, 1024);
+          const uint64_t bd = tc::sdesc_sw128(tc::smem_u32(sq + kb * q_half), 16, 1024);
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) tc::mma_bf16(d, ad + 2ull * k4, bd + 2ull * k4, id, (kb | k4) ? 1u : 0u);
+        }
+        tc::mma_commit(&done[buf]);
+      }
+    }
+    const bool got = tc::mbar_wait(&done[buf], par, abort_flag);
+    tc::tc_fence_after();
+    if (got && tid == 0 && i + kFuseBufs < mine) issue(issued++);
+    const int pi = pa + i;
+    const int slot = 2 * pi + (tid >> 6);
+    const int j = slot < nunits ? units[slot] * 64 + (tid & 63) : limit;
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(buf * N);
+    float acc = 0.f;
+    for (int h0 = 0; h0 < N; h0 += 16) {
+      uint32_t v[16];
+      tc::tmem_ld16_wait(lane_base + (uint32_t)h0, v);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) acc = fmaf(w_s[h0 + k], fmaxf(__uint_as_float(v[k]), 0.f), acc);
+    }
+    const bool valid = got && j < limit;
+    vals[i * TILE + tid] = valid ? topk_value(acc, j) : 0ull;
+    my_valid += valid ? 1u : 0u;
+    tc::tc_fence_before();
+    const int failed = __syncthreads_or(!got);
+    tc::tc_fence_after();
+    ++done_pairs;
+    if (failed) break;
+  }
+  if (tid == 0) {
+    // copies that may still be in flight (none unless a wait gave up): let them land, bounded
+    const uint64_t t0w = tc::global_ns();
+    auto drain = [&](uint64_t *bar, uint32_t par) {
+      while (!tc::mbar_try_wait(bar, par) && tc::global_ns() - t0w < tc::kWaitLimitNs) {
+      }
+    };
+    if (!q_landed) drain(qbar, 0);
+    for (int i = landed; i < issued; ++i) drain(&full[i % kFuseBufs], (uint32_t)(i / kFuseBufs) & 1u);
+  }
+  // ---- the selection, across the cluster ---------------------------------------------------------
+  const int n_iter = done_pairs * TILE;
+  unsigned wv = my_valid;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) wv += __shfl_xor_sync(0xffffffffu, wv, o);
+  if (lane == 0) atomicAdd(&sh.count, wv);
+  __syncthreads();
+  if (tid == 0) xchg[0] = sh.count;
+  tc::cluster_sync();  // every CTA's count is published
+  unsigned total = 0;
+  for (int c = 0; c < P.P; ++c) total += tc::ld_cluster_u32(tc::cluster_map(tc::smem_u32(&xchg[0]), (uint32_t)c));
+  const bool all = total <= (unsigned)P.K;
+  int fs = 0;
+  unsigned long long thr = 0ull;
+  if (!all) {
+    int pass = 0;
+    for (int shift = 56; shift >= 0; shift -= 8, ++pass) {
+      unsigned *hist = hists + (pass & 1) * 256;
+      for (int i = tid; i < 256; i += kThreads) hist[i] = 0;
+      __syncthreads();
+      const unsigned long long prefix = sh.prefix;
+      const unsigned long long hi_mask = shift == 56 ? 0ull : (~0ull << (shift + 8));
+      for (int i = tid; i < n_iter; i += kThreads) {
+        const unsigned long long v = vals[i];
+        if (v && (v & hi_mask) == (prefix & hi_mask)) atomicAdd(&hist[(v >> shift) & 255u], 1u);
+      }
+      tc::cluster_sync();  // every CTA's histogram of this pass is complete
+      for (int i = tid; i < 256; i += kThreads) {
+        unsigned t = 0;
+        for (int c = 0; c < P.P; ++c) t += tc::ld_cluster_u32(tc::cluster_map(tc::smem_u32(&hist[i]), (uint32_t)c));
+        sh.hist[i] = t;
+      }
+      __syncthreads();
+      if (warp == 0) radix_pick(sh, sh.hist, shift);
+      __syncthreads();
+      if (sh.done) break;  // the same in every CTA: each summed the same histograms
+    }
+    fs = sh.shift;
+    thr = sh.prefix >> fs;
+  }
+  // taken positions: this CTA's in ascending order, after those of the CTAs before it
+  unsigned mine_taken = 0;
+  for (int i = tid; i < n_iter; i += kThreads) {
+    const unsigned long long v = vals[i];
+    mine_taken += (v != 0ull && (all || (v >> fs) >= thr)) ? 1u : 0u;
+  }
+#pragma unroll
+  for (int o2 = 16; o2 > 0; o2 >>= 1) mine_taken += __shfl_xor_sync(0xffffffffu, mine_taken, o2);
+  if (tid == 0) xchg[1] = 0;
+  __syncthreads();
+  if (lane == 0) atomicAdd(&xchg[1], mine_taken);
+  tc::cluster_sync();  // every CTA's taken count is published
+  unsigned before = 0, taken_all = 0;
+  for (int c = 0; c < P.P; ++c) {
+    const unsigned t = tc::ld_cluster_u32(tc::cluster_map(tc::smem_u32(&xchg[1]), (uint32_t)c));
+    if (c < (int)rank) before += t;
+    taken_all += t;
+  }
+  int32_t *o = P.out + (int64_t)b * P.K;
+  unsigned base = before;
+  for (int i0 = 0; i0 < n_iter; i0 += kThreads) {
+    const int i = i0 + tid;
+    const unsigned long long v = i < n_iter ? vals[i] : 0ull;
+    const bool take = v != 0ull && (all || (v >> fs) >= thr);
+    const unsigned s2 = ordered_slot(sh, take, base);
+    if (take && s2 < (unsigned)P.K) o[s2] = (int32_t)(~(uint32_t)(v & 0xffffffffull)) + P.offset;
+  }
+  if (rank == (uint32_t)P.P - 1)
+    for (int k = (int)taken_all + tid; k < P.K; k += kThreads) o[k] = -1;
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, ncols);
+  }
+  if (tid == 0 && *abort_flag && P.status) atomicOr(P.status, kStatusTimeout);
+  tc::cluster_sync();  // no CTA leaves while another may still read its shared memory
+}
+
 // ---- fused scores + top-k for short decode rows --------------------------------------------------
 // A decode query (T == 1) with at most kFusedTiles * 128 valid positions: one CTA loads all its key
 // tiles and Q^I by TMA, runs one MMA chain per tile into its own TMEM columns, and the epilogue turns
@@ -337,6 +595,9 @@ struct FusedParams {
 };
 
 __global__ void __launch_bounds__(kFusedThreads, 1) k_index_topk_fused_tc(const __grid_constant__ FusedParams P) {
+  // the attention after this kernel may start its set-up now (it waits for this grid before it reads
+  // the selection)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = tc::smem_u32(smem_raw);
   uint8_t *smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
@@ -536,6 +797,86 @@ cudaError_t launch_index_scores_tc(const bf16 *qI, const float *wI, const bf16 *
                                          cand_width, cand_block, S, status, s);
   dim3 grid(tiles, (T + p.QG - 1) / p.QG, B);
   k_index_scores_tc<<<grid, kThreads, smem, s>>>(p);
+  return cudaGetLastError();
+}
+
+// CTAs per query of the cluster-fused gathered scores + top-k, or 0 when the launch does not take it:
+// a decode query with a candidate mask in 64-key units whose span exceeds 1024 keys (where the
+// gathered kernel pays), P <= 8 CTAs (a portable cluster) that each hold at most kFuseVals / 128 unit
+// pairs even if the mask kept every block, as many as fill two CTAs an SM in one wave otherwise.
+static int gather_topk_ctas(const bf16 *qI, const bf16 *KI, int B, int T, int start_pos, int Hi, int dI,
+                            int compress_len, int ratio, const uint8_t *cand, int cand_width, int cand_block, int K,
+                            int num_sms) {
+  using namespace idx;
+  if (!cand || T != 1 || ratio <= 0 || cand_block % 64 || K > kTopkMaxK || B <= 0) return 0;
+  if (!index_scores_tc_supported(qI, KI, Hi, dI) || Hi * kFuseBufs > 512) return 0;
+  const int limit = std::min((start_pos + 1) / ratio, compress_len);
+  const int nblk = std::min((limit + cand_block - 1) / cand_block, cand_width);
+  if ((int64_t)nblk * cand_block <= 1024) return 0;
+  const int max_pairs = (nblk * (cand_block / 64) + 1) / 2;
+  const int need = (max_pairs + kFuseVals / TILE - 1) / (kFuseVals / TILE);
+  if (need > 8) return 0;
+  return std::max(need, std::min(8, std::min(max_pairs, 2 * num_sms / B)));
+}
+
+bool index_gather_topk_supported(const bf16 *qI, const bf16 *KI, int B, int T, int start_pos, int Hi, int dI,
+                                 int compress_len, int ratio, const uint8_t *cand, int cand_width, int cand_block,
+                                 int K, int num_sms) {
+  return gather_topk_ctas(qI, KI, B, T, start_pos, Hi, dI, compress_len, ratio, cand, cand_width, cand_block, K,
+                          num_sms) > 0;
+}
+
+cudaError_t launch_index_gather_topk(const bf16 *qI, const float *wI, const bf16 *KI, int B, int start_pos, int Hi,
+                                     int Lstride, int compress_len, int ratio, const uint8_t *cand, int cand_width,
+                                     int cand_block, int K, int offset, int32_t *out, int *status, int num_sms,
+                                     cudaStream_t s) {
+  using namespace idx;
+  const int Pc = gather_topk_ctas(qI, KI, B, 1, start_pos, Hi, DI, compress_len, ratio, cand, cand_width, cand_block, K,
+                                  num_sms);
+  if (Pc <= 0) return cudaErrorInvalidValue;
+  GatherTopkParams p;
+  memset(&p, 0, sizeof(p));
+  const int limit = std::min((start_pos + 1) / ratio, compress_len);
+  const int nblk = std::min((limit + cand_block - 1) / cand_block, cand_width);
+  p.max_units = nblk * (cand_block / 64);
+  if (!tma_map_2d_bf16(&p.tm_k, KI, DI, (uint64_t)B * Lstride, DI, 64, 64)) return cudaErrorInvalidValue;
+  if (!tma_map_2d_bf16(&p.tm_q, qI, DI, (uint64_t)B * Hi, DI, 64, (uint32_t)Hi)) return cudaErrorInvalidValue;
+  p.wI = wI;
+  p.Hi = Hi;
+  p.Lstride = Lstride;
+  p.compress_len = std::min(compress_len, Lstride);
+  p.ratio = ratio;
+  p.start_pos = start_pos;
+  p.P = Pc;
+  p.cand = cand;
+  p.cand_width = cand_width;
+  p.cand_block = cand_block;
+  p.K = K;
+  p.offset = offset;
+  p.out = out;
+  p.status = status;
+  const size_t smem = 1024 + (size_t)kFuseBufs * TILE * 128 * 2 + 2 * (size_t)Hi * 128 + kMaxN * 4 +
+                      (size_t)kFuseVals * 8 + 514 * 4 + 4 * (size_t)((p.max_units + 1) & ~1) +
+                      (2 * kFuseBufs + 1) * 8 + 16;
+  if (smem > 200 * 1024) return cudaErrorInvalidValue;
+  static SmemAttr attr;
+  cudaError_t e = attr.ensure((const void *)k_index_gather_topk_tc, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(Pc, B);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = Pc;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, k_index_gather_topk_tc, p);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -71,13 +71,49 @@ __device__ __forceinline__ unsigned ordered_slot(TopkShared &sh, bool take, unsi
   return slot;
 }
 
+// One radix step, run by warp 0: in the 256-bin histogram `hist` of the values that match the
+// current prefix at digit `shift`, find the digit holding the remain-th largest value; update the
+// prefix, remain and shift, and set done when every value with the new prefix is taken.
+__device__ __forceinline__ void radix_pick(TopkShared &sh, const unsigned *hist, int shift) {
+  const int lane = threadIdx.x & 31;
+  unsigned c[8], tot = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    c[k] = hist[255 - 8 * lane - k];
+    tot += c[k];
+  }
+  unsigned incl = tot;
+#pragma unroll
+  for (int o2 = 1; o2 < 32; o2 <<= 1) {
+    const unsigned n = __shfl_up_sync(0xffffffffu, incl, o2);
+    if (lane >= o2) incl += n;
+  }
+  const unsigned excl = incl - tot, remain = sh.remain;
+  if (excl < remain && remain <= incl) {
+    unsigned above = excl;
+    int d = 255 - 8 * lane;
+    unsigned cd = 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      d = 255 - 8 * lane - k;
+      cd = c[k];
+      if (above + cd >= remain) break;
+      above += cd;
+    }
+    sh.prefix = sh.prefix | ((unsigned long long)d << shift);
+    sh.remain = remain - above;
+    sh.shift = shift;
+    if (cd == remain - above) sh.done = 1;  // every value with this prefix is taken
+  }
+}
+
 // The selection of one query.  value_at(i, ok) gives candidate i < n_iter in ascending position
 // (ok false: not a valid position); nvalid counts the valid ones.  All blockDim.x threads call this;
 // o receives the query's K outputs.
 template <class ValueAt>
 __device__ __forceinline__ void topk_select(TopkShared &sh, unsigned nvalid, int n_iter, ValueAt value_at, int K,
                                             int offset, int32_t *o) {
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int tid = threadIdx.x, wid = tid >> 5;
   unsigned *hist = sh.hist;
   const bool all = nvalid <= (unsigned)K;
   int fs = 0;
@@ -98,38 +134,8 @@ __device__ __forceinline__ void topk_select(TopkShared &sh, unsigned nvalid, int
         }
       }
       __syncthreads();
-      if (wid == 0) {
-        // the digit holding the remain-th largest value: lane l scans digits 255-8l down to 248-8l
-        unsigned c[8], tot = 0;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          c[k] = hist[255 - 8 * lane - k];
-          tot += c[k];
-        }
-        unsigned incl = tot;
-#pragma unroll
-        for (int o2 = 1; o2 < 32; o2 <<= 1) {
-          const unsigned n = __shfl_up_sync(0xffffffffu, incl, o2);
-          if (lane >= o2) incl += n;
-        }
-        const unsigned excl = incl - tot, remain = sh.remain;
-        if (excl < remain && remain <= incl) {
-          unsigned above = excl;
-          int d = 255 - 8 * lane;
-          unsigned cd = 0;
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            d = 255 - 8 * lane - k;
-            cd = c[k];
-            if (above + cd >= remain) break;
-            above += cd;
-          }
-          sh.prefix = prefix | ((unsigned long long)d << shift);
-          sh.remain = remain - above;
-          sh.shift = shift;
-          if (cd == remain - above) sh.done = 1;  // every value with this prefix is taken
-        }
-      }
+      // the digit holding the remain-th largest value: lane l scans digits 255-8l down to 248-8l
+      if (wid == 0) radix_pick(sh, hist, shift);
       __syncthreads();
       if (sh.done) break;
     }

@@ -14,6 +14,8 @@ Distributions (the pages publish no data; these stand in for it):
   * window ring rows ~ N(0, 1) bf16 [B, W, hd] (callers pass them through the fp8 round trip)
   * candidate block mask: per query, of the causal blocks of cand_block positions, a seeded
     permutation keeps exactly ``keep`` of them (a fraction or a count).
+  * a kv source's compressor: kv and gate ~ N(0, 1/dim) f32 [hd, dim] (bf16 kv at ratio 1), index-key
+    projection ~ N(0, 1/hd) bf16 [index_hd, hd]; norms as above.
 """
 from dataclasses import dataclass, field, asdict
 import math
@@ -134,7 +136,34 @@ def f32_normal(shape, std, seed):
 
 # tensor ids for the seeds
 _IDS = dict(x=1, wq_a=2, wq_b=3, wkv=4, wo_a=5, wo_b=6, idx_wq_b=7, idx_wproj=8, sink=9, q_norm=10, kv_norm=11,
-            compress_kv=12, index_k=13, ring=14, cand=15)
+            compress_kv=12, index_k=13, ring=14, cand=15, comp_wkv=16, comp_wgate=17, comp_norm=18, idx_wk=19,
+            idx_k_norm=20)
+
+
+def compressor_weights(g, ratio, seed_base=1000, with_index_keys=True, norm_ones=False):
+    """A kv source's compressor weights: comp_wkv ~ N(0, 1/dim) [hd, dim] (f32 at ratio > 1, bf16 bits
+    at ratio 1), comp_wgate ~ N(0, 1/dim) f32 (ratio > 1), comp_norm, and the index-key projection
+    idx_wk ~ N(0, 1/hd) bf16 [index_hd, hd] with idx_k_norm.  Norm weights are 1, or bf16-valued
+    1 + 0.1 N(0, 1) stored f32."""
+    hd, dim = g.head_dim, g.dim
+    w = {}
+    if ratio > 1:
+        w["comp_wkv"] = f32_normal((hd, dim), 1.0 / math.sqrt(dim), seed_base + _IDS["comp_wkv"])
+        w["comp_wgate"] = f32_normal((hd, dim), 1.0 / math.sqrt(dim), seed_base + _IDS["comp_wgate"])
+    else:
+        w["comp_wkv"] = bf16_normal((hd, dim), 1.0 / math.sqrt(dim), seed_base + _IDS["comp_wkv"])
+
+    def norm(name, n):
+        if norm_ones:
+            return np.ones(n, np.float32)
+        t = 1.0 + 0.1 * torch.randn(n, generator=_gen(seed_base + _IDS[name]))
+        return t.to(torch.bfloat16).to(torch.float32).numpy().copy()
+
+    w["comp_norm"] = norm("comp_norm", hd)
+    if with_index_keys:
+        w["idx_wk"] = bf16_normal((g.index_hd, hd), 1.0 / math.sqrt(hd), seed_base + _IDS["idx_wk"])
+        w["idx_k_norm"] = norm("idx_k_norm", g.index_hd)
+    return w
 
 
 def weights(g: Geometry, with_indexer=True, seed_base=1000, norm_ones=True):

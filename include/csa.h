@@ -54,7 +54,7 @@ enum {
   CSA_ERR_NO_KV_SOURCE = -3,   /* ratio > 0 and no published latent cache ([attn_v41] "Invariants") */
   CSA_ERR_NO_SELECTION = -4,   /* a ratio > 0 layer that reuses the selection, and none is published */
   CSA_ERR_TOO_WIDE = -5,       /* selection wider than window + index_topk or 2048 ([attn_v41] "Invariants") */
-  CSA_ERR_UNSUPPORTED = -6,    /* kv-source (compressor) or candidate-source roles: not in this library */
+  CSA_ERR_UNSUPPORTED = -6,    /* a role or shape this library does not take */
   CSA_ERR_CUDA = -7,           /* a CUDA call failed */
   CSA_ERR_DEVICE_TIMEOUT = -8, /* a bounded device-side wait ran out (kernel returned early, output invalid) */
   CSA_ERR_NOMEM = -9           /* workspace allocation failed in csa_create */
@@ -87,7 +87,9 @@ typedef struct csa_role {
  * wq_a [q_rank, dim], wq_b [n_heads*head_dim, q_rank], wkv [head_dim, dim],
  * wo_a [groups*o_rank, gw], wo_b [dim, groups*o_rank], idx_wq_b [index_heads*index_hd, q_rank],
  * idx_wproj [index_heads, dim].  sink [n_heads], q_norm [q_rank], kv_norm [head_dim] are f32.
- * idx_* may be NULL unless role.is_index_source.
+ * idx_* may be NULL unless role.is_index_source.  A candidate source (an index source with
+ * role.is_candidate_source) also writes shared->candidates from its own scores, as
+ * csa_candidate_blocks with K = cfg.cand_topk_blocks, for the index sources after it.
  * The grouped wo_a may instead stay in fp8 ([atlas] Attention excerpt: the checkpoint's converter
  * dequantises it to bf16, and an fp8 grouped product would halve its memory): wo_a_fp8 uint8
  * [groups*o_rank, gw] holds e4m3 codes and wo_a_scale f32 [groups*o_rank/128 rounded up][gw/128
@@ -99,12 +101,28 @@ typedef struct csa_layer_weights {
   const csa_bf16 *wq_a, *wq_b, *wkv, *wo_a, *wo_b, *idx_wq_b, *idx_wproj;
   const uint8_t *wo_a_fp8;
   const float *wo_a_scale;
+  /* kv sources only ([attn_v41] CompressorWeightsGpu, IndexerWeightsGpu): comp_wkv [head_dim, dim],
+   * f32 at ratio > 1 and bf16 at ratio 1; comp_wgate f32 [head_dim, dim] at ratio > 1 (NULL at
+   * ratio 1); comp_norm f32 [head_dim].  idx_wk bf16 [index_hd, head_dim] and idx_k_norm f32
+   * [index_hd] produce the index keys (NULL: the kv source publishes no index keys). */
+  const void *comp_wkv;
+  const float *comp_wgate, *comp_norm;
+  const csa_bf16 *idx_wk;
+  const float *idx_k_norm;
 } csa_layer_weights;
 
 /* One layer's per-sequence state ([attn_v41] AttnV41LayerState): the window ring bf16
- * [max_batch][window][head_dim]; slot of position p is p mod window. */
+ * [max_batch][window][head_dim]; slot of position p is p mod window.  A kv source also holds the
+ * compressor's partial group, comp_kv and comp_score f32 [max_batch][comp_ratio][head_dim] (scores
+ * -inf for empty slots), and the caches it publishes: latent bf16 [max_batch][cache_rows][head_dim]
+ * and index_keys bf16 [max_batch][cache_rows][index_hd] (cache_rows >= max_seq / ratio).  Other
+ * layers leave these NULL / 0. */
 typedef struct csa_layer_state {
   csa_bf16 *window;
+  float *comp_kv, *comp_score;
+  int comp_ratio;
+  csa_bf16 *latent, *index_keys;
+  int cache_rows;
 } csa_layer_state;
 
 /* What source layers publish ([attn_v41] SharedV41), device buffers:
@@ -114,14 +132,14 @@ typedef struct csa_layer_state {
  *   topk_idxs    int32 [B*T][topk]: the selection, offset past the window rows, -1 = absent; an
  *                index-source layer writes it (has_topk becomes 1), a reuse layer reads it
  *   candidates   uint8 [B*T][cand_width], nonzero = block j / cand_block allowed (may be NULL
- *                unless the layer uses candidates) */
+ *                unless the layer uses candidates); the candidate source writes it */
 typedef struct csa_shared {
   const csa_bf16 *compress_kv;
   const csa_bf16 *index_k;
   int compress_len, compress_stride;
   int32_t *topk_idxs;
   int topk, has_topk;
-  const uint8_t *candidates;
+  uint8_t *candidates;
   int cand_width;
 } csa_shared;
 
@@ -159,7 +177,9 @@ CSA_API int csa_create(const csa_cfg *cfg, csa_ctx **out);
 /* Free a context and its workspaces (after synchronising the device).  NULL is a no-op. */
 CSA_API int csa_destroy(csa_ctx *ctx);
 
-/* Zero the window ring of `batch` sequences ([attn_v41] AttnV41LayerState::new), on `stream`. */
+/* Zero the window ring of `batch` sequences ([attn_v41] AttnV41LayerState::new), on `stream`; on a
+ * kv source's state also empty the compressor's partial group (kv 0, scores -inf: "the score state
+ * starts at -inf"). */
 CSA_API int csa_state_init(csa_ctx *ctx, csa_layer_state *state, int batch, csa_stream stream);
 
 /* One layer forward ([atlas] Attention.forward; [attn_v41] AttnV41::forward) for `batch` sequences
@@ -175,6 +195,24 @@ CSA_API int attn_v41_forward(csa_ctx *ctx, const csa_layer_weights *w, csa_layer
  * once the work is enqueued; out_host is valid after the stream is synchronised. */
 CSA_API int attn_v41_forward_host(csa_ctx *ctx, const csa_layer_weights *w, csa_layer_state *state, const csa_bf16 *x_host,
                           int batch, int T, int start_pos, csa_shared *shared, csa_bf16 *out_host, csa_stream stream);
+
+/* The compressor of a kv-source layer ([attn_v41] module description: the compressor pooling;
+ * CompressorWeightsGpu; AttnV41LayerState; SharedV41), for `batch` sequences of T tokens at
+ * start_pos (prefill at 0, or one decode token): k_p = x_p comp_wkv^T and s_p = x_p comp_wgate^T in
+ * f32 (at ratio 1, k_p = linear_bf16(x_p, comp_wkv) and no score) fill slot p mod ratio of the
+ * state's partial group; every group j the call closes (positions j*ratio .. j*ratio + ratio - 1) is
+ * pooled per feature with the softmax of its scores, z = sum_i e^{s_i} k_i / sum_i e^{s_i}, normed,
+ * y = bf16(RMSNorm(z) * comp_norm); with idx_wk its index key bf16(RMSNorm(linear_bf16(y, idx_wk)) *
+ * idx_k_norm) goes to row j of state->index_keys, and y with RoPE on its last rope_dim at position
+ * j * ratio and the fp8 round trip to row j of state->latent.  The pooling is a reading (the pages
+ * name the step but print no formula).  shared (may be NULL) then publishes the caches:
+ * compress_kv = latent, index_k = index_keys (when written), compress_stride = cache_rows,
+ * compress_len = max(compress_len, (start_pos + T) / ratio).  x bf16 [batch][T][dim] (16-byte
+ * aligned); w->role.ratio in 1..16, head_dim <= 1024 a multiple of 64, index_hd <= 256; y_dbg (may
+ * be NULL) bf16 [batch][cache_rows][head_dim] receives y.  attn_v41_forward runs this first on a kv
+ * source.  The context's workspace holds the f32 partial products. */
+CSA_API int csa_compress(csa_ctx *ctx, const csa_layer_weights *w, csa_layer_state *state, const csa_bf16 *x,
+                         int batch, int T, int start_pos, csa_shared *shared, csa_bf16 *y_dbg, csa_stream stream);
 
 /* Text of the calling thread's last error ("" if none). */
 CSA_API const char *attn_v41_last_error(void);
@@ -272,6 +310,18 @@ CSA_API int csa_kv_finish(const csa_bf16 *kv_in, csa_bf16 *kv_out, int B, int T,
 CSA_API int csa_index_scores(const csa_bf16 *qI, const float *wI, const csa_bf16 *KI, int B, int T, int start_pos, int Hi,
                      int dI, int Lstride, int compress_len, int ratio, const uint8_t *cand, int cand_width,
                      int cand_block, float *S, csa_stream stream);
+
+/* The candidate source's block mask ([attn_v41] module description: the candidate-source layer
+ * publishes a block-level candidate mask that later index sources apply; SharedV41 candidates;
+ * [atlas] config.json candidate_block_size, candidate_topk_blocks): per query t, block c (positions
+ * c*cand_block .. c*cand_block + cand_block - 1) scores the largest of its valid scores S[t][j]
+ * (j < floor((start_pos + t%T + 1) / ratio), j < compress_len), a block without a valid position
+ * is no candidate, and the K blocks of highest score (equal scores to the lower block, -0 == +0) get
+ * mask[t][c] = 1, every other column 0.  The block score is a reading (the pages print none).
+ * S f32 [B*T][Lstride] (this source's own scores, unmasked), mask uint8 [B*T][cand_width] with
+ * cand_width * cand_block >= min(compress_len, Lstride); K <= 2048, cand_width <= 25600. */
+CSA_API int csa_candidate_blocks(const float *S, int B, int T, int start_pos, int Lstride, int compress_len, int ratio,
+                                 int cand_block, int K, uint8_t *mask, int cand_width, csa_stream stream);
 
 /* Index top-k ([atlas] I_t = top_K over the valid scores; [attn_v41] selection offset past the
  * window rows, -1 = absent): per query, the K valid positions of highest score, equal scores to the

@@ -8,6 +8,10 @@ benchmark's ``cpu_baseline`` leg and reference arm may import it; the GPU librar
 two share no code.  bf16 tensors travel as ``uint16`` arrays of their bit patterns.
 :func:`dequant_fp8_blocks` (fp8 weight storage back to bf16) composes the C primitives in numpy.
 
+Parity unpinned: :func:`compress` (the kv source's compressor).  Its pooling formula is a reading
+(the pages give the weights, state and caches only); tests/test_oracle_compress.py pins what
+mathematics fixes, not agreement with the real model.
+
 The YaRN form of :func:`rope_table` follows the published method (the pages give its constants
 only).  Pinned are its classes (pairs with at least beta_fast turns over the original length keep
 their frequency, those with at most beta_slow turns run at frequency / factor, the others lie strictly
@@ -81,6 +85,12 @@ def lib():
         L.orc_sparse_attn.restype = I32
         L.orc_attn_forward.argtypes = [P, P, P, P, P, I32, I64, I64, P, P, I64, P, P, P]
         L.orc_attn_forward.restype = I32
+        L.orc_candidate_blocks.argtypes = [P, I64, I64, P, I32, I64, I32, I32, I32, P]
+        L.orc_candidate_blocks.restype = None
+        L.orc_compress.argtypes = [P, I32, P, P, P, P, I32, I64, I64, P, I64, P, P, I64, P, P]
+        L.orc_compress.restype = I32
+        L.orc_compress_state_init.argtypes = [P, P, I64]
+        L.orc_compress_state_init.restype = None
         L.orc_param_counts.argtypes = [P, I32, P]
         L.orc_param_counts.restype = None
         L.orc_n_idx.argtypes = [P, P]
@@ -264,6 +274,18 @@ def index_topk(S, K, pos, ratio, compress_len, cand=None, cand_block=1, offset=0
     return out
 
 
+def candidate_blocks(S, pos, ratio, compress_len, cand_block, cand_topk, cand_width):
+    """The candidate source's block mask (see orc_candidate_blocks): per query, the cand_topk blocks
+    of cand_block positions whose largest valid score is highest (ties to the lower block), as uint8
+    [n, cand_width].  S [n, L] f32 (invalid entries ignored by position)."""
+    S = _c(S, np.float32)
+    n, L = S.shape
+    pos = _c(pos, np.int32)
+    m = np.zeros((n, cand_width), np.uint8)
+    lib().orc_candidate_blocks(_p(S), n, L, _p(pos), ratio, compress_len, cand_block, cand_topk, cand_width, _p(m))
+    return m
+
+
 def sparse_attn(q, rows_a, rows_b, idx, sink, scale):
     """q [n, H, hd], rows_a [Na, hd], rows_b [Nb, hd] or None, idx [n, n_idx], sink [H] -> o [n, H, hd]."""
     q = _c(q, np.uint16)
@@ -392,6 +414,57 @@ def attn_forward(cfg, role, w, ring, x, start_pos, rope_tab, shared=None, tok_ma
     res = dict(out=out)
     res.update(dbg)
     return res
+
+
+class _CompWeights(ctypes.Structure):
+    _fields_ = [(n, P) for n in ("wkv_f32", "wgate", "wkv_bf16", "norm", "wk", "k_norm")]
+
+
+def compress_state(B, ratio, hd):
+    """A kv source's empty partial group: kv [B, ratio, hd] = 0, score = -inf (f32)."""
+    kv = np.empty((B, ratio, hd), np.float32)
+    sc = np.empty((B, ratio, hd), np.float32)
+    lib().orc_compress_state_init(_p(kv), _p(sc), kv.size)
+    return kv, sc
+
+
+def compress(cfg, ratio, w, st_kv, st_score, x, start_pos, rope_tab, Z, KI=None, compress_len=0, y_dbg=None):
+    """The kv source's compressor over x [B, T, dim] bf16 bits at start_pos (see orc_compress): updates
+    the partial group st_kv / st_score [B, ratio, hd] f32 and writes the closed groups' rows of the
+    latent cache Z [B, L, hd] and (with w["wk"]) the index keys KI [B, L, dI], both bf16 bits, in
+    place.  ``w`` maps wkv (f32 [hd, dim] at ratio > 1, bf16 bits at ratio 1), wgate (f32, ratio > 1),
+    norm (f32 [hd]), and optionally wk (bf16 bits [dI, hd]) and k_norm (f32 [dI]).  y_dbg ([B, L, hd]
+    bf16 bits, optional) receives the normed rows before RoPE and fp8.  Returns compress_len."""
+    x = _c(x, np.uint16)
+    B, T, dim = x.shape
+    c = _cfg_struct(cfg)
+    keep = []
+
+    def ptr(a, dtype):
+        if a is None:
+            return None
+        a = _c(a, dtype)
+        keep.append(a)
+        return a.ctypes.data
+
+    for a, dt in ((st_kv, np.float32), (st_score, np.float32), (Z, np.uint16)):
+        assert a.flags.c_contiguous and a.dtype == dt
+    if KI is not None:
+        assert KI.flags.c_contiguous and KI.dtype == np.uint16
+    if y_dbg is not None:
+        assert y_dbg.flags.c_contiguous and y_dbg.dtype == np.uint16
+    cw = _CompWeights(ptr(w["wkv"], np.float32) if ratio > 1 else None, ptr(w.get("wgate"), np.float32),
+                      ptr(w["wkv"], np.uint16) if ratio == 1 else None, ptr(w["norm"], np.float32),
+                      ptr(w.get("wk"), np.uint16), ptr(w.get("k_norm"), np.float32))
+    n = ctypes.c_int64(int(compress_len))
+    rope_tab = _c(rope_tab, np.float32)
+    rc = lib().orc_compress(ctypes.byref(c), int(ratio), ctypes.byref(cw), _p(st_kv), _p(st_score), _p(x), B, T,
+                            int(start_pos), _p(rope_tab), rope_tab.shape[0], _p(Z),
+                            None if KI is None else KI.ctypes.data, Z.shape[1], ctypes.byref(n),
+                            None if y_dbg is None else y_dbg.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle compress refused the call (code %d)" % rc)
+    return int(n.value)
 
 
 def num_threads():

@@ -28,6 +28,12 @@
  * RoPE table follows the published method, as the pages give its constants but not its formula: its
  * frequency classes by rotation count and the blend weight of every pair inside the ramp are checked
  * against ramp ends found by searching the rotation counts.
+ *
+ * Parity unpinned: orc_compress, the kv source's compressor.  The pages give its weights, state and
+ * caches but not its pooling formula, so the reading it follows (softmax-gated pooling of each closed
+ * group, RMSNorm, RoPE at the group's first position, the fp8 round trip) is checked only against
+ * what mathematics fixes (products, closed forms of the pooling, composition of pinned steps,
+ * complete-group publication, chunking invariance), not against the real model.
  */
 #include <math.h>
 #include <stdint.h>
@@ -618,6 +624,177 @@ int orc_attn_forward(const orc_cfg *c, const orc_role *role, const orc_weights *
   free(need_tok);
   free(need_kv);
   return rc;
+}
+
+/* The candidate source's block mask ([attn_v41] module description: the candidate-source layer
+ * publishes a block-level candidate mask that later index sources apply; SharedV41 candidates
+ * [queries][cand_width]; [atlas] config.json candidate_block_size, candidate_topk_blocks; the
+ * candidate-block selection runs as a top-k, like the index selection).  The pages give no block
+ * score; the reading taken here: block c of query t scores the largest of its valid positions'
+ * indexer scores S[t][j] (j in [c*cb, (c+1)*cb), j < floor((pos+1)/ratio), j < compress_len); a block
+ * with no valid position is not a candidate; the top cand_topk blocks by score (ties to the lower
+ * block; -0 == +0) are marked 1, the rest 0.  S [n_tok][Lstride] f32 (this source's own, unmasked),
+ * mask [n_tok][cand_width] uint8. */
+void orc_candidate_blocks(const float *S, int64_t n_tok, int64_t Lstride, const int32_t *pos, int ratio,
+                          int64_t compress_len, int cand_block, int cand_topk, int cand_width, uint8_t *mask) {
+  orc_cand *c = (orc_cand *)malloc(sizeof(orc_cand) * (size_t)(cand_width > 0 ? cand_width : 1));
+  for (int64_t t = 0; t < n_tok; ++t) {
+    int64_t limit = ((int64_t)pos[t] + 1) / ratio;
+    if (limit > compress_len) limit = compress_len;
+    int n = 0;
+    for (int b = 0; b < cand_width; ++b) {
+      float best = 0.0f;
+      int any = 0;
+      for (int64_t j = (int64_t)b * cand_block; j < (int64_t)(b + 1) * cand_block && j < limit; ++j) {
+        float v = S[t * Lstride + j];
+        if (!any || v > best) best = v;
+        any = 1;
+      }
+      if (any) {
+        c[n].s = best == 0.0f ? 0.0f : best; /* -0 -> +0 */
+        c[n].j = b;
+        ++n;
+      }
+    }
+    qsort(c, (size_t)n, sizeof(orc_cand), cand_cmp);
+    uint8_t *m = mask + t * cand_width;
+    for (int b = 0; b < cand_width; ++b) m[b] = 0;
+    for (int k = 0; k < n && k < cand_topk; ++k) m[c[k].j] = 1;
+  }
+  free(c);
+}
+
+/* ------------------------------------------------------------------------------------------------
+ * Compressor of a kv-source layer
+ * ----------------------------------------------------------------------------------------------*/
+
+/* Weights of the compressor ([attn_v41] CompressorWeightsGpu): at ratio > 1 kv and gate are f32
+ * [hd][dim]; at ratio 1 kv is bf16 [hd][dim] and there is no gate; norm is f32 [hd].  The index
+ * keys of a kv source that is also an index source come from wk bf16 [dI][hd] and k_norm f32 [dI]
+ * ([attn_v41] IndexerWeightsGpu); wk may be NULL (no index keys published). */
+typedef struct orc_comp_weights {
+  const float *wkv_f32;    /* ratio > 1 */
+  const float *wgate;      /* ratio > 1 */
+  const uint16_t *wkv_bf16; /* ratio 1 */
+  const float *norm;
+  const uint16_t *wk;
+  const float *k_norm;
+} orc_comp_weights;
+
+/* The compressor ([attn_v41] module description "the compressor pooling"; AttnV41LayerState: the
+ * partial group of f32 kv and score [ratio][hd], the score starting at -inf, the bf16 latent cache
+ * [max_seq/ratio][hd] and index-key cache [max_seq/ratio][dI]; SharedV41: compress_len, the number
+ * of groups written, only grows).  The pages give these shapes but not the pooling formula, so its
+ * parity against the real model is unpinned; the reading taken here, token by token in position
+ * order p = start_pos + t of each sequence:
+ *   k_p = x_p Wkv^T and s_p = x_p Wgate^T, each an f32 [hd] (sums exact in double, one rounding to
+ *     f32); at ratio 1 k_p = linear_bf16(x_p, Wkv) and there is no score;
+ *   they fill slot p mod ratio of the partial group;
+ *   when p closes group j = p / ratio ((p + 1) mod ratio == 0): per feature d, the group's rows are
+ *     pooled with softmax weights of their scores, z[d] = sum_i e^{s_i[d]} k_i[d] / sum_i e^{s_i[d]}
+ *     (at ratio 1, z = k_p), rounded to f32; y = RMSNorm(z) * norm (f32 arithmetic, bf16 result, as
+ *     every RMSNorm of the precision contract); the index key is RMSNorm(linear_bf16(y, wk)) * k_norm;
+ *     the latent row is y with RoPE on its last rd at the group's first position j * ratio, then the
+ *     fp8 round trip of the window rows ([ref-attn] act_quant_inplace); row j of both caches is
+ *     written, compress_len becomes at least j + 1, and the partial group restarts empty (scores
+ *     -inf, kv 0), so rows of an unfinished group are never published.
+ * st_kv, st_score: [B][ratio][hd]; Z [B][Lstride][hd], KI [B][Lstride][dI] (KI ignored without wk);
+ * y_dbg (NULL or [B][Lstride][hd]): the normed rows before RoPE and fp8. */
+int orc_compress(const orc_cfg *c, int ratio, const orc_comp_weights *w, float *st_kv, float *st_score,
+                 const uint16_t *x, int B, int64_t T, int64_t start_pos, const float *rope_tab, int64_t rope_rows,
+                 uint16_t *Z, uint16_t *KI, int64_t Lstride, int64_t *compress_len, uint16_t *y_dbg) {
+  const int hd = c->head_dim, rd = c->rope_dim, dim = c->dim, dI = c->index_hd;
+  if (ratio <= 0 || B <= 0 || T <= 0 || start_pos < 0 || !w || !w->norm) return ORC_ERR_ARG;
+  if (ratio > 1 && (!w->wkv_f32 || !w->wgate)) return ORC_ERR_ARG;
+  if (ratio == 1 && !w->wkv_bf16) return ORC_ERR_ARG;
+  if ((start_pos + T) / ratio > Lstride) return ORC_ERR_ARG;
+  double *z = (double *)malloc(sizeof(double) * (size_t)hd);
+  float *zf = (float *)malloc(sizeof(float) * (size_t)hd);
+  uint16_t *kb = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)hd);
+  uint16_t *y = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)hd);
+  uint16_t *kraw = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)(dI > 0 ? dI : 1));
+  for (int b = 0; b < B; ++b) {
+    float *skv = st_kv + (int64_t)b * ratio * hd, *ssc = st_score + (int64_t)b * ratio * hd;
+    for (int64_t t = 0; t < T; ++t) {
+      const int64_t p = start_pos + t;
+      const uint16_t *xr = x + ((int64_t)b * T + t) * dim;
+      const int slot = (int)(p % ratio);
+      if (ratio > 1) {
+        for (int d = 0; d < hd; ++d) {
+          double a = 0.0, g = 0.0;
+          for (int k = 0; k < dim; ++k) {
+            a += bfd(xr[k]) * (double)w->wkv_f32[(int64_t)d * dim + k];
+            g += bfd(xr[k]) * (double)w->wgate[(int64_t)d * dim + k];
+          }
+          skv[slot * hd + d] = (float)a;
+          ssc[slot * hd + d] = (float)g;
+        }
+      } else {
+        orc_linear_bf16(xr, 1, dim, dim, w->wkv_bf16, hd, dim, kb, hd);
+        for (int d = 0; d < hd; ++d) skv[d] = orc_bf16_to_f32(kb[d]);
+      }
+      if ((p + 1) % ratio) continue;
+      const int64_t j = p / ratio;
+      /* pooling of the closed group */
+      for (int d = 0; d < hd; ++d) {
+        if (ratio == 1) {
+          z[d] = skv[d];
+          continue;
+        }
+        double m = -INFINITY;
+        for (int i = 0; i < ratio; ++i)
+          if ((double)ssc[i * hd + d] > m) m = (double)ssc[i * hd + d];
+        double num = 0.0, den = 0.0;
+        for (int i = 0; i < ratio; ++i) {
+          double e = exp((double)ssc[i * hd + d] - m);
+          num += e * (double)skv[i * hd + d];
+          den += e;
+        }
+        z[d] = num / den;
+      }
+      /* RMSNorm of the f32 pooled row */
+      double ss = 0.0;
+      for (int d = 0; d < hd; ++d) {
+        zf[d] = (float)z[d];
+        ss += (double)zf[d] * (double)zf[d];
+      }
+      double rs = 1.0 / sqrt(ss / (double)hd + (double)c->eps);
+      for (int d = 0; d < hd; ++d) y[d] = orc_f32_to_bf16((float)((double)zf[d] * rs * (double)w->norm[d]));
+      if (y_dbg) memcpy(y_dbg + ((int64_t)b * Lstride + j) * hd, y, sizeof(uint16_t) * (size_t)hd);
+      /* index key */
+      if (w->wk && KI) {
+        orc_linear_bf16(y, 1, hd, hd, w->wk, dI, hd, kraw, dI);
+        orc_rmsnorm(kraw, 1, dI, w->k_norm, c->eps, KI + ((int64_t)b * Lstride + j) * dI);
+      }
+      /* latent row: RoPE at the group's first position, then the fp8 round trip */
+      uint16_t *zr = Z + ((int64_t)b * Lstride + j) * hd;
+      memcpy(zr, y, sizeof(uint16_t) * (size_t)hd);
+      int32_t gp = (int32_t)(j * ratio);
+      if (gp >= rope_rows) {
+        free(z), free(zf), free(kb), free(y), free(kraw);
+        return ORC_ERR_INDEX;
+      }
+      orc_apply_rotary(zr, 1, hd, rd, &gp, 1, rope_tab, rope_rows, 0);
+      orc_act_quant(zr, hd, NULL, NULL);
+      if (j + 1 > *compress_len) *compress_len = j + 1;
+      /* the partial group restarts empty */
+      for (int i = 0; i < ratio * hd; ++i) {
+        skv[i] = 0.0f;
+        ssc[i] = -INFINITY;
+      }
+    }
+  }
+  free(z), free(zf), free(kb), free(y), free(kraw);
+  return ORC_OK;
+}
+
+/* A kv source's partial group before its first token: kv 0, scores -inf ([attn_v41]
+ * AttnV41LayerState::new, "the score state starts at -inf"). */
+void orc_compress_state_init(float *st_kv, float *st_score, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) {
+    st_kv[i] = 0.0f;
+    st_score[i] = -INFINITY;
+  }
 }
 
 /* Element counts of the weights orc_attn_forward reads, in the order of the [atlas] parameter

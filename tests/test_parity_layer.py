@@ -286,9 +286,18 @@ def test_layer_refusals(csa):
     with pytest.raises(csa.CsaError) as e:
         ctx.forward(w, dict(ratio=2, is_index_source=0), ring, x, 0, shared=sh)
     assert e.value.code == -4
+    # a kv source without its compressor weights and state, a candidate source without a mask to
+    # write or that would apply one: argument errors, nothing launched
     with pytest.raises(csa.CsaError) as e:
         ctx.forward(w, dict(ratio=2, is_kv_source=1), ring, x, 0, shared=sh)
-    assert e.value.code == -6
+    assert e.value.code == -1
+    with pytest.raises(csa.CsaError) as e:
+        ctx.forward(w, dict(ratio=2, is_index_source=1, is_candidate_source=1), ring, x, 0, shared=sh)
+    assert e.value.code == -1
+    with pytest.raises(csa.CsaError) as e:
+        ctx.forward(w, dict(ratio=2, is_index_source=1, is_candidate_source=1, uses_candidates=1), ring, x, 0,
+                    shared=sh)
+    assert e.value.code == -1
     with pytest.raises(csa.CsaError) as e:
         ctx.forward(w, dict(ratio=0), ring, torch.zeros((1, 41, g.dim), dtype=torch.bfloat16, device="cuda"), 0)
     assert e.value.code == -2
@@ -430,3 +439,41 @@ def test_fp8_wo_a_layer(csa, orc):
                     candidates=shared["candidates"][b * T:(b + 1) * T])
         res = orc.attn_forward(gd, role, w, ring0[b:b + 1].copy(), x[b:b + 1], start, tab, sh_o)
         assert_close_bf16(got[b * T:(b + 1) * T], res["out"].reshape(-1, g.dim), what="fp8 wo_a layer out")
+
+
+@pytest.mark.parametrize("B,keep", [(2, 256), (64, 64), (5, 100), (3, 7)])
+def test_cluster_gather_topk_selection(csa, orc, B, keep):
+    """Long decode rows under a candidate mask (16384 latent keys at p = 65535, ratio 4, blocks of 64)
+    take the gathered scores and the top-k in one launch, a thread-block cluster selecting together.
+    Its published selection must equal, bit for bit, the two-kernel path's (debug scores requested)
+    and the oracle's top-k of those very scores -- from a mask keeping every block (the most keys a
+    cluster holds) down to one keeping fewer keys than K."""
+    g = Geometry(dim=128, n_heads=4, head_dim=64, rope_dim=16, q_rank=64, o_rank=32, groups=2, window=8,
+                 index_heads=32, index_hd=128, index_topk=512, cand_block=64, max_seq=65536, max_tokens=1,
+                 max_batch=B)
+    gd = g.as_dict()
+    T, start, L = 1, 65535, 16384
+    w = weights(g, with_indexer=True, norm_ones=False, seed_base=1400)
+    x = activations(g, B, T, seed_base=2500 + B)
+    Z, KI = latent_cache(g, B, L, seed_base=3400)
+    pos = positions(B, T, start)
+    cm = candidate_mask(B * T, pos, 4, L, g.cand_block, L // g.cand_block, keep, 99 + B)
+    ring0 = orc.act_quant(ring_rows(g, B))[0]
+    role = dict(ratio=4, is_index_source=1, uses_candidates=1)
+    ctx = csa.Context(gd)
+    wd = _dev_weights(w)
+    K = g.index_topk
+    sel_d = torch.full((B * T, K), -7, dtype=torch.int32, device="cuda")
+    sh = csa.Shared(to_dev(Z), to_dev(KI), L, sel_d, K, to_dev(cm))
+    ctx.forward(wd, role, to_dev(ring0), to_dev(x), start, shared=sh)
+    sel_fast = sel_d.clone()
+    dbg = _dbg(B * T, g, L, g.window + K)
+    ctx.forward(wd, role, to_dev(ring0), to_dev(x), start, shared=sh, debug=dbg)
+    torch.cuda.synchronize()
+    assert ctx.status() == 0
+    assert torch.equal(sel_fast, sel_d), "the cluster path changes the selection"
+    S = to_np(dbg["scores"])[:, :L].astype(np.float32)
+    S = np.where(np.isnan(S), -np.inf, S).astype(np.float32)
+    want = orc.index_topk(S, K, pos, 4, L, cm, g.cand_block, offset=g.window)
+    assert_same_selection(to_np(sel_fast), want)
+    ctx.close()
