@@ -644,6 +644,14 @@ int attn_v41_forward(csa_ctx *ctx, const csa_layer_weights *w, csa_layer_state *
   }
   if (ctx->trace != 2) ctx->n_stages = 0;
   ctx->launches = 0;
+  // while the stream is being captured, a traced stage's events become event-record nodes of the
+  // graph; outside a capture they are plain records
+  unsigned ev_flags = cudaEventRecordDefault;
+  if (ctx->trace) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+      ev_flags = cudaEventRecordExternal;
+  }
   // one traced stage: events around it when tracing is on (recorded as event nodes when the stream
   // is being captured, so a replayed graph times its stages too); counts the kernels it launches
 #define STAGE(call, what, kernels)                                                             \
@@ -652,11 +660,11 @@ int attn_v41_forward(csa_ctx *ctx, const csa_layer_weights *w, csa_layer_state *
     if (ctx->trace && ctx->n_stages < (int)ctx->stages.size()) {                               \
       st_ = &ctx->stages[ctx->n_stages++];                                                     \
       st_->name = what;                                                                        \
-      cudaEventRecordWithFlags(st_->a, s, cudaEventRecordExternal);                            \
+      cudaEventRecordWithFlags(st_->a, s, ev_flags);                                           \
     }                                                                                          \
     cudaError_t e_ = (call);                                                                   \
     if (e_ != cudaSuccess) return cuda_fail(e_, what);                                         \
-    if (st_) cudaEventRecordWithFlags(st_->b, s, cudaEventRecordExternal);                     \
+    if (st_) cudaEventRecordWithFlags(st_->b, s, ev_flags);                                    \
     ctx->launches += (kernels);                                                                \
   } while (0)
 #define STEP(call, what) STAGE(call, what, 1)

@@ -46,6 +46,10 @@ constexpr int BK = 64;  // one 128-byte swizzle atom of K
 #endif
 constexpr int ATOMS = CSA_GEMM_ATOMS;  // k-slices per pipeline stage: ATOMS * 128 contiguous bytes per weight row
 constexpr int kThreads = 192;
+// fp8 weights: four more warps (6-9) expand the weights beside the epilogue warps
+constexpr int kThreadsF8 = 320;
+template <bool kF8>
+constexpr int threads_of() { return kF8 ? kThreadsF8 : kThreads; }
 constexpr int kCounterInts = 65536;            // arrival counters at the head of the workspace
 constexpr size_t kCounterBytes = kCounterInts * sizeof(int);
 constexpr int kMaxContrib = 320;  // >= grid + 1 for any grid of one CTA per SM
@@ -130,22 +134,32 @@ __device__ __forceinline__ void seg_range(const Params &P, int s, int &ub, int &
   }
 }
 
-// fp8 weights: the 128 epilogue threads expand one stage's e4m3 weight slice (128 rows x 64 codes,
-// row-major, 64 bytes a row) into the bf16 operand the MMA reads (128 rows x 128 bytes, 128-byte
+// fp8 weights: one stage's e4m3 codes (128 rows x 128 codes, row-major, 128 bytes a row: two 64-wide
+// k-slices) are expanded into the two bf16 operands the MMA reads (each 128 rows x 128 bytes, 128-byte
 // swizzle: 16-byte chunk c of row r at r * 128 + ((c ^ (r % 8)) << 4)), each value times its tile's
-// scale: w = bf16(f32(e4m3) * scale) with one f32 rounding of the product (exact e4m3 -> f32), which is
-// the bf16 weight the converter of the pages' checkpoint would produce.  Thread t takes the 16-byte
-// code chunks t, t + 128, ... (contiguous per warp); row0 = the tile's first weight row, rows at or
-// past nrows (the ragged end) get scale 0.
+// scale: w = bf16(f32(e4m3) * scale) with one f32 rounding of the product (exact e4m3 -> f32), the
+// bf16 weight the converter of the pages' checkpoint produces.  Two groups of 128 threads share a
+// stage: group IT0 / 4 takes the 16-byte code chunks q = it * 128 + t for it = IT0 .. IT0 + 3
+// (contiguous per warp; chunk q is row q / 8, codes 16 (q % 8) ..).  row0 = the tile's first weight
+// row; rows at or past nrows (the ragged end) get scale 0.
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
-__device__ __forceinline__ void fp8_expand_stage(const uint8_t *raw, uint8_t *dst, const float *scale, int ld_scale,
-                                                 int row0, int nrows, int kcol, int t) {
+// The scale of a stage whose 128 rows lie in one 128-row scale block (every aligned tile), read ahead
+// of the stage's wait so that its latency hides behind the copy; 0 for a tile across two blocks.
+__device__ __forceinline__ float fp8_stage_scale(const float *scale, int ld_scale, int row0, int nrows, int kcol) {
+  const bool one = (row0 & 127) == 0 && row0 + 128 <= nrows;
+  return one ? __ldg(scale + (int64_t)(row0 >> 7) * ld_scale + kcol) : 0.f;
+}
+
+template <int IT0>
+__device__ __forceinline__ void fp8_expand_half(const uint8_t *raw, uint8_t *dst, const float *scale, int ld_scale,
+                                                int row0, int nrows, int kcol, int t, float sc0) {
+  const bool one = (row0 & 127) == 0 && row0 + 128 <= nrows;
 #pragma unroll
-  for (int it = 0; it < 4; ++it) {
-    const int q = it * 128 + t, r = q >> 2, part = q & 3;
+  for (int it = IT0; it < IT0 + 4; ++it) {
+    const int q = it * 128 + t, r = q >> 3, slice = (q >> 2) & 1, part = q & 3;
     const int gr = row0 + r;
-    const float sc = gr < nrows ? __ldg(scale + (int64_t)(gr >> 7) * ld_scale + kcol) : 0.f;
+    const float sc = one ? sc0 : (gr < nrows ? __ldg(scale + (int64_t)(gr >> 7) * ld_scale + kcol) : 0.f);
     const uint4 v = *reinterpret_cast<const uint4 *>(raw + q * 16);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
     uint32_t o[8];
@@ -159,7 +173,7 @@ __device__ __forceinline__ void fp8_expand_stage(const uint8_t *raw, uint8_t *ds
         o[2 * k + h] = *reinterpret_cast<const uint32_t *>(&b2);
       }
     }
-    uint8_t *rp = dst + r * 128;
+    uint8_t *rp = dst + slice * (BM * BK * 2) + r * 128;
     *reinterpret_cast<uint4 *>(rp + (((2 * part) ^ (r & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
     *reinterpret_cast<uint4 *>(rp + (((2 * part + 1) ^ (r & 7)) << 4)) = make_uint4(o[4], o[5], o[6], o[7]);
   }
@@ -168,17 +182,18 @@ __device__ __forceinline__ void fp8_expand_stage(const uint8_t *raw, uint8_t *ds
 // The product for few token tiles (decode) and split-K: each CTA one contiguous Stream-K range of
 // units (or one k-range of a tile).
 template <bool kF8>
-__global__ void __launch_bounds__(kThreads, 2) k_gemm_tc(const __grid_constant__ Params P) {
+__global__ void __launch_bounds__(threads_of<kF8>(), kF8 ? 1 : 2) k_gemm_tc(const __grid_constant__ Params P) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = tc::smem_u32(smem_raw);
   uint8_t *smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
   const int S = P.stages, BN = P.BN;
   const uint32_t a_atom = BM * BK * 2, b_atom = (uint32_t)BN * BK * 2;
-  const uint32_t a_bytes = ATOMS * a_atom, b_bytes = ATOMS * b_atom;
-  // kF8: a stage holds the fp8 codes (a8_bytes) and B; the expanded bf16 weights go to a ring of
-  // SC slots of a_bytes after the stages
-  constexpr uint32_t a8_bytes = BM * BK;
-  static_assert(!kF8 || ATOMS == 1, "fp8 weights take one k-slice a stage");
+  // k-slices a stage holds: fp8 weights take two, so that each code row of a stage is 128 bytes
+  constexpr int KS = kF8 ? 2 : ATOMS;
+  const uint32_t a_bytes = KS * a_atom, b_bytes = KS * b_atom;
+  // kF8: a stage holds the fp8 codes (a8_bytes: 128 rows x 128 codes) and B; the expanded bf16
+  // weights go to a ring of SC slots of a_bytes after the stages
+  constexpr uint32_t a8_bytes = BM * BK * KS;
   const uint32_t a_in = kF8 ? a8_bytes : a_bytes;  // bytes of A in a stage
   const uint32_t stage_bytes = a_in + b_bytes;
   const int SC = kF8 ? P.cstages : 0;
@@ -219,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemm_tc(const __grid_constant__
       tc::mbar_init(&empty[s], 1);
     }
     for (int c = 0; c < SC; ++c) {
-      tc::mbar_init(&cfull[c], 128);
+      tc::mbar_init(&cfull[c], 256);  // both converter groups
       tc::mbar_init(&cempty[c], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -264,9 +279,10 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemm_tc(const __grid_constant__
         uint8_t *sa = smem + stage * stage_bytes;
         tc::mbar_expect_tx(&full[stage], stage_bytes);
 #pragma unroll
-        for (int a = 0; a < ATOMS; ++a) {
-          const int k0 = (un.kb * ATOMS + a) * BK;
-          tc::tma_load_2d(sa + a * a_atom, &pr->tmA, &full[stage], k0, g * pr->N + tn * BM, pol_w);
+        for (int a = 0; a < KS; ++a) {
+          const int k0 = (un.kb * KS + a) * BK;
+          if (!kF8 || a == 0)  // (fp8: one box of 128 codes a row covers both slices)
+            tc::tma_load_2d(sa + a * a_atom, &pr->tmA, &full[stage], k0, g * pr->N + tn * BM, pol_w);
           tc::tma_load_2d(sa + a_in + a * b_atom, &pr->tmB, &full[stage], g * pr->Kg + k0, tm * BN, pol_x);
         }
         ++issued;
@@ -334,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemm_tc(const __grid_constant__
           const uint32_t sa = tc::smem_u32(smem + stage * stage_bytes);
           const uint32_t sa_w = kF8 ? tc::smem_u32(conv + cst * a_bytes) : sa;
 #pragma unroll
-          for (int a = 0; a < ATOMS; ++a) {
+          for (int a = 0; a < KS; ++a) {
             const uint64_t ad = tc::sdesc_sw128(sa_w + a * a_atom, 16, 1024);
             const uint64_t bd = tc::sdesc_sw128(sa + a_in + a * b_atom, 16, 1024);
 #pragma unroll
@@ -366,7 +382,41 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemm_tc(const __grid_constant__
       while (!tc::mbar_try_wait(drain, 0) && tc::global_ns() - t0 < tc::kWaitLimitNs) {
       }
     }
-  } else {
+  } else if (kF8 && warp >= 6) {
+    // ---------------------------------------------------------------- fp8 expansion (warps 6-9)
+    // the second half of every stage's codes, in unit order, beside the epilogue warps' first half
+    const int t = threadIdx.x - 192;
+    int rst = 0, cst = 0;
+    uint32_t rph = 0, cph = 0;
+    for (int sg = 0; sg < 1; ++sg) {
+      int ub, ue;
+      ub = u0;
+      ue = u1;
+      bool okc = true;
+      for (int v = ub; v < ue; ++v) {
+        const Unit un = decode_unit(P, v);
+        const Problem &pr = P.prob[un.p];
+        const int rest = un.tile / pr.tiles_m, tn = rest % pr.tiles_n, g = rest / pr.tiles_n;
+        const int row0 = g * pr.N + tn * BM, kcol = un.kb;
+        const float sc0 = fp8_stage_scale(pr.scale, pr.ld_scale, row0, pr.N * pr.groups, kcol);
+        if (!(okc = tc::mbar_wait(&full[rst], rph, abort_flag))) break;
+        if (!(okc = tc::mbar_wait(&cempty[cst], cph ^ 1u, abort_flag))) break;
+        fp8_expand_half<4>(smem + rst * stage_bytes, conv + cst * a_bytes, pr.scale, pr.ld_scale, row0,
+                           pr.N * pr.groups, kcol, t, sc0);
+        fence_proxy_async_smem();
+        tc::mbar_arrive(&cfull[cst]);
+        if (++rst == S) {
+          rst = 0;
+          rph ^= 1u;
+        }
+        if (++cst == SC) {
+          cst = 0;
+          cph ^= 1u;
+        }
+      }
+      if (!okc) break;
+    }
+  } else if (warp < 4) {
     // ---------------------------------------------------------------- epilogue (warps 0-3)
     const int row = warp * 32 + lane;  // feature within the tile
     int done[2] = {0, 0};
@@ -381,10 +431,12 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemm_tc(const __grid_constant__
     uint32_t rph = 0, cph = 0;
     auto convert_units = [&](int v0, int v1, const Problem &pr, int row0, int kb0) -> bool {
       for (int v = v0; v < v1; ++v) {
+        const int kcol = kb0 + v - v0;  // (a unit is one 128-wide scale column)
+        const float sc0 = fp8_stage_scale(pr.scale, pr.ld_scale, row0, pr.N * pr.groups, kcol);
         if (!tc::mbar_wait(&full[rst], rph, abort_flag)) return false;
         if (!tc::mbar_wait(&cempty[cst], cph ^ 1u, abort_flag)) return false;
-        fp8_expand_stage(smem + rst * stage_bytes, conv + cst * a_bytes, pr.scale, pr.ld_scale, row0,
-                         pr.N * pr.groups, ((kb0 + v - v0) * BK) >> 7, threadIdx.x);
+        fp8_expand_half<0>(smem + rst * stage_bytes, conv + cst * a_bytes, pr.scale, pr.ld_scale, row0,
+                           pr.N * pr.groups, kcol, threadIdx.x, sc0);
         fence_proxy_async_smem();
         tc::mbar_arrive(&cfull[cst]);
         if (++rst == S) {
@@ -545,18 +597,19 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemm_tc(const __grid_constant__
 // the whole tiles c, c + G, ... and then its Stream-K share of the tiles of the last, partial wave.
 // (A separate kernel: folding the segment loops into the one above measured slower at decode.)
 template <bool kF8>
-__global__ void __launch_bounds__(kThreads, 2) k_gemm_tc_waves(const __grid_constant__ Params P) {
+__global__ void __launch_bounds__(threads_of<kF8>(), kF8 ? 1 : 2) k_gemm_tc_waves(const __grid_constant__ Params P) {
   constexpr bool kWaves = true;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = tc::smem_u32(smem_raw);
   uint8_t *smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
   const int S = P.stages, BN = P.BN;
   const uint32_t a_atom = BM * BK * 2, b_atom = (uint32_t)BN * BK * 2;
-  const uint32_t a_bytes = ATOMS * a_atom, b_bytes = ATOMS * b_atom;
-  // kF8: a stage holds the fp8 codes (a8_bytes) and B; the expanded bf16 weights go to a ring of
-  // SC slots of a_bytes after the stages
-  constexpr uint32_t a8_bytes = BM * BK;
-  static_assert(!kF8 || ATOMS == 1, "fp8 weights take one k-slice a stage");
+  // k-slices a stage holds: fp8 weights take two, so that each code row of a stage is 128 bytes
+  constexpr int KS = kF8 ? 2 : ATOMS;
+  const uint32_t a_bytes = KS * a_atom, b_bytes = KS * b_atom;
+  // kF8: a stage holds the fp8 codes (a8_bytes: 128 rows x 128 codes) and B; the expanded bf16
+  // weights go to a ring of SC slots of a_bytes after the stages
+  constexpr uint32_t a8_bytes = BM * BK * KS;
   const uint32_t a_in = kF8 ? a8_bytes : a_bytes;  // bytes of A in a stage
   const uint32_t stage_bytes = a_in + b_bytes;
   const int SC = kF8 ? P.cstages : 0;
@@ -588,7 +641,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemm_tc_waves(const __grid_cons
       tc::mbar_init(&empty[s], 1);
     }
     for (int c = 0; c < SC; ++c) {
-      tc::mbar_init(&cfull[c], 128);
+      tc::mbar_init(&cfull[c], 256);  // both converter groups
       tc::mbar_init(&cempty[c], 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -641,9 +694,10 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemm_tc_waves(const __grid_cons
         uint8_t *sa = smem + stage * stage_bytes;
         tc::mbar_expect_tx(&full[stage], stage_bytes);
 #pragma unroll
-        for (int a = 0; a < ATOMS; ++a) {
-          const int k0 = (un.kb * ATOMS + a) * BK;
-          tc::tma_load_2d(sa + a * a_atom, &pr->tmA, &full[stage], k0, g * N + tn * BM, pa);
+        for (int a = 0; a < KS; ++a) {
+          const int k0 = (un.kb * KS + a) * BK;
+          if (!kF8 || a == 0)  // (fp8: one box of 128 codes a row covers both slices)
+            tc::tma_load_2d(sa + a * a_atom, &pr->tmA, &full[stage], k0, g * N + tn * BM, pa);
           tc::tma_load_2d(sa + a_in + a * b_atom, &pr->tmB, &full[stage], g * Kg + k0, tm * BN, pb);
         }
         ++issued;
@@ -724,7 +778,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemm_tc_waves(const __grid_cons
           const uint32_t sa = tc::smem_u32(smem + stage * stage_bytes);
           const uint32_t sa_w = kF8 ? tc::smem_u32(conv + cst * a_bytes) : sa;
 #pragma unroll
-          for (int a = 0; a < ATOMS; ++a) {
+          for (int a = 0; a < KS; ++a) {
             const uint64_t ad = tc::sdesc_sw128(sa_w + a * a_atom, 16, 1024);
             const uint64_t bd = tc::sdesc_sw128(sa + a_in + a * b_atom, 16, 1024);
 #pragma unroll
@@ -757,7 +811,40 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemm_tc_waves(const __grid_cons
       while (!tc::mbar_try_wait(drain, 0) && tc::global_ns() - t0 < tc::kWaitLimitNs) {
       }
     }
-  } else {
+  } else if (kF8 && warp >= 6) {
+    // ---------------------------------------------------------------- fp8 expansion (warps 6-9)
+    // the second half of every stage's codes, in unit order, beside the epilogue warps' first half
+    const int t = threadIdx.x - 192;
+    int rst = 0, cst = 0;
+    uint32_t rph = 0, cph = 0;
+    for (int sg = 0; sg < nseg; ++sg) {
+      int ub, ue;
+      seg_range<kWaves>(P, sg, ub, ue);
+      bool okc = true;
+      for (int v = ub; v < ue; ++v) {
+        const Unit un = decode_unit(P, v);
+        const Problem &pr = P.prob[un.p];
+        const int rest = un.tile / pr.tiles_m, tn = rest % pr.tiles_n, g = rest / pr.tiles_n;
+        const int row0 = g * pr.N + tn * BM, kcol = un.kb;
+        const float sc0 = fp8_stage_scale(pr.scale, pr.ld_scale, row0, pr.N * pr.groups, kcol);
+        if (!(okc = tc::mbar_wait(&full[rst], rph, abort_flag))) break;
+        if (!(okc = tc::mbar_wait(&cempty[cst], cph ^ 1u, abort_flag))) break;
+        fp8_expand_half<4>(smem + rst * stage_bytes, conv + cst * a_bytes, pr.scale, pr.ld_scale, row0,
+                           pr.N * pr.groups, kcol, t, sc0);
+        fence_proxy_async_smem();
+        tc::mbar_arrive(&cfull[cst]);
+        if (++rst == S) {
+          rst = 0;
+          rph ^= 1u;
+        }
+        if (++cst == SC) {
+          cst = 0;
+          cph ^= 1u;
+        }
+      }
+      if (!okc) break;
+    }
+  } else if (warp < 4) {
     // ---------------------------------------------------------------- epilogue (warps 0-3)
     const int row = warp * 32 + lane;  // feature within the tile
     int done[2] = {0, 0};
@@ -772,10 +859,12 @@ __global__ void __launch_bounds__(kThreads, 2) k_gemm_tc_waves(const __grid_cons
     uint32_t rph = 0, cph = 0;
     auto convert_units = [&](int v0, int v1, const Problem &pr, int row0, int kb0) -> bool {
       for (int v = v0; v < v1; ++v) {
+        const int kcol = kb0 + v - v0;  // (a unit is one 128-wide scale column)
+        const float sc0 = fp8_stage_scale(pr.scale, pr.ld_scale, row0, pr.N * pr.groups, kcol);
         if (!tc::mbar_wait(&full[rst], rph, abort_flag)) return false;
         if (!tc::mbar_wait(&cempty[cst], cph ^ 1u, abort_flag)) return false;
-        fp8_expand_stage(smem + rst * stage_bytes, conv + cst * a_bytes, pr.scale, pr.ld_scale, row0,
-                         pr.N * pr.groups, ((kb0 + v - v0) * BK) >> 7, threadIdx.x);
+        fp8_expand_half<0>(smem + rst * stage_bytes, conv + cst * a_bytes, pr.scale, pr.ld_scale, row0,
+                           pr.N * pr.groups, kcol, threadIdx.x, sc0);
         fence_proxy_async_smem();
         tc::mbar_arrive(&cfull[cst]);
         if (++rst == S) {
@@ -1017,8 +1106,8 @@ static void unify_policies(gemm::Params &P, int nprob) {
   }
 }
 
-int gemm_tc_bn(int M) {
-  if (M > 256) return 256;
+int gemm_tc_bn(int M, bool f8) {
+  if (M > 256) return f8 ? 128 : 256;  // (fp8 stages hold two k-slices: 256-token tiles leave room for one)
   int bn = (M + 15) / 16 * 16;
   return bn < 16 ? 16 : bn;
 }
@@ -1031,22 +1120,22 @@ cudaError_t launch_gemm_tc(const LinearProblem *probs, int nprob, float *ws, siz
   const int M = probs[0].M;
   Params P;
   memset(&P, 0, sizeof(P));
-  P.BN = gemm_tc_bn(M);
-  // fp8 weights: every problem of the launch, one k-slice a stage; the stages hold the codes (half
-  // the bytes of bf16, so twice the stages fit and twice the weight k-slices are in flight) and a ring
-  // of four expanded bf16 slices feeds the MMA
+  // fp8 weights: every problem of the launch; a stage holds two k-slices of codes (128 bytes a
+  // weight row, one TMA box) and of activations, and a ring of two expanded bf16 stages feeds the MMA
   const bool f8 = probs[0].W8 != nullptr;
   for (int i = 1; i < nprob; ++i)
     if ((probs[i].W8 != nullptr) != f8) return cudaErrorInvalidValue;
-  if (f8 && ATOMS != 1) return cudaErrorInvalidValue;
-  const int stage_bytes = f8 ? BM * BK + P.BN * BK * 2 : ATOMS * (BM * BK * 2 + P.BN * BK * 2);
+  P.BN = gemm_tc_bn(M, f8);
+  const int ks = f8 ? 2 : ATOMS;  // k-slices a stage (fp8: two, so each code row is 128 bytes)
+  const int stage_bytes = f8 ? 2 * (BM * BK + P.BN * BK * 2) : ATOMS * (BM * BK * 2 + P.BN * BK * 2);
   // one CTA per SM: two per SM (five stages each) measured slower at decode, because twice the CTAs
   // split each tile's k-range twice as often and the Stream-K fixups dominate
   const int per_sm = 1;
-  P.cstages = f8 ? 4 : 0;
-  const int conv_bytes = P.cstages * BM * BK * 2;
+  P.cstages = f8 ? 2 : 0;
+  const int conv_bytes = P.cstages * 2 * BM * BK * 2;
+  // (fp8: the shared memory left beside the expansion ring, short of the barriers and the 1 KB alignment)
   P.stages = per_sm == 2 ? std::min(5, (100 * 1024) / stage_bytes)
-                         : std::min(f8 ? 16 : 8, (200 * 1024 - conv_bytes) / stage_bytes);
+                         : std::min(8, ((f8 ? 222 : 200) * 1024 - conv_bytes) / stage_bytes);
   if (P.stages < 2) return cudaErrorInvalidValue;
   int units = 0, tiles = 0;
   for (int i = 0; i < nprob; ++i) {
@@ -1054,7 +1143,7 @@ cudaError_t launch_gemm_tc(const LinearProblem *probs, int nprob, float *ws, siz
     if (q.M != M) return cudaErrorInvalidValue;
     Problem &p = P.prob[i];
     if (f8) {
-      if (!q.w8_scale || !map_2d_u8(&p.tmA, q.W8, (uint64_t)q.K, (uint64_t)q.N * q.groups, (uint64_t)q.ldw, BK, BM))
+      if (!q.w8_scale || !map_2d_u8(&p.tmA, q.W8, (uint64_t)q.K, (uint64_t)q.N * q.groups, (uint64_t)q.ldw, 2 * BK, BM))
         return cudaErrorInvalidValue;
       p.scale = q.w8_scale;
       p.ld_scale = (q.K + 127) / 128;
@@ -1069,7 +1158,7 @@ cudaError_t launch_gemm_tc(const LinearProblem *probs, int nprob, float *ws, siz
     p.M = M;
     p.groups = q.groups;
     p.Kg = q.K;
-    p.kblocks = (q.K + BK * ATOMS - 1) / (BK * ATOMS);
+    p.kblocks = (q.K + BK * ks - 1) / (BK * ks);
     p.tiles_n = (q.N + BM - 1) / BM;
     p.tiles_m = (M + P.BN - 1) / P.BN;
     p.tiles = p.tiles_n * p.tiles_m * q.groups;
@@ -1146,12 +1235,12 @@ cudaError_t launch_gemm_tc(const LinearProblem *probs, int nprob, float *ws, siz
   }
   if (P.dp_waves > 0) {
     if (f8)
-      k_gemm_tc_waves<true><<<grid, kThreads, smem, s>>>(P);
+      k_gemm_tc_waves<true><<<grid, kThreadsF8, smem, s>>>(P);
     else
       k_gemm_tc_waves<false><<<grid, kThreads, smem, s>>>(P);
   } else {
     if (f8)
-      k_gemm_tc<true><<<grid, kThreads, smem, s>>>(P);
+      k_gemm_tc<true><<<grid, kThreadsF8, smem, s>>>(P);
     else
       k_gemm_tc<false><<<grid, kThreads, smem, s>>>(P);
   }
@@ -1160,7 +1249,7 @@ cudaError_t launch_gemm_tc(const LinearProblem *probs, int nprob, float *ws, siz
 
 int gemm_tc_split_count(const LinearProblem *probs, int nprob, int max_ctas, int max_S) {
   using namespace gemm;
-  const int BN = gemm_tc_bn(probs[0].M);
+  const int BN = gemm_tc_bn(probs[0].M, false);
   int tiles = 0;
   for (int i = 0; i < nprob; ++i)
     tiles += ((probs[i].N + BM - 1) / BM) * ((probs[i].M + BN - 1) / BN) * probs[i].groups;
@@ -1177,7 +1266,7 @@ cudaError_t launch_gemm_tc_split(const LinearProblem *probs, int nprob, int S, i
   const int M = probs[0].M, K = probs[0].K;
   Params P;
   memset(&P, 0, sizeof(P));
-  P.BN = gemm_tc_bn(M);
+  P.BN = gemm_tc_bn(M, false);
   const int stage_bytes = ATOMS * (BM * BK * 2 + P.BN * BK * 2);
   P.stages = std::min(8, (200 * 1024) / stage_bytes);
   if (P.stages < 2) return cudaErrorInvalidValue;
@@ -1232,7 +1321,7 @@ bool gemm_tc_supported(const LinearProblem &q) {
   if (q.W8) {  // fp8 weights: 16-byte aligned codes and rows
     if (((uintptr_t)q.W8 & 15) || q.ldw % 16 || q.K % 16 || !q.w8_scale || ((uintptr_t)q.x & 15) || q.ldx % 8)
       return false;
-    if (q.groups > 1 && q.K % gemm::BK) return false;
+    if (q.groups > 1 && q.K % (2 * gemm::BK)) return false;  // (a group's k-range is whole 128-wide units)
     return q.M > 0 && q.N > 0 && gemm::encoder() != nullptr;
   }
   if (((uintptr_t)q.x & 15) || ((uintptr_t)q.W & 15)) return false;

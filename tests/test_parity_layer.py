@@ -477,3 +477,29 @@ def test_cluster_gather_topk_selection(csa, orc, B, keep):
     want = orc.index_topk(S, K, pos, 4, L, cm, g.cand_block, offset=g.window)
     assert_same_selection(to_np(sel_fast), want)
     ctx.close()
+
+
+def test_stage_tracing_eager(csa, orc):
+    """Per-stage tracing outside a graph capture: each forward lists its stages (mode 1), or appends to
+    one list over several forwards (mode 2), with positive times; the output is unchanged by tracing."""
+    g = _small_geom()
+    w = weights(g, with_indexer=False)
+    x = activations(g, 1, 4)
+    ctx = csa.Context(g.as_dict())
+    wd = _dev_weights(w)
+    ring = torch.zeros((1, g.window, g.head_dim), dtype=torch.bfloat16, device="cuda")
+    ref = ctx.forward(wd, dict(ratio=0), ring.clone(), to_dev(x), 0)
+    ctx.trace(True)
+    out = ctx.forward(wd, dict(ratio=0), ring.clone(), to_dev(x), 0)
+    st = ctx.trace_read()
+    names = [n for n, _ in st]
+    assert "proj x" in names and "sparse_attn" in names and "wo_b" in names
+    assert all(ms > 0 for _, ms in st)
+    assert torch.equal(out, ref)
+    ctx.trace(True, append=True)
+    for _ in range(3):
+        ctx.forward(wd, dict(ratio=0), ring.clone(), to_dev(x), 0)
+    assert len(ctx.trace_read()) == 3 * len(st)
+    ctx.trace(False)
+    assert ctx.status() == 0
+    ctx.close()
