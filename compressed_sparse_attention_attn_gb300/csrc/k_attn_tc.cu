@@ -11,25 +11,27 @@
 // the accumulators in TMEM:
 //   S^T[r][h] = sum_d G[r][d] q[h][d]       (M = 128 rows, N = 64 heads, K = 512; G and q K-major)
 //   softmax step: a running maximum per head, raised only when a tile's maximum exceeds it by more
-//   than 2^8 (the accumulated output and sum are then rescaled), p = exp(S - m) rounded to bf16 in
+//   than 2^8 (the accumulated output and sums are then rescaled), p = exp(S - m) rounded to bf16 in
 //   shared memory (K-major [64][128]); eight warps share it (a TMEM lane quadrant and 32 heads each),
-//   and the maxima and sums over the rows are butterfly reductions that leave each lane one head
+//   the maxima over the rows are butterfly reductions that leave each lane one head, and each
+//   thread keeps its own f32 sums of p per head, reduced over the CTA once after the last tile
 //   O^T[d][h] += sum_r G[r][d] P[h][r]      (M = 4 x 128 features, N = 64, K = 128 rows; the same tile
 //                                            read as an MN-major operand)
 // When a query's tiles are split over several CTAs (decode: few queries; the split minimises tiles
-// per CTA x waves of CTAs), each CTA writes (m, l, O / l) for its tiles and a second, wide kernel
-// merges the shares in CTA order with the sink, which enters the denominator only:
+// per CTA x waves of CTAs), each CTA writes (m, l) and its share O / l, and a second, wide kernel (a
+// programmatic dependent) merges the shares in CTA order with the sink, which enters the
+// denominator only:
 //   O = sum_c e^{m_c - M} O_c / (e^{sink - M} + sum_c e^{m_c - M} l_c).
-// A query held by one CTA (prefill: many queries) is finished in place.  The result is staged in
-// shared memory and written with 16-byte stores as bf16, together with the inverse rotation of its
-// last rope_dim features at the query's position.
+// A query held by one CTA (prefill: many queries) is finished in place.  The result (or share) is
+// staged in shared memory and written with 16-byte stores as bf16, the result together with the
+// inverse rotation of its last rope_dim features at the query's position.
 //
-// Warps 0-7: softmax and staging of the result; warps 4-7 also run the index pass and the row
-// copies, each owning two 64-feature K-blocks of the tile, which it refills for the next tile as
-// soon as the P.V chunk reading them has completed; warp 8: TMEM allocation and MMA issue; all nine
-// warps write the result or the share.  Every mbarrier wait is time-bounded.
-#include "csa_internal.cuh"
-#include "tc_ptx.cuh"
+// Warps 0-7: softmax and the result or share; warps 4-7 also run the index pass and the row copies,
+// each owning two 64-feature K-blocks of the tile, which it refills for the next tile as soon as the
+// P.V chunk reading them has completed (the next tile's rows are prefetched into L2 once the current
+// one has landed); warp 8: TMEM allocation and MMA issue; all nine warps write the result or share.
+// Every mbarrier wait is time-bounded.
+#include "attn_common.cuh"
 
 namespace csa {
 
@@ -39,9 +41,6 @@ bool tma_map_2d_bf16(CUtensorMap *m, const void *base, uint64_t inner, uint64_t 
 
 namespace attn {
 
-constexpr int HD = 512;       // head_dim this kernel serves
-constexpr int KB = HD / 64;   // 64-feature K-blocks
-constexpr int TILE = 128;     // entries per tile
 constexpr int HG = 64;        // heads per CTA
 constexpr int kThreads = 288;
 constexpr int kMaxTiles = 6;  // index lists up to 768 entries
@@ -71,103 +70,6 @@ struct Params {
   bf16 *part_o;     // [NT][nsplit][H][512]  O_c / l_c of each split
   float *part_ml;   // [NT][nsplit][H][2]    (m_c, l_c), log2 domain
 };
-
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0) : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-__device__ __forceinline__ void tma_load_2d_nohint(uint32_t dst, const CUtensorMap *tm, uint64_t *bar, int c0, int c1) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-      "l"((uint64_t)tm), "r"(tc::smem_u32(bar)), "r"(c0), "r"(c1)
-      : "memory");
-}
-__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
-      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-      : "memory");
-}
-__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
-// 32 lanes x 32 consecutive columns, then the wait (the registers are operands of the wait)
-__device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  tc::tmem_ld32(taddr, r);
-  asm volatile("tcgen05.wait::ld.sync.aligned;"
-               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
-                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]),
-                 "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
-                 "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
-               :
-               : "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// Reduce v[h] (h < 32) over the 32 lanes of the warp for max or sum; lane l ends with head l.
-template <bool kMax>
-__device__ __forceinline__ float warp_reduce_32(const float (&v)[32], int lane) {
-  auto op = [](float a, float b) { return kMax ? fmaxf(a, b) : a + b; };
-  float b[16], c[8], d[4], e[2];
-  bool up = (lane & 16) != 0;
-#pragma unroll
-  for (int j = 0; j < 16; ++j) b[j] = op(up ? v[j + 16] : v[j], __shfl_xor_sync(0xffffffffu, up ? v[j] : v[j + 16], 16));
-  up = (lane & 8) != 0;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) c[j] = op(up ? b[j + 8] : b[j], __shfl_xor_sync(0xffffffffu, up ? b[j] : b[j + 8], 8));
-  up = (lane & 4) != 0;
-#pragma unroll
-  for (int j = 0; j < 4; ++j) d[j] = op(up ? c[j + 4] : c[j], __shfl_xor_sync(0xffffffffu, up ? c[j] : c[j + 4], 4));
-  up = (lane & 2) != 0;
-#pragma unroll
-  for (int j = 0; j < 2; ++j) e[j] = op(up ? d[j + 2] : d[j], __shfl_xor_sync(0xffffffffu, up ? d[j] : d[j + 2], 2));
-  up = (lane & 1) != 0;
-  return op(up ? e[1] : e[0], __shfl_xor_sync(0xffffffffu, up ? e[0] : e[1], 1));
-}
-
-// 16 floats from shared memory (16-byte aligned) into registers
-__device__ __forceinline__ void lds16(float (&d)[16], const float *src) {
-#pragma unroll
-  for (int k = 0; k < 16; k += 4) *reinterpret_cast<float4 *>(d + k) = *reinterpret_cast<const float4 *>(src + k);
-}
-
-// bf16 of the inverse rotation of the pair (x0, x1) (both already bf16 values) at table entry cs
-__device__ __forceinline__ void unrotate(float x0, float x1, float2 cs, float &re, float &im) {
-  const float sn = -cs.y;
-  re = __fsub_rn(__fmul_rn(x0, cs.x), __fmul_rn(x1, sn));
-  im = __fadd_rn(__fmul_rn(x0, sn), __fmul_rn(x1, cs.x));
-}
-
-// Write the bf16 vector ob (features d0 .. d0+7 of one head, element offset off) to o, and its
-// inverse rotation to o_rot: pairs at or past `tail` turn back by their angle at the query's
-// position (tp: that position's row of the cos/sin table), the others are copied.
-__device__ __forceinline__ void store_out(bf16 *o, bf16 *o_rot, int64_t off, int d0, int tail, const float2 *tp,
-                                          uint4 ob) {
-  if (o) *reinterpret_cast<uint4 *>(o + off) = ob;
-  if (o_rot) {
-    uint4 orr = ob;
-    if (d0 >= tail) {
-      const float4 c01 = *reinterpret_cast<const float4 *>(tp + ((d0 - tail) >> 1));
-      const float4 c23 = *reinterpret_cast<const float4 *>(tp + ((d0 - tail) >> 1) + 2);
-      const float2 cs[4] = {make_float2(c01.x, c01.y), make_float2(c01.z, c01.w), make_float2(c23.x, c23.y),
-                            make_float2(c23.z, c23.w)};
-      const bf16 *xb = reinterpret_cast<const bf16 *>(&ob);
-      bf16 *yb = reinterpret_cast<bf16 *>(&orr);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float re, im;
-        unrotate(__bfloat162float(xb[2 * q]), __bfloat162float(xb[2 * q + 1]), cs[q], re, im);
-        yb[2 * q] = __float2bfloat16_rn(re);
-        yb[2 * q + 1] = __float2bfloat16_rn(im);
-      }
-    }
-    *reinterpret_cast<uint4 *>(o_rot + off) = orr;
-  }
-}
 
 struct Smem {
   static constexpr size_t g = 0;                                         // KB x 16 KiB: one tile; output staging
@@ -201,7 +103,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
            *sm_bar = bars + 11, *drain = bars + 12, *q_ready = bars + 13;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::misc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-  int *s_rescale = const_cast<int *>(abort_flag) + 1;
+  int *s_rescale = const_cast<int *>(abort_flag) + 1;  // [2]: by tile parity
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t row = blockIdx.x;  // query b*T + t
@@ -222,7 +124,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
     tc::mbar_init(q_ready, 256);
     tc::mbar_init(drain, 1);
     *abort_flag = 0;
-    *s_rescale = 0;
+    s_rescale[0] = s_rescale[1] = 0;
     tc::fence_barrier_init();
     // q of this query's head group, independent of the selection
     tc::prefetch_tmap(&P.tm_q);
@@ -365,10 +267,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
       tc::mbar_arrive(sm_bar);
       return tc::mbar_wait(sm_bar, (sm_uses++) & 1u, abort_flag);
     };
-    if (tid < HG) {
-      m_sm[tid] = -INFINITY;
-      l_sm[tid] = 0.f;
-    }
+    if (tid < HG) m_sm[tid] = -INFINITY;
+    // this thread's sums of p over its rows, per head (reduced over the CTA at the end)
+    float lsum[32];
+#pragma unroll
+    for (int h = 0; h < 32; ++h) lsum[h] = 0.f;
     // RoPE on q's last rd features, in place in the swizzled K-blocks: one 16-byte chunk (four
     // adjacent pairs) of one head per unit, at most two units per thread; the same f32 arithmetic
     // as the separate pass.  The angles are read while q is still in flight.
@@ -422,6 +325,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
         cp_async_wait_all();
         fence_proxy_async();
         tc::mbar_arrive(&g_full[lw]);
+        // the next tile's segments of this warp's K-blocks on their way to L2 while this one is used
+        int nx = i + 1;
+        while (nx < nk && !tile_ok(nx)) ++nx;
+        if (nx < nk) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const bf16 *pr = src_list[nx * TILE + lane + 32 * k];
+            if (pr) {
+              asm volatile("prefetch.global.L2 [%0];" ::"l"(pr + 128 * lw));
+              asm volatile("prefetch.global.L2 [%0];" ::"l"(pr + 128 * lw + 64));
+            }
+          }
+        }
       }
       if (!(ok = tc::mbar_wait(s_full, (uint32_t)(n & 1), abort_flag))) break;
       tc::tc_fence_after();
@@ -439,13 +355,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
         if (tmax > m_sm[tid] + 8.0f) {  // keep exp2(s - m) below 2^8; rescale what has accumulated
           a = exp2f(m_sm[tid] - tmax);
           m_sm[tid] = tmax;
-          l_sm[tid] *= a;
-          if (n > 0) *s_rescale = 1;
+          if (n > 0) s_rescale[n & 1] = 1;
         }
         alpha_sm[tid] = a;
+        if (tid == 0) s_rescale[(n + 1) & 1] = 0;  // the previous tile's flag, read by all by now
       }
       if (!(ok = sm_sync())) break;
-      if (*s_rescale) {
+      if (s_rescale[n & 1]) {
         // the previous tile's product has completed: its commit released this tile's rows
 #pragma unroll 1
         for (int c = 0; c < KB / 2; ++c) {
@@ -463,6 +379,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
           }
         }
         tmem_st_wait();
+#pragma unroll
+        for (int h0 = 0; h0 < 32; h0 += 16) {
+          float av[16];
+          lds16(av, alpha_sm + hh + h0);
+#pragma unroll
+          for (int k = 0; k < 16; ++k) lsum[h0 + k] *= av[k];
+        }
       }
       uint8_t *prow = sP + (r / 64) * HG * 128;
       const int rc = (r % 64) / 8, ro = (r % 8) * 2;
@@ -474,21 +397,21 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
         for (int k = 0; k < 16; ++k) {
           const int h = hh + h0 + k;
           s[h0 + k] = exp2f(s[h0 + k] - mv[k]);  // 0 for masked rows
+          lsum[h0 + k] += s[h0 + k];
           *reinterpret_cast<bf16 *>(prow + h * 128 + ((rc ^ (h & 7)) << 4) + ro) = __float2bfloat16_rn(s[h0 + k]);
         }
       }
       fence_proxy_async();
       tc::tc_fence_before();
       tc::mbar_arrive(p_full);
-      red_sum[quad * HG + hh + lane] = warp_reduce_32<false>(s, lane);
-      if (!(ok = sm_sync())) break;
-      if (tid < HG) {
-        l_sm[tid] += (red_sum[tid] + red_sum[HG + tid]) + (red_sum[2 * HG + tid] + red_sum[3 * HG + tid]);
-        if (tid == 0) *s_rescale = 0;
-      }
       ++n;
     }
     if (loader) cp_async_wait_all();
+    // l per head: this thread's sums over the warp, then over the four lane quadrants
+    red_sum[quad * HG + hh + lane] = warp_reduce_32<false>(lsum, lane);
+    if (ok) ok = sm_sync();
+    if (ok && tid < HG)
+      l_sm[tid] = (red_sum[tid] + red_sum[HG + tid]) + (red_sum[2 * HG + tid] + red_sum[3 * HG + tid]);
     if (ok && nmine > 0) ok = tc::mbar_wait(&pv_done[3], (uint32_t)((nmine - 1) & 1), abort_flag);
     if (ok && tid < HG) {
       if (single) {  // finish in place: the sink joins the denominator
@@ -554,9 +477,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
 
 // Merge of the split shares: block (query, 8 heads), one warp per head, two 16-byte vectors per
 // thread.  The weights e^{m_c - M} l_c / den put each share O_c / l_c back on the common scale, with
-// the sink in den; every thread forms its head's weights itself (no barrier), after loading the
-// weights' inputs and its vectors of every share at once, and shares of CTAs that found nothing
-// (l_c = 0) weigh 0 and are skipped.
+// the sink in den; every thread forms its head's weights itself (no barrier).  The (m, l) of every
+// share are read first, and only the shares of CTAs that found something (l > 0; the others never
+// wrote theirs) after them.
 constexpr int kCombHeads = 8;
 constexpr int kCombThreads = 256;
 struct CombineParams {
@@ -573,34 +496,41 @@ __global__ void __launch_bounds__(kCombThreads) k_attn_combine(const __grid_cons
   const int64_t row = blockIdx.x;
   const int h0 = blockIdx.y * kCombHeads, tid = threadIdx.x;
   const int t = (int)(row % C.T);
-  const float2 *tp = C.o_rot ? reinterpret_cast<const float2 *>(C.tab) + (int64_t)(C.start_pos + t) * (C.rd >> 1)
-                             : nullptr;
   constexpr int kPer = kCombHeads * (HD / 8) / kCombThreads;  // consecutive vectors per thread
   static_assert((HD / 8) % kPer == 0, "a thread's vectors belong to one head");
   const int h = h0 + (tid * kPer) / (HD / 8);
-  // this head's weights e^{m_c - M} l_c / den, computed by each of its threads (same addresses)
+  const int dv = ((tid * kPer) % (HD / 8)) * 8;  // this thread's first feature
+  // what does not depend on the attention kernel, before the wait: the sink term and the angles
   const float s2 = C.sink[h] * 1.4426950408889634f;
+  const int tail = HD - C.rd;
+  const float2 *tp = C.o_rot ? reinterpret_cast<const float2 *>(C.tab) + (int64_t)(C.start_pos + t) * (C.rd >> 1)
+                             : nullptr;
+  float4 cs[kPer][2];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int d0 = dv + 8 * k;
+    if (tp && d0 >= tail) {
+      cs[k][0] = *reinterpret_cast<const float4 *>(tp + ((d0 - tail) >> 1));
+      cs[k][1] = *reinterpret_cast<const float4 *>(tp + ((d0 - tail) >> 1) + 2);
+    }
+  }
   // (a programmatic dependent of the attention kernel: the shares are read after this wait)
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  // every share's (m, l) and vectors in flight together; shares of CTAs that found nothing (l = 0,
-  // their buffers never written) are read but never used
   float2 ml[kMaxTiles];
-  uint4 u[kPer][kMaxTiles];
 #pragma unroll
   for (int c = 0; c < kMaxTiles; ++c) {
     ml[c] = make_float2(-INFINITY, 0.f);
     if (c < C.nsplit) ml[c] = __ldcg(reinterpret_cast<const float2 *>(C.part_ml + ((row * C.nsplit + c) * C.H + h) * 2));
   }
+  uint4 u[kPer][kMaxTiles];
 #pragma unroll
-  for (int k = 0; k < kPer; ++k) {
-    const int d0 = ((tid * kPer + k) % (HD / 8)) * 8;
+  for (int c = 0; c < kMaxTiles; ++c)
 #pragma unroll
-    for (int c = 0; c < kMaxTiles; ++c) {
+    for (int k = 0; k < kPer; ++k) {
       u[k][c] = make_uint4(0u, 0u, 0u, 0u);
-      if (c < C.nsplit)
-        u[k][c] = __ldcg(reinterpret_cast<const uint4 *>(C.part_o + ((row * C.nsplit + c) * C.H + h) * (int64_t)HD + d0));
+      if (ml[c].y > 0.f)
+        u[k][c] = __ldcg(reinterpret_cast<const uint4 *>(C.part_o + ((row * C.nsplit + c) * C.H + h) * (int64_t)HD + dv + 8 * k));
     }
-  }
   // this head's weights e^{m_c - M} l_c / den
   float M = s2;
 #pragma unroll
@@ -615,7 +545,7 @@ __global__ void __launch_bounds__(kCombThreads) k_attn_combine(const __grid_cons
   const float inv = 1.0f / den;
 #pragma unroll
   for (int k = 0; k < kPer; ++k) {
-    const int d0 = ((tid * kPer + k) % (HD / 8)) * 8;
+    const int d0 = dv + 8 * k;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int c = 0; c < kMaxTiles; ++c) {
@@ -632,7 +562,25 @@ __global__ void __launch_bounds__(kCombThreads) k_attn_combine(const __grid_cons
     __nv_bfloat162 *po = reinterpret_cast<__nv_bfloat162 *>(&ob);
 #pragma unroll
     for (int q = 0; q < 4; ++q) po[q] = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
-    store_out(C.o, C.o_rot, (row * C.H + h) * (int64_t)HD + d0, d0, HD - C.rd, tp, ob);
+    const int64_t off = (row * C.H + h) * (int64_t)HD + d0;
+    if (C.o) *reinterpret_cast<uint4 *>(C.o + off) = ob;
+    if (C.o_rot) {
+      uint4 orr = ob;
+      if (d0 >= tail) {
+        const float2 c2[4] = {make_float2(cs[k][0].x, cs[k][0].y), make_float2(cs[k][0].z, cs[k][0].w),
+                              make_float2(cs[k][1].x, cs[k][1].y), make_float2(cs[k][1].z, cs[k][1].w)};
+        const bf16 *xb = reinterpret_cast<const bf16 *>(&ob);
+        bf16 *yb = reinterpret_cast<bf16 *>(&orr);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float re, im;
+          unrotate(__bfloat162float(xb[2 * q]), __bfloat162float(xb[2 * q + 1]), c2[q], re, im);
+          yb[2 * q] = __float2bfloat16_rn(re);
+          yb[2 * q + 1] = __float2bfloat16_rn(im);
+        }
+      }
+      *reinterpret_cast<uint4 *>(C.o_rot + off) = orr;
+    }
   }
 }
 
