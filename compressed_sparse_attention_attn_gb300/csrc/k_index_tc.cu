@@ -319,44 +319,54 @@ __global__ void __launch_bounds__(kThreads) k_index_scores_gather_tc(const __gri
 // ---- gathered scores + top-k across a cluster (long decode rows) ---------------------------------
 // The gathered variant's work for one query split over a thread-block cluster of P CTAs: CTA c takes
 // the contiguous run of kept unit pairs [c np / P, (c+1) np / P), so the CTAs' ranges are in
-// ascending position.  Each keeps its keys' scores in shared memory as the top-k's 64-bit values
-// (0 where a key is not valid), and the cluster then selects together: the counts and, per radix
-// pass, the 256-bin histograms are read from every CTA through distributed shared memory, every CTA
-// takes the same digit, and each writes its taken positions in ascending order at the offset of the
-// CTAs before it.  The scores never go to global memory and the top-k needs no launch of its own.
-constexpr int kFuseBufs = 2;
-constexpr int kFuseVals = 4096;  // values a CTA keeps (its pairs x 128 keys)
+// ascending position.  Within a CTA the work is a pipeline: warp 4 copies the pairs' keys by TMA into
+// a ring of NB 32 KiB slots as far ahead as the ring allows, warp 5 issues each pair's MMA chain into
+// one of two TMEM accumulators as soon as its keys have landed (the slot is free again when the chain
+// completes), and warps 0-3 turn each accumulator into scores while the next pair's chain runs.  Each
+// CTA keeps its keys' scores in shared memory as 32-bit order keys with a validity bit (the position
+// of entry i follows from the unit list), and the cluster then selects together: the counts and, per
+// radix pass, the 256-bin histograms are read from every CTA through distributed shared memory,
+// every CTA takes the same digit, and each writes its taken positions in ascending order at the
+// offset of the CTAs before it.  The scores never go to global memory and the top-k needs no launch
+// of its own.
+constexpr int kGtThreads = 192;   // warps 0-3: scores; warp 4: key copies; warp 5: TMEM and MMA
+constexpr int kGtMaxBufs = 6;     // key slots
+constexpr int kGtMaxKeys = 8192;  // keys a CTA holds (its pairs x 128)
+constexpr uint32_t kGtSlot = TILE * 128 * 2;  // a pair: two 64-column halves of 128 keys
 
 struct GatherTopkParams {
   CUtensorMap tm_k;  // K^I [B*Lstride][128], box {64, 64}
   CUtensorMap tm_q;  // Q^I [B*Hi][128], box {64, Hi}
   const float *wI;   // [B][Hi]
   int Hi, Lstride, compress_len, ratio, start_pos, P, max_units;
+  int nbufs, cap_keys;  // key slots; keys a CTA can hold (a multiple of 128)
   const uint8_t *cand;
   int cand_width, cand_block, K, offset;
   int32_t *out;  // [B][K]
   int *status;
 };
 
-__global__ void __launch_bounds__(kThreads) k_index_gather_topk_tc(const __grid_constant__ GatherTopkParams P) {
+__global__ void __launch_bounds__(kGtThreads) k_index_gather_topk_tc(const __grid_constant__ GatherTopkParams P) {
   // the attention after this kernel may start its set-up now (it waits for this grid before it reads
   // the selection)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = tc::smem_u32(smem_raw);
   uint8_t *smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
-  const int N = P.Hi;
-  constexpr uint32_t k_buf = TILE * 128 * 2;  // a pair: two 64-column halves of 128 keys
+  const int N = P.Hi, NB = P.nbufs;
   const uint32_t q_half = (uint32_t)N * 128;
-  uint8_t *sk = smem, *sq = smem + kFuseBufs * k_buf;
-  float *w_s = reinterpret_cast<float *>(sq + 2 * q_half);                              // [Hi]
-  unsigned long long *vals = reinterpret_cast<unsigned long long *>(w_s + kMaxN);       // [kFuseVals]
-  unsigned *hists = reinterpret_cast<unsigned *>(vals + kFuseVals);                     // [2][256] per pass
-  unsigned *xchg = hists + 512;                                                         // [2]: count, taken
-  int *units = reinterpret_cast<int *>(xchg + 2);                                       // [max_units]
+  uint8_t *sk = smem, *sq = smem + NB * kGtSlot;
+  float *w_s = reinterpret_cast<float *>(sq + 2 * q_half);      // [Hi]
+  uint32_t *keys = reinterpret_cast<uint32_t *>(w_s + kMaxN);   // [cap_keys] order keys
+  uint32_t *vmask = keys + P.cap_keys;                          // [cap_keys / 32] validity bits
+  unsigned *hists = vmask + P.cap_keys / 32;                    // [2][256] per pass
+  unsigned *xchg = hists + 512;  // [8]: count, taken, -, -, then the least and the largest value (u64)
+  unsigned long long *xval = reinterpret_cast<unsigned long long *>(xchg + 4);
+  int *units = reinterpret_cast<int *>(xchg + 8);               // [max_units]
   uint64_t *bars = reinterpret_cast<uint64_t *>(units + ((P.max_units + 1) & ~1));
-  uint64_t *full = bars, *done = bars + kFuseBufs, *qbar = bars + 2 * kFuseBufs;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(qbar + 1);
+  uint64_t *full = bars, *sfree = bars + NB, *done = bars + 2 * NB, *accfree = done + 2, *qbar = accfree + 2,
+           *drain = qbar + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   int *s_nunits = const_cast<int *>(abort_flag) + 1;
   __shared__ TopkShared sh;
@@ -366,11 +376,19 @@ __global__ void __launch_bounds__(kThreads) k_index_gather_topk_tc(const __grid_
   const int b = blockIdx.y;
   const int limit = min((P.start_pos + 1) / P.ratio, P.compress_len);
   const int per_block = P.cand_block / 64;
-  const uint32_t ncols = N * kFuseBufs <= 32 ? 32 : N * kFuseBufs <= 64 ? 64 : N * kFuseBufs <= 128 ? 128
-                         : N * kFuseBufs <= 256 ? 256 : 512;
+  const uint32_t ncols = 2 * N <= 32 ? 32 : 2 * N <= 64 ? 64 : 2 * N <= 128 ? 128 : 2 * N <= 256 ? 256 : 512;
 
   if (tid == 0) {
-    for (int i = 0; i < 2 * kFuseBufs + 1; ++i) tc::mbar_init(&bars[i], 1);
+    for (int i = 0; i < NB; ++i) {
+      tc::mbar_init(&full[i], 1);
+      tc::mbar_init(&sfree[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&done[i], 1);
+      tc::mbar_init(&accfree[i], 128);  // the scoring threads
+    }
+    tc::mbar_init(qbar, 1);
+    tc::mbar_init(drain, 1);
     *abort_flag = 0;
     topk_shared_init(sh, P.K);
     tc::fence_barrier_init();
@@ -380,7 +398,7 @@ __global__ void __launch_bounds__(kThreads) k_index_gather_topk_tc(const __grid_
     const uint64_t pol = tc::policy_evict_first();
     for (int kb = 0; kb < 2; ++kb) tc::tma_load_2d(sq + kb * q_half, &P.tm_q, qbar, kb * 64, b * N, pol);
   }
-  for (int e = tid; e < N; e += kThreads) w_s[e] = P.wI[(int64_t)b * N + e];
+  for (int e = tid; e < N; e += kGtThreads) w_s[e] = P.wI[(int64_t)b * N + e];
   if (warp == 1) {
     // the kept units in ascending key order
     const uint8_t *cr = P.cand + (int64_t)b * P.cand_width;
@@ -411,7 +429,7 @@ __global__ void __launch_bounds__(kThreads) k_index_gather_topk_tc(const __grid_
       *s_nunits = min(n, P.max_units);
     }
   }
-  if (warp == 0) tc::tmem_alloc(tmem_slot, ncols);
+  if (warp == 5) tc::tmem_alloc(tmem_slot, ncols);
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
@@ -419,110 +437,172 @@ __global__ void __launch_bounds__(kThreads) k_index_gather_topk_tc(const __grid_
   const int nunits = *s_nunits;
   const int npairs_all = (nunits + 1) / 2;
   const int pa = (int)(((int64_t)rank * npairs_all) / P.P), pb = (int)(((int64_t)(rank + 1) * npairs_all) / P.P);
-  const int mine = min(pb - pa, kFuseVals / TILE);  // (the host sizes P so that every range fits)
-  auto issue = [&](int i) {  // pair pa + i into buffer i % kFuseBufs
-    const int pi = pa + i;
-    const int u0 = units[2 * pi], two = 2 * pi + 1 < nunits;
-    uint64_t *bar = &full[i % kFuseBufs];
-    uint8_t *dst = sk + (i % kFuseBufs) * k_buf;
-    const uint64_t pol = tc::policy_evict_first();
-    tc::mbar_expect_tx(bar, (two ? 2u : 1u) * 2u * 64u * 128u);
-    for (int kb = 0; kb < 2; ++kb) {
-      tc::tma_load_2d(dst + kb * (k_buf / 2), &P.tm_k, bar, kb * 64, b * P.Lstride + u0 * 64, pol);
-      if (two)
-        tc::tma_load_2d(dst + kb * (k_buf / 2) + 64 * 128, &P.tm_k, bar, kb * 64,
-                        b * P.Lstride + units[2 * pi + 1] * 64, pol);
-    }
-  };
-  int issued = 0, landed = 0;
-  bool q_landed = false;
-  if (tid == 0)
-    for (; issued < min(mine, kFuseBufs); ++issued) issue(issued);
+  const int mine = min(pb - pa, P.cap_keys / TILE);  // (the host sizes P so that every range fits)
   bool ok = true;
-  if (tid == 0 && mine > 0) ok = q_landed = tc::mbar_wait(qbar, 0, abort_flag);
-  const uint32_t id = tc::idesc_bf16_f32(TILE, N);
   unsigned my_valid = 0;
-  int done_pairs = 0;
-  for (int i = 0; i < mine; ++i) {
-    const int buf = i % kFuseBufs;
-    const uint32_t par = (uint32_t)(i / kFuseBufs) & 1u;
-    if (tid == 0 && ok) {
-      ok = tc::mbar_wait(&full[buf], par, abort_flag);
-      if (ok) {
-        ++landed;
+  if (warp == 4) {
+    // ------------------------------------------------------------------ key copies
+    if (lane == 0) {
+      const uint64_t pol = tc::policy_evict_first();
+      int issued = 0;
+      for (int i = 0; i < mine && ok; ++i) {
+        const int buf = i % NB;
+        if (i >= NB && !(ok = tc::mbar_wait(&sfree[buf], (uint32_t)((i / NB) - 1) & 1u, abort_flag))) break;
+        const int pi = pa + i;
+        const int u0 = units[2 * pi], two = 2 * pi + 1 < nunits;
+        uint8_t *dst = sk + buf * kGtSlot;
+        tc::mbar_expect_tx(&full[buf], (two ? 2u : 1u) * 2u * 64u * 128u);
+        for (int kb = 0; kb < 2; ++kb) {
+          tc::tma_load_2d(dst + kb * (kGtSlot / 2), &P.tm_k, &full[buf], kb * 64, b * P.Lstride + u0 * 64, pol);
+          if (two)
+            tc::tma_load_2d(dst + kb * (kGtSlot / 2) + 64 * 128, &P.tm_k, &full[buf], kb * 64,
+                            b * P.Lstride + units[2 * pi + 1] * 64, pol);
+        }
+        ++issued;
+      }
+      // copies that may still be in flight (none unless a wait gave up): let them land, bounded
+      const uint64_t t0 = tc::global_ns();
+      for (int i = max(0, issued - NB); i < issued; ++i)
+        while (!tc::mbar_try_wait(&full[i % NB], (uint32_t)(i / NB) & 1u) && tc::global_ns() - t0 < tc::kWaitLimitNs) {
+        }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      const uint32_t id = tc::idesc_bf16_f32(TILE, N);
+      bool issued = false;
+      if (mine > 0) ok = tc::mbar_wait(qbar, 0, abort_flag);
+      for (int i = 0; i < mine && ok; ++i) {
+        const int buf = i % NB, acc = i & 1;
+        if (!(ok = tc::mbar_wait(&full[buf], (uint32_t)(i / NB) & 1u, abort_flag))) break;
+        if (i >= 2 && !(ok = tc::mbar_wait(&accfree[acc], (uint32_t)((i >> 1) - 1) & 1u, abort_flag))) break;
         tc::tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)(buf * N);
+        issued = true;
+        const uint32_t d = tmem + (uint32_t)(acc * N);
 #pragma unroll
         for (int kb = 0; kb < 2; ++kb) {
-          const uint64_t ad = tc::sdesc_sw128(tc::smem_u32(sk + buf * k_buf + kb * (k_buf / 2)), 16, 1024);
+          const uint64_t ad = tc::sdesc_sw128(tc::smem_u32(sk + buf * kGtSlot + kb * (kGtSlot / 2)), 16, 1024);
           const uint64_t bd = tc::sdesc_sw128(tc::smem_u32(sq + kb * q_half), 16, 1024);
 #pragma unroll
           for (int k4 = 0; k4 < 4; ++k4) tc::mma_bf16(d, ad + 2ull * k4, bd + 2ull * k4, id, (kb | k4) ? 1u : 0u);
         }
-        tc::mma_commit(&done[buf]);
+        tc::mma_commit(&done[acc]);
+        tc::mma_commit(&sfree[buf]);
+      }
+      if (mine > 0 && !ok) {  // q may still be in flight after a wait gave up: let it land, bounded
+        const uint64_t t0 = tc::global_ns();
+        while (!tc::mbar_try_wait(qbar, 0) && tc::global_ns() - t0 < tc::kWaitLimitNs) {
+        }
+      }
+      if (issued) {  // nothing may still write TMEM or read shared memory when the CTA moves on
+        tc::mma_commit(drain);
+        const uint64_t t0 = tc::global_ns();
+        while (!tc::mbar_try_wait(drain, 0) && tc::global_ns() - t0 < tc::kWaitLimitNs) {
+        }
       }
     }
-    const bool got = tc::mbar_wait(&done[buf], par, abort_flag);
-    tc::tc_fence_after();
-    if (got && tid == 0 && i + kFuseBufs < mine) issue(issued++);
-    const int pi = pa + i;
-    const int slot = 2 * pi + (tid >> 6);
-    const int j = slot < nunits ? units[slot] * 64 + (tid & 63) : limit;
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(buf * N);
-    float acc = 0.f;
-    for (int h0 = 0; h0 < N; h0 += 16) {
-      uint32_t v[16];
-      tc::tmem_ld16_wait(lane_base + (uint32_t)h0, v);
+  } else {
+    // ------------------------------------------------------------------ scores (warps 0-3)
+    for (int i = 0; i < mine && ok; ++i) {
+      const int acc = i & 1;
+      if (!(ok = tc::mbar_wait(&done[acc], (uint32_t)(i >> 1) & 1u, abort_flag))) break;
+      tc::tc_fence_after();
+      const int slot = 2 * (pa + i) + (tid >> 6);
+      const int j = slot < nunits ? units[slot] * 64 + (tid & 63) : limit;
+      const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(acc * N);
+      float sacc = 0.f;
+      for (int h0 = 0; h0 < N; h0 += 16) {
+        uint32_t v[16];
+        tc::tmem_ld16_wait(lane_base + (uint32_t)h0, v);
 #pragma unroll
-      for (int k = 0; k < 16; ++k) acc = fmaf(w_s[h0 + k], fmaxf(__uint_as_float(v[k]), 0.f), acc);
-    }
-    const bool valid = got && j < limit;
-    vals[i * TILE + tid] = valid ? topk_value(acc, j) : 0ull;
-    my_valid += valid ? 1u : 0u;
-    tc::tc_fence_before();
-    const int failed = __syncthreads_or(!got);
-    tc::tc_fence_after();
-    ++done_pairs;
-    if (failed) break;
-  }
-  if (tid == 0) {
-    // copies that may still be in flight (none unless a wait gave up): let them land, bounded
-    const uint64_t t0w = tc::global_ns();
-    auto drain = [&](uint64_t *bar, uint32_t par) {
-      while (!tc::mbar_try_wait(bar, par) && tc::global_ns() - t0w < tc::kWaitLimitNs) {
+        for (int k = 0; k < 16; ++k) sacc = fmaf(w_s[h0 + k], fmaxf(__uint_as_float(v[k]), 0.f), sacc);
       }
-    };
-    if (!q_landed) drain(qbar, 0);
-    for (int i = landed; i < issued; ++i) drain(&full[i % kFuseBufs], (uint32_t)(i / kFuseBufs) & 1u);
+      tc::tc_fence_before();
+      tc::mbar_arrive(&accfree[acc]);
+      const bool valid = j < limit;
+      keys[i * TILE + tid] = order_key(sacc);
+      const unsigned bal = __ballot_sync(0xffffffffu, valid);
+      if (lane == 0) vmask[i * 4 + warp] = bal;
+      my_valid += valid ? 1u : 0u;
+    }
   }
+  const int failed = __syncthreads_or(!ok);
   // ---- the selection, across the cluster ---------------------------------------------------------
-  const int n_iter = done_pairs * TILE;
-  unsigned wv = my_valid;
+  // entry i (key pair i / 128 of this CTA's range, row i % 128) as the top-k's 64-bit value (0: not a
+  // valid position), built once into the key slots, all copies and products having completed
+  const int n_iter = failed ? 0 : mine * TILE;
+  unsigned long long *vals = reinterpret_cast<unsigned long long *>(sk);  // (cap_keys x 8 <= 2 slots)
+  for (int i = tid; i < n_iter; i += kGtThreads) {
+    unsigned long long v = 0ull;
+    if ((vmask[i >> 5] >> (i & 31)) & 1u) {
+      const int row = i % TILE;
+      const int j = units[2 * (pa + i / TILE) + (row >> 6)] * 64 + (row & 63);
+      v = ((unsigned long long)keys[i] << 32) | (unsigned long long)(~(uint32_t)j);
+    }
+    vals[i] = v;
+  }
+  __syncthreads();
+  // thread t owns the contiguous entries [c0, c1) (ascending position) for the output
+  const int chunk = (n_iter + kGtThreads - 1) / kGtThreads;
+  const int c0 = min(n_iter, tid * chunk), c1 = min(n_iter, c0 + chunk);
+  unsigned wv = failed ? 0u : my_valid;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) wv += __shfl_xor_sync(0xffffffffu, wv, o);
-  if (lane == 0) atomicAdd(&sh.count, wv);
+  // the least and the largest valid value: the radix passes start at the first byte where they differ
+  unsigned long long vmin = ~0ull, vmax = 0ull;
+  for (int i = tid; i < n_iter; i += kGtThreads) {
+    const unsigned long long v = vals[i];
+    if (v) {
+      vmin = min(vmin, v);
+      vmax = max(vmax, v);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    vmin = min(vmin, __shfl_xor_sync(0xffffffffu, vmin, o));
+    vmax = max(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
+  }
+  if (tid == 0) {
+    xval[0] = ~0ull;
+    xval[1] = 0ull;
+  }
+  __syncthreads();
+  if (lane == 0) {
+    atomicAdd(&sh.count, wv);
+    atomicMin(&xval[0], vmin);
+    atomicMax(&xval[1], vmax);
+  }
   __syncthreads();
   if (tid == 0) xchg[0] = sh.count;
-  tc::cluster_sync();  // every CTA's count is published
+  tc::cluster_sync();  // every CTA's count and value range is published
   unsigned total = 0;
-  for (int c = 0; c < P.P; ++c) total += tc::ld_cluster_u32(tc::cluster_map(tc::smem_u32(&xchg[0]), (uint32_t)c));
+  unsigned long long gmin = ~0ull, gmax = 0ull;
+  for (int c = 0; c < P.P; ++c) {
+    total += tc::ld_cluster_u32(tc::cluster_map(tc::smem_u32(&xchg[0]), (uint32_t)c));
+    gmin = min(gmin, tc::ld_cluster_u64(tc::cluster_map(tc::smem_u32(&xval[0]), (uint32_t)c)));
+    gmax = max(gmax, tc::ld_cluster_u64(tc::cluster_map(tc::smem_u32(&xval[1]), (uint32_t)c)));
+  }
   const bool all = total <= (unsigned)P.K;
   int fs = 0;
   unsigned long long thr = 0ull;
   if (!all) {
+    // every valid value shares the bytes above the first one where the least and the largest differ
+    const unsigned long long diff = gmin ^ gmax;
+    const int start = diff ? ((63 - __clzll((long long)diff)) / 8) * 8 : 0;
+    if (tid == 0) sh.prefix = start == 56 ? 0ull : (gmin & (~0ull << (start + 8)));
     int pass = 0;
-    for (int shift = 56; shift >= 0; shift -= 8, ++pass) {
+    for (int shift = start; shift >= 0; shift -= 8, ++pass) {
       unsigned *hist = hists + (pass & 1) * 256;
-      for (int i = tid; i < 256; i += kThreads) hist[i] = 0;
+      for (int i = tid; i < 256; i += kGtThreads) hist[i] = 0;
       __syncthreads();
       const unsigned long long prefix = sh.prefix;
       const unsigned long long hi_mask = shift == 56 ? 0ull : (~0ull << (shift + 8));
-      for (int i = tid; i < n_iter; i += kThreads) {
+      for (int i = tid; i < n_iter; i += kGtThreads) {
         const unsigned long long v = vals[i];
         if (v && (v & hi_mask) == (prefix & hi_mask)) atomicAdd(&hist[(v >> shift) & 255u], 1u);
       }
       tc::cluster_sync();  // every CTA's histogram of this pass is complete
-      for (int i = tid; i < 256; i += kThreads) {
+      for (int i = tid; i < 256; i += kGtThreads) {
         unsigned t = 0;
         for (int c = 0; c < P.P; ++c) t += tc::ld_cluster_u32(tc::cluster_map(tc::smem_u32(&hist[i]), (uint32_t)c));
         sh.hist[i] = t;
@@ -535,17 +615,28 @@ __global__ void __launch_bounds__(kThreads) k_index_gather_topk_tc(const __grid_
     fs = sh.shift;
     thr = sh.prefix >> fs;
   }
-  // taken positions: this CTA's in ascending order, after those of the CTAs before it
-  unsigned mine_taken = 0;
-  for (int i = tid; i < n_iter; i += kThreads) {
+  // taken positions: this CTA's in ascending order (one block-wide scan of the chunks' counts), after
+  // those of the CTAs before it
+  unsigned cnt = 0;
+  for (int i = c0; i < c1; ++i) {
     const unsigned long long v = vals[i];
-    mine_taken += (v != 0ull && (all || (v >> fs) >= thr)) ? 1u : 0u;
+    cnt += (v != 0ull && (all || (v >> fs) >= thr)) ? 1u : 0u;
   }
+  unsigned incl = cnt;
 #pragma unroll
-  for (int o2 = 16; o2 > 0; o2 >>= 1) mine_taken += __shfl_xor_sync(0xffffffffu, mine_taken, o2);
-  if (tid == 0) xchg[1] = 0;
+  for (int o2 = 1; o2 < 32; o2 <<= 1) {
+    const unsigned n2 = __shfl_up_sync(0xffffffffu, incl, o2);
+    if (lane >= o2) incl += n2;
+  }
+  if (lane == 31) sh.wsum[warp] = incl;
   __syncthreads();
-  if (lane == 0) atomicAdd(&xchg[1], mine_taken);
+  unsigned excl = incl - cnt;
+  for (int w2 = 0; w2 < warp; ++w2) excl += sh.wsum[w2];
+  if (tid == 0) {
+    unsigned ct = 0;
+    for (int w2 = 0; w2 < kGtThreads / 32; ++w2) ct += sh.wsum[w2];
+    xchg[1] = ct;
+  }
   tc::cluster_sync();  // every CTA's taken count is published
   unsigned before = 0, taken_all = 0;
   for (int c = 0; c < P.P; ++c) {
@@ -554,19 +645,19 @@ __global__ void __launch_bounds__(kThreads) k_index_gather_topk_tc(const __grid_
     taken_all += t;
   }
   int32_t *o = P.out + (int64_t)b * P.K;
-  unsigned base = before;
-  for (int i0 = 0; i0 < n_iter; i0 += kThreads) {
-    const int i = i0 + tid;
-    const unsigned long long v = i < n_iter ? vals[i] : 0ull;
-    const bool take = v != 0ull && (all || (v >> fs) >= thr);
-    const unsigned s2 = ordered_slot(sh, take, base);
-    if (take && s2 < (unsigned)P.K) o[s2] = (int32_t)(~(uint32_t)(v & 0xffffffffull)) + P.offset;
+  unsigned slot = before + excl;
+  for (int i = c0; i < c1; ++i) {
+    const unsigned long long v = vals[i];
+    if (v != 0ull && (all || (v >> fs) >= thr)) {
+      if (slot < (unsigned)P.K) o[slot] = (int32_t)(~(uint32_t)(v & 0xffffffffull)) + P.offset;
+      ++slot;
+    }
   }
   if (rank == (uint32_t)P.P - 1)
-    for (int k = (int)taken_all + tid; k < P.K; k += kThreads) o[k] = -1;
+    for (int k = (int)taken_all + tid; k < P.K; k += kGtThreads) o[k] = -1;
   tc::tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 5) {
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, ncols);
   }
@@ -802,21 +893,21 @@ cudaError_t launch_index_scores_tc(const bf16 *qI, const float *wI, const bf16 *
 
 // CTAs per query of the cluster-fused gathered scores + top-k, or 0 when the launch does not take it:
 // a decode query with a candidate mask in 64-key units whose span exceeds 1024 keys (where the
-// gathered kernel pays), P <= 8 CTAs (a portable cluster) that each hold at most kFuseVals / 128 unit
-// pairs even if the mask kept every block, as many as fill two CTAs an SM in one wave otherwise.
+// gathered kernel pays), P <= 8 CTAs (a portable cluster) that each hold at most kGtMaxKeys keys even
+// if the mask kept every block, and otherwise as many as fill two CTAs an SM in one wave.
 static int gather_topk_ctas(const bf16 *qI, const bf16 *KI, int B, int T, int start_pos, int Hi, int dI,
                             int compress_len, int ratio, const uint8_t *cand, int cand_width, int cand_block, int K,
                             int num_sms) {
   using namespace idx;
   if (!cand || T != 1 || ratio <= 0 || cand_block % 64 || K > kTopkMaxK || B <= 0) return 0;
-  if (!index_scores_tc_supported(qI, KI, Hi, dI) || Hi * kFuseBufs > 512) return 0;
+  if (!index_scores_tc_supported(qI, KI, Hi, dI) || 2 * Hi > 512) return 0;
   const int limit = std::min((start_pos + 1) / ratio, compress_len);
   const int nblk = std::min((limit + cand_block - 1) / cand_block, cand_width);
   if ((int64_t)nblk * cand_block <= 1024) return 0;
   const int max_pairs = (nblk * (cand_block / 64) + 1) / 2;
-  const int need = (max_pairs + kFuseVals / TILE - 1) / (kFuseVals / TILE);
+  const int need = (max_pairs + kGtMaxKeys / TILE - 1) / (kGtMaxKeys / TILE);
   if (need > 8) return 0;
-  return std::max(need, std::min(8, std::min(max_pairs, 2 * num_sms / B)));
+  return std::max(need, std::min(8, std::min(max_pairs, std::max(1, 2 * num_sms / B))));
 }
 
 bool index_gather_topk_supported(const bf16 *qI, const bf16 *KI, int B, int T, int start_pos, int Hi, int dI,
@@ -855,17 +946,24 @@ cudaError_t launch_index_gather_topk(const bf16 *qI, const float *wI, const bf16
   p.offset = offset;
   p.out = out;
   p.status = status;
-  const size_t smem = 1024 + (size_t)kFuseBufs * TILE * 128 * 2 + 2 * (size_t)Hi * 128 + kMaxN * 4 +
-                      (size_t)kFuseVals * 8 + 514 * 4 + 4 * (size_t)((p.max_units + 1) & ~1) +
-                      (2 * kFuseBufs + 1) * 8 + 16;
-  if (smem > 200 * 1024) return cudaErrorInvalidValue;
+  // keys a CTA holds (its share of the unit pairs if the mask kept every block), then as many key
+  // slots as the shared memory left takes
+  const int max_pairs = (p.max_units + 1) / 2;
+  p.cap_keys = ((max_pairs + Pc - 1) / Pc) * TILE;
+  const size_t fixed = 1024 + 2 * (size_t)Hi * 128 + kMaxN * 4 + (size_t)p.cap_keys * 4 + (size_t)p.cap_keys / 8 +
+                       520 * 4 + 4 * (size_t)((p.max_units + 1) & ~1) + (2 * kGtMaxBufs + 6) * 8 + 16;
+  // two CTAs an SM when the grid needs them, else one with a deeper ring
+  const size_t budget = (size_t)B * Pc > (size_t)num_sms ? 112 * 1024 : 225 * 1024;
+  p.nbufs = fixed < budget ? (int)std::min<size_t>(kGtMaxBufs, (budget - fixed) / kGtSlot) : 0;
+  if (p.nbufs < 2) return cudaErrorInvalidValue;
+  const size_t smem = fixed + (size_t)p.nbufs * kGtSlot;
   static SmemAttr attr;
   cudaError_t e = attr.ensure((const void *)k_index_gather_topk_tc, (int)smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof(cfg));
   cfg.gridDim = dim3(Pc, B);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(kGtThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute at[1];
