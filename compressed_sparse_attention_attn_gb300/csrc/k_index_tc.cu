@@ -666,11 +666,13 @@ __global__ void __launch_bounds__(kGtThreads) k_index_gather_topk_tc(const __gri
 }
 
 // ---- fused scores + top-k for short decode rows --------------------------------------------------
-// A decode query (T == 1) with at most kFusedTiles * 128 valid positions: one CTA loads all its key
-// tiles and Q^I by TMA, runs one MMA chain per tile into its own TMEM columns, and the epilogue turns
-// each valid key's score straight into the top-k's 64-bit value in shared memory; the selection
-// and ordering then run in the same CTA (the scores never go to global memory, and the top-k needs
-// no launch of its own).  The scores' arithmetic is the dense kernel's, so the selection is the same.
+// A decode query (T == 1) with at most kFusedTiles * 128 valid positions: one CTA loads its key tiles
+// and Q^I by TMA (one barrier a tile, the copies issued by several lanes), runs one MMA chain per
+// tile into its own TMEM columns as soon as the tile has landed, and the epilogue turns each valid
+// key's score straight into the top-k's 64-bit value in shared memory, tile by tile behind the
+// chains; the selection and ordering then run in the same CTA (the scores never go to global memory,
+// and the top-k needs no launch of its own).  The scores' arithmetic is the dense kernel's, so the
+// selection is the same.
 constexpr int kFusedTiles = 4;
 constexpr int kFusedThreads = 512;
 
@@ -700,81 +702,109 @@ __global__ void __launch_bounds__(kFusedThreads, 1) k_index_topk_fused_tc(const 
   float *w_s = reinterpret_cast<float *>(sq + 2 * q_blk);                        // [Hi]
   unsigned long long *vals = reinterpret_cast<unsigned long long *>(w_s + kMaxN);  // [512] by position
   uint64_t *bars = reinterpret_cast<uint64_t *>(vals + kFusedTiles * TILE);
-  uint64_t *full = bars, *done = bars + 1;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2);
+  uint64_t *full = bars, *done = bars + kFusedTiles, *qbar = bars + 2 * kFusedTiles;  // full, done: a tile each
+  uint64_t *drain = qbar + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = blockIdx.x;
   const int limit = max(0, min((P.start_pos + 1) / P.ratio, P.compress_len));
   const int ntiles = min(kFusedTiles, (limit + TILE - 1) / TILE);
   const uint32_t ncols = N * kFusedTiles <= 32 ? 32 : N * kFusedTiles <= 64 ? 64 : N * kFusedTiles <= 128 ? 128
                          : N * kFusedTiles <= 256 ? 256 : 512;
   if (tid == 0) {
-    tc::mbar_init(full, 1);
-    tc::mbar_init(done, 1);
+    for (int i = 0; i < 2 * kFusedTiles + 2; ++i) tc::mbar_init(&bars[i], 1);
     *abort_flag = 0;
     topk_shared_init(sh, P.K);
     tc::fence_barrier_init();
-    if (ntiles > 0) {
-      tc::prefetch_tmap(&P.tm_k);
+  }
+  __syncthreads();
+  // the copies: lane 0 of warp 1 takes q, lane i + 1 tile i
+  if (warp == 1 && lane <= ntiles && ntiles > 0) {
+    const uint64_t pol = tc::policy_evict_first();
+    if (lane == 0) {
       tc::prefetch_tmap(&P.tm_q);
-      tc::mbar_expect_tx(full, (uint32_t)ntiles * 2 * k_blk + 2 * q_blk);
-      const uint64_t pol = tc::policy_evict_first();
-      for (int kb = 0; kb < 2; ++kb) tc::tma_load_2d(sq + kb * q_blk, &P.tm_q, full, kb * 64, b * N, pol);
-      for (int i = 0; i < ntiles; ++i)
-        for (int kb = 0; kb < 2; ++kb)
-          tc::tma_load_2d(sk + (2 * i + kb) * k_blk, &P.tm_k, full, kb * 64, b * P.Lstride + i * TILE, pol);
+      tc::mbar_expect_tx(qbar, 2 * q_blk);
+      for (int kb = 0; kb < 2; ++kb) tc::tma_load_2d(sq + kb * q_blk, &P.tm_q, qbar, kb * 64, b * N, pol);
+    } else {
+      const int i = lane - 1;
+      tc::prefetch_tmap(&P.tm_k);
+      tc::mbar_expect_tx(&full[i], 2 * k_blk);
+      for (int kb = 0; kb < 2; ++kb)
+        tc::tma_load_2d(sk + (2 * i + kb) * k_blk, &P.tm_k, &full[i], kb * 64, b * P.Lstride + i * TILE, pol);
     }
   }
   for (int e = tid; e < N; e += kFusedThreads) w_s[e] = P.wI[(int64_t)b * N + e];
+  // the epilogue threads' candidate-mask bytes, read while the keys are in flight
+  const uint8_t *cr = P.cand ? P.cand + (int64_t)b * P.cand_width : nullptr;
+  uint8_t keep[kFusedTiles];
+#pragma unroll
+  for (int i = 0; i < kFusedTiles; ++i) {
+    const int j = i * TILE + tid;
+    keep[i] = (warp < 4 && i < ntiles && j < limit) ? (cr ? cr[j / P.cand_block] : (uint8_t)1) : (uint8_t)0;
+  }
   if (warp == 0) tc::tmem_alloc(tmem_slot, ncols);
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  if (tid == 0 && ntiles > 0) {
-    if (tc::mbar_wait(full, 0, abort_flag)) {
+  if (warp == 2 && lane == 0 && ntiles > 0) {
+    bool issued = false;
+    // one MMA chain per tile as it lands
+    bool ok = tc::mbar_wait(qbar, 0, abort_flag);
+    const uint32_t id = tc::idesc_bf16_f32(TILE, N);
+    for (int i = 0; i < ntiles && ok; ++i) {
+      if (!(ok = tc::mbar_wait(&full[i], 0, abort_flag))) break;
       tc::tc_fence_after();
-      const uint32_t id = tc::idesc_bf16_f32(TILE, N);
-      for (int i = 0; i < ntiles; ++i) {
+      issued = true;
 #pragma unroll
-        for (int kb = 0; kb < 2; ++kb) {
-          const uint64_t ad = tc::sdesc_sw128(tc::smem_u32(sk + (2 * i + kb) * k_blk), 16, 1024);
-          const uint64_t bd = tc::sdesc_sw128(tc::smem_u32(sq + kb * q_blk), 16, 1024);
+      for (int kb = 0; kb < 2; ++kb) {
+        const uint64_t ad = tc::sdesc_sw128(tc::smem_u32(sk + (2 * i + kb) * k_blk), 16, 1024);
+        const uint64_t bd = tc::sdesc_sw128(tc::smem_u32(sq + kb * q_blk), 16, 1024);
 #pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4)
-            tc::mma_bf16(tmem + (uint32_t)(i * N), ad + 2ull * k4, bd + 2ull * k4, id, (kb | k4) ? 1u : 0u);
-        }
+        for (int k4 = 0; k4 < 4; ++k4)
+          tc::mma_bf16(tmem + (uint32_t)(i * N), ad + 2ull * k4, bd + 2ull * k4, id, (kb | k4) ? 1u : 0u);
       }
-      tc::mma_commit(done);
-    } else {
-      // the copies may still land: wait for them (bounded) before the CTA can exit
+      tc::mma_commit(&done[i]);
+    }
+    if (!ok) {
+      // copies that may still land: wait for them (bounded) before the CTA can exit
       const uint64_t t0w = tc::global_ns();
-      while (!tc::mbar_try_wait(full, 0) && tc::global_ns() - t0w < tc::kWaitLimitNs) {
+      while (!tc::mbar_try_wait(qbar, 0) && tc::global_ns() - t0w < tc::kWaitLimitNs) {
+      }
+      for (int i = 0; i < ntiles; ++i)
+        while (!tc::mbar_try_wait(&full[i], 0) && tc::global_ns() - t0w < tc::kWaitLimitNs) {
+        }
+    }
+    if (issued) {  // nothing may still write TMEM when the CTA frees it
+      tc::mma_commit(drain);
+      const uint64_t t0 = tc::global_ns();
+      while (!tc::mbar_try_wait(drain, 0) && tc::global_ns() - t0 < tc::kWaitLimitNs) {
       }
     }
   }
   // scores of the valid keys as 64-bit values at their positions, 0 for an invalid one (warps 0-3:
-  // TMEM lane = key within a tile)
-  const bool got = ntiles == 0 || tc::mbar_wait(done, 0, abort_flag);
-  tc::tc_fence_after();
+  // TMEM lane = key within a tile), tile by tile as each chain completes
+  bool got = true;
   if (warp < 4) {
-    const uint8_t *cr = P.cand ? P.cand + (int64_t)b * P.cand_width : nullptr;
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
     for (int i = 0; i < ntiles; ++i) {
+      got = got && tc::mbar_wait(&done[i], 0, abort_flag);
+      tc::tc_fence_after();
       const int j = i * TILE + tid;
       float acc = 0.f;
-      for (int h0 = 0; h0 < N; h0 += 16) {
-        uint32_t v[16];
-        tc::tmem_ld16_wait(lane_base + (uint32_t)(i * N + h0), v);
+      if (got)
+        for (int h0 = 0; h0 < N; h0 += 16) {
+          uint32_t v[16];
+          tc::tmem_ld16_wait(lane_base + (uint32_t)(i * N + h0), v);
 #pragma unroll
-        for (int k = 0; k < 16; ++k) acc = fmaf(w_s[h0 + k], fmaxf(__uint_as_float(v[k]), 0.f), acc);
-      }
-      const bool ok = got && j < limit && (cr == nullptr || cr[j / P.cand_block] != 0);
+          for (int k = 0; k < 16; ++k) acc = fmaf(w_s[h0 + k], fmaxf(__uint_as_float(v[k]), 0.f), acc);
+        }
+      const bool ok = got && keep[i] != 0;
       vals[j] = ok ? topk_value(acc, j) : 0ull;
       const unsigned bal = __ballot_sync(0xffffffffu, ok);
-      if ((tid & 31) == 0 && bal) atomicAdd(&sh.count, (unsigned)__popc(bal));
+      if (lane == 0 && bal) atomicAdd(&sh.count, (unsigned)__popc(bal));
     }
   }
   tc::tc_fence_before();
@@ -1008,12 +1038,12 @@ cudaError_t launch_index_topk_fused(const bf16 *qI, const float *wI, const bf16 
   p.out = out;
   p.status = status;
   const size_t smem = 1024 + (size_t)kFusedTiles * 2 * TILE * 128 + 2 * (size_t)Hi * 128 + kMaxN * 4 +
-                      (size_t)kFusedTiles * TILE * 8 + 2 * 8 + 16;
+                      (size_t)kFusedTiles * TILE * 8 + (2 * kFusedTiles + 2) * 8 + 16;
   static SmemAttr attr;
   {
     cudaError_t e = attr.ensure((const void *)k_index_topk_fused_tc,
                                 (int)(1024 + kFusedTiles * 2 * TILE * 128 + 2 * kMaxN * 128 + kMaxN * 4 +
-                                      kFusedTiles * TILE * 8 + 2 * 8 + 16));
+                                      kFusedTiles * TILE * 8 + (2 * kFusedTiles + 2) * 8 + 16));
     if (e != cudaSuccess) return e;
   }
   k_index_topk_fused_tc<<<B, kFusedThreads, smem, s>>>(p);
