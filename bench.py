@@ -38,8 +38,8 @@ NOMINAL_HBM_GBS = 8000.0
 # qr, wo_a, wo_b), copied from the ncu capture summarised in the file below (not measured in this
 # run); set to None whenever those kernels change after the capture
 GEMM_TRAFFIC_SOURCE = "ncu capture, profiles/k_gemm_tc_reindex_decode_r2.md"
-GEMM_TRAFFIC_BYTES = {"reindex_decode_r2": (19058688 + 0) + (94515456 + 446976) + (69254656 + 12544) +
-                                           (84549120 + 157440)}
+GEMM_TRAFFIC_BYTES = {"reindex_decode_r2": (19059456 + 0) + (94509056 + 188416) + (69255680 + 13568) +
+                                           (84567040 + 174336)}
 
 
 def parse():
