@@ -360,9 +360,11 @@ __global__ void __launch_bounds__(kGtThreads) k_index_gather_topk_tc(const __gri
   uint32_t *keys = reinterpret_cast<uint32_t *>(w_s + kMaxN);   // [cap_keys] order keys
   uint32_t *vmask = keys + P.cap_keys;                          // [cap_keys / 32] validity bits
   unsigned *hists = vmask + P.cap_keys / 32;                    // [2][256] per pass
-  unsigned *xchg = hists + 512;  // [8]: count, taken, -, -, then the least and the largest value (u64)
+  // [12]: count, taken, count of positive scores, -, then the least, the largest and the least
+  // positive value (u64)
+  unsigned *xchg = hists + 512;
   unsigned long long *xval = reinterpret_cast<unsigned long long *>(xchg + 4);
-  int *units = reinterpret_cast<int *>(xchg + 8);               // [max_units]
+  int *units = reinterpret_cast<int *>(xchg + 12);              // [max_units]
   uint64_t *bars = reinterpret_cast<uint64_t *>(units + ((P.max_units + 1) & ~1));
   uint64_t *full = bars, *sfree = bars + NB, *done = bars + 2 * NB, *accfree = done + 2, *qbar = accfree + 2,
            *drain = qbar + 1;
@@ -548,69 +550,110 @@ __global__ void __launch_bounds__(kGtThreads) k_index_gather_topk_tc(const __gri
   unsigned wv = failed ? 0u : my_valid;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) wv += __shfl_xor_sync(0xffffffffu, wv, o);
-  // the least and the largest valid value: the radix passes start at the first byte where they differ
-  unsigned long long vmin = ~0ull, vmax = 0ull;
+  // the range the selection lies in: the least and the largest valid value, and the least value of
+  // a positive score (its top bit set) with their count -- when at least K scores are positive the
+  // K largest all are, and only the positive range needs resolving
+  unsigned long long vmin = ~0ull, vmax = 0ull, vpos = ~0ull;
+  unsigned npos = 0;
   for (int i = tid; i < n_iter; i += kGtThreads) {
     const unsigned long long v = vals[i];
     if (v) {
       vmin = min(vmin, v);
       vmax = max(vmax, v);
+      if (v >> 63) {
+        vpos = min(vpos, v);
+        ++npos;
+      }
     }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     vmin = min(vmin, __shfl_xor_sync(0xffffffffu, vmin, o));
     vmax = max(vmax, __shfl_xor_sync(0xffffffffu, vmax, o));
+    vpos = min(vpos, __shfl_xor_sync(0xffffffffu, vpos, o));
+    npos += __shfl_xor_sync(0xffffffffu, npos, o);
   }
   if (tid == 0) {
     xval[0] = ~0ull;
     xval[1] = 0ull;
+    xval[2] = ~0ull;
+    xchg[2] = 0;
   }
   __syncthreads();
   if (lane == 0) {
     atomicAdd(&sh.count, wv);
     atomicMin(&xval[0], vmin);
     atomicMax(&xval[1], vmax);
+    atomicMin(&xval[2], vpos);
+    atomicAdd(&xchg[2], npos);
   }
   __syncthreads();
   if (tid == 0) xchg[0] = sh.count;
-  tc::cluster_sync();  // every CTA's count and value range is published
-  unsigned total = 0;
-  unsigned long long gmin = ~0ull, gmax = 0ull;
-  for (int c = 0; c < P.P; ++c) {
-    total += tc::ld_cluster_u32(tc::cluster_map(tc::smem_u32(&xchg[0]), (uint32_t)c));
-    gmin = min(gmin, tc::ld_cluster_u64(tc::cluster_map(tc::smem_u32(&xval[0]), (uint32_t)c)));
-    gmax = max(gmax, tc::ld_cluster_u64(tc::cluster_map(tc::smem_u32(&xval[1]), (uint32_t)c)));
+  tc::cluster_sync();  // every CTA's counts and value ranges are published
+  // lane c of every warp reads CTA c's figures (all remote loads in flight together), then the warp
+  // reduces them
+  unsigned total = 0, total_pos = 0;
+  unsigned long long gmin = ~0ull, gmax = 0ull, gpos = ~0ull;
+  if (lane < P.P) {
+    const uint32_t c = (uint32_t)lane;
+    total = tc::ld_cluster_u32(tc::cluster_map(tc::smem_u32(&xchg[0]), c));
+    total_pos = tc::ld_cluster_u32(tc::cluster_map(tc::smem_u32(&xchg[2]), c));
+    gmin = tc::ld_cluster_u64(tc::cluster_map(tc::smem_u32(&xval[0]), c));
+    gmax = tc::ld_cluster_u64(tc::cluster_map(tc::smem_u32(&xval[1]), c));
+    gpos = tc::ld_cluster_u64(tc::cluster_map(tc::smem_u32(&xval[2]), c));
   }
+#pragma unroll
+  for (int o = 4; o > 0; o >>= 1) {  // (P <= 8 lanes hold figures)
+    total += __shfl_xor_sync(0xffffffffu, total, o);
+    total_pos += __shfl_xor_sync(0xffffffffu, total_pos, o);
+    gmin = min(gmin, __shfl_xor_sync(0xffffffffu, gmin, o));
+    gmax = max(gmax, __shfl_xor_sync(0xffffffffu, gmax, o));
+    gpos = min(gpos, __shfl_xor_sync(0xffffffffu, gpos, o));
+  }
+  total = __shfl_sync(0xffffffffu, total, 0);
+  total_pos = __shfl_sync(0xffffffffu, total_pos, 0);
+  gmin = __shfl_sync(0xffffffffu, gmin, 0);
+  gmax = __shfl_sync(0xffffffffu, gmax, 0);
+  gpos = __shfl_sync(0xffffffffu, gpos, 0);
+  if (total_pos >= (unsigned)P.K) gmin = gpos;
   const bool all = total <= (unsigned)P.K;
   int fs = 0;
   unsigned long long thr = 0ull;
   if (!all) {
-    // every valid value shares the bytes above the first one where the least and the largest differ
+    // the K largest share the bits above the first one where the least value of their range and the
+    // largest differ: each pass resolves the next (up to) 8 bits below the resolved ones, bit-aligned
     const unsigned long long diff = gmin ^ gmax;
-    const int start = diff ? ((63 - __clzll((long long)diff)) / 8) * 8 : 0;
-    if (tid == 0) sh.prefix = start == 56 ? 0ull : (gmin & (~0ull << (start + 8)));
+    int lo = diff ? 64 - __clzll((long long)diff) : 0;  // bits >= lo are resolved
+    if (tid == 0) sh.prefix = lo >= 64 ? 0ull : (gmax & (~0ull << lo));
     int pass = 0;
-    for (int shift = start; shift >= 0; shift -= 8, ++pass) {
+    for (; lo > 0; ++pass) {
+      const int w = min(8, lo), shift = lo - w;
       unsigned *hist = hists + (pass & 1) * 256;
       for (int i = tid; i < 256; i += kGtThreads) hist[i] = 0;
       __syncthreads();
       const unsigned long long prefix = sh.prefix;
-      const unsigned long long hi_mask = shift == 56 ? 0ull : (~0ull << (shift + 8));
+      const unsigned long long hi_mask = lo >= 64 ? 0ull : (~0ull << lo);
+      const unsigned dmask = (1u << w) - 1u;
       for (int i = tid; i < n_iter; i += kGtThreads) {
         const unsigned long long v = vals[i];
-        if (v && (v & hi_mask) == (prefix & hi_mask)) atomicAdd(&hist[(v >> shift) & 255u], 1u);
+        if (v && (v & hi_mask) == (prefix & hi_mask)) atomicAdd(&hist[(unsigned)(v >> shift) & dmask], 1u);
       }
       tc::cluster_sync();  // every CTA's histogram of this pass is complete
       for (int i = tid; i < 256; i += kGtThreads) {
+        unsigned hv[8];  // every CTA's bin, the remote loads in flight together
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          hv[c] = c < P.P ? tc::ld_cluster_u32(tc::cluster_map(tc::smem_u32(&hist[i]), (uint32_t)c)) : 0u;
         unsigned t = 0;
-        for (int c = 0; c < P.P; ++c) t += tc::ld_cluster_u32(tc::cluster_map(tc::smem_u32(&hist[i]), (uint32_t)c));
+#pragma unroll
+        for (int c = 0; c < 8; ++c) t += hv[c];
         sh.hist[i] = t;
       }
       __syncthreads();
       if (warp == 0) radix_pick(sh, sh.hist, shift);
       __syncthreads();
       if (sh.done) break;  // the same in every CTA: each summed the same histograms
+      lo = shift;
     }
     fs = sh.shift;
     thr = sh.prefix >> fs;
@@ -639,10 +682,17 @@ __global__ void __launch_bounds__(kGtThreads) k_index_gather_topk_tc(const __gri
   }
   tc::cluster_sync();  // every CTA's taken count is published
   unsigned before = 0, taken_all = 0;
-  for (int c = 0; c < P.P; ++c) {
-    const unsigned t = tc::ld_cluster_u32(tc::cluster_map(tc::smem_u32(&xchg[1]), (uint32_t)c));
-    if (c < (int)rank) before += t;
-    taken_all += t;
+  {
+    const unsigned t = lane < P.P ? tc::ld_cluster_u32(tc::cluster_map(tc::smem_u32(&xchg[1]), (uint32_t)lane)) : 0u;
+    before = lane < (int)rank ? t : 0u;
+    taken_all = t;
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) {
+      before += __shfl_xor_sync(0xffffffffu, before, o);
+      taken_all += __shfl_xor_sync(0xffffffffu, taken_all, o);
+    }
+    before = __shfl_sync(0xffffffffu, before, 0);
+    taken_all = __shfl_sync(0xffffffffu, taken_all, 0);
   }
   int32_t *o = P.out + (int64_t)b * P.K;
   unsigned slot = before + excl;
@@ -981,7 +1031,7 @@ cudaError_t launch_index_gather_topk(const bf16 *qI, const float *wI, const bf16
   const int max_pairs = (p.max_units + 1) / 2;
   p.cap_keys = ((max_pairs + Pc - 1) / Pc) * TILE;
   const size_t fixed = 1024 + 2 * (size_t)Hi * 128 + kMaxN * 4 + (size_t)p.cap_keys * 4 + (size_t)p.cap_keys / 8 +
-                       520 * 4 + 4 * (size_t)((p.max_units + 1) & ~1) + (2 * kGtMaxBufs + 6) * 8 + 16;
+                       524 * 4 + 4 * (size_t)((p.max_units + 1) & ~1) + (2 * kGtMaxBufs + 6) * 8 + 16;
   // two CTAs an SM when the grid needs them, else one with a deeper ring
   const size_t budget = (size_t)B * Pc > (size_t)num_sms ? 112 * 1024 : 225 * 1024;
   p.nbufs = fixed < budget ? (int)std::min<size_t>(kGtMaxBufs, (budget - fixed) / kGtSlot) : 0;
