@@ -85,6 +85,10 @@ struct LinearProblem {
   // tile, w8_scale [ceil(groups*N/128)][ceil(K/128)]; the product uses w = bf16(e4m3 * scale)
   const uint8_t *W8 = nullptr;
   const float *w8_scale = nullptr;
+  // 1: the kernel launched right after this product is a programmatic dependent that reads the
+  // product's output only after its dependency wait, so the tensor-core launch lets it start as soon
+  // as this grid's CTAs have started (set on every problem of the launch)
+  int early_dependents = 0;
 };
 // Products sharing M run in one tensor-core launch (up to 4 at a time).  ws/ws_bytes: Stream-K
 // arrival counters and partials (the counters must be zero between launches).

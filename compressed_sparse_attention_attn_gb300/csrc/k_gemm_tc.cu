@@ -81,6 +81,7 @@ struct Params {
   // data-parallel waves: CTA c first takes the whole tiles c, c + G, ... (dp_waves of them; tiles
   // [0, dp_waves G) in all), then its Stream-K share of the units from sk_unit0 on
   int dp_waves, sk_unit0;
+  int early_dependents;  // let a programmatic dependent launch once every CTA here has started
   float *partials;  // [grid][2][BM][BN]
   int *counters;    // [total_tiles]
   int *status;
@@ -183,6 +184,9 @@ __device__ __forceinline__ void fp8_expand_half(const uint8_t *raw, uint8_t *dst
 // units (or one k-range of a tile).
 template <bool kF8>
 __global__ void __launch_bounds__(threads_of<kF8>(), kF8 ? 1 : 2) k_gemm_tc(const __grid_constant__ Params P) {
+  // a programmatic dependent after this launch that reads its output only after its dependency wait
+  // (the fused indexer after proj qr) may start on the SMs this grid leaves
+  if (P.early_dependents) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = tc::smem_u32(smem_raw);
   uint8_t *smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
@@ -1169,6 +1173,7 @@ cudaError_t launch_gemm_tc(const LinearProblem *probs, int nprob, float *ws, siz
     tiles += p.tiles;
   }
   P.nprob = nprob;
+  for (int q = 0; q < nprob; ++q) P.early_dependents |= probs[q].early_dependents;
   unify_policies(P, nprob);
   P.total_units = units;
   P.total_tiles = tiles;

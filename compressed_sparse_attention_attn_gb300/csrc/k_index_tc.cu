@@ -738,9 +738,6 @@ struct FusedParams {
 };
 
 __global__ void __launch_bounds__(kFusedThreads, 1) k_index_topk_fused_tc(const __grid_constant__ FusedParams P) {
-  // the attention after this kernel may start its set-up now (it waits for this grid before it reads
-  // the selection)
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = tc::smem_u32(smem_raw);
   uint8_t *smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
@@ -770,11 +767,17 @@ __global__ void __launch_bounds__(kFusedThreads, 1) k_index_topk_fused_tc(const 
     tc::fence_barrier_init();
   }
   __syncthreads();
-  // the copies: lane 0 of warp 1 takes q, lane i + 1 tile i
+  // the copies: lane 0 of warp 1 takes q, lane i + 1 tile i.  Launched as a programmatic dependent of
+  // the projection that writes Q^I: the key tiles, w^I and the mask (all written before that launch
+  // began) are read at once, Q^I only after the dependency wait.
   if (warp == 1 && lane <= ntiles && ntiles > 0) {
     const uint64_t pol = tc::policy_evict_first();
     if (lane == 0) {
       tc::prefetch_tmap(&P.tm_q);
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      // the attention after this kernel may start its set-up now: it reads q (written by the
+      // projection just waited for) before its own wait, and the selection only after it
+      asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
       tc::mbar_expect_tx(qbar, 2 * q_blk);
       for (int kb = 0; kb < 2; ++kb) tc::tma_load_2d(sq + kb * q_blk, &P.tm_q, qbar, kb * 64, b * N, pol);
     } else {
@@ -867,6 +870,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1) k_index_topk_fused_tc(const 
     return v;
   };
   const unsigned nvalid = sh.count;
+  // (every thread past the dependency wait before the selection is written: the kernels before may
+  // read the previous selection)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   topk_select(sh, nvalid, nvalid ? ntiles * TILE : 0, at, P.K, P.offset, P.out + (int64_t)b * P.K);
   tc::tc_fence_before();
   __syncthreads();
@@ -1096,8 +1102,21 @@ cudaError_t launch_index_topk_fused(const bf16 *qI, const float *wI, const bf16 
                                       kFusedTiles * TILE * 8 + (2 * kFusedTiles + 2) * 8 + 16));
     if (e != cudaSuccess) return e;
   }
-  k_index_topk_fused_tc<<<B, kFusedThreads, smem, s>>>(p);
-  return cudaGetLastError();
+  // a programmatic dependent launch: the CTAs start (barriers, TMEM, the key tiles' copies) while the
+  // projection before them on the stream finishes, and wait for it before they read Q^I
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(B);
+  cfg.blockDim = dim3(kFusedThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, k_index_topk_fused_tc, p);
+  return e == cudaSuccess ? cudaGetLastError() : e;
 }
 
 }  // namespace csa
