@@ -705,12 +705,17 @@ int attn_v41_forward(csa_ctx *ctx, const csa_layer_weights *w, csa_layer_state *
                         (float)(1.0 / std::sqrt((double)dI * std::max(Hi, 1))), wI};
     STEP(csa::launch_x_finish(xa, s), "x finish");
   }
-  // the short decode row's selection is the fused indexer + top-k, a programmatic dependent that reads
-  // proj qr's output only after its dependency wait: proj qr lets it start early
+  // a decode row's selection in one kernel (the fused indexer + top-k, or its cluster form for long
+  // rows under a mask) is a programmatic dependent that reads proj qr's output only after its
+  // dependency wait: proj qr lets it start early
   const int K_sel = r.ratio > 0 ? g.index_topk : 0;
-  const bool fused_sel = r.ratio > 0 && r.is_index_source && !(dbg && dbg->scores) && !r.is_candidate_source &&
-                         csa::index_fused_supported(qI, (const bf16 *)sh->index_k, T, start_pos, Hi, dI,
-                                                    sh->compress_len, r.ratio, K_sel);
+  const bool fused_sel =
+      r.ratio > 0 && r.is_index_source && !(dbg && dbg->scores) && !r.is_candidate_source &&
+      (csa::index_fused_supported(qI, (const bf16 *)sh->index_k, T, start_pos, Hi, dI, sh->compress_len, r.ratio,
+                                  K_sel) ||
+       csa::index_gather_topk_supported(qI, (const bf16 *)sh->index_k, B, T, start_pos, Hi, dI, sh->compress_len,
+                                        r.ratio, r.uses_candidates ? sh->candidates : nullptr, sh->cand_width,
+                                        g.cand_block, K_sel, ctx->num_sms));
   // q path: q = wq_b qr (+ the indexer query q^I = W_IQ qr); RoPE on each head's tail
   {
     csa::LinearProblem pq[2] = {lin(qr, g.q_rank, g.q_rank, w->wq_b, H * hd, q, H * hd, 1),

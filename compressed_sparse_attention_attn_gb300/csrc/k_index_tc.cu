@@ -347,9 +347,10 @@ struct GatherTopkParams {
 };
 
 __global__ void __launch_bounds__(kGtThreads) k_index_gather_topk_tc(const __grid_constant__ GatherTopkParams P) {
-  // the attention after this kernel may start its set-up now (it waits for this grid before it reads
-  // the selection)
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // Launched as a programmatic dependent of the projection that writes Q^I: the unit list, the head
+  // weights and the key copies (all written before that launch began) start at once, Q^I is read only
+  // after the dependency wait, and the attention after this kernel (which reads q before its own
+  // wait) may launch only after it.
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = tc::smem_u32(smem_raw);
   uint8_t *smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
@@ -396,9 +397,6 @@ __global__ void __launch_bounds__(kGtThreads) k_index_gather_topk_tc(const __gri
     tc::fence_barrier_init();
     tc::prefetch_tmap(&P.tm_k);
     tc::prefetch_tmap(&P.tm_q);
-    tc::mbar_expect_tx(qbar, 2 * q_half);
-    const uint64_t pol = tc::policy_evict_first();
-    for (int kb = 0; kb < 2; ++kb) tc::tma_load_2d(sq + kb * q_half, &P.tm_q, qbar, kb * 64, b * N, pol);
   }
   for (int e = tid; e < N; e += kGtThreads) w_s[e] = P.wI[(int64_t)b * N + e];
   if (warp == 1) {
@@ -473,7 +471,14 @@ __global__ void __launch_bounds__(kGtThreads) k_index_gather_topk_tc(const __gri
     if (lane == 0) {
       const uint32_t id = tc::idesc_bf16_f32(TILE, N);
       bool issued = false;
-      if (mine > 0) ok = tc::mbar_wait(qbar, 0, abort_flag);
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+      if (mine > 0) {
+        tc::mbar_expect_tx(qbar, 2 * q_half);
+        const uint64_t pol = tc::policy_evict_first();
+        for (int kb = 0; kb < 2; ++kb) tc::tma_load_2d(sq + kb * q_half, &P.tm_q, qbar, kb * 64, b * N, pol);
+        ok = tc::mbar_wait(qbar, 0, abort_flag);
+      }
       for (int i = 0; i < mine && ok; ++i) {
         const int buf = i % NB, acc = i & 1;
         if (!(ok = tc::mbar_wait(&full[buf], (uint32_t)(i / NB) & 1u, abort_flag))) break;
@@ -528,6 +533,9 @@ __global__ void __launch_bounds__(kGtThreads) k_index_gather_topk_tc(const __gri
       my_valid += valid ? 1u : 0u;
     }
   }
+  // (every thread past the dependency wait before the selection is written: the kernels before may
+  // read the previous selection)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int failed = __syncthreads_or(!ok);
   // ---- the selection, across the cluster ---------------------------------------------------------
   // entry i (key pair i / 128 of this CTA's range, row i % 128) as the top-k's 64-bit value (0: not a
@@ -1052,13 +1060,16 @@ cudaError_t launch_index_gather_topk(const bf16 *qI, const float *wI, const bf16
   cfg.blockDim = dim3(kGtThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute at[1];
+  cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeClusterDimension;
   at[0].val.clusterDim.x = Pc;
   at[0].val.clusterDim.y = 1;
   at[0].val.clusterDim.z = 1;
+  // a programmatic dependent of the projection before it (see the kernel)
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, k_index_gather_topk_tc, p);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
