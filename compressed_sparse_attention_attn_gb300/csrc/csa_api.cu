@@ -698,6 +698,8 @@ int attn_v41_forward(csa_ctx *ctx, const csa_layer_weights *w, csa_layer_state *
     for (auto &p : px) p.ldp = ldp;
     const int np = idx_src ? 3 : 2;
     const int S = csa::gemm_tc_split_count(px, np, ctx->num_sms, std::max(1, ctx->xpart_rows / NT));
+    // x finish, next, is a programmatic dependent that reads the slices only after its dependency wait
+    for (int i = 0; i < np; ++i) px[i].early_dependents = 1;
     STEP(csa::launch_gemm_tc_split(px, np, S, ctx->status, s), "proj x");
     csa::XFinishArgs xa{ctx->xpart, S, ldp, g.q_rank, hd, idx_src ? Hi : 0, w->q_norm, w->kv_norm, g.eps, qr, kv, B,
                         T, start_pos, rd, tab, (bf16 *)st->window, W, win_idx, idx_stride,

@@ -7,6 +7,8 @@
 // round-to-nearest-even saturating convert.
 #include <cuda_fp8.h>
 
+#include <cstring>
+
 #include "csa_internal.cuh"
 #include "rowops.cuh"
 
@@ -176,6 +178,9 @@ __global__ void k_kv_finish(const bf16 *kv_in, bf16 *kv_out, int T, int start_po
 __global__ void __launch_bounds__(1024) k_x_finish(XFinishArgs a) {
   extern __shared__ float xs[];  // [ldp] the token's projections, rounded to bf16
   __shared__ float red[2][32];
+  // a programmatic dependent of the split-K projection writing the slices: nothing is read or written
+  // before that grid has completed
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t row = blockIdx.x;
   const int b = (int)(row / a.T), t = (int)(row % a.T);
   const int M = a.B * a.T;
@@ -269,8 +274,21 @@ cudaError_t launch_x_finish(const XFinishArgs &a, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(k_x_finish, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
-  k_x_finish<<<M, threads, smem, s>>>(a);
-  return cudaGetLastError();
+  // launched as a programmatic dependent: its CTAs can be resident (beside the projection's) when the
+  // projection ends
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(M);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, k_x_finish, a);
+  return e == cudaSuccess ? cudaGetLastError() : e;
 }
 
 cudaError_t launch_kv_finish(const bf16 *kv_in, bf16 *kv_out, int B, int T, int start_pos, int hd, int rd,

@@ -1303,6 +1303,7 @@ cudaError_t launch_gemm_tc_split(const LinearProblem *probs, int nprob, int S, i
     tiles += p.tiles;
   }
   P.nprob = nprob;
+  for (int q = 0; q < nprob; ++q) P.early_dependents |= probs[q].early_dependents;
   unify_policies(P, nprob);
   P.total_units = units;
   P.total_tiles = tiles;
