@@ -143,6 +143,12 @@ __device__ __forceinline__ void seg_range(const Params &P, int s, int &ub, int &
 // stage: group IT0 / 4 takes the 16-byte code chunks q = it * 128 + t for it = IT0 .. IT0 + 3
 // (contiguous per warp; chunk q is row q / 8, codes 16 (q % 8) ..).  row0 = the tile's first weight
 // row; rows at or past nrows (the ragged end) get scale 0.
+// atomicAdd with acquire-release semantics at gpu scope (returns the old value)
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int *p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // The scale of a stage whose 128 rows lie in one 128-row scale block (every aligned tile), read ahead
@@ -528,17 +534,18 @@ __global__ void __launch_bounds__(threads_of<kF8>(), kF8 ? 1 : 2) k_gemm_tc(cons
       ++done[buf];
       buf ^= 1;
       if (!whole) {
-        // Stream-K fixup: the last contributor of this tile sums the partials in CTA order.
-        __threadfence();
+        // Stream-K fixup: the last contributor of this tile sums the partials in CTA order.  The
+        // partials are published by one gpu-scope release after the CTA's barrier (the barrier
+        // orders every thread's stores before it), and the last arriver's acquire on the same
+        // counter, passed on by the barrier after it, orders its reads after the others' stores.
         if (!epi_sync()) break;
         const int64_t c_first = unit_owner(tile_u0, U, G), c_last = unit_owner(tile_u1 - 1, U, G);
         if (threadIdx.x == 0) {
-          const int old = atomicAdd(&P.counters[gtile], 1);
+          const int old = atom_add_acq_rel_gpu(&P.counters[gtile], 1);
           *s_last = (old == (int)(c_last - c_first)) ? 1 : 0;
         }
         if (!epi_sync()) break;
         if (*s_last) {
-          __threadfence();
           const int nc = (int)(c_last - c_first + 1);
           for (int i = threadIdx.x; i < nc; i += 128) {
             const int64_t c = c_first + i;
@@ -963,17 +970,16 @@ __global__ void __launch_bounds__(threads_of<kF8>(), kF8 ? 1 : 2) k_gemm_tc_wave
       ++done[buf];
       buf ^= 1;
       if (!whole) {
-        // Stream-K fixup: the last contributor of this tile sums the partials in CTA order.
-        __threadfence();
+        // Stream-K fixup: the last contributor of this tile sums the partials in CTA order (published
+        // and acquired as in the kernel above).
         if (!(eok = epi_sync())) break;
         const int64_t c_first = unit_owner(tile_u0 - sk0, Usk, G), c_last = unit_owner(tile_u1 - 1 - sk0, Usk, G);
         if (threadIdx.x == 0) {
-          const int old = atomicAdd(&P.counters[gtile], 1);
+          const int old = atom_add_acq_rel_gpu(&P.counters[gtile], 1);
           *s_last = (old == (int)(c_last - c_first)) ? 1 : 0;
         }
         if (!(eok = epi_sync())) break;
         if (*s_last) {
-          __threadfence();
           const int nc = (int)(c_last - c_first + 1);
           for (int i = threadIdx.x; i < nc; i += 128) {
             const int64_t c = c_first + i;
