@@ -508,7 +508,9 @@ __global__ void __launch_bounds__(threads_of<kF8>(), kF8 ? 1 : 2) k_gemm_tc(cons
         continue;
       }
       const int slot = (int)blockIdx.x * 2 + (gtile == first_tile_global ? 0 : 1);
-      float *mine = P.partials + (size_t)slot * BM * BN + (size_t)row * BN;
+      // partial tile layout: 4-column groups, the group's 128 rows contiguous (row r, columns 4c..4c+3
+      // at (c * BM + r) * 4), so that a warp's 16-byte stores and loads cover 512 contiguous bytes
+      float *mine = P.partials + (size_t)slot * BM * BN;
       for (int c0 = 0; c0 < BN; c0 += 16) {
         uint32_t r[16];
         tc::tmem_ld16(taddr + (uint32_t)c0, r);
@@ -524,7 +526,7 @@ __global__ void __launch_bounds__(threads_of<kF8>(), kF8 ? 1 : 2) k_gemm_tc(cons
         } else {
 #pragma unroll
           for (int i = 0; i < 16; i += 4)
-            *reinterpret_cast<float4 *>(mine + c0 + i) =
+            *reinterpret_cast<float4 *>(mine + ((size_t)((c0 + i) >> 2) * BM + row) * 4) =
                 make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]), __uint_as_float(r[i + 2]),
                             __uint_as_float(r[i + 3]));
         }
@@ -554,7 +556,7 @@ __global__ void __launch_bounds__(threads_of<kF8>(), kF8 ? 1 : 2) k_gemm_tc(cons
           }
           if (!epi_sync()) break;
           // sum the contributors' rows in CTA order, four contributors' 16-column chunks in flight
-          const float *base = P.partials + (size_t)row * BN;
+          const float *base = P.partials + (size_t)row * 4;
           for (int c0 = 0; c0 < BN; c0 += 16) {
             float a[16];
 #pragma unroll
@@ -564,9 +566,9 @@ __global__ void __launch_bounds__(threads_of<kF8>(), kF8 ? 1 : 2) k_gemm_tc(cons
 #pragma unroll
               for (int q = 0; q < 4; ++q)
                 if (i + q < nc) {
-                  const float4 *src = reinterpret_cast<const float4 *>(base + (size_t)cslot[i + q] * BM * BN + c0);
+                  const float *src = base + (size_t)cslot[i + q] * BM * BN + (size_t)(c0 >> 2) * BM * 4;
 #pragma unroll
-                  for (int k = 0; k < 4; ++k) v[q][k] = __ldcg(src + k);
+                  for (int k = 0; k < 4; ++k) v[q][k] = __ldcg(reinterpret_cast<const float4 *>(src + (size_t)k * BM * 4));
                 }
 #pragma unroll
               for (int q = 0; q < 4; ++q)
@@ -944,7 +946,9 @@ __global__ void __launch_bounds__(threads_of<kF8>(), kF8 ? 1 : 2) k_gemm_tc_wave
         continue;
       }
       const int slot = (int)blockIdx.x * 2 + (gtile == first_tile_global ? 0 : 1);
-      float *mine = P.partials + (size_t)slot * BM * BN + (size_t)row * BN;
+      // partial tile layout: 4-column groups, the group's 128 rows contiguous (row r, columns 4c..4c+3
+      // at (c * BM + r) * 4), so that a warp's 16-byte stores and loads cover 512 contiguous bytes
+      float *mine = P.partials + (size_t)slot * BM * BN;
       for (int c0 = 0; c0 < BN; c0 += 16) {
         uint32_t r[16];
         tc::tmem_ld16(taddr + (uint32_t)c0, r);
@@ -960,7 +964,7 @@ __global__ void __launch_bounds__(threads_of<kF8>(), kF8 ? 1 : 2) k_gemm_tc_wave
         } else {
 #pragma unroll
           for (int i = 0; i < 16; i += 4)
-            *reinterpret_cast<float4 *>(mine + c0 + i) =
+            *reinterpret_cast<float4 *>(mine + ((size_t)((c0 + i) >> 2) * BM + row) * 4) =
                 make_float4(__uint_as_float(r[i]), __uint_as_float(r[i + 1]), __uint_as_float(r[i + 2]),
                             __uint_as_float(r[i + 3]));
         }
@@ -988,7 +992,7 @@ __global__ void __launch_bounds__(threads_of<kF8>(), kF8 ? 1 : 2) k_gemm_tc_wave
           }
           if (!(eok = epi_sync())) break;
           // sum the contributors' rows in CTA order, four contributors' 16-column chunks in flight
-          const float *base = P.partials + (size_t)row * BN;
+          const float *base = P.partials + (size_t)row * 4;
           for (int c0 = 0; c0 < BN; c0 += 16) {
             float a[16];
 #pragma unroll
@@ -998,9 +1002,9 @@ __global__ void __launch_bounds__(threads_of<kF8>(), kF8 ? 1 : 2) k_gemm_tc_wave
 #pragma unroll
               for (int q = 0; q < 4; ++q)
                 if (i + q < nc) {
-                  const float4 *src = reinterpret_cast<const float4 *>(base + (size_t)cslot[i + q] * BM * BN + c0);
+                  const float *src = base + (size_t)cslot[i + q] * BM * BN + (size_t)(c0 >> 2) * BM * 4;
 #pragma unroll
-                  for (int k = 0; k < 4; ++k) v[q][k] = __ldcg(src + k);
+                  for (int k = 0; k < 4; ++k) v[q][k] = __ldcg(reinterpret_cast<const float4 *>(src + (size_t)k * BM * 4));
                 }
 #pragma unroll
               for (int q = 0; q < 4; ++q)
