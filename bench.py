@@ -37,9 +37,14 @@ NOMINAL_HBM_GBS = 8000.0
 # ncu dram__bytes_read.sum + dram__bytes_write.sum of one forward's projection launches (proj x, proj
 # qr, wo_a, wo_b), copied from the ncu capture summarised in the file below (not measured in this
 # run); set to None whenever those kernels change after the capture
-GEMM_TRAFFIC_SOURCE = "ncu capture, profiles/k_gemm_tc_reindex_decode_r2.md"
-GEMM_TRAFFIC_BYTES = {"reindex_decode_r2": (19059456 + 0) + (94509056 + 188416) + (69255680 + 13568) +
-                                           (84567040 + 174336)}
+GEMM_TRAFFIC_SOURCE = "ncu capture, profiles/k_gemm_tc_projections_all_workloads.md"
+GEMM_TRAFFIC_BYTES = {
+    "reindex_decode_r2": (19060224 + 0) + (94515968 + 178176) + (69255680 + 12800) + (84573440 + 408064),
+    "longctx_decode_r4": (19388416 + 0) + (94589184 + 529408) + (71355392 + 78336) + (85204224 + 327680),
+    "ratio0_decode": (18731776 + 0) + (84022272 + 150528) + (69256448 + 13568) + (84579840 + 388608),
+    "prefill_r4": (73533440 + 8106496) + (426359296 + 305024000) + (467602432 + 63765504) +
+                  (1080135936 + 50343168),
+}
 
 
 def parse():
