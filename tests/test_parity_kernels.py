@@ -353,7 +353,10 @@ def test_index_topk_bit_exact(csa, orc, B, T, start, L, clen, ratio, keep, cb, K
                                                         (128, 512, 128, 256, 128, 300, 2, 1),
                                                         (64, 512, 64, 256, 64, 400, 2, 100),
                                                         # the widest list the tensor-core kernel takes: 6 tiles
-                                                        (64, 512, 128, 640, 128, 900, 4, 1)])
+                                                        (64, 512, 128, 640, 128, 900, 4, 1),
+                                                        # more than two waves of queries
+                                                        (64, 512, 128, 512, 128, 900, 2, 200),
+                                                        (128, 512, 128, 256, 128, 300, 1, 200)])
 def test_sparse_attn(csa, orc, H, hd, na, nb, a_len, b_len, B, T):
     rng = np.random.default_rng(8 + H)
     q = _rng_bf16(orc, rng, (B * T, H, hd))
