@@ -135,6 +135,282 @@ __global__ void __launch_bounds__(kThreads) k_index_scores_tc(const __grid_const
   if (tid == 0 && *abort_flag && P.status) atomicOr(P.status, kStatusTimeout);
 }
 
+// An empty instruction that takes the 16 registers as inputs and outputs: placed after a
+// tcgen05.wait::ld, it keeps every use of the loaded values below the wait.
+__device__ __forceinline__ void tie_regs16(uint32_t (&r)[16]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]));
+}
+
+// ---- many query groups (prefill): persistent CTAs, Q^I resident, the key tiles streamed -------------
+// With more query groups than SMs, a CTA takes whole groups in turn (largest causal range first, the
+// groups dealt to the CTAs in a back-and-forth order so that every CTA gets about the same number of
+// key tiles) and runs each group's key tiles through a pipeline: warp 8 copies Q^I (two buffers, the
+// next group's while the current one is in use) and the key tiles (a ring of three) by TMA, warp 9
+// issues each tile's MMA chain into one of two TMEM accumulators, and warps 0-7 (two per TMEM lane
+// quadrant, each half of the group's queries) form the head-weighted ReLU sums of a finished tile
+// while the next one is multiplied.
+constexpr int kRowsThreads = 576;  // warps 0-15: sums; warp 16: TMA; warp 17: TMEM and MMA
+constexpr int kRowsEpi = 512;      // the epilogue threads
+constexpr int kRowsKSlots = 3;
+
+struct RowsParams {
+  CUtensorMap tm_k;  // K^I [B*Lstride][128], box {64, 128}
+  CUtensorMap tm_q;  // Q^I [B*T*Hi][128], box {64, QG*Hi}
+  const float *wI;   // [B*T][Hi]
+  int T, Hi, QG, Lstride, compress_len, ratio, start_pos;
+  int gps, ngroups;  // query groups a sequence, B * gps
+  const uint8_t *cand;
+  int cand_width, cand_block;
+  float *S;  // [B*T][Lstride]
+  int *status;
+};
+
+// The r-th group in order of decreasing key range: the sequences' last groups first.
+__device__ __forceinline__ void rows_group(const RowsParams &P, int r, int &b, int &t0, int &nqg, int &ntiles) {
+  const int B = P.ngroups / P.gps;
+  b = r % B;
+  const int gq = P.gps - 1 - r / B;
+  t0 = gq * P.QG;
+  nqg = min(P.QG, P.T - t0);
+  const int lim = min((P.start_pos + t0 + nqg) / P.ratio, P.compress_len);
+  ntiles = lim > 0 ? (lim + TILE - 1) / TILE : 0;
+}
+// The k-th group of CTA c among G: rounds of G ranks, every other round dealt in reverse.
+__device__ __forceinline__ int rows_rank(int k, int c, int G) { return k * G + ((k & 1) ? G - 1 - c : c); }
+
+__global__ void __launch_bounds__(kRowsThreads, 1) k_index_scores_rows_tc(const __grid_constant__ RowsParams P) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = tc::smem_u32(smem_raw);
+  uint8_t *smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
+  const int N = P.QG * P.Hi;
+  constexpr uint32_t k_blk = TILE * 128, k_slot = 2 * k_blk;
+  const uint32_t q_blk = (uint32_t)N * 128, q_buf = 2 * q_blk;
+  uint8_t *sk = smem, *sq = smem + kRowsKSlots * k_slot;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sq + 2 * q_buf);
+  uint64_t *k_full = bars, *k_empty = bars + kRowsKSlots, *q_full = bars + 2 * kRowsKSlots, *q_empty = q_full + 2,
+           *acc_full = q_full + 4, *acc_empty = q_full + 6, *drain = q_full + 8, *wbar = q_full + 9;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 16);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  float *w_s = reinterpret_cast<float *>(bars + 18);  // [QG * Hi]: the current group's head weights, then
+                                                      // [QG <= 16] int: its queries' causal limits
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = gridDim.x, c = blockIdx.x;
+  const uint32_t acc_cols = N <= 32 ? 32 : N <= 64 ? 64 : N <= 128 ? 128 : 256;
+
+  if (tid == 0) {
+    for (int s = 0; s < kRowsKSlots; ++s) {
+      tc::mbar_init(&k_full[s], 1);
+      tc::mbar_init(&k_empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&q_full[i], 1);
+      tc::mbar_init(&q_empty[i], 1);
+      tc::mbar_init(&acc_full[i], 1);
+      tc::mbar_init(&acc_empty[i], kRowsEpi);
+    }
+    tc::mbar_init(drain, 1);
+    tc::mbar_init(wbar, kRowsEpi);
+    *abort_flag = 0;
+    tc::fence_barrier_init();
+  }
+  if (warp == 17) tc::tmem_alloc(tmem_slot, 2 * acc_cols);
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 16) {
+    // ---------------------------------------------------------------- TMA: Q^I per group, key tiles
+    if (lane == 0) {
+      tc::prefetch_tmap(&P.tm_k);
+      tc::prefetch_tmap(&P.tm_q);
+      const uint64_t pol_k = tc::policy_evict_last(), pol_q = tc::policy_evict_first();
+      int qi = 0, ki = 0;
+      bool ok = true;
+      for (int k = 0; ok && k * G < P.ngroups; ++k) {
+        const int r = rows_rank(k, c, G);
+        if (r >= P.ngroups) continue;
+        int b, t0, nqg, nt;
+        rows_group(P, r, b, t0, nqg, nt);
+        if (nt == 0) continue;
+        const int qb = qi & 1;
+        if (qi >= 2 && !(ok = tc::mbar_wait(&q_empty[qb], (uint32_t)((qi / 2 - 1) & 1), abort_flag))) break;
+        tc::mbar_expect_tx(&q_full[qb], 2 * q_blk);
+        for (int kb = 0; kb < 2; ++kb)
+          tc::tma_load_2d(sq + qb * q_buf + kb * q_blk, &P.tm_q, &q_full[qb], kb * 64, (b * P.T + t0) * P.Hi, pol_q);
+        ++qi;
+        for (int kt = 0; kt < nt; ++kt, ++ki) {
+          const int s = ki % kRowsKSlots;
+          if (ki >= kRowsKSlots &&
+              !(ok = tc::mbar_wait(&k_empty[s], (uint32_t)((ki / kRowsKSlots - 1) & 1), abort_flag)))
+            break;
+          tc::mbar_expect_tx(&k_full[s], k_slot);
+          for (int kb = 0; kb < 2; ++kb)
+            tc::tma_load_2d(sk + s * k_slot + kb * k_blk, &P.tm_k, &k_full[s], kb * 64, b * P.Lstride + kt * TILE,
+                            pol_k);
+        }
+      }
+      {  // every copy has landed before the CTA can exit (bounded, whatever the flag; at once normally)
+        for (int s = 0; s < kRowsKSlots && s < ki; ++s) {
+          const int last = ki - 1 - ((ki - 1 - s) % kRowsKSlots);  // the last copy into slot s
+          const uint64_t t0w = tc::global_ns();
+          while (!tc::mbar_try_wait(&k_full[last % kRowsKSlots], (uint32_t)((last / kRowsKSlots) & 1)) &&
+                 tc::global_ns() - t0w < tc::kWaitLimitNs) {
+          }
+        }
+        for (int i = (qi >= 2 ? qi - 2 : 0); i < qi; ++i) {
+          const uint64_t t0w = tc::global_ns();
+          while (!tc::mbar_try_wait(&q_full[i & 1], (uint32_t)((i / 2) & 1)) && tc::global_ns() - t0w < tc::kWaitLimitNs) {
+          }
+        }
+      }
+    }
+  } else if (warp == 17) {
+    // ---------------------------------------------------------------- MMA issue
+    if (lane == 0) {
+      const uint32_t id = tc::idesc_bf16_f32(TILE, N);
+      int qi = 0, ki = 0, ai = 0;
+      bool ok = true, issued = false;
+      for (int k = 0; ok && k * G < P.ngroups; ++k) {
+        const int r = rows_rank(k, c, G);
+        if (r >= P.ngroups) continue;
+        int b, t0, nqg, nt;
+        rows_group(P, r, b, t0, nqg, nt);
+        if (nt == 0) continue;
+        const int qb = qi & 1;
+        if (!(ok = tc::mbar_wait(&q_full[qb], (uint32_t)((qi / 2) & 1), abort_flag))) break;
+        for (int kt = 0; kt < nt; ++kt, ++ki, ++ai) {
+          const int s = ki % kRowsKSlots, a = ai & 1;
+          if (!(ok = tc::mbar_wait(&k_full[s], (uint32_t)((ki / kRowsKSlots) & 1), abort_flag))) break;
+          if (ai >= 2 && !(ok = tc::mbar_wait(&acc_empty[a], (uint32_t)((ai / 2 - 1) & 1), abort_flag))) break;
+          tc::tc_fence_after();
+          issued = true;
+#pragma unroll
+          for (int kb = 0; kb < 2; ++kb) {
+            const uint64_t ad = tc::sdesc_sw128(tc::smem_u32(sk + s * k_slot + kb * k_blk), 16, 1024);
+            const uint64_t bd = tc::sdesc_sw128(tc::smem_u32(sq + qb * q_buf + kb * q_blk), 16, 1024);
+#pragma unroll
+            for (int k4 = 0; k4 < 4; ++k4)
+              tc::mma_bf16(tmem + (uint32_t)a * acc_cols, ad + 2ull * k4, bd + 2ull * k4, id, (kb | k4) ? 1u : 0u);
+          }
+          tc::mma_commit(&k_empty[s]);
+          tc::mma_commit(&acc_full[a]);
+        }
+        if (!ok) break;
+        tc::mma_commit(&q_empty[qb]);
+        ++qi;
+      }
+      if (issued) {  // nothing may still write TMEM when the CTA frees it
+        tc::mma_commit(drain);
+        const uint64_t t0w = tc::global_ns();
+        while (!tc::mbar_try_wait(drain, 0) && tc::global_ns() - t0w < tc::kWaitLimitNs) {
+        }
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- warps 0-15: the weighted sums
+    // warp w: TMEM lane quadrant w % 4 (32 keys of the tile) and a quarter of the group's queries; the
+    // group's head weights and causal limits staged in shared memory once per group.  The sums run
+    // on pairs of heads (packed f32x2 multiply-adds) in four independent chains.
+    const int quad = warp & 3, part = warp >> 2;
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const int bpq = P.Hi / 16;  // 16-column blocks a query
+    int *lim_s = reinterpret_cast<int *>(w_s + kMaxN);
+    int ai = 0;
+    uint32_t syncs = 0;
+    auto ep_sync = [&]() -> bool {  // the epilogue threads, a bounded wait
+      tc::mbar_arrive(wbar);
+      return tc::mbar_wait(wbar, (syncs++) & 1u, abort_flag);
+    };
+    bool ok = true;
+    for (int k = 0; ok && k * G < P.ngroups; ++k) {
+      const int r = rows_rank(k, c, G);
+      if (r >= P.ngroups) continue;
+      int b, t0, nqg, nt;
+      rows_group(P, r, b, t0, nqg, nt);
+      if (nt == 0) continue;
+      if (!(ok = ep_sync())) break;  // every epilogue warp is done with the previous group's values
+      if (tid < N) w_s[tid] = tid / P.Hi < nqg ? P.wI[(int64_t)(b * P.T + t0) * P.Hi + tid] : 0.f;
+      if (tid < nqg) lim_s[tid] = min((P.start_pos + t0 + tid + 1) / P.ratio, P.compress_len);
+      if (!(ok = ep_sync())) break;
+      const int qw = (nqg + 3) / 4, qa = min(nqg, part * qw), qe = min(nqg, qa + qw);
+      const int blk0 = qa * bpq, blk1 = qe * bpq;  // this warp's blocks, in query order
+      const int64_t row0 = (int64_t)b * P.T + t0;
+      for (int kt = 0; kt < nt; ++kt, ++ai) {
+        const int a = ai & 1;
+        if (!(ok = tc::mbar_wait(&acc_full[a], (uint32_t)((ai / 2) & 1), abort_flag))) break;
+        tc::tc_fence_after();
+        const uint32_t tb = tmem + (uint32_t)a * acc_cols + lane_off;
+        const int j = kt * TILE + quad * 32 + lane;
+        uint64_t acc2[4] = {0, 0, 0, 0};  // pairs of f32 partial sums (0.0f is all zero bits)
+        int tq = qa, hb = 0;              // query, and block within it, of the next block
+        if (blk1 <= blk0) {               // no queries for this warp
+          tc::tc_fence_before();
+          tc::mbar_arrive(&acc_empty[a]);
+        }
+        for (int k0 = blk0; k0 < blk1; k0 += 2) {
+          // up to two 16-column blocks in flight, then one wait
+          uint32_t v[2][16];
+          const int nb = min(2, blk1 - k0);
+#pragma unroll
+          for (int u = 0; u < 2; ++u)
+            if (u < nb) tc::tmem_ld16(tb + (uint32_t)((k0 + u) * 16), v[u]);
+          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+          for (int u = 0; u < 2; ++u)
+            if (u < nb) tie_regs16(v[u]);  // no use of a loaded register moves above the wait
+          if (k0 + nb >= blk1) {  // every load of this accumulator has completed: the MMA may reuse it
+            tc::tc_fence_before();
+            tc::mbar_arrive(&acc_empty[a]);
+          }
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            if (u >= nb) break;
+            const ulonglong2 *w2 = reinterpret_cast<const ulonglong2 *>(w_s + tq * P.Hi + hb * 16);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              const ulonglong2 w = w2[q4];  // heads 4 q4 .. 4 q4 + 3 as two f32 pairs
+              uint64_t r0, r1;
+              asm("mov.b64 %0, {%1, %2};"
+                  : "=l"(r0)
+                  : "f"(fmaxf(__uint_as_float(v[u][4 * q4]), 0.f)), "f"(fmaxf(__uint_as_float(v[u][4 * q4 + 1]), 0.f)));
+              asm("mov.b64 %0, {%1, %2};"
+                  : "=l"(r1)
+                  : "f"(fmaxf(__uint_as_float(v[u][4 * q4 + 2]), 0.f)), "f"(fmaxf(__uint_as_float(v[u][4 * q4 + 3]), 0.f)));
+              asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc2[(2 * q4) & 3]) : "l"(w.x), "l"(r0));
+              asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc2[(2 * q4 + 1) & 3]) : "l"(w.y), "l"(r1));
+            }
+            if (++hb == bpq) {  // query tq is complete
+              float sp[8];
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                asm("mov.b64 {%0, %1}, %2;" : "=f"(sp[2 * e]), "=f"(sp[2 * e + 1]) : "l"(acc2[e]));
+              const float acc = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
+              const int64_t row = row0 + tq;
+              if (j < lim_s[tq] && (P.cand == nullptr || P.cand[row * P.cand_width + j / P.cand_block] != 0))
+                P.S[row * P.Lstride + j] = acc;
+#pragma unroll
+              for (int e = 0; e < 4; ++e) acc2[e] = 0;
+              hb = 0;
+              ++tq;
+            }
+          }
+        }
+      }
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 17) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, 2 * acc_cols);
+  }
+  if (tid == 0 && *abort_flag && P.status) atomicOr(P.status, kStatusTimeout);
+}
+
 
 // ---- candidate-gathered variant (one query per CTA group, T == 1) --------------------------------
 // With a candidate block mask, only the kept blocks' keys can be selected, so only those are read:
@@ -942,6 +1218,43 @@ static cudaError_t launch_index_scores_gather_tc(const bf16 *qI, const float *wI
   return cudaGetLastError();
 }
 
+// Many query groups: persistent CTAs (one an SM), each running whole groups' key tiles.
+static cudaError_t launch_index_scores_rows_tc(const bf16 *qI, const float *wI, const bf16 *KI, int B, int T,
+                                               int start_pos, int Hi, int QG, int Lstride, int compress_len, int ratio,
+                                               const uint8_t *cand, int cand_width, int cand_block, float *S,
+                                               int *status, int grid, cudaStream_t s) {
+  using namespace idx;
+  RowsParams p;
+  memset(&p, 0, sizeof(p));
+  p.QG = QG;
+  if (!tma_map_2d_bf16(&p.tm_k, KI, DI, (uint64_t)B * Lstride, DI, 64, TILE)) return cudaErrorInvalidValue;
+  if (!tma_map_2d_bf16(&p.tm_q, qI, DI, (uint64_t)B * T * Hi, DI, 64, (uint32_t)(QG * Hi)))
+    return cudaErrorInvalidValue;
+  p.wI = wI;
+  p.T = T;
+  p.Hi = Hi;
+  p.Lstride = Lstride;
+  p.compress_len = compress_len;
+  p.ratio = ratio;
+  p.start_pos = start_pos;
+  p.gps = (T + QG - 1) / QG;
+  p.ngroups = B * p.gps;
+  p.cand = cand;
+  p.cand_width = cand_width;
+  p.cand_block = cand_block;
+  p.S = S;
+  p.status = status;
+  const size_t smem = 1024 + (size_t)kRowsKSlots * 2 * TILE * 128 + 2 * 2 * (size_t)QG * Hi * 128 + 18 * 8 + kMaxN * 4 + 16 * 4;
+  static SmemAttr attr;
+  {
+    cudaError_t e = attr.ensure((const void *)k_index_scores_rows_tc,
+                                (int)(1024 + kRowsKSlots * 2 * TILE * 128 + 4 * kMaxN * 128 + 18 * 8 + kMaxN * 4 + 16 * 4));
+    if (e != cudaSuccess) return e;
+  }
+  k_index_scores_rows_tc<<<std::min(grid, p.ngroups), kRowsThreads, smem, s>>>(p);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_index_scores_tc(const bf16 *qI, const float *wI, const bf16 *KI, int B, int T, int start_pos,
                                    int Hi, int Lstride, int compress_len, int ratio, const uint8_t *cand,
                                    int cand_width, int cand_block, float *S, int *status, cudaStream_t s) {
@@ -980,6 +1293,12 @@ cudaError_t launch_index_scores_tc(const bf16 *qI, const float *wI, const bf16 *
               cand_block > 1024)
     return launch_index_scores_gather_tc(qI, wI, KI, B, start_pos, Hi, Lstride, p.compress_len, ratio, cand,
                                          cand_width, cand_block, S, status, s);
+  // more query groups than SMs: persistent CTAs keep each group's Q^I resident over its key tiles
+  int dev = 0, nsm = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+      T > 1 && (int64_t)B * ((T + p.QG - 1) / p.QG) >= nsm && ((uintptr_t)wI & 15) == 0)
+    return launch_index_scores_rows_tc(qI, wI, KI, B, T, start_pos, Hi, p.QG, Lstride, p.compress_len, ratio, cand,
+                                       cand_width, cand_block, S, status, nsm, s);
   dim3 grid(tiles, (T + p.QG - 1) / p.QG, B);
   k_index_scores_tc<<<grid, kThreads, smem, s>>>(p);
   return cudaGetLastError();

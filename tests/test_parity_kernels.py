@@ -276,6 +276,51 @@ def test_index_scores_head_counts(csa, orc, Hi, B, T, start, L, clen, ratio, kee
     assert (np.abs(got[valid].astype(np.float64) - S[valid]) <= tol).all()
 
 
+@pytest.mark.parametrize("Hi,B,T,start,L,clen,ratio,keep", [
+    (32, 1, 4096, 0, 1024, 1024, 4, 0),       # the prefill chunk: 512 groups of 8 queries
+    (64, 2, 400, 100, 700, 650, 1, 0.5),      # 4-query groups, two sequences, a mask, ragged last tile
+    (16, 1, 3000, 3, 1300, 1250, 2, 0),       # 16-query groups, ragged last group
+])
+def test_index_scores_many_groups(csa, orc, Hi, B, T, start, L, clen, ratio, keep):
+    """More query groups than SMs: the persistent kernel that keeps a group's Q^I resident over its
+    key tiles.  The oracle runs on sampled queries (first and last of every sequence, group edges,
+    the ragged last group, random ones); every query's unwritten positions are checked."""
+    rng = np.random.default_rng(120 + Hi + T)
+    qI = _rng_bf16(orc, rng, (B * T, Hi, 128))
+    wI = (rng.standard_normal((B * T, Hi)) / 64).astype(np.float32)
+    KI = _rng_bf16(orc, rng, (B, L, 128))
+    pos = positions(B, T, start)
+    cand = None if not keep else candidate_mask(B * T, pos, ratio, clen, 64, -(-L // 64), keep, 79)
+    Sd = torch.full((B * T, L), float("nan"), device="cuda")
+    csa.index_scores(to_dev(qI), to_dev(wI), to_dev(KI), B, T, start, clen, ratio, Sd,
+                     None if cand is None else to_dev(cand), 64)
+    got = to_np(Sd)
+    QG = 256 // Hi
+    rows = set()
+    for b in range(B):
+        base = b * T
+        rows.update([base, base + 1, base + T - 1, base + T - 2])
+        rows.update(base + g * QG + d for g in (1, T // QG // 2, (T - 1) // QG) for d in (-1, 0, QG - 1) if 0 <= g * QG + d < T)
+        rows.update(base + int(t) for t in rng.choice(T, 24, replace=False))
+    rows = sorted(rows)
+    for r in rows:
+        b = r // T
+        want = orc.index_scores(qI[r:r + 1], wI[r:r + 1], KI[b], pos[r:r + 1], ratio, clen,
+                                None if cand is None else cand[r:r + 1], 64)[0]
+        v = np.isfinite(want)
+        assert np.isnan(got[r, ~v]).all()
+        if v.any():
+            a, w = got[r, v].astype(np.float64), want[v].astype(np.float64)
+            assert (np.abs(a - w) <= 1e-3 * np.abs(w) + 1e-3 * np.abs(w).max()).all(), r
+    # every query: the valid positions written, the others not
+    t = np.arange(B * T) % T
+    lim = np.minimum((start + t + 1) // ratio, clen)
+    valid = np.arange(L)[None, :] < lim[:, None]
+    if cand is not None:
+        valid &= cand[:, np.arange(L) // 64] != 0
+    assert np.isfinite(got[valid]).all() and np.isnan(got[~valid]).all()
+
+
 @pytest.mark.parametrize("Hi,B,start,L,clen,ratio,keep,cb", [
     (32, 5, 4000, 2048, 2000, 2, 7, 64),        # odd number of kept units
     (32, 3, 3000, 2048, 1500, 2, 0.3, 128),     # blocks of two 64-key units, last one partial
