@@ -47,6 +47,7 @@ constexpr int kMaxTiles = 6;  // index lists up to 768 entries
 constexpr int kBlockBytes = TILE * 128;  // one K-block of a tile
 constexpr int kMaxHeadGroups = 4;        // H <= 256
 constexpr int kVecs = HG * (HD / 8);     // 16-byte vectors of one head group's output
+constexpr int kRotPairs = 64;            // angles of the result's inverse rotation kept in shared memory
 
 struct Params {
   CUtensorMap tm_q;  // q [NT*H][512], box {64, 64}
@@ -82,7 +83,8 @@ struct Smem {
   static constexpr size_t wcnt = stat + (size_t)4 * HG * 4;              // int [kMaxTiles][4]
   static constexpr size_t bars = wcnt + (size_t)kMaxTiles * 4 * 4;       // u64 [16]
   static constexpr size_t misc = bars + (size_t)16 * 8;
-  static constexpr size_t total = misc + 64;
+  static constexpr size_t rot = misc + 64;                               // float2 [kRotPairs]
+  static constexpr size_t total = rot + (size_t)kRotPairs * 8;
 };
 
 __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_constant__ Params P) {
@@ -103,7 +105,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
            *sm_bar = bars + 11, *drain = bars + 12, *q_ready = bars + 13;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::misc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-  int *s_rescale = const_cast<int *>(abort_flag) + 1;  // [2]: by tile parity
+  int *s_need = const_cast<int *>(abort_flag) + 1;  // [2]: by tile parity, some score above its head's maximum
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int64_t row = blockIdx.x;  // query b*T + t
@@ -124,7 +126,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
     tc::mbar_init(q_ready, 256);
     tc::mbar_init(drain, 1);
     *abort_flag = 0;
-    s_rescale[0] = s_rescale[1] = 0;
+    s_need[0] = s_need[1] = 0;
     tc::fence_barrier_init();
     // q of this query's head group, independent of the selection
     tc::prefetch_tmap(&P.tm_q);
@@ -289,6 +291,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
         }
       }
     }
+    // the angles of the result's inverse rotation, read while q is in flight (used after the tiles)
+    if (single && P.o_rot && (P.rd >> 1) <= kRotPairs && tid < (P.rd >> 1))
+      reinterpret_cast<float2 *>(smem + L::rot)[tid] =
+          reinterpret_cast<const float2 *>(P.tab)[(int64_t)(P.start_pos + t) * (P.rd >> 1) + tid];
     bool ok = tc::mbar_wait(q_full, 0, abort_flag);
     if (ok && P.rope_q) {
 #pragma unroll
@@ -346,45 +352,63 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
       const bool vr = valid[i * TILE + r] != 0;
 #pragma unroll
       for (int h = 0; h < 32; ++h) s[h] = vr ? s[h] * P.scale_log2 : -INFINITY;
-      red_max[quad * HG + hh + lane] = warp_reduce_32<true>(s, lane);
-      if (!(ok = sm_sync())) break;
-      if (tid < HG) {
-        const float tmax =
-            fmaxf(fmaxf(red_max[tid], red_max[HG + tid]), fmaxf(red_max[2 * HG + tid], red_max[3 * HG + tid]));
-        float a = 1.0f;
-        if (tmax > m_sm[tid] + 8.0f) {  // keep exp2(s - m) below 2^8; rescale what has accumulated
-          a = exp2f(m_sm[tid] - tmax);
-          m_sm[tid] = tmax;
-          if (n > 0) s_rescale[n & 1] = 1;
-        }
-        alpha_sm[tid] = a;
-        if (tid == 0) s_rescale[(n + 1) & 1] = 0;  // the previous tile's flag, read by all by now
-      }
-      if (!(ok = sm_sync())) break;
-      if (s_rescale[n & 1]) {
-        // the previous tile's product has completed: its commit released this tile's rows
-#pragma unroll 1
-        for (int c = 0; c < KB / 2; ++c) {
-#pragma unroll
-          for (int c0 = 0; c0 < 32; c0 += 16) {
-            uint32_t v[16];
-            const uint32_t ta = tO + (uint32_t)(c * HG + hh + c0) + lane_off;
-            float av[16];
-            lds16(av, alpha_sm + hh + c0);
-            tc::tmem_ld16(ta, v);
-            tc::tmem_ld_wait();
-#pragma unroll
-            for (int q = 0; q < 16; ++q) v[q] = __float_as_uint(__uint_as_float(v[q]) * av[q]);
-            tmem_st16(ta, v);
-          }
-        }
-        tmem_st_wait();
+      // The running maximum of a head moves only when a score exceeds it by more than 2^8 (that keeps
+      // exp2(s - m) below 2^8): every thread checks its scores against it and the maxima over the
+      // tile are formed only when one of them does.
+      bool full = true;  // the first tile always
+      if (n > 0) {
+        bool need = false;
 #pragma unroll
         for (int h0 = 0; h0 < 32; h0 += 16) {
-          float av[16];
-          lds16(av, alpha_sm + hh + h0);
+          float mv[16];
+          lds16(mv, m_sm + hh + h0);
 #pragma unroll
-          for (int k = 0; k < 16; ++k) lsum[h0 + k] *= av[k];
+          for (int k = 0; k < 16; ++k) need |= s[h0 + k] > mv[k] + 8.0f;
+        }
+        if (need) s_need[n & 1] = 1;
+        if (!(ok = sm_sync())) break;
+        full = s_need[n & 1] != 0;
+        if (tid == 0) s_need[(n + 1) & 1] = 0;  // the previous tile's flag, read by all by now
+      }
+      if (full) {
+        red_max[quad * HG + hh + lane] = warp_reduce_32<true>(s, lane);
+        if (!(ok = sm_sync())) break;
+        if (tid < HG) {
+          const float tmax =
+              fmaxf(fmaxf(red_max[tid], red_max[HG + tid]), fmaxf(red_max[2 * HG + tid], red_max[3 * HG + tid]));
+          float a = 1.0f;
+          if (tmax > m_sm[tid] + 8.0f) {  // rescale what has accumulated
+            a = exp2f(m_sm[tid] - tmax);
+            m_sm[tid] = tmax;
+          }
+          alpha_sm[tid] = a;
+        }
+        if (!(ok = sm_sync())) break;
+        if (n > 0) {
+          // the previous tile's product has completed: its commit released this tile's rows
+#pragma unroll 1
+          for (int c = 0; c < KB / 2; ++c) {
+#pragma unroll
+            for (int c0 = 0; c0 < 32; c0 += 16) {
+              uint32_t v[16];
+              const uint32_t ta = tO + (uint32_t)(c * HG + hh + c0) + lane_off;
+              float av[16];
+              lds16(av, alpha_sm + hh + c0);
+              tc::tmem_ld16(ta, v);
+              tc::tmem_ld_wait();
+#pragma unroll
+              for (int q = 0; q < 16; ++q) v[q] = __float_as_uint(__uint_as_float(v[q]) * av[q]);
+              tmem_st16(ta, v);
+            }
+          }
+          tmem_st_wait();
+#pragma unroll
+          for (int h0 = 0; h0 < 32; h0 += 16) {
+            float av[16];
+            lds16(av, alpha_sm + hh + h0);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) lsum[h0 + k] *= av[k];
+          }
         }
       }
       uint8_t *prow = sP + (r / 64) * HG * 128;
@@ -452,8 +476,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
   // features d0 .. d0+7)
   const bf16 *stage = reinterpret_cast<const bf16 *>(smem + L::g);
   if (single) {
-    const float2 *tp = P.o_rot ? reinterpret_cast<const float2 *>(P.tab) + (int64_t)(P.start_pos + t) * (P.rd >> 1)
-                               : nullptr;
+    const float2 *tp = !P.o_rot ? nullptr
+                       : (P.rd >> 1) <= kRotPairs
+                           ? reinterpret_cast<const float2 *>(smem + L::rot)
+                           : reinterpret_cast<const float2 *>(P.tab) + (int64_t)(P.start_pos + t) * (P.rd >> 1);
     for (int it = tid; it < kVecs; it += kThreads) {
       const int h = it >> 6, d0 = (it & 63) * 8;
       uint4 ob = make_uint4(0u, 0u, 0u, 0u);
