@@ -6,14 +6,15 @@
 // group of 64 heads, and a range of 128-entry tiles of the query's index list J = [idx_a; idx_b]:
 // tile k covers entries 128k .. 128k+127 as they stand (an invalid entry, -1, is a masked row that
 // fetches nothing; a tile with no valid entry is skipped).  Y = [rows_a; rows_b] is never
-// materialised: the four loader warps copy each tile's rows straight from the two sources
-// (cp.async, 16 lanes per 256-byte row segment) into the 128-byte swizzled layout.  Per tile, with
-// the accumulators in TMEM:
+// materialised: eight warps copy each tile's rows straight from the two sources (cp.async, a warp
+// per 64-feature K-block, 8 lanes per 128-byte row segment) into the 128-byte swizzled layout.  Per
+// tile, with the accumulators in TMEM:
 //   S^T[r][h] = sum_d G[r][d] q[h][d]       (M = 128 rows, N = 64 heads, K = 512; G and q K-major)
-//   softmax step: a running maximum per head, raised only when a tile's maximum exceeds it by more
-//   than 2^8 (the accumulated output and sums are then rescaled), p = exp(S - m) rounded to bf16 in
-//   shared memory (K-major [64][128]); eight warps share it (a TMEM lane quadrant and 32 heads each),
-//   the maxima over the rows are butterfly reductions that leave each lane one head, and each
+//   softmax step: a running maximum per head, raised only when a score exceeds it by more than 2^8
+//   (the accumulated output and sums are then rescaled), p = exp(S - m) rounded to bf16 in shared
+//   memory (K-major [64][128]); eight warps share it (a TMEM lane quadrant and 32 heads each).  After
+//   the first tile every thread checks its scores against the running maxima and the tile's maxima
+//   (butterfly reductions that leave each lane one head) are formed only when one exceeds them; each
 //   thread keeps its own f32 sums of p per head, reduced over the CTA once after the last tile
 //   O^T[d][h] += sum_r G[r][d] P[h][r]      (M = 4 x 128 features, N = 64, K = 128 rows; the same tile
 //                                            read as an MN-major operand)
@@ -26,9 +27,9 @@
 // staged in shared memory and written with 16-byte stores as bf16, the result together with the
 // inverse rotation of its last rope_dim features at the query's position.
 //
-// Warps 0-7: softmax and the result or share; warps 4-7 also run the index pass and the row copies,
-// each owning two 64-feature K-blocks of the tile, which it refills for the next tile as soon as the
-// P.V chunk reading them has completed (the next tile's rows are prefetched into L2 once the current
+// Warps 0-7: softmax, the row copies and the result or share; warps 4-7 also run the index pass.
+// Each owns one 64-feature K-block of the tile, which it refills for the next tile as soon as the
+// P.V chunk reading it has completed (the next tile's rows are prefetched into L2 once the current
 // one has landed); warp 8: TMEM allocation and MMA issue; all nine warps write the result or share.
 // Every mbarrier wait is time-bounded.
 #include "attn_common.cuh"
@@ -117,7 +118,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
 
   // ---- phase 1: barriers, q, TMEM, and the index pass with the first tile's copies in flight
   if (tid == 0) {
-    for (int i = 0; i < 4; ++i) tc::mbar_init(&g_full[i], 32);  // the lanes of the loader warp
+    for (int i = 0; i < 4; ++i) tc::mbar_init(&g_full[i], 64);  // the lanes of the pair's two loader warps
     tc::mbar_init(q_full, 1);
     tc::mbar_init(s_full, 1);
     tc::mbar_init(p_full, 256);
@@ -143,29 +144,30 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
 
   const int n_all = P.na + P.nb;
   const int n_rows = P.a_len + P.b_len;
-  // loader geometry: warp w copies K-blocks 2w, 2w+1 (one 256-byte segment of each row), two rows
-  // per instruction, 16 lanes per row
-  const int lw = warp - 4, half = lane >> 4, sub = lane & 15;
+  // loader geometry: each of warps 0-7 copies one K-block (a 128-byte segment of every row), four
+  // rows per instruction, 8 lanes per row; warps 4-7 take K-blocks 0-3 (they run the index pass and
+  // the first S^T chunks wait for those), warps 0-3 K-blocks 4-7.  K-block pair c (features 128c ..
+  // 128c+127) is one P.V chunk and one g_full barrier.
+  const int kbw = (warp + 4) & 7, pw = kbw >> 1, rq = lane >> 3, cc = lane & 7;
   auto issue_tile = [&](int i) {
-    const uint32_t blk = s_g + (2 * lw + (sub >> 3)) * kBlockBytes;
-    const int cc = sub & 7;
+    const uint32_t blk = s_g + kbw * kBlockBytes;
     const bf16 *const *srcs = src_list + i * TILE;
 #pragma unroll 1
-    for (int i0 = 0; i0 < TILE / 2; i0 += 8) {
+    for (int i0 = 0; i0 < TILE / 4; i0 += 8) {
       const bf16 *ps[8];  // eight row addresses read before the copies that use them are issued
 #pragma unroll
-      for (int u = 0; u < 8; ++u) ps[u] = srcs[2 * (i0 + u) + half];
+      for (int u = 0; u < 8; ++u) ps[u] = srcs[4 * (i0 + u) + rq];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        const int r = 2 * (i0 + u) + half;
-        cp_async16(blk + r * 128 + ((cc ^ (r & 7)) << 4), ps[u] ? ps[u] + 128 * lw + 8 * sub : P.rows_a,
+        const int r = 4 * (i0 + u) + rq;
+        cp_async16(blk + r * 128 + ((cc ^ (r & 7)) << 4), ps[u] ? ps[u] + 64 * kbw + 8 * cc : P.rows_a,
                    ps[u] != nullptr);
       }
     }
   };
   auto tile_ok = [&](int i) { return (wcnt[4 * i] | wcnt[4 * i + 1] | wcnt[4 * i + 2] | wcnt[4 * i + 3]) != 0; };
   if (warp >= 4 && warp < 8) {
-    const int j = tid - 128;
+    const int j = tid - 128, iw = warp - 4;
     int v[kMaxTiles];
 #pragma unroll
     for (int i = 0; i < kMaxTiles; ++i) {  // every index of this CTA's tiles, loaded up front
@@ -186,10 +188,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
         src_list[i * TILE + j] = p;
         valid[i * TILE + j] = ok;
         const unsigned bal = __ballot_sync(0xffffffffu, ok);
-        if (lane == 0) wcnt[4 * i + lw] = __popc(bal);
+        if (lane == 0) wcnt[4 * i + iw] = __popc(bal);
       }
     }
-    tc::named_bar(1, 128);
+  }
+  if (warp < 8) {  // the first live tile's copies, once the index pass has filled the lists
+    tc::named_bar(1, 256);
     for (int i = 0; i < nk; ++i)
       if (tile_ok(i)) {
         issue_tile(i);
@@ -218,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
       for (int i = 0; i < nk && ok; ++i) {
         if (!tile_ok(i)) continue;
         const uint32_t par = (uint32_t)(n & 1);
-        // S^T = G q^T, each K-block pair as soon as its loader warp is done
+        // S^T = G q^T, each K-block pair as soon as its two loader warps are done
         for (int w = 0; w < 4 && ok; ++w) {
           if (!(ok = tc::mbar_wait(&g_full[w], par, abort_flag))) break;
           tc::tc_fence_after();
@@ -236,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
         if (!(ok = tc::mbar_wait(p_full, par, abort_flag))) break;
         tc::tc_fence_after();
         // O^T += G^T P^T, feature chunk c = K-blocks 2c, 2c+1; each chunk's completion frees those
-        // K-blocks for loader warp c
+        // K-blocks for their loader warps
 #pragma unroll
         for (int c = 0; c < KB / 2; ++c) {
 #pragma unroll
@@ -259,8 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
   } else {
     // ------------------------------------------------------------------ warps 0-7: softmax + staging
     // warp w: TMEM lane quadrant w % 4 (tile rows, and features of an O^T chunk), heads hh .. hh+31;
-    // warps 4-7 also copy the rows (loader warp lw = w - 4 owns K-blocks 2lw, 2lw+1)
-    const bool loader = warp >= 4;
+    // every one of these warps also copies its K-block of each tile's rows
     const int quad = warp & 3, hh = (warp >> 2) * 32;
     const int r = quad * 32 + lane;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
@@ -323,25 +326,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
     int n = 0;
     for (int i = 0; i < nk && ok; ++i) {
       if (!tile_ok(i)) continue;
-      if (loader) {
-        if (n > 0) {  // this warp's K-blocks of the previous tile have been read by its P.V chunk
-          if (!(ok = tc::mbar_wait(&pv_done[lw], (uint32_t)((n - 1) & 1), abort_flag))) break;
+      {
+        if (n > 0) {  // this warp's K-block of the previous tile has been read by its P.V chunk
+          if (!(ok = tc::mbar_wait(&pv_done[pw], (uint32_t)((n - 1) & 1), abort_flag))) break;
           issue_tile(i);
         }
         cp_async_wait_all();
         fence_proxy_async();
-        tc::mbar_arrive(&g_full[lw]);
-        // the next tile's segments of this warp's K-blocks on their way to L2 while this one is used
+        tc::mbar_arrive(&g_full[pw]);
+        // the next tile's segments of this warp's K-block on their way to L2 while this one is used
         int nx = i + 1;
         while (nx < nk && !tile_ok(nx)) ++nx;
         if (nx < nk) {
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const bf16 *pr = src_list[nx * TILE + lane + 32 * k];
-            if (pr) {
-              asm volatile("prefetch.global.L2 [%0];" ::"l"(pr + 128 * lw));
-              asm volatile("prefetch.global.L2 [%0];" ::"l"(pr + 128 * lw + 64));
-            }
+            if (pr) asm volatile("prefetch.global.L2 [%0];" ::"l"(pr + 64 * kbw));
           }
         }
       }
@@ -430,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
       tc::mbar_arrive(p_full);
       ++n;
     }
-    if (loader) cp_async_wait_all();
+    cp_async_wait_all();
     // l per head: this thread's sums over the warp, then over the four lane quadrants
     red_sum[quad * HG + hh + lane] = warp_reduce_32<false>(lsum, lane);
     if (ok) ok = sm_sync();
