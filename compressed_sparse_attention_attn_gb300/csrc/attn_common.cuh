@@ -111,5 +111,110 @@ __device__ __forceinline__ void store_out(bf16 *o, bf16 *o_rot, int64_t off, int
   }
 }
 
+// ---- the sparse-attention kernels' shared parameters -----------------------------------------------
+constexpr int HG = 64;        // heads per CTA
+constexpr int kMaxTiles = 6;  // index lists up to 768 entries
+constexpr int kBlockBytes = TILE * 128;  // one K-block of a tile
+constexpr int kMaxHeadGroups = 4;        // H <= 256
+constexpr int kVecs = HG * (HD / 8);     // 16-byte vectors of one head group's output
+constexpr int kRotPairs = 64;            // angles of the result's inverse rotation kept in shared memory
+
+struct Params {
+  CUtensorMap tm_q;  // q [NT*H][512], box {64, 64}
+  const bf16 *rows_a, *rows_b;
+  int T, H;
+  int64_t a_seq_rows, b_seq_rows;
+  int a_len, b_len;
+  const int32_t *idx_a;
+  int na;
+  const int32_t *idx_b;
+  int nb;
+  const float *sink;
+  float scale_log2;  // softmax scale * log2(e)
+  bf16 *o, *o_rot;
+  int rd, start_pos;
+  const float *tab;
+  int *status;
+  int rope_q;       // turn q's last rd features by RoPE in shared memory before the scores
+  int ntiles;       // tiles of the index list
+  int tpc, nsplit;  // tiles per CTA, CTAs per query
+  bf16 *part_o;     // [NT][nsplit][H][512]  O_c / l_c of each split
+  float *part_ml;   // [NT][nsplit][H][2]    (m_c, l_c), log2 domain
+};
+
+
+// The index pass of one 128-entry slot j of a CTA's tiles k0 .. k0+nk-1 (a thread per slot, four
+// warps): each entry's row address (nullptr for an invalid entry, -1), its validity, and per tile the
+// count of valid entries of this thread's warp (warp iw of the four).  An index outside -1 .. rows-1
+// raises the bad-index status.
+__device__ __forceinline__ void index_pass(const Params &P, int64_t row, int b, int k0, int nk, int j, int iw, int lane,
+                                           const bf16 **src_list, uint8_t *valid, int *wcnt) {
+  const int n_all = P.na + P.nb, n_rows = P.a_len + P.b_len;
+  int v[kMaxTiles];
+#pragma unroll
+  for (int i = 0; i < kMaxTiles; ++i) {  // every index of this CTA's tiles, loaded up front
+    const int e = (k0 + i) * TILE + j;
+    v[i] = -1;
+    if (i < nk) v[i] = e < P.na ? P.idx_a[row * P.na + e] : (e < n_all ? P.idx_b[row * P.nb + (e - P.na)] : -1);
+  }
+#pragma unroll
+  for (int i = 0; i < kMaxTiles; ++i) {
+    if (i < nk) {
+      const int e = (k0 + i) * TILE + j;
+      if (e < n_all && (v[i] < -1 || v[i] >= n_rows)) atomicOr(P.status, kStatusBadIndex);
+      const bool ok = e < n_all && v[i] >= 0 && v[i] < n_rows;
+      const bf16 *p = nullptr;
+      if (ok)
+        p = v[i] < P.a_len ? P.rows_a + (b * P.a_seq_rows + v[i]) * HD
+                           : P.rows_b + (b * P.b_seq_rows + (v[i] - P.a_len)) * HD;
+      src_list[i * TILE + j] = p;
+      valid[i * TILE + j] = ok;
+      const unsigned bal = __ballot_sync(0xffffffffu, ok);
+      if (lane == 0) wcnt[4 * i + iw] = __popc(bal);
+    }
+  }
+}
+
+// RoPE on q's last rd features, in place in the swizzled K-blocks (64 heads, [KB][64][128 B]): one
+// 16-byte chunk (four adjacent pairs) of one head per unit, at most two units for each of 256 threads;
+// the same f32 arithmetic as the separate pass.  rope_q_angles reads the angles (while q is still in
+// flight), rope_q_apply turns q once it has landed.
+__device__ __forceinline__ void rope_q_angles(const Params &P, int t, int tid, float4 (&qcs)[2][2]) {
+  const int q_tail = HD - P.rd, q_nch = P.rd / 8;
+  const float2 *tp = reinterpret_cast<const float2 *>(P.tab) + (int64_t)(P.start_pos + t) * (P.rd >> 1);
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int u = tid + 256 * k;
+    if (u < HG * q_nch) {
+      const int f0 = q_tail + 8 * (u % q_nch);
+      qcs[k][0] = *reinterpret_cast<const float4 *>(tp + (f0 - q_tail) / 2);
+      qcs[k][1] = *reinterpret_cast<const float4 *>(tp + (f0 - q_tail) / 2 + 2);
+    }
+  }
+}
+__device__ __forceinline__ void rope_q_apply(const Params &P, uint8_t *sq, int tid, const float4 (&qcs)[2][2]) {
+  const int q_tail = HD - P.rd, q_nch = P.rd / 8;
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int u = tid + 256 * k;
+    if (u >= HG * q_nch) continue;
+    const int h = u / q_nch, f0 = q_tail + 8 * (u % q_nch);
+    uint8_t *cp = sq + (f0 / 64) * HG * 128 + h * 128 + ((((f0 % 64) / 8) ^ (h & 7)) << 4);
+    uint4 x = *reinterpret_cast<const uint4 *>(cp);
+    const float cs[8] = {qcs[k][0].x, qcs[k][0].y, qcs[k][0].z, qcs[k][0].w,
+                         qcs[k][1].x, qcs[k][1].y, qcs[k][1].z, qcs[k][1].w};
+    __nv_bfloat162 *pv = reinterpret_cast<__nv_bfloat162 *>(&x);
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      const float a = __low2float(pv[jj]), bb = __high2float(pv[jj]), c = cs[2 * jj], sn = cs[2 * jj + 1];
+      const float re = __fsub_rn(__fmul_rn(a, c), __fmul_rn(bb, sn));
+      const float im = __fadd_rn(__fmul_rn(a, sn), __fmul_rn(bb, c));
+      pv[jj] = __halves2bfloat162(__float2bfloat16_rn(re), __float2bfloat16_rn(im));
+    }
+    *reinterpret_cast<uint4 *>(cp) = x;
+  }
+  fence_proxy_async();  // the turned q is read by the MMA (async proxy)
+}
+
 }  // namespace attn
 }  // namespace csa

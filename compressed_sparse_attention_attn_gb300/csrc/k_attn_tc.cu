@@ -42,36 +42,7 @@ bool tma_map_2d_bf16(CUtensorMap *m, const void *base, uint64_t inner, uint64_t 
 
 namespace attn {
 
-constexpr int HG = 64;        // heads per CTA
 constexpr int kThreads = 288;
-constexpr int kMaxTiles = 6;  // index lists up to 768 entries
-constexpr int kBlockBytes = TILE * 128;  // one K-block of a tile
-constexpr int kMaxHeadGroups = 4;        // H <= 256
-constexpr int kVecs = HG * (HD / 8);     // 16-byte vectors of one head group's output
-constexpr int kRotPairs = 64;            // angles of the result's inverse rotation kept in shared memory
-
-struct Params {
-  CUtensorMap tm_q;  // q [NT*H][512], box {64, 64}
-  const bf16 *rows_a, *rows_b;
-  int T, H;
-  int64_t a_seq_rows, b_seq_rows;
-  int a_len, b_len;
-  const int32_t *idx_a;
-  int na;
-  const int32_t *idx_b;
-  int nb;
-  const float *sink;
-  float scale_log2;  // softmax scale * log2(e)
-  bf16 *o, *o_rot;
-  int rd, start_pos;
-  const float *tab;
-  int *status;
-  int rope_q;       // turn q's last rd features by RoPE in shared memory before the scores
-  int ntiles;       // tiles of the index list
-  int tpc, nsplit;  // tiles per CTA, CTAs per query
-  bf16 *part_o;     // [NT][nsplit][H][512]  O_c / l_c of each split
-  float *part_ml;   // [NT][nsplit][H][2]    (m_c, l_c), log2 domain
-};
 
 struct Smem {
   static constexpr size_t g = 0;                                         // KB x 16 KiB: one tile; output staging
@@ -142,8 +113,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
   // after this wait.
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
-  const int n_all = P.na + P.nb;
-  const int n_rows = P.a_len + P.b_len;
   // loader geometry: each of warps 0-7 copies one K-block (a 128-byte segment of every row), four
   // rows per instruction, 8 lanes per row; warps 4-7 take K-blocks 0-3 (they run the index pass and
   // the first S^T chunks wait for those), warps 0-3 K-blocks 4-7.  K-block pair c (features 128c ..
@@ -166,32 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
     }
   };
   auto tile_ok = [&](int i) { return (wcnt[4 * i] | wcnt[4 * i + 1] | wcnt[4 * i + 2] | wcnt[4 * i + 3]) != 0; };
-  if (warp >= 4 && warp < 8) {
-    const int j = tid - 128, iw = warp - 4;
-    int v[kMaxTiles];
-#pragma unroll
-    for (int i = 0; i < kMaxTiles; ++i) {  // every index of this CTA's tiles, loaded up front
-      const int e = (k0 + i) * TILE + j;
-      v[i] = -1;
-      if (i < nk) v[i] = e < P.na ? P.idx_a[row * P.na + e] : (e < n_all ? P.idx_b[row * P.nb + (e - P.na)] : -1);
-    }
-#pragma unroll
-    for (int i = 0; i < kMaxTiles; ++i) {
-      if (i < nk) {
-        const int e = (k0 + i) * TILE + j;
-        if (e < n_all && (v[i] < -1 || v[i] >= n_rows)) atomicOr(P.status, kStatusBadIndex);
-        const bool ok = e < n_all && v[i] >= 0 && v[i] < n_rows;
-        const bf16 *p = nullptr;
-        if (ok)
-          p = v[i] < P.a_len ? P.rows_a + (b * P.a_seq_rows + v[i]) * HD
-                             : P.rows_b + (b * P.b_seq_rows + (v[i] - P.a_len)) * HD;
-        src_list[i * TILE + j] = p;
-        valid[i * TILE + j] = ok;
-        const unsigned bal = __ballot_sync(0xffffffffu, ok);
-        if (lane == 0) wcnt[4 * i + iw] = __popc(bal);
-      }
-    }
-  }
+  if (warp >= 4 && warp < 8) index_pass(P, row, b, k0, nk, tid - 128, warp - 4, lane, src_list, valid, wcnt);
   if (warp < 8) {  // the first live tile's copies, once the index pass has filled the lists
     tc::named_bar(1, 256);
     for (int i = 0; i < nk; ++i)
@@ -277,50 +221,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
     float lsum[32];
 #pragma unroll
     for (int h = 0; h < 32; ++h) lsum[h] = 0.f;
-    // RoPE on q's last rd features, in place in the swizzled K-blocks: one 16-byte chunk (four
-    // adjacent pairs) of one head per unit, at most two units per thread; the same f32 arithmetic
-    // as the separate pass.  The angles are read while q is still in flight.
-    const int q_tail = HD - P.rd, q_nch = P.rd / 8;
+    // RoPE on q's last rd features (the angles read while q is still in flight)
     float4 qcs[2][2];
-    if (P.rope_q) {
-      const float2 *tp = reinterpret_cast<const float2 *>(P.tab) + (int64_t)(P.start_pos + t) * (P.rd >> 1);
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int u = tid + 256 * k;
-        if (u < HG * q_nch) {
-          const int f0 = q_tail + 8 * (u % q_nch);
-          qcs[k][0] = *reinterpret_cast<const float4 *>(tp + (f0 - q_tail) / 2);
-          qcs[k][1] = *reinterpret_cast<const float4 *>(tp + (f0 - q_tail) / 2 + 2);
-        }
-      }
-    }
+    if (P.rope_q) rope_q_angles(P, t, tid, qcs);
     // the angles of the result's inverse rotation, read while q is in flight (used after the tiles)
     if (single && P.o_rot && (P.rd >> 1) <= kRotPairs && tid < (P.rd >> 1))
       reinterpret_cast<float2 *>(smem + L::rot)[tid] =
           reinterpret_cast<const float2 *>(P.tab)[(int64_t)(P.start_pos + t) * (P.rd >> 1) + tid];
     bool ok = tc::mbar_wait(q_full, 0, abort_flag);
-    if (ok && P.rope_q) {
-#pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int u = tid + 256 * k;
-        if (u >= HG * q_nch) continue;
-        const int h = u / q_nch, f0 = q_tail + 8 * (u % q_nch);
-        uint8_t *cp = smem + L::q + (f0 / 64) * HG * 128 + h * 128 + ((((f0 % 64) / 8) ^ (h & 7)) << 4);
-        uint4 x = *reinterpret_cast<const uint4 *>(cp);
-        const float cs[8] = {qcs[k][0].x, qcs[k][0].y, qcs[k][0].z, qcs[k][0].w,
-                             qcs[k][1].x, qcs[k][1].y, qcs[k][1].z, qcs[k][1].w};
-        __nv_bfloat162 *pv = reinterpret_cast<__nv_bfloat162 *>(&x);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float a = __low2float(pv[j]), bb = __high2float(pv[j]), c = cs[2 * j], sn = cs[2 * j + 1];
-          const float re = __fsub_rn(__fmul_rn(a, c), __fmul_rn(bb, sn));
-          const float im = __fadd_rn(__fmul_rn(a, sn), __fmul_rn(bb, c));
-          pv[j] = __halves2bfloat162(__float2bfloat16_rn(re), __float2bfloat16_rn(im));
-        }
-        *reinterpret_cast<uint4 *>(cp) = x;
-      }
-      fence_proxy_async();  // the turned q is read by the MMA (async proxy)
-    }
+    if (ok && P.rope_q) rope_q_apply(P, smem + L::q, tid, qcs);
     tc::mbar_arrive(q_ready);
     if (ok) ok = sm_sync();
     int n = 0;

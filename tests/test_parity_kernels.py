@@ -430,3 +430,36 @@ def test_sparse_attn(csa, orc, H, hd, na, nb, a_len, b_len, B, T):
     assert (got[0] == 0).all()
     assert_close_bf16(got, want, what="sparse_attn")
     assert_close_bf16(to_np(o_rot), want_rot, what="sparse_attn o_rot")
+
+
+@pytest.mark.parametrize("T,nb,b_len,keep", [(300, 512, 200, 0.8), (260, 256, 600, 0.5)])
+def test_sparse_attn_prefill_lists(csa, orc, T, nb, b_len, keep):
+    """Prefill-shaped lists, one CTA a query over its whole list: the causal window of the chunk's own
+    rows (its first entries -1 for early queries, so whole 64-entry halves are empty) and compressed
+    entries with runs of -1 (some halves empty, some partial)."""
+    rng = np.random.default_rng(31 + T)
+    H, hd, W, B = 64, 512, 128, 1
+    q = _rng_bf16(orc, rng, (T, H, hd))
+    ra = _rng_bf16(orc, rng, (B, T, hd))
+    rb = _rng_bf16(orc, rng, (B, b_len, hd))
+    sink = rng.standard_normal(H).astype(np.float32)
+    t = np.arange(T)[:, None]
+    ia = (t - W + 1 + np.arange(W)[None, :]).astype(np.int32)
+    ia[ia < 0] = -1
+    ib = (rng.integers(0, b_len, (T, nb)) + T).astype(np.int32)
+    ib[rng.random((T, nb)) > keep] = -1
+    ib[:, 64:192] = -1            # two empty halves in the middle of the compressed part
+    ib[5, :] = -1
+    ia[7, :] = -1                 # a query with compressed rows only
+    scale = 1 / math.sqrt(hd)
+    rd = 64
+    tab = orc.rope_table(rd, max(64, T), 10000.0)
+    want = orc.sparse_attn(q, ra[0], rb[0], np.concatenate([ia, ib], 1), sink, scale)
+    want_rot = orc.apply_rotary(want.reshape(-1, hd), rd, positions(B, T, 0), tab, inverse=True,
+                                rows_per_pos=H).reshape(want.shape)
+    ctx, _ = _ctx(csa, dim=64, max_tokens=1, max_batch=1, max_seq=16)
+    o_rot = torch.empty((T, H, hd), dtype=torch.bfloat16, device="cuda")
+    ctx.sparse_attn(to_dev(q), to_dev(ra), T, to_dev(ia), to_dev(sink), scale, rows_b=to_dev(rb), b_len=b_len,
+                    idx_b=to_dev(ib), o_rot=o_rot, rd=rd, start_pos=0, tab=to_dev(tab), B=B, T=T)
+    assert ctx.status() == 0
+    assert_close_bf16(to_np(o_rot), want_rot, what="sparse_attn o_rot (prefill lists)")
