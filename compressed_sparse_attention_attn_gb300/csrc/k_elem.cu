@@ -115,10 +115,17 @@ cudaError_t launch_act_quant(bf16 *x, int64_t n, uint8_t *codes, int8_t *scale_e
 // last rd, then FP8), plus the ring update and window selection ("deepseek_v41_ref::attn"
 // WindowCache, window_topk_idxs).  One CTA of hd threads per token row; warp w owns fp8 block w.
 // ---------------------------------------------------------------------------------------------
+// The angle of window-row element i's RoPE pair at position p ((1, 0) outside the last rd elements).
+__device__ __forceinline__ float2 kv_angle(const float *__restrict__ tab, int p, int rd, int hd, int i) {
+  const int tail = hd - rd;
+  return i >= tail ? reinterpret_cast<const float2 *>(tab)[(int64_t)p * (rd >> 1) + ((i - tail) >> 1)]
+                   : make_float2(1.f, 0.f);
+}
+
 // Element i of window row `row` (b, t): v is the normed bf16 value.  Called by every thread of
 // whole warps (the pair partner and the fp8 block come from lane shuffles).
 __device__ __forceinline__ void kv_row_finish(float v, int64_t row, int b, int t, int i, int T, int start_pos,
-                                              int hd, int rd, const float *__restrict__ tab, bf16 *kv_out,
+                                              int hd, int rd, float2 cs, bf16 *kv_out,
                                               bf16 *__restrict__ ring, int W, int32_t *__restrict__ win_idx,
                                               int idx_stride, uint8_t *__restrict__ codes,
                                               int8_t *__restrict__ scales, int nthreads) {
@@ -126,9 +133,7 @@ __device__ __forceinline__ void kv_row_finish(float v, int64_t row, int b, int t
   const int tail = hd - rd;
   // RoPE: lanes (2k, 2k+1) hold one complex number; each lane produces its own component.
   const float partner = __shfl_xor_sync(0xffffffffu, v, 1);
-  if (i >= tail) {
-    const int pair = (i - tail) >> 1;
-    const float2 cs = reinterpret_cast<const float2 *>(tab)[(int64_t)p * (rd >> 1) + pair];
+  if (i >= tail) {  // cs: the angle of element i's pair at position p (read by the caller)
     float re, im;
     if ((i & 1) == 0)
       rotate_pair(v, partner, cs.x, cs.y, re, im);
@@ -166,7 +171,8 @@ __global__ void k_kv_finish(const bf16 *kv_in, bf16 *kv_out, int T, int start_po
   const int b = (int)(row / T), t = (int)(row % T);
   const int i = threadIdx.x;
   const float v = __bfloat162float(kv_in[row * hd + i]);
-  kv_row_finish(v, row, b, t, i, T, start_pos, hd, rd, tab, kv_out, ring, W, win_idx, idx_stride, codes, scales,
+  kv_row_finish(v, row, b, t, i, T, start_pos, hd, rd, kv_angle(tab, start_pos + t, rd, hd, i), kv_out, ring, W,
+                win_idx, idx_stride, codes, scales,
                 blockDim.x);
 }
 
@@ -178,11 +184,22 @@ __global__ void k_kv_finish(const bf16 *kv_in, bf16 *kv_out, int T, int start_po
 __global__ void __launch_bounds__(1024) k_x_finish(XFinishArgs a) {
   extern __shared__ float xs[];  // [ldp] the token's projections, rounded to bf16
   __shared__ float red[2][32];
+  const int64_t row = blockIdx.x;
+  const int b = (int)(row / a.T), t = (int)(row % a.T);
+  // the norm weights and the angle (inputs of no kernel before) read before the dependency wait
+  constexpr int kQn = 3;
+  float qn[kQn];
+#pragma unroll
+  for (int k = 0; k < kQn; ++k) {
+    const int c = threadIdx.x + k * blockDim.x;
+    qn[k] = c < a.q_rank ? __ldg(a.q_norm + c) : 0.f;
+  }
+  const bool kv_thread = threadIdx.x < a.hd;
+  const float kvn = kv_thread ? __ldg(a.kv_norm + threadIdx.x) : 0.f;
+  const float2 cs = kv_thread ? kv_angle(a.tab, a.start_pos + t, a.rd, a.hd, threadIdx.x) : make_float2(1.f, 0.f);
   // a programmatic dependent of the split-K projection writing the slices: nothing is read or written
   // before that grid has completed
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int64_t row = blockIdx.x;
-  const int b = (int)(row / a.T), t = (int)(row % a.T);
   const int M = a.B * a.T;
   const int n = a.q_rank + a.hd + a.Hi;
   float sq = 0.f, skv = 0.f;
@@ -254,31 +271,110 @@ __global__ void __launch_bounds__(1024) k_x_finish(XFinishArgs a) {
   __syncthreads();
   const float rq = 1.0f / sqrtf(red[0][0] / (float)a.q_rank + a.eps);
   const float rkv = 1.0f / sqrtf(red[1][0] / (float)a.hd + a.eps);
-  for (int c = threadIdx.x; c < a.q_rank; c += blockDim.x)
+#pragma unroll
+  for (int k = 0; k < kQn; ++k) {
+    const int c = threadIdx.x + k * blockDim.x;
+    if (c < a.q_rank) a.qr[row * a.q_rank + c] = __float2bfloat16_rn(xs[c] * rq * qn[k]);
+  }
+  for (int c = threadIdx.x + kQn * blockDim.x; c < a.q_rank; c += blockDim.x)
     a.qr[row * a.q_rank + c] = __float2bfloat16_rn(xs[c] * rq * a.q_norm[c]);
   for (int h = threadIdx.x; h < a.Hi; h += blockDim.x) a.wI[row * a.Hi + h] = xs[a.q_rank + a.hd + h] * a.wscale;
-  if (threadIdx.x < a.hd) {
+  if (kv_thread) {
     const int i = threadIdx.x;
-    const float v = __bfloat162float(__float2bfloat16_rn(xs[a.q_rank + i] * rkv * a.kv_norm[i]));
-    kv_row_finish(v, row, b, t, i, a.T, a.start_pos, a.hd, a.rd, a.tab, a.kv, a.ring, a.W, a.win_idx, a.idx_stride,
+    const float v = __bfloat162float(__float2bfloat16_rn(xs[a.q_rank + i] * rkv * kvn));
+    kv_row_finish(v, row, b, t, i, a.T, a.start_pos, a.hd, a.rd, cs, a.kv, a.ring, a.W, a.win_idx, a.idx_stride,
                   a.codes, a.scales, a.hd);
+  }
+}
+
+// The same for many tokens (a prefill chunk): a warp per token, eight tokens a CTA.  Each lane sums
+// the slices of its 16-byte groups of the token's columns into the warp's shared row (rounded to bf16,
+// as above, and kept as bf16) with the sums of squares by warp shuffles; then qr and w^I from the
+// row, and the window row in 32-element rounds (a round is one fp8 block, the RoPE pairs adjacent
+// lanes).  The window norm weights (for the CTA) and each token's angles go to shared memory before
+// the dependency wait.
+constexpr int kXRowsWarps = 8;
+__global__ void __launch_bounds__(kXRowsWarps * 32) k_x_finish_rows(XFinishArgs a) {
+  extern __shared__ __align__(16) uint8_t xsm[];  // bf16 rows [kXRowsWarps][ldr], kv_norm [hd], angles [warps][rd/2]
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int64_t row = (int64_t)blockIdx.x * kXRowsWarps + wid;
+  const int M = a.B * a.T;
+  const int b = (int)(row / a.T), t = (int)(row % a.T);
+  const int n = a.q_rank + a.hd + a.Hi, ldr = (n + 7) & ~7, tail = a.hd - a.rd;
+  bf16 *xs = reinterpret_cast<bf16 *>(xsm) + (size_t)wid * ldr;
+  float *kvn = reinterpret_cast<float *>(xsm + (size_t)kXRowsWarps * ldr * 2);
+  float2 *cs = reinterpret_cast<float2 *>(kvn + a.hd) + (size_t)wid * (a.rd >> 1);
+  for (int i = threadIdx.x; i < a.hd; i += blockDim.x) kvn[i] = __ldg(a.kv_norm + i);
+  if (row < M)
+    for (int k = lane; k < (a.rd >> 1); k += 32)
+      cs[k] = reinterpret_cast<const float2 *>(a.tab)[(int64_t)(a.start_pos + t) * (a.rd >> 1) + k];
+  __syncthreads();
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (row >= M) return;
+  float sq = 0.f, skv = 0.f;
+  for (int c4 = lane; c4 < n / 4; c4 += 32) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < a.S; ++s) {
+      const float4 v = __ldcg(reinterpret_cast<const float4 *>(a.part + ((int64_t)s * M + row) * a.ldp) + c4);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    // linear_bf16 rounds the projection to bf16
+    const __nv_bfloat162 h0 = __floats2bfloat162_rn(acc.x, acc.y), h1 = __floats2bfloat162_rn(acc.z, acc.w);
+    *reinterpret_cast<__nv_bfloat162 *>(xs + 4 * c4) = h0;
+    *reinterpret_cast<__nv_bfloat162 *>(xs + 4 * c4 + 2) = h1;
+    const float r0 = __low2float(h0), r1 = __high2float(h0), r2 = __low2float(h1), r3 = __high2float(h1);
+    const float s2 = fmaf(r0, r0, fmaf(r1, r1, fmaf(r2, r2, r3 * r3)));
+    if (4 * c4 < a.q_rank)  // q_rank and hd are multiples of 4: a group lies in one part
+      sq += s2;
+    else if (4 * c4 < a.q_rank + a.hd)
+      skv += s2;
+  }
+  sq = warp_sum(sq);
+  skv = warp_sum(skv);
+  __syncwarp();
+  const float rq = 1.0f / sqrtf(sq / (float)a.q_rank + a.eps);
+  const float rkv = 1.0f / sqrtf(skv / (float)a.hd + a.eps);
+  for (int c4 = lane; c4 < a.q_rank / 4; c4 += 32) {
+    const __nv_bfloat162 x0 = *reinterpret_cast<const __nv_bfloat162 *>(xs + 4 * c4);
+    const __nv_bfloat162 x1 = *reinterpret_cast<const __nv_bfloat162 *>(xs + 4 * c4 + 2);
+    const float4 w = __ldg(reinterpret_cast<const float4 *>(a.q_norm) + c4);
+    const __nv_bfloat162 o0 = __floats2bfloat162_rn(__low2float(x0) * rq * w.x, __high2float(x0) * rq * w.y);
+    const __nv_bfloat162 o1 = __floats2bfloat162_rn(__low2float(x1) * rq * w.z, __high2float(x1) * rq * w.w);
+    *reinterpret_cast<__nv_bfloat162 *>(a.qr + row * a.q_rank + 4 * c4) = o0;
+    *reinterpret_cast<__nv_bfloat162 *>(a.qr + row * a.q_rank + 4 * c4 + 2) = o1;
+  }
+  for (int h = lane; h < a.Hi; h += 32)
+    a.wI[row * a.Hi + h] = __bfloat162float(xs[a.q_rank + a.hd + h]) * a.wscale;
+  for (int i = lane; i < a.hd; i += 32) {
+    const float v = __bfloat162float(__float2bfloat16_rn(__bfloat162float(xs[a.q_rank + i]) * rkv * kvn[i]));
+    kv_row_finish(v, row, b, t, i, a.T, a.start_pos, a.hd, a.rd, i >= tail ? cs[(i - tail) >> 1] : make_float2(1.f, 0.f),
+                  a.kv, a.ring, a.W, a.win_idx, a.idx_stride, a.codes, a.scales, a.hd);
   }
 }
 
 cudaError_t launch_x_finish(const XFinishArgs &a, cudaStream_t s) {
   const int M = a.B * a.T;
   if (M <= 0) return cudaSuccess;
-  const int threads = a.hd > 256 ? a.hd : 256;
-  const size_t smem = sizeof(float) * (size_t)(a.q_rank + a.hd + a.Hi);
+  const int n = a.q_rank + a.hd + a.Hi;
+  const bool rows = M >= 512 && a.q_rank % 4 == 0 && a.hd % 32 == 0 && a.Hi % 4 == 0 && a.ldp % 4 == 0 &&
+                    ((uintptr_t)a.part & 15) == 0 && ((uintptr_t)a.q_norm & 15) == 0 && ((uintptr_t)a.qr & 7) == 0;
+  const int threads = rows ? kXRowsWarps * 32 : (a.hd > 256 ? a.hd : 256);
+  const size_t smem = rows ? sizeof(bf16) * (size_t)kXRowsWarps * ((n + 7) & ~7) + sizeof(float) * (size_t)a.hd +
+                                 sizeof(float2) * (size_t)kXRowsWarps * (a.rd >> 1)
+                           : sizeof(float) * (size_t)n;
+  const void *fn = rows ? (const void *)k_x_finish_rows : (const void *)k_x_finish;
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(k_x_finish, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
   }
   // launched as a programmatic dependent: its CTAs can be resident (beside the projection's) when the
   // projection ends
   cudaLaunchConfig_t cfg;
   memset(&cfg, 0, sizeof(cfg));
-  cfg.gridDim = dim3(M);
+  cfg.gridDim = dim3(rows ? (unsigned)((M + kXRowsWarps - 1) / kXRowsWarps) : (unsigned)M);
   cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
@@ -287,7 +383,7 @@ cudaError_t launch_x_finish(const XFinishArgs &a, cudaStream_t s) {
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, k_x_finish, a);
+  cudaError_t e = rows ? cudaLaunchKernelEx(&cfg, k_x_finish_rows, a) : cudaLaunchKernelEx(&cfg, k_x_finish, a);
   return e == cudaSuccess ? cudaGetLastError() : e;
 }
 

@@ -39,7 +39,10 @@ __device__ __forceinline__ float pow2_ceil_f(float v) {
 __device__ __forceinline__ float fp8_block_roundtrip(float v, uint8_t &code, int &sexp) {
   float amax = warp_max(fabsf(v));
   float s = pow2_ceil_f(__fdiv_rn(fmaxf(amax, 1e-4f), 448.0f));
-  float r = __fdiv_rn(v, s);
+  // s is a power of two (2^-22 .. 2^120 for finite values), so v / s is v times the exact reciprocal
+  // 2^-e: the same exact quotient, rounded once (to 0 when s is infinite)
+  const uint32_t eb = (__float_as_uint(s) >> 23) & 0xffu;
+  float r = __fmul_rn(v, eb >= 254u ? 0.f : __uint_as_float((254u - eb) << 23));
   r = fminf(fmaxf(r, -448.0f), 448.0f);
   __nv_fp8_storage_t c = __nv_cvt_float_to_fp8(r, __NV_SATFINITE, __NV_E4M3);
   __half_raw hr = __nv_cvt_fp8_to_halfraw(c, __NV_E4M3);
