@@ -348,10 +348,76 @@ __global__ void __launch_bounds__(kXRowsWarps * 32) k_x_finish_rows(XFinishArgs 
   }
   for (int h = lane; h < a.Hi; h += 32)
     a.wI[row * a.Hi + h] = __bfloat162float(xs[a.q_rank + a.hd + h]) * a.wscale;
-  for (int i = lane; i < a.hd; i += 32) {
-    const float v = __bfloat162float(__float2bfloat16_rn(__bfloat162float(xs[a.q_rank + i]) * rkv * kvn[i]));
-    kv_row_finish(v, row, b, t, i, a.T, a.start_pos, a.hd, a.rd, i >= tail ? cs[(i - tail) >> 1] : make_float2(1.f, 0.f),
-                  a.kv, a.ring, a.W, a.win_idx, a.idx_stride, a.codes, a.scales, a.hd);
+  // the window row (hd = 512): lane l holds elements 16l .. 16l+15, so a RoPE pair lies in one lane
+  // and an fp8 block of 32 in the lanes (2m, 2m+1); the same arithmetic as kv_row_finish
+  const int p = a.start_pos + t, i0 = 16 * lane;
+  float v[16];
+  {
+    const uint4 x0 = *reinterpret_cast<const uint4 *>(xs + a.q_rank + i0);
+    const uint4 x1 = *reinterpret_cast<const uint4 *>(xs + a.q_rank + i0 + 8);
+    const bf16 *xb0 = reinterpret_cast<const bf16 *>(&x0), *xb1 = reinterpret_cast<const bf16 *>(&x1);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      v[k] = __bfloat162float(__float2bfloat16_rn(__bfloat162float(xb0[k]) * rkv * kvn[i0 + k]));
+      v[8 + k] = __bfloat162float(__float2bfloat16_rn(__bfloat162float(xb1[k]) * rkv * kvn[i0 + 8 + k]));
+    }
+  }
+#pragma unroll
+  for (int m = 0; m < 8; ++m) {
+    const int i = i0 + 2 * m;
+    if (i >= tail) {
+      const float2 c2 = cs[(i - tail) >> 1];
+      float re, im;
+      rotate_pair(v[2 * m], v[2 * m + 1], c2.x, c2.y, re, im);
+      v[2 * m] = __bfloat162float(__float2bfloat16_rn(re));
+      v[2 * m + 1] = __bfloat162float(__float2bfloat16_rn(im));
+    }
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) amax = fmaxf(amax, fabsf(v[k]));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  const float sc = pow2_ceil_f(__fdiv_rn(fmaxf(amax, 1e-4f), 448.0f));
+  const uint32_t eb = (__float_as_uint(sc) >> 23) & 0xffu;
+  const float inv = eb >= 254u ? 0.f : __uint_as_float((254u - eb) << 23);  // exact: sc is a power of two
+  uint32_t qw[8], cw[4];
+#pragma unroll
+  for (int k = 0; k < 16; k += 2) {
+    float qv[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const float r = fminf(fmaxf(__fmul_rn(v[k + e], inv), -448.0f), 448.0f);
+      const __nv_fp8_storage_t c = __nv_cvt_float_to_fp8(r, __NV_SATFINITE, __NV_E4M3);
+      const __half_raw hr = __nv_cvt_fp8_to_halfraw(c, __NV_E4M3);
+      qv[e] = __fmul_rn(__half2float(__half(hr)), sc);
+      const int kk = k + e;
+      if ((kk & 3) == 0) cw[kk >> 2] = 0u;
+      cw[kk >> 2] |= (uint32_t)c << (8 * (kk & 3));
+    }
+    const __nv_bfloat162 qb = __floats2bfloat162_rn(qv[0], qv[1]);
+    qw[k >> 1] = *reinterpret_cast<const uint32_t *>(&qb);
+  }
+  const uint4 q0 = make_uint4(qw[0], qw[1], qw[2], qw[3]), q1 = make_uint4(qw[4], qw[5], qw[6], qw[7]);
+  uint4 *ko = reinterpret_cast<uint4 *>(a.kv + row * a.hd + i0);
+  ko[0] = q0;
+  ko[1] = q1;
+  if (a.codes) *reinterpret_cast<uint4 *>(a.codes + row * a.hd + i0) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+  if (a.scales && (lane & 1) == 0)
+    a.scales[row * (a.hd / 32) + (lane >> 1)] = (int8_t)((int)eb - 127);
+  if (t >= a.T - a.W) {  // ring: position p lives in slot p mod W; of a chunk only the last W rows land
+    uint4 *ro = reinterpret_cast<uint4 *>(a.ring + ((int64_t)b * a.W + (p % a.W)) * a.hd + i0);
+    ro[0] = q0;
+    ro[1] = q1;
+  }
+  if (a.win_idx) {
+    int32_t *wi = a.win_idx + row * a.idx_stride;
+    for (int k = lane; k < a.W; k += 32) {
+      const int pk = p - a.W + 1 + k;
+      if (a.start_pos == 0)
+        wi[k] = pk >= 0 ? pk : -1;  // the chunk's own rows
+      else
+        wi[k] = pk >= 0 ? (p + 1 + k) % a.W : -1;  // ring slots, oldest first
+    }
   }
 }
 
@@ -359,8 +425,9 @@ cudaError_t launch_x_finish(const XFinishArgs &a, cudaStream_t s) {
   const int M = a.B * a.T;
   if (M <= 0) return cudaSuccess;
   const int n = a.q_rank + a.hd + a.Hi;
-  const bool rows = M >= 512 && a.q_rank % 4 == 0 && a.hd % 32 == 0 && a.Hi % 4 == 0 && a.ldp % 4 == 0 &&
-                    ((uintptr_t)a.part & 15) == 0 && ((uintptr_t)a.q_norm & 15) == 0 && ((uintptr_t)a.qr & 7) == 0;
+  const bool rows = M >= 512 && a.q_rank % 4 == 0 && a.hd == 512 && a.Hi % 4 == 0 && a.ldp % 4 == 0 &&
+                    ((uintptr_t)a.part & 15) == 0 && ((uintptr_t)a.q_norm & 15) == 0 && ((uintptr_t)a.qr & 7) == 0 &&
+                    ((uintptr_t)a.kv & 15) == 0 && ((uintptr_t)a.ring & 15) == 0 && ((uintptr_t)a.codes & 15) == 0;
   const int threads = rows ? kXRowsWarps * 32 : (a.hd > 256 ? a.hd : 256);
   const size_t smem = rows ? sizeof(bf16) * (size_t)kXRowsWarps * ((n + 7) & ~7) + sizeof(float) * (size_t)a.hd +
                                  sizeof(float2) * (size_t)kXRowsWarps * (a.rd >> 1)
