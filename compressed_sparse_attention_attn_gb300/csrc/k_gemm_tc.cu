@@ -1043,6 +1043,206 @@ __global__ void __launch_bounds__(threads_of<kF8>(), kF8 ? 1 : 2) k_gemm_tc_wave
   if (threadIdx.x == 0 && *abort_flag) atomicOr(P.status, kStatusTimeout);
 }
 
+// ---- pairs: clusters of two CTAs sharing the token tile ----------------------------------------------
+// For launches with many token tiles: the two CTAs of a cluster take the weight tiles 2j and 2j + 1 of
+// one 256-token tile; each copies half of the activation tile (128 tokens) and multicasts it into both
+// CTAs' stages, so that a CTA reads 32 instead of 48 KiB from L2 per 64-wide k-slice (the prefill
+// projections are bound by that traffic).  Whole pair tiles in waves (cluster v takes pair tiles v,
+// v + NP, ...; token tile fastest, so the clusters in flight share the weight tiles too), no Stream-K.
+// A stage is refilled only once both CTAs' MMAs have read it: its empty barrier counts the commits of
+// both, each MMA issuer committing to the two CTAs' barriers at once.
+__device__ __forceinline__ void tma_load_2d_mc(void *dst, const CUtensorMap *tm, uint64_t *bar, int c0, int c1,
+                                               uint16_t mask, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster.L2::cache_hint"
+      " [%0], [%1, {%3, %4}], [%2], %5, %6;" ::"r"(tc::smem_u32(dst)),
+      "l"((uint64_t)tm), "r"(tc::smem_u32(bar)), "r"(c0), "r"(c1), "h"(mask), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit_mc(uint64_t *bar, uint16_t mask) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                   tc::smem_u32(bar)),
+               "h"(mask)
+               : "memory");
+}
+
+// Pair tile pt of the launch: problem, token tile, weight-tile pair, group.
+struct PairTile {
+  int p, tm, j, g;
+};
+__device__ __forceinline__ PairTile decode_pair(const Params &P, int pt) {
+  int p = 0;
+  while (p + 1 < P.nprob && pt >= P.prob[p + 1].tile_begin / 2) ++p;
+  const Problem &pr = P.prob[p];
+  const int local = pt - pr.tile_begin / 2, half_n = pr.tiles_n / 2;
+  return PairTile{p, local % pr.tiles_m, (local / pr.tiles_m) % half_n, local / (pr.tiles_m * half_n)};
+}
+
+constexpr int kPairBN = 256;  // tokens of a tile (the pair's shared operand)
+
+__global__ void __launch_bounds__(kThreads, 1) k_gemm_tc_pairs(const __grid_constant__ Params P) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = tc::smem_u32(smem_raw);
+  uint8_t *smem = smem_raw + ((1024 - (raw & 1023)) & 1023);
+  const int S = P.stages;
+  constexpr uint32_t a_bytes = BM * BK * 2, b_half = 128 * BK * 2, b_bytes = 2 * b_half;
+  constexpr uint32_t stage_bytes = a_bytes + b_bytes;
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + S * stage_bytes);
+  uint64_t *empty = full + S;
+  uint64_t *accf = empty + S;  // [2]
+  uint64_t *acce = accf + 2;   // [2]
+  uint64_t *drain = acce + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = (int)tc::cluster_ctarank();
+  const int v0 = blockIdx.x >> 1, NP = gridDim.x >> 1, PT = P.total_tiles / 2;
+  constexpr uint16_t kBoth = 3;
+  constexpr uint32_t tmem_cols = 2 * kPairBN;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      tc::mbar_init(&full[s], 1);
+      tc::mbar_init(&empty[s], 2);  // both CTAs' MMA commits
+    }
+    for (int b = 0; b < 2; ++b) {
+      tc::mbar_init(&accf[b], 1);
+      tc::mbar_init(&acce[b], 128);
+    }
+    tc::mbar_init(drain, 1);
+    *abort_flag = 0;
+    tc::fence_barrier_init();
+  }
+  if (warp == 5) tc::tmem_alloc(tmem_slot, tmem_cols);
+  if (warp == 4 && lane == 0) {
+    for (int p = 0; p < P.nprob; ++p) {
+      tc::prefetch_tmap(&P.prob[p].tmA);
+      tc::prefetch_tmap(&P.prob[p].tmB);
+    }
+  }
+  tc::tc_fence_before();
+  // the peer's barriers are initialised before any copy or commit of this CTA reaches them
+  tc::cluster_sync();
+  tc::tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 4) {
+    // ---------------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      const uint64_t pol_normal = tc::policy_evict_normal(), pol_last = tc::policy_evict_last();
+      int stage = 0, issued = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int pt = v0; pt < PT && ok; pt += NP) {
+        const PairTile q = decode_pair(P, pt);
+        const Problem &pr = P.prob[q.p];
+        const int tn = 2 * q.j + rank;
+        const uint64_t pa = pr.pol_a == 2 ? pol_last : pol_normal, pb = pr.pol_b == 2 ? pol_last : pol_normal;
+        for (int kb = 0; kb < pr.kblocks; ++kb) {
+          if (!(ok = tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag))) break;
+          uint8_t *sa = smem + stage * stage_bytes;
+          tc::mbar_expect_tx(&full[stage], stage_bytes);
+          const int k0 = kb * BK;
+          tc::tma_load_2d(sa, &pr.tmA, &full[stage], k0, q.g * pr.N + tn * BM, pa);
+          tma_load_2d_mc(sa + a_bytes + rank * b_half, &pr.tmB, &full[stage], q.g * pr.Kg + k0,
+                         q.tm * kPairBN + rank * 128, kBoth, pb);
+          ++issued;
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      // every copy into this CTA has landed before it can exit (the peer's halves included)
+      for (int i = issued - S > 0 ? issued - S : 0; i < issued; ++i) {
+        const uint64_t t0 = tc::global_ns();
+        while (!tc::mbar_try_wait(&full[i % S], (uint32_t)((i / S) & 1)) && tc::global_ns() - t0 < tc::kWaitLimitNs) {
+        }
+      }
+    }
+  } else if (warp == 5) {
+    // ---------------------------------------------------------------- MMA issue
+    if (lane == 0) {
+      const uint32_t idesc = tc::idesc_bf16_f32(BM, kPairBN);
+      int stage = 0, buf = 0;
+      uint32_t phase = 0;
+      int used[2] = {0, 0};
+      bool ok = true;
+      for (int pt = v0; pt < PT && ok; pt += NP) {
+        const PairTile q = decode_pair(P, pt);
+        const int kblocks = P.prob[q.p].kblocks;
+        if (!(ok = tc::mbar_wait(&acce[buf], (uint32_t)(used[buf] & 1) ^ 1u, abort_flag))) break;
+        tc::tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)(buf * kPairBN);
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!(ok = tc::mbar_wait(&full[stage], phase, abort_flag))) break;
+          tc::tc_fence_after();
+          const uint32_t sa = tc::smem_u32(smem + stage * stage_bytes);
+          const uint64_t ad = tc::sdesc_sw128(sa, 16, 1024);
+          const uint64_t bd = tc::sdesc_sw128(sa + a_bytes, 16, 1024);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            tc::mma_bf16(d, ad + 2ull * k, bd + 2ull * k, idesc, (kb == 0 && k == 0) ? 0u : 1u);
+          mma_commit_mc(&empty[stage], kBoth);  // both CTAs may refill their halves of this stage
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        tc::mma_commit(&accf[buf]);
+        ++used[buf];
+        buf ^= 1;
+      }
+      // every MMA issued (and every commit it makes to either CTA) has completed once this arrives
+      tc::mma_commit(drain);
+      const uint64_t t0 = tc::global_ns();
+      while (!tc::mbar_try_wait(drain, 0) && tc::global_ns() - t0 < tc::kWaitLimitNs) {
+      }
+    }
+  } else if (warp < 4) {
+    // ---------------------------------------------------------------- epilogue (warps 0-3)
+    const int row = warp * 32 + lane;  // feature within the tile
+    int buf = 0, done[2] = {0, 0};
+    for (int pt = v0; pt < PT; pt += NP) {
+      const PairTile q = decode_pair(P, pt);
+      const Problem &pr = P.prob[q.p];
+      const int f = (2 * q.j + rank) * BM + row;
+      const bool f_ok = f < pr.N;
+      bf16 *ycol = pr.y + (int64_t)q.g * pr.N + f;
+      if (!tc::mbar_wait(&accf[buf], (uint32_t)(done[buf] & 1), abort_flag)) break;
+      tc::tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(buf * kPairBN);
+      for (int c0 = 0; c0 < kPairBN; c0 += 16) {
+        uint32_t r[16];
+        tc::tmem_ld16(taddr + (uint32_t)c0, r);
+        tc::tmem_ld_wait();
+        if (f_ok) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int jt = q.tm * kPairBN + c0 + i;
+            if (jt < pr.M) ycol[(int64_t)jt * pr.ldy] = __float2bfloat16_rn(__uint_as_float(r[i]));
+          }
+        }
+      }
+      tc::tc_fence_before();
+      tc::mbar_arrive(&acce[buf]);
+      ++done[buf];
+      buf ^= 1;
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  // neither CTA exits while the other may still copy into it or commit to its barriers
+  tc::cluster_sync();
+  if (warp == 5) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem_base, tmem_cols);
+  }
+  if (threadIdx.x == 0 && *abort_flag) atomicOr(P.status, kStatusTimeout);
+}
+
 // ---- host ---------------------------------------------------------------------------------------
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -1151,6 +1351,10 @@ cudaError_t launch_gemm_tc(const LinearProblem *probs, int nprob, float *ws, siz
   P.stages = per_sm == 2 ? std::min(5, (100 * 1024) / stage_bytes)
                          : std::min(8, ((f8 ? 222 : 200) * 1024 - conv_bytes) / stage_bytes);
   if (P.stages < 2) return cudaErrorInvalidValue;
+  // many token tiles (prefill): clusters of two CTAs on adjacent weight tiles sharing the token tile,
+  // when every problem has an even number of weight tiles
+  bool pairs = !f8 && P.BN == 256 && ATOMS == 1 && M >= 2048;
+  for (int i = 0; i < nprob; ++i) pairs = pairs && ((probs[i].N + BM - 1) / BM) % 2 == 0;
   int units = 0, tiles = 0;
   for (int i = 0; i < nprob; ++i) {
     const LinearProblem &q = probs[i];
@@ -1164,7 +1368,8 @@ cudaError_t launch_gemm_tc(const LinearProblem *probs, int nprob, float *ws, siz
     } else if (!map_2d(&p.tmA, q.W, (uint64_t)q.K, (uint64_t)q.N * q.groups, (uint64_t)q.ldw, BK, BM)) {
       return cudaErrorInvalidValue;
     }
-    if (!map_2d(&p.tmB, q.x, (uint64_t)q.K * q.groups, (uint64_t)M, (uint64_t)q.ldx, BK, (uint32_t)P.BN))
+    if (!map_2d(&p.tmB, q.x, (uint64_t)q.K * q.groups, (uint64_t)M, (uint64_t)q.ldx, BK,
+                (uint32_t)(pairs ? P.BN / 2 : P.BN)))  // pairs: each CTA copies half the token tile
       return cudaErrorInvalidValue;
     p.y = q.y;
     p.ldy = q.ldy;
@@ -1237,6 +1442,33 @@ cudaError_t launch_gemm_tc(const LinearProblem *probs, int nprob, float *ws, siz
   P.counters = reinterpret_cast<int *>(ws);
   P.partials = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(ws) + kCounterBytes);
   P.status = status;
+  if (pairs) {
+    const size_t psmem = 1024 + (size_t)P.stages * stage_bytes + (size_t)(2 * P.stages + 5) * 8 + 16;
+    static SmemAttr attr_pairs;
+    cudaError_t e = attr_pairs.ensure((const void *)k_gemm_tc_pairs, 227 * 1024);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = psmem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    // as many clusters as fit on the GPU at once (an SM each CTA), at most one per pair tile
+    cfg.gridDim = dim3(2 * (num_sms / 2));
+    int nclusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&nclusters, (const void *)k_gemm_tc_pairs, &cfg);
+    if (e != cudaSuccess) return e;
+    nclusters = std::min(std::max(nclusters, 1), std::max(1, tiles / 2));
+    cfg.gridDim = dim3(2 * nclusters);
+    e = cudaLaunchKernelEx(&cfg, k_gemm_tc_pairs, P);
+    return e == cudaSuccess ? cudaGetLastError() : e;
+  }
   const size_t smem = 1024 + (size_t)P.stages * stage_bytes + conv_bytes +
                       (size_t)(2 * P.stages + 2 * P.cstages + 8) * 8 + 64 + kMaxContrib * sizeof(int);
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
