@@ -700,7 +700,13 @@ int attn_v41_forward(csa_ctx *ctx, const csa_layer_weights *w, csa_layer_state *
     const int S = csa::gemm_tc_split_count(px, np, ctx->num_sms, std::max(1, ctx->xpart_rows / NT));
     // x finish, next, is a programmatic dependent that reads the slices only after its dependency wait
     for (int i = 0; i < np; ++i) px[i].early_dependents = 1;
-    STEP(csa::launch_gemm_tc_split(px, np, S, ctx->status, s), "proj x");
+    // many tokens and one slice: the paired-CTA kernel writes the f32 slice itself
+    bool paired = S == 1 && NT >= 2048;
+    for (int i = 0; i < np; ++i) paired = paired && csa::gemm_tc_supported(px[i]);
+    if (paired)
+      STEP(csa::launch_gemm_tc(px, np, ctx->ws, ctx->gemm_ws_bytes(), ctx->num_sms, ctx->status, s), "proj x");
+    else
+      STEP(csa::launch_gemm_tc_split(px, np, S, ctx->status, s), "proj x");
     csa::XFinishArgs xa{ctx->xpart, S, ldp, g.q_rank, hd, idx_src ? Hi : 0, w->q_norm, w->kv_norm, g.eps, qr, kv, B,
                         T, start_pos, rd, tab, (bf16 *)st->window, W, win_idx, idx_stride,
                         dbg ? dbg->kv_codes : nullptr, dbg ? dbg->kv_scale : nullptr,

@@ -101,6 +101,10 @@ cudaError_t set_gemm_stall(unsigned long long ns);
 // Split-K without fixup: products sharing M and K; CTA (tile, s) writes its f32 partial sum over
 // its K range to part[s][m][col] (every problem's part/ldp set).  The consumer sums the S slices.
 cudaError_t launch_gemm_tc_split(const LinearProblem *probs, int nprob, int S, int *status, cudaStream_t s);
+// The Stream-K / waves / paired launch of up to four problems sharing the activations (the paired
+// kernel, chosen for many token tiles, may write a problem's f32 result to `part` as one split slice).
+cudaError_t launch_gemm_tc(const LinearProblem *probs, int nprob, float *ws, size_t ws_bytes, int num_sms,
+                           int *status, cudaStream_t s);
 // The largest split count S <= max_S dividing the problems' k-slices with tiles * S <= max_ctas (>= 1).
 int gemm_tc_split_count(const LinearProblem *probs, int nprob, int max_ctas, int max_S);
 bool gemm_tc_supported(const LinearProblem &q);

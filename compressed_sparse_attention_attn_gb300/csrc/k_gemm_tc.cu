@@ -1066,15 +1066,18 @@ __device__ __forceinline__ void mma_commit_mc(uint64_t *bar, uint16_t mask) {
                : "memory");
 }
 
-// Pair tile pt of the launch: problem, token tile, weight-tile pair, group.
+// Pair tile pt of the launch: problem, token tile, weight-tile pair, group.  A problem with an odd
+// number of weight tiles has a last pair whose second tile lies past N (its copies read zeros or the
+// next group's rows, its stores are masked).
 struct PairTile {
   int p, tm, j, g;
 };
+__device__ __forceinline__ int pair_tiles_of(const Problem &pr) { return pr.tiles_m * ((pr.tiles_n + 1) / 2) * pr.groups; }
 __device__ __forceinline__ PairTile decode_pair(const Params &P, int pt) {
-  int p = 0;
-  while (p + 1 < P.nprob && pt >= P.prob[p + 1].tile_begin / 2) ++p;
+  int p = 0, begin = 0;
+  while (p + 1 < P.nprob && pt >= begin + pair_tiles_of(P.prob[p])) begin += pair_tiles_of(P.prob[p++]);
   const Problem &pr = P.prob[p];
-  const int local = pt - pr.tile_begin / 2, half_n = pr.tiles_n / 2;
+  const int local = pt - begin, half_n = (pr.tiles_n + 1) / 2;
   return PairTile{p, local % pr.tiles_m, (local / pr.tiles_m) % half_n, local / (pr.tiles_m * half_n)};
 }
 
@@ -1097,7 +1100,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc_pairs(const __grid_cons
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = (int)tc::cluster_ctarank();
-  const int v0 = blockIdx.x >> 1, NP = gridDim.x >> 1, PT = P.total_tiles / 2;
+  const int v0 = blockIdx.x >> 1, NP = gridDim.x >> 1;
+  int PT = 0;
+  for (int p = 0; p < P.nprob; ++p) PT += pair_tiles_of(P.prob[p]);
   constexpr uint16_t kBoth = 3;
   constexpr uint32_t tmem_cols = 2 * kPairBN;
 
@@ -1210,7 +1215,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc_pairs(const __grid_cons
       const Problem &pr = P.prob[q.p];
       const int f = (2 * q.j + rank) * BM + row;
       const bool f_ok = f < pr.N;
-      bf16 *ycol = pr.y + (int64_t)q.g * pr.N + f;
+      bf16 *ycol = pr.y ? pr.y + (int64_t)q.g * pr.N + f : nullptr;
+      float *pcol = pr.part ? pr.part + (int64_t)q.g * pr.N + f : nullptr;  // f32 result (one split slice)
       if (!tc::mbar_wait(&accf[buf], (uint32_t)(done[buf] & 1), abort_flag)) break;
       tc::tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(buf * kPairBN);
@@ -1218,7 +1224,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc_pairs(const __grid_cons
         uint32_t r[16];
         tc::tmem_ld16(taddr + (uint32_t)c0, r);
         tc::tmem_ld_wait();
-        if (f_ok) {
+        if (f_ok && pcol) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int jt = q.tm * kPairBN + c0 + i;
+            if (jt < pr.M) pcol[(int64_t)jt * pr.ldp] = __uint_as_float(r[i]);
+          }
+        } else if (f_ok) {
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int jt = q.tm * kPairBN + c0 + i;
@@ -1351,10 +1363,10 @@ cudaError_t launch_gemm_tc(const LinearProblem *probs, int nprob, float *ws, siz
   P.stages = per_sm == 2 ? std::min(5, (100 * 1024) / stage_bytes)
                          : std::min(8, ((f8 ? 222 : 200) * 1024 - conv_bytes) / stage_bytes);
   if (P.stages < 2) return cudaErrorInvalidValue;
-  // many token tiles (prefill): clusters of two CTAs on adjacent weight tiles sharing the token tile,
-  // when every problem has an even number of weight tiles
-  bool pairs = !f8 && P.BN == 256 && ATOMS == 1 && M >= 2048;
-  for (int i = 0; i < nprob; ++i) pairs = pairs && ((probs[i].N + BM - 1) / BM) % 2 == 0;
+  // many token tiles (prefill): clusters of two CTAs on adjacent weight tiles sharing the token tile
+  const bool pairs = !f8 && P.BN == 256 && ATOMS == 1 && M >= 2048;
+  for (int i = 0; i < nprob; ++i)  // an f32 result (a split-K slice layout) only from the paired kernel
+    if (probs[i].part && !pairs) return cudaErrorInvalidValue;
   int units = 0, tiles = 0;
   for (int i = 0; i < nprob; ++i) {
     const LinearProblem &q = probs[i];
@@ -1373,6 +1385,8 @@ cudaError_t launch_gemm_tc(const LinearProblem *probs, int nprob, float *ws, siz
       return cudaErrorInvalidValue;
     p.y = q.y;
     p.ldy = q.ldy;
+    p.part = q.part;
+    p.ldp = q.ldp;
     p.N = q.N;
     p.M = M;
     p.groups = q.groups;
@@ -1464,7 +1478,10 @@ cudaError_t launch_gemm_tc(const LinearProblem *probs, int nprob, float *ws, siz
     int nclusters = 0;
     e = cudaOccupancyMaxActiveClusters(&nclusters, (const void *)k_gemm_tc_pairs, &cfg);
     if (e != cudaSuccess) return e;
-    nclusters = std::min(std::max(nclusters, 1), std::max(1, tiles / 2));
+    int pair_tiles = 0;
+    for (int i = 0; i < nprob; ++i)
+      pair_tiles += P.prob[i].tiles_m * ((P.prob[i].tiles_n + 1) / 2) * P.prob[i].groups;
+    nclusters = std::min(std::max(nclusters, 1), std::max(1, pair_tiles));
     cfg.gridDim = dim3(2 * nclusters);
     e = cudaLaunchKernelEx(&cfg, k_gemm_tc_pairs, P);
     return e == cudaSuccess ? cudaGetLastError() : e;
