@@ -20,6 +20,9 @@
 // Prefill-sized launches (many token tiles, activations far beyond L2) run k_gemm_tc_waves instead:
 // whole tiles in data-parallel waves (CTA c takes tiles c, c + G, ...), so that the tiles in flight
 // together are consecutive ones whose operands share L2, then Stream-K over the last partial wave.
+// Launches of 2048 tokens or more on bf16 weights go one step further, to k_gemm_tc_pairs: clusters
+// of two CTAs on neighbouring weight tiles of one 256-token tile, each copying half of the token
+// tile and multicasting it into both (a third less L2 operand traffic a CTA).
 // L2 policies follow the reuse: weights read by one token tile only stream past evict-first,
 // activations small next to L2 stay evict-last, everything else is normal.
 //
