@@ -192,29 +192,35 @@ __device__ __forceinline__ void rope_q_angles(const Params &P, int t, int tid, f
     }
   }
 }
+// Turn one 16-byte chunk of q in shared memory (features f0 .. f0+7 of head h, four adjacent pairs)
+// by the angles cs (cos, sin of each pair).
+__device__ __forceinline__ void rope_q_chunk(uint8_t *sq, int h, int f0, const float (&cs)[8]) {
+  uint8_t *cp = sq + (f0 / 64) * HG * 128 + h * 128 + ((((f0 % 64) / 8) ^ (h & 7)) << 4);
+  uint4 x = *reinterpret_cast<const uint4 *>(cp);
+  __nv_bfloat162 *pv = reinterpret_cast<__nv_bfloat162 *>(&x);
+#pragma unroll
+  for (int jj = 0; jj < 4; ++jj) {
+    const float a = __low2float(pv[jj]), bb = __high2float(pv[jj]), c = cs[2 * jj], sn = cs[2 * jj + 1];
+    const float re = __fsub_rn(__fmul_rn(a, c), __fmul_rn(bb, sn));
+    const float im = __fadd_rn(__fmul_rn(a, sn), __fmul_rn(bb, c));
+    pv[jj] = __halves2bfloat162(__float2bfloat16_rn(re), __float2bfloat16_rn(im));
+  }
+  *reinterpret_cast<uint4 *>(cp) = x;
+}
 __device__ __forceinline__ void rope_q_apply(const Params &P, uint8_t *sq, int tid, const float4 (&qcs)[2][2]) {
   const int q_tail = HD - P.rd, q_nch = P.rd / 8;
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
     const int u = tid + 256 * k;
     if (u >= HG * q_nch) continue;
-    const int h = u / q_nch, f0 = q_tail + 8 * (u % q_nch);
-    uint8_t *cp = sq + (f0 / 64) * HG * 128 + h * 128 + ((((f0 % 64) / 8) ^ (h & 7)) << 4);
-    uint4 x = *reinterpret_cast<const uint4 *>(cp);
     const float cs[8] = {qcs[k][0].x, qcs[k][0].y, qcs[k][0].z, qcs[k][0].w,
                          qcs[k][1].x, qcs[k][1].y, qcs[k][1].z, qcs[k][1].w};
-    __nv_bfloat162 *pv = reinterpret_cast<__nv_bfloat162 *>(&x);
-#pragma unroll
-    for (int jj = 0; jj < 4; ++jj) {
-      const float a = __low2float(pv[jj]), bb = __high2float(pv[jj]), c = cs[2 * jj], sn = cs[2 * jj + 1];
-      const float re = __fsub_rn(__fmul_rn(a, c), __fmul_rn(bb, sn));
-      const float im = __fadd_rn(__fmul_rn(a, sn), __fmul_rn(bb, c));
-      pv[jj] = __halves2bfloat162(__float2bfloat16_rn(re), __float2bfloat16_rn(im));
-    }
-    *reinterpret_cast<uint4 *>(cp) = x;
+    rope_q_chunk(sq, u / q_nch, q_tail + 8 * (u % q_nch), cs);
   }
   fence_proxy_async();  // the turned q is read by the MMA (async proxy)
 }
+
+cudaError_t launch_sparse_attn_queries_tc(const Params &p, int units, int num_sms, cudaStream_t s);
 
 }  // namespace attn
 }  // namespace csa

@@ -589,6 +589,12 @@ cudaError_t launch_sparse_attn_tc(const AttnArgs &a, float *ws, size_t ws_bytes,
   }
   p.tpc = tpc;
   p.nsplit = (p.ntiles + tpc - 1) / tpc;
+  // many units held whole (a prefill chunk): a persistent CTA an SM takes a sequence of them, the work
+  // between two units overlapping the tile pipeline
+  if (p.nsplit == 1 && (int64_t)nq * groups >= 2 * (int64_t)num_sms) {
+    *kernels = 1;
+    return launch_sparse_attn_queries_tc(p, nq * groups, num_sms, s);
+  }
   uint8_t *base = reinterpret_cast<uint8_t *>(ws) + kGemmCounterBytes;
   p.part_o = reinterpret_cast<bf16 *>(base);
   p.part_ml = reinterpret_cast<float *>(base + (size_t)nq * p.nsplit * a.H * HD * sizeof(bf16));

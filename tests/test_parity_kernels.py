@@ -451,11 +451,14 @@ def test_sparse_attn(csa, orc, H, hd, na, nb, a_len, b_len, B, T):
     assert_close_bf16(to_np(o_rot), want_rot, what="sparse_attn o_rot")
 
 
-@pytest.mark.parametrize("T,nb,b_len,keep", [(300, 512, 200, 0.8), (260, 256, 600, 0.5)])
+@pytest.mark.parametrize("T,nb,b_len,keep", [(300, 512, 200, 0.8), (260, 256, 600, 0.5), (700, 512, 300, 0.6),
+                                              (1000, 256, 900, 0.3)])
 def test_sparse_attn_prefill_lists(csa, orc, T, nb, b_len, keep):
     """Prefill-shaped lists, one CTA a query over its whole list: the causal window of the chunk's own
     rows (its first entries -1 for early queries, so whole 64-entry halves are empty) and compressed
-    entries with runs of -1 (some halves empty, some partial)."""
+    entries with runs of -1 (some halves empty, some partial).  From a few hundred queries on, the
+    queries run on the persistent kernel (a CTA an SM taking a sequence of them): there a query with
+    nothing selected in the middle of a CTA's sequence writes zeros and the next one is unaffected."""
     rng = np.random.default_rng(31 + T)
     H, hd, W, B = 64, 512, 128, 1
     q = _rng_bf16(orc, rng, (T, H, hd))
@@ -470,6 +473,9 @@ def test_sparse_attn_prefill_lists(csa, orc, T, nb, b_len, keep):
     ib[:, 64:192] = -1            # two empty halves in the middle of the compressed part
     ib[5, :] = -1
     ia[7, :] = -1                 # a query with compressed rows only
+    if T > 400:
+        ia[T - 300, :] = -1       # nothing selected, between two queries of the same CTA
+        ib[T - 300, :] = -1
     scale = 1 / math.sqrt(hd)
     rd = 64
     tab = orc.rope_table(rd, max(64, T), 10000.0)
@@ -481,4 +487,7 @@ def test_sparse_attn_prefill_lists(csa, orc, T, nb, b_len, keep):
     ctx.sparse_attn(to_dev(q), to_dev(ra), T, to_dev(ia), to_dev(sink), scale, rows_b=to_dev(rb), b_len=b_len,
                     idx_b=to_dev(ib), o_rot=o_rot, rd=rd, start_pos=0, tab=to_dev(tab), B=B, T=T)
     assert ctx.status() == 0
-    assert_close_bf16(to_np(o_rot), want_rot, what="sparse_attn o_rot (prefill lists)")
+    got = to_np(o_rot)
+    if T > 400:
+        assert ((got[T - 300] & 0x7FFF) == 0).all()  # zeros (the inverse rotation may leave -0)
+    assert_close_bf16(got, want_rot, what="sparse_attn o_rot (prefill lists)")
