@@ -12,7 +12,7 @@
 //     the last scores MMA of the unit before has read q;
 //   * warps 0-7 start copying the next unit's first tile as soon as the last P.V chunks have freed
 //     its K-blocks, and write the finished unit's result (staged a warp at a time through the P
-//     buffer, 16-byte stores) while those rows are in flight;
+//     buffer, 16-byte stores) while that tile's scores are formed;
 //   * warp 8 issues the MMAs of consecutive units without a break (TMEM allocated once).
 // Every mbarrier wait is time-bounded.
 #include "attn_common.cuh"
@@ -278,31 +278,49 @@ __global__ void __launch_bounds__(kQThreads, 1) k_sparse_attn_queries_tc(const _
 #pragma unroll
     for (int h = 0; h < 32; ++h) lsum[h] = 0.f;
     int G = 0;  // tiles completed so far (all units): the barriers' phases
-    // The result of the unit before (row pr_row, head group pr_hg, pr_live tiles with rows): the
-    // sums over the CTA, the factor with the sink, then O * f a 128-feature chunk at a time, staged
-    // per warp in the P buffer (its last reader, the P.V of tile G - 1, has completed) and written
-    // with 16-byte stores.  Leaves m = -inf and the sums at 0 for the next unit.
+    // A unit's result in two steps.  finish_sums, right after its last softmax (overlapping its last
+    // P.V): the sums over the CTA, the factor f with the sink, the inverse rotation's angles of this
+    // lane's last-chunk features; m back to -inf and the sums to 0 for the next unit.  finish_write,
+    // once the next unit's first rows are published to the MMA (so its scores are formed meanwhile):
+    // O * f a 128-feature chunk at a time, staged per warp in the P buffer (its last reader, the
+    // unit's last P.V, has completed) and written with 16-byte stores.
     int64_t pr_row = -1;
     int pr_hg = 0, pr_live = 0;
-    auto finish = [&]() -> bool {
+    bool pending = false;
+    const int tail = HD - P.rd;
+    const int d3 = 3 * 128 + quad * 32 + (lane & 3) * 8;  // this lane's first feature of the last chunk
+    float4 rc01 = make_float4(0.f, 0.f, 0.f, 0.f), rc23 = rc01;
+    auto finish_sums = [&](int64_t row, int hg, int live) -> bool {
       red_sum[quad * HG + hh + lane] = warp_reduce_32<false>(lsum, lane);
 #pragma unroll
       for (int h = 0; h < 32; ++h) lsum[h] = 0.f;
+      if (P.o_rot && d3 >= tail) {
+        const float2 *tp = reinterpret_cast<const float2 *>(P.tab) + (int64_t)(P.start_pos + row % P.T) * (P.rd >> 1);
+        rc01 = *reinterpret_cast<const float4 *>(tp + ((d3 - tail) >> 1));
+        rc23 = *reinterpret_cast<const float4 *>(tp + ((d3 - tail) >> 1) + 2);
+      }
       if (!sm_sync()) return false;
       if (tid < HG) {
         const float l = (red_sum[tid] + red_sum[HG + tid]) + (red_sum[2 * HG + tid] + red_sum[3 * HG + tid]);
-        const float s2 = P.sink[pr_hg * HG + tid] * 1.4426950408889634f;
+        const float s2 = P.sink[hg * HG + tid] * 1.4426950408889634f;
         const float M = fmaxf(m_sm[tid], s2);
-        const float em = pr_live > 0 ? exp2f(m_sm[tid] - M) : 0.f;
+        const float em = live > 0 ? exp2f(m_sm[tid] - M) : 0.f;
         f_sm[tid] = em / (l * em + exp2f(s2 - M));
         m_sm[tid] = -INFINITY;
       }
       if (!sm_sync()) return false;
+      pr_row = row;
+      pr_hg = hg;
+      pr_live = live;
+      pending = true;
+      return true;
+    };
+    auto finish_write = [&]() -> bool {
+      pending = false;
       if (G > 0 && !tc::mbar_wait(&pv_done[3], (uint32_t)((G - 1) & 1), abort_flag)) return false;
       tc::tc_fence_after();
-      const int t = (int)(pr_row % P.T);
-      const float2 *tp =
-          P.o_rot ? reinterpret_cast<const float2 *>(P.tab) + (int64_t)(P.start_pos + t) * (P.rd >> 1) : nullptr;
+      const float2 *tp = P.o_rot ? reinterpret_cast<const float2 *>(P.tab) + (int64_t)(P.start_pos + pr_row % P.T) * (P.rd >> 1)
+                                 : nullptr;
       bf16 *stg = reinterpret_cast<bf16 *>(sP + warp * 2048);  // [32 heads][32 features]
       const int64_t obase = (pr_row * P.H + pr_hg * HG + hh) * (int64_t)HD;
 #pragma unroll 1
@@ -322,12 +340,41 @@ __global__ void __launch_bounds__(kQThreads, 1) k_sparse_attn_queries_tc(const _
           for (int k = 0; k < 16; ++k) stg[(h0 + k) * 32 + lane] = __float2bfloat16_rn(v[h0 + k] * fv[k]);
         }
         __syncwarp();
+        // lane l writes features d0 .. d0+7 (d0 the same for all four of its vectors) of heads
+        // l/4, l/4 + 8, l/4 + 16, l/4 + 24
+        const int d0 = c * 128 + quad * 32 + (lane & 3) * 8;
+        const bool turn = P.o_rot && d0 >= tail;
+        float2 cs[4] = {make_float2(rc01.x, rc01.y), make_float2(rc01.z, rc01.w), make_float2(rc23.x, rc23.y),
+                        make_float2(rc23.z, rc23.w)};
+        if (turn && c < 3) {  // (features below the last chunk turn only when rope_dim > 128)
+          const float4 c01 = *reinterpret_cast<const float4 *>(tp + ((d0 - tail) >> 1));
+          const float4 c23 = *reinterpret_cast<const float4 *>(tp + ((d0 - tail) >> 1) + 2);
+          cs[0] = make_float2(c01.x, c01.y);
+          cs[1] = make_float2(c01.z, c01.w);
+          cs[2] = make_float2(c23.x, c23.y);
+          cs[3] = make_float2(c23.z, c23.w);
+        }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const int vi = lane + 32 * k, h = vi >> 2, seg = vi & 3;
-          const uint4 ob = *reinterpret_cast<const uint4 *>(stg + h * 32 + seg * 8);
-          const int d0 = c * 128 + quad * 32 + seg * 8;
-          store_out(P.o, P.o_rot, obase + (int64_t)h * HD + d0, d0, HD - P.rd, tp, ob);
+          const int h = (lane >> 2) + 8 * k;
+          const uint4 ob = *reinterpret_cast<const uint4 *>(stg + h * 32 + (lane & 3) * 8);
+          const int64_t off = obase + (int64_t)h * HD + d0;
+          if (P.o) *reinterpret_cast<uint4 *>(P.o + off) = ob;
+          if (P.o_rot) {
+            uint4 orr = ob;
+            if (turn) {
+              const bf16 *xb = reinterpret_cast<const bf16 *>(&ob);
+              bf16 *yb = reinterpret_cast<bf16 *>(&orr);
+#pragma unroll
+              for (int qq = 0; qq < 4; ++qq) {
+                float re, im;
+                unrotate(__bfloat162float(xb[2 * qq]), __bfloat162float(xb[2 * qq + 1]), cs[qq], re, im);
+                yb[2 * qq] = __float2bfloat16_rn(re);
+                yb[2 * qq + 1] = __float2bfloat16_rn(im);
+              }
+            }
+            *reinterpret_cast<uint4 *>(P.o_rot + off) = orr;
+          }
         }
         __syncwarp();
       }
@@ -347,11 +394,11 @@ __global__ void __launch_bounds__(kQThreads, 1) k_sparse_attn_queries_tc(const _
         // P.V chunk: refill it
         if (G > 0 && !(ok = tc::mbar_wait(&pv_done[pw], (uint32_t)((G - 1) & 1), abort_flag))) break;
         issue_tile(srcj + i * TILE);
-        // the unit before is finished while this unit's first rows are in flight
-        if (n == 0 && j > 0 && !(ok = finish())) break;
         cp_async_wait_all();
         fence_proxy_async();
         tc::mbar_arrive(&g_full[pw]);
+        // the unit before is written while this unit's first scores are formed
+        if (pending && !(ok = finish_write())) break;
         {  // the next tile's segments of this warp's K-block on their way to L2 while this one is used
           int nx = i + 1;
           while (nx < P.ntiles && !tile_live(wc, nx)) ++nx;
@@ -452,13 +499,11 @@ __global__ void __launch_bounds__(kQThreads, 1) k_sparse_attn_queries_tc(const _
       if (!ok) break;
       // this unit's lists are no longer read
       tc::mbar_arrive(&list_free[bj]);
-      // a unit without rows: the unit before is finished here
-      if (n == 0 && j > 0 && !(ok = finish())) break;
-      pr_row = unit_row(j);
-      pr_hg = unit_hg(j);
-      pr_live = n;
+      // a unit without rows: the unit before is written here
+      if (pending && !(ok = finish_write())) break;
+      if (!(ok = finish_sums(unit_row(j), unit_hg(j), n))) break;
     }
-    if (ok && nmy > 0) ok = finish();  // the last unit's result
+    if (ok && pending) ok = finish_write();  // the last unit's result
     cp_async_wait_all();
   }
   tc::tc_fence_before();
