@@ -700,6 +700,8 @@ int attn_v41_forward(csa_ctx *ctx, const csa_layer_weights *w, csa_layer_state *
     const int S = csa::gemm_tc_split_count(px, np, ctx->num_sms, std::max(1, ctx->xpart_rows / NT));
     // x finish, next, is a programmatic dependent that reads the slices only after its dependency wait
     for (int i = 0; i < np; ++i) px[i].early_dependents = 1;
+    // and it is itself one of the kernel before (the layer's input is read after the wait)
+    for (int i = 0; i < np; ++i) px[i].pdl = 1;
     // many tokens and one slice: the paired-CTA kernel writes the f32 slice itself
     bool paired = S == 1 && NT >= 2048;
     for (int i = 0; i < np; ++i) paired = paired && csa::gemm_tc_supported(px[i]);
@@ -729,6 +731,7 @@ int attn_v41_forward(csa_ctx *ctx, const csa_layer_weights *w, csa_layer_state *
     csa::LinearProblem pq[2] = {lin(qr, g.q_rank, g.q_rank, w->wq_b, H * hd, q, H * hd, 1),
                                 lin(qr, g.q_rank, g.q_rank, w->idx_wq_b, Hi * dI, qI, Hi * dI, 1)};
     pq[0].early_dependents = pq[1].early_dependents = fused_sel ? 1 : 0;
+    pq[0].pdl = pq[1].pdl = 1;  // (x finish lets it start early)
     STEP(csa::launch_linear(pq, idx_src ? 2 : 1, ctx->ws, ctx->gemm_ws_bytes(), ctx->num_sms, ctx->status, s), "proj qr");
   }
   // the sparse attention's arguments: the selection's buffers are known before the index stages fill
@@ -811,8 +814,12 @@ int attn_v41_forward(csa_ctx *ctx, const csa_layer_weights *w, csa_layer_state *
       pa.w8_scale = w->wo_a_scale;
       pa.ldw = gw;
     }
+    // wo_a and wo_b: programmatic dependents of the kernels before them (their weights start to stream
+    // while those finish), each letting the next launch early
+    pa.pdl = pa.early_dependents = 1;
     STEP(csa::launch_linear(&pa, 1, ctx->ws, ctx->gemm_ws_bytes(), ctx->num_sms, ctx->status, s), "wo_a");
     csa::LinearProblem pb = lin(og, G * g.o_rank, G * g.o_rank, w->wo_b, g.dim, out, g.dim, 1);
+    pb.pdl = pb.early_dependents = 1;
     STEP(csa::launch_linear(&pb, 1, ctx->ws, ctx->gemm_ws_bytes(), ctx->num_sms, ctx->status, s), "wo_b");
   }
 #undef STEP

@@ -89,6 +89,9 @@ struct LinearProblem {
   // product's output only after its dependency wait, so the tensor-core launch lets it start as soon
   // as this grid's CTAs have started (set on every problem of the launch)
   int early_dependents = 0;
+  // 1: launched as a programmatic dependent of the kernel before it (decode-sized launches): the
+  // weights of each CTA's first stages are copied before the dependency wait, the activations after
+  int pdl = 0;
 };
 // Products sharing M run in one tensor-core launch (up to 4 at a time).  ws/ws_bytes: Stream-K
 // arrival counters and partials (the counters must be zero between launches).

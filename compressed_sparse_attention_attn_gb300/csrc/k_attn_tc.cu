@@ -110,7 +110,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
   if (warp == 8) tc::tmem_alloc(tmem_slot, kCols);
   // Launched as a programmatic dependent of the selection kernel before it: everything above (and
   // q, written two launches earlier) overlaps that kernel; the index lists it writes are read only
-  // after this wait.
+  // after this wait.  The kernel after (the merge, or wo_a: programmatic dependents reading this
+  // kernel's output after their own waits) may start at once.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // loader geometry: each of warps 0-7 copies one K-block (a 128-byte segment of every row), four
@@ -449,7 +451,9 @@ __global__ void __launch_bounds__(kCombThreads) k_attn_combine(const __grid_cons
       cs[k][1] = *reinterpret_cast<const float4 *>(tp + ((d0 - tail) >> 1) + 2);
     }
   }
-  // (a programmatic dependent of the attention kernel: the shares are read after this wait)
+  // (a programmatic dependent of the attention kernel: the shares are read after this wait; wo_a,
+  // a programmatic dependent of this kernel, may start at once)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   float2 ml[kMaxTiles];
 #pragma unroll

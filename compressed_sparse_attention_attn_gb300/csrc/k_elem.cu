@@ -198,7 +198,9 @@ __global__ void __launch_bounds__(1024) k_x_finish(XFinishArgs a) {
   const float kvn = kv_thread ? __ldg(a.kv_norm + threadIdx.x) : 0.f;
   const float2 cs = kv_thread ? kv_angle(a.tab, a.start_pos + t, a.rd, a.hd, threadIdx.x) : make_float2(1.f, 0.f);
   // a programmatic dependent of the split-K projection writing the slices: nothing is read or written
-  // before that grid has completed
+  // before that grid has completed; the projection after it (also a programmatic dependent, reading
+  // this kernel's output after its own wait) may start at once
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int M = a.B * a.T;
   const int n = a.q_rank + a.hd + a.Hi;
@@ -309,6 +311,7 @@ __global__ void __launch_bounds__(kXRowsWarps * 32) k_x_finish_rows(XFinishArgs 
     for (int k = lane; k < (a.rd >> 1); k += 32)
       cs[k] = reinterpret_cast<const float2 *>(a.tab)[(int64_t)(a.start_pos + t) * (a.rd >> 1) + k];
   __syncthreads();
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (row >= M) return;
   float sq = 0.f, skv = 0.f;

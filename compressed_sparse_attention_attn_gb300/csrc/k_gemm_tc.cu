@@ -85,6 +85,9 @@ struct Params {
   // [0, dp_waves G) in all), then its Stream-K share of the units from sk_unit0 on
   int dp_waves, sk_unit0;
   int early_dependents;  // let a programmatic dependent launch once every CTA here has started
+  // launched as a programmatic dependent of the kernel before it (k_gemm_tc only): the producer
+  // copies the weights of its first stages, then waits for that kernel, then copies their activations
+  int pdl;
   float *partials;  // [grid][2][BM][BN]
   int *counters;    // [total_tiles]
   int *status;
@@ -238,7 +241,10 @@ __global__ void __launch_bounds__(threads_of<kF8>(), kF8 ? 1 : 2) k_gemm_tc(cons
     u0 = (int)cta_start(blockIdx.x, U, G);
     u1 = (int)cta_start(blockIdx.x + 1, U, G);
   }
-  if (u0 >= u1) return;
+  if (u0 >= u1) {
+    if (P.pdl) asm volatile("griddepcontrol.wait;" ::: "memory");  // (this grid ends after the one before)
+    return;
+  }
   const uint32_t tmem_cols = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128 : (2 * BN <= 256) ? 256 : 512;
 
   if (threadIdx.x == 0) {
@@ -287,22 +293,18 @@ __global__ void __launch_bounds__(threads_of<kF8>(), kF8 ? 1 : 2) k_gemm_tc(cons
       const Problem *pr = &P.prob[un.p];
       int tm = un.tile % pr->tiles_m, tn = (un.tile / pr->tiles_m) % pr->tiles_n;
       int g = un.tile / (pr->tiles_m * pr->tiles_n);
-      for (int u = u0; u < u1; ++u) {
-        if (!tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag)) break;
-        uint8_t *sa = smem + stage * stage_bytes;
-        tc::mbar_expect_tx(&full[stage], stage_bytes);
+      // the copies of one unit into a stage: its weights (A) and / or its activations (B)
+      auto load = [&](int st, bool a_part, bool b_part) {
+        uint8_t *sa = smem + st * stage_bytes;
 #pragma unroll
         for (int a = 0; a < KS; ++a) {
           const int k0 = (un.kb * KS + a) * BK;
-          if (!kF8 || a == 0)  // (fp8: one box of 128 codes a row covers both slices)
-            tc::tma_load_2d(sa + a * a_atom, &pr->tmA, &full[stage], k0, g * pr->N + tn * BM, pol_w);
-          tc::tma_load_2d(sa + a_in + a * b_atom, &pr->tmB, &full[stage], g * pr->Kg + k0, tm * BN, pol_x);
+          if (a_part && (!kF8 || a == 0))  // (fp8: one box of 128 codes a row covers both slices)
+            tc::tma_load_2d(sa + a * a_atom, &pr->tmA, &full[st], k0, g * pr->N + tn * BM, pol_w);
+          if (b_part) tc::tma_load_2d(sa + a_in + a * b_atom, &pr->tmB, &full[st], g * pr->Kg + k0, tm * BN, pol_x);
         }
-        ++issued;
-        if (++stage == S) {
-          stage = 0;
-          phase ^= 1;
-        }
+      };
+      auto advance = [&]() {
         if (++un.kb == pr->kblocks) {  // next tile: token tile fastest, then weight tile, then group
           un.kb = 0;
           if (++un.tile == pr->tiles) {
@@ -317,6 +319,45 @@ __global__ void __launch_bounds__(threads_of<kF8>(), kF8 ? 1 : 2) k_gemm_tc(cons
             }
           }
         }
+      };
+      int u = u0;
+      if (P.pdl) {
+        // the weights of the first stages stream in while the kernel before finishes; its output
+        // (the activations) is copied only after the dependency wait
+        const Unit un0 = un;
+        const Problem *pr0 = pr;
+        const int tm0 = tm, tn0 = tn, g0 = g;
+        const int npre = min(S, u1 - u0);
+        for (int i = 0; i < npre; ++i) {
+          tc::mbar_expect_tx(&full[i], stage_bytes);
+          load(i, true, false);
+          advance();
+        }
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        un = un0;
+        pr = pr0;
+        tm = tm0;
+        tn = tn0;
+        g = g0;
+        for (int i = 0; i < npre; ++i) {
+          load(i, false, true);
+          advance();
+        }
+        issued = npre;
+        u = u0 + npre;
+        stage = npre == S ? 0 : npre;
+        phase = npre == S ? 1u : 0u;
+      }
+      for (; u < u1; ++u) {
+        if (!tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag)) break;
+        tc::mbar_expect_tx(&full[stage], stage_bytes);
+        load(stage, true, true);
+        ++issued;
+        if (++stage == S) {
+          stage = 0;
+          phase ^= 1;
+        }
+        advance();
       }
       // let every copy this CTA issued land before the CTA can exit
       for (int i = issued - S > 0 ? issued - S : 0; i < issued; ++i) {
@@ -1406,6 +1447,7 @@ cudaError_t launch_gemm_tc(const LinearProblem *probs, int nprob, float *ws, siz
   }
   P.nprob = nprob;
   for (int q = 0; q < nprob; ++q) P.early_dependents |= probs[q].early_dependents;
+  for (int q = 0; q < nprob; ++q) P.pdl |= probs[q].pdl;
   unify_policies(P, nprob);
   P.total_units = units;
   P.total_tiles = tiles;
@@ -1459,6 +1501,7 @@ cudaError_t launch_gemm_tc(const LinearProblem *probs, int nprob, float *ws, siz
   P.counters = reinterpret_cast<int *>(ws);
   P.partials = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(ws) + kCounterBytes);
   P.status = status;
+  if (pairs || P.dp_waves > 0) P.pdl = 0;  // (the programmatic prologue is k_gemm_tc's)
   if (pairs) {
     const size_t psmem = 1024 + (size_t)P.stages * stage_bytes + (size_t)(2 * P.stages + 5) * 8 + 16;
     static SmemAttr attr_pairs;
@@ -1505,6 +1548,20 @@ cudaError_t launch_gemm_tc(const LinearProblem *probs, int nprob, float *ws, siz
       k_gemm_tc_waves<true><<<grid, kThreadsF8, smem, s>>>(P);
     else
       k_gemm_tc_waves<false><<<grid, kThreads, smem, s>>>(P);
+  } else if (P.pdl) {
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(f8 ? kThreadsF8 : kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    const cudaError_t e = f8 ? cudaLaunchKernelEx(&cfg, k_gemm_tc<true>, P) : cudaLaunchKernelEx(&cfg, k_gemm_tc<false>, P);
+    if (e != cudaSuccess) return e;
   } else {
     if (f8)
       k_gemm_tc<true><<<grid, kThreadsF8, smem, s>>>(P);
@@ -1579,7 +1636,24 @@ cudaError_t launch_gemm_tc_split(const LinearProblem *probs, int nprob, int S, i
     cudaError_t e = attr.ensure((const void *)k_gemm_tc<false>, 227 * 1024);
     if (e != cudaSuccess) return e;
   }
-  k_gemm_tc<false><<<tiles * S, kThreads, smem, s>>>(P);
+  for (int q = 0; q < nprob; ++q) P.pdl |= probs[q].pdl;
+  if (P.pdl) {
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(tiles * S);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, k_gemm_tc<false>, P);
+    if (e != cudaSuccess) return e;
+  } else {
+    k_gemm_tc<false><<<tiles * S, kThreads, smem, s>>>(P);
+  }
   return cudaGetLastError();
 }
 
