@@ -39,11 +39,11 @@ NOMINAL_HBM_GBS = 8000.0
 # run); set to None whenever those kernels change after the capture
 GEMM_TRAFFIC_SOURCE = "ncu capture, profiles/k_gemm_tc_projections_all_workloads.md"
 GEMM_TRAFFIC_BYTES = {
-    "reindex_decode_r2": (19060224 + 0) + (94515968 + 178176) + (69255680 + 12800) + (84573440 + 408064),
-    "longctx_decode_r4": (19388416 + 0) + (94589184 + 529408) + (71355392 + 78336) + (85204224 + 327680),
-    "ratio0_decode": (18731776 + 0) + (84022272 + 150528) + (69256448 + 13568) + (84579840 + 388608),
-    "prefill_r4": (68539136 + 5178880) + (104948736 + 249565952) + (425600768 + 50698240) +
-                  (400599808 + 33128704),
+    "reindex_decode_r2": (19072000 + 0) + (94519040 + 151808) + (69267712 + 6656) + (84563712 + 164608),
+    "longctx_decode_r4": (19400960 + 0) + (94602496 + 142592) + (71365888 + 62208) + (85174272 + 237056),
+    "ratio0_decode": (18744320 + 0) + (84032000 + 179712) + (69281792 + 12800) + (84606208 + 143872),
+    "prefill_r4": (68472320 + 5142784) + (105049856 + 249741056) + (430870016 + 50650368) +
+                  (401271040 + 33303296),
 }
 
 
