@@ -553,7 +553,9 @@ def run_csa(args, rank, world, dist):
                 "traffic": None if traffic is None else traffic * wl.layers,
                 "traffic_source": None if traffic is None else GEMM_TRAFFIC_SOURCE,
                 "algorithmic_bytes": int(lin_bytes), "algorithmic_flops": int(lin_flops), "peak_source": peak_src,
-                "share_of_step": round(lin_ms / ms_per_step, 3) if ms_per_step else None}
+                # of the traced stages' time (each stage bracketed by event records, so launches that
+                # overlap in the untraced step do not here; their sum can exceed the untraced step)
+                "share_of_traced_stages": round(lin_ms / sum(stage_ms.values()), 3) if stage_ms else None}
 
     # ---- end to end through the host-buffer entry point (pinned x in, out back to the host)
     x_host = S.x.cpu().pin_memory()
