@@ -129,6 +129,12 @@ __global__ void __launch_bounds__(NT, 2048 / NT) k_index_topk(const float *__res
   const uint8_t *cr = cand ? cand + row * cand_width : nullptr;
   const float *Sr = S + row * Lstride;
   const int tid = threadIdx.x;
+  // no mask and at most K valid positions: all are taken, and in ascending position they are
+  // 0 .. limit-1, so the scores need not be read (the early queries of a prefill chunk)
+  if (!cr && limit <= K) {
+    for (int k = tid; k < K; k += NT) out[row * K + k] = k < limit ? k + offset : -1;
+    return;
+  }
 
   if (tid == 0) topk_shared_init(sh, K);
   __syncthreads();
