@@ -461,13 +461,28 @@ def attn_indexer_report(wl, sh_np, stage_ms, hbm_peak):
             "index_topk_ms": round(t_topk, 5), "gathered_rows": counts[0], "candidate_keys": counts[1]}
 
 
+def scored_pairs(wl, sh_np):
+    """Valid query-key pairs whose scores the selection reads: without a candidate mask, a query with
+    at most index_topk valid positions takes all of them and its scores are not computed."""
+    if sh_np["cand"] is not None:
+        return selection_counts(wl, sh_np)[1]
+    n = 0
+    for r in range(wl.batch * wl.tokens):
+        p = wl.start_pos + r % wl.tokens
+        limit = min((p + 1) // wl.ratio, sh_np["L"]) if wl.ratio else 0
+        if limit > wl.geom.index_topk:
+            n += limit
+    return n
+
+
 def prefill_tensor_report(wl, sh_np, stage_ms, tflops_peak):
     """Algorithmic tensor work of the prefill's sparse attention (QK^T and PV over the gathered rows,
-    4 H hd flops a row) and indexer scores (2 Hi dI flops per valid query-key pair) over their times."""
+    4 H hd flops a row) and indexer scores (2 Hi dI flops per scored query-key pair: the pairs of the
+    queries whose selection reads scores) over their times."""
     g = wl.geom
     rows, n_valid = selection_counts(wl, sh_np)
     f_attn = 4.0 * g.n_heads * g.head_dim * rows * wl.layers
-    f_idx = 2.0 * g.index_heads * g.index_hd * n_valid * wl.layers
+    f_idx = 2.0 * g.index_heads * g.index_hd * scored_pairs(wl, sh_np) * wl.layers
     t_attn = stage_ms.get("sparse_attn", 0.0)
     t_idx = stage_ms.get("index scores", 0.0) + stage_ms.get("index scores + topk", 0.0)
     out = {}
@@ -475,6 +490,7 @@ def prefill_tensor_report(wl, sh_np, stage_ms, tflops_peak):
         tf = f / (t * 1e9) if t > 0 else None
         out[name] = {"gflop": round(f / 1e9, 2), "ms": round(t, 5), "tflops": None if tf is None else round(tf, 1),
                      "frac_of_measured_bf16": None if tf is None else round(tf / tflops_peak, 4)}
+    out["index_scores"]["gflop_all_valid_pairs"] = round(2.0 * g.index_heads * g.index_hd * n_valid * wl.layers / 1e9, 2)
     out["index_topk_ms"] = round(stage_ms.get("index topk", 0.0), 5)
     return out
 

@@ -774,9 +774,12 @@ int attn_v41_forward(csa_ctx *ctx, const csa_layer_weights *w, csa_layer_state *
                                            rows_a_len, sh->topk_idxs, ctx->status, ctx->num_sms, s),
              "index scores + topk");
       } else {
+        // (the rows whose selection takes every valid position are not scored, unless the scores are
+        // wanted: in the debug buffer, or for the candidate blocks below)
+        const int skip_k = (dbg && dbg->scores) || r.is_candidate_source || cand ? 0 : K;
         STEP(csa::launch_index_scores(qI, wI, (const bf16 *)sh->index_k, B, T, start_pos, Hi, dI,
                                       sh->compress_stride, sh->compress_len, r.ratio, cand, sh->cand_width,
-                                      g.cand_block, S, s, ctx->status),
+                                      g.cand_block, S, s, ctx->status, skip_k),
              "index scores");
         STEP(csa::launch_index_topk(S, B, T, start_pos, sh->compress_stride, sh->compress_len, r.ratio, cand,
                                     sh->cand_width, g.cand_block, K, rows_a_len, sh->topk_idxs, s),

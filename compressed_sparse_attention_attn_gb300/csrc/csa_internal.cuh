@@ -137,9 +137,11 @@ cudaError_t launch_x_finish(const XFinishArgs &a, cudaStream_t s);
 
 // Tensor-core kernel when dI == 128, Hi is a multiple of 16 (<= 256) and qI, KI are 16-byte
 // aligned; else the CUDA-core kernel.  status (may be NULL): the device status word for timeouts.
+// skip_k > 0 (no candidate mask): the rows of queries with at most skip_k valid positions may be left
+// unwritten -- a top-k of K = skip_k over the same limits takes all of them without reading a score.
 cudaError_t launch_index_scores(const bf16 *qI, const float *wI, const bf16 *KI, int B, int T, int start_pos, int Hi,
                                 int dI, int Lstride, int compress_len, int ratio, const uint8_t *cand, int cand_width,
-                                int cand_block, float *S, cudaStream_t s, int *status = nullptr);
+                                int cand_block, float *S, cudaStream_t s, int *status = nullptr, int skip_k = 0);
 cudaError_t launch_index_topk(const float *S, int B, int T, int start_pos, int Lstride, int compress_len, int ratio,
                               const uint8_t *cand, int cand_width, int cand_block, int K, int offset, int32_t *out,
                               cudaStream_t s);

@@ -62,15 +62,15 @@ __global__ void __launch_bounds__(128) k_index_scores(const bf16 *__restrict__ q
 bool index_scores_tc_supported(const bf16 *qI, const bf16 *KI, int Hi, int dI);
 cudaError_t launch_index_scores_tc(const bf16 *qI, const float *wI, const bf16 *KI, int B, int T, int start_pos,
                                    int Hi, int Lstride, int compress_len, int ratio, const uint8_t *cand,
-                                   int cand_width, int cand_block, float *S, int *status, cudaStream_t s);
+                                   int cand_width, int cand_block, float *S, int *status, cudaStream_t s, int skip_k);
 
 cudaError_t launch_index_scores(const bf16 *qI, const float *wI, const bf16 *KI, int B, int T, int start_pos, int Hi,
                                 int dI, int Lstride, int compress_len, int ratio, const uint8_t *cand, int cand_width,
-                                int cand_block, float *S, cudaStream_t s, int *status) {
+                                int cand_block, float *S, cudaStream_t s, int *status, int skip_k) {
   if (B * T <= 0 || Lstride <= 0) return cudaSuccess;
   if (index_scores_tc_supported(qI, KI, Hi, dI))
     return launch_index_scores_tc(qI, wI, KI, B, T, start_pos, Hi, Lstride, compress_len, ratio, cand, cand_width,
-                                  cand_block, S, status, s);
+                                  cand_block, S, status, s, skip_k);
   const size_t smem = sizeof(float) * (size_t)Hi * (dI + 1);
   dim3 grid((Lstride + 127) / 128, B * T);
   switch (dI) {

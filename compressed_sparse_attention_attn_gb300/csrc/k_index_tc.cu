@@ -161,6 +161,8 @@ struct RowsParams {
   const float *wI;   // [B*T][Hi]
   int T, Hi, QG, Lstride, compress_len, ratio, start_pos;
   int gps, ngroups;  // query groups a sequence, B * gps
+  int nwork;         // groups run: the first nwork in order of decreasing key range (the others'
+                     // selections take every valid position, so their scores are not needed)
   const uint8_t *cand;
   int cand_width, cand_block;
   float *S;  // [B*T][Lstride]
@@ -230,9 +232,9 @@ __global__ void __launch_bounds__(kRowsThreads, 1) k_index_scores_rows_tc(const 
       const uint64_t pol_k = tc::policy_evict_last(), pol_q = tc::policy_evict_first();
       int qi = 0, ki = 0;
       bool ok = true;
-      for (int k = 0; ok && k * G < P.ngroups; ++k) {
+      for (int k = 0; ok && k * G < P.nwork; ++k) {
         const int r = rows_rank(k, c, G);
-        if (r >= P.ngroups) continue;
+        if (r >= P.nwork) continue;
         int b, t0, nqg, nt;
         rows_group(P, r, b, t0, nqg, nt);
         if (nt == 0) continue;
@@ -274,9 +276,9 @@ __global__ void __launch_bounds__(kRowsThreads, 1) k_index_scores_rows_tc(const 
       const uint32_t id = tc::idesc_bf16_f32(TILE, N);
       int qi = 0, ki = 0, ai = 0;
       bool ok = true, issued = false;
-      for (int k = 0; ok && k * G < P.ngroups; ++k) {
+      for (int k = 0; ok && k * G < P.nwork; ++k) {
         const int r = rows_rank(k, c, G);
-        if (r >= P.ngroups) continue;
+        if (r >= P.nwork) continue;
         int b, t0, nqg, nt;
         rows_group(P, r, b, t0, nqg, nt);
         if (nt == 0) continue;
@@ -326,9 +328,9 @@ __global__ void __launch_bounds__(kRowsThreads, 1) k_index_scores_rows_tc(const 
       return tc::mbar_wait(wbar, (syncs++) & 1u, abort_flag);
     };
     bool ok = true;
-    for (int k = 0; ok && k * G < P.ngroups; ++k) {
+    for (int k = 0; ok && k * G < P.nwork; ++k) {
       const int r = rows_rank(k, c, G);
-      if (r >= P.ngroups) continue;
+      if (r >= P.nwork) continue;
       int b, t0, nqg, nt;
       rows_group(P, r, b, t0, nqg, nt);
       if (nt == 0) continue;
@@ -1222,7 +1224,7 @@ static cudaError_t launch_index_scores_gather_tc(const bf16 *qI, const float *wI
 static cudaError_t launch_index_scores_rows_tc(const bf16 *qI, const float *wI, const bf16 *KI, int B, int T,
                                                int start_pos, int Hi, int QG, int Lstride, int compress_len, int ratio,
                                                const uint8_t *cand, int cand_width, int cand_block, float *S,
-                                               int *status, int grid, cudaStream_t s) {
+                                               int *status, int grid, int skip_k, int skip_len, cudaStream_t s) {
   using namespace idx;
   RowsParams p;
   memset(&p, 0, sizeof(p));
@@ -1239,6 +1241,19 @@ static cudaError_t launch_index_scores_rows_tc(const bf16 *qI, const float *wI, 
   p.start_pos = start_pos;
   p.gps = (T + QG - 1) / QG;
   p.ngroups = B * p.gps;
+  p.nwork = p.ngroups;
+  if (skip_k > 0 && !cand) {
+    // the leading groups whose every query has at most skip_k valid positions (by the selection's own
+    // limit, skip_len being its compress_len) are not run: those selections take every position
+    int gq_min = 0;
+    while (gq_min < p.gps) {
+      const int t_last = std::min(T, (gq_min + 1) * QG) - 1;
+      if (std::min((start_pos + t_last + 1) / ratio, skip_len) > skip_k) break;
+      ++gq_min;
+    }
+    p.nwork = B * (p.gps - gq_min);
+    if (p.nwork == 0) return cudaSuccess;
+  }
   p.cand = cand;
   p.cand_width = cand_width;
   p.cand_block = cand_block;
@@ -1251,13 +1266,13 @@ static cudaError_t launch_index_scores_rows_tc(const bf16 *qI, const float *wI, 
                                 (int)(1024 + kRowsKSlots * 2 * TILE * 128 + 4 * kMaxN * 128 + 18 * 8 + kMaxN * 4 + 16 * 4));
     if (e != cudaSuccess) return e;
   }
-  k_index_scores_rows_tc<<<std::min(grid, p.ngroups), kRowsThreads, smem, s>>>(p);
+  k_index_scores_rows_tc<<<std::min(grid, p.nwork), kRowsThreads, smem, s>>>(p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_index_scores_tc(const bf16 *qI, const float *wI, const bf16 *KI, int B, int T, int start_pos,
                                    int Hi, int Lstride, int compress_len, int ratio, const uint8_t *cand,
-                                   int cand_width, int cand_block, float *S, int *status, cudaStream_t s) {
+                                   int cand_width, int cand_block, float *S, int *status, cudaStream_t s, int skip_k) {
   using namespace idx;
   Params p;
   memset(&p, 0, sizeof(p));
@@ -1298,7 +1313,7 @@ cudaError_t launch_index_scores_tc(const bf16 *qI, const float *wI, const bf16 *
   if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
       T > 1 && (int64_t)B * ((T + p.QG - 1) / p.QG) >= nsm && ((uintptr_t)wI & 15) == 0)
     return launch_index_scores_rows_tc(qI, wI, KI, B, T, start_pos, Hi, p.QG, Lstride, p.compress_len, ratio, cand,
-                                       cand_width, cand_block, S, status, nsm, s);
+                                       cand_width, cand_block, S, status, nsm, skip_k, compress_len, s);
   dim3 grid(tiles, (T + p.QG - 1) / p.QG, B);
   k_index_scores_tc<<<grid, kThreads, smem, s>>>(p);
   return cudaGetLastError();

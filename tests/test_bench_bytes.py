@@ -99,3 +99,18 @@ def test_projection_bytes_match_the_parameter_table():
     got = bench.projection_bytes(wl)
     assert set(got) == {"proj x", "proj qr", "wo_a", "wo_b"}
     assert sum(got.values()) == 2 * (weights + acts) == 270403584
+
+
+def test_prefill_scored_pairs_closed_form():
+    """The indexer's scored pairs at prefill: only the queries with more than K = 512 valid positions
+    are scored (the others' selections take every position).  floor((t+1)/4) > 512 from t = 2051 on;
+    each value v = 513..1023 occurs for four consecutive t, and 1024 once (t = 4095)."""
+    import bench
+    wl = WORKLOADS["prefill_r4"]
+    want = 4 * sum(range(513, 1024)) + 1024
+    assert bench.scored_pairs(wl, _shared(wl)) == want == 1570816
+    # with a candidate mask every valid pair is scored
+    wl2 = WORKLOADS["longctx_decode_r4"]
+    sh2 = _shared(wl2)
+    assert bench.scored_pairs(wl2, sh2) == bench.selection_counts(wl2, sh2)[1]
+
