@@ -415,7 +415,9 @@ int csa_linear(csa_ctx *ctx, const csa_bf16 *x, int M, int K, int ldx, const csa
     return fail(CSA_ERR_ARG, "csa_linear: bad shape M=%d K=%d N=%d groups=%d", M, K, N, groups);
   if (int rc = check_device(ctx, "csa_linear")) return rc;
   csa::LinearProblem pr{(const bf16 *)x, M, K, ldx, (const bf16 *)W, N, ldw, (bf16 *)y, ldy, groups};
-  CSA_CUDA(csa::launch_linear(&pr, 1, ctx->ws, ctx->gemm_ws_bytes(), ctx->num_sms, ctx->status, (cudaStream_t)stream),
+  int kernels = 0;  // (counted, so that a paired launch may split its last wave)
+  CSA_CUDA(csa::launch_linear(&pr, 1, ctx->ws, ctx->gemm_ws_bytes(), ctx->num_sms, ctx->status, (cudaStream_t)stream,
+                              &kernels),
            "csa_linear");
   return CSA_OK;
 }
@@ -823,7 +825,9 @@ int attn_v41_forward(csa_ctx *ctx, const csa_layer_weights *w, csa_layer_state *
     STEP(csa::launch_linear(&pa, 1, ctx->ws, ctx->gemm_ws_bytes(), ctx->num_sms, ctx->status, s), "wo_a");
     csa::LinearProblem pb = lin(og, G * g.o_rank, G * g.o_rank, w->wo_b, g.dim, out, g.dim, 1);
     pb.pdl = pb.early_dependents = 1;
-    STEP(csa::launch_linear(&pb, 1, ctx->ws, ctx->gemm_ws_bytes(), ctx->num_sms, ctx->status, s), "wo_b");
+    int wo_b_kernels = 0;  // (a prefill chunk's wo_b may split its last wave: three launches)
+    STAGE(csa::launch_linear(&pb, 1, ctx->ws, ctx->gemm_ws_bytes(), ctx->num_sms, ctx->status, s, &wo_b_kernels),
+          "wo_b", wo_b_kernels);
   }
 #undef STEP
 #undef COPY

@@ -94,9 +94,10 @@ struct LinearProblem {
   int pdl = 0;
 };
 // Products sharing M run in one tensor-core launch (up to 4 at a time).  ws/ws_bytes: Stream-K
-// arrival counters and partials (the counters must be zero between launches).
+// arrival counters and partials (the counters must be zero between launches).  kernels (may be NULL):
+// receives the kernels launched.
 cudaError_t launch_linear(const LinearProblem *probs, int n, float *ws, size_t ws_bytes, int num_sms, int *status,
-                          cudaStream_t s);
+                          cudaStream_t s, int *kernels = nullptr);
 constexpr size_t kGemmCounterBytes = 65536 * sizeof(int);
 // Failure-detection test hook of the current device: while ns != 0 the projection kernels first
 // wait, up to ns nanoseconds, on a barrier phase that nothing completes, then take their timeout path.
@@ -106,8 +107,11 @@ cudaError_t set_gemm_stall(unsigned long long ns);
 cudaError_t launch_gemm_tc_split(const LinearProblem *probs, int nprob, int S, int *status, cudaStream_t s);
 // The Stream-K / waves / paired launch of up to four problems sharing the activations (the paired
 // kernel, chosen for many token tiles, may write a problem's f32 result to `part` as one split slice).
+// kernels (may be NULL): receives the kernels launched; only a caller that counts them lets a paired
+// launch of one problem split its last partial wave by k-range (two more launches: the split tiles
+// and their sum).
 cudaError_t launch_gemm_tc(const LinearProblem *probs, int nprob, float *ws, size_t ws_bytes, int num_sms,
-                           int *status, cudaStream_t s);
+                           int *status, cudaStream_t s, int *kernels = nullptr);
 // The largest split count S <= max_S dividing the problems' k-slices with tiles * S <= max_ctas (>= 1).
 int gemm_tc_split_count(const LinearProblem *probs, int nprob, int max_ctas, int max_S);
 bool gemm_tc_supported(const LinearProblem &q);

@@ -84,6 +84,10 @@ struct Params {
   // data-parallel waves: CTA c first takes the whole tiles c, c + G, ... (dp_waves of them; tiles
   // [0, dp_waves G) in all), then its Stream-K share of the units from sk_unit0 on
   int dp_waves, sk_unit0;
+  // k_gemm_tc_pairs: the pair tiles [pt_begin, pt_begin + pt_count) of the launch; ksplit > 1: each
+  // split over ksplit equal k-ranges, the f32 partial sums to tail_part [ksplit][pt_count][256][256]
+  int pt_begin, pt_count, ksplit;
+  float *tail_part;
   int early_dependents;  // let a programmatic dependent launch once every CTA here has started
   // launched as a programmatic dependent of the kernel before it (k_gemm_tc only): the producer
   // copies the weights of its first stages, then waits for that kernel, then copies their activations
@@ -1145,8 +1149,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc_pairs(const __grid_cons
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = (int)tc::cluster_ctarank();
   const int v0 = blockIdx.x >> 1, NP = gridDim.x >> 1;
-  int PT = 0;
-  for (int p = 0; p < P.nprob; ++p) PT += pair_tiles_of(P.prob[p]);
+  const int KSP = P.ksplit > 1 ? P.ksplit : 1;
+  const int W = P.pt_count * KSP;  // work items: (pair tile, k-range)
+  // work item w: its pair tile and k-slices [kb0, kb1)
+  auto item = [&](int w, int &pt, int &kb0, int &kb1, int kbl) {
+    pt = P.pt_begin + w / KSP;
+    const int sp = w % KSP;
+    kb0 = sp * kbl / KSP;
+    kb1 = (sp + 1) * kbl / KSP;
+  };
   constexpr uint16_t kBoth = 3;
   constexpr uint32_t tmem_cols = 2 * kPairBN;
 
@@ -1183,12 +1194,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc_pairs(const __grid_cons
       int stage = 0, issued = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int pt = v0; pt < PT && ok; pt += NP) {
+      for (int w = v0; w < W && ok; w += NP) {
+        int pt, kb0, kb1;
+        item(w, pt, kb0, kb1, P.prob[0].kblocks);
         const PairTile q = decode_pair(P, pt);
         const Problem &pr = P.prob[q.p];
+        if (KSP == 1) kb1 = pr.kblocks;
         const int tn = 2 * q.j + rank;
         const uint64_t pa = pr.pol_a == 2 ? pol_last : pol_normal, pb = pr.pol_b == 2 ? pol_last : pol_normal;
-        for (int kb = 0; kb < pr.kblocks; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!(ok = tc::mbar_wait(&empty[stage], phase ^ 1, abort_flag))) break;
           uint8_t *sa = smem + stage * stage_bytes;
           tc::mbar_expect_tx(&full[stage], stage_bytes);
@@ -1218,13 +1232,15 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc_pairs(const __grid_cons
       uint32_t phase = 0;
       int used[2] = {0, 0};
       bool ok = true;
-      for (int pt = v0; pt < PT && ok; pt += NP) {
+      for (int w = v0; w < W && ok; w += NP) {
+        int pt, kb0, kb1;
+        item(w, pt, kb0, kb1, P.prob[0].kblocks);
         const PairTile q = decode_pair(P, pt);
-        const int kblocks = P.prob[q.p].kblocks;
+        if (KSP == 1) kb1 = P.prob[q.p].kblocks;
         if (!(ok = tc::mbar_wait(&acce[buf], (uint32_t)(used[buf] & 1) ^ 1u, abort_flag))) break;
         tc::tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)(buf * kPairBN);
-        for (int kb = 0; kb < kblocks; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!(ok = tc::mbar_wait(&full[stage], phase, abort_flag))) break;
           tc::tc_fence_after();
           const uint32_t sa = tc::smem_u32(smem + stage * stage_bytes);
@@ -1232,7 +1248,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc_pairs(const __grid_cons
           const uint64_t bd = tc::sdesc_sw128(sa + a_bytes, 16, 1024);
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            tc::mma_bf16(d, ad + 2ull * k, bd + 2ull * k, idesc, (kb == 0 && k == 0) ? 0u : 1u);
+            tc::mma_bf16(d, ad + 2ull * k, bd + 2ull * k, idesc, (kb == kb0 && k == 0) ? 0u : 1u);
           mma_commit_mc(&empty[stage], kBoth);  // both CTAs may refill their halves of this stage
           if (++stage == S) {
             stage = 0;
@@ -1254,13 +1270,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc_pairs(const __grid_cons
     // ---------------------------------------------------------------- epilogue (warps 0-3)
     const int row = warp * 32 + lane;  // feature within the tile
     int buf = 0, done[2] = {0, 0};
-    for (int pt = v0; pt < PT; pt += NP) {
+    for (int w = v0; w < W; w += NP) {
+      int pt, kb0, kb1;
+      item(w, pt, kb0, kb1, P.prob[0].kblocks);
       const PairTile q = decode_pair(P, pt);
       const Problem &pr = P.prob[q.p];
       const int f = (2 * q.j + rank) * BM + row;
       const bool f_ok = f < pr.N;
       bf16 *ycol = pr.y ? pr.y + (int64_t)q.g * pr.N + f : nullptr;
       float *pcol = pr.part ? pr.part + (int64_t)q.g * pr.N + f : nullptr;  // f32 result (one split slice)
+      // a k-range's partial sums: [split][item][token in tile][feature in pair], lanes on features
+      float *tcol = KSP > 1 ? P.tail_part + ((size_t)((w % KSP) * P.pt_count + (pt - P.pt_begin)) * kPairBN) * 256 +
+                                  rank * BM + row
+                            : nullptr;
       if (!tc::mbar_wait(&accf[buf], (uint32_t)(done[buf] & 1), abort_flag)) break;
       tc::tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(warp * 32) << 16) + (uint32_t)(buf * kPairBN);
@@ -1268,7 +1290,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc_pairs(const __grid_cons
         uint32_t r[16];
         tc::tmem_ld16(taddr + (uint32_t)c0, r);
         tc::tmem_ld_wait();
-        if (f_ok && pcol) {
+        if (tcol) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) tcol[(size_t)(c0 + i) * 256] = __uint_as_float(r[i]);
+        } else if (f_ok && pcol) {
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int jt = q.tm * kPairBN + c0 + i;
@@ -1297,6 +1322,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_gemm_tc_pairs(const __grid_cons
     tc::tmem_dealloc(tmem_base, tmem_cols);
   }
   if (threadIdx.x == 0 && *abort_flag) atomicOr(P.status, kStatusTimeout);
+}
+
+// The split tail's sums: block (item, token) adds the k-ranges' partials of one token row of a pair
+// tile (256 features, a thread each) and writes them as bf16.
+__global__ void __launch_bounds__(256) k_pair_tail_sum(const float *__restrict__ part, int ksplit, int pt_begin,
+                                                       int pt_count, int tiles_m, int half_n, int M, int N,
+                                                       bf16 *__restrict__ y, int ldy) {
+  const int w = blockIdx.x / kPairBN, tok = blockIdx.x % kPairBN, f = threadIdx.x;
+  const int pt = pt_begin + w;
+  const int tm = pt % tiles_m, j = (pt / tiles_m) % half_n;
+  const int row = tm * kPairBN + tok, col = j * 2 * BM + f;
+  float acc = 0.f;
+  for (int sp = 0; sp < ksplit; ++sp) acc += __ldcg(part + ((size_t)(sp * pt_count + w) * kPairBN + tok) * 256 + f);
+  if (row < M && col < N) y[(int64_t)row * ldy + col] = __float2bfloat16_rn(acc);
 }
 
 // ---- host ---------------------------------------------------------------------------------------
@@ -1384,7 +1423,7 @@ int gemm_tc_bn(int M, bool f8) {
 
 // Launch up to kMaxProblems products that share M (token count) in one persistent Stream-K grid.
 cudaError_t launch_gemm_tc(const LinearProblem *probs, int nprob, float *ws, size_t ws_bytes, int num_sms,
-                           int *status, cudaStream_t s) {
+                           int *status, cudaStream_t s, int *kernels) {
   using namespace gemm;
   if (nprob <= 0 || nprob > kMaxProblems) return cudaErrorInvalidValue;
   const int M = probs[0].M;
@@ -1529,8 +1568,38 @@ cudaError_t launch_gemm_tc(const LinearProblem *probs, int nprob, float *ws, siz
       pair_tiles += P.prob[i].tiles_m * ((P.prob[i].tiles_n + 1) / 2) * P.prob[i].groups;
     nclusters = std::min(std::max(nclusters, 1), std::max(1, pair_tiles));
     cfg.gridDim = dim3(2 * nclusters);
+    P.pt_begin = 0;
+    P.pt_count = pair_tiles;
+    P.ksplit = 1;
+    P.tail_part = nullptr;
+    // the last, partial wave of whole pair tiles split by k-range over the clusters (one problem with
+    // a bf16 result): the k-ranges' f32 sums go to the workspace, and a small kernel adds them
+    const int full = (pair_tiles / nclusters) * nclusters, tail = pair_tiles - full;
+    int ks = 0;
+    if (kernels && tail > 0 && full > 0 && nprob == 1 && !probs[0].part && probs[0].groups == 1) {
+      const int kbl = P.prob[0].kblocks;
+      for (int c = 2; c <= 8; ++c)
+        if (tail * c <= nclusters && kbl % c == 0 && kbl / c >= 4) ks = c;
+      if (ks && ws_bytes < kCounterBytes + (size_t)ks * tail * kPairBN * 256 * sizeof(float)) ks = 0;
+    }
+    if (ks) P.pt_count = full;
     e = cudaLaunchKernelEx(&cfg, k_gemm_tc_pairs, P);
-    return e == cudaSuccess ? cudaGetLastError() : e;
+    if (e != cudaSuccess) return e;
+    if (kernels) *kernels = 1;
+    if (!ks) return cudaGetLastError();
+    Params P2 = P;
+    P2.pt_begin = full;
+    P2.pt_count = tail;
+    P2.ksplit = ks;
+    P2.tail_part = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(ws) + kCounterBytes);
+    cfg.gridDim = dim3(2 * tail * ks);
+    e = cudaLaunchKernelEx(&cfg, k_gemm_tc_pairs, P2);
+    if (e != cudaSuccess) return e;
+    const Problem &q0 = P.prob[0];
+    k_pair_tail_sum<<<tail * kPairBN, 256, 0, s>>>(P2.tail_part, ks, full, tail, q0.tiles_m, (q0.tiles_n + 1) / 2, M,
+                                                   q0.N, q0.y, q0.ldy);
+    *kernels = 3;
+    return cudaGetLastError();
   }
   const size_t smem = 1024 + (size_t)P.stages * stage_bytes + conv_bytes +
                       (size_t)(2 * P.stages + 2 * P.cstages + 8) * 8 + 64 + kMaxContrib * sizeof(int);

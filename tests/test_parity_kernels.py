@@ -171,12 +171,13 @@ def test_linear_waves(csa, orc, M, K, N, groups):
 
 
 @pytest.mark.parametrize("M,K,N,groups", [(2100, 1280, 4096, 1), (3000, 640, 1024, 2), (2048, 96, 256, 1),
-                                          (2304, 5120, 1280, 1)])
+                                          (2304, 5120, 1280, 1), (4096, 1024, 1280, 1), (4096, 8192, 5120, 1)])
 def test_linear_pairs(csa, orc, M, K, N, groups):
     """Many token tiles and an even number of weight tiles: clusters of two CTAs on adjacent weight
     tiles, each copying half of the shared token tile into both.  Ragged last token tile, a k-range
-    that is not a whole number of 64-wide slices, two groups.  The oracle computes sampled rows (every
-    token tile's edges and the ragged last one), all columns."""
+    that is not a whole number of 64-wide slices, two groups; more pair tiles than a wave of clusters
+    (4096 x 1280: 80 pair tiles, the last four split by k-range and summed by a second kernel).  The
+    oracle computes sampled rows (every token tile's edges and the ragged last one), all columns."""
     rng = np.random.default_rng(50 + M + N)
     x = _rng_bf16(orc, rng, (M, K * groups))
     W = _rng_bf16(orc, rng, (N * groups, K), 1.0 / math.sqrt(K))
@@ -184,7 +185,7 @@ def test_linear_pairs(csa, orc, M, K, N, groups):
     got = to_np(ctx.linear(to_dev(x), to_dev(W), groups=groups))
     assert ctx.status() == 0
     rows = sorted(set([0, 1, 127, 128, 255, 256, M - 1, M - 2] + list(range(130, M, 256)) +
-                      list(rng.integers(0, M, 16))))
+                      list(rng.integers(0, M, 16)) + list(rng.integers(max(0, M - 1024), M, 8))))
     want = np.concatenate([orc.linear_bf16(x[rows, g * K:(g + 1) * K], W[g * N:(g + 1) * N]) for g in range(groups)], 1)
     assert_close_bf16(got[rows], want, what="linear (pairs)")
 
