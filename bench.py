@@ -42,8 +42,9 @@ GEMM_TRAFFIC_BYTES = {
     "reindex_decode_r2": (19072000 + 0) + (94519040 + 151808) + (69267712 + 6656) + (84563712 + 164608),
     "longctx_decode_r4": (19400960 + 0) + (94602496 + 142592) + (71365888 + 62208) + (85174272 + 237056),
     "ratio0_decode": (18744320 + 0) + (84032000 + 179712) + (69281792 + 12800) + (84606208 + 143872),
-    "prefill_r4": (68472320 + 5142784) + (105049856 + 249741056) + (430870016 + 50650368) +
-                  (401271040 + 33303296),
+    # (prefill: wo_b's whole waves, its split last wave and their sum are three launches)
+    "prefill_r4": (68499712 + 5202944) + (104963840 + 251502336) + (428238080 + 50825728) +
+                  (353134848 + 29880064) + (71337728 + 114688) + (16785152 + 0),
 }
 
 
