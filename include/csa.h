@@ -261,7 +261,9 @@ CSA_API int csa_last_launches(const csa_ctx *ctx);
  * x [M][K] with row stride ldx, W [N][K] row stride ldw, y [M][N] row stride ldy (elements).
  * groups > 1 runs `groups` independent products in one call ([atlas] "Grouped output", the
  * block-diagonal wo_a): product g reads x columns [g*K, (g+1)*K), W rows [g*N, (g+1)*N) and writes
- * y columns [g*N, (g+1)*N).  ctx provides the split-K workspace. */
+ * y columns [g*N, (g+1)*N).  ctx provides the split-K workspace (a call on one context at a time
+ * per stream: the workspace also holds the f32 partial sums when a product of 2048 or more rows
+ * splits its last wave of tiles by k-range, which enqueues two more kernels). */
 CSA_API int csa_linear(csa_ctx *ctx, const csa_bf16 *x, int M, int K, int ldx, const csa_bf16 *W, int N, int ldw, csa_bf16 *y,
                int ldy, int groups, csa_stream stream);
 
