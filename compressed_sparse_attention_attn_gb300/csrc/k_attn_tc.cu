@@ -108,12 +108,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
       tma_load_2d_nohint(s_q + kb * HG * 128, &P.tm_q, q_full, kb * 64, (int)(row * P.H + hg * HG));
   }
   if (warp == 8) tc::tmem_alloc(tmem_slot, kCols);
-  // Launched as a programmatic dependent of the selection kernel before it: everything above (and
-  // q, written two launches earlier) overlaps that kernel; the index lists it writes are read only
-  // after this wait.  The kernel after (the merge, or wo_a: programmatic dependents reading this
-  // kernel's output after their own waits) may start at once.
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // loader geometry: each of warps 0-7 copies one K-block (a 128-byte segment of every row), four
   // rows per instruction, 8 lanes per row; warps 4-7 take K-blocks 0-3 (they run the index pass and
@@ -137,14 +131,35 @@ __global__ void __launch_bounds__(kThreads, 1) k_sparse_attn_tc(const __grid_con
     }
   };
   auto tile_ok = [&](int i) { return (wcnt[4 * i] | wcnt[4 * i + 1] | wcnt[4 * i + 2] | wcnt[4 * i + 3]) != 0; };
-  if (warp >= 4 && warp < 8) index_pass(P, row, b, k0, nk, tid - 128, warp - 4, lane, src_list, valid, wcnt);
-  if (warp < 8) {  // the first live tile's copies, once the index pass has filled the lists
+  // A CTA whose first tile is a whole tile of the first list (the window: its indices and rows were
+  // written two or more launches earlier) forms that tile's list and starts its copies before the
+  // dependency wait.
+  const bool early = k0 == 0 && nk > 0 && P.na >= TILE;
+  if (early) {
+    if (warp >= 4 && warp < 8) index_pass(P, row, b, 0, 1, tid - 128, warp - 4, lane, src_list, valid, wcnt);
+    if (warp < 8) {
+      tc::named_bar(1, 256);
+      if (tile_ok(0)) issue_tile(0);
+    }
+  }
+  // Launched as a programmatic dependent of the selection kernel before it: everything above (and
+  // q, written two launches earlier) overlaps that kernel; the index lists it writes are read only
+  // after this wait.  The kernel after (the merge, or wo_a: programmatic dependents reading this
+  // kernel's output after their own waits) may start at once.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int t1 = early ? 1 : 0;  // the first tile the pass after the wait forms
+  if (warp >= 4 && warp < 8 && nk > t1)
+    index_pass(P, row, b, k0 + t1, nk - t1, tid - 128, warp - 4, lane, src_list + t1 * TILE, valid + t1 * TILE,
+               wcnt + 4 * t1);
+  if (warp < 8) {  // the first live tile's copies (unless already started), once the lists are filled
     tc::named_bar(1, 256);
-    for (int i = 0; i < nk; ++i)
-      if (tile_ok(i)) {
-        issue_tile(i);
-        break;
-      }
+    if (!(early && tile_ok(0)))
+      for (int i = t1; i < nk; ++i)
+        if (tile_ok(i)) {
+          issue_tile(i);
+          break;
+        }
   }
   tc::tc_fence_before();
   __syncthreads();
